@@ -1,0 +1,158 @@
+/*
+ * mdn.h — C ABI of the Momentum DeltaNet (MDN) memory-update library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method: "MDN: Parallelizing Stepwise Momentum for Delta Linear
+ * Attention" (arXiv 2605.05838).  Per head, two states S, M in R^{dk x dv}
+ * (memory and momentum) and four scalar gates per token (alpha retention,
+ * mu momentum retention, beta step, eta gradient scale) evolve as
+ *
+ *     vres_t = v_t - alpha_t S_{t-1}^T k_t
+ *     M_t    = mu_t M_{t-1} - eta_t k_t vres_t^T
+ *     S_t    = alpha_t S_{t-1} - beta_t M_t
+ *     o_t    = S_t^T q_t
+ *
+ * (paper-reading slides, frame "MDN adds a momentum matrix to the delta
+ * update", Eqs. (3)-(5); reading notes section 2.2).
+ *
+ * General conventions
+ *  - Every pointer argument except cu_seqlens' host use is a DEVICE pointer
+ *    to memory the caller owns; the library keeps no pointer after a call
+ *    returns and allocates no device memory.
+ *  - All device work is enqueued on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream) and runs asynchronously; a call returns as soon as
+ *    its kernels are enqueued.
+ *  - Gates and states are fp32.  q, k, v, o share one element type `dtype`.
+ *    Accumulation is fp32.  Inputs are never modified (except the in-place
+ *    states of mdn_decode_step).
+ *  - Tensors are dense, row-major, innermost dimension last; no strides.
+ *  - Preconditions documented, not checked on the device: alpha in (0, 1],
+ *    mu in [0, 1], beta >= 0, eta >= 0, all finite.  mu = 0 is supported.
+ *  - Errors: a call validates its arguments before enqueuing anything and
+ *    returns MDN_ERR_INVALID_ARG (null required pointer, non-positive or
+ *    inconsistent size, pointer not 16-byte aligned, workspace too small),
+ *    MDN_ERR_UNSUPPORTED (dk != dv, dk not in {64, 128}, chunk != 64, device
+ *    is not compute capability 10.3) or MDN_ERR_CUDA (a CUDA call or launch
+ *    failed; cudaGetLastError() is cleared).  On any error nothing was
+ *    enqueued except for MDN_ERR_CUDA, where earlier launches of the same call
+ *    may have been.  Device-side bounded waits that expire set
+ *    MDN_ERR_DEVICE_TIMEOUT in a device status word read by
+ *    mdn_get_device_status; the kernel then returns without hanging.
+ */
+#ifndef MDN_H_
+#define MDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MDN_ABI_VERSION 1
+
+typedef enum mdn_status {
+    MDN_OK = 0,
+    MDN_ERR_INVALID_ARG = 1,
+    MDN_ERR_UNSUPPORTED = 2,
+    MDN_ERR_CUDA = 3,
+    MDN_ERR_DEVICE_TIMEOUT = 4
+} mdn_status;
+
+typedef enum mdn_dtype {
+    MDN_F32 = 0,   /* IEEE binary32 */
+    MDN_BF16 = 1   /* bfloat16 */
+} mdn_dtype;
+
+/* Returns MDN_ABI_VERSION of the built library. */
+int mdn_abi_version(void);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *mdn_status_string(mdn_status status);
+
+/*
+ * Bytes of device workspace mdn_chunk_fwd needs for these sizes (a multiple
+ * of 256; 0 for invalid sizes).  The bound covers every split of T_total into
+ * n_seq sequences, so it does not need cu_seqlens.
+ */
+size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
+                                    int dv, mdn_dtype dtype);
+
+/*
+ * mdn_chunk_fwd — prefill: run the recurrence above over whole sequences in
+ * the exact chunkwise-parallel form.
+ *
+ * Defined by: slides, frames "Reorder the triangular sum to isolate scalar
+ * coefficients" (Eqs. (7)-(9), Appendix C Eqs. (30)-(31)), "Solve the unknown
+ * residuals with a lower triangular system" (Eqs. (15)-(18)), "Chunk outputs
+ * combine incoming states and local writes" (Appendix C Eqs. (40)-(42)) and
+ * the backup frames on the row shift and on the log-domain coefficients
+ * (Algorithm 1); reading notes sections 2.3-2.6.  In exact arithmetic the
+ * result equals the token recurrence; chunks hold 64 tokens and each sequence
+ * is chunked from its own start (a shorter last chunk uses its own length).
+ *
+ * Layout.  Without cu_seqlens: B sequences of T tokens each, n_seq == B,
+ *   q, k [B, T, H, dk];  v, o [B, T, H, dv];  alpha, mu, eta, beta [B, T, H].
+ * With cu_seqlens (device int32 [n_seq + 1], cu_seqlens[0] = 0, non-
+ *   decreasing, cu_seqlens[n_seq] == T): B must be 1 and the n_seq sequences
+ *   are packed along T; sequence s owns tokens [cu_seqlens[s],
+ *   cu_seqlens[s+1]).  Empty sequences are allowed (their final states equal
+ *   their initial states).
+ * States S0, M0, S_T, M_T: [n_seq, H, dk, dv] fp32.
+ *
+ * Arguments
+ *   q, k, v        inputs (dtype)
+ *   alpha, mu, eta gates (fp32), required
+ *   beta           step gate (fp32) or NULL for beta = 1
+ *   S0, M0         initial states or NULL for zero (each independently)
+ *   o              output (dtype), written for every token
+ *   S_T, M_T       final states, or NULL to skip writing that state.  S_T may
+ *                  alias S0 and M_T may alias M0 (same pointer, not partial
+ *                  overlap); no other output may overlap an input.
+ *   workspace      device scratch of at least workspace_bytes >=
+ *                  mdn_chunk_fwd_workspace_size(...), 256-byte aligned; its
+ *                  contents on entry do not matter and are undefined on exit.
+ *                  Two calls in flight at once need separate workspaces.
+ *   chunk          must be 64
+ *   stream         cudaStream_t (as void*) the work is enqueued on
+ */
+mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *mu, const float *eta,
+                         const float *beta, const float *S0, const float *M0,
+                         void *o, float *S_T, float *M_T,
+                         const int32_t *cu_seqlens, int n_seq, int B, int T,
+                         int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mdn_decode_step — one recurrent step for N sequences (one token each),
+ * updating both states in place.
+ *
+ * Defined by: the token recurrence above (slides Eqs. (3)-(5); reading notes
+ * section 2.2); the slides note decoding uses this recurrence with the two
+ * fixed-size states ("Chunk outputs combine incoming states ..." frame).
+ *
+ * Layout: q, k [N, H, dk]; v, o [N, H, dv] (dtype); alpha, mu, eta, beta
+ * [N, H] fp32 (beta NULL = 1); S, M [N, H, dk, dv] fp32, read and replaced by
+ * S_t, M_t.  o receives S_t^T q.  o must not overlap any input.
+ */
+mdn_status mdn_decode_step(const void *q, const void *k, const void *v,
+                           const float *alpha, const float *mu,
+                           const float *eta, const float *beta, float *S,
+                           float *M, void *o, int N, int H, int dk, int dv,
+                           mdn_dtype dtype, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns MDN_OK if no kernel reported a problem since the
+ * last read, MDN_ERR_DEVICE_TIMEOUT if a bounded device-side wait expired
+ * (that launch's outputs are then undefined), MDN_ERR_CUDA if the
+ * synchronisation or the read failed.
+ */
+mdn_status mdn_get_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MDN_H_ */
