@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the MDN memory update on one GB300 (or N replicas).
+
+Main metric: chunkwise-forward tokens/s on the 400M-model-shaped prefill
+(B=8, H=8, T=2048, d=128, bf16 q/k/v, fp32 gates and states), plus the
+roofline fraction of its dominant kernel.  The decode step (256 sequences x
+16 heads x d=128, 1000 steps) is reported beside it in ``decode``.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Timing: W warm-up steps, then exactly K steps; before every timed step L2 is
+flushed by writing a 256 MiB buffer (outside the timed interval); each step
+is bracketed by CUDA events on the launching stream, and the library records
+caller-created events at its stage boundaries so the dominant kernel is timed
+live.  With N > 1 (torchrun) every rank runs the same workload independently
+(replicas: the method has no exchange step), timing is bracketed by a barrier
+and synchronize on both sides and the MAX over ranks is taken.
+"""
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+SMS = 152
+FP32_LANES_PER_SM = 128          # FFMA lanes per SM per clock
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["mdn", "reference"], default="mdn")
+    p.add_argument("--workload", default=W.PREFILL_400M.name,
+                   choices=[w.name for w in W.ALL if not w.decode_steps])
+    p.add_argument("--decode-steps", type=int, default=W.DECODE.decode_steps)
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="minimum CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = list(csv.reader(io.StringIO(f.read())))
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel_key, source_file):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current source of the kernel (sha256 of its .cu file)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+        with open(source_file, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError, AttributeError):
+        return None
+    if not rec or rec.get("source_sha256") != sha:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- work units
+
+def flops_per_token_head(d, C=64):
+    """Algorithmic FLOPs of each stage per (token, head)."""
+    state = 12 * d * d + 4 * C * d        # K[S|M], Q[S|M], carry; T R, (A_O T) R
+    prep = 4 * C * d + 2 * C * C + C * C // 3   # two Grams, A_O T, triangular inverse
+    return {"prep": prep, "state": state}
+
+
+def state_pass_bytes(x, prep_bytes_per_chunk_head):
+    """Algorithmic HBM bytes of the state pass: q, k, v read, o written,
+    prepared blocks read, states read and written once per chain."""
+    el = 2 if x["dtype"] == "bf16" else 4
+    th = x["B"] * x["T"] * x["H"]
+    D = x["D"]
+    chunks = sum((L + 63) // 64 for L in seq_lengths(x)) * x["H"]
+    n_chain = x["n_seq"] * x["H"]
+    return (th * 4 * D * el + chunks * prep_bytes_per_chunk_head
+            + n_chain * 4 * D * D * 4)
+
+
+def seq_lengths(x):
+    if x["cu_seqlens"] is not None:
+        cu = x["cu_seqlens"].tolist()
+        return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    return [x["T"]] * x["B"]
+
+
+# ---------------------------------------------------------------- arms
+
+def run_cpu_oracle(x, seconds, max_seqs=None):
+    """Time the fp64 oracle (as it stands) on the host cores."""
+    from oracle import recurrence
+    import numpy as np
+    lens = seq_lengths(x)
+    n_use = len(lens) if max_seqs is None else min(max_seqs, len(lens))
+    cu = [0]
+    for L in lens[:n_use]:
+        cu.append(cu[-1] + L)
+    H, D = x["H"], x["D"]
+    T_use = cu[-1]
+    sl = slice(0, T_use)
+    flat = lambda t: t.reshape(-1, *t.shape[2:])[sl].double().numpy()
+    args = [flat(x[n]) for n in ("q", "k", "v", "alpha", "mu", "eta")]
+    beta = flat(x["beta"]) if x["beta"] is not None else None
+    S0 = x["S0"][:n_use].double().numpy() if x["S0"] is not None else None
+    M0 = x["M0"][:n_use].double().numpy() if x["M0"] is not None else None
+    cores = host_cores()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        recurrence.forward(*args, beta=beta, S0=S0, M0=M0,
+                           cu_seqlens=np.array(cu, np.int32), n_threads=cores)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    tokens = T_use * reps
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": "%d of %d sequences (%d tokens x %d heads, d=%d), fp64 "
+                      "token recurrence, %d repetition(s) in %.1f s" %
+                      (n_use, len(lens), T_use, H, D, reps, dt)}
+
+
+def reference_arm(args, rank, world):
+    """The oracle timed on the host cores, same metric/config as the GPU arm."""
+    if rank != 0:
+        return
+    w = W.BY_NAME[args.workload]
+    x = W.make_prefill(w)
+    steps, warm = args.steps, args.warmup
+    # each step: a bounded sample (two sequences) so the run ends in minutes
+    per = []
+    for i in range(warm + steps):
+        r = run_cpu_oracle(x, seconds=0.0, max_seqs=2)
+        if i >= warm:
+            per.append(r)
+    val = statistics.mean(r["value"] for r in per)
+    tokens_per_step = sum(seq_lengths(x)[:2])
+    line = {
+        "impl": "reference", "metric": "MDN chunkwise fwd tokens/s",
+        "value": val, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": 1e3 * tokens_per_step / val,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, x, "none (host oracle)"),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": per[0]["cores"],
+                         "kind": "oracle", "sample": per[0]["sample"] + " per step"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, x, l2):
+    cfg = {"workload": w.name, "B": x["B"], "T": x["T"], "H": x["H"],
+           "d_k": x["D"], "d_v": x["D"], "chunk": 64, "inputs": x["dtype"],
+           "gates_states": "fp32", "n_seq": x["n_seq"], "l2": l2,
+           "parallelism": "replicas"}
+    return cfg
+
+
+def time_prefill(mdn, x_dev, w, steps, warmup, world, flush):
+    dev = x_dev["q"].device
+    o = torch.empty_like(x_dev["v"])
+    S_T = torch.empty((x_dev["n_seq"], x_dev["H"], x_dev["D"], x_dev["D"]),
+                      dtype=torch.float32, device=dev)
+    M_T = torch.empty_like(S_T)
+    need = mdn.workspace_size(x_dev["n_seq"], x_dev["B"] * x_dev["T"], x_dev["H"],
+                              x_dev["D"], x_dev["q"].dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    info = {}
+
+    def step(evs=None):
+        mdn.chunk_fwd(x_dev["q"], x_dev["k"], x_dev["v"], x_dev["alpha"],
+                      x_dev["mu"], x_dev["eta"], x_dev["beta"], x_dev["S0"],
+                      x_dev["M0"], cu_seqlens=x_dev["cu_seqlens"], o=o, S_T=S_T,
+                      M_T=M_T, workspace=ws, stage_events=evs, info=info)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    st = mdn.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after the timed region" % st)
+    stage0 = [e[0].elapsed_time(e[1]) for e in evs]
+    stage1 = [e[1].elapsed_time(e[2]) for e in evs]
+    total = [e[0].elapsed_time(e[2]) for e in evs]
+    return {"total_ms": sum(total), "stage_ms": [statistics.mean(stage0),
+                                                 statistics.mean(stage1)],
+            "wall_s": wall, "path": info.get("path"),
+            "launches_per_step": 2 + (1 if x_dev["cu_seqlens"] is not None else 0)}
+
+
+def time_e2e(mdn, x, x_dev, steps, warmup):
+    """Same metric through the public API from pinned host buffers: every
+    step copies its inputs host->device, runs, and reads o and the final
+    states back to pinned host memory."""
+    names = ["q", "k", "v", "alpha", "mu", "eta", "beta", "S0", "M0"]
+    host = {n: x[n].pin_memory() for n in names if x[n] is not None}
+    dev = {n: torch.empty_like(x_dev[n]) for n in host}
+    o_h = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
+    S_h = torch.empty((x["n_seq"], x["H"], x["D"], x["D"])).pin_memory()
+    M_h = torch.empty_like(S_h).pin_memory()
+    o = torch.empty_like(x_dev["v"])
+    S_T = torch.empty((x["n_seq"], x["H"], x["D"], x["D"]), device=o.device)
+    M_T = torch.empty_like(S_T)
+    need = mdn.workspace_size(x["n_seq"], x["B"] * x["T"], x["H"], x["D"], x["q"].dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=o.device)
+    cu = x_dev["cu_seqlens"]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in (o_h, S_h, M_h))
+
+    def step():
+        for n, t in host.items():
+            dev[n].copy_(t, non_blocking=True)
+        mdn.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["mu"],
+                      dev["eta"], dev.get("beta"), dev.get("S0"), dev.get("M0"),
+                      cu_seqlens=cu, o=o, S_T=S_T, M_T=M_T, workspace=ws)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S_T, non_blocking=True)
+        M_h.copy_(M_T, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()          # the result is on the host now
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times), h2d, d2h
+
+
+def time_decode(mdn, steps, dev, peaks):
+    w = W.DECODE
+    S0, M0 = W.make_decode_state(w, device=dev)
+    xs = W.make_decode_steps(w, steps, device=dev)
+    o = torch.empty_like(xs["v"][0])
+    S, M = S0.clone(), M0.clone()
+    for t in range(3):                        # warm-up on a scratch copy
+        mdn.decode_step(xs["q"][t], xs["k"][t], xs["v"][t], xs["alpha"][t],
+                        xs["mu"][t], xs["eta"][t], S, M, o=o)
+    S.copy_(S0)
+    M.copy_(M0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for t in range(steps):
+        mdn.decode_step(xs["q"][t], xs["k"][t], xs["v"][t], xs["alpha"][t],
+                        xs["mu"][t], xs["eta"][t], S, M, o=o)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    st = mdn.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after decode" % st)
+    N, H, D = w.B, w.H, w.D
+    bytes_step = (N * H * D * D * 4 * 4            # S, M read + write
+                  + N * H * D * 2 * 4              # q, k, v read, o write (bf16)
+                  + N * H * 4 * 3)                 # gates
+    per_step_s = ms / 1e3 / steps
+    achieved = bytes_step / per_step_s / 1e9
+    return {"metric": "MDN decode steps/s", "value": steps / (ms / 1e3),
+            "unit": "steps/s", "tokens_per_s": N * steps / (ms / 1e3),
+            "steps": steps, "ms_per_step": ms / steps,
+            "config": {"workload": w.name, "N": N, "H": H, "d_k": D, "d_v": D,
+                       "inputs": "bf16", "states": "fp32, in place",
+                       "l2": "states (1.07 GB) exceed L2; no flush"},
+            "gpu_launches": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic_record("decode_step", os.path.join(
+                             ROOT, "momentum_delta_rule_gb300", "csrc", "mdn_decode.cu"))}}
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(val, world, dev):
+    if world == 1:
+        return val
+    import torch.distributed as dist
+    t = torch.tensor([val], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import momentum_delta_rule_gb300 as mdn
+    mdn.lib()                                    # fails loudly if not built
+    peaks, peak_src = load_peaks()
+    w = W.BY_NAME[args.workload]
+    x = W.make_prefill(w)
+    x_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    clocks = ClockSampler(local).start()
+    r = time_prefill(mdn, x_dev, w, args.steps, args.warmup, world, flush)
+    clk = clocks.stop()
+    max_ms = max_over_ranks(r["total_ms"], world, dev)
+    tokens = sum(seq_lengths(x))
+    ms_per_step = max_ms / args.steps
+    value = world * tokens / (ms_per_step / 1e3)
+
+    # dominant kernel roofline (per launch, live CUDA-event duration)
+    d = x["D"]
+    fl = flops_per_token_head(d)
+    th = tokens * x["H"]
+    stage = max(range(2), key=lambda i: r["stage_ms"][i])
+    stage_name = ["prep", "state"][stage]
+    tensor = r["path"] == 1
+    flops = fl[stage_name] * th
+    kernel_s = r["stage_ms"][stage] / 1e3
+    if tensor:
+        peak, bound = peaks["bf16_tflops"], "tensor"
+    else:
+        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
+        peak, bound = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12, "alu"
+    achieved = flops / kernel_s / 1e12
+    src = os.path.join(ROOT, "momentum_delta_rule_gb300", "csrc",
+                       "mdn_chunk_tc.cu" if tensor else "mdn_chunk_simt.cu")
+    kernel_key = ("chunk_%s_%s" % (stage_name, "tc" if tensor else "simt"))
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic_record(kernel_key, src),
+                "kernel": kernel_key, "kernel_ms": r["stage_ms"][stage],
+                "flops_per_launch": flops,
+                "peak_source": ("%s bf16 burst" % peak_src) if tensor else
+                "fp32 FFMA from unit counts: 152 SMs x 128 lanes x 2 x %.0f MHz"
+                % peaks.get("sm_max_mhz", 2070.0),
+                "hbm_bytes_per_launch_algorithmic": state_pass_bytes(
+                    x, 34816) if stage_name == "state" else None,
+                "stage_ms": {"prep": r["stage_ms"][0], "state": r["stage_ms"][1]}}
+
+    line = {"metric": "MDN chunkwise fwd tokens/s", "value": value,
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if tensor else "f32", "data": "synthetic",
+            "config": config_of(w, x, "flushed (256 MiB write) before every timed step"),
+            "gpu_launches": r["launches_per_step"] * args.steps,
+            "path": "tensor_core" if tensor else "cuda_core",
+            "roofline": roofline, "clocks": clk, "peaks": peak_src}
+
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
+        e_ms = max_over_ranks(e_ms, world, dev)
+        line["e2e"] = {"value": world * tokens / (e_ms / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e_ms}
+    if not args.no_decode:
+        line["decode"] = time_decode(mdn, args.decode_steps, dev, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_oracle(x, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -124,6 +124,33 @@ mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
                          int H, int dk, int dv, mdn_dtype dtype, int chunk,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/* Implementation paths of mdn_chunk_fwd (reported by the profiled variant). */
+typedef enum mdn_path {
+    MDN_PATH_CUDA_CORE = 0,   /* fp32 FFMA kernels: fp32 inputs, head size 64 */
+    MDN_PATH_TENSOR_CORE = 1  /* tcgen05 kernels: bf16 inputs, head size 128 */
+} mdn_path;
+
+/*
+ * mdn_chunk_fwd_profiled — exactly mdn_chunk_fwd (same arguments, same
+ * results, same errors) plus two instrumentation outputs:
+ *   stage_events    NULL, or an array of n_stage_events cudaEvent_t handles
+ *                   (as void*) created by the caller.  Event i is recorded on
+ *                   `stream` before stage i; the last one after the last
+ *                   stage.  Stages: 0 = per-chunk preparation (offsets,
+ *                   coefficients, Gram matrices, triangular inverse),
+ *                   1 = sequential state pass (residuals, outputs, carry).
+ *                   n_stage_events must be 0 or 3.
+ *   path_out        NULL, or receives the mdn_path that ran.
+ */
+mdn_status mdn_chunk_fwd_profiled(
+    const void *q, const void *k, const void *v, const float *alpha,
+    const float *mu, const float *eta, const float *beta, const float *S0,
+    const float *M0, void *o, float *S_T, float *M_T,
+    const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
+    mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
+    void *stream, void *const *stage_events, int n_stage_events,
+    int *path_out);
+
 /*
  * mdn_decode_step — one recurrent step for N sequences (one token each),
  * updating both states in place.

@@ -1,0 +1,248 @@
+"""Momentum DeltaNet (MDN) memory update on GB300 — Python binding.
+
+A thin ctypes layer over the C ABI in ``include/mdn.h`` (``libmdn.so``, built
+in-tree by ``momentum_delta_rule_gb300.build``).  It only marshals arguments:
+checks dtypes, devices and contiguity, allocates outputs and the workspace
+with PyTorch, passes raw device pointers and the current CUDA stream.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+other code path.  If the library is missing, every call raises.
+
+Entry points (same names as the C ABI):
+  chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
+            cu_seqlens=None, ...)               -> (o, S_T, M_T)
+  decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None) -> o
+  workspace_size(n_seq, T_total, H, D, dtype)
+  device_status(stream=None), abi_version(), status_string(code)
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = ["chunk_fwd", "decode_step", "workspace_size", "device_status",
+           "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
+           "EXPORTED_SYMBOLS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmdn.so")
+
+MDN_OK = 0
+MDN_ERR_INVALID_ARG = 1
+MDN_ERR_UNSUPPORTED = 2
+MDN_ERR_CUDA = 3
+MDN_ERR_DEVICE_TIMEOUT = 4
+MDN_F32 = 0
+MDN_BF16 = 1
+CHUNK = 64
+
+EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
+                    "mdn_chunk_fwd_workspace_size", "mdn_chunk_fwd",
+                    "mdn_chunk_fwd_profiled", "mdn_decode_step",
+                    "mdn_get_device_status"]
+MDN_PATH_CUDA_CORE = 0
+MDN_PATH_TENSOR_CORE = 1
+
+_LIB = None
+
+
+class MdnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def lib():
+    """Load ``libmdn.so`` once; raise if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            "libmdn.so not found at %s; build it with "
+            "`python -m momentum_delta_rule_gb300.build`" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, fp, ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    c_int, c_size = ctypes.c_int, ctypes.c_size_t
+    L.mdn_abi_version.restype = c_int
+    L.mdn_abi_version.argtypes = []
+    L.mdn_status_string.restype = ctypes.c_char_p
+    L.mdn_status_string.argtypes = [c_int]
+    L.mdn_chunk_fwd_workspace_size.restype = c_size
+    L.mdn_chunk_fwd_workspace_size.argtypes = [c_int] * 5 + [c_int]
+    L.mdn_chunk_fwd.restype = c_int
+    L.mdn_chunk_fwd.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, ip]
+                                + [c_int] * 8 + [vp, c_size, vp])
+    L.mdn_chunk_fwd_profiled.restype = c_int
+    L.mdn_chunk_fwd_profiled.argtypes = (L.mdn_chunk_fwd.argtypes
+                                         + [ctypes.POINTER(ctypes.c_void_p), c_int,
+                                            ctypes.POINTER(ctypes.c_int)])
+    L.mdn_decode_step.restype = c_int
+    L.mdn_decode_step.argtypes = [vp] * 3 + [fp] * 6 + [vp] + [c_int] * 5 + [vp]
+    L.mdn_get_device_status.restype = c_int
+    L.mdn_get_device_status.argtypes = [vp]
+    _LIB = L
+    return L
+
+
+def abi_version():
+    return lib().mdn_abi_version()
+
+
+def status_string(code):
+    try:
+        return lib().mdn_status_string(int(code)).decode()
+    except RuntimeError:
+        return "status %d" % code
+
+
+def _dtype_code(t):
+    if t == torch.bfloat16:
+        return MDN_BF16
+    if t == torch.float32:
+        return MDN_F32
+    raise TypeError("q/k/v must be float32 or bfloat16, got %s" % t)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device, stream):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_cuda(name, t, dtype=None, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def workspace_size(n_seq, T_total, H, D, dtype):
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().mdn_chunk_fwd_workspace_size(n_seq, T_total, H, D, D, code))
+
+
+def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
+              cu_seqlens=None, o=None, S_T=None, M_T=None,
+              output_final_state=True, workspace=None, stream=None,
+              stage_events=None, info=None):
+    """Prefill over whole sequences (``mdn_chunk_fwd``).
+
+    q, k ``[B, T, H, D]`` and v ``[B, T, H, D]`` (fp32 or bf16, same dtype);
+    gates ``[B, T, H]`` fp32; S0/M0 ``[n_seq, H, D, D]`` fp32 or None;
+    ``cu_seqlens`` int32 CUDA tensor ``[n_seq + 1]`` for packed sequences
+    (then B == 1).  Returns ``(o, S_T, M_T)``; the states are None when
+    ``output_final_state`` is False.
+    """
+    L = lib()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, D]")
+    B, T, H, D = q.shape
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype, dev)
+        if tuple(t.shape) != (B, T, H, D):
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), (B, T, H, D)))
+    for name, t in (("alpha", alpha), ("mu", mu), ("eta", eta), ("beta", beta)):
+        if name != "beta" and t is None:
+            raise ValueError("%s is required" % name)
+        _check_cuda(name, t, torch.float32, dev)
+        if t is not None and tuple(t.shape) != (B, T, H):
+            raise ValueError("%s must be [B, T, H]" % name)
+    if cu_seqlens is not None:
+        _check_cuda("cu_seqlens", cu_seqlens, torch.int32, dev)
+        n_seq = cu_seqlens.numel() - 1
+    else:
+        n_seq = B
+    for name, t in (("S0", S0), ("M0", M0)):
+        _check_cuda(name, t, torch.float32, dev)
+        if t is not None and tuple(t.shape) != (n_seq, H, D, D):
+            raise ValueError("%s must be [n_seq, H, D, D]" % name)
+    if o is None:
+        o = torch.empty_like(v)
+    _check_cuda("o", o, q.dtype, dev)
+    if output_final_state:
+        if S_T is None:
+            S_T = torch.empty((n_seq, H, D, D), dtype=torch.float32, device=dev)
+        if M_T is None:
+            M_T = torch.empty((n_seq, H, D, D), dtype=torch.float32, device=dev)
+    _check_cuda("S_T", S_T, torch.float32, dev)
+    _check_cuda("M_T", M_T, torch.float32, dev)
+    need = int(L.mdn_chunk_fwd_workspace_size(n_seq, B * T, H, D, D, code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace, torch.uint8, dev)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(mu), _ptr(eta),
+            _ptr(beta), _ptr(S0), _ptr(M0), _ptr(o), _ptr(S_T), _ptr(M_T),
+            _ptr(cu_seqlens), n_seq, B, T, H, D, D, code, CHUNK,
+            _ptr(workspace), workspace.numel(), _stream_handle(dev, stream))
+    with torch.cuda.device(dev):
+        if stage_events is None and info is None:
+            st = L.mdn_chunk_fwd(*args)
+        else:
+            n_ev = 0 if stage_events is None else len(stage_events)
+            for e in (stage_events or []):
+                if e.cuda_event == 0:       # torch creates events lazily
+                    e.record(torch.cuda.current_stream(dev) if stream is None else stream)
+            arr = (ctypes.c_void_p * max(n_ev, 1))(
+                *[ctypes.c_void_p(e.cuda_event) for e in (stage_events or [])])
+            path = ctypes.c_int(-1)
+            st = L.mdn_chunk_fwd_profiled(*args, arr if n_ev else None, n_ev,
+                                          ctypes.byref(path))
+            if info is not None:
+                info["path"] = path.value
+    if st != MDN_OK:
+        raise MdnError(st, "mdn_chunk_fwd")
+    return o, S_T, M_T
+
+
+def decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None, stream=None):
+    """One recurrent step per sequence (``mdn_decode_step``), S and M in place.
+
+    q, k, v ``[N, H, D]``; gates ``[N, H]`` fp32; S, M ``[N, H, D, D]`` fp32.
+    Returns o ``[N, H, D]`` in the dtype of q.
+    """
+    L = lib()
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, D]")
+    N, H, D = q.shape
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype, dev)
+        if tuple(t.shape) != (N, H, D):
+            raise ValueError("%s must be [N, H, D]" % name)
+    for name, t in (("alpha", alpha), ("mu", mu), ("eta", eta), ("beta", beta)):
+        _check_cuda(name, t, torch.float32, dev)
+        if t is not None and tuple(t.shape) != (N, H):
+            raise ValueError("%s must be [N, H]" % name)
+    for name, t in (("S", S), ("M", M)):
+        _check_cuda(name, t, torch.float32, dev)
+        if tuple(t.shape) != (N, H, D, D):
+            raise ValueError("%s must be [N, H, D, D]" % name)
+    if o is None:
+        o = torch.empty_like(v)
+    _check_cuda("o", o, q.dtype, dev)
+    with torch.cuda.device(dev):
+        st = L.mdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(mu),
+                               _ptr(eta), _ptr(beta), _ptr(S), _ptr(M), _ptr(o),
+                               N, H, D, D, code, _stream_handle(dev, stream))
+    if st != MDN_OK:
+        raise MdnError(st, "mdn_decode_step")
+    return o
+
+
+def device_status(stream=None, device=None):
+    """Synchronise and read/clear the device status word (``MDN_OK`` = 0)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        return lib().mdn_get_device_status(_stream_handle(dev, stream))

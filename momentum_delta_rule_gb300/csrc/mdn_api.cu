@@ -1,0 +1,257 @@
+// C ABI of the MDN library: argument validation, workspace layout, dispatch
+// and the device status word.  Declarations and the contract: include/mdn.h.
+#include <stdint.h>
+#include <string.h>
+
+#include "mdn_internal.cuh"
+
+// Device status word (one per device that loads the library).  Kernels with
+// bounded waits write MDN_ERR_DEVICE_TIMEOUT here instead of hanging.
+__device__ int g_mdn_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int checked;      // 0 = unknown, 1 = supported, -1 = unsupported
+    int *status;      // device address of g_mdn_status
+};
+DeviceInfo g_dev[kMaxDevices];
+
+bool aligned16(const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+// Supported device (compute capability 10.3) and its status-word address.
+mdn_status current_device(int **status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return MDN_ERR_UNSUPPORTED;
+    DeviceInfo &di = g_dev[dev];
+    if (di.checked == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return MDN_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
+            di.checked = -1;
+        } else {
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_mdn_status) != cudaSuccess) {
+                cudaGetLastError();
+                return MDN_ERR_CUDA;
+            }
+            di.status = static_cast<int *>(addr);
+            di.checked = 1;
+        }
+    }
+    if (di.checked < 0) return MDN_ERR_UNSUPPORTED;
+    *status = di.status;
+    return MDN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Upper bound on the chunk slots of any split of T_total into n_seq
+// sequences: sum ceil(L_s / 64) <= floor(T_total / 64) + n_seq.
+long chunk_slots_bound(int n_seq, int T_total) {
+    return (long)(T_total / mdn::kChunk) + (long)n_seq;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mdn_abi_version(void) { return MDN_ABI_VERSION; }
+
+const char *mdn_status_string(mdn_status status) {
+    switch (status) {
+        case MDN_OK: return "MDN_OK: success";
+        case MDN_ERR_INVALID_ARG: return "MDN_ERR_INVALID_ARG: invalid argument";
+        case MDN_ERR_UNSUPPORTED: return "MDN_ERR_UNSUPPORTED: unsupported size, chunk or device";
+        case MDN_ERR_CUDA: return "MDN_ERR_CUDA: a CUDA call or kernel launch failed";
+        case MDN_ERR_DEVICE_TIMEOUT: return "MDN_ERR_DEVICE_TIMEOUT: a bounded device-side wait expired";
+    }
+    return "MDN: unknown status";
+}
+
+size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
+                                    int dv, mdn_dtype dtype) {
+    if (n_seq < 0 || T_total < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
+    if (dtype != MDN_F32 && dtype != MDN_BF16) return 0;
+    const size_t offsets = round256(sizeof(int32_t) * ((size_t)n_seq + 1));
+    const size_t prep = (size_t)chunk_slots_bound(n_seq, T_total) * (size_t)H *
+                        mdn::kPrepBytesMax;
+    return round256(offsets + prep);
+}
+
+mdn_status mdn_chunk_fwd_profiled(
+    const void *q, const void *k, const void *v, const float *alpha,
+    const float *mu, const float *eta, const float *beta, const float *S0,
+    const float *M0, void *o, float *S_T, float *M_T,
+    const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
+    mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
+    void *stream, void *const *stage_events, int n_stage_events,
+    int *path_out) {
+    if (n_stage_events != 0 && n_stage_events != 3) return MDN_ERR_INVALID_ARG;
+    if (n_stage_events && !stage_events) return MDN_ERR_INVALID_ARG;
+    for (int i = 0; i < n_stage_events; ++i)
+        if (!stage_events[i]) return MDN_ERR_INVALID_ARG;
+    // ---- shapes
+    if (B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || n_seq < 0)
+        return MDN_ERR_INVALID_ARG;
+    if (dtype != MDN_F32 && dtype != MDN_BF16) return MDN_ERR_INVALID_ARG;
+    if (cu_seqlens) {
+        if (B != 1) return MDN_ERR_INVALID_ARG;
+    } else if (n_seq != B) {
+        return MDN_ERR_INVALID_ARG;
+    }
+    if (chunk != mdn::kChunk) return MDN_ERR_UNSUPPORTED;
+    if (dk != dv || (dk != 64 && dk != 128)) return MDN_ERR_UNSUPPORTED;
+    const long T_total = (long)B * T;
+    if (T_total > 0x7fffffffL / 2) return MDN_ERR_INVALID_ARG;
+    if ((long)T_total * H * dk > 0x7fffffffffffL) return MDN_ERR_INVALID_ARG;
+    // ---- pointers
+    if (!alpha || !mu || !eta) return MDN_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !o)) return MDN_ERR_INVALID_ARG;
+    const void *ptrs16[] = {q, k, v, o, S0, M0, S_T, M_T};
+    for (const void *ptr : ptrs16)
+        if (ptr && !aligned16(ptr)) return MDN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {alpha, mu, eta, beta, cu_seqlens};
+    for (const void *ptr : ptrs4)
+        if (ptr && ((uintptr_t)ptr & 3u)) return MDN_ERR_INVALID_ARG;
+    if ((S_T && S_T != S0 && S0 && (const void *)S_T == (const void *)M0) ||
+        (M_T && M_T != M0 && M0 && (const void *)M_T == (const void *)S0))
+        return MDN_ERR_INVALID_ARG;
+    if (S_T && M_T && S_T == M_T) return MDN_ERR_INVALID_ARG;
+    const size_t need = mdn_chunk_fwd_workspace_size(n_seq, (int)T_total, H, dk, dv, dtype);
+    if (n_seq > 0 && T_total > 0) {
+        if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
+            return MDN_ERR_INVALID_ARG;
+    }
+
+    int *status = nullptr;
+    mdn_status st = current_device(&status);
+    if (st != MDN_OK) return st;
+    if (n_seq == 0) return MDN_OK;
+
+    mdn::ChunkProblem p;
+    memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v;
+    p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
+    p.S0 = S0; p.M0 = M0; p.o = o; p.S_T = S_T; p.M_T = M_T;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seq = n_seq; p.B = B; p.T = T; p.H = H; p.D = dk;
+    p.T_total = (int)T_total;
+    p.dtype = dtype;
+    p.status = status;
+    if (cu_seqlens) {
+        p.max_chunks = (int)chunk_slots_bound(n_seq, (int)T_total);
+    } else {
+        p.max_chunks = B * ((T + mdn::kChunk - 1) / mdn::kChunk);
+    }
+    if (T_total == 0) p.max_chunks = 0;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const size_t off_bytes = round256(sizeof(int32_t) * ((size_t)n_seq + 1));
+    p.chunk_offsets = reinterpret_cast<int32_t *>(ws);
+    p.prep = ws ? ws + off_bytes : nullptr;
+    p.prep_stride = mdn::kPrepBytesMax;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    for (int i = 0; i < n_stage_events; ++i) ev[i] = static_cast<cudaEvent_t>(stage_events[i]);
+    const int path = MDN_PATH_CUDA_CORE;
+    if (path_out) *path_out = path;
+    cudaError_t err = cudaSuccess;
+    if (ev[0]) err = cudaEventRecord(ev[0], cs);
+    if (err == cudaSuccess && cu_seqlens && p.max_chunks > 0)
+        err = mdn::launch_chunk_offsets(p, cs);
+    if (err == cudaSuccess) err = mdn::launch_chunk_prep_simt(p, cs);
+    if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
+    if (err == cudaSuccess) err = mdn::launch_chunk_state_simt(p, cs);
+    if (err == cudaSuccess && ev[2]) err = cudaEventRecord(ev[2], cs);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    return MDN_OK;
+}
+
+mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *mu, const float *eta,
+                         const float *beta, const float *S0, const float *M0,
+                         void *o, float *S_T, float *M_T,
+                         const int32_t *cu_seqlens, int n_seq, int B, int T,
+                         int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    return mdn_chunk_fwd_profiled(q, k, v, alpha, mu, eta, beta, S0, M0, o,
+                                  S_T, M_T, cu_seqlens, n_seq, B, T, H, dk, dv,
+                                  dtype, chunk, workspace, workspace_bytes,
+                                  stream, nullptr, 0, nullptr);
+}
+
+mdn_status mdn_decode_step(const void *q, const void *k, const void *v,
+                           const float *alpha, const float *mu,
+                           const float *eta, const float *beta, float *S,
+                           float *M, void *o, int N, int H, int dk, int dv,
+                           mdn_dtype dtype, void *stream) {
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return MDN_ERR_INVALID_ARG;
+    if (dtype != MDN_F32 && dtype != MDN_BF16) return MDN_ERR_INVALID_ARG;
+    if (dk != dv || (dk != 64 && dk != 128)) return MDN_ERR_UNSUPPORTED;
+    if ((long)N * H > 0x7fffffffL / 4) return MDN_ERR_INVALID_ARG;
+    if (N > 0) {
+        if (!q || !k || !v || !alpha || !mu || !eta || !S || !M || !o)
+            return MDN_ERR_INVALID_ARG;
+        const void *ptrs16[] = {S, M};
+        for (const void *ptr : ptrs16)
+            if (!aligned16(ptr)) return MDN_ERR_INVALID_ARG;
+        const uintptr_t emask = dtype == MDN_BF16 ? 1u : 3u;
+        const void *ptrs_e[] = {q, k, v, o};
+        for (const void *ptr : ptrs_e)
+            if ((uintptr_t)ptr & emask) return MDN_ERR_INVALID_ARG;
+        const void *ptrs4[] = {alpha, mu, eta, beta};
+        for (const void *ptr : ptrs4)
+            if (ptr && ((uintptr_t)ptr & 3u)) return MDN_ERR_INVALID_ARG;
+        if (S == M) return MDN_ERR_INVALID_ARG;
+    }
+    int *status = nullptr;
+    mdn_status st = current_device(&status);
+    if (st != MDN_OK) return st;
+    if (N == 0) return MDN_OK;
+
+    mdn::DecodeProblem p;
+    p.q = q; p.k = k; p.v = v;
+    p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
+    p.S = S; p.M = M; p.o = o;
+    p.N = N; p.H = H; p.D = dk; p.dtype = dtype;
+    p.status = status;
+    if (mdn::launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    return MDN_OK;
+}
+
+mdn_status mdn_get_device_status(void *stream) {
+    int *status = nullptr;
+    mdn_status st = current_device(&status);
+    if (st != MDN_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    int value = 0;
+    const int zero = 0;
+    if (cudaMemcpy(&value, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    return value == 0 ? MDN_OK : (mdn_status)value;
+}
+
+}  // extern "C"

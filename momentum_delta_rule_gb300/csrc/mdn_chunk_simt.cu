@@ -1,0 +1,484 @@
+// MDN chunkwise forward, CUDA-core (FFMA) path.
+//
+// Serves fp32 inputs (where one bf16/tf32 tensor-core pass would not hold an
+// fp32-level error) and head size 64.  It follows the same two-stage plan as
+// the tensor-core path:
+//
+//   prep  (one CTA per chunk and head, all chunks in parallel)
+//         log-space prefix scans of alpha and mu, the coefficient matrix
+//         Gamma, the Gram matrices K K^T and Q K^T, the unit-lower-triangular
+//         system matrix, its inverse T and the intra-chunk output operator
+//         A_O T, written to a prepared block in the workspace;
+//   state (one CTA per sequence, head and 32-column slice, chunks in order)
+//         the state-dependent part of each chunk: residual right-hand side,
+//         residuals, outputs and the carry of S and M.
+//
+// Equations: "MDN: Parallelizing Stepwise Momentum for Delta Linear
+// Attention" slides, frames "Reorder the triangular sum ..." (Eqs. (7)-(9)),
+// "Solve the unknown residuals with a lower triangular system" (Eqs.
+// (15)-(18)), "Chunk outputs combine incoming states and local writes"
+// (Appendix C Eqs. (40)-(42)), backup frames on the one-row shift and on the
+// log-domain coefficients (Algorithm 1); reading notes sections 2.3-2.6.
+//
+// With p_i = alpha_i k_i the residual right-hand side simplifies:
+// Diag(abar_shifted) P = Diag(abar) K and Diag(b_shifted) P = Diag(b_{i-1}
+// alpha_i) K, so the state pass needs only K S_0 and K M_0.  Writing
+// R = V - Diag(abar) K S_0 + Diag(b_{i-1} alpha_i) K M_0, the residuals are
+// Vres = T R and the in-chunk output term is (A_O T) R.
+#include "mdn_internal.cuh"
+
+namespace mdn {
+namespace {
+
+constexpr int kThreads = 256;
+
+// ------------------------------------------------------------- offsets
+
+// off[s] = sum_{s' < s} ceil(len_{s'} / 64), s = 0..n_seq (one CTA).
+__global__ void __launch_bounds__(1024)
+chunk_offsets_kernel(const int32_t *cu, int n_seq, int32_t *off) {
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int base = 0; base < n_seq; base += 1024) {
+        const int s = base + threadIdx.x;
+        int32_t x = 0;
+        if (s < n_seq) x = (cu[s + 1] - cu[s] + kChunk - 1) / kChunk;
+        int32_t incl = x;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int32_t wbase = 0;
+        for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+        const int32_t c0 = carry;
+        if (s < n_seq) off[s] = c0 + wbase + incl - x;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = c0 + wbase + incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) off[n_seq] = carry;
+}
+
+// ---------------------------------------------------------------- prep
+
+template <int D>
+struct PrepSmem {
+    static constexpr int LD = D + 1;          // padded row stride of K, Q
+    static constexpr int LM = kChunk + 1;     // padded row stride of 64x64
+    static constexpr int kFloats =
+        2 * kChunk * LD + 4 * kChunk * LM + 10 * kChunk + 64;
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+// Inclusive sum over the 64 lanes of warps 0 and 1.  Every thread of the
+// block must call it (it synchronises the block).
+__device__ __forceinline__ float scan64(float x, float *xch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (warp == 0 && lane == 31) *xch = x;
+    __syncthreads();
+    if (warp == 1) x += *xch;
+    __syncthreads();
+    return x;
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(kThreads)
+chunk_prep_simt_kernel(ChunkProblem p) {
+    using SM = PrepSmem<D>;
+    constexpr int LD = SM::LD, LM = SM::LM;
+    const int gc = blockIdx.x, h = blockIdx.y;
+    ChunkLoc loc;
+    if (!locate_chunk(p, gc, loc)) return;
+    const int n = loc.n;
+    const int tid = threadIdx.x;
+
+    extern __shared__ float smem[];
+    float *Ks = smem;                      // [64][LD]
+    float *Qs = Ks + kChunk * LD;          // [64][LD]
+    float *G = Qs + kChunk * LD;           // Gamma [64][LM]
+    float *L = G + kChunk * LM;            // system matrix (strict lower)
+    float *Tm = L + kChunk * LM;           // its inverse
+    float *AO = Tm + kChunk * LM;          // output operator (lower)
+    float *va = AO + kChunk * LM;          // alpha
+    float *vb = va + kChunk;               // beta
+    float *ve = vb + kChunk;               // eta
+    float *vA = ve + kChunk;               // A_i = sum log alpha
+    float *vU = vA + kChunk;               // U'_i = sum of finite log mu
+    float *vZ = vU + kChunk;               // number of zero mu so far
+    float *vbb = vZ + kChunk;              // b_i
+    float *xch = vbb + kChunk;             // scan exchange
+
+    const size_t rs = (size_t)p.H * D;     // token row stride
+    const Tin *kg = static_cast<const Tin *>(p.k) + (size_t)loc.t0 * rs + (size_t)h * D;
+    const Tin *qg = static_cast<const Tin *>(p.q) + (size_t)loc.t0 * rs + (size_t)h * D;
+    for (int idx = tid; idx < kChunk * D; idx += kThreads) {
+        const int i = idx / D, d = idx - i * D;
+        float kv = 0.f, qv = 0.f;
+        if (i < n) {
+            kv = to_f32(kg[(size_t)i * rs + d]);
+            qv = to_f32(qg[(size_t)i * rs + d]);
+        }
+        Ks[i * LD + d] = kv;
+        Qs[i * LD + d] = qv;
+    }
+
+    // ---- gates and log-space prefix scans (lanes 0..63 = tokens)
+    float a = 1.f, mu = 0.f, be = 0.f, et = 0.f;
+    if (tid < kChunk && tid < n) {
+        const size_t gi = (size_t)(loc.t0 + tid) * p.H + h;
+        a = p.alpha[gi];
+        mu = p.mu[gi];
+        et = p.eta[gi];
+        be = p.beta ? p.beta[gi] : 1.f;
+    }
+    const bool zero_mu = (mu == 0.f);
+    const float A = scan64(tid < kChunk ? logf(a) : 0.f, xch);
+    const float U = scan64(tid < kChunk && !zero_mu ? logf(mu) : 0.f, xch);
+    const float Z = scan64(tid < kChunk && zero_mu ? 1.f : 0.f, xch);
+    if (tid < kChunk) {
+        va[tid] = a;
+        vb[tid] = be;
+        ve[tid] = et;
+        vA[tid] = A;
+        vU[tid] = U;
+        vZ[tid] = Z;
+    }
+    __syncthreads();
+
+    // ---- Gamma, column j per lane: gamma_{j,j} = beta_j and
+    //      gamma_{i,j} = alpha_i gamma_{i-1,j} + beta_i prod_{u=j+1}^{i} mu_u,
+    //      the product taken from the log-space prefix sums (exponent <= 0).
+    //      b_i = sum_{r<=i} beta_r exp(A_i - A_r) mubar_r (exponents <= 0).
+    if (tid < kChunk) {
+        const int j = tid;
+        float g = vb[j];
+        for (int i = 0; i < j; ++i) G[i * LM + j] = 0.f;
+        G[j * LM + j] = g;
+        for (int i = j + 1; i < kChunk; ++i) {
+            const float m = (vZ[i] == vZ[j]) ? expf(vU[i] - vU[j]) : 0.f;
+            g = va[i] * g + vb[i] * m;
+            G[i * LM + j] = g;
+        }
+        float bsum = 0.f;
+        for (int r = 0; r <= j; ++r) {
+            if (vZ[r] == 0.f) bsum += vb[r] * expf(vA[j] - vA[r] + vU[r]);
+        }
+        vbb[j] = bsum;
+    }
+    __syncthreads();
+
+    // ---- Gram tiles: thread owns a 4 x 4 block of both 64 x 64 products
+    {
+        const int ti = tid >> 4, tj = tid & 15;
+        float gk[4][4] = {}, gq[4][4] = {};
+        for (int d = 0; d < D; ++d) {
+            float kr[4], qr[4], kc[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                kr[r] = Ks[(4 * ti + r) * LD + d];
+                qr[r] = Qs[(4 * ti + r) * LD + d];
+                kc[r] = Ks[(4 * tj + r) * LD + d];
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    gk[r][c] += kr[r] * kc[c];
+                    gq[r][c] += qr[r] * kc[c];
+                }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * ti + r, j = 4 * tj + c;
+                // (P Khat^T) . Gamma_shifted: alpha_i (k_i.k_j) eta_j gamma_{i-1,j}, j < i
+                L[i * LM + j] = (j < i) ? va[i] * gk[r][c] * ve[j] * G[(i - 1) * LM + j] : 0.f;
+                // (Q Khat^T) . Gamma: (q_i.k_j) eta_j gamma_{i,j}, j <= i
+                AO[i * LM + j] = (j <= i) ? gq[r][c] * ve[j] * G[i * LM + j] : 0.f;
+                Tm[i * LM + j] = (i == j) ? 1.f : 0.f;
+            }
+    }
+    __syncthreads();
+
+    // ---- T = (I + L)^{-1} by forward substitution, one row at a time:
+    //      T[i][j] = -sum_{k=j}^{i-1} L[i][k] T[k][j]  (j < i)
+    {
+        const int j = tid >> 2, part = tid & 3;
+        for (int i = 1; i < kChunk; ++i) {
+            float s = 0.f;
+            if (j < i)
+                for (int k = j + part; k < i; k += 4) s += L[i * LM + k] * Tm[k * LM + j];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (j < i && part == 0) Tm[i * LM + j] = -s;
+            __syncthreads();
+        }
+    }
+
+    // ---- write the prepared block
+    unsigned char *blk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
+    float *Tg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffT);
+    float *AOTg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffAOT);
+    float *vec = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffVec);
+    {
+        const int ti = tid >> 4, tj = tid & 15;
+        float acc[4][4] = {};
+        for (int k = 0; k < kChunk; ++k) {
+            float ar[4], tc[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                ar[r] = AO[(4 * ti + r) * LM + k];
+                tc[r] = Tm[k * LM + 4 * tj + r];
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[r][c] += ar[r] * tc[c];
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * ti + r, j = 4 * tj + c;
+                AOTg[i * kChunk + j] = acc[r][c];
+                Tg[i * kChunk + j] = Tm[i * LM + j];
+            }
+    }
+    if (tid < kChunk) {
+        const int i = tid;
+        const bool valid = i < n;
+        const int last = n - 1;
+        const float abar = expf(vA[i]);
+        vec[kVecAbar * kChunk + i] = valid ? abar : 0.f;
+        vec[kVecBmA * kChunk + i] = (valid && i > 0) ? vbb[i - 1] * va[i] : 0.f;
+        vec[kVecB * kChunk + i] = valid ? vbb[i] : 0.f;
+        vec[kVecGS * kChunk + i] = valid ? G[last * LM + i] * ve[i] : 0.f;
+        const float mtail = (vZ[last] == vZ[i]) ? expf(vU[last] - vU[i]) : 0.f;
+        vec[kVecGM * kChunk + i] = valid ? mtail * ve[i] : 0.f;
+        float sc = 0.f;
+        if (i == 0) sc = expf(vA[last]);
+        if (i == 1) sc = vbb[last];
+        if (i == 2) sc = (vZ[last] == 0.f) ? expf(vU[last]) : 0.f;
+        if (i == 3) sc = (float)n;
+        vec[kVecScal * kChunk + i] = sc;
+    }
+}
+
+// --------------------------------------------------------------- state
+
+constexpr int kNS = 32;   // state columns per CTA
+
+template <int D>
+struct StateSmem {
+    static constexpr int kFloats = 2 * kChunk * D        // K, Q
+                                 + kChunk * kNS          // V slice
+                                 + 2 * kChunk * kChunk   // T, AOT
+                                 + kVecRows * kChunk     // vectors
+                                 + 2 * D * kNS           // S, M slices
+                                 + 2 * kChunk * kNS;     // R, scaled residuals
+    static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(kThreads)
+chunk_state_simt_kernel(ChunkProblem p) {
+    constexpr int kSlices = D / kNS;
+    constexpr int kRowsA = kChunk / (kThreads / 32);   // 8 token rows per warp
+    constexpr int kRowsC = D / (kThreads / 32);        // state rows per warp
+    const int slice = blockIdx.x % kSlices;
+    const int sh = blockIdx.x / kSlices;
+    const int s = sh / p.H, h = sh - s * p.H;
+    const int tid = threadIdx.x, cc = tid & 31, wg = tid >> 5;
+    const int col0 = slice * kNS;
+
+    extern __shared__ float smem[];
+    float *Ks = smem;
+    float *Qs = Ks + kChunk * D;
+    float *Vs = Qs + kChunk * D;
+    float *Ts = Vs + kChunk * kNS;
+    float *AOTs = Ts + kChunk * kChunk;
+    float *vec = AOTs + kChunk * kChunk;
+    float *Ss = vec + kVecRows * kChunk;
+    float *Ms = Ss + D * kNS;
+    float *Rs = Ms + D * kNS;
+    float *Vr = Rs + kChunk * kNS;
+
+    int start, len, slot0;
+    sequence_range(p, s, start, len, slot0);
+    const int nchunks = (len + kChunk - 1) / kChunk;
+    const size_t st_off = (size_t)sh * D * D;
+
+    for (int idx = tid; idx < D * kNS; idx += kThreads) {
+        const int d = idx / kNS, c = idx - d * kNS;
+        const size_t g = st_off + (size_t)d * D + col0 + c;
+        Ss[idx] = p.S0 ? p.S0[g] : 0.f;
+        Ms[idx] = p.M0 ? p.M0[g] : 0.f;
+    }
+
+    const size_t rs = (size_t)p.H * D;
+    const Tin *kg0 = static_cast<const Tin *>(p.k) + (size_t)h * D;
+    const Tin *qg0 = static_cast<const Tin *>(p.q) + (size_t)h * D;
+    const Tin *vg0 = static_cast<const Tin *>(p.v) + (size_t)h * D + col0;
+    Tin *og0 = static_cast<Tin *>(p.o) + (size_t)h * D + col0;
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int t0 = start + c * kChunk;
+        const int n = min(kChunk, len - c * kChunk);
+        const unsigned char *blk = p.prep + ((size_t)(slot0 + c) * p.H + h) * p.prep_stride;
+        const float *Tg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffT);
+        const float *AOTg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffAOT);
+        const float *vg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffVec);
+
+        __syncthreads();   // previous chunk finished with every buffer
+        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
+            const int i = idx / D, d = idx - i * D;
+            float kv = 0.f, qv = 0.f;
+            if (i < n) {
+                kv = to_f32(kg0[(size_t)(t0 + i) * rs + d]);
+                qv = to_f32(qg0[(size_t)(t0 + i) * rs + d]);
+            }
+            Ks[idx] = kv;
+            Qs[idx] = qv;
+        }
+        for (int idx = tid; idx < kChunk * kNS; idx += kThreads) {
+            const int i = idx / kNS, cx = idx - i * kNS;
+            Vs[idx] = (i < n) ? to_f32(vg0[(size_t)(t0 + i) * rs + cx]) : 0.f;
+        }
+        for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+            Ts[idx] = Tg[idx];
+            AOTs[idx] = AOTg[idx];
+        }
+        for (int idx = tid; idx < kVecRows * kChunk; idx += kThreads) vec[idx] = vg[idx];
+        __syncthreads();
+
+        // ---- K S_0, K M_0, Q S_0, Q M_0 for 8 token rows x 1 column
+        float ks[kRowsA] = {}, km[kRowsA] = {}, qs[kRowsA] = {}, qm[kRowsA] = {};
+        for (int d = 0; d < D; ++d) {
+            const float sv = Ss[d * kNS + cc], mv = Ms[d * kNS + cc];
+#pragma unroll
+            for (int r = 0; r < kRowsA; ++r) {
+                const int i = wg * kRowsA + r;
+                const float kv = Ks[i * D + d], qv = Qs[i * D + d];
+                ks[r] += kv * sv;
+                km[r] += kv * mv;
+                qs[r] += qv * sv;
+                qm[r] += qv * mv;
+            }
+        }
+        float oint[kRowsA];
+#pragma unroll
+        for (int r = 0; r < kRowsA; ++r) {
+            const int i = wg * kRowsA + r;
+            Rs[i * kNS + cc] = Vs[i * kNS + cc] - vec[kVecAbar * kChunk + i] * ks[r]
+                               + vec[kVecBmA * kChunk + i] * km[r];
+            oint[r] = vec[kVecAbar * kChunk + i] * qs[r] - vec[kVecB * kChunk + i] * qm[r];
+        }
+        __syncthreads();
+
+        // ---- residuals Vres = T R, outputs O = O_inter + (A_O T) R
+#pragma unroll
+        for (int r = 0; r < kRowsA; ++r) {
+            const int i = wg * kRowsA + r;
+            float vr = 0.f, oi = 0.f;
+            for (int j = 0; j <= i; ++j) {
+                const float rv = Rs[j * kNS + cc];
+                vr += Ts[i * kChunk + j] * rv;
+                oi += AOTs[i * kChunk + j] * rv;
+            }
+            Vr[i * kNS + cc] = vr;
+            if (i < n) og0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(oint[r] + oi);
+        }
+        __syncthreads();
+
+        // ---- carry, both from the old S_0, M_0:
+        //      S <- abar_n S - b_n M + sum_i k_i gamma_{n,i} eta_i vres_i^T
+        //      M <- mubar_n M - sum_i k_i (prod_{u>i} mu_u) eta_i vres_i^T
+        const float abar_n = vec[kVecScal * kChunk + 0];
+        const float b_n = vec[kVecScal * kChunk + 1];
+        const float mubar_n = vec[kVecScal * kChunk + 2];
+#pragma unroll 4
+        for (int r = 0; r < kRowsC; ++r) {
+            const int d = wg * kRowsC + r;
+            float as = 0.f, am = 0.f;
+            for (int i = 0; i < n; ++i) {
+                const float kv = Ks[i * D + d];
+                const float vv = Vr[i * kNS + cc];
+                as += kv * (vec[kVecGS * kChunk + i] * vv);
+                am += kv * (vec[kVecGM * kChunk + i] * vv);
+            }
+            const float so = Ss[d * kNS + cc], mo = Ms[d * kNS + cc];
+            Ss[d * kNS + cc] = abar_n * so - b_n * mo + as;
+            Ms[d * kNS + cc] = mubar_n * mo - am;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < D * kNS; idx += kThreads) {
+        const int d = idx / kNS, cx = idx - d * kNS;
+        const size_t g = st_off + (size_t)d * D + col0 + cx;
+        if (p.S_T) p.S_T[g] = Ss[idx];
+        if (p.M_T) p.M_T[g] = Ms[idx];
+    }
+}
+
+template <int D, typename Tin>
+cudaError_t launch_prep_t(const ChunkProblem &p, cudaStream_t st) {
+    if (p.max_chunks == 0) return cudaSuccess;
+    auto kp = chunk_prep_simt_kernel<D, Tin>;
+    cudaError_t err = cudaFuncSetAttribute(
+        kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepSmem<D>::kBytes);
+    if (err != cudaSuccess) return err;
+    dim3 grid(p.max_chunks, p.H);
+    kp<<<grid, kThreads, PrepSmem<D>::kBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, typename Tin>
+cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
+    auto ks = chunk_state_simt_kernel<D, Tin>;
+    cudaError_t err = cudaFuncSetAttribute(
+        ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)StateSmem<D>::kBytes);
+    if (err != cudaSuccess) return err;
+    const long blocks = (long)p.n_seq * p.H * (D / kNS);
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    ks<<<(unsigned)blocks, kThreads, StateSmem<D>::kBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
+    chunk_offsets_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.chunk_offsets);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st) {
+    if (p.D == 128) {
+        return p.dtype == MDN_BF16 ? launch_prep_t<128, __nv_bfloat16>(p, st)
+                                   : launch_prep_t<128, float>(p, st);
+    }
+    return p.dtype == MDN_BF16 ? launch_prep_t<64, __nv_bfloat16>(p, st)
+                               : launch_prep_t<64, float>(p, st);
+}
+
+cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st) {
+    if (p.D == 128) {
+        return p.dtype == MDN_BF16 ? launch_state_t<128, __nv_bfloat16>(p, st)
+                                   : launch_state_t<128, float>(p, st);
+    }
+    return p.dtype == MDN_BF16 ? launch_state_t<64, __nv_bfloat16>(p, st)
+                               : launch_state_t<64, float>(p, st);
+}
+
+}  // namespace mdn

@@ -1,0 +1,140 @@
+// Internal declarations shared by the MDN CUDA translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mdn.h"
+
+namespace mdn {
+
+constexpr int kChunk = 64;  // tokens per chunk (the pages' default C)
+
+// Per-(chunk, head) prepared block written by the prep kernel and read by the
+// state-pass kernel.  Matrices are row-major 64 x 64 of `MatT`; vectors fp32.
+//   T    = [I + (P Khat^T) . Gamma_shifted]^{-1}
+//   AOT  = [(Q Khat^T) . Gamma] T
+//   vec  = kVecRows rows of 64 fp32 (see VecRow)
+enum VecRow {
+    kVecAbar = 0,     // abar_i = prod_{r<=i} alpha_r        (also abar_{i-1} alpha_i)
+    kVecBmA = 1,      // b_{i-1} alpha_i  (b_0 = 0)
+    kVecB = 2,        // b_i
+    kVecGS = 3,       // gamma_{n,i} eta_i      (carry weight of S)
+    kVecGM = 4,       // prod_{u=i+1}^{n} mu_u eta_i (carry weight of M)
+    kVecScal = 5,     // [0] abar_n, [1] b_n, [2] mubar_n, [3] n (as float)
+    kVecRows = 8
+};
+
+template <typename MatT>
+struct PrepLayout {
+    static constexpr size_t kMatBytes = sizeof(MatT) * kChunk * kChunk;
+    static constexpr size_t kVecBytes = sizeof(float) * kChunk * kVecRows;
+    static constexpr size_t kOffT = 0;
+    static constexpr size_t kOffAOT = kMatBytes;
+    static constexpr size_t kOffVec = 2 * kMatBytes;
+    static constexpr size_t kBytes = 2 * kMatBytes + kVecBytes;
+};
+
+// Largest prepared block of any path (fp32 matrices).
+constexpr size_t kPrepBytesMax = PrepLayout<float>::kBytes;
+
+struct ChunkProblem {
+    const void *q, *k, *v;
+    const float *alpha, *mu, *eta, *beta;
+    const float *S0, *M0;
+    void *o;
+    float *S_T, *M_T;
+    const int32_t *cu_seqlens;   // device, or nullptr for equal lengths
+    int n_seq, B, T, H, D;       // dk == dv == D
+    int T_total;                 // B * T
+    int max_chunks;              // prepared-block slots per head
+    mdn_dtype dtype;
+    int32_t *chunk_offsets;      // [n_seq + 1] in the workspace (varlen only)
+    unsigned char *prep;         // max_chunks * H prepared blocks
+    size_t prep_stride;          // bytes per prepared block
+    int *status;                 // device status word
+};
+
+struct DecodeProblem {
+    const void *q, *k, *v;
+    const float *alpha, *mu, *eta, *beta;
+    float *S, *M;
+    void *o;
+    int N, H, D;
+    mdn_dtype dtype;
+    int *status;
+};
+
+// Launchers (return the first CUDA error, or cudaSuccess).
+cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
+cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
+cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
+
+// ---------------------------------------------------------------- device
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Where chunk `gc` (a global chunk slot) lives.  Equal-length batches chunk
+// every sequence of T tokens from its own start; packed varlen batches use
+// the per-sequence chunk offsets computed on the device.
+struct ChunkLoc {
+    int seq;     // sequence index
+    int t0;      // first token (row of the packed [T_total, H, *] tensors)
+    int n;       // tokens in this chunk, 1..64
+};
+
+__device__ __forceinline__ bool locate_chunk(const ChunkProblem &p, int gc,
+                                             ChunkLoc &loc) {
+    if (p.cu_seqlens == nullptr) {
+        const int cps = (p.T + kChunk - 1) / kChunk;
+        if (cps == 0) return false;
+        const int s = gc / cps;
+        if (s >= p.n_seq) return false;
+        const int c = gc - s * cps;
+        loc.seq = s;
+        loc.t0 = s * p.T + c * kChunk;
+        loc.n = min(kChunk, p.T - c * kChunk);
+        return true;
+    }
+    const int32_t *off = p.chunk_offsets;
+    if (gc >= off[p.n_seq]) return false;
+    // largest s with off[s] <= gc (empty sequences have off[s] == off[s+1])
+    int lo = 0, hi = p.n_seq;     // off[lo] <= gc < off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= gc) lo = mid; else hi = mid;
+    }
+    const int c = gc - off[lo];
+    const int start = p.cu_seqlens[lo];
+    const int len = p.cu_seqlens[lo + 1] - start;
+    loc.seq = lo;
+    loc.t0 = start + c * kChunk;
+    loc.n = min(kChunk, len - c * kChunk);
+    return true;
+}
+
+// Token range and chunk-slot base of one sequence.
+__device__ __forceinline__ void sequence_range(const ChunkProblem &p, int s,
+                                               int &start, int &len,
+                                               int &slot0) {
+    if (p.cu_seqlens == nullptr) {
+        start = s * p.T;
+        len = p.T;
+        slot0 = s * ((p.T + kChunk - 1) / kChunk);
+    } else {
+        start = p.cu_seqlens[s];
+        len = p.cu_seqlens[s + 1] - start;
+        slot0 = len > 0 ? p.chunk_offsets[s] : 0;   // offsets exist only if T > 0
+    }
+}
+
+}  // namespace mdn

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments with a status (no GPU needed:
+validation runs before any device work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import momentum_delta_rule_gb300 as mdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "mdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mdn_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from momentum_delta_rule_gb300 import build
+    build.build()
+    return mdn.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared_functions()
+    assert set(declared) == set(mdn.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_version_and_strings(L):
+    assert mdn.abi_version() == 1
+    for code in range(5):
+        s = mdn.status_string(code)
+        assert s.startswith("MDN")
+    assert "unknown" in mdn.status_string(99)
+
+
+def test_workspace_size(L):
+    a = mdn.workspace_size(8, 16384, 8, 128, 1)
+    assert a > 0 and a % 256 == 0
+    assert mdn.workspace_size(-1, 10, 1, 64, 1) == 0
+    assert mdn.workspace_size(1, 10, 1, 64, 7) == 0
+    # monotone in the number of tokens and heads
+    assert mdn.workspace_size(8, 16384, 16, 128, 1) > a
+
+
+FAKE = ctypes.c_void_p(0x10000)       # a non-null pointer never dereferenced
+
+
+def _chunk(L, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
+                beta=None, S0=None, M0=None, o=FAKE, S_T=None, M_T=None,
+                cu=None, n_seq=2, B=2, T=64, H=2, dk=128, dv=128, dtype=1,
+                chunk=64, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    return L.mdn_chunk_fwd(args["q"], args["k"], args["v"], args["alpha"],
+                           args["mu"], args["eta"], args["beta"], args["S0"],
+                           args["M0"], args["o"], args["S_T"], args["M_T"],
+                           args["cu"], args["n_seq"], args["B"], args["T"],
+                           args["H"], args["dk"], args["dv"], args["dtype"],
+                           args["chunk"], args["ws"], args["ws_bytes"],
+                           args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(alpha=None), 1), (dict(o=None), 1),
+    (dict(H=0), 1), (dict(T=-1), 1), (dict(n_seq=3), 1), (dict(dtype=5), 1),
+    (dict(q=ctypes.c_void_p(0x10008)), 1), (dict(ws=None), 1),
+    (dict(ws_bytes=16), 1), (dict(ws=ctypes.c_void_p(0x10010)), 1),
+    (dict(cu=FAKE, B=2), 1),
+    (dict(S_T=FAKE, M_T=FAKE), 1),
+    (dict(chunk=32), 2), (dict(dk=96, dv=96), 2), (dict(dk=128, dv=64), 2),
+])
+def test_chunk_fwd_rejects(L, over, code):
+    assert _chunk(L, **over) == code
+
+
+def _decode(L, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
+                beta=None, S=FAKE, M=ctypes.c_void_p(0x20000), o=FAKE, N=4,
+                H=2, dk=128, dv=128, dtype=1, stream=None)
+    args.update(over)
+    return L.mdn_decode_step(args["q"], args["k"], args["v"], args["alpha"],
+                             args["mu"], args["eta"], args["beta"], args["S"],
+                             args["M"], args["o"], args["N"], args["H"],
+                             args["dk"], args["dv"], args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=None), 1), (dict(q=None), 1), (dict(N=-1), 1), (dict(H=0), 1),
+    (dict(S=ctypes.c_void_p(0x10004)), 1), (dict(M=FAKE), 1),
+    (dict(q=ctypes.c_void_p(0x10001)), 1), (dict(dtype=3), 1),
+    (dict(dk=32, dv=32), 2), (dict(dk=64, dv=128), 2),
+])
+def test_decode_rejects(L, over, code):
+    assert _decode(L, **over) == code
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+    x = torch.zeros(1, 64, 1, 64)
+    g = torch.zeros(1, 64, 1)
+    with pytest.raises(ValueError):
+        mdn.chunk_fwd(x, x, x, g, g, g)

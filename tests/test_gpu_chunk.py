@@ -1,0 +1,123 @@
+"""GPU parity of mdn_chunk_fwd (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output; the full-size workloads run exactly as the
+bench launches them and compare sampled independent (sequence, head) chains,
+each against a full oracle run of that chain.
+"""
+import pytest
+import torch
+
+import workloads as W
+from tests._helpers import TOL, chains, compare, gpu_chunk_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(x, n, seed=0):
+    ch = chains(x)
+    g = torch.Generator().manual_seed(seed)
+    idx = torch.randperm(len(ch), generator=g)[:n].tolist()
+    return [ch[i] for i in sorted(idx)]
+
+
+def test_tiny_fp32_full_parity():
+    x = W.make_prefill(W.TINY_FP32)
+    out = gpu_chunk_fwd(x)
+    errs = compare(x, out, chains(x))
+    assert errs["o"] <= TOL["fp32"]
+
+
+def test_tiny_fp32_with_beta():
+    x = W.make_prefill(W.TINY_FP32, with_beta=True)
+    compare(x, gpu_chunk_fwd(x), chains(x))
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp32", 128), ("bf16", 64)])
+def test_small_ragged(T, dtype, D):
+    w = W.Workload("small", dtype=dtype, state="randn", seed=11)
+    x = W.make_prefill(w, B=2, T=T, H=2, D=D, with_beta=True)
+    compare(x, gpu_chunk_fwd(x), chains(x))
+
+
+def test_varlen_small_with_empty_sequences():
+    x = W.make_prefill(W.VARLEN_PACKED, H=2, lengths=[1, 64, 0, 65, 130, 7, 0])
+    compare(x, gpu_chunk_fwd(x), chains(x))
+
+
+def test_mu_zero_and_beta_zero():
+    w = W.Workload("edge", dtype="bf16", state="randn", seed=12)
+    x = W.make_prefill(w, B=1, T=150, H=2, D=128, with_beta=True)
+    x["mu"][:, ::5] = 0.0
+    x["mu"][:, 70:80] = 0.0
+    x["beta"][:, 3::7] = 0.0
+    x["alpha"][:, 100:110] = 1.0
+    compare(x, gpu_chunk_fwd(x), chains(x))
+
+
+def test_state_alias_and_optional_states():
+    import momentum_delta_rule_gb300 as mdn
+    w = W.Workload("alias", dtype="bf16", state="randn", seed=13)
+    x = W.make_prefill(w, B=2, T=100, H=2, D=128)
+    ref = gpu_chunk_fwd(x)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    S, M = d["S0"].clone(), d["M0"].clone()
+    o, S_T, M_T = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"],
+                                d["eta"], None, S, M, S_T=S, M_T=M)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref[0]) and torch.equal(S, ref[1]) and torch.equal(M, ref[2])
+    o2, S2, M2 = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"],
+                               d["eta"], None, d["S0"], d["M0"],
+                               output_final_state=False)
+    torch.cuda.synchronize()
+    assert S2 is None and M2 is None and torch.equal(o2, ref[0])
+
+
+def test_deterministic():
+    x = W.make_prefill(W.PREFILL_400M, B=2, T=300, H=4)
+    a = gpu_chunk_fwd(x)
+    b = gpu_chunk_fwd(x)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_split_sequence_state_passing():
+    """fwd(x) equals fwd(second half) started from fwd(first half)'s states."""
+    w = W.Workload("split", dtype="bf16", state="randn", seed=14)
+    x = W.make_prefill(w, B=1, T=256, H=2, D=128)
+    full = gpu_chunk_fwd(x)
+    first = dict(x)
+    for n in ("q", "k", "v", "alpha", "mu", "eta"):
+        first[n] = x[n][:, :128].contiguous()
+    first["T"] = 128
+    o1, S1, M1 = gpu_chunk_fwd(first)
+    second = dict(x)
+    for n in ("q", "k", "v", "alpha", "mu", "eta"):
+        second[n] = x[n][:, 128:].contiguous()
+    second["S0"], second["M0"] = S1.cpu(), M1.cpu()
+    o2, S2, M2 = gpu_chunk_fwd(second)
+    rel = lambda a, b: ((a.float() - b.float()).norm() / b.float().norm()).item()
+    assert rel(torch.cat([o1, o2], 1), full[0]) < 1e-2
+    assert rel(S2, full[1]) < 1e-3 and rel(M2, full[2]) < 1e-3
+
+
+# ---------------------------------------------------------------- full size
+
+def test_prefill_400m_full_size_sampled():
+    x = W.make_prefill(W.PREFILL_400M)
+    out = gpu_chunk_fwd(x)
+    compare(x, out, _sample(x, 4))
+
+
+def test_prefill_1p3b_long_full_size_sampled():
+    x = W.make_prefill(W.PREFILL_1P3B_LONG)
+    out = gpu_chunk_fwd(x)
+    compare(x, out, _sample(x, 2))
+
+
+def test_varlen_packed_full_size_sampled():
+    x = W.make_prefill(W.VARLEN_PACKED)
+    out = gpu_chunk_fwd(x)
+    ch = chains(x)
+    shortest = min(ch, key=lambda c: c[2].stop - c[2].start)
+    compare(x, out, _sample(x, 4) + [shortest])
