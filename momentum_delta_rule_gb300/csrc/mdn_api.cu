@@ -164,15 +164,19 @@ mdn_status mdn_chunk_fwd_profiled(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     for (int i = 0; i < n_stage_events; ++i) ev[i] = static_cast<cudaEvent_t>(stage_events[i]);
-    const int path = MDN_PATH_CUDA_CORE;
+    // bf16 inputs with head size 128 run on the tensor cores; fp32 inputs (an
+    // fp32-level error bound) and head size 64 on the CUDA cores.
+    const bool tensor = dtype == MDN_BF16 && dk == 128 && T_total > 0;
+    const int path = tensor ? MDN_PATH_TENSOR_CORE : MDN_PATH_CUDA_CORE;
     if (path_out) *path_out = path;
     cudaError_t err = cudaSuccess;
     if (ev[0]) err = cudaEventRecord(ev[0], cs);
     if (err == cudaSuccess && cu_seqlens && p.max_chunks > 0)
         err = mdn::launch_chunk_offsets(p, cs);
-    if (err == cudaSuccess) err = mdn::launch_chunk_prep_simt(p, cs);
+    if (err == cudaSuccess) err = mdn::launch_chunk_prep_simt(p, cs, tensor);
     if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
-    if (err == cudaSuccess) err = mdn::launch_chunk_state_simt(p, cs);
+    if (err == cudaSuccess)
+        err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_chunk_state_simt(p, cs);
     if (err == cudaSuccess && ev[2]) err = cudaEventRecord(ev[2], cs);
     if (err != cudaSuccess) {
         cudaGetLastError();

@@ -1,0 +1,459 @@
+// MDN chunkwise forward — sequential state pass on the 5th-generation tensor
+// cores (tcgen05, TMEM accumulators, TMA-staged operands), bf16 inputs, head
+// size 128.
+//
+// Chunk equations ("MDN: Parallelizing Stepwise Momentum for Delta Linear
+// Attention" slides, frames "Solve the unknown residuals with a lower
+// triangular system", Eqs. (15)-(18), and "Chunk outputs combine incoming
+// states and local writes", Appendix C Eqs. (40)-(42); reading notes 2.4-2.5),
+// with the chunk-local matrices T and A_O T and the coefficient vectors taken
+// from the prepared block of the prep kernel:
+//
+//   MMA1  D1 = [K; Q] [S_0 | M_0]          (M=128 tokens x2, N=2x64, K=dk)
+//         R  = V - Diag(abar) K S_0 + Diag(b_{i-1} alpha_i) K M_0
+//         O_inter = Diag(abar) Q S_0 - Diag(b) Q M_0
+//   MMA2  D2 = [T; A_O T] R                 (M=128, N=64, K=64 tokens)
+//         Vres = rows 0..63,  O = O_inter + rows 64..127
+//   MMA3  D3 = K^T [Diag(gS) Vres | Diag(gM) Vres]   (M=dk, N=2x64, K=64)
+//         S <- abar_n S - b_n M + D3[:, :64],  M <- mubar_n M - D3[:, 64:]
+//
+// with gS_i = gamma_{n,i} eta_i and gM_i = prod_{u>i} mu_u eta_i, both carries
+// computed from the old S_0, M_0.  The fp32 state lives in the registers of
+// the epilogue warps (row d of S and M in the thread that owns TMEM lane d of
+// D3); only its bf16 copy goes to shared memory as MMA1's B operand.
+//
+// One CTA owns one (sequence, head, 64-column slice): columns of S and M
+// evolve independently (column j of Vres depends only on column j of S_0 and
+// M_0), so the two slices of a head never communicate.
+//
+// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// 4..11 epilogue (TMEM lane quadrant = warp % 4, column half = (warp-4)/4).
+// Every wait is bounded (1 s); on expiry the CTA records
+// MDN_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "mdn_internal.cuh"
+#include "mdn_sm100.cuh"
+
+namespace mdn {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 128;                  // head size (dk = dv)
+constexpr int kNS = 64;                  // state columns per CTA
+constexpr int kSlices = kD / kNS;
+constexpr int kThreadsTC = 384;
+constexpr int kStages = 2;
+
+// shared memory (byte offsets from the 1024-aligned base)
+constexpr uint32_t kKQBytes = 32768;     // per 64-wide dk half: K rows, then Q rows
+constexpr uint32_t kVBytes = 8192;       // V slice, 64 tokens x 64 columns, swizzled
+constexpr uint32_t kPrepBytes = (uint32_t)PrepLayoutTC::kBytes;   // 18432
+constexpr uint32_t kOffV = kKQBytes;
+constexpr uint32_t kOffPrep = kKQBytes + kVBytes;
+constexpr uint32_t kStageBytes = kKQBytes + kVBytes + kPrepBytes;  // 59392
+constexpr uint32_t kOffB1 = kStages * kStageBytes;   // [S | M] bf16, dk rows x 128, MN-major
+constexpr uint32_t kB1Bytes = 32768;
+constexpr uint32_t kOffR = kOffB1 + kB1Bytes;        // R bf16, 64 token rows x 64, MN-major
+constexpr uint32_t kRBytes = 8192;
+constexpr uint32_t kOffB3 = kOffR + kRBytes;         // [gS Vres | gM Vres], 64 rows x 128
+constexpr uint32_t kB3Bytes = 16384;
+constexpr uint32_t kOffBar = kOffB3 + kB3Bytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+
+// tensor memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColD1 = 0;      // 128 columns
+constexpr uint32_t kColD2 = 128;    // 64 columns
+constexpr uint32_t kColD3 = 256;    // 128 columns
+
+struct Bars {
+    uint64_t full[kStages];    // TMA bytes of a stage landed
+    uint64_t empty[kStages];   // stage free again (MMA commit + 8 epilogue warps)
+    uint64_t d1, r, d2, v, d3, state, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+constexpr uint32_t kIdesc1 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdesc2 = idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdesc3 = idesc_bf16(128, 128, true, true);
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float *f) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+// Write 32 fp32 values as bf16 into row `row`, 16-byte chunks [chunk0,
+// chunk0+4) of a 128-byte-swizzled tile.
+__device__ __forceinline__ void store_row32(unsigned char *tile, uint32_t row, uint32_t chunk0,
+                                            const float *x, float scale) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        uint4 w;
+        w.x = pack_bf16x2(scale * x[8 * cc + 0], scale * x[8 * cc + 1]);
+        w.y = pack_bf16x2(scale * x[8 * cc + 2], scale * x[8 * cc + 3]);
+        w.z = pack_bf16x2(scale * x[8 * cc + 4], scale * x[8 * cc + 5]);
+        w.w = pack_bf16x2(scale * x[8 * cc + 6], scale * x[8 * cc + 7]);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, chunk0 + cc)) = w;
+    }
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_q,
+                      const __grid_constant__ CUtensorMap map_v) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
+    volatile int *abort = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slice = blockIdx.x % kSlices;
+    const int sh = blockIdx.x / kSlices;
+    const int s = sh / p.H, h = sh - s * p.H;
+    const int col0 = slice * kNS;
+    int start, len, slot0;
+    sequence_range(p, s, start, len, slot0);
+    const int nchunks = (len + kChunk - 1) / kChunk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bars->full[i], 1);
+            mbar_init(&bars->empty[i], 1 + 8);
+        }
+        mbar_init(&bars->d1, 1);
+        mbar_init(&bars->r, 4);
+        mbar_init(&bars->d2, 1);
+        mbar_init(&bars->v, 4);
+        mbar_init(&bars->d3, 1);
+        mbar_init(&bars->state, 8);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_k);
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int last_use[kStages] = {-1, -1};
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1, use = c >> 1;
+                if (!mbar_wait(&bars->empty[st], (use & 1) ^ 1, abort)) break;
+                unsigned char *stage = smem + st * kStageBytes;
+                const int t0 = start + c * kChunk;
+                const unsigned char *blk =
+                    p.prep + ((size_t)(slot0 + c) * p.H + h) * p.prep_stride;
+                mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+                tma_load_3d(stage + 0, &map_k, &bars->full[st], 0, h, t0);
+                tma_load_3d(stage + 8192, &map_q, &bars->full[st], 0, h, t0);
+                tma_load_3d(stage + 16384, &map_k, &bars->full[st], 64, h, t0);
+                tma_load_3d(stage + 24576, &map_q, &bars->full[st], 64, h, t0);
+                tma_load_3d(stage + kOffV, &map_v, &bars->full[st], col0, h, t0);
+                bulk_load(stage + kOffPrep, blk, kPrepBytes, &bars->full[st]);
+                last_use[st] = use;
+            }
+            // drain: every issued copy must land before the CTA may exit
+            for (int st = 0; st < kStages; ++st) {
+                if (last_use[st] < 0) continue;
+                int dummy = 0;
+                mbar_wait(&bars->full[st], last_use[st] & 1, &dummy);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t b1 = smem_u32(smem + kOffB1);
+            const uint32_t rr = smem_u32(smem + kOffR);
+            const uint32_t b3 = smem_u32(smem + kOffB3);
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1, use = c >> 1;
+                const uint32_t kq = smem_u32(smem + st * kStageBytes);
+                const uint32_t prep = kq + kOffPrep;
+                if (!mbar_wait(&bars->full[st], use & 1, abort)) break;
+                if (!mbar_wait(&bars->state, c & 1, abort)) break;
+                tc_fence_after();
+                // MMA1: D1 = [K; Q] [S | M]; K-steps of 16 over dk (two 64-wide halves)
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(b1 + (kb * 4 + kk) * 2048, 16384, 1024);
+                        mma_bf16(tmem + kColD1, a, b, kIdesc1, (kb | kk) != 0);
+                    }
+                mma_commit(&bars->d1);
+                if (!mbar_wait(&bars->r, c & 1, abort)) break;
+                tc_fence_after();
+                // MMA2: D2 = [T; A_O T] R; K-steps of 16 tokens
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = sdesc_sw128(prep + kk * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
+                    mma_bf16(tmem + kColD2, a, b, kIdesc2, kk != 0);
+                }
+                mma_commit(&bars->d2);
+                if (!mbar_wait(&bars->v, c & 1, abort)) break;
+                tc_fence_after();
+                // MMA3: D3 = K^T [gS Vres | gM Vres]; K-steps of 16 tokens
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = sdesc_sw128(kq + kk * 2048, 16384, 1024);
+                    const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
+                    mma_bf16(tmem + kColD3, a, b, kIdesc3, kk != 0);
+                }
+                mma_commit(&bars->d3);
+                mma_commit(&bars->empty[st]);
+            }
+            // drain: all issued MMAs complete before TMEM is freed
+            mma_commit(&bars->drain);
+            int dummy = 0;
+            mbar_wait(&bars->drain, 0, &dummy);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quadrant
+        const int hc = (warp - 4) >> 2;         // 32-column half of the slice
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        const int row = 32 * q + lane;          // TMEM lane = D row
+        const int d = row;                      // state row (dk index) for D3
+        const size_t st_off = (size_t)sh * kD * kD + (size_t)d * kD + col0 + hc * 32;
+        float S[32], M[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), mv = sv;
+            if (p.S0) sv = *reinterpret_cast<const float4 *>(p.S0 + st_off + j);
+            if (p.M0) mv = *reinterpret_cast<const float4 *>(p.M0 + st_off + j);
+            S[j] = sv.x; S[j + 1] = sv.y; S[j + 2] = sv.z; S[j + 3] = sv.w;
+            M[j] = mv.x; M[j + 1] = mv.y; M[j + 2] = mv.z; M[j + 3] = mv.w;
+        }
+        unsigned char *b1 = smem + kOffB1;
+        unsigned char *rt = smem + kOffR;
+        unsigned char *b3 = smem + kOffB3;
+        if (nchunks > 0) {
+            store_row32(b1, d, hc * 4, S, 1.f);
+            store_row32(b1 + 16384, d, hc * 4, M, 1.f);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->state);
+        }
+        const size_t rs = (size_t)p.H * kD;
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + hc * 32;
+        float oint[32];
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1, use = c >> 1;
+            unsigned char *stage = smem + st * kStageBytes;
+            const float *vec = reinterpret_cast<const float *>(stage + kOffPrep + PrepLayoutTC::kOffVec);
+            const int n = min(kChunk, len - c * kChunk);
+            const int t0 = start + c * kChunk;
+            if (!warp_wait(&bars->full[st], use & 1, abort)) break;
+
+            // ---- residual right-hand side R (token rows) / O_inter (query rows)
+            if (!warp_wait(&bars->d1, c & 1, abort)) break;
+            tc_fence_after();
+            {
+                float xs[32], xm[32];
+                tmem_ld32(lane_base + kColD1 + hc * 32, xs);
+                tmem_ld32(lane_base + kColD1 + 64 + hc * 32, xm);
+                tmem_ld_wait();
+                tc_fence_before();
+                if (q < 2) {
+                    const int i = row;                  // token row of K
+                    const float ab = vec[kVecAbar * kChunk + i];
+                    const float bma = vec[kVecBmA * kChunk + i];
+                    const unsigned char *vt = stage + kOffV;
+                    const float keep = (i < n) ? 1.f : 0.f;   // rows past the chunk end
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float vv[8], r[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(vt + sw128_offset(i, hc * 4 + cc)), vv);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * cc + e;
+                            r[e] = keep * (vv[e] - ab * xs[j] + bma * xm[j]);
+                        }
+                        uint4 w;
+                        w.x = pack_bf16x2(r[0], r[1]);
+                        w.y = pack_bf16x2(r[2], r[3]);
+                        w.z = pack_bf16x2(r[4], r[5]);
+                        w.w = pack_bf16x2(r[6], r[7]);
+                        *reinterpret_cast<uint4 *>(rt + sw128_offset(i, hc * 4 + cc)) = w;
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->r);
+                } else {
+                    const int i = row - 64;             // token row of Q
+                    const float ab = vec[kVecAbar * kChunk + i];
+                    const float bb = vec[kVecB * kChunk + i];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) oint[j] = ab * xs[j] - bb * xm[j];
+                }
+            }
+
+            // ---- residuals (token rows) / outputs (query rows)
+            if (!warp_wait(&bars->d2, c & 1, abort)) break;
+            tc_fence_after();
+            {
+                float x[32];
+                tmem_ld32(lane_base + kColD2 + hc * 32, x);
+                tmem_ld_wait();
+                tc_fence_before();
+                if (q < 2) {
+                    const int i = row;
+                    const float gs = vec[kVecGS * kChunk + i];
+                    const float gm = vec[kVecGM * kChunk + i];
+                    store_row32(b3, i, hc * 4, x, gs);
+                    store_row32(b3 + 8192, i, hc * 4, x, gm);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->v);
+                } else {
+                    const int i = row - 64;
+                    if (i < n) {
+                        __nv_bfloat16 *dst = og + (size_t)(t0 + i) * rs;
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            uint4 w;
+                            w.x = pack_bf16x2(oint[8 * cc + 0] + x[8 * cc + 0], oint[8 * cc + 1] + x[8 * cc + 1]);
+                            w.y = pack_bf16x2(oint[8 * cc + 2] + x[8 * cc + 2], oint[8 * cc + 3] + x[8 * cc + 3]);
+                            w.z = pack_bf16x2(oint[8 * cc + 4] + x[8 * cc + 4], oint[8 * cc + 5] + x[8 * cc + 5]);
+                            w.w = pack_bf16x2(oint[8 * cc + 6] + x[8 * cc + 6], oint[8 * cc + 7] + x[8 * cc + 7]);
+                            *reinterpret_cast<uint4 *>(dst + 8 * cc) = w;
+                        }
+                    }
+                }
+            }
+
+            // ---- carry of S and M (state rows)
+            if (!warp_wait(&bars->d3, c & 1, abort)) break;
+            tc_fence_after();
+            {
+                float xs[32], xm[32];
+                tmem_ld32(lane_base + kColD3 + hc * 32, xs);
+                tmem_ld32(lane_base + kColD3 + 64 + hc * 32, xm);
+                tmem_ld_wait();
+                tc_fence_before();
+                const float ab_n = vec[kVecScal * kChunk + 0];
+                const float b_n = vec[kVecScal * kChunk + 1];
+                const float mb_n = vec[kVecScal * kChunk + 2];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float s_old = S[j], m_old = M[j];
+                    S[j] = ab_n * s_old - b_n * m_old + xs[j];
+                    M[j] = mb_n * m_old - xm[j];
+                }
+                const bool more = c + 1 < nchunks;
+                if (more) {
+                    store_row32(b1, d, hc * 4, S, 1.f);
+                    store_row32(b1 + 16384, d, hc * 4, M, 1.f);
+                    fence_proxy_async();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (more) mbar_arrive(&bars->state);
+                    mbar_arrive(&bars->empty[st]);
+                }
+            }
+        }
+        if (!*abort) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                if (p.S_T)
+                    *reinterpret_cast<float4 *>(p.S_T + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                if (p.M_T)
+                    *reinterpret_cast<float4 *>(p.M_T + st_off + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (threadIdx.x == 0 && *abort && p.status) atomicExch(p.status, (int)MDN_ERR_DEVICE_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, h, t); box 64 x 1 x 64.
+bool make_map(CUtensorMap *map, const void *base, int T_total, int H, bool swizzle) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
+    if (p.D != kD || p.dtype != MDN_BF16) return cudaErrorInvalidValue;
+    if (p.prep_stride % 16 != 0) return cudaErrorInvalidValue;
+    CUtensorMap mk, mq, mv;
+    const int Tt = p.T_total > 0 ? p.T_total : 1;
+    if (!make_map(&mk, p.k, Tt, p.H, true) || !make_map(&mq, p.q, Tt, p.H, true) ||
+        !make_map(&mv, p.v, Tt, p.H, true))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(chunk_state_tc_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    const long blocks = (long)p.n_seq * p.H * kSlices;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    chunk_state_tc_kernel<<<(unsigned)blocks, kThreadsTC, kSmemBytes, st>>>(p, mk, mq, mv);
+    return cudaGetLastError();
+}
+
+}  // namespace mdn

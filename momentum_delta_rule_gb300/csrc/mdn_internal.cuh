@@ -36,6 +36,19 @@ struct PrepLayout {
     static constexpr size_t kBytes = 2 * kMatBytes + kVecBytes;
 };
 
+// Prepared block of the tensor-core path: T and A_O T in bf16, each 64 rows
+// of 128 bytes stored in the 128-byte-swizzled K-major operand layout of
+// tcgen05.mma (16-byte chunk c of row r at (r/8)*1024 + (r%8)*128 +
+// ((c ^ (r%8)) * 16)), followed by the fp32 vectors.  One bulk copy of the
+// whole block into 1024-byte-aligned shared memory yields the MMA operand
+// [T; A_O T] directly.
+struct PrepLayoutTC {
+    static constexpr size_t kOffT = 0;
+    static constexpr size_t kOffAOT = 8192;
+    static constexpr size_t kOffVec = 16384;
+    static constexpr size_t kBytes = 16384 + sizeof(float) * kChunk * kVecRows;
+};
+
 // Largest prepared block of any path (fp32 matrices).
 constexpr size_t kPrepBytesMax = PrepLayout<float>::kBytes;
 
@@ -68,7 +81,9 @@ struct DecodeProblem {
 
 // Launchers (return the first CUDA error, or cudaSuccess).
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
-cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
+cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st,
+                                   bool tc_layout);
+cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 

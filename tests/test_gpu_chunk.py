@@ -121,3 +121,17 @@ def test_varlen_packed_full_size_sampled():
     ch = chains(x)
     shortest = min(ch, key=lambda c: c[2].stop - c[2].start)
     compare(x, out, _sample(x, 4) + [shortest])
+
+
+def test_path_selection():
+    """bf16 inputs with head size 128 run on the tensor-core path; fp32 inputs
+    and head size 64 on the CUDA-core path."""
+    import momentum_delta_rule_gb300 as mdn
+    for dtype, D, want in (("bf16", 128, mdn.MDN_PATH_TENSOR_CORE),
+                           ("fp32", 128, mdn.MDN_PATH_CUDA_CORE),
+                           ("bf16", 64, mdn.MDN_PATH_CUDA_CORE)):
+        w = W.Workload("path", dtype=dtype, state="zero", seed=15)
+        x = W.make_prefill(w, B=1, T=70, H=1, D=D)
+        info = {}
+        gpu_chunk_fwd(x, info=info)
+        assert info["path"] == want, (dtype, D, info)
