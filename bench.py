@@ -172,8 +172,9 @@ def state_pass_bytes(x, prep_bytes_per_chunk_head):
     D = x["D"]
     chunks = sum((L + 63) // 64 for L in seq_lengths(x)) * x["H"]
     n_chain = x["n_seq"] * x["H"]
+    states = (2 if x["S0"] is not None else 0) + 2     # S0/M0 read, S_T/M_T written
     return (th * 4 * D * el + chunks * prep_bytes_per_chunk_head
-            + n_chain * 4 * D * D * 4)
+            + n_chain * states * D * D * 4)
 
 
 def seq_lengths(x):
@@ -458,7 +459,7 @@ def main():
                 "fp32 FFMA from unit counts: 152 SMs x 128 lanes x 2 x %.0f MHz"
                 % peaks.get("sm_max_mhz", 2070.0),
                 "hbm_bytes_per_launch_algorithmic": state_pass_bytes(
-                    x, 34816) if stage_name == "state" else None,
+                    x, 18432 if tensor else 34816) if stage_name == "state" else None,
                 "stage_ms": {"prep": r["stage_ms"][0], "state": r["stage_ms"][1]}}
 
     line = {"metric": "MDN chunkwise fwd tokens/s", "value": value,
