@@ -151,6 +151,42 @@ mdn_status mdn_chunk_fwd_profiled(
     void *stream, void *const *stage_events, int n_stage_events,
     int *path_out);
 
+/* Size of the library-owned scratch array of mdn_chunk_fwd_static_ws. */
+#define MDN_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * mdn_chunk_fwd_static_ws — mdn_chunk_fwd without a caller-provided
+ * workspace, for callers that cannot allocate device memory where they run
+ * the prefill (for example a server that reserves all device memory at start
+ * and forbids allocation afterwards, since cudaMalloc may synchronise the
+ * device and take unbounded time, or plugin code with no handle to its host's
+ * allocator).  The paper has no counterpart: this is a deployment interface.
+ *
+ * Arguments, layouts, results and errors are those of mdn_chunk_fwd (minus
+ * workspace and workspace_bytes).  The scratch is a file-scope device array of
+ * MDN_STATIC_WORKSPACE_BYTES (32 MiB) inside the library; a device holds it
+ * from the first use until the process exits.  The call allocates and frees
+ * nothing.
+ *  - Size limit: if mdn_chunk_fwd_workspace_size(n_seq, B*T, H, dk, dv, dtype)
+ *    exceeds MDN_STATIC_WORKSPACE_BYTES the call returns MDN_ERR_UNSUPPORTED
+ *    and enqueues nothing.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Sharing: every call on a device uses the same array.  Nothing in it must
+ *    start at zero (each call writes all it reads), but calls whose work
+ *    overlaps on the GPU (other streams, other host threads) race on it:
+ *    serialise them, e.g. on one stream.
+ */
+mdn_status mdn_chunk_fwd_static_ws(const void *q, const void *k, const void *v,
+                                   const float *alpha, const float *mu,
+                                   const float *eta, const float *beta,
+                                   const float *S0, const float *M0, void *o,
+                                   float *S_T, float *M_T,
+                                   const int32_t *cu_seqlens, int n_seq, int B,
+                                   int T, int H, int dk, int dv,
+                                   mdn_dtype dtype, int chunk, void *stream);
+
 /*
  * mdn_decode_step — one recurrent step for N sequences (one token each),
  * updating both states in place.

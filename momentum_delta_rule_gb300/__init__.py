@@ -37,8 +37,8 @@ CHUNK = 64
 
 EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_workspace_size", "mdn_chunk_fwd",
-                    "mdn_chunk_fwd_profiled", "mdn_decode_step",
-                    "mdn_get_device_status"]
+                    "mdn_chunk_fwd_profiled", "mdn_chunk_fwd_static_ws",
+                    "mdn_decode_step", "mdn_get_device_status"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
 
@@ -76,6 +76,9 @@ def lib():
     L.mdn_chunk_fwd_profiled.argtypes = (L.mdn_chunk_fwd.argtypes
                                          + [ctypes.POINTER(ctypes.c_void_p), c_int,
                                             ctypes.POINTER(ctypes.c_int)])
+    L.mdn_chunk_fwd_static_ws.restype = c_int
+    L.mdn_chunk_fwd_static_ws.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, ip]
+                                          + [c_int] * 8 + [vp])
     L.mdn_decode_step.restype = c_int
     L.mdn_decode_step.argtypes = [vp] * 3 + [fp] * 6 + [vp] + [c_int] * 5 + [vp]
     L.mdn_get_device_status.restype = c_int

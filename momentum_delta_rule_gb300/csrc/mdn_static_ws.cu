@@ -1,0 +1,65 @@
+// Allocation-free variant of mdn_chunk_fwd.
+//
+// mdn_chunk_fwd needs device scratch (the per-chunk prepared blocks and the
+// chunk offsets of packed sequences) that its caller allocates.  Some callers
+// cannot allocate device memory at the point where they run the prefill: an
+// inference server that reserves all device memory when it starts and forbids
+// allocation afterwards (cudaMalloc can synchronise the device and take an
+// unbounded time), or plugin code that has no handle to its host's allocator.
+// For them, mdn_chunk_fwd_static_ws runs the same kernels on a scratch array
+// that lives in this library's own device memory.
+//
+// The array below is a file-scope __device__ variable.  Its name in host code
+// is only a host-side stand-in, not a device address: the device address is
+// fetched with cudaGetSymbolAddress, once per device, with that device
+// current, on the first call made on that device.  Every call on a device
+// shares the array and it keeps the previous call's contents; nothing in it
+// needs to start at zero, because every byte a call reads was written earlier
+// in the same call.
+#include <stdint.h>
+
+#include "mdn_internal.cuh"
+
+static __device__ __align__(256) unsigned char g_mdn_static_ws[MDN_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+void *g_static_ws_addr[kMaxDevices];   // device address of g_mdn_static_ws, per device
+
+}  // namespace
+
+extern "C" mdn_status mdn_chunk_fwd_static_ws(
+    const void *q, const void *k, const void *v, const float *alpha, const float *mu,
+    const float *eta, const float *beta, const float *S0, const float *M0, void *o,
+    float *S_T, float *M_T, const int32_t *cu_seqlens, int n_seq, int B, int T, int H,
+    int dk, int dv, mdn_dtype dtype, int chunk, void *stream) {
+    const long T_total = (long)B * (long)T;
+    const bool sizes_ok = B >= 0 && T >= 0 && n_seq >= 0 && H > 0 && dk > 0 && dv > 0 &&
+                          T_total <= 0x3fffffffL;
+    if (!sizes_ok) {
+        // let the regular entry point report the invalid argument
+        return mdn_chunk_fwd(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, cu_seqlens,
+                             n_seq, B, T, H, dk, dv, dtype, chunk, nullptr, 0, stream);
+    }
+    const size_t need = mdn_chunk_fwd_workspace_size(n_seq, (int)T_total, H, dk, dv, dtype);
+    if (need > (size_t)MDN_STATIC_WORKSPACE_BYTES) return MDN_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return MDN_ERR_UNSUPPORTED;
+    if (g_static_ws_addr[dev] == nullptr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_mdn_static_ws) != cudaSuccess || addr == nullptr) {
+            cudaGetLastError();
+            return MDN_ERR_CUDA;
+        }
+        g_static_ws_addr[dev] = addr;
+    }
+    return mdn_chunk_fwd(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, cu_seqlens, n_seq,
+                         B, T, H, dk, dv, dtype, chunk, g_static_ws_addr[dev],
+                         (size_t)MDN_STATIC_WORKSPACE_BYTES, stream);
+}
