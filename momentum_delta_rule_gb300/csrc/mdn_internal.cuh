@@ -83,6 +83,7 @@ struct DecodeProblem {
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st,
                                    bool tc_layout);
+cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
