@@ -169,22 +169,33 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         vec[vU * kChunk + i] = U;
         vec[vZ * kChunk + i] = Z;
         asm volatile("bar.sync 1, 64;" ::: "memory");
-        // column j = i of Gamma
+        // column j = i of Gamma (only the lower triangle is ever read)
         {
             const int j = i;
             float g = be;
-            for (int r = 0; r < j; ++r) G[r * LM + j] = 0.f;
             G[j * LM + j] = g;
             for (int r = j + 1; r < kChunk; ++r) {
-                const float m = (vec[vZ * kChunk + r] == Z) ? expf(vec[vU * kChunk + r] - U) : 0.f;
+                const float m = (vec[vZ * kChunk + r] == Z) ? __expf(vec[vU * kChunk + r] - U) : 0.f;
                 g = vec[vAlpha * kChunk + r] * g + vec[vBeta * kChunk + r] * m;
                 G[r * LM + j] = g;
             }
         }
-        float bsum = 0.f;
-        for (int r = 0; r <= i; ++r)
-            if (vec[vZ * kChunk + r] == 0.f)
-                bsum += vec[vBeta * kChunk + r] * expf(A - vec[vA * kChunk + r] + vec[vU * kChunk + r]);
+        // b_i = alpha_i b_{i-1} + beta_i mubar_i as an affine prefix scan:
+        // each lane holds the map x -> ca x + cb of its token; maps compose.
+        float ca = a;
+        float cb = (Z == 0.f) ? be * __expf(U) : 0.f;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float pa = __shfl_up_sync(0xffffffffu, ca, d);
+            const float pb = __shfl_up_sync(0xffffffffu, cb, d);
+            if ((i & 31) >= d) {
+                cb = ca * pb + cb;
+                ca = ca * pa;
+            }
+        }
+        if (warp == 0 && lane == 31) vec[vScan * kChunk] = cb;
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        const float bsum = (warp == 1) ? ca * vec[vScan * kChunk] + cb : cb;
         vec[vB * kChunk + i] = bsum;
         asm volatile("bar.sync 1, 64;" ::: "memory");
         // carry vectors of the prepared block
@@ -266,25 +277,71 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     }
     __syncthreads();   // L ready; Gamma no longer needed
 
-    // ---- T = (I + L)^{-1}, one row at a time:  T[i][j] = -sum_{k=j}^{i-1} L[i][k] T[k][j]
+    // ---- T = (I + L)^{-1}, blocked:
+    //   diagonal 16x16 blocks by forward substitution in registers (one lane
+    //   per column), then [[A,0],[C,B]]^{-1} = [[A^-1,0],[-B^-1 C A^-1, B^-1]]
+    //   for the 16-blocks inside each 32-block and for the two 32-blocks.
     float *Tm = G;
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreadsP) {
-        const int r = idx >> 6, c = idx & 63;
-        Tm[r * LM + c] = (r == c) ? 1.f : 0.f;
-    }
-    __syncthreads();
-    {
-        const int j = tid >> 2, part = tid & 3;
-        for (int i = 1; i < n; ++i) {
-            float s = 0.f;
-            if (j < i)
-                for (int k = j + part; k < i; k += 4) s += L[i * LM + k] * Tm[k * LM + j];
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (j < i && part == 0) Tm[i * LM + j] = -s;
-            __syncthreads();
+    float *X = reinterpret_cast<float *>(smem + kOffB2);    // scratch until B2 is built
+    constexpr int LX = 33;
+    if (warp < 2) {
+        const int blk = warp * 2 + (lane >> 4);
+        const int c = lane & 15;
+        const int base = blk * 16;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < r; ++k) acc += L[(base + r) * LM + base + k] * t[k];
+            t[r] = (r < c) ? 0.f : ((r == c) ? 1.f : -acc);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tm[(base + r) * LM + base + c] = t[r];
+    } else {
+        // zero the blocks above the diagonal blocks
+        for (int idx = tid - 64; idx < kChunk * kChunk; idx += kThreadsP - 64) {
+            const int r = idx >> 6, cc = idx & 63;
+            if ((cc >> 4) > (r >> 4)) Tm[r * LM + cc] = 0.f;
         }
     }
+    __syncthreads();
+    // 16-blocks below the diagonal inside each 32-block (two of them)
+    for (int idx = tid; idx < 512; idx += kThreadsP) {
+        const int pb = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+        const int r0 = 32 * pb + 16, c0 = 32 * pb;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc += L[(r0 + i) * LM + c0 + k] * Tm[(c0 + k) * LM + c0 + j];
+        X[(pb * 16 + i) * LX + j] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 512; idx += kThreadsP) {
+        const int pb = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+        const int r0 = 32 * pb + 16, c0 = 32 * pb;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc += Tm[(r0 + i) * LM + r0 + k] * X[(pb * 16 + k) * LX + j];
+        Tm[(r0 + i) * LM + c0 + j] = -acc;
+    }
+    __syncthreads();
+    // the 32-block below the diagonal: -T_B (L_C T_A)
+    for (int idx = tid; idx < 1024; idx += kThreadsP) {
+        const int i = idx >> 5, j = idx & 31;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) acc += L[(32 + i) * LM + k] * Tm[k * LM + j];
+        X[i * LX + j] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 1024; idx += kThreadsP) {
+        const int i = idx >> 5, j = idx & 31;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) acc += Tm[(32 + i) * LM + 32 + k] * X[k * LX + j];
+        Tm[(32 + i) * LM + j] = -acc;
+    }
+    __syncthreads();
 
     // ---- bf16(T) as the MN-major B operand (rows k, columns j)
     for (int idx = tid; idx < kChunk * 8; idx += kThreadsP) {
