@@ -14,20 +14,22 @@
 //         O_inter = Diag(abar) Q S_0 - Diag(b) Q M_0
 //   MMA2  D2 = [T; A_O T] R                 (M=128, N=64, K=64 tokens)
 //         Vres = rows 0..63,  O = O_inter + rows 64..127
-//   MMA3  D3 = K^T [Diag(gS) Vres | Diag(gM) Vres]   (M=dk, N=2x64, K=64)
-//         S <- abar_n S - b_n M + D3[:, :64],  M <- mubar_n M - D3[:, 64:]
+//   MMA3  [S | M] += K^T [Diag(gS) Vres | -Diag(gM) Vres]  (M=dk, N=2x64, K=64)
 //
-// with gS_i = gamma_{n,i} eta_i and gM_i = prod_{u>i} mu_u eta_i, both carries
-// computed from the old S_0, M_0.  The fp32 state lives in the registers of
-// the epilogue warps (row d of S and M in the thread that owns TMEM lane d of
-// D3); only its bf16 copy goes to shared memory as MMA1's B operand.
+// with gS_i = gamma_{n,i} eta_i and gM_i = prod_{u>i} mu_u eta_i.  The fp32
+// state [S | M] of the slice lives in TMEM as MMA3's accumulator; before MMA3
+// the epilogue rescales it in place to [abar_n S - b_n M | mubar_n M] (both
+// carries use the old S_0, M_0), off the critical path while MMA2 runs.  Only
+// a bf16 copy of the state goes to shared memory, as MMA1's B operand.
 //
 // One CTA owns one (sequence, head, 64-column slice): columns of S and M
 // evolve independently (column j of Vres depends only on column j of S_0 and
 // M_0), so the two slices of a head never communicate.
 //
-// Warp roles (12 warps): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 4..11 epilogue (TMEM lane quadrant = warp % 4, column half = (warp-4)/4).
+// Warp roles (18 warps): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// 2..17 epilogue (TMEM lane quadrant = warp % 4, 16-column quarter of the
+// slice = (warp-2)/4), so every critical-path epilogue step is spread over
+// 512 threads.
 // Every wait is bounded (1 s); on expiry the CTA records
 // MDN_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -43,7 +45,9 @@ using namespace sm100;
 constexpr int kD = 128;                  // head size (dk = dv)
 constexpr int kNS = 64;                  // state columns per CTA
 constexpr int kSlices = kD / kNS;
-constexpr int kThreadsTC = 384;
+constexpr int kThreadsTC = 576;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiCols = 16;             // state columns per epilogue thread
 constexpr int kStages = 2;
 
 // shared memory (byte offsets from the 1024-aligned base)
@@ -66,12 +70,12 @@ constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD1 = 0;      // 128 columns
 constexpr uint32_t kColD2 = 128;    // 64 columns
-constexpr uint32_t kColD3 = 256;    // 128 columns
+constexpr uint32_t kColSt = 256;    // fp32 state [S | M] of the slice, 128 columns
 
 struct Bars {
     uint64_t full[kStages];    // TMA bytes of a stage landed
-    uint64_t empty[kStages];   // stage free again (MMA commit + 8 epilogue warps)
-    uint64_t d1, r, d2, v, d3, state, drain;
+    uint64_t empty[kStages];   // stage free again (MMA commit + 16 epilogue warps)
+    uint64_t d1, r, d2, v, d3, state, drain;   // d3: the state accumulation finished
     uint32_t tmem_base;
     int abort;
 };
@@ -96,12 +100,12 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float *f) {
     }
 }
 
-// Write 32 fp32 values as bf16 into row `row`, 16-byte chunks [chunk0,
-// chunk0+4) of a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_row32(unsigned char *tile, uint32_t row, uint32_t chunk0,
+// Write 16 fp32 values as bf16 into row `row`, 16-byte chunks [chunk0,
+// chunk0+2) of a 128-byte-swizzled tile.
+__device__ __forceinline__ void store_row16(unsigned char *tile, uint32_t row, uint32_t chunk0,
                                             const float *x, float scale) {
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
         uint4 w;
         w.x = pack_bf16x2(scale * x[8 * cc + 0], scale * x[8 * cc + 1]);
         w.y = pack_bf16x2(scale * x[8 * cc + 2], scale * x[8 * cc + 3]);
@@ -138,14 +142,14 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars->full[i], 1);
-            mbar_init(&bars->empty[i], 1 + 8);
+            mbar_init(&bars->empty[i], 1 + kEpiWarps);
         }
         mbar_init(&bars->d1, 1);
-        mbar_init(&bars->r, 4);
+        mbar_init(&bars->r, kEpiWarps / 2);
         mbar_init(&bars->d2, 1);
-        mbar_init(&bars->v, 4);
+        mbar_init(&bars->v, kEpiWarps);
         mbar_init(&bars->d3, 1);
-        mbar_init(&bars->state, 8);
+        mbar_init(&bars->state, kEpiWarps);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -226,12 +230,12 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 mma_commit(&bars->d2);
                 if (!mbar_wait(&bars->v, c & 1, abort)) break;
                 tc_fence_after();
-                // MMA3: D3 = K^T [gS Vres | gM Vres]; K-steps of 16 tokens
+                // MMA3: [S | M] += K^T [gS Vres | -gM Vres]; K-steps of 16 tokens
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t a = sdesc_sw128(kq + kk * 2048, 16384, 1024);
                     const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
-                    mma_bf16(tmem + kColD3, a, b, kIdesc3, kk != 0);
+                    mma_bf16(tmem + kColSt, a, b, kIdesc3, 1);
                 }
                 mma_commit(&bars->d3);
                 mma_commit(&bars->empty[st]);
@@ -241,36 +245,46 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             int dummy = 0;
             mbar_wait(&bars->drain, 0, &dummy);
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quadrant
-        const int hc = (warp - 4) >> 2;         // 32-column half of the slice
+        const int qc = (warp - 2) >> 2;         // 16-column quarter of the slice
+        const int c0 = qc * kEpiCols;           // first column (within the slice)
+        const uint32_t ch0 = qc * 2;            // first 16-byte chunk of those columns
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const int row = 32 * q + lane;          // TMEM lane = D row
-        const int d = row;                      // state row (dk index) for D3
-        const size_t st_off = (size_t)sh * kD * kD + (size_t)d * kD + col0 + hc * 32;
-        float S[32], M[32];
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), mv = sv;
-            if (p.S0) sv = *reinterpret_cast<const float4 *>(p.S0 + st_off + j);
-            if (p.M0) mv = *reinterpret_cast<const float4 *>(p.M0 + st_off + j);
-            S[j] = sv.x; S[j + 1] = sv.y; S[j + 2] = sv.z; S[j + 3] = sv.w;
-            M[j] = mv.x; M[j + 1] = mv.y; M[j + 2] = mv.z; M[j + 3] = mv.w;
-        }
+        const int d = row;                      // state row (dk index)
+        const uint32_t st_s = lane_base + kColSt + c0;          // S columns of this thread
+        const uint32_t st_m = lane_base + kColSt + 64 + c0;     // M columns
+        const size_t st_off = (size_t)sh * kD * kD + (size_t)d * kD + col0 + c0;
         unsigned char *b1 = smem + kOffB1;
         unsigned char *rt = smem + kOffR;
         unsigned char *b3 = smem + kOffB3;
-        if (nchunks > 0) {
-            store_row32(b1, d, hc * 4, S, 1.f);
-            store_row32(b1 + 16384, d, hc * 4, M, 1.f);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->state);
+        {
+            float S[kEpiCols], M[kEpiCols];
+#pragma unroll
+            for (int j = 0; j < kEpiCols; j += 4) {
+                float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), mv = sv;
+                if (p.S0) sv = *reinterpret_cast<const float4 *>(p.S0 + st_off + j);
+                if (p.M0) mv = *reinterpret_cast<const float4 *>(p.M0 + st_off + j);
+                S[j] = sv.x; S[j + 1] = sv.y; S[j + 2] = sv.z; S[j + 3] = sv.w;
+                M[j] = mv.x; M[j + 1] = mv.y; M[j + 2] = mv.z; M[j + 3] = mv.w;
+            }
+            tmem_st16(st_s, S);
+            tmem_st16(st_m, M);
+            tmem_st_wait();
+            if (nchunks > 0) {
+                store_row16(b1, d, ch0, S, 1.f);
+                store_row16(b1 + 16384, d, ch0, M, 1.f);
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->state);
+            }
         }
         const size_t rs = (size_t)p.H * kD;
-        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + hc * 32;
-        float oint[32];
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + c0;
+        float oint[kEpiCols];
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1, use = c >> 1;
             unsigned char *stage = smem + st * kStageBytes;
@@ -278,47 +292,82 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             const int n = min(kChunk, len - c * kChunk);
             const int t0 = start + c * kChunk;
             if (!warp_wait(&bars->full[st], use & 1, abort)) break;
+            // Everything that depends only on the staged inputs is read before
+            // waiting on the MMAs, so the critical path sees no shared loads.
+            const int i = (q < 2) ? row : row - 64;     // token row (K rows / Q rows)
+            const float ab = vec[kVecAbar * kChunk + i];
+            const float cb = vec[(q < 2 ? kVecBmA : kVecB) * kChunk + i];
+            const float gs = vec[kVecGS * kChunk + i];
+            const float gm = vec[kVecGM * kChunk + i];
+            const bool in_chunk = i < n;
+            uint4 vraw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            if (q < 2) {
+                const unsigned char *vt = stage + kOffV;
+                vraw[0] = *reinterpret_cast<const uint4 *>(vt + sw128_offset(i, ch0));
+                vraw[1] = *reinterpret_cast<const uint4 *>(vt + sw128_offset(i, ch0 + 1));
+            }
 
             // ---- residual right-hand side R (token rows) / O_inter (query rows)
             if (!warp_wait(&bars->d1, c & 1, abort)) break;
             tc_fence_after();
             {
-                float xs[32], xm[32];
-                tmem_ld32(lane_base + kColD1 + hc * 32, xs);
-                tmem_ld32(lane_base + kColD1 + 64 + hc * 32, xm);
+                float xs[kEpiCols], xm[kEpiCols];
+                tmem_ld16(lane_base + kColD1 + c0, xs);
+                tmem_ld16(lane_base + kColD1 + 64 + c0, xm);
                 tmem_ld_wait();
-                tc_fence_before();
                 if (q < 2) {
-                    const int i = row;                  // token row of K
-                    const float ab = vec[kVecAbar * kChunk + i];
-                    const float bma = vec[kVecBmA * kChunk + i];
-                    const unsigned char *vt = stage + kOffV;
-                    const float keep = (i < n) ? 1.f : 0.f;   // rows past the chunk end
+                    // R = V - abar K S_0 + b_{i-1} alpha_i K M_0; zero past the chunk end
+                    const float keep = in_chunk ? 1.f : 0.f;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
+                    for (int cc = 0; cc < 2; ++cc) {
                         float vv[8], r[8];
-                        unpack_bf16x8(*reinterpret_cast<const uint4 *>(vt + sw128_offset(i, hc * 4 + cc)), vv);
+                        unpack_bf16x8(vraw[cc], vv);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int j = 8 * cc + e;
-                            r[e] = keep * (vv[e] - ab * xs[j] + bma * xm[j]);
+                            r[e] = keep * (vv[e] - ab * xs[j] + cb * xm[j]);
                         }
                         uint4 w;
                         w.x = pack_bf16x2(r[0], r[1]);
                         w.y = pack_bf16x2(r[2], r[3]);
                         w.z = pack_bf16x2(r[4], r[5]);
                         w.w = pack_bf16x2(r[6], r[7]);
-                        *reinterpret_cast<uint4 *>(rt + sw128_offset(i, hc * 4 + cc)) = w;
+                        *reinterpret_cast<uint4 *>(rt + sw128_offset(i, ch0 + cc)) = w;
                     }
                     fence_proxy_async();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->r);
                 } else {
-                    const int i = row - 64;             // token row of Q
-                    const float ab = vec[kVecAbar * kChunk + i];
-                    const float bb = vec[kVecB * kChunk + i];
+                    // O_inter = abar Q S_0 - b Q M_0
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) oint[j] = ab * xs[j] - bb * xm[j];
+                    for (int j = 0; j < kEpiCols; ++j) oint[j] = ab * xs[j] - cb * xm[j];
+                }
+            }
+
+            // ---- rescale the TMEM state for this chunk's carry (not on the
+            //      critical path: runs while MMA2 computes)
+            {
+                const float ab_n = vec[kVecScal * kChunk + 0];
+                const float b_n = vec[kVecScal * kChunk + 1];
+                const float mb_n = vec[kVecScal * kChunk + 2];
+                float S[kEpiCols], M[kEpiCols];
+                tmem_ld16(st_s, S);
+                tmem_ld16(st_m, M);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < kEpiCols; ++j) {
+                    const float s_old = S[j];
+                    S[j] = ab_n * s_old - b_n * M[j];
+                    M[j] = mb_n * M[j];
+                }
+                tmem_st16(st_s, S);
+                tmem_st16(st_m, M);
+                tmem_st_wait();
+                if (q >= 2) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->v);
                 }
             }
 
@@ -326,60 +375,45 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             if (!warp_wait(&bars->d2, c & 1, abort)) break;
             tc_fence_after();
             {
-                float x[32];
-                tmem_ld32(lane_base + kColD2 + hc * 32, x);
+                float x[kEpiCols];
+                tmem_ld16(lane_base + kColD2 + c0, x);
                 tmem_ld_wait();
-                tc_fence_before();
                 if (q < 2) {
-                    const int i = row;
-                    const float gs = vec[kVecGS * kChunk + i];
-                    const float gm = vec[kVecGM * kChunk + i];
-                    store_row32(b3, i, hc * 4, x, gs);
-                    store_row32(b3 + 8192, i, hc * 4, x, gm);
+                    store_row16(b3, i, ch0, x, gs);
+                    store_row16(b3 + 8192, i, ch0, x, -gm);
                     fence_proxy_async();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->v);
-                } else {
-                    const int i = row - 64;
-                    if (i < n) {
-                        __nv_bfloat16 *dst = og + (size_t)(t0 + i) * rs;
+                } else if (in_chunk) {
+                    __nv_bfloat16 *dst = og + (size_t)(t0 + i) * rs;
 #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            uint4 w;
-                            w.x = pack_bf16x2(oint[8 * cc + 0] + x[8 * cc + 0], oint[8 * cc + 1] + x[8 * cc + 1]);
-                            w.y = pack_bf16x2(oint[8 * cc + 2] + x[8 * cc + 2], oint[8 * cc + 3] + x[8 * cc + 3]);
-                            w.z = pack_bf16x2(oint[8 * cc + 4] + x[8 * cc + 4], oint[8 * cc + 5] + x[8 * cc + 5]);
-                            w.w = pack_bf16x2(oint[8 * cc + 6] + x[8 * cc + 6], oint[8 * cc + 7] + x[8 * cc + 7]);
-                            *reinterpret_cast<uint4 *>(dst + 8 * cc) = w;
-                        }
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint4 w;
+                        w.x = pack_bf16x2(oint[8 * cc + 0] + x[8 * cc + 0], oint[8 * cc + 1] + x[8 * cc + 1]);
+                        w.y = pack_bf16x2(oint[8 * cc + 2] + x[8 * cc + 2], oint[8 * cc + 3] + x[8 * cc + 3]);
+                        w.z = pack_bf16x2(oint[8 * cc + 4] + x[8 * cc + 4], oint[8 * cc + 5] + x[8 * cc + 5]);
+                        w.w = pack_bf16x2(oint[8 * cc + 6] + x[8 * cc + 6], oint[8 * cc + 7] + x[8 * cc + 7]);
+                        *reinterpret_cast<uint4 *>(dst + 8 * cc) = w;
                     }
                 }
             }
 
-            // ---- carry of S and M (state rows)
+            // ---- new state: bf16 copy for the next chunk's MMA1
             if (!warp_wait(&bars->d3, c & 1, abort)) break;
             tc_fence_after();
             {
-                float xs[32], xm[32];
-                tmem_ld32(lane_base + kColD3 + hc * 32, xs);
-                tmem_ld32(lane_base + kColD3 + 64 + hc * 32, xm);
-                tmem_ld_wait();
-                tc_fence_before();
-                const float ab_n = vec[kVecScal * kChunk + 0];
-                const float b_n = vec[kVecScal * kChunk + 1];
-                const float mb_n = vec[kVecScal * kChunk + 2];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float s_old = S[j], m_old = M[j];
-                    S[j] = ab_n * s_old - b_n * m_old + xs[j];
-                    M[j] = mb_n * m_old - xm[j];
-                }
                 const bool more = c + 1 < nchunks;
                 if (more) {
-                    store_row32(b1, d, hc * 4, S, 1.f);
-                    store_row32(b1 + 16384, d, hc * 4, M, 1.f);
+                    float S[kEpiCols], M[kEpiCols];
+                    tmem_ld16(st_s, S);
+                    tmem_ld16(st_m, M);
+                    tmem_ld_wait();
+                    store_row16(b1, d, ch0, S, 1.f);
+                    store_row16(b1 + 16384, d, ch0, M, 1.f);
                     fence_proxy_async();
                 }
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     if (more) mbar_arrive(&bars->state);
@@ -388,8 +422,12 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             }
         }
         if (!*abort) {
+            float S[kEpiCols], M[kEpiCols];
+            tmem_ld16(st_s, S);
+            tmem_ld16(st_m, M);
+            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
+            for (int j = 0; j < kEpiCols; j += 4) {
                 if (p.S_T)
                     *reinterpret_cast<float4 *>(p.S_T + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                 if (p.M_T)
@@ -449,6 +487,10 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
     if (err != cudaSuccess) return err;
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, chunk_state_tc_kernel);
+    if (err != cudaSuccess) return err;
+    if (fa.maxThreadsPerBlock < kThreadsTC) return cudaErrorLaunchOutOfResources;
     const long blocks = (long)p.n_seq * p.H * kSlices;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
