@@ -115,6 +115,27 @@ __device__ __forceinline__ void store_row16(unsigned char *tile, uint32_t row, u
     }
 }
 
+// In-place rescale of this thread's 16 columns of the TMEM state for the
+// carry of the current chunk: S <- abar_n S - b_n M, M <- mubar_n M.
+__device__ __forceinline__ void rescale_state(uint32_t st_s, uint32_t st_m, const float *vec) {
+    const float ab_n = vec[kVecScal * kChunk + 0];
+    const float b_n = vec[kVecScal * kChunk + 1];
+    const float mb_n = vec[kVecScal * kChunk + 2];
+    float S[kEpiCols], M[kEpiCols];
+    tmem_ld16(st_s, S);
+    tmem_ld16(st_m, M);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < kEpiCols; ++j) {
+        const float s_old = S[j];
+        S[j] = ab_n * s_old - b_n * M[j];
+        M[j] = mb_n * M[j];
+    }
+    tmem_st16(st_s, S);
+    tmem_st16(st_m, M);
+    tmem_st_wait();
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
@@ -307,16 +328,16 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 vraw[1] = *reinterpret_cast<const uint4 *>(vt + sw128_offset(i, ch0 + 1));
             }
 
-            // ---- residual right-hand side R (token rows) / O_inter (query rows)
-            if (!warp_wait(&bars->d1, c & 1, abort)) break;
-            tc_fence_after();
-            {
-                float xs[kEpiCols], xm[kEpiCols];
-                tmem_ld16(lane_base + kColD1 + c0, xs);
-                tmem_ld16(lane_base + kColD1 + 64 + c0, xm);
-                tmem_ld_wait();
-                if (q < 2) {
-                    // R = V - abar K S_0 + b_{i-1} alpha_i K M_0; zero past the chunk end
+            if (q < 2) {
+                // ======== token-row warps: the critical path of the chunk
+                // R = V - abar K S_0 + b_{i-1} alpha_i K M_0 (zero past the chunk end)
+                if (!warp_wait(&bars->d1, c & 1, abort)) break;
+                tc_fence_after();
+                {
+                    float xs[kEpiCols], xm[kEpiCols];
+                    tmem_ld16(lane_base + kColD1 + c0, xs);
+                    tmem_ld16(lane_base + kColD1 + 64 + c0, xm);
+                    tmem_ld_wait();
                     const float keep = in_chunk ? 1.f : 0.f;
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
@@ -338,68 +359,51 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->r);
-                } else {
-                    // O_inter = abar Q S_0 - b Q M_0
-#pragma unroll
-                    for (int j = 0; j < kEpiCols; ++j) oint[j] = ab * xs[j] - cb * xm[j];
                 }
-            }
-
-            // ---- rescale the TMEM state for this chunk's carry (not on the
-            //      critical path: runs while MMA2 computes)
-            {
-                const float ab_n = vec[kVecScal * kChunk + 0];
-                const float b_n = vec[kVecScal * kChunk + 1];
-                const float mb_n = vec[kVecScal * kChunk + 2];
-                float S[kEpiCols], M[kEpiCols];
-                tmem_ld16(st_s, S);
-                tmem_ld16(st_m, M);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < kEpiCols; ++j) {
-                    const float s_old = S[j];
-                    S[j] = ab_n * s_old - b_n * M[j];
-                    M[j] = mb_n * M[j];
-                }
-                tmem_st16(st_s, S);
-                tmem_st16(st_m, M);
-                tmem_st_wait();
-                if (q >= 2) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->v);
-                }
-            }
-
-            // ---- residuals (token rows) / outputs (query rows)
-            if (!warp_wait(&bars->d2, c & 1, abort)) break;
-            tc_fence_after();
-            {
-                float x[kEpiCols];
-                tmem_ld16(lane_base + kColD2 + c0, x);
-                tmem_ld_wait();
-                if (q < 2) {
+                rescale_state(st_s, st_m, vec);                 // overlaps MMA2
+                // Vres rows scaled by gS and -gM: MMA3's B operand
+                if (!warp_wait(&bars->d2, c & 1, abort)) break;
+                tc_fence_after();
+                {
+                    float x[kEpiCols];
+                    tmem_ld16(lane_base + kColD2 + c0, x);
+                    tmem_ld_wait();
                     store_row16(b3, i, ch0, x, gs);
                     store_row16(b3 + 8192, i, ch0, x, -gm);
                     fence_proxy_async();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->v);
-                } else if (in_chunk) {
-                    __nv_bfloat16 *dst = og + (size_t)(t0 + i) * rs;
+                }
+            } else {
+                // ======== query-row warps: their own work waits until the
+                // token-row warps are past the critical step, then overlaps MMAs
+                if (!warp_wait(&bars->r, c & 1, abort)) break;
+                tc_fence_after();
+                {
+                    float xs[kEpiCols], xm[kEpiCols];
+                    tmem_ld16(lane_base + kColD1 + c0, xs);
+                    tmem_ld16(lane_base + kColD1 + 64 + c0, xm);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint4 w;
-                        w.x = pack_bf16x2(oint[8 * cc + 0] + x[8 * cc + 0], oint[8 * cc + 1] + x[8 * cc + 1]);
-                        w.y = pack_bf16x2(oint[8 * cc + 2] + x[8 * cc + 2], oint[8 * cc + 3] + x[8 * cc + 3]);
-                        w.z = pack_bf16x2(oint[8 * cc + 4] + x[8 * cc + 4], oint[8 * cc + 5] + x[8 * cc + 5]);
-                        w.w = pack_bf16x2(oint[8 * cc + 6] + x[8 * cc + 6], oint[8 * cc + 7] + x[8 * cc + 7]);
-                        *reinterpret_cast<uint4 *>(dst + 8 * cc) = w;
-                    }
+                    for (int j = 0; j < kEpiCols; ++j) oint[j] = ab * xs[j] - cb * xm[j];
+                }
+                rescale_state(st_s, st_m, vec);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->v);
+                if (!warp_wait(&bars->d2, c & 1, abort)) break;
+                tc_fence_after();
+                {
+                    float x[kEpiCols];
+                    tmem_ld16(lane_base + kColD2 + c0, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < kEpiCols; ++j) oint[j] += x[j];   // O = O_inter + O_intra
                 }
             }
 
-            // ---- new state: bf16 copy for the next chunk's MMA1
+            // ---- new state: bf16 copy for the next chunk's MMA1 (all warps)
             if (!warp_wait(&bars->d3, c & 1, abort)) break;
             tc_fence_after();
             {
@@ -418,6 +422,19 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 if (lane == 0) {
                     if (more) mbar_arrive(&bars->state);
                     mbar_arrive(&bars->empty[st]);
+                }
+            }
+            // ---- outputs of this chunk (off the critical path)
+            if (q >= 2 && in_chunk) {
+                __nv_bfloat16 *dst = og + (size_t)(t0 + i) * rs;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint4 w;
+                    w.x = pack_bf16x2(oint[8 * cc + 0], oint[8 * cc + 1]);
+                    w.y = pack_bf16x2(oint[8 * cc + 2], oint[8 * cc + 3]);
+                    w.z = pack_bf16x2(oint[8 * cc + 4], oint[8 * cc + 5]);
+                    w.w = pack_bf16x2(oint[8 * cc + 6], oint[8 * cc + 7]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * cc) = w;
                 }
             }
         }

@@ -122,29 +122,13 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 2) {
-        // ---- K and Q tiles in, Gram MMA out
+        // ---- K and Q tiles in (the Gram MMA is issued once Gamma is done)
         if (lane == 0) {
-            const uint32_t kq = smem_u32(smem + kOffKQ);
             mbar_arrive_expect_tx(&bars->tma, 32768);
             tma_load_3d(smem + kOffKQ + 0, &map_k, &bars->tma, 0, h, loc.t0);
             tma_load_3d(smem + kOffKQ + 8192, &map_q, &bars->tma, 0, h, loc.t0);
             tma_load_3d(smem + kOffKQ + 16384, &map_k, &bars->tma, 64, h, loc.t0);
             tma_load_3d(smem + kOffKQ + 24576, &map_q, &bars->tma, 64, h, loc.t0);
-            if (mbar_wait(&bars->tma, 0, abort)) {
-                tc_fence_after();
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
-                        mma_bf16(tmem + kColG, a, b, kIdescGram, (kb | kk) != 0);
-                    }
-                mma_commit(&bars->gram);
-            } else {
-                int dummy = 0;           // the copy must land before the CTA exits
-                mbar_wait(&bars->tma, 0, &dummy);
-            }
         }
     } else if (warp < 2) {
         // ---- gates, log-space prefix scans, Gamma, b, carry vectors
@@ -169,17 +153,76 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         vec[vU * kChunk + i] = U;
         vec[vZ * kChunk + i] = Z;
         asm volatile("bar.sync 1, 64;" ::: "memory");
-        // column j = i of Gamma (only the lower triangle is ever read)
-        {
-            const int j = i;
-            float g = be;
-            G[j * LM + j] = g;
-            for (int r = j + 1; r < kChunk; ++r) {
-                const float m = (vec[vZ * kChunk + r] == Z) ? __expf(vec[vU * kChunk + r] - U) : 0.f;
-                g = vec[vAlpha * kChunk + r] * g + vec[vBeta * kChunk + r] * m;
+    } else {
+        // ---- identity rows of [I; A_O] while the others work (warps 3..7)
+        for (int idx = tid - 96; idx < 64 * 8; idx += kThreadsP - 96) {
+            const int r = idx >> 3, c = idx & 7;
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if ((r >> 3) == c) {
+                const int e = r & 7;                       // 1.0 at column r
+                const uint32_t one = 0x3F80u;              // bf16 1.0
+                uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
+                wp[e >> 1] = (e & 1) ? (one << 16) : one;
+            }
+            *reinterpret_cast<uint4 *>(A2 + sw128_offset(r, c)) = w;
+        }
+    }
+    __syncthreads();   // gates and prefix scans are in shared memory
+
+    // ---- Gamma, one column per lane of warps 0-1:
+    //      gamma_{j,j} = beta_j, gamma_{r,j} = alpha_r gamma_{r-1,j} + beta_r m_{r,j},
+    //      m_{r,j} = [Z_r = Z_j] exp(U_r - U_j).  The gates of all 64 tokens
+    //      sit in registers (token l and 32 + l in lane l) and step r
+    //      broadcasts token r by shuffles: the dependent chain touches no
+    //      memory.  Only the lower triangle is ever read.
+    if (warp < 2) {
+        const int j = tid;
+        const float a_lo = vec[vAlpha * kChunk + lane], a_hi = vec[vAlpha * kChunk + 32 + lane];
+        const float b_lo = vec[vBeta * kChunk + lane], b_hi = vec[vBeta * kChunk + 32 + lane];
+        const float u_lo = vec[vU * kChunk + lane], u_hi = vec[vU * kChunk + 32 + lane];
+        const float z_lo = vec[vZ * kChunk + lane], z_hi = vec[vZ * kChunk + 32 + lane];
+        const float Uj = vec[vU * kChunk + j], Zj = vec[vZ * kChunk + j];
+        float g = vec[vBeta * kChunk + j];
+        G[j * LM + j] = g;
+#pragma unroll
+        for (int r = 1; r < kChunk; ++r) {
+            const float ar = __shfl_sync(0xffffffffu, r < 32 ? a_lo : a_hi, r & 31);
+            const float br = __shfl_sync(0xffffffffu, r < 32 ? b_lo : b_hi, r & 31);
+            const float ur = __shfl_sync(0xffffffffu, r < 32 ? u_lo : u_hi, r & 31);
+            const float zr = __shfl_sync(0xffffffffu, r < 32 ? z_lo : z_hi, r & 31);
+            const float m = (zr == Zj) ? __expf(ur - Uj) : 0.f;
+            const float gn = ar * g + br * m;
+            if (r > j) {
+                g = gn;
                 G[r * LM + j] = g;
             }
         }
+    }
+    __syncthreads();   // Gamma complete
+    if (warp == 2 && lane == 0) {
+        // Gram MMA: G = [K; Q] K^T (the copy landed long ago)
+        const uint32_t kq = smem_u32(smem + kOffKQ);
+        if (mbar_wait(&bars->tma, 0, abort)) {
+            tc_fence_after();
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
+                    mma_bf16(tmem + kColG, a, b, kIdescGram, (kb | kk) != 0);
+                }
+            mma_commit(&bars->gram);
+        } else {
+            int dummy = 0;           // the copy must land before the CTA exits
+            mbar_wait(&bars->tma, 0, &dummy);
+        }
+    }
+    if (warp < 2) {
+        const int i = tid;
+        const float a = vec[vAlpha * kChunk + i], be = vec[vBeta * kChunk + i];
+        const float et = vec[vEta * kChunk + i];
+        const float A = vec[vA * kChunk + i], U = vec[vU * kChunk + i], Z = vec[vZ * kChunk + i];
         // b_i = alpha_i b_{i-1} + beta_i mubar_i as an affine prefix scan:
         // each lane holds the map x -> ca x + cb of its token; maps compose.
         float ca = a;
@@ -216,21 +259,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         if (i == 2) sc = (vec[vZ * kChunk + last] == 0.f) ? expf(vec[vU * kChunk + last]) : 0.f;
         if (i == 3) sc = (float)n;
         gv[kVecScal * kChunk + i] = sc;
-    } else {
-        // ---- identity rows of [I; A_O] while the others work (warps 3..7)
-        for (int idx = tid - 96; idx < 64 * 8; idx += kThreadsP - 96) {
-            const int r = idx >> 3, c = idx & 7;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if ((r >> 3) == c) {
-                const int e = r & 7;                       // 1.0 at column r
-                const uint32_t one = 0x3F80u;              // bf16 1.0
-                uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
-                wp[e >> 1] = (e & 1) ? (one << 16) : one;
-            }
-            *reinterpret_cast<uint4 *>(A2 + sw128_offset(r, c)) = w;
-        }
     }
-    __syncthreads();   // Gamma and the vectors are ready
+    __syncthreads();   // vectors ready
 
     // ---- Gram results -> L (fp32) and A_O (bf16 rows 64..127 of A2)
     {
@@ -306,40 +336,65 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         }
     }
     __syncthreads();
-    // 16-blocks below the diagonal inside each 32-block (two of them)
-    for (int idx = tid; idx < 512; idx += kThreadsP) {
-        const int pb = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+    // 16-blocks below the diagonal inside each 32-block (two of them); each
+    // thread computes two adjacent outputs of one row
+    {
+        const int pb = tid >> 7, i = (tid >> 3) & 15, j = (tid & 7) * 2;
         const int r0 = 32 * pb + 16, c0 = 32 * pb;
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc += L[(r0 + i) * LM + c0 + k] * Tm[(c0 + k) * LM + c0 + j];
-        X[(pb * 16 + i) * LX + j] = acc;
+        for (int k = 0; k < 16; ++k) {
+            const float l = L[(r0 + i) * LM + c0 + k];
+            const float *t = Tm + (c0 + k) * LM + c0 + j;
+            a0 += l * t[0];
+            a1 += l * t[1];
+        }
+        X[(pb * 16 + i) * LX + j] = a0;
+        X[(pb * 16 + i) * LX + j + 1] = a1;
     }
     __syncthreads();
-    for (int idx = tid; idx < 512; idx += kThreadsP) {
-        const int pb = idx >> 8, i = (idx >> 4) & 15, j = idx & 15;
+    {
+        const int pb = tid >> 7, i = (tid >> 3) & 15, j = (tid & 7) * 2;
         const int r0 = 32 * pb + 16, c0 = 32 * pb;
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc += Tm[(r0 + i) * LM + r0 + k] * X[(pb * 16 + k) * LX + j];
-        Tm[(r0 + i) * LM + c0 + j] = -acc;
+        for (int k = 0; k < 16; ++k) {
+            const float t = Tm[(r0 + i) * LM + r0 + k];
+            a0 += t * X[(pb * 16 + k) * LX + j];
+            a1 += t * X[(pb * 16 + k) * LX + j + 1];
+        }
+        Tm[(r0 + i) * LM + c0 + j] = -a0;
+        Tm[(r0 + i) * LM + c0 + j + 1] = -a1;
     }
     __syncthreads();
-    // the 32-block below the diagonal: -T_B (L_C T_A)
-    for (int idx = tid; idx < 1024; idx += kThreadsP) {
-        const int i = idx >> 5, j = idx & 31;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) acc += L[(32 + i) * LM + k] * Tm[k * LM + j];
-        X[i * LX + j] = acc;
+    // the 32-block below the diagonal: -T_B (L_C T_A).  X = L_C T_A: warp w
+    // owns columns [4w, 4w+4) of all 32 rows, so k runs over T_A's nonzero
+    // rows k >= 4w only (warp-uniform trip count).
+    {
+        const int i = lane, j0 = warp * 4;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = j0; k < 32; ++k) {
+            const float l = L[(32 + i) * LM + k];
+            const float *t = Tm + k * LM + j0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] += l * t[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) X[i * LX + j0 + e] = a[e];
     }
     __syncthreads();
-    for (int idx = tid; idx < 1024; idx += kThreadsP) {
-        const int i = idx >> 5, j = idx & 31;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) acc += Tm[(32 + i) * LM + 32 + k] * X[k * LX + j];
-        Tm[(32 + i) * LM + j] = -acc;
+    // T_C = -T_B X: warp w owns rows [4w, 4w+4), lane = column; k runs over
+    // T_B's nonzero columns k <= 4w+3 only.
+    {
+        const int i0 = warp * 4, j = lane;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < i0 + 4; ++k) {
+            const float x = X[k * LX + j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] += Tm[(32 + i0 + e) * LM + 32 + k] * x;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Tm[(32 + i0 + e) * LM + j] = -a[e];
     }
     __syncthreads();
 
