@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-other-workloads", action="store_true",
+                   help="skip timing the other prefill workloads")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="minimum CPU time of the oracle baseline sample")
     return p.parse_args()
@@ -164,17 +166,55 @@ def flops_per_token_head(d, C=64):
     return {"prep": prep, "state": state}
 
 
-def state_pass_bytes(x, prep_bytes_per_chunk_head):
-    """Algorithmic HBM bytes of the state pass: q, k, v read, o written,
-    prepared blocks read, states read and written once per chain."""
+PREP_BLOCK_BYTES = {True: 18432, False: 34816}   # tensor-core / CUDA-core layout
+
+
+def stage_bytes(x, tensor):
+    """Algorithmic HBM bytes of each stage.
+
+    prep : q and k read, the alpha/mu/eta (and beta) gates read, one prepared
+           block per (chunk, head) written.
+    state: q, k, v read and o written, the prepared blocks read, the initial
+           states read (when given) and the final states written.
+    """
     el = 2 if x["dtype"] == "bf16" else 4
     th = x["B"] * x["T"] * x["H"]
     D = x["D"]
     chunks = sum((L + 63) // 64 for L in seq_lengths(x)) * x["H"]
+    blk = PREP_BLOCK_BYTES[bool(tensor)] * chunks
+    n_gates = 3 + (1 if x["beta"] is not None else 0)
     n_chain = x["n_seq"] * x["H"]
-    states = (2 if x["S0"] is not None else 0) + 2     # S0/M0 read, S_T/M_T written
-    return (th * 4 * D * el + chunks * prep_bytes_per_chunk_head
-            + n_chain * states * D * D * 4)
+    states = (2 if x["S0"] is not None else 0) + 2
+    return {"prep": th * 2 * D * el + th * n_gates * 4 + blk,
+            "state": th * 4 * D * el + blk + n_chain * states * D * D * 4}
+
+
+def stage_roofline(name, x, tensor, ms, peaks, peak_src):
+    """Binding roofline of one stage: whichever of HBM bytes or FLOPs needs
+    more time at the measured peak."""
+    fl = flops_per_token_head(x["D"])[name] * sum(seq_lengths(x)) * x["H"]
+    by = stage_bytes(x, tensor)[name]
+    s = ms / 1e3
+    if tensor:
+        tflops_peak = peaks["bf16_tflops"]
+        fl_src = "%s bf16 burst" % peak_src
+    else:
+        tflops_peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        fl_src = "fp32 FFMA from unit counts (152 SMs x 128 lanes x 2 x max clock)"
+    t_fl = fl / (tflops_peak * 1e12)
+    t_by = by / (peaks["hbm_gbs"] * 1e9)
+    if t_by >= t_fl:
+        ach = by / s / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": by,
+                "algorithmic_flops": fl, "kernel_ms": ms,
+                "peak_source": "%s HBM copy" % peak_src,
+                "other_roof_frac": (fl / s / 1e12) / tflops_peak}
+    ach = fl / s / 1e12
+    return {"bound": "tensor" if tensor else "alu", "achieved": ach, "peak": tflops_peak,
+            "unit": "TFLOP/s", "frac": ach / tflops_peak, "algorithmic_bytes": by,
+            "algorithmic_flops": fl, "kernel_ms": ms, "peak_source": fl_src,
+            "other_roof_frac": (by / s / 1e9) / peaks["hbm_gbs"]}
 
 
 def seq_lengths(x):
@@ -433,34 +473,20 @@ def main():
     value = world * tokens / (ms_per_step / 1e3)
 
     # dominant kernel roofline (per launch, live CUDA-event duration)
-    d = x["D"]
-    fl = flops_per_token_head(d)
-    th = tokens * x["H"]
+    tensor = r["path"] == 1
     stage = max(range(2), key=lambda i: r["stage_ms"][i])
     stage_name = ["prep", "state"][stage]
-    tensor = r["path"] == 1
-    flops = fl[stage_name] * th
-    kernel_s = r["stage_ms"][stage] / 1e3
-    if tensor:
-        peak, bound = peaks["bf16_tflops"], "tensor"
-    else:
-        sm_mhz = peaks.get("sm_max_mhz", 2070.0)
-        peak, bound = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12, "alu"
-    achieved = flops / kernel_s / 1e12
+    kernel_key = "chunk_%s_%s" % (stage_name, "tc" if tensor else "simt")
     src = os.path.join(ROOT, "momentum_delta_rule_gb300", "csrc",
-                       "mdn_chunk_tc.cu" if tensor else "mdn_chunk_simt.cu")
-    kernel_key = ("chunk_%s_%s" % (stage_name, "tc" if tensor else "simt"))
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic_record(kernel_key, src),
-                "kernel": kernel_key, "kernel_ms": r["stage_ms"][stage],
-                "flops_per_launch": flops,
-                "peak_source": ("%s bf16 burst" % peak_src) if tensor else
-                "fp32 FFMA from unit counts: 152 SMs x 128 lanes x 2 x %.0f MHz"
-                % peaks.get("sm_max_mhz", 2070.0),
-                "hbm_bytes_per_launch_algorithmic": state_pass_bytes(
-                    x, 18432 if tensor else 34816) if stage_name == "state" else None,
-                "stage_ms": {"prep": r["stage_ms"][0], "state": r["stage_ms"][1]}}
+                       ("mdn_prep_tc.cu" if stage_name == "prep" else "mdn_chunk_tc.cu")
+                       if tensor else "mdn_chunk_simt.cu")
+    roofline = stage_roofline(stage_name, x, tensor, r["stage_ms"][stage], peaks, peak_src)
+    roofline["kernel"] = kernel_key
+    roofline["traffic"] = traffic_record(kernel_key, src)
+    other = 1 - stage
+    stages = {["prep", "state"][i]: stage_roofline(["prep", "state"][i], x, tensor,
+                                                   r["stage_ms"][i], peaks, peak_src)
+              for i in range(2)}
 
     line = {"metric": "MDN chunkwise fwd tokens/s", "value": value,
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -470,7 +496,7 @@ def main():
             "config": config_of(w, x, "flushed (256 MiB write) before every timed step"),
             "gpu_launches": r["launches_per_step"] * args.steps,
             "path": "tensor_core" if tensor else "cuda_core",
-            "roofline": roofline, "clocks": clk, "peaks": peak_src}
+            "roofline": roofline, "stages": stages, "clocks": clk, "peaks": peak_src}
 
     if not args.no_e2e:
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
@@ -480,6 +506,24 @@ def main():
                        "ms_per_step": e_ms}
     if not args.no_decode:
         line["decode"] = time_decode(mdn, args.decode_steps, dev, peaks)
+    if not args.no_other_workloads:
+        others = {}
+        for wo in W.ALL:
+            if wo.decode_steps or wo.name == w.name:
+                continue
+            xo = W.make_prefill(wo)
+            xo_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in xo.items()}
+            ro = time_prefill(mdn, xo_dev, wo, max(3, min(args.steps, 5)), 3, world, flush)
+            tok = sum(seq_lengths(xo))
+            t_o = ro["path"] == 1
+            others[wo.name] = {
+                "tokens_per_s": tok / (ro["total_ms"] / max(3, min(args.steps, 5)) / 1e3),
+                "ms_per_step": ro["total_ms"] / max(3, min(args.steps, 5)),
+                "path": "tensor_core" if t_o else "cuda_core",
+                "stages": {nm: stage_roofline(nm, xo, t_o, ro["stage_ms"][i], peaks, peak_src)
+                           for i, nm in enumerate(["prep", "state"])}}
+            del xo_dev
+        line["other_workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_oracle(x, args.cpu_seconds)
     if rank == 0:
