@@ -43,47 +43,57 @@ namespace {
 using namespace sm100;
 
 constexpr int kD = 128;                  // head size (dk = dv)
-constexpr int kNS = 64;                  // state columns per CTA
-constexpr int kSlices = kD / kNS;
-constexpr int kThreadsTC = 576;
-constexpr int kEpiWarps = 16;
-constexpr int kEpiCols = 16;             // state columns per epilogue thread
 constexpr int kStages = 2;
+constexpr int kEpiCols = 16;             // state columns per epilogue thread
 
-// shared memory (byte offsets from the 1024-aligned base)
+// shared memory of one pipeline stage (byte offsets from the stage base)
 constexpr uint32_t kKQBytes = 32768;     // per 64-wide dk half: K rows, then Q rows
-constexpr uint32_t kVBytes = 8192;       // V slice, 64 tokens x 64 columns, swizzled
+constexpr uint32_t kVBytes = 8192;       // V tile, 64 tokens x 64 columns, swizzled
 constexpr uint32_t kPrepBytes = (uint32_t)PrepLayoutTC::kBytes;   // 18432
 constexpr uint32_t kOffV = kKQBytes;
 constexpr uint32_t kOffPrep = kKQBytes + kVBytes;
 constexpr uint32_t kStageBytes = kKQBytes + kVBytes + kPrepBytes;  // 59392
-constexpr uint32_t kOffB1 = kStages * kStageBytes;   // [S | M] bf16, dk rows x 128, MN-major
-constexpr uint32_t kB1Bytes = 32768;
-constexpr uint32_t kOffR = kOffB1 + kB1Bytes;        // R bf16, 64 token rows x 64, MN-major
-constexpr uint32_t kRBytes = 8192;
-constexpr uint32_t kOffB3 = kOffR + kRBytes;         // [gS Vres | gM Vres], 64 rows x 128
-constexpr uint32_t kB3Bytes = 16384;
-constexpr uint32_t kOffBar = kOffB3 + kB3Bytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 
-// tensor memory columns
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD1 = 0;      // 128 columns
-constexpr uint32_t kColD2 = 128;    // 64 columns
-constexpr uint32_t kColSt = 256;    // fp32 state [S | M] of the slice, 128 columns
+// Everything that depends on the slice width NS (state columns per CTA).
+// In the N dimension of [S | M]-shaped operands, S takes columns [0, NS) and
+// M [NS, 2NS); operands are MN-major in blocks of 64 columns, so for NS = 64
+// the M half is a second block and for NS = 32 or 16 it shares the block.
+template <int NS>
+struct Cfg {
+    static_assert(NS == 16 || NS == 32 || NS == 64, "slice width");
+    static constexpr int kSlices = kD / NS;
+    static constexpr int kEpiWarps = 4 * NS / kEpiCols;      // 4 lane quadrants
+    static constexpr int kThreads = 32 * (2 + kEpiWarps);
+    static constexpr uint32_t kOffB1 = kStages * kStageBytes;  // [S | M] bf16, dk rows x 2NS
+    static constexpr uint32_t kB1Bytes = NS == 64 ? 32768 : 16384;
+    static constexpr uint32_t kB1M = NS == 64 ? 16384 : 0;    // byte offset of the M half
+    static constexpr uint32_t kOffR = kOffB1 + kB1Bytes;      // R bf16, 64 token rows x NS
+    static constexpr uint32_t kRBytes = 8192;
+    static constexpr uint32_t kOffB3 = kOffR + kRBytes;       // [gS Vres | -gM Vres]
+    static constexpr uint32_t kB3Bytes = NS == 64 ? 16384 : 8192;
+    static constexpr uint32_t kB3M = NS == 64 ? 8192 : 0;
+    static constexpr uint32_t kChM = NS == 64 ? 0 : NS / 8;   // chunk offset of the M half
+    static constexpr uint32_t kOffBar = kOffB3 + kB3Bytes;
+    static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+    // tensor memory columns
+    static constexpr uint32_t kColD1 = 0;                     // 2NS columns
+    static constexpr uint32_t kColD2 = 2 * NS;                // NS columns
+    static constexpr uint32_t kColSt = 4 * NS;                // fp32 state [S | M], 2NS columns
+    static constexpr uint32_t kTmemCols = 8 * NS;
+    static constexpr uint32_t kIdesc1 = idesc_bf16(128, 2 * NS, false, true);
+    static constexpr uint32_t kIdesc2 = idesc_bf16(128, NS, false, true);
+    static constexpr uint32_t kIdesc3 = idesc_bf16(128, 2 * NS, true, true);
+};
 
 struct Bars {
     uint64_t full[kStages];    // TMA bytes of a stage landed
-    uint64_t empty[kStages];   // stage free again (MMA commit + 16 epilogue warps)
+    uint64_t empty[kStages];   // stage free again (MMA commit + every epilogue warp)
     uint64_t d1, r, d2, v, d3, state, drain;   // d3: the state accumulation finished
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-constexpr uint32_t kIdesc1 = idesc_bf16(128, 128, false, true);
-constexpr uint32_t kIdesc2 = idesc_bf16(128, 64, false, true);
-constexpr uint32_t kIdesc3 = idesc_bf16(128, 128, true, true);
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -141,21 +151,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-__global__ void __launch_bounds__(kThreadsTC, 1)
+template <int NS>
+__global__ void __launch_bounds__(Cfg<NS>::kThreads, 1)
 chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_v) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
+    Bars *bars = reinterpret_cast<Bars *>(smem + Cfg<NS>::kOffBar);
     volatile int *abort = &bars->abort;
 
+    using C = Cfg<NS>;
+    constexpr int kEpiWarps = C::kEpiWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slice = blockIdx.x % kSlices;
-    const int sh = blockIdx.x / kSlices;
+    const int slice = blockIdx.x % C::kSlices;
+    const int sh = blockIdx.x / C::kSlices;
     const int s = sh / p.H, h = sh - s * p.H;
-    const int col0 = slice * kNS;
+    const int col0 = slice * NS;
     int start, len, slot0;
     sequence_range(p, s, start, len, slot0);
     const int nchunks = (len + kChunk - 1) / kChunk;
@@ -181,7 +194,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         prefetch_tensormap(&map_v);
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -219,9 +232,9 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t b1 = smem_u32(smem + kOffB1);
-            const uint32_t rr = smem_u32(smem + kOffR);
-            const uint32_t b3 = smem_u32(smem + kOffB3);
+            const uint32_t b1 = smem_u32(smem + C::kOffB1);
+            const uint32_t rr = smem_u32(smem + C::kOffR);
+            const uint32_t b3 = smem_u32(smem + C::kOffB3);
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c & 1, use = c >> 1;
                 const uint32_t kq = smem_u32(smem + st * kStageBytes);
@@ -236,7 +249,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
                         const uint64_t b = sdesc_sw128(b1 + (kb * 4 + kk) * 2048, 16384, 1024);
-                        mma_bf16(tmem + kColD1, a, b, kIdesc1, (kb | kk) != 0);
+                        mma_bf16(tmem + C::kColD1, a, b, C::kIdesc1, (kb | kk) != 0);
                     }
                 mma_commit(&bars->d1);
                 if (!mbar_wait(&bars->r, c & 1, abort)) break;
@@ -246,7 +259,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t a = sdesc_sw128(prep + kk * 32, 16, 1024);
                     const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
-                    mma_bf16(tmem + kColD2, a, b, kIdesc2, kk != 0);
+                    mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, kk != 0);
                 }
                 mma_commit(&bars->d2);
                 if (!mbar_wait(&bars->v, c & 1, abort)) break;
@@ -256,7 +269,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t a = sdesc_sw128(kq + kk * 2048, 16384, 1024);
                     const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
-                    mma_bf16(tmem + kColSt, a, b, kIdesc3, 1);
+                    mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
                 }
                 mma_commit(&bars->d3);
                 mma_commit(&bars->empty[st]);
@@ -275,12 +288,12 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         const int row = 32 * q + lane;          // TMEM lane = D row
         const int d = row;                      // state row (dk index)
-        const uint32_t st_s = lane_base + kColSt + c0;          // S columns of this thread
-        const uint32_t st_m = lane_base + kColSt + 64 + c0;     // M columns
+        const uint32_t st_s = lane_base + C::kColSt + c0;       // S columns of this thread
+        const uint32_t st_m = lane_base + C::kColSt + NS + c0;  // M columns
         const size_t st_off = (size_t)sh * kD * kD + (size_t)d * kD + col0 + c0;
-        unsigned char *b1 = smem + kOffB1;
-        unsigned char *rt = smem + kOffR;
-        unsigned char *b3 = smem + kOffB3;
+        unsigned char *b1 = smem + C::kOffB1;
+        unsigned char *rt = smem + C::kOffR;
+        unsigned char *b3 = smem + C::kOffB3;
         {
             float S[kEpiCols], M[kEpiCols];
 #pragma unroll
@@ -296,7 +309,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             tmem_st_wait();
             if (nchunks > 0) {
                 store_row16(b1, d, ch0, S, 1.f);
-                store_row16(b1 + 16384, d, ch0, M, 1.f);
+                store_row16(b1 + C::kB1M, d, ch0 + C::kChM, M, 1.f);
                 fence_proxy_async();
                 tc_fence_before();
                 __syncwarp();
@@ -335,8 +348,8 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_after();
                 {
                     float xs[kEpiCols], xm[kEpiCols];
-                    tmem_ld16(lane_base + kColD1 + c0, xs);
-                    tmem_ld16(lane_base + kColD1 + 64 + c0, xm);
+                    tmem_ld16(lane_base + C::kColD1 + c0, xs);
+                    tmem_ld16(lane_base + C::kColD1 + NS + c0, xm);
                     tmem_ld_wait();
                     const float keep = in_chunk ? 1.f : 0.f;
 #pragma unroll
@@ -366,10 +379,10 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_after();
                 {
                     float x[kEpiCols];
-                    tmem_ld16(lane_base + kColD2 + c0, x);
+                    tmem_ld16(lane_base + C::kColD2 + c0, x);
                     tmem_ld_wait();
                     store_row16(b3, i, ch0, x, gs);
-                    store_row16(b3 + 8192, i, ch0, x, -gm);
+                    store_row16(b3 + C::kB3M, i, ch0 + C::kChM, x, -gm);
                     fence_proxy_async();
                     tc_fence_before();
                     __syncwarp();
@@ -382,8 +395,8 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_after();
                 {
                     float xs[kEpiCols], xm[kEpiCols];
-                    tmem_ld16(lane_base + kColD1 + c0, xs);
-                    tmem_ld16(lane_base + kColD1 + 64 + c0, xm);
+                    tmem_ld16(lane_base + C::kColD1 + c0, xs);
+                    tmem_ld16(lane_base + C::kColD1 + NS + c0, xm);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < kEpiCols; ++j) oint[j] = ab * xs[j] - cb * xm[j];
@@ -396,7 +409,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_after();
                 {
                     float x[kEpiCols];
-                    tmem_ld16(lane_base + kColD2 + c0, x);
+                    tmem_ld16(lane_base + C::kColD2 + c0, x);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < kEpiCols; ++j) oint[j] += x[j];   // O = O_inter + O_intra
@@ -414,7 +427,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                     tmem_ld16(st_m, M);
                     tmem_ld_wait();
                     store_row16(b1, d, ch0, S, 1.f);
-                    store_row16(b1 + 16384, d, ch0, M, 1.f);
+                    store_row16(b1 + C::kB1M, d, ch0 + C::kChM, M, 1.f);
                     fence_proxy_async();
                 }
                 tc_fence_before();
@@ -456,7 +469,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
     if (threadIdx.x == 0 && *abort && p.status) atomicExch(p.status, (int)MDN_ERR_DEVICE_TIMEOUT);
 }
 
@@ -490,8 +503,42 @@ bool make_map(CUtensorMap *map, const void *base, int T_total, int H, bool swizz
     return r == CUDA_SUCCESS;
 }
 
+template <int NS>
+cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const CUtensorMap &mk,
+                              const CUtensorMap &mq, const CUtensorMap &mv) {
+    using C = Cfg<NS>;
+    auto kern = chunk_state_tc_kernel<NS>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.maxThreadsPerBlock < C::kThreads) return cudaErrorLaunchOutOfResources;
+    const long blocks = (long)p.n_seq * p.H * C::kSlices;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)blocks, C::kThreads, C::kSmemBytes, st>>>(p, mk, mq, mv);
+    return cudaGetLastError();
+}
+
+int sm_count() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
 }  // namespace
 
+// The slice width trades per-chunk latency (narrow slices: smaller MMAs and
+// epilogues) against CTA count: the narrowest slices (16, 32 or 64 columns)
+// whose CTAs still fit on the GPU in one wave.
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
     if (p.D != kD || p.dtype != MDN_BF16) return cudaErrorInvalidValue;
     if (p.prep_stride % 16 != 0) return cudaErrorInvalidValue;
@@ -500,19 +547,11 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
     if (!make_map(&mk, p.k, Tt, p.H, true) || !make_map(&mq, p.q, Tt, p.H, true) ||
         !make_map(&mv, p.v, Tt, p.H, true))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(chunk_state_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemBytes);
-    if (err != cudaSuccess) return err;
-    cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, chunk_state_tc_kernel);
-    if (err != cudaSuccess) return err;
-    if (fa.maxThreadsPerBlock < kThreadsTC) return cudaErrorLaunchOutOfResources;
-    const long blocks = (long)p.n_seq * p.H * kSlices;
-    if (blocks == 0) return cudaSuccess;
-    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    chunk_state_tc_kernel<<<(unsigned)blocks, kThreadsTC, kSmemBytes, st>>>(p, mk, mq, mv);
-    return cudaGetLastError();
+    const long chains = (long)p.n_seq * p.H;
+    const int sms = sm_count();
+    if (sms > 0 && chains * Cfg<16>::kSlices <= sms) return launch_state_tc_t<16>(p, st, mk, mq, mv);
+    if (sms > 0 && chains * Cfg<32>::kSlices <= sms) return launch_state_tc_t<32>(p, st, mk, mq, mv);
+    return launch_state_tc_t<64>(p, st, mk, mq, mv);
 }
 
 }  // namespace mdn

@@ -135,3 +135,13 @@ def test_path_selection():
         info = {}
         gpu_chunk_fwd(x, info=info)
         assert info["path"] == want, (dtype, D, info)
+
+
+@pytest.mark.parametrize("B,H", [(2, 2), (5, 5), (5, 10)])
+def test_slice_widths(B, H):
+    """The tensor-core state pass picks 16-, 32- or 64-column state slices by
+    the number of (sequence, head) chains (4, 25 and 50 chains here select
+    each width on a 152-SM GPU); every width must match the oracle."""
+    w = W.Workload("widths", dtype="bf16", state="randn", seed=16)
+    x = W.make_prefill(w, B=B, T=130, H=H, D=128, with_beta=True)
+    compare(x, gpu_chunk_fwd(x), chains(x))
