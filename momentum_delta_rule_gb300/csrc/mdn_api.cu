@@ -56,6 +56,13 @@ mdn_status current_device(int **status) {
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Workspace head: chunk offsets [n_seq + 1] and the longest-first sequence
+// order [n_seq] (both int32), each 256-byte aligned; prepared blocks follow.
+size_t meta_bytes(int n_seq) {
+    return round256(sizeof(int32_t) * ((size_t)n_seq + 1)) +
+           round256(sizeof(int32_t) * ((size_t)n_seq + 1));
+}
+
 // Upper bound on the chunk slots of any split of T_total into n_seq
 // sequences: sum ceil(L_s / 64) <= floor(T_total / 64) + n_seq.
 long chunk_slots_bound(int n_seq, int T_total) {
@@ -83,10 +90,9 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
                                     int dv, mdn_dtype dtype) {
     if (n_seq < 0 || T_total < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
     if (dtype != MDN_F32 && dtype != MDN_BF16) return 0;
-    const size_t offsets = round256(sizeof(int32_t) * ((size_t)n_seq + 1));
     const size_t prep = (size_t)chunk_slots_bound(n_seq, T_total) * (size_t)H *
                         mdn::kPrepBytesMax;
-    return round256(offsets + prep);
+    return round256(meta_bytes(n_seq) + prep);
 }
 
 mdn_status mdn_chunk_fwd_profiled(
@@ -156,9 +162,12 @@ mdn_status mdn_chunk_fwd_profiled(
     }
     if (T_total == 0) p.max_chunks = 0;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    const size_t off_bytes = round256(sizeof(int32_t) * ((size_t)n_seq + 1));
     p.chunk_offsets = reinterpret_cast<int32_t *>(ws);
-    p.prep = ws ? ws + off_bytes : nullptr;
+    p.seq_order = (cu_seqlens && ws)
+                      ? reinterpret_cast<int32_t *>(ws + round256(sizeof(int32_t) * ((size_t)n_seq + 1)))
+                      : nullptr;
+    p.prep = ws ? ws + meta_bytes(n_seq) : nullptr;
+    if (p.max_chunks == 0) p.seq_order = nullptr;   // the offsets kernel does not run
     p.prep_stride = mdn::kPrepBytesMax;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -34,9 +34,28 @@ constexpr int kThreads = 256;
 
 // ------------------------------------------------------------- offsets
 
-// off[s] = sum_{s' < s} ceil(len_{s'} / 64), s = 0..n_seq (one CTA).
+// off[s] = sum_{s' < s} ceil(len_{s'} / 64), s = 0..n_seq (one CTA), and
+// order[] = the sequences sorted by decreasing length (ties by index): the
+// rank of s counts the sequences that come before it.  Quadratic in n_seq,
+// so beyond kMaxOrdered sequences the order is the identity.
+constexpr int kMaxOrdered = 4096;
+
 __global__ void __launch_bounds__(1024)
-chunk_offsets_kernel(const int32_t *cu, int n_seq, int32_t *off) {
+chunk_offsets_kernel(const int32_t *cu, int n_seq, int32_t *off, int32_t *order) {
+    if (order) {
+        for (int s = threadIdx.x; s < n_seq; s += blockDim.x) {
+            int rank = s;
+            if (n_seq <= kMaxOrdered) {
+                const int ls = cu[s + 1] - cu[s];
+                rank = 0;
+                for (int t = 0; t < n_seq; ++t) {
+                    const int lt = cu[t + 1] - cu[t];
+                    rank += (lt > ls) || (lt == ls && t < s);
+                }
+            }
+            order[rank] = s;
+        }
+    }
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     if (threadIdx.x == 0) carry = 0;
@@ -320,8 +339,9 @@ chunk_state_simt_kernel(ChunkProblem p) {
     constexpr int kRowsA = kChunk / (kThreads / 32);   // 8 token rows per warp
     constexpr int kRowsC = D / (kThreads / 32);        // state rows per warp
     const int slice = blockIdx.x % kSlices;
-    const int sh = blockIdx.x / kSlices;
-    const int s = sh / p.H, h = sh - s * p.H;
+    const int kh = blockIdx.x / kSlices;
+    const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
+    const int sh = s * p.H + h;
     const int tid = threadIdx.x, cc = tid & 31, wg = tid >> 5;
     const int col0 = slice * kNS;
 
@@ -481,7 +501,8 @@ cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
-    chunk_offsets_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.chunk_offsets);
+    chunk_offsets_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.chunk_offsets,
+                                              p.seq_order);
     return cudaGetLastError();
 }
 

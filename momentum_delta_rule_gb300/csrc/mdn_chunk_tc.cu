@@ -166,8 +166,9 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
     constexpr int kEpiWarps = C::kEpiWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x % C::kSlices;
-    const int sh = blockIdx.x / C::kSlices;
-    const int s = sh / p.H, h = sh - s * p.H;
+    const int kh = blockIdx.x / C::kSlices;
+    const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
+    const int sh = s * p.H + h;                 // (sequence, head) of the states
     const int col0 = slice * NS;
     int start, len, slot0;
     sequence_range(p, s, start, len, slot0);

@@ -64,6 +64,7 @@ struct ChunkProblem {
     int max_chunks;              // prepared-block slots per head
     mdn_dtype dtype;
     int32_t *chunk_offsets;      // [n_seq + 1] in the workspace (varlen only)
+    int32_t *seq_order;          // [n_seq] sequences longest first (varlen only), or null
     unsigned char *prep;         // max_chunks * H prepared blocks
     size_t prep_stride;          // bytes per prepared block
     int *status;                 // device status word
@@ -136,6 +137,12 @@ __device__ __forceinline__ bool locate_chunk(const ChunkProblem &p, int gc,
     loc.t0 = start + c * kChunk;
     loc.n = min(kChunk, len - c * kChunk);
     return true;
+}
+
+// The state pass walks sequences longest first when an order is given, so the
+// longest chains start in the first wave (longest-processing-time order).
+__device__ __forceinline__ int ordered_sequence(const ChunkProblem &p, int k) {
+    return p.seq_order ? p.seq_order[k] : k;
 }
 
 // Token range and chunk-slot base of one sequence.
