@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-other-workloads", action="store_true",
                    help="skip timing the other prefill workloads")
+    p.add_argument("--decode-only", action="store_true",
+                   help="time only the decode workload and print its object")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="minimum CPU time of the oracle baseline sample")
     return p.parse_args()
@@ -459,6 +461,11 @@ def main():
     import momentum_delta_rule_gb300 as mdn
     mdn.lib()                                    # fails loudly if not built
     peaks, peak_src = load_peaks()
+    if args.decode_only:
+        d = time_decode(mdn, args.decode_steps, dev, peaks)
+        if rank == 0:
+            print(json.dumps(d), flush=True)
+        return
     w = W.BY_NAME[args.workload]
     x = W.make_prefill(w)
     x_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
