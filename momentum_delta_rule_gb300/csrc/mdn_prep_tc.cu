@@ -38,15 +38,25 @@ constexpr int kD = 128;
 constexpr int kThreadsP = 256;
 constexpr int LM = kChunk + 1;                 // padded fp32 row stride
 
-// shared memory (bytes from the 1024-aligned base)
-constexpr uint32_t kOffKQ = 0;                 // K/Q tiles (32 KiB); later L and B2
-constexpr uint32_t kOffL = 0;                  // L fp32 [64][65]
-constexpr uint32_t kOffB2 = 17408;             // bf16(T), MN-major B operand (8 KiB), 1024-aligned
-constexpr uint32_t kOffG = 32768;              // Gamma fp32 [64][65]; later T fp32 [64][65]
-constexpr uint32_t kOffA2 = kOffG + 17408;     // [I; A_O] bf16, K-major A operand (16 KiB), 1024-aligned
-constexpr uint32_t kOffVec = kOffA2 + 16384;   // 8 x 64 fp32 scalars per token
-constexpr uint32_t kOffBarP = kOffVec + 2048;
+// shared memory (bytes from the 1024-aligned base), 55 KiB so that four CTAs
+// share an SM.  Regions are reused once their last reader is done:
+//   [0, 32768)       K/Q tiles (TMA), read by the Gram MMA only; then
+//   [0, 16640)       Gamma fp32 [64][65], later T fp32 [64][65]
+//   [17408, 34048)   L fp32 [64][65]; after the inverse, bf16(T) (8 KiB)
+//   [34048, 38272)   the per-token vectors (2 KiB); after L is built, the
+//                    inverse's 32 x 33 fp32 scratch
+//   [38912, 55296)   [I; A_O] bf16, K-major A operand
+constexpr uint32_t kOffKQ = 0;
+constexpr uint32_t kOffG = 0;
+constexpr uint32_t kOffL = 17408;
+constexpr uint32_t kOffB2 = 17408;
+constexpr uint32_t kOffVec = 34048;
+constexpr uint32_t kOffXs = 34048;
+constexpr uint32_t kOffA2 = 38912;
+constexpr uint32_t kOffBarP = kOffA2 + 16384;
 constexpr uint32_t kSmemP = kOffBarP + 128 + 1024;
+static_assert(kOffL + 4 * 64 * 65 <= kOffVec + 0 && kOffXs + 4 * 32 * 33 <= kOffA2, "prep layout");
+static_assert(kSmemP <= 57344, "four CTAs per SM");
 
 constexpr uint32_t kTmemColsP = 128;
 constexpr uint32_t kColG = 0;                  // Gram accumulator, 64 columns
@@ -84,7 +94,7 @@ __device__ __forceinline__ float scan64(float x, float *xch) {
     return x;
 }
 
-__global__ void __launch_bounds__(kThreadsP, 3)
+__global__ void __launch_bounds__(kThreadsP, 4)
 chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q) {
     extern __shared__ unsigned char smem_raw[];
@@ -103,6 +113,15 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     if (!locate_chunk(p, gc, loc)) return;
     const int n = loc.n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // gates first: their latency overlaps the setup below
+    float g_a = 1.f, g_mu = 0.f, g_be = 0.f, g_et = 0.f;
+    if (tid < n) {
+        const size_t gi = (size_t)(loc.t0 + tid) * p.H + h;
+        g_a = p.alpha[gi];
+        g_mu = p.mu[gi];
+        g_et = p.eta[gi];
+        g_be = p.beta ? p.beta[gi] : 1.f;
+    }
 
     if (tid == 0) {
         mbar_init(&bars->tma, 1);
@@ -122,25 +141,35 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 2) {
-        // ---- K and Q tiles in (the Gram MMA is issued once Gamma is done)
+        // ---- K and Q tiles in, then the Gram MMA
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars->tma, 32768);
             tma_load_3d(smem + kOffKQ + 0, &map_k, &bars->tma, 0, h, loc.t0);
             tma_load_3d(smem + kOffKQ + 8192, &map_q, &bars->tma, 0, h, loc.t0);
             tma_load_3d(smem + kOffKQ + 16384, &map_k, &bars->tma, 64, h, loc.t0);
             tma_load_3d(smem + kOffKQ + 24576, &map_q, &bars->tma, 64, h, loc.t0);
+            // Gram MMA G = [K; Q] K^T as soon as the tiles land: Gamma reuses
+            // their space
+            const uint32_t kq = smem_u32(smem + kOffKQ);
+            if (mbar_wait(&bars->tma, 0, abort)) {
+                tc_fence_after();
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
+                        mma_bf16(tmem + kColG, a, a, kIdescGram, (kb | kk) != 0);
+                    }
+                mma_commit(&bars->gram);
+            } else {
+                int dummy = 0;           // the copy must land before the CTA exits
+                mbar_wait(&bars->tma, 0, &dummy);
+            }
         }
     } else if (warp < 2) {
         // ---- gates, log-space prefix scans, Gamma, b, carry vectors
         const int i = tid;                 // token 0..63
-        float a = 1.f, mu = 0.f, be = 0.f, et = 0.f;
-        if (i < n) {
-            const size_t gi = (size_t)(loc.t0 + i) * p.H + h;
-            a = p.alpha[gi];
-            mu = p.mu[gi];
-            et = p.eta[gi];
-            be = p.beta ? p.beta[gi] : 1.f;
-        }
+        const float a = g_a, mu = g_mu, be = g_be, et = g_et;
         const bool zmu = (mu == 0.f);
         float *xch = vec + vScan * kChunk;
         const float A = scan64(logf(a), xch);
@@ -169,55 +198,67 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     }
     __syncthreads();   // gates and prefix scans are in shared memory
 
-    // ---- Gamma, one column per lane of warps 0-1:
-    //      gamma_{j,j} = beta_j, gamma_{r,j} = alpha_r gamma_{r-1,j} + beta_r m_{r,j},
-    //      m_{r,j} = [Z_r = Z_j] exp(U_r - U_j).  The gates of all 64 tokens
-    //      sit in registers (token l and 32 + l in lane l) and step r
-    //      broadcasts token r by shuffles: the dependent chain touches no
-    //      memory.  Only the lower triangle is ever read.
-    if (warp < 2) {
-        const int j = tid;
-        const float a_lo = vec[vAlpha * kChunk + lane], a_hi = vec[vAlpha * kChunk + 32 + lane];
-        const float b_lo = vec[vBeta * kChunk + lane], b_hi = vec[vBeta * kChunk + 32 + lane];
-        const float u_lo = vec[vU * kChunk + lane], u_hi = vec[vU * kChunk + 32 + lane];
-        const float z_lo = vec[vZ * kChunk + lane], z_hi = vec[vZ * kChunk + 32 + lane];
+    // ---- Gamma: gamma_{j,j} = beta_j, gamma_{r,j} = alpha_r gamma_{r-1,j} +
+    //      beta_r m_{r,j} with m_{r,j} = [Z_r = Z_j] exp(U_r - U_j), in four
+    //      row segments of 16 run side by side (thread = segment x column).
+    //      Each segment starts from zero; as the recurrence is affine,
+    //      gamma_{r,j} = local_{r,j} + (prod_{u=r0..r} alpha_u) gamma_{r0-1,j}
+    //      restores the exact values (segment ends first, in order).  Only
+    //      the lower triangle is ever read.
+    float *F = vec + vB * kChunk;      // prod of alpha from the segment start (b comes later)
+    // Gamma overwrites the K/Q tiles: the Gram MMA must have read them
+    const bool gram_ok = __all_sync(0xffffffffu, mbar_wait(&bars->gram, 0, abort));
+    if (gram_ok) {
+        tc_fence_after();
+    }
+    {
+        const int j = tid & 63, r0 = 16 * (tid >> 6);
         const float Uj = vec[vU * kChunk + j], Zj = vec[vZ * kChunk + j];
-        float g = vec[vBeta * kChunk + j];
-        G[j * LM + j] = g;
+        float gl = 0.f, pa = 1.f;
 #pragma unroll
-        for (int r = 1; r < kChunk; ++r) {
-            const float ar = __shfl_sync(0xffffffffu, r < 32 ? a_lo : a_hi, r & 31);
-            const float br = __shfl_sync(0xffffffffu, r < 32 ? b_lo : b_hi, r & 31);
-            const float ur = __shfl_sync(0xffffffffu, r < 32 ? u_lo : u_hi, r & 31);
-            const float zr = __shfl_sync(0xffffffffu, r < 32 ? z_lo : z_hi, r & 31);
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = r0 + rr;
+            const float ar = vec[vAlpha * kChunk + r], br = vec[vBeta * kChunk + r];
+            const float ur = vec[vU * kChunk + r], zr = vec[vZ * kChunk + r];
+            pa *= ar;
             const float m = (zr == Zj) ? __expf(ur - Uj) : 0.f;
-            const float gn = ar * g + br * m;
-            if (r > j) {
-                g = gn;
-                G[r * LM + j] = g;
+            const float gn = (r == j) ? br : ar * gl + br * m;
+            if (r >= j) {
+                gl = gn;
+                G[r * LM + j] = gl;
+            }
+            if (j == 0) F[r] = pa;
+        }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        // exact values at rows 31 and 47 (row 15 is exact already)
+        const int j = tid;
+        float e = G[15 * LM + j];
+#pragma unroll
+        for (int g = 1; g < 4; ++g) {
+            const int rend = 16 * g + 15;
+            if (j < 16 * g) {
+                e = G[rend * LM + j] + F[rend] * e;
+                G[rend * LM + j] = e;
+            } else if (j <= rend) {
+                e = G[rend * LM + j];
+            }
+        }
+    }
+    __syncthreads();
+    {
+        const int j = tid & 63, r0 = 16 * (tid >> 6);
+        if (j < r0) {
+            const float e = G[(r0 - 1) * LM + j];
+#pragma unroll
+            for (int rr = 0; rr < 15; ++rr) {
+                const int r = r0 + rr;
+                G[r * LM + j] += F[r] * e;
             }
         }
     }
     __syncthreads();   // Gamma complete
-    if (warp == 2 && lane == 0) {
-        // Gram MMA: G = [K; Q] K^T (the copy landed long ago)
-        const uint32_t kq = smem_u32(smem + kOffKQ);
-        if (mbar_wait(&bars->tma, 0, abort)) {
-            tc_fence_after();
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
-                    mma_bf16(tmem + kColG, a, b, kIdescGram, (kb | kk) != 0);
-                }
-            mma_commit(&bars->gram);
-        } else {
-            int dummy = 0;           // the copy must land before the CTA exits
-            mbar_wait(&bars->tma, 0, &dummy);
-        }
-    }
     if (warp < 2) {
         const int i = tid;
         const float a = vec[vAlpha * kChunk + i], be = vec[vBeta * kChunk + i];
@@ -312,7 +353,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     //   per column), then [[A,0],[C,B]]^{-1} = [[A^-1,0],[-B^-1 C A^-1, B^-1]]
     //   for the 16-blocks inside each 32-block and for the two 32-blocks.
     float *Tm = G;
-    float *X = reinterpret_cast<float *>(smem + kOffB2);    // scratch until B2 is built
+    float *X = reinterpret_cast<float *>(smem + kOffXs);    // scratch (the vectors are consumed)
     constexpr int LX = 33;
     if (warp < 2) {
         const int blk = warp * 2 + (lane >> 4);
