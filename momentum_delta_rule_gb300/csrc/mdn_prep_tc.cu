@@ -130,6 +130,13 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
+        // K and Q tiles: issued before the block-wide setup, their latency
+        // gates the Gram MMA and with it Gamma
+        mbar_arrive_expect_tx(&bars->tma, 32768);
+        tma_load_3d(smem + kOffKQ + 0, &map_k, &bars->tma, 0, h, loc.t0);
+        tma_load_3d(smem + kOffKQ + 8192, &map_q, &bars->tma, 0, h, loc.t0);
+        tma_load_3d(smem + kOffKQ + 16384, &map_k, &bars->tma, 64, h, loc.t0);
+        tma_load_3d(smem + kOffKQ + 24576, &map_q, &bars->tma, 64, h, loc.t0);
     }
     if (warp == 2) {
         tmem_alloc(&bars->tmem_base, kTmemColsP);
@@ -141,13 +148,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 2) {
-        // ---- K and Q tiles in, then the Gram MMA
+        // ---- the Gram MMA once the K/Q tiles land
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->tma, 32768);
-            tma_load_3d(smem + kOffKQ + 0, &map_k, &bars->tma, 0, h, loc.t0);
-            tma_load_3d(smem + kOffKQ + 8192, &map_q, &bars->tma, 0, h, loc.t0);
-            tma_load_3d(smem + kOffKQ + 16384, &map_k, &bars->tma, 64, h, loc.t0);
-            tma_load_3d(smem + kOffKQ + 24576, &map_q, &bars->tma, 64, h, loc.t0);
             // Gram MMA G = [K; Q] K^T as soon as the tiles land: Gamma reuses
             // their space
             const uint32_t kq = smem_u32(smem + kOffKQ);
@@ -352,6 +354,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     //   diagonal 16x16 blocks by forward substitution in registers (one lane
     //   per column), then [[A,0],[C,B]]^{-1} = [[A^-1,0],[-B^-1 C A^-1, B^-1]]
     //   for the 16-blocks inside each 32-block and for the two 32-blocks.
+    //   The blocks above the diagonal 16-blocks are never read; bf16(T)
+    //   writes zeros there.
     float *Tm = G;
     float *X = reinterpret_cast<float *>(smem + kOffXs);    // scratch (the vectors are consumed)
     constexpr int LX = 33;
@@ -369,12 +373,6 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tm[(base + r) * LM + base + c] = t[r];
-    } else {
-        // zero the blocks above the diagonal blocks
-        for (int idx = tid - 64; idx < kChunk * kChunk; idx += kThreadsP - 64) {
-            const int r = idx >> 6, cc = idx & 63;
-            if ((cc >> 4) > (r >> 4)) Tm[r * LM + cc] = 0.f;
-        }
     }
     __syncthreads();
     // 16-blocks below the diagonal inside each 32-block (two of them); each
@@ -443,11 +441,13 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     for (int idx = tid; idx < kChunk * 8; idx += kThreadsP) {
         const int r = idx >> 3, c = idx & 7;
         const float *src = Tm + r * LM + c * 8;
-        uint4 w;
-        w.x = pack2(src[0], src[1]);
-        w.y = pack2(src[2], src[3]);
-        w.z = pack2(src[4], src[5]);
-        w.w = pack2(src[6], src[7]);
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if ((c >> 1) <= (r >> 4)) {              // above the diagonal blocks T is zero
+            w.x = pack2(src[0], src[1]);
+            w.y = pack2(src[2], src[3]);
+            w.z = pack2(src[4], src[5]);
+            w.w = pack2(src[6], src[7]);
+        }
         *reinterpret_cast<uint4 *>(B2 + sw128_offset(r, c)) = w;
     }
     fence_proxy_async();
