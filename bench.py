@@ -321,22 +321,35 @@ def time_prefill(mdn, x_dev, w, steps, warmup, world, flush):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # Timed steps: events around the whole call only, so the state pass may
+    # overlap the prep kernel's last wave (programmatic dependent launch).
+    cur = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(steps):
         flush.zero_()
-        step(evs[i])
+        evs[i][0].record(cur)
+        step()
+        evs[i][1].record(cur)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     st = mdn.device_status()
     if st != 0:
         raise RuntimeError("device status %d after the timed region" % st)
-    stage0 = [e[0].elapsed_time(e[1]) for e in evs]
-    stage1 = [e[1].elapsed_time(e[2]) for e in evs]
-    total = [e[0].elapsed_time(e[2]) for e in evs]
+    total = [a.elapsed_time(b) for a, b in evs]
+    # Per-stage split from separate steps with an event between the kernels
+    # (which serialises them): for the per-kernel rooflines only.
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        step(sevs[i])
+    torch.cuda.synchronize()
+    stage0 = [e[0].elapsed_time(e[1]) for e in sevs]
+    stage1 = [e[1].elapsed_time(e[2]) for e in sevs]
     return {"total_ms": sum(total), "stage_ms": [statistics.mean(stage0),
                                                  statistics.mean(stage1)],
             "wall_s": wall, "path": info.get("path"),

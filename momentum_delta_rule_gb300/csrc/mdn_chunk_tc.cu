@@ -167,6 +167,12 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x % C::kSlices;
     const int kh = blockIdx.x / C::kSlices;
+    // This grid may start while the prep kernel finishes (programmatic
+    // dependent launch).  Packed sequences read the chunk offsets first: wait
+    // for the preceding grids right away.  Fixed-length batches run their
+    // setup and initial-state loads first; the producer waits before its
+    // first prepared-block copy.
+    if (p.cu_seqlens != nullptr) grid_dependency_wait();
     const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
     const int sh = s * p.H + h;                 // (sequence, head) of the states
     const int col0 = slice * NS;
@@ -209,6 +215,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             int last_use[kStages] = {-1, -1};
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c & 1, use = c >> 1;
+                if (c == 0) grid_dependency_wait();   // the prepared blocks are complete
                 if (!mbar_wait(&bars->empty[st], (use & 1) ^ 1, abort)) break;
                 unsigned char *stage = smem + st * kStageBytes;
                 const int t0 = start + c * kChunk;
@@ -519,8 +526,18 @@ cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const CUte
     const long blocks = (long)p.n_seq * p.H * C::kSlices;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)blocks, C::kThreads, C::kSmemBytes, st>>>(p, mk, mq, mv);
-    return cudaGetLastError();
+    // programmatic dependent launch: may start while the prep kernel drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, mk, mq, mv);
 }
 
 int sm_count() {

@@ -108,6 +108,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     unsigned char *A2 = smem + kOffA2;
     unsigned char *B2 = smem + kOffB2;
 
+    // The state pass may be scheduled as soon as every CTA of this grid has
+    // started; it waits for this grid's completion before it reads a
+    // prepared block.
+    grid_launch_dependents();
     const int gc = blockIdx.x, h = blockIdx.y;
     ChunkLoc loc;
     if (!locate_chunk(p, gc, loc)) return;
