@@ -183,7 +183,7 @@ mdn_status mdn_chunk_fwd_profiled(
     if (err == cudaSuccess && cu_seqlens && p.max_chunks > 0)
         err = mdn::launch_chunk_offsets(p, cs);
     if (err == cudaSuccess)
-        err = tensor ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs, false);
+        err = tensor ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs);
     if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
     if (err == cudaSuccess)
         err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_chunk_state_simt(p, cs);

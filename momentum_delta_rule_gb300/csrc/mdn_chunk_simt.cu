@@ -111,7 +111,7 @@ __device__ __forceinline__ float scan64(float x, float *xch) {
     return x;
 }
 
-template <int D, typename Tin, bool kTC>
+template <int D, typename Tin>
 __global__ void __launch_bounds__(kThreads)
 chunk_prep_simt_kernel(ChunkProblem p) {
     using SM = PrepSmem<D>;
@@ -250,8 +250,7 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     unsigned char *blk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
     float *Tg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffT);
     float *AOTg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffAOT);
-    float *vec = reinterpret_cast<float *>(
-        blk + (kTC ? PrepLayoutTC::kOffVec : PrepLayout<float>::kOffVec));
+    float *vec = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffVec);
     {
         const int ti = tid >> 4, tj = tid & 15;
         float acc[4][4] = {};
@@ -267,35 +266,14 @@ chunk_prep_simt_kernel(ChunkProblem p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[r][c] += ar[r] * tc[c];
         }
-        if constexpr (kTC) {
-            // bf16, four consecutive columns (8 bytes) per row and matrix
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = 4 * ti + r, j0 = 4 * tj;
-                const uint32_t off = (uint32_t)((i >> 3) * 1024 + (i & 7) * 128 +
-                                                ((((j0 >> 3) ^ (i & 7)) << 4)) + (j0 & 7) * 2);
-                __nv_bfloat162 t01 = __floats2bfloat162_rn(Tm[i * LM + j0], Tm[i * LM + j0 + 1]);
-                __nv_bfloat162 t23 = __floats2bfloat162_rn(Tm[i * LM + j0 + 2], Tm[i * LM + j0 + 3]);
-                __nv_bfloat162 a01 = __floats2bfloat162_rn(acc[r][0], acc[r][1]);
-                __nv_bfloat162 a23 = __floats2bfloat162_rn(acc[r][2], acc[r][3]);
-                uint2 tv, av;
-                tv.x = *reinterpret_cast<uint32_t *>(&t01);
-                tv.y = *reinterpret_cast<uint32_t *>(&t23);
-                av.x = *reinterpret_cast<uint32_t *>(&a01);
-                av.y = *reinterpret_cast<uint32_t *>(&a23);
-                *reinterpret_cast<uint2 *>(blk + PrepLayoutTC::kOffT + off) = tv;
-                *reinterpret_cast<uint2 *>(blk + PrepLayoutTC::kOffAOT + off) = av;
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * ti + r, j = 4 * tj + c;
+                AOTg[i * kChunk + j] = acc[r][c];
+                Tg[i * kChunk + j] = Tm[i * LM + j];
             }
-        } else {
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int i = 4 * ti + r, j = 4 * tj + c;
-                    AOTg[i * kChunk + j] = acc[r][c];
-                    Tg[i * kChunk + j] = Tm[i * LM + j];
-                }
-        }
     }
     if (tid < kChunk) {
         const int i = tid;
@@ -474,10 +452,10 @@ chunk_state_simt_kernel(ChunkProblem p) {
     }
 }
 
-template <int D, typename Tin, bool kTC>
+template <int D, typename Tin>
 cudaError_t launch_prep_t(const ChunkProblem &p, cudaStream_t st) {
     if (p.max_chunks == 0) return cudaSuccess;
-    auto kp = chunk_prep_simt_kernel<D, Tin, kTC>;
+    auto kp = chunk_prep_simt_kernel<D, Tin>;
     cudaError_t err = cudaFuncSetAttribute(
         kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepSmem<D>::kBytes);
     if (err != cudaSuccess) return err;
@@ -506,18 +484,13 @@ cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st,
-                                   bool tc_layout) {
-    if (tc_layout) {
-        if (p.D != 128 || p.dtype != MDN_BF16) return cudaErrorInvalidValue;
-        return launch_prep_t<128, __nv_bfloat16, true>(p, st);
-    }
+cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st) {
     if (p.D == 128) {
-        return p.dtype == MDN_BF16 ? launch_prep_t<128, __nv_bfloat16, false>(p, st)
-                                   : launch_prep_t<128, float, false>(p, st);
+        return p.dtype == MDN_BF16 ? launch_prep_t<128, __nv_bfloat16>(p, st)
+                                   : launch_prep_t<128, float>(p, st);
     }
-    return p.dtype == MDN_BF16 ? launch_prep_t<64, __nv_bfloat16, false>(p, st)
-                               : launch_prep_t<64, float, false>(p, st);
+    return p.dtype == MDN_BF16 ? launch_prep_t<64, __nv_bfloat16>(p, st)
+                               : launch_prep_t<64, float>(p, st);
 }
 
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st) {

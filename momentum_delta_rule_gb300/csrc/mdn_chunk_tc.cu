@@ -26,10 +26,14 @@
 // evolve independently (column j of Vres depends only on column j of S_0 and
 // M_0), so the two slices of a head never communicate.
 //
-// Warp roles (18 warps): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 2..17 epilogue (TMEM lane quadrant = warp % 4, 16-column quarter of the
-// slice = (warp-2)/4), so every critical-path epilogue step is spread over
-// 512 threads.
+// Warp roles (18 warps for 64-column slices): 0 TMA producer, 1 MMA issuer
+// + TMEM owner, 2..17 epilogue (TMEM lane quadrant = warp % 4, 16-column
+// group of the slice = (warp-2)/4).  A warp reaches only the TMEM lanes of
+// its quadrant, and the warps of a quadrant share one scheduler; [K; Q] and
+// [T; A_O T] rows are therefore interleaved in blocks of 16 (tc_row), so that
+// every quadrant holds 16 token rows and 16 query rows and the token-row
+// steps (R, Vres) use all four schedulers (16x32bx2 TMEM loads: lanes t and
+// t + 16 take 8 columns each).
 // Every wait is bounded (1 s); on expiry the CTA records
 // MDN_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -186,7 +190,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             mbar_init(&bars->empty[i], 1 + kEpiWarps);
         }
         mbar_init(&bars->d1, 1);
-        mbar_init(&bars->r, kEpiWarps / 2);
+        mbar_init(&bars->r, kEpiWarps);
         mbar_init(&bars->d2, 1);
         mbar_init(&bars->v, kEpiWarps);
         mbar_init(&bars->d3, 1);
@@ -222,10 +226,15 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 const unsigned char *blk =
                     p.prep + ((size_t)(slot0 + c) * p.H + h) * p.prep_stride;
                 mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
-                tma_load_3d(stage + 0, &map_k, &bars->full[st], 0, h, t0);
-                tma_load_3d(stage + 8192, &map_q, &bars->full[st], 0, h, t0);
-                tma_load_3d(stage + 16384, &map_k, &bars->full[st], 64, h, t0);
-                tma_load_3d(stage + 24576, &map_q, &bars->full[st], 64, h, t0);
+                // [K; Q] rows interleaved by 16 (tc_row): 16-token boxes
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        unsigned char *dst = stage + hh * 16384 + g * 4096;
+                        tma_load_3d(dst, &map_k, &bars->full[st], 64 * hh, h, t0 + 16 * g);
+                        tma_load_3d(dst + 2048, &map_q, &bars->full[st], 64 * hh, h, t0 + 16 * g);
+                    }
                 tma_load_3d(stage + kOffV, &map_v, &bars->full[st], col0, h, t0);
                 bulk_load(stage + kOffPrep, blk, kPrepBytes, &bars->full[st]);
                 last_use[st] = use;
@@ -275,7 +284,8 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 // MMA3: [S | M] += K^T [gS Vres | -gM Vres]; K-steps of 16 tokens
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(kq + kk * 2048, 16384, 1024);
+                    // K tokens 16kk..16kk+15 sit at tile rows 32kk..32kk+15
+                    const uint64_t a = sdesc_sw128(kq + kk * 4096, 16384, 1024);
                     const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
                     mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
                 }
@@ -324,9 +334,17 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 if (lane == 0) mbar_arrive(&bars->state);
             }
         }
+        // Token rows: the lower 16 lanes of this warp's quadrant hold the K
+        // rows of tokens tok = 16 q + lane % 16, the upper 16 the Q rows of
+        // the same tokens (tc_row order); lanes t and t + 16 split the
+        // warp's 16 columns into two halves of 8 (16x32bx2 TMEM loads).
+        const int tok = 16 * q + (lane & 15);
+        const int cg = c0 + 8 * (lane >> 4);          // first of this thread's 8 columns
+        const uint32_t chk = (uint32_t)(cg >> 3);     // their 16-byte chunk
+        const uint32_t lk = tmem + ((uint32_t)(32 * q) << 16);        // K / T rows
+        const uint32_t lq = tmem + ((uint32_t)(32 * q + 16) << 16);   // Q / A_O T rows
         const size_t rs = (size_t)p.H * kD;
-        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + c0;
-        float oint[kEpiCols];
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + cg;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1, use = c >> 1;
             unsigned char *stage = smem + st * kStageBytes;
@@ -336,95 +354,83 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             if (!warp_wait(&bars->full[st], use & 1, abort)) break;
             // Everything that depends only on the staged inputs is read before
             // waiting on the MMAs, so the critical path sees no shared loads.
-            const int i = (q < 2) ? row : row - 64;     // token row (K rows / Q rows)
-            const float ab = vec[kVecAbar * kChunk + i];
-            const float cb = vec[(q < 2 ? kVecBmA : kVecB) * kChunk + i];
-            const float gs = vec[kVecGS * kChunk + i];
-            const float gm = vec[kVecGM * kChunk + i];
-            const bool in_chunk = i < n;
-            uint4 vraw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-            if (q < 2) {
-                const unsigned char *vt = stage + kOffV;
-                vraw[0] = *reinterpret_cast<const uint4 *>(vt + sw128_offset(i, ch0));
-                vraw[1] = *reinterpret_cast<const uint4 *>(vt + sw128_offset(i, ch0 + 1));
-            }
+            // Past the chunk end the coefficients and V are zero, so R is too.
+            const bool in_chunk = tok < n;
+            const float ab = vec[kVecAbar * kChunk + tok];
+            const float cbk = in_chunk ? vec[kVecBmA * kChunk + tok] : 0.f;
+            const float abk = in_chunk ? ab : 0.f;
+            const float cbq = vec[kVecB * kChunk + tok];
+            const float gs = vec[kVecGS * kChunk + tok];
+            const float gm = vec[kVecGM * kChunk + tok];
+            uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
+            if (in_chunk) vraw = *reinterpret_cast<const uint4 *>(stage + kOffV + sw128_offset(tok, chk));
 
-            if (q < 2) {
-                // ======== token-row warps: the critical path of the chunk
-                // R = V - abar K S_0 + b_{i-1} alpha_i K M_0 (zero past the chunk end)
-                if (!warp_wait(&bars->d1, c & 1, abort)) break;
-                tc_fence_after();
-                {
-                    float xs[kEpiCols], xm[kEpiCols];
-                    tmem_ld16(lane_base + C::kColD1 + c0, xs);
-                    tmem_ld16(lane_base + C::kColD1 + NS + c0, xm);
-                    tmem_ld_wait();
-                    const float keep = in_chunk ? 1.f : 0.f;
+            // ---- R = V - abar K S_0 + b_{i-1} alpha_i K M_0: the critical step
+            if (!warp_wait(&bars->d1, c & 1, abort)) break;
+            tc_fence_after();
+            {
+                float xs[8], xm[8], vv[8], r[8];
+                tmem_ld_16x2x8(lk + C::kColD1 + c0, xs);
+                tmem_ld_16x2x8(lk + C::kColD1 + NS + c0, xm);
+                tmem_ld_wait();
+                unpack_bf16x8(vraw, vv);
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        float vv[8], r[8];
-                        unpack_bf16x8(vraw[cc], vv);
+                for (int e = 0; e < 8; ++e) r[e] = vv[e] - abk * xs[e] + cbk * xm[e];
+                uint4 w;
+                w.x = pack_bf16x2(r[0], r[1]);
+                w.y = pack_bf16x2(r[2], r[3]);
+                w.z = pack_bf16x2(r[4], r[5]);
+                w.w = pack_bf16x2(r[6], r[7]);
+                *reinterpret_cast<uint4 *>(rt + sw128_offset(tok, chk)) = w;
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->r);
+            }
+            // ---- O_inter = abar Q S_0 - b Q M_0, then the state rescale (both
+            //      overlap MMA2)
+            float oint[8];
+            {
+                float xs[8], xm[8];
+                tmem_ld_16x2x8(lq + C::kColD1 + c0, xs);
+                tmem_ld_16x2x8(lq + C::kColD1 + NS + c0, xm);
+                tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * cc + e;
-                            r[e] = keep * (vv[e] - ab * xs[j] + cb * xm[j]);
-                        }
-                        uint4 w;
-                        w.x = pack_bf16x2(r[0], r[1]);
-                        w.y = pack_bf16x2(r[2], r[3]);
-                        w.z = pack_bf16x2(r[4], r[5]);
-                        w.w = pack_bf16x2(r[6], r[7]);
-                        *reinterpret_cast<uint4 *>(rt + sw128_offset(i, ch0 + cc)) = w;
-                    }
-                    fence_proxy_async();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->r);
-                }
-                rescale_state(st_s, st_m, vec);                 // overlaps MMA2
-                // Vres rows scaled by gS and -gM: MMA3's B operand
-                if (!warp_wait(&bars->d2, c & 1, abort)) break;
-                tc_fence_after();
-                {
-                    float x[kEpiCols];
-                    tmem_ld16(lane_base + C::kColD2 + c0, x);
-                    tmem_ld_wait();
-                    store_row16(b3, i, ch0, x, gs);
-                    store_row16(b3 + C::kB3M, i, ch0 + C::kChM, x, -gm);
-                    fence_proxy_async();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->v);
-                }
-            } else {
-                // ======== query-row warps: their own work waits until the
-                // token-row warps are past the critical step, then overlaps MMAs
-                if (!warp_wait(&bars->r, c & 1, abort)) break;
-                tc_fence_after();
-                {
-                    float xs[kEpiCols], xm[kEpiCols];
-                    tmem_ld16(lane_base + C::kColD1 + c0, xs);
-                    tmem_ld16(lane_base + C::kColD1 + NS + c0, xm);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < kEpiCols; ++j) oint[j] = ab * xs[j] - cb * xm[j];
-                }
-                rescale_state(st_s, st_m, vec);
+                for (int e = 0; e < 8; ++e) oint[e] = ab * xs[e] - cbq * xm[e];
+            }
+            rescale_state(st_s, st_m, vec);
+            // ---- Vres rows scaled by gS and -gM: MMA3's B operand; O_intra
+            if (!warp_wait(&bars->d2, c & 1, abort)) break;
+            tc_fence_after();
+            {
+                float x[8];
+                tmem_ld_16x2x8(lk + C::kColD2 + c0, x);
+                tmem_ld_wait();
+                uint4 w;
+                w.x = pack_bf16x2(gs * x[0], gs * x[1]);
+                w.y = pack_bf16x2(gs * x[2], gs * x[3]);
+                w.z = pack_bf16x2(gs * x[4], gs * x[5]);
+                w.w = pack_bf16x2(gs * x[6], gs * x[7]);
+                *reinterpret_cast<uint4 *>(b3 + sw128_offset(tok, chk)) = w;
+                w.x = pack_bf16x2(-gm * x[0], -gm * x[1]);
+                w.y = pack_bf16x2(-gm * x[2], -gm * x[3]);
+                w.z = pack_bf16x2(-gm * x[4], -gm * x[5]);
+                w.w = pack_bf16x2(-gm * x[6], -gm * x[7]);
+                *reinterpret_cast<uint4 *>(b3 + C::kB3M + sw128_offset(tok, chk + C::kChM)) = w;
+                fence_proxy_async();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->v);
-                if (!warp_wait(&bars->d2, c & 1, abort)) break;
-                tc_fence_after();
-                {
-                    float x[kEpiCols];
-                    tmem_ld16(lane_base + C::kColD2 + c0, x);
-                    tmem_ld_wait();
+            }
+            {
+                float x[8];
+                tmem_ld_16x2x8(lq + C::kColD2 + c0, x);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < kEpiCols; ++j) oint[j] += x[j];   // O = O_inter + O_intra
-                }
+                for (int e = 0; e < 8; ++e) oint[e] += x[e];     // O = O_inter + O_intra
             }
 
-            // ---- new state: bf16 copy for the next chunk's MMA1 (all warps)
+            // ---- new state: bf16 copy for the next chunk's MMA1
             if (!warp_wait(&bars->d3, c & 1, abort)) break;
             tc_fence_after();
             {
@@ -446,17 +452,13 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 }
             }
             // ---- outputs of this chunk (off the critical path)
-            if (q >= 2 && in_chunk) {
-                __nv_bfloat16 *dst = og + (size_t)(t0 + i) * rs;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint4 w;
-                    w.x = pack_bf16x2(oint[8 * cc + 0], oint[8 * cc + 1]);
-                    w.y = pack_bf16x2(oint[8 * cc + 2], oint[8 * cc + 3]);
-                    w.z = pack_bf16x2(oint[8 * cc + 4], oint[8 * cc + 5]);
-                    w.w = pack_bf16x2(oint[8 * cc + 6], oint[8 * cc + 7]);
-                    *reinterpret_cast<uint4 *>(dst + 8 * cc) = w;
-                }
+            if (in_chunk) {
+                uint4 w;
+                w.x = pack_bf16x2(oint[0], oint[1]);
+                w.y = pack_bf16x2(oint[2], oint[3]);
+                w.z = pack_bf16x2(oint[4], oint[5]);
+                w.w = pack_bf16x2(oint[6], oint[7]);
+                *reinterpret_cast<uint4 *>(og + (size_t)(t0 + tok) * rs) = w;
             }
         }
         if (!*abort) {
@@ -496,13 +498,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, h, t); box 64 x 1 x 64.
-bool make_map(CUtensorMap *map, const void *base, int T_total, int H, bool swizzle) {
+// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, h, t); box 64 x 1 x box_t.
+bool make_map(CUtensorMap *map, const void *base, int T_total, int H, bool swizzle,
+              int box_t = 64) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_t};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -562,7 +565,7 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
     if (p.prep_stride % 16 != 0) return cudaErrorInvalidValue;
     CUtensorMap mk, mq, mv;
     const int Tt = p.T_total > 0 ? p.T_total : 1;
-    if (!make_map(&mk, p.k, Tt, p.H, true) || !make_map(&mq, p.q, Tt, p.H, true) ||
+    if (!make_map(&mk, p.k, Tt, p.H, true, 16) || !make_map(&mq, p.q, Tt, p.H, true, 16) ||
         !make_map(&mv, p.v, Tt, p.H, true))
         return cudaErrorInvalidValue;
     const long chains = (long)p.n_seq * p.H;

@@ -42,6 +42,16 @@ struct PrepLayout {
 // ((c ^ (r%8)) * 16)), followed by the fp32 vectors.  One bulk copy of the
 // whole block into 1024-byte-aligned shared memory yields the MMA operand
 // [T; A_O T] directly.
+//
+// Row order: the 128 operand rows are interleaved in blocks of 16 so that
+// every 32-lane TMEM quadrant of the products holds 16 rows of each half:
+// T (or K) row i sits at row 32 (i / 16) + i % 16, A_O T (or Q) row i at
+// row 32 (i / 16) + 16 + i % 16.  The state pass loads its [K; Q] tiles in
+// the same order.
+__host__ __device__ constexpr int tc_row(int r) {
+    return r < kChunk ? 32 * (r >> 4) + (r & 15) : 32 * ((r - kChunk) >> 4) + 16 + (r & 15);
+}
+
 struct PrepLayoutTC {
     static constexpr size_t kOffT = 0;
     static constexpr size_t kOffAOT = 8192;
@@ -82,8 +92,7 @@ struct DecodeProblem {
 
 // Launchers (return the first CUDA error, or cudaSuccess).
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
-cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st,
-                                   bool tc_layout);
+cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);

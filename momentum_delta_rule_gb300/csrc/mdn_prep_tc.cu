@@ -21,7 +21,8 @@
 //   MMA   [T; A_O T] = [I; A_O] T                          (M=128, N=64, K=64)
 //
 // and writes the prepared block: [T; A_O T] in bf16 in the 128-byte-swizzled
-// K-major operand layout of the state pass, then the fp32 carry vectors.
+// K-major operand layout of the state pass (rows interleaved by tc_row), then
+// the fp32 carry vectors.
 // Rows and columns past the chunk end are masked (T is the identity there and
 // every vector entry is zero).
 #include <cudaTypedefs.h>
@@ -488,7 +489,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 w.y = pack2(x[cc * 8 + 2], x[cc * 8 + 3]);
                 w.z = pack2(x[cc * 8 + 4], x[cc * 8 + 5]);
                 w.w = pack2(x[cc * 8 + 6], x[cc * 8 + 7]);
-                *reinterpret_cast<uint4 *>(blk + sw128_offset(row, half * 4 + cc)) = w;
+                *reinterpret_cast<uint4 *>(blk + sw128_offset(tc_row(row), half * 4 + cc)) = w;
             }
         }
         tc_fence_before();

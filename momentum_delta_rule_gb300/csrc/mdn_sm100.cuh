@@ -185,6 +185,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
 }
 
 // 32 lanes x 16 consecutive 32-bit columns.
+// 16 lanes x 2 x 8 consecutive 32-bit columns: thread t of the warp
+// receives columns [col + 8 (t / 16), col + 8 (t / 16) + 8) of TMEM lane
+// (lane of taddr) + t % 16.
+__device__ __forceinline__ void tmem_ld_16x2x8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], 8;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
     uint32_t r[16];
     asm volatile(
