@@ -481,7 +481,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             float x[32];
             tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + kColD2 + half * 32, x);
             tmem_ld_wait();
-            unsigned char *blk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
+            // staged in shared memory (the MMA that read [I; A_O] is done),
+            // then one bulk copy writes whole lines of the prepared block
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint4 w;
@@ -489,12 +490,18 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 w.y = pack2(x[cc * 8 + 2], x[cc * 8 + 3]);
                 w.z = pack2(x[cc * 8 + 4], x[cc * 8 + 5]);
                 w.w = pack2(x[cc * 8 + 6], x[cc * 8 + 7]);
-                *reinterpret_cast<uint4 *>(blk + sw128_offset(tc_row(row), half * 4 + cc)) = w;
+                *reinterpret_cast<uint4 *>(A2 + sw128_offset(tc_row(row), half * 4 + cc)) = w;
             }
+            fence_proxy_async();
         }
         tc_fence_before();
     }
     __syncthreads();
+    if (tid == 0 && !*abort) {
+        bulk_store(p.prep + ((size_t)gc * p.H + h) * p.prep_stride + PrepLayoutTC::kOffT, A2, 16384);
+        bulk_commit_group();
+        bulk_wait_group0();
+    }
     if (warp == 2) {
         // every MMA issued by this CTA completes before TMEM is freed
         if (lane == 0) {
