@@ -358,45 +358,71 @@ def time_prefill(mdn, x_dev, w, steps, warmup, world, flush):
 
 def time_e2e(mdn, x, x_dev, steps, warmup):
     """Same metric through the public API from pinned host buffers: every
-    step copies its inputs host->device, runs, and reads o and the final
-    states back to pinned host memory."""
+    step copies its inputs host->device, runs, and copies o and the final
+    states back to pinned host memory.  Steps stream as a user would run
+    them: host->device copies, kernels and device->host copies on three
+    streams over two device buffer sets, so step i's copies overlap the
+    kernels of its neighbours.  Time = first copy in to last copy out, / K."""
     names = ["q", "k", "v", "alpha", "mu", "eta", "beta", "S0", "M0"]
     host = {n: x[n].pin_memory() for n in names if x[n] is not None}
-    dev = {n: torch.empty_like(x_dev[n]) for n in host}
     o_h = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
     S_h = torch.empty((x["n_seq"], x["H"], x["D"], x["D"])).pin_memory()
     M_h = torch.empty_like(S_h).pin_memory()
-    o = torch.empty_like(x_dev["v"])
-    S_T = torch.empty((x["n_seq"], x["H"], x["D"], x["D"]), device=o.device)
-    M_T = torch.empty_like(S_T)
+    devc = x_dev["q"].device
     need = mdn.workspace_size(x["n_seq"], x["B"] * x["T"], x["H"], x["D"], x["q"].dtype)
-    ws = torch.empty(need, dtype=torch.uint8, device=o.device)
+    bufs = []
+    for _ in range(2):
+        bufs.append({
+            "in": {n: torch.empty_like(x_dev[n]) for n in host},
+            "o": torch.empty_like(x_dev["v"]),
+            "S": torch.empty((x["n_seq"], x["H"], x["D"], x["D"]), device=devc),
+            "M": torch.empty((x["n_seq"], x["H"], x["D"], x["D"]), device=devc),
+            "ws": torch.empty(need, dtype=torch.uint8, device=devc),
+        })
     cu = x_dev["cu_seqlens"]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in (o_h, S_h, M_h))
+    s_in, s_run, s_out = (torch.cuda.Stream(devc) for _ in range(3))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "run", "out")}
+    for k in ev:               # every buffer starts free
+        for e in ev[k]:
+            e.record(torch.cuda.current_stream(devc))
 
-    def step():
-        for n, t in host.items():
-            dev[n].copy_(t, non_blocking=True)
-        mdn.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["alpha"], dev["mu"],
-                      dev["eta"], dev.get("beta"), dev.get("S0"), dev.get("M0"),
-                      cu_seqlens=cu, o=o, S_T=S_T, M_T=M_T, workspace=ws)
-        o_h.copy_(o, non_blocking=True)
-        S_h.copy_(S_T, non_blocking=True)
-        M_h.copy_(M_T, non_blocking=True)
+    def step(i):
+        b = bufs[i & 1]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev["run"][i & 1])        # inputs of step i-2 consumed
+            for n, t in host.items():
+                b["in"][n].copy_(t, non_blocking=True)
+            ev["in"][i & 1].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev["in"][i & 1])
+            s_run.wait_event(ev["out"][i & 1])       # outputs of step i-2 copied out
+            d = b["in"]
+            mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
+                          d.get("beta"), d.get("S0"), d.get("M0"), cu_seqlens=cu,
+                          o=b["o"], S_T=b["S"], M_T=b["M"], workspace=b["ws"],
+                          stream=s_run)
+            ev["run"][i & 1].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["run"][i & 1])
+            o_h.copy_(b["o"], non_blocking=True)
+            S_h.copy_(b["S"], non_blocking=True)
+            M_h.copy_(b["M"], non_blocking=True)
+            ev["out"][i & 1].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
-    times = []
-    for _ in range(steps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        step()
-        b.record()
-        b.synchronize()          # the result is on the host now
-        times.append(a.elapsed_time(b))
-    return statistics.mean(times), h2d, d2h
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(steps):
+        step(i)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_run)
+    t1.record(s_out)
+    t1.synchronize()             # the last result is on the host now
+    return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
 def time_decode(mdn, steps, dev, peaks):
@@ -523,7 +549,9 @@ def main():
         e_ms = max_over_ranks(e_ms, world, dev)
         line["e2e"] = {"value": world * tokens / (e_ms / 1e3), "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": e_ms}
+                       "ms_per_step": e_ms,
+                       "streams": "copies in, kernels and copies out on three streams, "
+                                  "two device buffer sets"}
     if not args.no_decode:
         line["decode"] = time_decode(mdn, args.decode_steps, dev, peaks)
     if not args.no_other_workloads:
