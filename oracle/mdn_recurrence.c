@@ -23,6 +23,9 @@
  *   S0, M0, S_T, M_T       [n_seq, H, dk, dv]  (S0/M0 may be NULL: zero)
  *   cu_seqlens  [n_seq + 1] host int32, cu_seqlens[0] = 0,
  *               sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]).
+ *   vres_out    [T_total, H, dv] or NULL: the residual of every token (the
+ *               corrected values the slides' frame "Backward computation"
+ *               says the forward saves for the gradient pass)
  * Each (sequence, head) pair is an independent chain; chains run in parallel
  * under OpenMP, tokens inside a chain strictly in order.
  */
@@ -44,12 +47,12 @@ int mdn_oracle_max_threads(void) {
 }
 
 /* Returns 0 on success, -1 on a bad argument, -2 on allocation failure. */
-int mdn_oracle_forward(const double *q, const double *k, const double *v,
-                       const double *alpha, const double *mu, const double *eta,
-                       const double *beta, const double *S0, const double *M0,
-                       double *o, double *S_T, double *M_T,
-                       const int32_t *cu_seqlens, int n_seq, int H, int dk,
-                       int dv, int n_threads) {
+int mdn_oracle_forward_vres(const double *q, const double *k, const double *v,
+                            const double *alpha, const double *mu, const double *eta,
+                            const double *beta, const double *S0, const double *M0,
+                            double *o, double *S_T, double *M_T, double *vres_out,
+                            const int32_t *cu_seqlens, int n_seq, int H, int dk,
+                            int dv, int n_threads) {
     if (!q || !k || !v || !alpha || !mu || !eta || !o || !cu_seqlens)
         return -1;
     if (n_seq < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
@@ -101,6 +104,7 @@ int mdn_oracle_forward(const double *q, const double *k, const double *v,
                 const double *Srow = S + (size_t)i * dv;
                 for (int j = 0; j < dv; ++j) vres[j] -= Srow[j] * p;
             }
+            if (vres_out) memcpy(vres_out + g * dv, vres, (size_t)dv * sizeof(double));
             /* momentum: M = mu M - eta k vres^T */
             for (int i = 0; i < dk; ++i) {
                 double *Mrow = M + (size_t)i * dv;
@@ -125,4 +129,14 @@ int mdn_oracle_forward(const double *q, const double *k, const double *v,
         free(S); free(M); free(vres);
     }
     return bad_alloc ? -2 : 0;
+}
+
+int mdn_oracle_forward(const double *q, const double *k, const double *v,
+                       const double *alpha, const double *mu, const double *eta,
+                       const double *beta, const double *S0, const double *M0,
+                       double *o, double *S_T, double *M_T,
+                       const int32_t *cu_seqlens, int n_seq, int H, int dk,
+                       int dv, int n_threads) {
+    return mdn_oracle_forward_vres(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T,
+                                   NULL, cu_seqlens, n_seq, H, dk, dv, n_threads);
 }

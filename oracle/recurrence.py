@@ -28,6 +28,9 @@ def _lib():
         lib.mdn_oracle_forward.restype = ctypes.c_int
         lib.mdn_oracle_forward.argtypes = (
             [dp] * 12 + [ctypes.POINTER(ctypes.c_int32)] + [ctypes.c_int] * 5)
+        lib.mdn_oracle_forward_vres.restype = ctypes.c_int
+        lib.mdn_oracle_forward_vres.argtypes = (
+            [dp] * 13 + [ctypes.POINTER(ctypes.c_int32)] + [ctypes.c_int] * 5)
         lib.mdn_oracle_max_threads.restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -52,12 +55,14 @@ def _ptr(a):
 
 
 def forward(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
-            cu_seqlens=None, n_threads=0):
+            cu_seqlens=None, n_threads=0, return_vres=False):
     """Run the recurrence over packed sequences.
 
     ``q, k, v`` are ``[T_total, H, d]`` (or ``[B, T, H, d]`` with
     ``cu_seqlens=None``, meaning B equal-length sequences).  Returns
     ``(o, S_T, M_T)`` as fp64 numpy arrays; ``o`` has the shape of ``v``.
+    With ``return_vres`` the residual of every token, vres_t = v_t -
+    S_{t-1}^T (alpha_t k_t), comes fourth, shaped like ``v``.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     alpha, mu, eta, beta = _f64(alpha), _f64(mu), _f64(eta), _f64(beta)
@@ -94,13 +99,16 @@ def forward(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
     o = np.zeros((T_total, H, dv), dtype=np.float64)
     S_T = np.zeros(sshape, dtype=np.float64)
     M_T = np.zeros(sshape, dtype=np.float64)
-    rc = _lib().mdn_oracle_forward(
+    vres = np.zeros((T_total, H, dv), dtype=np.float64) if return_vres else None
+    rc = _lib().mdn_oracle_forward_vres(
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(mu), _ptr(eta),
-        _ptr(beta), _ptr(S0), _ptr(M0), _ptr(o), _ptr(S_T), _ptr(M_T),
+        _ptr(beta), _ptr(S0), _ptr(M0), _ptr(o), _ptr(S_T), _ptr(M_T), _ptr(vres),
         cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
         n_seq, H, dk, dv, int(n_threads))
     if rc != 0:
         raise RuntimeError("mdn_oracle_forward failed with code %d" % rc)
+    if return_vres:
+        return o.reshape(out_shape), S_T, M_T, vres.reshape(out_shape)
     return o.reshape(out_shape), S_T, M_T
 
 

@@ -230,6 +230,44 @@ def test_deltanet_reduction():
     assert pin_deltanet_reduction(oracle_forward)
 
 
+def pin_deltanet_residual(seed=5):
+    """The per-token residual the forward can save ("Backward computation"
+    frame: save the corrected values) reduces, for mu = 0, alpha = 1,
+    eta = 1, to DeltaNet's prediction error v_t - S'_{t-1} k_t in the other
+    page's key-to-value orientation; checked against that form written out,
+    with a nonzero initial state and a state carried over a sequence split."""
+    rng = np.random.default_rng(seed)
+    x = _rand_inputs(rng, 9, 2, 3, 5, mu_zero=True, alpha_one=True, eta_one=True)
+    _, _, _, vres = recurrence.forward(x["q"], x["k"], x["v"], x["alpha"], x["mu"],
+                                       x["eta"], x["beta"], x["S0"], x["M0"],
+                                       cu_seqlens=[0, 9], return_vres=True)
+    ok = True
+    for h in range(2):
+        Sp = x["S0"][0, h].T.copy()
+        for t in range(9):
+            kt, b = x["k"][t, h], x["beta"][t, h]
+            err = x["v"][t, h] - Sp @ kt
+            ok &= np.allclose(vres[t, h], err, atol=1e-12)
+            Sp = Sp + b * np.outer(err, kt)
+    return bool(ok)
+
+
+def test_deltanet_residual():
+    assert pin_deltanet_residual()
+
+
+def test_residual_output_does_not_change_the_forward():
+    rng = np.random.default_rng(6)
+    x = _rand_inputs(rng, 11, 2, 4, 3)
+    a = oracle_forward(x)
+    b = recurrence.forward(x["q"], x["k"], x["v"], x["alpha"], x["mu"], x["eta"],
+                           x["beta"], x["S0"], x["M0"], cu_seqlens=[0, 11],
+                           return_vres=True)
+    for u, w in zip(a, b[:3]):
+        assert np.array_equal(u, w)
+    assert b[3].shape == x["v"].shape
+
+
 def test_two_step_worked_example_golden():
     rows = [l.split() for l in open(os.path.join(GOLDEN, "two_step_weight.txt"))
             if l.strip() and not l.startswith("#")]
