@@ -124,6 +124,28 @@ mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
                          int H, int dk, int dv, mdn_dtype dtype, int chunk,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * mdn_chunk_fwd_vres — mdn_chunk_fwd that also writes every token's residual
+ *   vres_t = v_t - S_{t-1}^T (alpha_t k_t)
+ * (the corrected values of Eq. (3)), which the slides' frame "Backward
+ * computation" (Sec. 3.1, Algorithm 1) has the forward save so that a
+ * gradient pass can rebuild the states without storing every (S, M) pair;
+ * reading notes section 2.6 ends with the same trade.
+ *
+ * Arguments as mdn_chunk_fwd, plus
+ *   vres   output laid out like v ([B, T, H, dv], or packed), in dtype,
+ *          16-byte aligned; required when B * T > 0; must not be q, k, v or o.
+ * Errors: as mdn_chunk_fwd; MDN_ERR_INVALID_ARG for a missing or aliasing
+ * vres.  o, S_T and M_T are the same values mdn_chunk_fwd writes.
+ */
+mdn_status mdn_chunk_fwd_vres(const void *q, const void *k, const void *v,
+                              const float *alpha, const float *mu, const float *eta,
+                              const float *beta, const float *S0, const float *M0,
+                              void *o, float *S_T, float *M_T, void *vres,
+                              const int32_t *cu_seqlens, int n_seq, int B, int T,
+                              int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
 /* Implementation paths of mdn_chunk_fwd (reported by the profiled variant). */
 typedef enum mdn_path {
     MDN_PATH_CUDA_CORE = 0,   /* fp32 FFMA kernels: fp32 inputs, head size 64 */

@@ -10,6 +10,7 @@ other code path.  If the library is missing, every call raises.
 Entry points (same names as the C ABI):
   chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
             cu_seqlens=None, ...)               -> (o, S_T, M_T)
+            (return_vres=True: (o, S_T, M_T, vres) via mdn_chunk_fwd_vres)
   decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None) -> o
   workspace_size(n_seq, T_total, H, D, dtype)
   device_status(stream=None), abi_version(), status_string(code)
@@ -38,6 +39,7 @@ CHUNK = 64
 EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_workspace_size", "mdn_chunk_fwd",
                     "mdn_chunk_fwd_profiled", "mdn_chunk_fwd_static_ws",
+                    "mdn_chunk_fwd_vres",
                     "mdn_decode_step", "mdn_get_device_status"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
@@ -76,6 +78,9 @@ def lib():
     L.mdn_chunk_fwd_profiled.argtypes = (L.mdn_chunk_fwd.argtypes
                                          + [ctypes.POINTER(ctypes.c_void_p), c_int,
                                             ctypes.POINTER(ctypes.c_int)])
+    L.mdn_chunk_fwd_vres.restype = c_int
+    L.mdn_chunk_fwd_vres.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, vp, ip]
+                                     + [c_int] * 8 + [vp, c_size, vp])
     L.mdn_chunk_fwd_static_ws.restype = c_int
     L.mdn_chunk_fwd_static_ws.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, ip]
                                           + [c_int] * 8 + [vp])
@@ -136,14 +141,15 @@ def workspace_size(n_seq, T_total, H, D, dtype):
 def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
               cu_seqlens=None, o=None, S_T=None, M_T=None,
               output_final_state=True, workspace=None, stream=None,
-              stage_events=None, info=None):
+              stage_events=None, info=None, return_vres=False, vres=None):
     """Prefill over whole sequences (``mdn_chunk_fwd``).
 
     q, k ``[B, T, H, D]`` and v ``[B, T, H, D]`` (fp32 or bf16, same dtype);
     gates ``[B, T, H]`` fp32; S0/M0 ``[n_seq, H, D, D]`` fp32 or None;
     ``cu_seqlens`` int32 CUDA tensor ``[n_seq + 1]`` for packed sequences
     (then B == 1).  Returns ``(o, S_T, M_T)``; the states are None when
-    ``output_final_state`` is False.
+    ``output_final_state`` is False.  With ``return_vres`` (or a ``vres``
+    buffer shaped like v) the per-token residuals come fourth.
     """
     L = lib()
     if q.dim() != 4:
@@ -180,6 +186,15 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
             M_T = torch.empty((n_seq, H, D, D), dtype=torch.float32, device=dev)
     _check_cuda("S_T", S_T, torch.float32, dev)
     _check_cuda("M_T", M_T, torch.float32, dev)
+    want_vres = return_vres or vres is not None
+    if want_vres:
+        if stage_events is not None or info is not None:
+            raise ValueError("stage_events/info are not available with the residual output")
+        if vres is None:
+            vres = torch.empty_like(v)
+        _check_cuda("vres", vres, q.dtype, dev)
+        if tuple(vres.shape) != (B, T, H, D):
+            raise ValueError("vres must have the shape of v")
     need = int(L.mdn_chunk_fwd_workspace_size(n_seq, B * T, H, D, D, code))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -189,6 +204,11 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
             _ptr(cu_seqlens), n_seq, B, T, H, D, D, code, CHUNK,
             _ptr(workspace), workspace.numel(), _stream_handle(dev, stream))
     with torch.cuda.device(dev):
+        if want_vres:
+            st = L.mdn_chunk_fwd_vres(*(args[:12] + (_ptr(vres),) + args[12:]))
+            if st != MDN_OK:
+                raise MdnError(st, "mdn_chunk_fwd_vres")
+            return o, S_T, M_T, vres
         if stage_events is None and info is None:
             st = L.mdn_chunk_fwd(*args)
         else:

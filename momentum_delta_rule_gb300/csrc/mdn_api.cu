@@ -95,10 +95,16 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
     return round256(meta_bytes(n_seq) + prep);
 }
 
-mdn_status mdn_chunk_fwd_profiled(
+}  // extern "C"
+
+namespace {
+
+// Every chunk-forward entry point: validation, workspace carve-up, path
+// choice and the launches.  vres (nullable) receives the per-token residuals.
+mdn_status chunk_fwd_impl(
     const void *q, const void *k, const void *v, const float *alpha,
     const float *mu, const float *eta, const float *beta, const float *S0,
-    const float *M0, void *o, float *S_T, float *M_T,
+    const float *M0, void *o, float *S_T, float *M_T, void *vres,
     const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
     mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
     void *stream, void *const *stage_events, int n_stage_events,
@@ -124,7 +130,7 @@ mdn_status mdn_chunk_fwd_profiled(
     // ---- pointers
     if (!alpha || !mu || !eta) return MDN_ERR_INVALID_ARG;
     if (T_total > 0 && (!q || !k || !v || !o)) return MDN_ERR_INVALID_ARG;
-    const void *ptrs16[] = {q, k, v, o, S0, M0, S_T, M_T};
+    const void *ptrs16[] = {q, k, v, o, S0, M0, S_T, M_T, vres};
     for (const void *ptr : ptrs16)
         if (ptr && !aligned16(ptr)) return MDN_ERR_INVALID_ARG;
     const void *ptrs4[] = {alpha, mu, eta, beta, cu_seqlens};
@@ -149,7 +155,7 @@ mdn_status mdn_chunk_fwd_profiled(
     memset(&p, 0, sizeof(p));
     p.q = q; p.k = k; p.v = v;
     p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
-    p.S0 = S0; p.M0 = M0; p.o = o; p.S_T = S_T; p.M_T = M_T;
+    p.S0 = S0; p.M0 = M0; p.o = o; p.S_T = S_T; p.M_T = M_T; p.vres = vres;
     p.cu_seqlens = cu_seqlens;
     p.n_seq = n_seq; p.B = B; p.T = T; p.H = H; p.D = dk;
     p.T_total = (int)T_total;
@@ -195,6 +201,23 @@ mdn_status mdn_chunk_fwd_profiled(
     return MDN_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+mdn_status mdn_chunk_fwd_profiled(
+    const void *q, const void *k, const void *v, const float *alpha,
+    const float *mu, const float *eta, const float *beta, const float *S0,
+    const float *M0, void *o, float *S_T, float *M_T,
+    const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
+    mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
+    void *stream, void *const *stage_events, int n_stage_events,
+    int *path_out) {
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr,
+                          cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
+                          workspace_bytes, stream, stage_events, n_stage_events, path_out);
+}
+
 mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *alpha, const float *mu, const float *eta,
                          const float *beta, const float *S0, const float *M0,
@@ -202,10 +225,23 @@ mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
                          const int32_t *cu_seqlens, int n_seq, int B, int T,
                          int H, int dk, int dv, mdn_dtype dtype, int chunk,
                          void *workspace, size_t workspace_bytes, void *stream) {
-    return mdn_chunk_fwd_profiled(q, k, v, alpha, mu, eta, beta, S0, M0, o,
-                                  S_T, M_T, cu_seqlens, n_seq, B, T, H, dk, dv,
-                                  dtype, chunk, workspace, workspace_bytes,
-                                  stream, nullptr, 0, nullptr);
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr,
+                          cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
+                          workspace_bytes, stream, nullptr, 0, nullptr);
+}
+
+mdn_status mdn_chunk_fwd_vres(const void *q, const void *k, const void *v,
+                              const float *alpha, const float *mu, const float *eta,
+                              const float *beta, const float *S0, const float *M0,
+                              void *o, float *S_T, float *M_T, void *vres,
+                              const int32_t *cu_seqlens, int n_seq, int B, int T,
+                              int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    if ((long)B * T > 0 && !vres) return MDN_ERR_INVALID_ARG;
+    if (vres && (vres == o || vres == v || vres == q || vres == k)) return MDN_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, vres,
+                          cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
+                          workspace_bytes, stream, nullptr, 0, nullptr);
 }
 
 mdn_status mdn_decode_step(const void *q, const void *k, const void *v,

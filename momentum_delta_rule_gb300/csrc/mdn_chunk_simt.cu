@@ -352,6 +352,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
     const Tin *qg0 = static_cast<const Tin *>(p.q) + (size_t)h * D;
     const Tin *vg0 = static_cast<const Tin *>(p.v) + (size_t)h * D + col0;
     Tin *og0 = static_cast<Tin *>(p.o) + (size_t)h * D + col0;
+    Tin *rg0 = p.vres ? static_cast<Tin *>(p.vres) + (size_t)h * D + col0 : nullptr;
 
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = start + c * kChunk;
@@ -419,6 +420,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
             }
             Vr[i * kNS + cc] = vr;
             if (i < n) og0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(oint[r] + oi);
+            if (rg0 && i < n) rg0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(vr);
         }
         __syncthreads();
 

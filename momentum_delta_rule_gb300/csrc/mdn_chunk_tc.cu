@@ -345,6 +345,8 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         const uint32_t lq = tmem + ((uint32_t)(32 * q + 16) << 16);   // Q / A_O T rows
         const size_t rs = (size_t)p.H * kD;
         __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + cg;
+        __nv_bfloat16 *vg = p.vres ? static_cast<__nv_bfloat16 *>(p.vres) + (size_t)h * kD + col0 + cg
+                                   : nullptr;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c & 1, use = c >> 1;
             unsigned char *stage = smem + st * kStageBytes;
@@ -418,6 +420,14 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 w.w = pack_bf16x2(-gm * x[6], -gm * x[7]);
                 *reinterpret_cast<uint4 *>(b3 + C::kB3M + sw128_offset(tok, chk + C::kChM)) = w;
                 fence_proxy_async();
+                if (vg && in_chunk) {
+                    // the residuals themselves, for a gradient pass
+                    w.x = pack_bf16x2(x[0], x[1]);
+                    w.y = pack_bf16x2(x[2], x[3]);
+                    w.z = pack_bf16x2(x[4], x[5]);
+                    w.w = pack_bf16x2(x[6], x[7]);
+                    *reinterpret_cast<uint4 *>(vg + (size_t)(t0 + tok) * rs) = w;
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->v);

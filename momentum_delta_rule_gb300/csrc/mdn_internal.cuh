@@ -68,6 +68,7 @@ struct ChunkProblem {
     const float *S0, *M0;
     void *o;
     float *S_T, *M_T;
+    void *vres;                  // per-token residuals like v, or nullptr
     const int32_t *cu_seqlens;   // device, or nullptr for equal lengths
     int n_seq, B, T, H, D;       // dk == dv == D
     int T_total;                 // B * T

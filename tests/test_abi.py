@@ -80,6 +80,32 @@ def test_chunk_fwd_rejects(L, over, code):
     assert _chunk(L, **over) == code
 
 
+def _chunk_vres(L, vres, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
+                beta=None, S0=None, M0=None, o=FAKE, S_T=None, M_T=None,
+                cu=None, n_seq=2, B=2, T=64, H=2, dk=128, dv=128, dtype=1,
+                chunk=64, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    return L.mdn_chunk_fwd_vres(args["q"], args["k"], args["v"], args["alpha"],
+                                args["mu"], args["eta"], args["beta"], args["S0"],
+                                args["M0"], args["o"], args["S_T"], args["M_T"], vres,
+                                args["cu"], args["n_seq"], args["B"], args["T"],
+                                args["H"], args["dk"], args["dv"], args["dtype"],
+                                args["chunk"], args["ws"], args["ws_bytes"],
+                                args["stream"])
+
+
+@pytest.mark.parametrize("vres,over,code", [
+    (None, {}, 1),                                   # required when tokens exist
+    (FAKE, {}, 1),                                   # aliases o (and q, k, v)
+    (ctypes.c_void_p(0x30008), {}, 1),               # not 16-byte aligned
+    (ctypes.c_void_p(0x30000), dict(chunk=32), 2),   # the rest as mdn_chunk_fwd
+    (ctypes.c_void_p(0x30000), dict(q=None), 1),
+])
+def test_chunk_fwd_vres_rejects(L, vres, over, code):
+    assert _chunk_vres(L, vres, **over) == code
+
+
 def _decode(L, **over):
     args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
                 beta=None, S=FAKE, M=ctypes.c_void_p(0x20000), o=FAKE, N=4,
