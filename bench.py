@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--decode-steps", type=int, default=W.DECODE.decode_steps)
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-vres", action="store_true",
+                   help="skip timing the forward that also writes the residuals")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-other-workloads", action="store_true",
                    help="skip timing the other prefill workloads")
@@ -356,6 +358,35 @@ def time_prefill(mdn, x_dev, w, steps, warmup, world, flush):
             "launches_per_step": 2 + (1 if x_dev["cu_seqlens"] is not None else 0)}
 
 
+def time_vres(mdn, x_dev, steps, warmup, flush):
+    """The forward that also writes every token's residual (mdn_chunk_fwd_vres),
+    same inputs, L2 flushed before each step: ms per step."""
+    dev = x_dev["q"].device
+    vres = torch.empty_like(x_dev["v"])
+    o = torch.empty_like(x_dev["v"])
+
+    def step():
+        mdn.chunk_fwd(x_dev["q"], x_dev["k"], x_dev["v"], x_dev["alpha"], x_dev["mu"],
+                      x_dev["eta"], x_dev["beta"], x_dev["S0"], x_dev["M0"],
+                      cu_seqlens=x_dev["cu_seqlens"], o=o, vres=vres)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        step()
+        b.record(cur)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ts), vres.numel() * vres.element_size()
+
+
 def time_e2e(mdn, x, x_dev, steps, warmup):
     """Same metric through the public API from pinned host buffers: every
     step copies its inputs host->device, runs, and copies o and the final
@@ -544,6 +575,13 @@ def main():
             "path": "tensor_core" if tensor else "cuda_core",
             "roofline": roofline, "stages": stages, "clocks": clk, "peaks": peak_src}
 
+    if not args.no_vres and tensor:
+        v_ms, v_bytes = time_vres(mdn, x_dev, max(3, min(args.steps, 10)), 2, flush)
+        line["vres"] = {"what": "forward that also writes every token's residual "
+                                "(mdn_chunk_fwd_vres)",
+                        "ms_per_step": v_ms, "tokens_per_s": tokens / (v_ms / 1e3),
+                        "extra_bytes_written": v_bytes,
+                        "overhead_vs_forward": v_ms / ms_per_step - 1.0}
     if not args.no_e2e:
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
         e_ms = max_over_ranks(e_ms, world, dev)
