@@ -210,6 +210,37 @@ mdn_status mdn_chunk_fwd_static_ws(const void *q, const void *k, const void *v,
                                    mdn_dtype dtype, int chunk, void *stream);
 
 /*
+ * mdn_prepare_inputs — the inputs of one MDN layer in one pass: the four gates
+ * from their per-head scalar projections z = W x_t, and the L2-normalised
+ * queries and keys with the Comba output correction.
+ *
+ * Defined by: slides, frame "Coupled gates restrict the spectral region"
+ * (Sec. 3.3) and reading notes section 2.8 for the gates,
+ *   eta   = 1 + tanh(z_eta / tau)                           in (0, 2)
+ *   alpha = alpha_max exp(f(z_alpha)),   alpha_max = cos^2(arctan(s eta))
+ *   beta  = sigmoid(z_beta) beta_max,    beta_max  = sin^2(arctan(s eta))
+ *   mu    = exp(max(f(z_mu), log_mu_min)),   f(z) = -a softplus(z + b)
+ * (so alpha + beta <= 1; the reported experiments use log_mu_min = -2), and
+ * reading notes section 2.9 for q_hat = (q - comba_d k) / |q - comba_d k|,
+ * k_hat = k / |k| per (token, head); a row of norm zero is written as zeros.
+ *
+ * Layout: q_in, k_in, q_out, k_out [n_tokens, H, d] in dtype (d = 64 or 128),
+ *   16-byte aligned; z_* and the gate outputs [n_tokens, H] fp32, the layout
+ *   mdn_chunk_fwd and mdn_decode_step take.
+ * Ownership: all buffers are the caller's device memory.  q_out may be q_in
+ *   and k_out may be k_in (in place); no other overlap.
+ * Errors: MDN_ERR_INVALID_ARG for a missing or misaligned pointer, a negative
+ *   size, a <= 0 or tau <= 0; MDN_ERR_UNSUPPORTED for d not in {64, 128};
+ *   MDN_ERR_CUDA for a launch failure.  Asynchronous on `stream`.
+ */
+mdn_status mdn_prepare_inputs(const void *q_in, const void *k_in, const float *z_alpha,
+                              const float *z_beta, const float *z_mu, const float *z_eta,
+                              void *q_out, void *k_out, float *alpha, float *beta,
+                              float *mu, float *eta, int n_tokens, int H, int d,
+                              mdn_dtype dtype, float a, float b, float s, float tau,
+                              float log_mu_min, float comba_d, void *stream);
+
+/*
  * mdn_decode_step — one recurrent step for N sequences (one token each),
  * updating both states in place.
  *

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
             cu_seqlens=None, ...)               -> (o, S_T, M_T)
             (return_vres=True: (o, S_T, M_T, vres) via mdn_chunk_fwd_vres)
   decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None) -> o
+  prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
+                 log_mu_min=-2.0, comba_d=0.0) -> (q_hat, k_hat, alpha, beta, mu, eta)
   workspace_size(n_seq, T_total, H, D, dtype)
   device_status(stream=None), abi_version(), status_string(code)
 """
@@ -20,7 +22,7 @@ import os
 
 import torch
 
-__all__ = ["chunk_fwd", "decode_step", "workspace_size", "device_status",
+__all__ = ["chunk_fwd", "decode_step", "prepare_inputs", "workspace_size", "device_status",
            "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
 
@@ -39,7 +41,7 @@ CHUNK = 64
 EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_workspace_size", "mdn_chunk_fwd",
                     "mdn_chunk_fwd_profiled", "mdn_chunk_fwd_static_ws",
-                    "mdn_chunk_fwd_vres",
+                    "mdn_chunk_fwd_vres", "mdn_prepare_inputs",
                     "mdn_decode_step", "mdn_get_device_status"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
@@ -86,6 +88,10 @@ def lib():
                                           + [c_int] * 8 + [vp])
     L.mdn_decode_step.restype = c_int
     L.mdn_decode_step.argtypes = [vp] * 3 + [fp] * 6 + [vp] + [c_int] * 5 + [vp]
+    L.mdn_prepare_inputs.restype = c_int
+    c_float = ctypes.c_float
+    L.mdn_prepare_inputs.argtypes = ([vp] * 2 + [fp] * 4 + [vp] * 2 + [fp] * 4
+                                     + [c_int] * 4 + [c_float] * 6 + [vp])
     L.mdn_get_device_status.restype = c_int
     L.mdn_get_device_status.argtypes = [vp]
     _LIB = L
@@ -262,6 +268,45 @@ def decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None, stream=None):
     if st != MDN_OK:
         raise MdnError(st, "mdn_decode_step")
     return o
+
+
+def prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
+                   log_mu_min=-2.0, comba_d=0.0, q_out=None, k_out=None, stream=None):
+    """Gates from their projections and normalised q, k (``mdn_prepare_inputs``).
+
+    q, k ``[..., H, d]`` (fp32 or bf16, same dtype; the leading dims are the
+    tokens); z_* ``[..., H]`` fp32.  Returns ``(q_hat, k_hat, alpha, beta, mu,
+    eta)``; q_out / k_out may be q / k for in-place normalisation.
+    """
+    L = lib()
+    if q.dim() < 2:
+        raise ValueError("q must be [..., H, d]")
+    H, D = q.shape[-2], q.shape[-1]
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    _check_cuda("q", q, q.dtype, dev)
+    _check_cuda("k", k, q.dtype, dev)
+    if k.shape != q.shape:
+        raise ValueError("k must have the shape of q")
+    n_tokens = q.numel() // (H * D)
+    for name, t in (("z_alpha", z_alpha), ("z_beta", z_beta), ("z_mu", z_mu), ("z_eta", z_eta)):
+        _check_cuda(name, t, torch.float32, dev)
+        if tuple(t.shape) != tuple(q.shape[:-1]):
+            raise ValueError("%s must be shaped like q without its last dimension" % name)
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    k_out = torch.empty_like(k) if k_out is None else k_out
+    _check_cuda("q_out", q_out, q.dtype, dev)
+    _check_cuda("k_out", k_out, q.dtype, dev)
+    gates = [torch.empty(q.shape[:-1], dtype=torch.float32, device=dev) for _ in range(4)]
+    with torch.cuda.device(dev):
+        st = L.mdn_prepare_inputs(_ptr(q), _ptr(k), _ptr(z_alpha), _ptr(z_beta), _ptr(z_mu),
+                                  _ptr(z_eta), _ptr(q_out), _ptr(k_out), *[_ptr(g) for g in gates],
+                                  n_tokens, H, D, code, float(a), float(b), float(s),
+                                  float(tau), float(log_mu_min), float(comba_d),
+                                  _stream_handle(dev, stream))
+    if st != MDN_OK:
+        raise MdnError(st, "mdn_prepare_inputs")
+    return (q_out, k_out) + tuple(gates)
 
 
 def device_status(stream=None, device=None):

@@ -244,6 +244,49 @@ mdn_status mdn_chunk_fwd_vres(const void *q, const void *k, const void *v,
                           workspace_bytes, stream, nullptr, 0, nullptr);
 }
 
+mdn_status mdn_prepare_inputs(const void *q_in, const void *k_in, const float *z_alpha,
+                              const float *z_beta, const float *z_mu, const float *z_eta,
+                              void *q_out, void *k_out, float *alpha, float *beta,
+                              float *mu, float *eta, int n_tokens, int H, int d,
+                              mdn_dtype dtype, float a, float b, float s, float tau,
+                              float log_mu_min, float comba_d, void *stream) {
+    if (n_tokens < 0 || H <= 0) return MDN_ERR_INVALID_ARG;
+    if (dtype != MDN_F32 && dtype != MDN_BF16) return MDN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return MDN_ERR_UNSUPPORTED;
+    if (!(a > 0.f) || !(tau > 0.f)) return MDN_ERR_INVALID_ARG;   // also rejects NaN
+    const long rows = (long)n_tokens * H;
+    if (rows > 0) {
+        const void *need[] = {q_in, k_in, z_alpha, z_beta, z_mu, z_eta, q_out, k_out,
+                              alpha, beta, mu, eta};
+        for (const void *ptr : need)
+            if (!ptr) return MDN_ERR_INVALID_ARG;
+    }
+    const void *ptrs16[] = {q_in, k_in, q_out, k_out};
+    for (const void *ptr : ptrs16)
+        if (ptr && !aligned16(ptr)) return MDN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {z_alpha, z_beta, z_mu, z_eta, alpha, beta, mu, eta};
+    for (const void *ptr : ptrs4)
+        if (ptr && ((uintptr_t)ptr & 3u)) return MDN_ERR_INVALID_ARG;
+    if (q_out && q_out == k_out) return MDN_ERR_INVALID_ARG;
+    if ((q_out && q_out == k_in) || (k_out && k_out == q_in)) return MDN_ERR_INVALID_ARG;
+    int *status = nullptr;
+    mdn_status st = current_device(&status);
+    if (st != MDN_OK) return st;
+    if (rows == 0) return MDN_OK;
+    mdn::InputsProblem p;
+    p.q_in = q_in; p.k_in = k_in;
+    p.z_alpha = z_alpha; p.z_beta = z_beta; p.z_mu = z_mu; p.z_eta = z_eta;
+    p.q_out = q_out; p.k_out = k_out;
+    p.alpha = alpha; p.beta = beta; p.mu = mu; p.eta = eta;
+    p.rows = rows; p.D = d; p.dtype = dtype;
+    p.a = a; p.b = b; p.s = s; p.tau = tau; p.log_mu_min = log_mu_min; p.comba_d = comba_d;
+    if (mdn::launch_prepare_inputs(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    return MDN_OK;
+}
+
 mdn_status mdn_decode_step(const void *q, const void *k, const void *v,
                            const float *alpha, const float *mu,
                            const float *eta, const float *beta, float *S,

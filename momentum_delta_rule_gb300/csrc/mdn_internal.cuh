@@ -92,6 +92,18 @@ struct DecodeProblem {
 };
 
 // Launchers (return the first CUDA error, or cudaSuccess).
+struct InputsProblem {
+    const void *q_in, *k_in;
+    const float *z_alpha, *z_beta, *z_mu, *z_eta;
+    void *q_out, *k_out;
+    float *alpha, *beta, *mu, *eta;
+    long rows;                   // tokens x heads
+    int D;
+    mdn_dtype dtype;
+    float a, b, s, tau, log_mu_min, comba_d;
+};
+
+cudaError_t launch_prepare_inputs(const InputsProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);

@@ -106,6 +106,30 @@ def test_chunk_fwd_vres_rejects(L, vres, over, code):
     assert _chunk_vres(L, vres, **over) == code
 
 
+def _prep(L, **over):
+    args = dict(q=FAKE, k=ctypes.c_void_p(0x20000), za=FAKE, zb=FAKE, zm=FAKE, ze=FAKE,
+                qo=ctypes.c_void_p(0x30000), ko=ctypes.c_void_p(0x40000), al=FAKE, be=FAKE,
+                mu=FAKE, eta=FAKE, n=16, H=2, d=128, dtype=1, a=1.0, b=0.0, s=1.0,
+                tau=1.0, lmin=-2.0, cd=0.0, stream=None)
+    args.update(over)
+    return L.mdn_prepare_inputs(args["q"], args["k"], args["za"], args["zb"], args["zm"],
+                                args["ze"], args["qo"], args["ko"], args["al"], args["be"],
+                                args["mu"], args["eta"], args["n"], args["H"], args["d"],
+                                args["dtype"], args["a"], args["b"], args["s"], args["tau"],
+                                args["lmin"], args["cd"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(za=None), 1), (dict(eta=None), 1), (dict(n=-1), 1),
+    (dict(H=0), 1), (dict(dtype=7), 1), (dict(a=0.0), 1), (dict(a=float("nan")), 1),
+    (dict(tau=0.0), 1), (dict(qo=ctypes.c_void_p(0x30004)), 1),
+    (dict(al=ctypes.c_void_p(0x10002)), 1), (dict(ko=ctypes.c_void_p(0x30000)), 1),
+    (dict(qo=ctypes.c_void_p(0x20000)), 1), (dict(d=96), 2),
+])
+def test_prepare_inputs_rejects(L, over, code):
+    assert _prep(L, **over) == code
+
+
 def _decode(L, **over):
     args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
                 beta=None, S=FAKE, M=ctypes.c_void_p(0x20000), o=FAKE, N=4,
