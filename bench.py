@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-vres", action="store_true",
                    help="skip timing the forward that also writes the residuals")
+    p.add_argument("--no-inputs", action="store_true",
+                   help="skip timing the gate / query-key preparation kernel")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-other-workloads", action="store_true",
                    help="skip timing the other prefill workloads")
@@ -387,6 +389,42 @@ def time_vres(mdn, x_dev, steps, warmup, flush):
     return statistics.mean(a.elapsed_time(b) for a, b in ts), vres.numel() * vres.element_size()
 
 
+GATE_PARAMS = dict(a=1.0, b=0.0, s=1.0, tau=8.0, log_mu_min=-2.0, comba_d=0.0)
+
+
+def time_inputs(mdn, x_dev, steps, warmup, flush, peaks):
+    """mdn_prepare_inputs on the workload's q, k with synthetic projections
+    z ~ N(0, 1): ms per call and its HBM roofline (reads q, k and four
+    projections, writes q_hat, k_hat and four gates)."""
+    q, k = x_dev["q"], x_dev["k"]
+    g = torch.Generator(device=q.device).manual_seed(7)
+    z = [torch.randn(q.shape[:-1], generator=g, device=q.device) for _ in range(4)]
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    for _ in range(warmup):
+        flush.zero_()
+        mdn.prepare_inputs(q, k, *z, q_out=qo, k_out=ko, **GATE_PARAMS)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(q.device)
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        mdn.prepare_inputs(q, k, *z, q_out=qo, k_out=ko, **GATE_PARAMS)
+        b.record(cur)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    rows = q.numel() // q.shape[-1]
+    nbytes = 4 * q.numel() * q.element_size() + rows * 8 * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"what": "gates from their projections + L2-normalised q, k (mdn_prepare_inputs)",
+            "ms_per_call": ms, "rows": rows,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "algorithmic_bytes": nbytes}}
+
+
 def time_e2e(mdn, x, x_dev, steps, warmup):
     """Same metric through the public API from pinned host buffers: every
     step copies its inputs host->device, runs, and copies o and the final
@@ -582,6 +620,8 @@ def main():
                         "ms_per_step": v_ms, "tokens_per_s": tokens / (v_ms / 1e3),
                         "extra_bytes_written": v_bytes,
                         "overhead_vs_forward": v_ms / ms_per_step - 1.0}
+    if not args.no_inputs:
+        line["inputs"] = time_inputs(mdn, x_dev, max(3, min(args.steps, 10)), 2, flush, peaks)
     if not args.no_e2e:
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
         e_ms = max_over_ranks(e_ms, world, dev)
