@@ -10,21 +10,24 @@
 // reading notes 2.3-2.6):
 //
 //   A_i = sum_{r<=i} log alpha_r, U_i = sum_{r<=i, mu_r>0} log mu_r,
-//   Z_i = #{r <= i : mu_r = 0}            (warp-shuffle prefix scans)
-//   gamma_{j,j} = beta_j,  gamma_{i,j} = alpha_i gamma_{i-1,j}
-//                 + beta_i [Z_i = Z_j] exp(U_i - U_j)       (column recurrence)
-//   b_i = sum_{r<=i} beta_r [Z_r = 0] exp(A_i - A_r + U_r)
-//   MMA   G = [K; Q] K^T                                   (M=128, N=64, K=128)
-//   L_{i,j}   = alpha_i G_K[i,j] eta_j gamma_{i-1,j}   (j < i, the shifted Gamma)
-//   A_O[i,j]  = G_Q[i,j] eta_j gamma_{i,j}             (j <= i)
-//   T = (I + L)^{-1}                     (forward substitution, fp32)
-//   MMA   [T; A_O T] = [I; A_O] T                          (M=128, N=64, K=64)
+//   Z_i = #{r <= i : mu_r = 0}                       (warp-shuffle prefix scans)
+//   Gt = Gamma Diag(eta) by the column recurrence
+//       m_{j,j} = eta_j,           m_{i,j} = mu_i m_{i-1,j}  (= eta_j prod_{u=j+1}^{i} mu_u)
+//       Gt_{j,j} = beta_j eta_j,   Gt_{i,j} = alpha_i Gt_{i-1,j} + beta_i m_{i,j}
+//     in four row segments of 16 run side by side and joined exactly (the
+//     recurrence is affine); it needs no exponential per entry and no
+//     difference of prefix sums, so mu = 0 is exact
+//   b_i = alpha_i b_{i-1} + beta_i [Z_i = 0] exp(U_i)  (affine prefix scan)
+//   MMA   G = [K; Q] K^T                                 (M=128, N=64, K=128)
+//   L_{i,j}   = alpha_i G_K[i,j] Gt_{i-1,j}     (j < i: the row-shifted Gamma)
+//   A_O[i,j]  = G_Q[i,j] Gt_{i,j}               (j <= i)
+//   T = (I + L)^{-1}                   (blocked forward substitution, fp32)
+//   MMA   A_O T                                          (M=128, N=64, K=64)
 //
-// and writes the prepared block: [T; A_O T] in bf16 in the 128-byte-swizzled
+// and writes the prepared block: T and A_O T in bf16 in the 128-byte-swizzled
 // K-major operand layout of the state pass (rows interleaved by tc_row), then
-// the fp32 carry vectors.
-// Rows and columns past the chunk end are masked (T is the identity there and
-// every vector entry is zero).
+// the fp32 carry vectors.  Rows and columns past the chunk end are masked (T
+// is the identity there and every vector entry is zero).
 #include <cudaTypedefs.h>
 
 #include "mdn_internal.cuh"
@@ -39,29 +42,36 @@ constexpr int kD = 128;
 constexpr int kThreadsP = 256;
 constexpr int LM = kChunk + 1;                 // padded fp32 row stride
 
-// shared memory (bytes from the 1024-aligned base), 55 KiB so that four CTAs
-// share an SM.  Regions are reused once their last reader is done:
+// shared memory (bytes from the 1024-aligned base), under 56 KiB so that four
+// CTAs share an SM.  Regions are reused once their last reader is done:
 //   [0, 32768)       K/Q tiles (TMA), read by the Gram MMA only; then
-//   [0, 16640)       Gamma fp32 [64][65], later T fp32 [64][65]
-//   [17408, 34048)   L fp32 [64][65]; after the inverse, bf16(T) (8 KiB)
-//   [34048, 38272)   the per-token vectors (2 KiB); after L is built, the
-//                    inverse's 32 x 33 fp32 scratch
-//   [38912, 55296)   [I; A_O] bf16, K-major A operand
+//   [0, 16640)       L fp32 [64][65]; after the inverse, bf16(T) as the
+//                    MMA's B operand (8 KiB)
+//   [16640, 20864)   the inverse's 32 x 33 fp32 scratch
+//   [24576, 32768)   A_O bf16, K-major A operand (rows 0..63; the MMA's rows
+//                    64..127 read the next region and are never used)
+//   [32768, 49408)   Gt fp32 [64][65], computed while the copy and the Gram
+//                    MMA are in flight; after L is built, T fp32 [64][65]
+//   [49408, 50432)   (alpha, beta, mu, eta) per token
+//   [50432, 52480)   per-token vectors (VecP rows of 64 fp32)
 constexpr uint32_t kOffKQ = 0;
-constexpr uint32_t kOffG = 0;
-constexpr uint32_t kOffL = 17408;
-constexpr uint32_t kOffB2 = 17408;
-constexpr uint32_t kOffVec = 34048;
-constexpr uint32_t kOffXs = 34048;
-constexpr uint32_t kOffA2 = 38912;
-constexpr uint32_t kOffBarP = kOffA2 + 16384;
+constexpr uint32_t kOffL = 0;
+constexpr uint32_t kOffB2 = 0;
+constexpr uint32_t kOffXs = 16640;
+constexpr uint32_t kOffAO = 24576;
+constexpr uint32_t kOffG = 32768;
+constexpr uint32_t kOffGate = 49408;
+constexpr uint32_t kOffVec = 50432;
+constexpr uint32_t kOffBarP = 52480;
 constexpr uint32_t kSmemP = kOffBarP + 128 + 1024;
-static_assert(kOffL + 4 * 64 * 65 <= kOffVec + 0 && kOffXs + 4 * 32 * 33 <= kOffA2, "prep layout");
+static_assert(kOffL + 4 * 64 * LM <= kOffXs && kOffXs + 4 * 32 * 33 <= kOffAO, "prep layout");
+static_assert(kOffAO + 8192 <= kOffG && kOffG + 4 * 64 * LM <= kOffGate, "prep layout");
+static_assert(kOffGate + 16 * 64 <= kOffVec && kOffVec + 8 * 4 * 64 <= kOffBarP, "prep layout");
 static_assert(kSmemP <= 57344, "four CTAs per SM");
 
 constexpr uint32_t kTmemColsP = 128;
 constexpr uint32_t kColG = 0;                  // Gram accumulator, 64 columns
-constexpr uint32_t kColD2 = 64;                // [T; A_O T] accumulator, 64 columns
+constexpr uint32_t kColD2 = 64;                // A_O T accumulator, 64 columns
 
 constexpr uint32_t kIdescGram = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescOut = idesc_bf16(128, 64, false, true);
@@ -72,7 +82,10 @@ struct BarsP {
     int abort;
 };
 
-enum { vAlpha = 0, vBeta, vEta, vA, vU, vZ, vB, vScan };
+// rows of the per-token vector block: prefix sums of log alpha / log mu,
+// zero-mu counts, alpha products from each 16-row segment start, b, and the
+// scans' exchange slot
+enum { vA = 0, vU, vZ, vF, vB, vScan };
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -103,10 +116,11 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     BarsP *bars = reinterpret_cast<BarsP *>(smem + kOffBarP);
     volatile int *abort = &bars->abort;
-    float *vec = reinterpret_cast<float *>(smem + kOffVec);    // [8][64]
-    float *G = reinterpret_cast<float *>(smem + kOffG);        // Gamma, then T
+    float4 *gate = reinterpret_cast<float4 *>(smem + kOffGate);   // (alpha, beta, mu, eta)
+    float *vec = reinterpret_cast<float *>(smem + kOffVec);
+    float *Gt = reinterpret_cast<float *>(smem + kOffG);
     float *L = reinterpret_cast<float *>(smem + kOffL);
-    unsigned char *A2 = smem + kOffA2;
+    unsigned char *AO = smem + kOffAO;
     unsigned char *B2 = smem + kOffB2;
 
     // The state pass may be scheduled as soon as every CTA of this grid has
@@ -118,7 +132,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     if (!locate_chunk(p, gc, loc)) return;
     const int n = loc.n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // gates first: their latency overlaps the setup below
+    unsigned char *pblk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
+    float *gv = reinterpret_cast<float *>(pblk + PrepLayoutTC::kOffVec);
+    // gates first: their latency overlaps the setup below (past the chunk
+    // end alpha = 1 and beta = mu = eta = 0)
     float g_a = 1.f, g_mu = 0.f, g_be = 0.f, g_et = 0.f;
     if (tid < n) {
         const size_t gi = (size_t)(loc.t0 + tid) * p.H + h;
@@ -135,8 +152,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
-        // K and Q tiles: issued before the block-wide setup, their latency
-        // gates the Gram MMA and with it Gamma
+        // K and Q tiles: their latency gates only the Gram MMA
         mbar_arrive_expect_tx(&bars->tma, 32768);
         tma_load_3d(smem + kOffKQ + 0, &map_k, &bars->tma, 0, h, loc.t0);
         tma_load_3d(smem + kOffKQ + 8192, &map_q, &bars->tma, 0, h, loc.t0);
@@ -152,11 +168,25 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 2) {
-        // ---- the Gram MMA once the K/Q tiles land
+    // ---- gates and their log-space prefix scans (warps 0, 1)
+    if (warp < 2) {
+        const int i = tid;
+        const bool zmu = (g_mu == 0.f);
+        float *xch = vec + vScan * kChunk;
+        const float A = scan64(logf(g_a), xch);
+        const float U = scan64(zmu ? 0.f : logf(g_mu), xch);
+        const float Z = scan64(zmu ? 1.f : 0.f, xch);
+        gate[i] = make_float4(g_a, g_be, g_mu, g_et);
+        vec[vA * kChunk + i] = A;
+        vec[vU * kChunk + i] = U;
+        vec[vZ * kChunk + i] = Z;
+    }
+    __syncthreads();
+
+    if (warp == 1) {
+        // ---- the Gram MMA G = [K; Q] K^T as soon as the tiles land (warp 1
+        //      has no column of segment 0's triangle)
         if (lane == 0) {
-            // Gram MMA G = [K; Q] K^T as soon as the tiles land: Gamma reuses
-            // their space
             const uint32_t kq = smem_u32(smem + kOffKQ);
             if (mbar_wait(&bars->tma, 0, abort)) {
                 tc_fence_after();
@@ -173,103 +203,72 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 mbar_wait(&bars->tma, 0, &dummy);
             }
         }
-    } else if (warp < 2) {
-        // ---- gates, log-space prefix scans, Gamma, b, carry vectors
-        const int i = tid;                 // token 0..63
-        const float a = g_a, mu = g_mu, be = g_be, et = g_et;
-        const bool zmu = (mu == 0.f);
-        float *xch = vec + vScan * kChunk;
-        const float A = scan64(logf(a), xch);
-        const float U = scan64(zmu ? 0.f : logf(mu), xch);
-        const float Z = scan64(zmu ? 1.f : 0.f, xch);
-        vec[vAlpha * kChunk + i] = a;
-        vec[vBeta * kChunk + i] = be;
-        vec[vEta * kChunk + i] = et;
-        vec[vA * kChunk + i] = A;
-        vec[vU * kChunk + i] = U;
-        vec[vZ * kChunk + i] = Z;
-        asm volatile("bar.sync 1, 64;" ::: "memory");
+        __syncwarp();
     } else {
-        // ---- identity rows of [I; A_O] while the others work (warps 3..7)
-        for (int idx = tid - 96; idx < 64 * 8; idx += kThreadsP - 96) {
-            const int r = idx >> 3, c = idx & 7;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if ((r >> 3) == c) {
-                const int e = r & 7;                       // 1.0 at column r
-                const uint32_t one = 0x3F80u;              // bf16 1.0
-                uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
-                wp[e >> 1] = (e & 1) ? (one << 16) : one;
-            }
-            *reinterpret_cast<uint4 *>(A2 + sw128_offset(r, c)) = w;
-        }
-    }
-    __syncthreads();   // gates and prefix scans are in shared memory
-
-    // ---- Gamma: gamma_{j,j} = beta_j, gamma_{r,j} = alpha_r gamma_{r-1,j} +
-    //      beta_r m_{r,j} with m_{r,j} = [Z_r = Z_j] exp(U_r - U_j), in four
-    //      row segments of 16 run side by side (thread = segment x column).
-    //      Each segment starts from zero; as the recurrence is affine,
-    //      gamma_{r,j} = local_{r,j} + (prod_{u=r0..r} alpha_u) gamma_{r0-1,j}
-    //      restores the exact values (segment ends first, in order).  Only
-    //      the lower triangle is ever read.
-    float *F = vec + vB * kChunk;      // prod of alpha from the segment start (b comes later)
-    // Gamma overwrites the K/Q tiles: the Gram MMA must have read them
-    const bool gram_ok = __all_sync(0xffffffffu, mbar_wait(&bars->gram, 0, abort));
-    if (gram_ok) {
-        tc_fence_after();
-    }
-    {
+        // ---- Gt = Gamma Diag(eta): thread = (row segment s of 16, column j);
+        //      a column that starts before the segment starts it from zero
+        //      (the alpha-carried part joins below) with m = eta_j times the
+        //      mu product over (j, r0], from the prefix sums (0 across a zero mu)
         const int j = tid & 63, r0 = 16 * (tid >> 6);
-        const float Uj = vec[vU * kChunk + j], Zj = vec[vZ * kChunk + j];
-        float gl = 0.f, pa = 1.f;
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = r0 + rr;
-            const float ar = vec[vAlpha * kChunk + r], br = vec[vBeta * kChunk + r];
-            const float ur = vec[vU * kChunk + r], zr = vec[vZ * kChunk + r];
-            pa *= ar;
-            const float m = (zr == Zj) ? __expf(ur - Uj) : 0.f;
-            const float gn = (r == j) ? br : ar * gl + br * m;
-            if (r >= j) {
-                gl = gn;
-                G[r * LM + j] = gl;
+        if (j <= r0 + 15) {
+            const float et = gate[j].w;
+            float m = et;
+            if (j < r0) {
+                const float Zj = vec[vZ * kChunk + j], Zr = vec[vZ * kChunk + r0];
+                m = (Zr == Zj) ? et * __expf(vec[vU * kChunk + r0] - vec[vU * kChunk + j]) : 0.f;
             }
-            if (j == 0) F[r] = pa;
+            const float4 g0 = gate[r0];
+            float g = g0.y * m;
+            float pa = g0.x;             // prod of alpha over [r0, r]
+            if (r0 >= j) Gt[r0 * LM + j] = g;
+            if (j == 0) vec[vF * kChunk + r0] = pa;
+#pragma unroll
+            for (int rr = 1; rr < 16; ++rr) {
+                const int r = r0 + rr;
+                const float4 gr = gate[r];
+                const bool diag = (r == j);
+                m = diag ? et : gr.z * m;
+                g = (diag ? 0.f : gr.x * g) + gr.y * m;
+                pa *= gr.x;
+                if (r >= j) Gt[r * LM + j] = g;
+                if (j == 0) vec[vF * kChunk + r] = pa;
+            }
         }
     }
     __syncthreads();
     if (tid < 64) {
-        // exact values at rows 31 and 47 (row 15 is exact already)
+        // exact values at rows 31 and 47 (row 15 is exact already):
+        // Gt_{r,j} = local_{r,j} + F_r Gt_{r0-1,j}
         const int j = tid;
-        float e = G[15 * LM + j];
+        float e = Gt[15 * LM + j];
 #pragma unroll
         for (int g = 1; g < 4; ++g) {
             const int rend = 16 * g + 15;
             if (j < 16 * g) {
-                e = G[rend * LM + j] + F[rend] * e;
-                G[rend * LM + j] = e;
+                e = Gt[rend * LM + j] + vec[vF * kChunk + rend] * e;
+                Gt[rend * LM + j] = e;
             } else if (j <= rend) {
-                e = G[rend * LM + j];
+                e = Gt[rend * LM + j];
             }
         }
     }
     __syncthreads();
-    {
+    if (warp >= 2) {
+        // the interior rows of segments 1..3 for the columns that started before
         const int j = tid & 63, r0 = 16 * (tid >> 6);
         if (j < r0) {
-            const float e = G[(r0 - 1) * LM + j];
+            const float e = Gt[(r0 - 1) * LM + j];
 #pragma unroll
             for (int rr = 0; rr < 15; ++rr) {
                 const int r = r0 + rr;
-                G[r * LM + j] += F[r] * e;
+                Gt[r * LM + j] += vec[vF * kChunk + r] * e;
             }
         }
-    }
-    __syncthreads();   // Gamma complete
-    if (warp < 2) {
+    } else {
+        // ---- b and the carry vectors that do not need Gamma (warps 0, 1)
         const int i = tid;
-        const float a = vec[vAlpha * kChunk + i], be = vec[vBeta * kChunk + i];
-        const float et = vec[vEta * kChunk + i];
+        const float4 gi = gate[i];
+        const float a = gi.x, be = gi.y, et = gi.w;
         const float A = vec[vA * kChunk + i], U = vec[vU * kChunk + i], Z = vec[vZ * kChunk + i];
         // b_i = alpha_i b_{i-1} + beta_i mubar_i as an affine prefix scan:
         // each lane holds the map x -> ca x + cb of its token; maps compose.
@@ -289,15 +288,11 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         const float bsum = (warp == 1) ? ca * vec[vScan * kChunk] + cb : cb;
         vec[vB * kChunk + i] = bsum;
         asm volatile("bar.sync 1, 64;" ::: "memory");
-        // carry vectors of the prepared block
         const int last = n - 1;
         const bool valid = i < n;
-        float *gv = reinterpret_cast<float *>(
-            p.prep + ((size_t)gc * p.H + h) * p.prep_stride + PrepLayoutTC::kOffVec);
         gv[kVecAbar * kChunk + i] = valid ? expf(A) : 0.f;
         gv[kVecBmA * kChunk + i] = (valid && i > 0) ? vec[vB * kChunk + i - 1] * a : 0.f;
         gv[kVecB * kChunk + i] = valid ? bsum : 0.f;
-        gv[kVecGS * kChunk + i] = valid ? G[last * LM + i] * et : 0.f;
         const float mtail =
             (vec[vZ * kChunk + last] == Z) ? expf(vec[vU * kChunk + last] - U) : 0.f;
         gv[kVecGM * kChunk + i] = valid ? mtail * et : 0.f;
@@ -308,10 +303,14 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         if (i == 3) sc = (float)n;
         gv[kVecScal * kChunk + i] = sc;
     }
-    __syncthreads();   // vectors ready
+    __syncthreads();   // Gt complete
 
-    // ---- Gram results -> L (fp32) and A_O (bf16 rows 64..127 of A2)
+    // ---- Gram results -> L (fp32) and A_O (bf16, K-major)
     {
+        if (warp < 2) {
+            const int i = tid;   // carry weight of S: gamma_{n,i} eta_i
+            gv[kVecGS * kChunk + i] = i < n ? Gt[(n - 1) * LM + i] : 0.f;
+        }
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->gram, 0, abort));
         const int q = warp & 3, half = warp >> 2;
         const int row = 32 * q + lane;
@@ -320,40 +319,39 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             float x[32];
             tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + kColG + half * 32, x);
             tmem_ld_wait();
-            const float *va = vec + vAlpha * kChunk;
-            const float *ve = vec + vEta * kChunk;
             if (row < 64) {
                 const int i = row;
-                const float ai = va[i];
+                const float ai = i < n ? gate[i].x : 0.f;      // rows past the chunk end: 0
+                const float *gp = Gt + max(i - 1, 0) * LM + half * 32;
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
-                    float v = 0.f;
-                    if (j < i && i < n) v = ai * x[jj] * ve[j] * G[(i - 1) * LM + j];
-                    L[i * LM + j] = v;       // padded stride: lanes hit distinct banks
+                    L[i * LM + j] = (j < i) ? ai * x[jj] * gp[jj] : 0.f;   // padded stride: distinct banks
                 }
             } else {
                 const int i = row - 64;
+                const float *gp = Gt + i * LM + half * 32;
+                const bool vi = i < n;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     float y[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int j = half * 32 + cc * 8 + e;
-                        y[e] = (j <= i && i < n) ? x[cc * 8 + e] * ve[j] * G[i * LM + j] : 0.f;
+                        y[e] = (j <= i && vi) ? x[cc * 8 + e] * gp[cc * 8 + e] : 0.f;
                     }
                     uint4 w;
                     w.x = pack2(y[0], y[1]);
                     w.y = pack2(y[2], y[3]);
                     w.z = pack2(y[4], y[5]);
                     w.w = pack2(y[6], y[7]);
-                    *reinterpret_cast<uint4 *>(A2 + sw128_offset(row, half * 4 + cc)) = w;
+                    *reinterpret_cast<uint4 *>(AO + sw128_offset(i, half * 4 + cc)) = w;
                 }
             }
         }
         tc_fence_before();
     }
-    __syncthreads();   // L ready; Gamma no longer needed
+    __syncthreads();   // L and A_O ready; Gt no longer needed
 
     // ---- T = (I + L)^{-1}, blocked:
     //   diagonal 16x16 blocks by forward substitution in registers (one lane
@@ -361,8 +359,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     //   for the 16-blocks inside each 32-block and for the two 32-blocks.
     //   The blocks above the diagonal 16-blocks are never read; bf16(T)
     //   writes zeros there.
-    float *Tm = G;
-    float *X = reinterpret_cast<float *>(smem + kOffXs);    // scratch (the vectors are consumed)
+    float *Tm = Gt;                                         // Gt is consumed
+    float *X = reinterpret_cast<float *>(smem + kOffXs);    // scratch
     constexpr int LX = 33;
     if (warp < 2) {
         const int blk = warp * 2 + (lane >> 4);
@@ -442,7 +440,9 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     }
     __syncthreads();
 
-    // ---- bf16(T) as the MN-major B operand (rows k, columns j)
+    // ---- bf16(T): the MMA's B operand (MN-major: rows k, columns j) and
+    //      the T rows of the prepared block (K-major rows at tc_row), one
+    //      16-byte chunk per store
     for (int idx = tid; idx < kChunk * 8; idx += kThreadsP) {
         const int r = idx >> 3, c = idx & 7;
         const float *src = Tm + r * LM + c * 8;
@@ -454,13 +454,14 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             w.w = pack2(src[6], src[7]);
         }
         *reinterpret_cast<uint4 *>(B2 + sw128_offset(r, c)) = w;
+        *reinterpret_cast<uint4 *>(pblk + PrepLayoutTC::kOffT + sw128_offset(tc_row(r), c)) = w;
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 2 && lane == 0 && !*abort) {
-        const uint32_t a2 = smem_u32(A2), b2 = smem_u32(B2);
+        const uint32_t a2 = smem_u32(AO), b2 = smem_u32(B2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const uint64_t a = sdesc_sw128(a2 + kk * 32, 16, 1024);
@@ -471,18 +472,17 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     }
     __syncwarp();
 
-    // ---- [T; A_O T] -> bf16 swizzled rows of the prepared block
-    {
+    // ---- A_O T (accumulator rows 0..63: lane quadrants 0, 1) -> bf16 rows
+    //      of the prepared block
+    if ((warp & 3) < 2) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->out, 0, abort));
         const int q = warp & 3, half = warp >> 2;
-        const int row = 32 * q + lane;
+        const int i = 32 * q + lane;
         if (ok) {
             tc_fence_after();
             float x[32];
             tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + kColD2 + half * 32, x);
             tmem_ld_wait();
-            // staged in shared memory (the MMA that read [I; A_O] is done),
-            // then one bulk copy writes whole lines of the prepared block
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint4 w;
@@ -490,18 +490,13 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 w.y = pack2(x[cc * 8 + 2], x[cc * 8 + 3]);
                 w.z = pack2(x[cc * 8 + 4], x[cc * 8 + 5]);
                 w.w = pack2(x[cc * 8 + 6], x[cc * 8 + 7]);
-                *reinterpret_cast<uint4 *>(A2 + sw128_offset(tc_row(row), half * 4 + cc)) = w;
+                *reinterpret_cast<uint4 *>(pblk + PrepLayoutTC::kOffT +
+                                           sw128_offset(tc_row(kChunk + i), half * 4 + cc)) = w;
             }
-            fence_proxy_async();
         }
-        tc_fence_before();
     }
+    tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !*abort) {
-        bulk_store(p.prep + ((size_t)gc * p.H + h) * p.prep_stride + PrepLayoutTC::kOffT, A2, 16384);
-        bulk_commit_group();
-        bulk_wait_group0();
-    }
     if (warp == 2) {
         // every MMA issued by this CTA completes before TMEM is freed
         if (lane == 0) {
