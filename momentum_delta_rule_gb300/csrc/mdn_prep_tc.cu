@@ -92,20 +92,33 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Inclusive prefix sum over lanes 0..63 (warps 0 and 1).  Called by those two
-// warps only; they synchronise on named barrier 1.
-__device__ __forceinline__ float scan64(float x, float *xch) {
+// Inclusive prefix sums of three values over lanes 0..63 (warps 0 and 1),
+// side by side.  Called by those two warps only; they synchronise on named
+// barrier 1.  xch: three exchange slots.
+__device__ __forceinline__ void scan64x3(float &x, float &y, float &z, float *xch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, d);
-        if (lane >= d) x += y;
+        const float px = __shfl_up_sync(0xffffffffu, x, d);
+        const float py = __shfl_up_sync(0xffffffffu, y, d);
+        const float pz = __shfl_up_sync(0xffffffffu, z, d);
+        if (lane >= d) {
+            x += px;
+            y += py;
+            z += pz;
+        }
     }
-    if (warp == 0 && lane == 31) *xch = x;
+    if (warp == 0 && lane == 31) {
+        xch[0] = x;
+        xch[1] = y;
+        xch[2] = z;
+    }
     asm volatile("bar.sync 1, 64;" ::: "memory");
-    if (warp == 1) x += *xch;
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    return x;
+    if (warp == 1) {
+        x += xch[0];
+        y += xch[1];
+        z += xch[2];
+    }
 }
 
 __global__ void __launch_bounds__(kThreadsP, 4)
@@ -172,10 +185,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     if (warp < 2) {
         const int i = tid;
         const bool zmu = (g_mu == 0.f);
-        float *xch = vec + vScan * kChunk;
-        const float A = scan64(logf(g_a), xch);
-        const float U = scan64(zmu ? 0.f : logf(g_mu), xch);
-        const float Z = scan64(zmu ? 1.f : 0.f, xch);
+        float A = logf(g_a), U = zmu ? 0.f : logf(g_mu), Z = zmu ? 1.f : 0.f;
+        scan64x3(A, U, Z, vec + vScan * kChunk);
         gate[i] = make_float4(g_a, g_be, g_mu, g_et);
         vec[vA * kChunk + i] = A;
         vec[vU * kChunk + i] = U;
@@ -184,8 +195,55 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     __syncthreads();
 
     if (warp == 1) {
-        // ---- the Gram MMA G = [K; Q] K^T as soon as the tiles land (warp 1
-        //      has no column of segment 0's triangle)
+        // ---- b_i = alpha_i b_{i-1} + beta_i mubar_i and the carry vectors
+        //      that do not need Gamma, in this warp alone (tokens 2l, 2l+1 per
+        //      lane; warp 1 has no column of segment 0's triangle): an affine
+        //      prefix scan of the maps x -> a x + c, composed pairwise first
+        const int i0 = 2 * lane, i1 = i0 + 1;
+        const float4 g0 = gate[i0], g1 = gate[i1];
+        const float A0 = vec[vA * kChunk + i0], A1 = vec[vA * kChunk + i1];
+        const float U0 = vec[vU * kChunk + i0], U1 = vec[vU * kChunk + i1];
+        const float Z0 = vec[vZ * kChunk + i0], Z1 = vec[vZ * kChunk + i1];
+        const float c0 = (Z0 == 0.f) ? g0.y * __expf(U0) : 0.f;
+        const float c1 = (Z1 == 0.f) ? g1.y * __expf(U1) : 0.f;
+        float ca = g1.x * g0.x, cb = g1.x * c0 + c1;          // the pair's map
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float pa = __shfl_up_sync(0xffffffffu, ca, d);
+            const float pb = __shfl_up_sync(0xffffffffu, cb, d);
+            if (lane >= d) {
+                cb = ca * pb + cb;
+                ca = ca * pa;
+            }
+        }
+        float bprev = __shfl_up_sync(0xffffffffu, cb, 1);     // b_{i0 - 1}
+        if (lane == 0) bprev = 0.f;
+        const float b0 = g0.x * bprev + c0, b1 = cb;
+        vec[vB * kChunk + i0] = b0;
+        vec[vB * kChunk + i1] = b1;
+        __syncwarp();
+        const int last = n - 1;
+        const float Al = vec[vA * kChunk + last], Ul = vec[vU * kChunk + last];
+        const float Zl = vec[vZ * kChunk + last], bl = vec[vB * kChunk + last];
+        const bool v0 = i0 < n, v1 = i1 < n;
+        auto put2 = [&](int row, float x0, float x1) {
+            *reinterpret_cast<float2 *>(gv + row * kChunk + i0) =
+                make_float2(v0 ? x0 : 0.f, v1 ? x1 : 0.f);
+        };
+        put2(kVecAbar, __expf(A0), __expf(A1));
+        put2(kVecBmA, bprev * g0.x, b0 * g1.x);               // b_0 = 0 before the first token
+        put2(kVecB, b0, b1);
+        put2(kVecGM, (Zl == Z0) ? __expf(Ul - U0) * g0.w : 0.f,
+             (Zl == Z1) ? __expf(Ul - U1) * g1.w : 0.f);
+        if (lane < 2) {
+            // [abar_n, b_n, mubar_n, n]
+            const float s0 = lane == 0 ? __expf(Al) : ((Zl == 0.f) ? __expf(Ul) : 0.f);
+            const float s1 = lane == 0 ? bl : (float)n;
+            *reinterpret_cast<float2 *>(gv + kVecScal * kChunk + 2 * lane) = make_float2(s0, s1);
+        } else if (lane < 32) {
+            *reinterpret_cast<float2 *>(gv + kVecScal * kChunk + 2 * lane) = make_float2(0.f, 0.f);
+        }
+        // ---- the Gram MMA G = [K; Q] K^T once the tiles have landed
         if (lane == 0) {
             const uint32_t kq = smem_u32(smem + kOffKQ);
             if (mbar_wait(&bars->tma, 0, abort)) {
@@ -264,44 +322,6 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 Gt[r * LM + j] += vec[vF * kChunk + r] * e;
             }
         }
-    } else {
-        // ---- b and the carry vectors that do not need Gamma (warps 0, 1)
-        const int i = tid;
-        const float4 gi = gate[i];
-        const float a = gi.x, be = gi.y, et = gi.w;
-        const float A = vec[vA * kChunk + i], U = vec[vU * kChunk + i], Z = vec[vZ * kChunk + i];
-        // b_i = alpha_i b_{i-1} + beta_i mubar_i as an affine prefix scan:
-        // each lane holds the map x -> ca x + cb of its token; maps compose.
-        float ca = a;
-        float cb = (Z == 0.f) ? be * __expf(U) : 0.f;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const float pa = __shfl_up_sync(0xffffffffu, ca, d);
-            const float pb = __shfl_up_sync(0xffffffffu, cb, d);
-            if ((i & 31) >= d) {
-                cb = ca * pb + cb;
-                ca = ca * pa;
-            }
-        }
-        if (warp == 0 && lane == 31) vec[vScan * kChunk] = cb;
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-        const float bsum = (warp == 1) ? ca * vec[vScan * kChunk] + cb : cb;
-        vec[vB * kChunk + i] = bsum;
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-        const int last = n - 1;
-        const bool valid = i < n;
-        gv[kVecAbar * kChunk + i] = valid ? expf(A) : 0.f;
-        gv[kVecBmA * kChunk + i] = (valid && i > 0) ? vec[vB * kChunk + i - 1] * a : 0.f;
-        gv[kVecB * kChunk + i] = valid ? bsum : 0.f;
-        const float mtail =
-            (vec[vZ * kChunk + last] == Z) ? expf(vec[vU * kChunk + last] - U) : 0.f;
-        gv[kVecGM * kChunk + i] = valid ? mtail * et : 0.f;
-        float sc = 0.f;
-        if (i == 0) sc = expf(vec[vA * kChunk + last]);
-        if (i == 1) sc = vec[vB * kChunk + last];
-        if (i == 2) sc = (vec[vZ * kChunk + last] == 0.f) ? expf(vec[vU * kChunk + last]) : 0.f;
-        if (i == 3) sc = (float)n;
-        gv[kVecScal * kChunk + i] = sc;
     }
     __syncthreads();   // Gt complete
 
