@@ -460,9 +460,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     }
     __syncthreads();
 
-    // ---- bf16(T): the MMA's B operand (MN-major: rows k, columns j) and
-    //      the T rows of the prepared block (K-major rows at tc_row), one
-    //      16-byte chunk per store
+    // ---- bf16(T) as the MMA's B operand (MN-major: rows k, columns j).  The
+    //      same bytes are the T rows of the prepared block: each group of 16
+    //      rows is one 2 KiB piece there (at prepared rows 32 g .. 32 g + 15,
+    //      same row mod 8, so the same swizzle), copied out in bulk below
     for (int idx = tid; idx < kChunk * 8; idx += kThreadsP) {
         const int r = idx >> 3, c = idx & 7;
         const float *src = Tm + r * LM + c * 8;
@@ -474,7 +475,6 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             w.w = pack2(src[6], src[7]);
         }
         *reinterpret_cast<uint4 *>(B2 + sw128_offset(r, c)) = w;
-        *reinterpret_cast<uint4 *>(pblk + PrepLayoutTC::kOffT + sw128_offset(tc_row(r), c)) = w;
     }
     fence_proxy_async();
     tc_fence_before();
@@ -489,11 +489,17 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             mma_bf16(tmem + kColD2, a, b, kIdescOut, kk != 0);
         }
         mma_commit(&bars->out);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            bulk_store(pblk + PrepLayoutTC::kOffT + g * 4096, B2 + g * 2048, 2048);
+        bulk_commit_group();
     }
     __syncwarp();
 
     // ---- A_O T (accumulator rows 0..63: lane quadrants 0, 1) -> bf16 rows
-    //      of the prepared block
+    //      staged in the A_O buffer (the MMA that read it is complete), then
+    //      copied out in bulk: rows 16 g .. 16 g + 15 to prepared rows
+    //      32 g + 16 .. 32 g + 31
     if ((warp & 3) < 2) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->out, 0, abort));
         const int q = warp & 3, half = warp >> 2;
@@ -510,16 +516,23 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 w.y = pack2(x[cc * 8 + 2], x[cc * 8 + 3]);
                 w.z = pack2(x[cc * 8 + 4], x[cc * 8 + 5]);
                 w.w = pack2(x[cc * 8 + 6], x[cc * 8 + 7]);
-                *reinterpret_cast<uint4 *>(pblk + PrepLayoutTC::kOffT +
-                                           sw128_offset(tc_row(kChunk + i), half * 4 + cc)) = w;
+                *reinterpret_cast<uint4 *>(AO + sw128_offset(i, half * 4 + cc)) = w;
             }
+            fence_proxy_async();
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
-        // every MMA issued by this CTA completes before TMEM is freed
         if (lane == 0) {
+            if (!*abort) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    bulk_store(pblk + PrepLayoutTC::kOffT + g * 4096 + 2048, AO + g * 2048, 2048);
+                bulk_commit_group();
+            }
+            bulk_wait_group0();          // shared memory stays valid until the copies are done
+            // every MMA issued by this CTA completes before TMEM is freed
             mma_commit(&bars->drain);
             int dummy = 0;
             mbar_wait(&bars->drain, 0, &dummy);
