@@ -552,6 +552,13 @@ def max_over_ranks(val, world, dev):
     return float(t.item())
 
 
+def whole_job_rate(tokens_per_rank, max_ms, steps, world):
+    """Tokens per second of the whole job: every rank processes its own
+    replica of `tokens_per_rank` tokens per step, and the slowest rank's time
+    (`max_ms` over `steps` steps) bounds the job."""
+    return world * tokens_per_rank / (max_ms / steps / 1e3)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -585,7 +592,7 @@ def main():
     max_ms = max_over_ranks(r["total_ms"], world, dev)
     tokens = sum(seq_lengths(x))
     ms_per_step = max_ms / args.steps
-    value = world * tokens / (ms_per_step / 1e3)
+    value = whole_job_rate(tokens, max_ms, args.steps, world)
 
     # dominant kernel roofline (per launch, live CUDA-event duration)
     tensor = r["path"] == 1
@@ -625,7 +632,7 @@ def main():
     if not args.no_e2e:
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
         e_ms = max_over_ranks(e_ms, world, dev)
-        line["e2e"] = {"value": world * tokens / (e_ms / 1e3), "unit": "tokens/s",
+        line["e2e"] = {"value": whole_job_rate(tokens, e_ms, 1, world), "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e_ms,
                        "streams": "copies in, kernels and copies out on three streams, "
