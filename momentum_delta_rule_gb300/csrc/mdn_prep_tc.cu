@@ -45,27 +45,33 @@ constexpr int LM = kChunk + 1;                 // padded fp32 row stride
 // shared memory (bytes from the 1024-aligned base), under 56 KiB so that four
 // CTAs share an SM.  Regions are reused once their last reader is done:
 //   [0, 32768)       K/Q tiles (TMA), read by the Gram MMA only; then
-//   [0, 16640)       L fp32 [64][65]; after the inverse, bf16(T) as the
-//                    MMA's B operand (8 KiB)
-//   [16640, 20864)   the inverse's 32 x 33 fp32 scratch
+//   [0, 8192)        L_o bf16 (off-diagonal 16-blocks of L, row-major); after
+//                    the first hop of the inverse, bf16 T (row-major)
+//   [8192, 16384)    Y bf16 (I - N, then the Horner iterates)
+//   [16384, 20736)   diagonal 16-blocks of L fp32 [4][16][17], then D in place
 //   [24576, 32768)   A_O bf16, K-major A operand (rows 0..63; the MMA's rows
 //                    64..127 read the next region and are never used)
 //   [32768, 49408)   Gt fp32 [64][65], computed while the copy and the Gram
-//                    MMA are in flight; after L is built, T fp32 [64][65]
+//                    MMA are in flight; after L is built, D bf16 [32768,
+//                    40960) and N bf16 [40960, 49152)
 //   [49408, 50432)   (alpha, beta, mu, eta) per token
 //   [50432, 52480)   per-token vectors (VecP rows of 64 fp32)
+constexpr int LB = 17;                         // padded row stride of a 16 x 16 block
 constexpr uint32_t kOffKQ = 0;
-constexpr uint32_t kOffL = 0;
+constexpr uint32_t kOffLo = 0;
 constexpr uint32_t kOffB2 = 0;
-constexpr uint32_t kOffXs = 16640;
+constexpr uint32_t kOffY = 8192;
+constexpr uint32_t kOffLd = 16384;
 constexpr uint32_t kOffAO = 24576;
 constexpr uint32_t kOffG = 32768;
+constexpr uint32_t kOffDbf = 32768;
+constexpr uint32_t kOffN = 40960;
 constexpr uint32_t kOffGate = 49408;
 constexpr uint32_t kOffVec = 50432;
 constexpr uint32_t kOffBarP = 52480;
 constexpr uint32_t kSmemP = kOffBarP + 128 + 1024;
-static_assert(kOffL + 4 * 64 * LM <= kOffXs && kOffXs + 4 * 32 * 33 <= kOffAO, "prep layout");
-static_assert(kOffAO + 8192 <= kOffG && kOffG + 4 * 64 * LM <= kOffGate, "prep layout");
+static_assert(kOffLd + 4 * 64 * LB <= kOffAO && kOffAO + 8192 <= kOffG, "prep layout");
+static_assert(kOffG + 4 * 64 * LM <= kOffGate && kOffN + 8192 <= kOffGate, "prep layout");
 static_assert(kOffGate + 16 * 64 <= kOffVec && kOffVec + 8 * 4 * 64 <= kOffBarP, "prep layout");
 static_assert(kSmemP <= 57344, "four CTAs per SM");
 
@@ -75,9 +81,10 @@ constexpr uint32_t kColD2 = 64;                // A_O T accumulator, 64 columns
 
 constexpr uint32_t kIdescGram = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescOut = idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdescHop = idesc_bf16(64, 64, false, true);   // the inverse's products
 
 struct BarsP {
-    uint64_t tma, gram, out, drain;
+    uint64_t tma, gram, hop, out, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -132,7 +139,11 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     float4 *gate = reinterpret_cast<float4 *>(smem + kOffGate);   // (alpha, beta, mu, eta)
     float *vec = reinterpret_cast<float *>(smem + kOffVec);
     float *Gt = reinterpret_cast<float *>(smem + kOffG);
-    float *L = reinterpret_cast<float *>(smem + kOffL);
+    float *Ldg = reinterpret_cast<float *>(smem + kOffLd);     // [4][16][LB]
+    unsigned char *Lo = smem + kOffLo;
+    unsigned char *Ybf = smem + kOffY;
+    unsigned char *Dbf = smem + kOffDbf;
+    unsigned char *Nbf = smem + kOffN;
     unsigned char *AO = smem + kOffAO;
     unsigned char *B2 = smem + kOffB2;
 
@@ -161,6 +172,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     if (tid == 0) {
         mbar_init(&bars->tma, 1);
         mbar_init(&bars->gram, 1);
+        mbar_init(&bars->hop, 1);
         mbar_init(&bars->out, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -325,7 +337,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     }
     __syncthreads();   // Gt complete
 
-    // ---- Gram results -> L (fp32) and A_O (bf16, K-major)
+    // ---- Gram results -> L and A_O.  L is split: its off-diagonal 16-blocks
+    //      L_o in bf16 (row-major, the B operand of N = D L_o), its diagonal
+    //      16-blocks in fp32 for the forward substitution.  A_O in bf16
+    //      (K-major A operand).
     {
         if (warp < 2) {
             const int i = tid;   // carry weight of S: gamma_{n,i} eta_i
@@ -340,13 +355,30 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + kColG + half * 32, x);
             tmem_ld_wait();
             if (row < 64) {
-                const int i = row;
+                const int i = row, bi = i >> 4;
                 const float ai = i < n ? gate[i].x : 0.f;      // rows past the chunk end: 0
                 const float *gp = Gt + max(i - 1, 0) * LM + half * 32;
+                float y[32];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
-                    L[i * LM + j] = (j < i) ? ai * x[jj] * gp[jj] : 0.f;   // padded stride: distinct banks
+                    y[jj] = (j < i) ? ai * x[jj] * gp[jj] : 0.f;
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (half * 4 + cc < 2 * bi) {                  // left of the diagonal block
+                        w.x = pack2(y[cc * 8 + 0], y[cc * 8 + 1]);
+                        w.y = pack2(y[cc * 8 + 2], y[cc * 8 + 3]);
+                        w.z = pack2(y[cc * 8 + 4], y[cc * 8 + 5]);
+                        w.w = pack2(y[cc * 8 + 6], y[cc * 8 + 7]);
+                    }
+                    *reinterpret_cast<uint4 *>(Lo + sw128_offset(i, half * 4 + cc)) = w;
+                }
+                if ((bi >> 1) == half) {                           // the diagonal block
+                    float *ld = Ldg + (bi * 16 + (i & 15)) * LB;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) ld[jj] = (bi & 1) ? y[16 + jj] : y[jj];
                 }
             } else {
                 const int i = row - 64;
@@ -371,115 +403,132 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         }
         tc_fence_before();
     }
-    __syncthreads();   // L and A_O ready; Gt no longer needed
+    __syncthreads();   // L_o, the diagonal blocks and A_O ready; Gt no longer needed
 
-    // ---- T = (I + L)^{-1}, blocked:
-    //   diagonal 16x16 blocks by forward substitution in registers (one lane
-    //   per column), then [[A,0],[C,B]]^{-1} = [[A^-1,0],[-B^-1 C A^-1, B^-1]]
-    //   for the 16-blocks inside each 32-block and for the two 32-blocks.
-    //   The blocks above the diagonal 16-blocks are never read; bf16(T)
-    //   writes zeros there.
-    float *Tm = Gt;                                         // Gt is consumed
-    float *X = reinterpret_cast<float *>(smem + kOffXs);    // scratch
-    constexpr int LX = 33;
+    // ---- T = (I + L)^{-1}.  With D = (I + L_d)^{-1} (the inverses of the
+    //      diagonal 16-blocks) and N = D L_o (strictly block-lower, so
+    //      N^4 = 0):  I + L = (I + L_d)(I + N)  and
+    //      T = (I + N)^{-1} D = (I - N + N^2 - N^3) D = (I - N (I - N (I - N))) D.
+    //      D by forward substitution in registers (one lane per column of a
+    //      block), then four 64 x 64 MMAs, each epilogue writing the next
+    //      bf16 operand.
     if (warp < 2) {
         const int blk = warp * 2 + (lane >> 4);
         const int c = lane & 15;
-        const int base = blk * 16;
+        const float *lb = Ldg + blk * 16 * LB;
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float acc = 0.f;
 #pragma unroll
-            for (int k = 0; k < r; ++k) acc += L[(base + r) * LM + base + k] * t[k];
+            for (int k = 0; k < r; ++k) acc += lb[r * LB + k] * t[k];
             t[r] = (r < c) ? 0.f : ((r == c) ? 1.f : -acc);
         }
+        asm volatile("bar.sync 1, 64;" ::: "memory");    // every lane has read its block of L
+        float *db = Ldg + blk * 16 * LB;                  // D replaces L_d in place
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tm[(base + r) * LM + base + c] = t[r];
+        for (int r = 0; r < 16; ++r) db[r * LB + c] = t[r];
     }
     __syncthreads();
-    // 16-blocks below the diagonal inside each 32-block (two of them); each
-    // thread computes two adjacent outputs of one row
-    {
-        const int pb = tid >> 7, i = (tid >> 3) & 15, j = (tid & 7) * 2;
-        const int r0 = 32 * pb + 16, c0 = 32 * pb;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float l = L[(r0 + i) * LM + c0 + k];
-            const float *t = Tm + (c0 + k) * LM + c0 + j;
-            a0 += l * t[0];
-            a1 += l * t[1];
-        }
-        X[(pb * 16 + i) * LX + j] = a0;
-        X[(pb * 16 + i) * LX + j + 1] = a1;
-    }
-    __syncthreads();
-    {
-        const int pb = tid >> 7, i = (tid >> 3) & 15, j = (tid & 7) * 2;
-        const int r0 = 32 * pb + 16, c0 = 32 * pb;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float t = Tm[(r0 + i) * LM + r0 + k];
-            a0 += t * X[(pb * 16 + k) * LX + j];
-            a1 += t * X[(pb * 16 + k) * LX + j + 1];
-        }
-        Tm[(r0 + i) * LM + c0 + j] = -a0;
-        Tm[(r0 + i) * LM + c0 + j + 1] = -a1;
-    }
-    __syncthreads();
-    // the 32-block below the diagonal: -T_B (L_C T_A).  X = L_C T_A: warp w
-    // owns columns [4w, 4w+4) of all 32 rows, so k runs over T_A's nonzero
-    // rows k >= 4w only (warp-uniform trip count).
-    {
-        const int i = lane, j0 = warp * 4;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k = j0; k < 32; ++k) {
-            const float l = L[(32 + i) * LM + k];
-            const float *t = Tm + k * LM + j0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a[e] += l * t[e];
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) X[i * LX + j0 + e] = a[e];
-    }
-    __syncthreads();
-    // T_C = -T_B X: warp w owns rows [4w, 4w+4), lane = column; k runs over
-    // T_B's nonzero columns k <= 4w+3 only.
-    {
-        const int i0 = warp * 4, j = lane;
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < i0 + 4; ++k) {
-            const float x = X[k * LX + j];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a[e] += Tm[(32 + i0 + e) * LM + 32 + k] * x;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Tm[(32 + i0 + e) * LM + j] = -a[e];
-    }
-    __syncthreads();
-
-    // ---- bf16(T) as the MMA's B operand (MN-major: rows k, columns j).  The
-    //      same bytes are the T rows of the prepared block: each group of 16
-    //      rows is one 2 KiB piece there (at prepared rows 32 g .. 32 g + 15,
-    //      same row mod 8, so the same swizzle), copied out in bulk below
+    // D in bf16, row-major (zero outside the diagonal blocks)
     for (int idx = tid; idx < kChunk * 8; idx += kThreadsP) {
         const int r = idx >> 3, c = idx & 7;
-        const float *src = Tm + r * LM + c * 8;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if ((c >> 1) <= (r >> 4)) {              // above the diagonal blocks T is zero
+        if ((c >> 1) == (r >> 4)) {
+            const float *src = Ldg + ((r >> 4) * 16 + (r & 15)) * LB + 8 * (c & 1);
             w.x = pack2(src[0], src[1]);
             w.y = pack2(src[2], src[3]);
             w.z = pack2(src[4], src[5]);
             w.w = pack2(src[6], src[7]);
         }
-        *reinterpret_cast<uint4 *>(B2 + sw128_offset(r, c)) = w;
+        *reinterpret_cast<uint4 *>(Dbf + sw128_offset(r, c)) = w;
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+
+    // Four hops: N = D L_o -> (N, Y1 = I - N); Z = N Y1 -> Y2 = I - Z;
+    // Z = N Y2 -> Y3 = I - Z; T = Y3 D -> bf16 T.  Each an M = 64 MMA (the
+    // 64 result rows sit in lanes 16 q .. 16 q + 15 of quadrant q), read by
+    // all eight warps: quadrant warp % 4, column half warp / 4.
+    uint32_t hop_parity = 0;
+#pragma unroll 1
+    for (int hop = 0; hop < 4; ++hop) {
+        const uint32_t col = (hop & 1) ? kColD2 : kColG;
+        if (warp == 2 && lane == 0 && !*abort) {
+            uint32_t aop, bop;
+            if (hop == 0) { aop = smem_u32(Dbf); bop = smem_u32(Lo); }
+            else if (hop < 3) { aop = smem_u32(Nbf); bop = smem_u32(Ybf); }
+            else { aop = smem_u32(Ybf); bop = smem_u32(Dbf); }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = sdesc_sw128(aop + kk * 32, 16, 1024);
+                const uint64_t b = sdesc_sw128(bop + kk * 2048, 8192, 1024);
+                mma_bf16(tmem + col, a, b, kIdescHop, kk != 0);
+            }
+            mma_commit(&bars->hop);
+        }
+        __syncwarp();
+        {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->hop, hop_parity, abort));
+            hop_parity ^= 1;
+            const int q = warp & 3, half = warp >> 2;
+            const int r = 16 * q + (lane & 15);
+            const int c1 = half * 32 + 8 * (lane >> 4);        // first column of each group of 8
+            if (ok) {
+                tc_fence_after();
+                float v[16];
+                const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + col + half * 32;
+                tmem_ld_16x2x8(ta, v);
+                tmem_ld_16x2x8(ta + 16, v + 8);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int cb = c1 + 16 * g;
+                    const uint32_t off = sw128_offset(r, (uint32_t)(cb >> 3));
+                    const float *z = v + 8 * g;
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = (cb + e == r ? 1.f : 0.f) - z[e];
+                    uint4 wy;
+                    wy.x = pack2(y[0], y[1]);
+                    wy.y = pack2(y[2], y[3]);
+                    wy.z = pack2(y[4], y[5]);
+                    wy.w = pack2(y[6], y[7]);
+                    if (hop == 3) {
+                        // T: the MMA's B operand and the prepared block's T rows
+                        uint4 wt;
+                        wt.x = pack2(z[0], z[1]);
+                        wt.y = pack2(z[2], z[3]);
+                        wt.z = pack2(z[4], z[5]);
+                        wt.w = pack2(z[6], z[7]);
+                        *reinterpret_cast<uint4 *>(B2 + off) = wt;
+                    } else {
+                        *reinterpret_cast<uint4 *>(Ybf + off) = wy;
+                        if (hop == 0) {
+                            uint4 wn;
+                            wn.x = pack2(z[0], z[1]);
+                            wn.y = pack2(z[2], z[3]);
+                            wn.z = pack2(z[4], z[5]);
+                            wn.w = pack2(z[6], z[7]);
+                            *reinterpret_cast<uint4 *>(Nbf + off) = wn;
+                        }
+                    }
+                }
+                fence_proxy_async();
+            }
+            tc_fence_before();
+        }
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    // ---- MMA A_O T (rows 0..63 of an M = 128 product: the A rows past A_O
+    //      read the next region and are never used); the T rows of the
+    //      prepared block leave in bulk: each group of 16 rows of the
+    //      row-major T is one 2 KiB piece there (prepared rows 32 g .. 32 g +
+    //      15, same row mod 8, so the same swizzle)
     if (warp == 2 && lane == 0 && !*abort) {
         const uint32_t a2 = smem_u32(AO), b2 = smem_u32(B2);
 #pragma unroll
