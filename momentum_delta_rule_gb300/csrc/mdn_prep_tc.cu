@@ -55,7 +55,7 @@ constexpr int LM = kChunk + 1;                 // padded fp32 row stride
 //                    MMA are in flight; after L is built, D bf16 [32768,
 //                    40960) and N bf16 [40960, 49152)
 //   [49408, 50432)   (alpha, beta, mu, eta) per token
-//   [50432, 52480)   per-token vectors (VecP rows of 64 fp32)
+//   [50432, 53504)   per-token vectors (12 rows of 64 fp32)
 constexpr int LB = 17;                         // padded row stride of a 16 x 16 block
 constexpr uint32_t kOffKQ = 0;
 constexpr uint32_t kOffLo = 0;
@@ -68,11 +68,11 @@ constexpr uint32_t kOffDbf = 32768;
 constexpr uint32_t kOffN = 40960;
 constexpr uint32_t kOffGate = 49408;
 constexpr uint32_t kOffVec = 50432;
-constexpr uint32_t kOffBarP = 52480;
+constexpr uint32_t kOffBarP = 53504;
 constexpr uint32_t kSmemP = kOffBarP + 128 + 1024;
 static_assert(kOffLd + 4 * 64 * LB <= kOffAO && kOffAO + 8192 <= kOffG, "prep layout");
 static_assert(kOffG + 4 * 64 * LM <= kOffGate && kOffN + 8192 <= kOffGate, "prep layout");
-static_assert(kOffGate + 16 * 64 <= kOffVec && kOffVec + 8 * 4 * 64 <= kOffBarP, "prep layout");
+static_assert(kOffGate + 16 * 64 <= kOffVec && kOffVec + 12 * 4 * 64 <= kOffBarP, "prep layout");
 static_assert(kSmemP <= 57344, "four CTAs per SM");
 
 constexpr uint32_t kTmemColsP = 128;
@@ -90,9 +90,10 @@ struct BarsP {
 };
 
 // rows of the per-token vector block: prefix sums of log alpha / log mu,
-// zero-mu counts, alpha products from each 16-row segment start, b, and the
-// scans' exchange slot
-enum { vA = 0, vU, vZ, vF, vB, vScan };
+// zero-mu counts, alpha products from each 16-row segment start, b, the
+// scans' exchange slot, the segments' lambda, and the three segments' column
+// factors
+enum { vA = 0, vU, vZ, vF, vB, vScan, vLam, vC };   // vC .. vC + 2: one row per segment
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -207,55 +208,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     __syncthreads();
 
     if (warp == 1) {
-        // ---- b_i = alpha_i b_{i-1} + beta_i mubar_i and the carry vectors
-        //      that do not need Gamma, in this warp alone (tokens 2l, 2l+1 per
-        //      lane; warp 1 has no column of segment 0's triangle): an affine
-        //      prefix scan of the maps x -> a x + c, composed pairwise first
-        const int i0 = 2 * lane, i1 = i0 + 1;
-        const float4 g0 = gate[i0], g1 = gate[i1];
-        const float A0 = vec[vA * kChunk + i0], A1 = vec[vA * kChunk + i1];
-        const float U0 = vec[vU * kChunk + i0], U1 = vec[vU * kChunk + i1];
-        const float Z0 = vec[vZ * kChunk + i0], Z1 = vec[vZ * kChunk + i1];
-        const float c0 = (Z0 == 0.f) ? g0.y * __expf(U0) : 0.f;
-        const float c1 = (Z1 == 0.f) ? g1.y * __expf(U1) : 0.f;
-        float ca = g1.x * g0.x, cb = g1.x * c0 + c1;          // the pair's map
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const float pa = __shfl_up_sync(0xffffffffu, ca, d);
-            const float pb = __shfl_up_sync(0xffffffffu, cb, d);
-            if (lane >= d) {
-                cb = ca * pb + cb;
-                ca = ca * pa;
-            }
-        }
-        float bprev = __shfl_up_sync(0xffffffffu, cb, 1);     // b_{i0 - 1}
-        if (lane == 0) bprev = 0.f;
-        const float b0 = g0.x * bprev + c0, b1 = cb;
-        vec[vB * kChunk + i0] = b0;
-        vec[vB * kChunk + i1] = b1;
+        // ---- the Gram MMA: this warp waits for the K/Q tiles alone and joins
+        //      the other warps again at the block barrier before L is built,
+        //      so the copy's latency hides behind everything up to there
         __syncwarp();
-        const int last = n - 1;
-        const float Al = vec[vA * kChunk + last], Ul = vec[vU * kChunk + last];
-        const float Zl = vec[vZ * kChunk + last], bl = vec[vB * kChunk + last];
-        const bool v0 = i0 < n, v1 = i1 < n;
-        auto put2 = [&](int row, float x0, float x1) {
-            *reinterpret_cast<float2 *>(gv + row * kChunk + i0) =
-                make_float2(v0 ? x0 : 0.f, v1 ? x1 : 0.f);
-        };
-        put2(kVecAbar, __expf(A0), __expf(A1));
-        put2(kVecBmA, bprev * g0.x, b0 * g1.x);               // b_0 = 0 before the first token
-        put2(kVecB, b0, b1);
-        put2(kVecGM, (Zl == Z0) ? __expf(Ul - U0) * g0.w : 0.f,
-             (Zl == Z1) ? __expf(Ul - U1) * g1.w : 0.f);
-        if (lane < 2) {
-            // [abar_n, b_n, mubar_n, n]
-            const float s0 = lane == 0 ? __expf(Al) : ((Zl == 0.f) ? __expf(Ul) : 0.f);
-            const float s1 = lane == 0 ? bl : (float)n;
-            *reinterpret_cast<float2 *>(gv + kVecScal * kChunk + 2 * lane) = make_float2(s0, s1);
-        } else if (lane < 32) {
-            *reinterpret_cast<float2 *>(gv + kVecScal * kChunk + 2 * lane) = make_float2(0.f, 0.f);
-        }
-        // ---- the Gram MMA G = [K; Q] K^T once the tiles have landed
         if (lane == 0) {
             const uint32_t kq = smem_u32(smem + kOffKQ);
             if (mbar_wait(&bars->tma, 0, abort)) {
@@ -275,64 +231,139 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         }
         __syncwarp();
     } else {
-        // ---- Gt = Gamma Diag(eta): thread = (row segment s of 16, column j);
-        //      a column that starts before the segment starts it from zero
-        //      (the alpha-carried part joins below) with m = eta_j times the
-        //      mu product over (j, r0], from the prefix sums (0 across a zero mu)
-        const int j = tid & 63, r0 = 16 * (tid >> 6);
-        if (j <= r0 + 15) {
-            const float et = gate[j].w;
-            float m = et;
-            if (j < r0) {
-                const float Zj = vec[vZ * kChunk + j], Zr = vec[vZ * kChunk + r0];
-                m = (Zr == Zj) ? et * __expf(vec[vU * kChunk + r0] - vec[vU * kChunk + j]) : 0.f;
-            }
-            const float4 g0 = gate[r0];
-            float g = g0.y * m;
-            float pa = g0.x;             // prod of alpha over [r0, r]
-            if (r0 >= j) Gt[r0 * LM + j] = g;
-            if (j == 0) vec[vF * kChunk + r0] = pa;
+        // every warp but warp 1 (224 threads, named barrier 2) from here to L
+        const int t7 = warp == 0 ? lane : tid - 32;
+        if (warp == 0) {
+            // ---- b_i = alpha_i b_{i-1} + beta_i mubar_i and the carry vectors
+            //      that do not need Gamma, in this warp alone (tokens 2l, 2l+1
+            //      per lane): an affine prefix scan of the maps x -> a x + c,
+            //      composed pairwise first
+            const int i0 = 2 * lane, i1 = i0 + 1;
+            const float4 g0 = gate[i0], g1 = gate[i1];
+            const float A0 = vec[vA * kChunk + i0], A1 = vec[vA * kChunk + i1];
+            const float U0 = vec[vU * kChunk + i0], U1 = vec[vU * kChunk + i1];
+            const float Z0 = vec[vZ * kChunk + i0], Z1 = vec[vZ * kChunk + i1];
+            const float c0 = (Z0 == 0.f) ? g0.y * __expf(U0) : 0.f;
+            const float c1 = (Z1 == 0.f) ? g1.y * __expf(U1) : 0.f;
+            float ca = g1.x * g0.x, cb = g1.x * c0 + c1;          // the pair's map
 #pragma unroll
-            for (int rr = 1; rr < 16; ++rr) {
-                const int r = r0 + rr;
+            for (int d = 1; d < 32; d <<= 1) {
+                const float pa = __shfl_up_sync(0xffffffffu, ca, d);
+                const float pb = __shfl_up_sync(0xffffffffu, cb, d);
+                if (lane >= d) {
+                    cb = ca * pb + cb;
+                    ca = ca * pa;
+                }
+            }
+            float bprev = __shfl_up_sync(0xffffffffu, cb, 1);     // b_{i0 - 1}
+            if (lane == 0) bprev = 0.f;
+            const float b0 = g0.x * bprev + c0, b1 = cb;
+            vec[vB * kChunk + i0] = b0;
+            vec[vB * kChunk + i1] = b1;
+            __syncwarp();
+            const int last = n - 1;
+            const float Al = vec[vA * kChunk + last], Ul = vec[vU * kChunk + last];
+            const float Zl = vec[vZ * kChunk + last], bl = vec[vB * kChunk + last];
+            const bool v0 = i0 < n, v1 = i1 < n;
+            auto put2 = [&](int row, float x0, float x1) {
+                *reinterpret_cast<float2 *>(gv + row * kChunk + i0) =
+                    make_float2(v0 ? x0 : 0.f, v1 ? x1 : 0.f);
+            };
+            put2(kVecAbar, __expf(A0), __expf(A1));
+            put2(kVecBmA, bprev * g0.x, b0 * g1.x);               // b_0 = 0 before the first token
+            put2(kVecB, b0, b1);
+            put2(kVecGM, (Zl == Z0) ? __expf(Ul - U0) * g0.w : 0.f,
+                 (Zl == Z1) ? __expf(Ul - U1) * g1.w : 0.f);
+            {
+                // [abar_n, b_n, mubar_n, n, 0, ...]
+                const float s0 = lane == 0 ? __expf(Al) : (lane == 1 ? ((Zl == 0.f) ? __expf(Ul) : 0.f) : 0.f);
+                const float s1 = lane == 0 ? bl : (lane == 1 ? (float)n : 0.f);
+                *reinterpret_cast<float2 *>(gv + kVecScal * kChunk + 2 * lane) = make_float2(s0, s1);
+            }
+            // ---- per segment s = 1..3 (rows r0 = 16 s ..): F_s(r) = prod of
+            //      alpha over [r0, r] and lambda_s(r) = alpha_r lambda_s(r-1) +
+            //      beta_r prod_{u=r0}^{r} mu_u (lambda_s(r0-1) = 0)
+            if (lane < 3) {
+                const int r0 = 16 * (lane + 1);
+                float F = 1.f, lam = 0.f, mt = 1.f;
+#pragma unroll 4
+                for (int rr = 0; rr < 16; ++rr) {
+                    const int r = r0 + rr;
+                    const float4 gr = gate[r];
+                    F *= gr.x;
+                    mt *= gr.z;
+                    lam = gr.x * lam + gr.y * mt;
+                    vec[vF * kChunk + r] = F;
+                    vec[vLam * kChunk + r] = lam;
+                }
+            }
+        } else if (warp == 2 || warp == 3) {
+            // ---- Gt = Gamma Diag(eta) on the four diagonal 16-blocks: thread
+            //      = (block b, column j = 16 b + jj), the column recurrence
+            //      from its diagonal entry down to the block's last row
+            const int t = tid - 64, blk = t >> 4, j = 16 * blk + (t & 15);
+            const float et = gate[j].w;
+            float m = 0.f, g = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * blk + rr;
                 const float4 gr = gate[r];
                 const bool diag = (r == j);
                 m = diag ? et : gr.z * m;
                 g = (diag ? 0.f : gr.x * g) + gr.y * m;
-                pa *= gr.x;
                 if (r >= j) Gt[r * LM + j] = g;
-                if (j == 0) vec[vF * kChunk + r] = pa;
+            }
+        } else {
+            // ---- column factors c_j^(s) = eta_j prod_{u=j+1}^{r0-1} mu_u for
+            //      the columns j < r0 = 16 s left of segment s, from the
+            //      prefix sums (0 across a zero mu)
+            const int t = tid - 128;
+            if (t < 96) {
+                const int sg = t < 16 ? 1 : (t < 48 ? 2 : 3);
+                const int j = t - (sg == 1 ? 0 : (sg == 2 ? 16 : 48));
+                const int rp = 16 * sg - 1;
+                const float c = (vec[vZ * kChunk + rp] == vec[vZ * kChunk + j])
+                                    ? gate[j].w * __expf(vec[vU * kChunk + rp] - vec[vU * kChunk + j])
+                                    : 0.f;
+                vec[(vC + sg - 1) * kChunk + j] = c;
             }
         }
-    }
-    __syncthreads();
-    if (tid < 64) {
-        // exact values at rows 31 and 47 (row 15 is exact already):
-        // Gt_{r,j} = local_{r,j} + F_r Gt_{r0-1,j}
-        const int j = tid;
-        float e = Gt[15 * LM + j];
-#pragma unroll
-        for (int g = 1; g < 4; ++g) {
-            const int rend = 16 * g + 15;
-            if (j < 16 * g) {
-                e = Gt[rend * LM + j] + vec[vF * kChunk + rend] * e;
-                Gt[rend * LM + j] = e;
-            } else if (j <= rend) {
-                e = Gt[rend * LM + j];
+        asm volatile("bar.sync 2, 224;" ::: "memory");
+        // Left of the diagonal blocks the recurrence is affine in the
+        // segment's start row:  Gt_{r,j} = F_s(r) Gt_{r0-1,j} + c_j^(s)
+        // lambda_s(r)  (j < r0, every term non-negative).  Rows 31 and 47
+        // first, in order (the next segments start from them) ...
+        if (warp == 2 || warp == 3) {
+            const int j = tid - 64;
+            float e = Gt[15 * LM + j];
+            if (j < 16) {
+                e = vec[vF * kChunk + 31] * e + vec[vC * kChunk + j] * vec[vLam * kChunk + 31];
+                Gt[31 * LM + j] = e;
+            } else if (j < 32) {
+                e = Gt[31 * LM + j];
             }
+            if (j < 32)
+                Gt[47 * LM + j] = vec[vF * kChunk + 47] * e +
+                                  vec[(vC + 1) * kChunk + j] * vec[vLam * kChunk + 47];
         }
-    }
-    __syncthreads();
-    if (warp >= 2) {
-        // the interior rows of segments 1..3 for the columns that started before
-        const int j = tid & 63, r0 = 16 * (tid >> 6);
-        if (j < r0) {
-            const float e = Gt[(r0 - 1) * LM + j];
-#pragma unroll
-            for (int rr = 0; rr < 15; ++rr) {
-                const int r = r0 + rr;
-                Gt[r * LM + j] += vec[vF * kChunk + r] * e;
+        asm volatile("bar.sync 2, 224;" ::: "memory");
+        // ... then every other entry left of the diagonal blocks at once:
+        // segment 1 rows 16..30 x columns 0..15, segment 2 rows 32..46 x
+        // 0..31, segment 3 rows 48..63 x 0..47
+        for (int idx = t7; idx < 240 + 480 + 768; idx += kThreadsP - 32) {
+            int sg, rr, j;
+            if (idx < 240) {
+                sg = 1; rr = idx >> 4; j = idx & 15;
+            } else if (idx < 720) {
+                const int k = idx - 240;
+                sg = 2; rr = k >> 5; j = k & 31;
+            } else {
+                const int k = idx - 720;
+                sg = 3; rr = k / 48; j = k - rr * 48;
             }
+            const int r0 = 16 * sg, r = r0 + rr;
+            Gt[r * LM + j] = vec[vF * kChunk + r] * Gt[(r0 - 1) * LM + j] +
+                             vec[(vC + sg - 1) * kChunk + j] * vec[vLam * kChunk + r];
         }
     }
     __syncthreads();   // Gt complete
