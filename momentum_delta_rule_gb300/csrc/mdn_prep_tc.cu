@@ -81,7 +81,8 @@ constexpr uint32_t kColD2 = 64;                // A_O T accumulator, 64 columns
 
 constexpr uint32_t kIdescGram = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescOut = idesc_bf16(128, 64, false, true);
-constexpr uint32_t kIdescHop = idesc_bf16(64, 64, false, true);   // the inverse's products
+constexpr uint32_t kIdescHop = idesc_bf16(64, 64, false, true);    // the inverse's products
+constexpr uint32_t kIdescHop2 = idesc_bf16(64, 128, false, true);  // ... with two B blocks
 
 struct BarsP {
     uint64_t tma, gram, hop, out, drain;
@@ -439,10 +440,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     // ---- T = (I + L)^{-1}.  With D = (I + L_d)^{-1} (the inverses of the
     //      diagonal 16-blocks) and N = D L_o (strictly block-lower, so
     //      N^4 = 0):  I + L = (I + L_d)(I + N)  and
-    //      T = (I + N)^{-1} D = (I - N + N^2 - N^3) D = (I - N (I - N (I - N))) D.
+    //      T = (I + N)^{-1} D = D - N D + N^2 D - N^3 D.
     //      D by forward substitution in registers (one lane per column of a
-    //      block), then four 64 x 64 MMAs, each epilogue writing the next
-    //      bf16 operand.
+    //      block), then three MMAs, each epilogue writing the next bf16
+    //      operands.
     if (warp < 2) {
         const int blk = warp * 2 + (lane >> 4);
         const int c = lane & 15;
@@ -479,24 +480,27 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     __syncthreads();
     tc_fence_after();
 
-    // Four hops: N = D L_o -> (N, Y1 = I - N); Z = N Y1 -> Y2 = I - Z;
-    // Z = N Y2 -> Y3 = I - Z; T = Y3 D -> bf16 T.  Each an M = 64 MMA (the
-    // 64 result rows sit in lanes 16 q .. 16 q + 15 of quadrant q), read by
+    // Three hops, T = D - N D + N^2 D - N^3 D: N = D L_o; [N D | N^2] =
+    // N [D | N]; [N^2 D | N^3 D] = N^2 [D | N D].  Each an M = 64 MMA (the 64
+    // result rows sit in lanes 16 q .. 16 q + 15 of quadrant q) whose B
+    // operand is two 64-column blocks 8 KiB apart (D, then N or N D), read by
     // all eight warps: quadrant warp % 4, column half warp / 4.
     uint32_t hop_parity = 0;
+    const int hq = warp & 3, hhalf = warp >> 2;
+    const int hr = 16 * hq + (lane & 15);                      // result row of this thread
+    const int hc1 = hhalf * 32 + 8 * (lane >> 4);              // first column of its two groups of 8
+    const uint32_t hta = tmem + ((uint32_t)(32 * hq) << 16) + hhalf * 32;
 #pragma unroll 1
-    for (int hop = 0; hop < 4; ++hop) {
-        const uint32_t col = (hop & 1) ? kColD2 : kColG;
+    for (int hop = 0; hop < 3; ++hop) {
         if (warp == 2 && lane == 0 && !*abort) {
-            uint32_t aop, bop;
-            if (hop == 0) { aop = smem_u32(Dbf); bop = smem_u32(Lo); }
-            else if (hop < 3) { aop = smem_u32(Nbf); bop = smem_u32(Ybf); }
-            else { aop = smem_u32(Ybf); bop = smem_u32(Dbf); }
+            const uint32_t aop = hop == 0 ? smem_u32(Dbf) : (hop == 1 ? smem_u32(Nbf) : smem_u32(Ybf));
+            const uint32_t bop = hop == 0 ? smem_u32(Lo) : smem_u32(Dbf);
+            const uint32_t idesc = hop == 0 ? kIdescHop : kIdescHop2;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t a = sdesc_sw128(aop + kk * 32, 16, 1024);
                 const uint64_t b = sdesc_sw128(bop + kk * 2048, 8192, 1024);
-                mma_bf16(tmem + col, a, b, kIdescHop, kk != 0);
+                mma_bf16(tmem + kColG, a, b, idesc, kk != 0);
             }
             mma_commit(&bars->hop);
         }
@@ -504,47 +508,51 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         {
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->hop, hop_parity, abort));
             hop_parity ^= 1;
-            const int q = warp & 3, half = warp >> 2;
-            const int r = 16 * q + (lane & 15);
-            const int c1 = half * 32 + 8 * (lane >> 4);        // first column of each group of 8
             if (ok) {
                 tc_fence_after();
-                float v[16];
-                const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + col + half * 32;
-                tmem_ld_16x2x8(ta, v);
-                tmem_ld_16x2x8(ta + 16, v + 8);
+                float v[16], w2[16];
+                tmem_ld_16x2x8(hta, v);                        // first 64 columns
+                tmem_ld_16x2x8(hta + 16, v + 8);
+                if (hop > 0) {
+                    tmem_ld_16x2x8(hta + 64, w2);              // second 64 columns
+                    tmem_ld_16x2x8(hta + 64 + 16, w2 + 8);
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
-                    const int cb = c1 + 16 * g;
-                    const uint32_t off = sw128_offset(r, (uint32_t)(cb >> 3));
-                    const float *z = v + 8 * g;
-                    float y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = (cb + e == r ? 1.f : 0.f) - z[e];
-                    uint4 wy;
-                    wy.x = pack2(y[0], y[1]);
-                    wy.y = pack2(y[2], y[3]);
-                    wy.z = pack2(y[4], y[5]);
-                    wy.w = pack2(y[6], y[7]);
-                    if (hop == 3) {
-                        // T: the MMA's B operand and the prepared block's T rows
-                        uint4 wt;
-                        wt.x = pack2(z[0], z[1]);
-                        wt.y = pack2(z[2], z[3]);
-                        wt.z = pack2(z[4], z[5]);
-                        wt.w = pack2(z[6], z[7]);
-                        *reinterpret_cast<uint4 *>(B2 + off) = wt;
+                    const int cb = hc1 + 16 * g;
+                    const uint32_t off = sw128_offset(hr, (uint32_t)(cb >> 3));
+                    const float *x = v + 8 * g, *y = w2 + 8 * g;
+                    uint4 o;
+                    if (hop == 0) {
+                        // N
+                        o.x = pack2(x[0], x[1]); o.y = pack2(x[2], x[3]);
+                        o.z = pack2(x[4], x[5]); o.w = pack2(x[6], x[7]);
+                        *reinterpret_cast<uint4 *>(Nbf + off) = o;
+                    } else if (hop == 1) {
+                        // N D replaces N (its MMA is complete); N^2
+                        o.x = pack2(x[0], x[1]); o.y = pack2(x[2], x[3]);
+                        o.z = pack2(x[4], x[5]); o.w = pack2(x[6], x[7]);
+                        *reinterpret_cast<uint4 *>(Nbf + off) = o;
+                        o.x = pack2(y[0], y[1]); o.y = pack2(y[2], y[3]);
+                        o.z = pack2(y[4], y[5]); o.w = pack2(y[6], y[7]);
+                        *reinterpret_cast<uint4 *>(Ybf + off) = o;
                     } else {
-                        *reinterpret_cast<uint4 *>(Ybf + off) = wy;
-                        if (hop == 0) {
-                            uint4 wn;
-                            wn.x = pack2(z[0], z[1]);
-                            wn.y = pack2(z[2], z[3]);
-                            wn.z = pack2(z[4], z[5]);
-                            wn.w = pack2(z[6], z[7]);
-                            *reinterpret_cast<uint4 *>(Nbf + off) = wn;
+                        // T = D - N D + N^2 D - N^3 D (D exact in fp32, block diagonal)
+                        const uint4 ndr = *reinterpret_cast<const uint4 *>(Nbf + off);
+                        const __nv_bfloat162 *nd2 = reinterpret_cast<const __nv_bfloat162 *>(&ndr);
+                        const bool in_blk = (cb >> 4) == (hr >> 4);
+                        const float *drow = Ldg + ((hr >> 4) * 16 + (hr & 15)) * LB + (cb & 15);
+                        float t[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 nd = __bfloat1622float2(nd2[e]);
+                            t[2 * e] = (in_blk ? drow[2 * e] : 0.f) - nd.x + x[2 * e] - y[2 * e];
+                            t[2 * e + 1] = (in_blk ? drow[2 * e + 1] : 0.f) - nd.y + x[2 * e + 1] - y[2 * e + 1];
                         }
+                        o.x = pack2(t[0], t[1]); o.y = pack2(t[2], t[3]);
+                        o.z = pack2(t[4], t[5]); o.w = pack2(t[6], t[7]);
+                        *reinterpret_cast<uint4 *>(B2 + off) = o;
                     }
                 }
                 fence_proxy_async();
