@@ -85,13 +85,17 @@ chunk_offsets_kernel(const int32_t *cu, int n_seq, int32_t *off, int32_t *order)
 }
 
 // ---------------------------------------------------------------- prep
+//
+// Tile copies are fully unrolled loops (constant trip counts), so that every
+// thread issues all of its loads of a tile before the first shared-memory
+// store instead of one load round trip per iteration.
 
 template <int D>
 struct PrepSmem {
     static constexpr int LD = D + 1;          // padded row stride of K, Q
     static constexpr int LM = kChunk + 1;     // padded row stride of 64x64
     static constexpr int kFloats =
-        2 * kChunk * LD + 4 * kChunk * LM + 10 * kChunk + 64;
+        2 * kChunk * LD + 4 * kChunk * LM + 12 * kChunk + 64;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
@@ -109,6 +113,28 @@ __device__ __forceinline__ float scan64(float x, float *xch) {
     if (warp == 1) x += *xch;
     __syncthreads();
     return x;
+}
+
+// Inclusive composition of the affine maps x -> a x + c over the 64 lanes of
+// warps 0 and 1 (token order); returns the composed map's c, i.e. the value
+// of the recurrence x_i = a_i x_{i-1} + c_i started from x = 0.  Every thread
+// of the block must call it (it synchronises the block).
+__device__ __forceinline__ float scan64_affine(float a, float c, float *xch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float pa = __shfl_up_sync(0xffffffffu, a, d);
+        const float pc = __shfl_up_sync(0xffffffffu, c, d);
+        if (lane >= d) {
+            c = a * pc + c;
+            a = a * pa;
+        }
+    }
+    if (warp == 0 && lane == 31) *xch = c;
+    __syncthreads();
+    if (warp == 1) c = a * *xch + c;
+    __syncthreads();
+    return c;
 }
 
 template <int D, typename Tin>
@@ -136,11 +162,14 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     float *vU = vA + kChunk;               // U'_i = sum of finite log mu
     float *vZ = vU + kChunk;               // number of zero mu so far
     float *vbb = vZ + kChunk;              // b_i
-    float *xch = vbb + kChunk;             // scan exchange
+    float *vm = vbb + kChunk;              // mu
+    float *vgs = vm + kChunk;              // gamma_{n,j} (Gamma's last row, kept for the carry)
+    float *xch = vgs + kChunk;             // scan exchange
 
     const size_t rs = (size_t)p.H * D;     // token row stride
     const Tin *kg = static_cast<const Tin *>(p.k) + (size_t)loc.t0 * rs + (size_t)h * D;
     const Tin *qg = static_cast<const Tin *>(p.q) + (size_t)loc.t0 * rs + (size_t)h * D;
+#pragma unroll
     for (int idx = tid; idx < kChunk * D; idx += kThreads) {
         const int i = idx / D, d = idx - i * D;
         float kv = 0.f, qv = 0.f;
@@ -165,6 +194,9 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     const float A = scan64(tid < kChunk ? logf(a) : 0.f, xch);
     const float U = scan64(tid < kChunk && !zero_mu ? logf(mu) : 0.f, xch);
     const float Z = scan64(tid < kChunk && zero_mu ? 1.f : 0.f, xch);
+    // b_i = alpha_i b_{i-1} + beta_i mubar_i  (mubar_i = exp(U_i) without a zero mu)
+    const float bsum = scan64_affine(tid < kChunk ? a : 1.f,
+                                     (tid < kChunk && Z == 0.f) ? be * expf(U) : 0.f, xch);
     if (tid < kChunk) {
         va[tid] = a;
         vb[tid] = be;
@@ -172,28 +204,26 @@ chunk_prep_simt_kernel(ChunkProblem p) {
         vA[tid] = A;
         vU[tid] = U;
         vZ[tid] = Z;
+        vbb[tid] = bsum;
+        vm[tid] = mu;
     }
     __syncthreads();
 
     // ---- Gamma, column j per lane: gamma_{j,j} = beta_j and
-    //      gamma_{i,j} = alpha_i gamma_{i-1,j} + beta_i prod_{u=j+1}^{i} mu_u,
-    //      the product taken from the log-space prefix sums (exponent <= 0).
-    //      b_i = sum_{r<=i} beta_r exp(A_i - A_r) mubar_r (exponents <= 0).
+    //      gamma_{i,j} = alpha_i gamma_{i-1,j} + beta_i m_{i,j} with the mu
+    //      product m_{i,j} = prod_{u=j+1}^{i} mu_u carried as m <- mu_i m
+    //      (exact for mu = 0, no exponential per entry)
     if (tid < kChunk) {
         const int j = tid;
-        float g = vb[j];
+        float g = vb[j], m = 1.f;
         for (int i = 0; i < j; ++i) G[i * LM + j] = 0.f;
         G[j * LM + j] = g;
         for (int i = j + 1; i < kChunk; ++i) {
-            const float m = (vZ[i] == vZ[j]) ? expf(vU[i] - vU[j]) : 0.f;
+            m *= vm[i];
             g = va[i] * g + vb[i] * m;
             G[i * LM + j] = g;
         }
-        float bsum = 0.f;
-        for (int r = 0; r <= j; ++r) {
-            if (vZ[r] == 0.f) bsum += vb[r] * expf(vA[j] - vA[r] + vU[r]);
-        }
-        vbb[j] = bsum;
+        vgs[j] = (j < n) ? G[(n - 1) * LM + j] : 0.f;
     }
     __syncthreads();
 
@@ -231,19 +261,93 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     }
     __syncthreads();
 
-    // ---- T = (I + L)^{-1} by forward substitution, one row at a time:
-    //      T[i][j] = -sum_{k=j}^{i-1} L[i][k] T[k][j]  (j < i)
+    // ---- T = (I + L)^{-1}, blocked: diagonal 16x16 blocks by forward
+    //      substitution in registers (one lane per column), then
+    //      [[A, 0], [C, B]]^{-1} = [[A^-1, 0], [-B^-1 C A^-1, B^-1]] for the
+    //      16-blocks inside each 32-block and for the two 32-blocks.  T holds
+    //      the identity from the step above, so everything above the
+    //      diagonal blocks stays zero.
     {
-        const int j = tid >> 2, part = tid & 3;
-        for (int i = 1; i < kChunk; ++i) {
-            float s = 0.f;
-            if (j < i)
-                for (int k = j + part; k < i; k += 4) s += L[i * LM + k] * Tm[k * LM + j];
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (j < i && part == 0) Tm[i * LM + j] = -s;
-            __syncthreads();
+        const int warp = tid >> 5, lane = tid & 31;
+        float *X = G;                      // scratch: Gamma is consumed
+        constexpr int LX = 33;
+        if (warp < 2) {
+            const int blk = warp * 2 + (lane >> 4);
+            const int c = lane & 15;
+            const int base = blk * 16;
+            float t[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < r; ++k) acc += L[(base + r) * LM + base + k] * t[k];
+                t[r] = (r < c) ? 0.f : ((r == c) ? 1.f : -acc);
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tm[(base + r) * LM + base + c] = t[r];
         }
+        __syncthreads();
+        // 16-blocks below the diagonal inside each 32-block (two of them);
+        // each thread computes two adjacent outputs of one row
+        {
+            const int pb = tid >> 7, i = (tid >> 3) & 15, j = (tid & 7) * 2;
+            const int r0 = 32 * pb + 16, c0 = 32 * pb;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float l = L[(r0 + i) * LM + c0 + k];
+                const float *t = Tm + (c0 + k) * LM + c0 + j;
+                a0 += l * t[0];
+                a1 += l * t[1];
+            }
+            X[(pb * 16 + i) * LX + j] = a0;
+            X[(pb * 16 + i) * LX + j + 1] = a1;
+        }
+        __syncthreads();
+        {
+            const int pb = tid >> 7, i = (tid >> 3) & 15, j = (tid & 7) * 2;
+            const int r0 = 32 * pb + 16, c0 = 32 * pb;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float t = Tm[(r0 + i) * LM + r0 + k];
+                a0 += t * X[(pb * 16 + k) * LX + j];
+                a1 += t * X[(pb * 16 + k) * LX + j + 1];
+            }
+            Tm[(r0 + i) * LM + c0 + j] = -a0;
+            Tm[(r0 + i) * LM + c0 + j + 1] = -a1;
+        }
+        __syncthreads();
+        // the 32-block below the diagonal: -T_B (L_C T_A).  X = L_C T_A: warp
+        // w owns columns [4w, 4w+4) of all 32 rows; k runs over T_A's nonzero
+        // rows k >= 4w only
+        {
+            const int i = lane, j0 = warp * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = j0; k < 32; ++k) {
+                const float l = L[(32 + i) * LM + k];
+                const float *t = Tm + k * LM + j0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] += l * t[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) X[i * LX + j0 + e] = acc[e];
+        }
+        __syncthreads();
+        // T_C = -T_B X: warp w owns rows [4w, 4w+4), lane = column; k runs
+        // over T_B's nonzero columns k <= 4w+3 only
+        {
+            const int i0 = warp * 4, j = lane;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < i0 + 4; ++k) {
+                const float x = X[k * LX + j];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] += Tm[(32 + i0 + e) * LM + 32 + k] * x;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Tm[(32 + i0 + e) * LM + j] = -acc[e];
+        }
+        __syncthreads();
     }
 
     // ---- write the prepared block
@@ -283,7 +387,7 @@ chunk_prep_simt_kernel(ChunkProblem p) {
         vec[kVecAbar * kChunk + i] = valid ? abar : 0.f;
         vec[kVecBmA * kChunk + i] = (valid && i > 0) ? vbb[i - 1] * va[i] : 0.f;
         vec[kVecB * kChunk + i] = valid ? vbb[i] : 0.f;
-        vec[kVecGS * kChunk + i] = valid ? G[last * LM + i] * ve[i] : 0.f;
+        vec[kVecGS * kChunk + i] = valid ? vgs[i] * ve[i] : 0.f;
         const float mtail = (vZ[last] == vZ[i]) ? expf(vU[last] - vU[i]) : 0.f;
         vec[kVecGM * kChunk + i] = valid ? mtail * ve[i] : 0.f;
         float sc = 0.f;
@@ -340,6 +444,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
     const int nchunks = (len + kChunk - 1) / kChunk;
     const size_t st_off = (size_t)sh * D * D;
 
+#pragma unroll
     for (int idx = tid; idx < D * kNS; idx += kThreads) {
         const int d = idx / kNS, c = idx - d * kNS;
         const size_t g = st_off + (size_t)d * D + col0 + c;
@@ -363,6 +468,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
         const float *vg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffVec);
 
         __syncthreads();   // previous chunk finished with every buffer
+#pragma unroll
         for (int idx = tid; idx < kChunk * D; idx += kThreads) {
             const int i = idx / D, d = idx - i * D;
             float kv = 0.f, qv = 0.f;
@@ -373,14 +479,17 @@ chunk_state_simt_kernel(ChunkProblem p) {
             Ks[idx] = kv;
             Qs[idx] = qv;
         }
+#pragma unroll
         for (int idx = tid; idx < kChunk * kNS; idx += kThreads) {
             const int i = idx / kNS, cx = idx - i * kNS;
             Vs[idx] = (i < n) ? to_f32(vg0[(size_t)(t0 + i) * rs + cx]) : 0.f;
         }
+#pragma unroll
         for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
             Ts[idx] = Tg[idx];
             AOTs[idx] = AOTg[idx];
         }
+#pragma unroll
         for (int idx = tid; idx < kVecRows * kChunk; idx += kThreads) vec[idx] = vg[idx];
         __syncthreads();
 
