@@ -30,7 +30,8 @@
 namespace mdn {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;     // prep
+constexpr int kThreadsS = 512;    // state pass: 16 warps, 4 token rows and D/16 state rows each
 
 // ------------------------------------------------------------- offsets
 
@@ -415,11 +416,11 @@ struct StateSmem {
 };
 
 template <int D, typename Tin>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreadsS)
 chunk_state_simt_kernel(ChunkProblem p) {
     constexpr int kSlices = D / kNS;
-    constexpr int kRowsA = kChunk / (kThreads / 32);   // 8 token rows per warp
-    constexpr int kRowsC = D / (kThreads / 32);        // state rows per warp
+    constexpr int kRowsA = kChunk / (kThreadsS / 32);   // token rows per warp
+    constexpr int kRowsC = D / (kThreadsS / 32);        // state rows per warp
     const int slice = blockIdx.x % kSlices;
     const int kh = blockIdx.x / kSlices;
     const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
@@ -445,7 +446,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
     const size_t st_off = (size_t)sh * D * D;
 
 #pragma unroll
-    for (int idx = tid; idx < D * kNS; idx += kThreads) {
+    for (int idx = tid; idx < D * kNS; idx += kThreadsS) {
         const int d = idx / kNS, c = idx - d * kNS;
         const size_t g = st_off + (size_t)d * D + col0 + c;
         Ss[idx] = p.S0 ? p.S0[g] : 0.f;
@@ -469,7 +470,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
 
         __syncthreads();   // previous chunk finished with every buffer
 #pragma unroll
-        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
+        for (int idx = tid; idx < kChunk * D; idx += kThreadsS) {
             const int i = idx / D, d = idx - i * D;
             float kv = 0.f, qv = 0.f;
             if (i < n) {
@@ -480,17 +481,17 @@ chunk_state_simt_kernel(ChunkProblem p) {
             Qs[idx] = qv;
         }
 #pragma unroll
-        for (int idx = tid; idx < kChunk * kNS; idx += kThreads) {
+        for (int idx = tid; idx < kChunk * kNS; idx += kThreadsS) {
             const int i = idx / kNS, cx = idx - i * kNS;
             Vs[idx] = (i < n) ? to_f32(vg0[(size_t)(t0 + i) * rs + cx]) : 0.f;
         }
 #pragma unroll
-        for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+        for (int idx = tid; idx < kChunk * kChunk; idx += kThreadsS) {
             Ts[idx] = Tg[idx];
             AOTs[idx] = AOTg[idx];
         }
 #pragma unroll
-        for (int idx = tid; idx < kVecRows * kChunk; idx += kThreads) vec[idx] = vg[idx];
+        for (int idx = tid; idx < kVecRows * kChunk; idx += kThreadsS) vec[idx] = vg[idx];
         __syncthreads();
 
         // ---- K S_0, K M_0, Q S_0, Q M_0 for 8 token rows x 1 column
@@ -555,7 +556,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < D * kNS; idx += kThreads) {
+    for (int idx = tid; idx < D * kNS; idx += kThreadsS) {
         const int d = idx / kNS, cx = idx - d * kNS;
         const size_t g = st_off + (size_t)d * D + col0 + cx;
         if (p.S_T) p.S_T[g] = Ss[idx];
@@ -583,7 +584,7 @@ cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
     if (err != cudaSuccess) return err;
     const long blocks = (long)p.n_seq * p.H * (D / kNS);
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    ks<<<(unsigned)blocks, kThreads, StateSmem<D>::kBytes, st>>>(p);
+    ks<<<(unsigned)blocks, kThreadsS, StateSmem<D>::kBytes, st>>>(p);
     return cudaGetLastError();
 }
 
