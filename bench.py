@@ -9,10 +9,11 @@ roofline fraction of its dominant kernel.  The decode step (256 sequences x
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
 Timing: W warm-up steps, then exactly K steps; before every timed step L2 is
-flushed by writing a 256 MiB buffer (outside the timed interval); each step
-is bracketed by CUDA events on the launching stream, and the library records
-caller-created events at its stage boundaries so the dominant kernel is timed
-live.  With N > 1 (torchrun) every rank runs the same workload independently
+flushed by writing a 256 MiB buffer and then reading a second one (outside
+the timed interval, so the flush's own dirty lines are written back before
+the timer starts); each step is bracketed by CUDA events on the launching
+stream, and the library records caller-created events at its stage
+boundaries so the dominant kernel is timed live.  With N > 1 (torchrun) every rank runs the same workload independently
 (replicas: the method has no exchange step), timing is bracketed by a barrier
 and synchronize on both sides and the MAX over ranks is taken.
 """
@@ -304,6 +305,23 @@ def config_of(w, x, l2):
     return cfg
 
 
+class L2Flush:
+    """Empties L2 of every input before a timed step: writes a buffer larger
+    than L2, then reads a second one, so that the timed kernels start with
+    neither cached inputs nor the write flush's dirty lines still waiting to
+    be written back (those would otherwise go out to HBM during the timed
+    kernels and be charged to them)."""
+
+    def __init__(self, nbytes, dev):
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(nbytes // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
+
+
 def time_prefill(mdn, x_dev, w, steps, warmup, world, flush):
     dev = x_dev["q"].device
     o = torch.empty_like(x_dev["v"])
@@ -584,7 +602,7 @@ def main():
     w = W.BY_NAME[args.workload]
     x = W.make_prefill(w)
     x_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(L2_FLUSH_BYTES, dev)
 
     clocks = ClockSampler(local).start()
     r = time_prefill(mdn, x_dev, w, args.steps, args.warmup, world, flush)
@@ -615,7 +633,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if tensor else "f32", "data": "synthetic",
-            "config": config_of(w, x, "flushed (256 MiB write) before every timed step"),
+            "config": config_of(w, x, "flushed before every timed step: 256 MiB written, "
+                                      "then another 256 MiB read"),
             "gpu_launches": r["launches_per_step"] * args.steps,
             "path": "tensor_core" if tensor else "cuda_core",
             "roofline": roofline, "stages": stages, "clocks": clk, "peaks": peak_src}

@@ -68,6 +68,18 @@ def test_prepare_inputs_in_place():
     _check(20, 2, 128, "bf16", seed=2, in_place=True)
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prepare_inputs_whole_tiles_and_tail(dtype, D):
+    """Several whole 16 KiB tiles stream through shared memory; the rows after
+    the last whole tile take the one-shot kernel."""
+    _check(301, 3, D, dtype, seed=6)
+
+
+def test_prepare_inputs_in_place_streaming():
+    _check(500, 2, 128, "bf16", seed=7, in_place=True)
+
+
 def test_prepare_inputs_no_correction():
     _check(20, 2, 128, "fp32", seed=3, comba_d=0.0)
 
