@@ -11,17 +11,24 @@
 //
 //   A_i = sum_{r<=i} log alpha_r, U_i = sum_{r<=i, mu_r>0} log mu_r,
 //   Z_i = #{r <= i : mu_r = 0}                       (warp-shuffle prefix scans)
-//   Gt = Gamma Diag(eta) by the column recurrence
+//   Gt = Gamma Diag(eta): on the four diagonal 16-blocks by the column
+//   recurrence
 //       m_{j,j} = eta_j,           m_{i,j} = mu_i m_{i-1,j}  (= eta_j prod_{u=j+1}^{i} mu_u)
-//       Gt_{j,j} = beta_j eta_j,   Gt_{i,j} = alpha_i Gt_{i-1,j} + beta_i m_{i,j}
-//     in four row segments of 16 run side by side and joined exactly (the
-//     recurrence is affine); it needs no exponential per entry and no
-//     difference of prefix sums, so mu = 0 is exact
+//       Gt_{j,j} = beta_j eta_j,   Gt_{i,j} = alpha_i Gt_{i-1,j} + beta_i m_{i,j},
+//   left of them (rows of segment s starting at r0, columns j < r0) by the
+//   exact split of that sum at r0
+//       Gt_{r,j} = F_s(r) Gt_{r0-1,j} + c_j^(s) lambda_s(r),
+//       F_s(r) = prod_{u=r0}^{r} alpha_u,  c_j^(s) = eta_j prod_{u=j+1}^{r0-1} mu_u,
+//       lambda_s(r) = alpha_r lambda_s(r-1) + beta_r prod_{u=r0}^{r} mu_u;
+//   no exponential per entry, no difference of prefix sums, so mu = 0 is
+//   exact and nothing cancels
 //   b_i = alpha_i b_{i-1} + beta_i [Z_i = 0] exp(U_i)  (affine prefix scan)
 //   MMA   G = [K; Q] K^T                                 (M=128, N=64, K=128)
 //   L_{i,j}   = alpha_i G_K[i,j] Gt_{i-1,j}     (j < i: the row-shifted Gamma)
 //   A_O[i,j]  = G_Q[i,j] Gt_{i,j}               (j <= i)
-//   T = (I + L)^{-1}                   (blocked forward substitution, fp32)
+//   T = (I + L)^{-1} = D - N D + N^2 D - N^3 D with D the inverses of L's
+//   diagonal 16-blocks (forward substitution, fp32) and N = D L_o (L_o: L
+//   off those blocks, so N^4 = 0): three MMAs (M=64)
 //   MMA   A_O T                                          (M=128, N=64, K=64)
 //
 // and writes the prepared block: T and A_O T in bf16 in the 128-byte-swizzled
