@@ -22,7 +22,9 @@
 //       lambda_s(r) = alpha_r lambda_s(r-1) + beta_r prod_{u=r0}^{r} mu_u;
 //   no exponential per entry, no difference of prefix sums, so mu = 0 is
 //   exact and nothing cancels
-//   b_i = alpha_i b_{i-1} + beta_i [Z_i = 0] exp(U_i)  (affine prefix scan)
+//   b_i = alpha_i b_{i-1} + beta_i mubar_i, F_s and lambda_s: one segmented
+//     prefix scan (one token per lane) of the maps (b, mubar) -> (alpha b +
+//     beta mu mubar, mu mubar), beside the log-space scans
 //   MMA   G = [K; Q] K^T                                 (M=128, N=64, K=128)
 //   L_{i,j}   = alpha_i G_K[i,j] Gt_{i-1,j}     (j < i: the row-shifted Gamma)
 //   A_O[i,j]  = G_Q[i,j] Gt_{i,j}               (j <= i)
@@ -108,32 +110,67 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Inclusive prefix sums of three values over lanes 0..63 (warps 0 and 1),
-// side by side.  Called by those two warps only; they synchronise on named
-// barrier 1.  xch: three exchange slots.
-__device__ __forceinline__ void scan64x3(float &x, float &y, float &z, float *xch) {
+// One token per lane over lanes 0..63 (warps 0 and 1, named barrier 1):
+// inclusive prefix sums of log alpha, log mu and the zero-mu count, and the
+// prefix products of the per-token maps (b, mubar) -> (alpha b + beta mu
+// mubar, mu mubar), i.e. upper-triangular 2 x 2 matrices [[a, c], [0, e]] =
+// [[alpha, beta mu], [0, mu]] composed later-times-earlier.  The matrix
+// products are taken within each segment of 16 tokens first (returned in
+// (fa, fc): for a token r of segment s they are F_s(r) = prod_{u=r0}^{r}
+// alpha_u and lambda_s(r)), then across segments; from the start (b_0 = 0,
+// mubar_0 = 1) the chunk-wide product's c entry is b_r.
+__device__ __forceinline__ void scan64_gates(float &A, float &U, float &Z, float &ta, float &tc,
+                                             float &te, float &fa, float &fc, float *xch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const float px = __shfl_up_sync(0xffffffffu, x, d);
-        const float py = __shfl_up_sync(0xffffffffu, y, d);
-        const float pz = __shfl_up_sync(0xffffffffu, z, d);
-        if (lane >= d) {
-            x += px;
-            y += py;
-            z += pz;
+    for (int d = 1; d < 16; d <<= 1) {
+        const float pA = __shfl_up_sync(0xffffffffu, A, d);
+        const float pU = __shfl_up_sync(0xffffffffu, U, d);
+        const float pZ = __shfl_up_sync(0xffffffffu, Z, d);
+        const float pa = __shfl_up_sync(0xffffffffu, ta, d);
+        const float pc = __shfl_up_sync(0xffffffffu, tc, d);
+        const float pe = __shfl_up_sync(0xffffffffu, te, d);
+        if ((lane & 15) >= d) {
+            A += pA;
+            U += pU;
+            Z += pZ;
+            tc = fmaf(ta, pc, tc * pe);
+            ta *= pa;
+            te *= pe;
         }
     }
+    fa = ta;
+    fc = tc;
+    // the second segment of each warp joins the first
+    {
+        const float qA = __shfl_sync(0xffffffffu, A, 15);
+        const float qU = __shfl_sync(0xffffffffu, U, 15);
+        const float qZ = __shfl_sync(0xffffffffu, Z, 15);
+        const float qa = __shfl_sync(0xffffffffu, ta, 15);
+        const float qc = __shfl_sync(0xffffffffu, tc, 15);
+        const float qe = __shfl_sync(0xffffffffu, te, 15);
+        if (lane >= 16) {
+            A += qA;
+            U += qU;
+            Z += qZ;
+            tc = fmaf(ta, qc, tc * qe);
+            ta *= qa;
+            te *= qe;
+        }
+    }
+    // warp 1 joins warp 0's total
     if (warp == 0 && lane == 31) {
-        xch[0] = x;
-        xch[1] = y;
-        xch[2] = z;
+        xch[0] = A; xch[1] = U; xch[2] = Z;
+        xch[3] = ta; xch[4] = tc; xch[5] = te;
     }
     asm volatile("bar.sync 1, 64;" ::: "memory");
     if (warp == 1) {
-        x += xch[0];
-        y += xch[1];
-        z += xch[2];
+        A += xch[0];
+        U += xch[1];
+        Z += xch[2];
+        tc = fmaf(ta, xch[4], tc * xch[5]);
+        ta *= xch[3];
+        te *= xch[5];
     }
 }
 
@@ -202,16 +239,21 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    // ---- gates and their log-space prefix scans (warps 0, 1)
+    // ---- gates, their log-space prefix scans, b and the segments' F and
+    //      lambda (warps 0, 1)
     if (warp < 2) {
         const int i = tid;
         const bool zmu = (g_mu == 0.f);
         float A = logf(g_a), U = zmu ? 0.f : logf(g_mu), Z = zmu ? 1.f : 0.f;
-        scan64x3(A, U, Z, vec + vScan * kChunk);
+        float ta = g_a, tc = g_be * g_mu, te = g_mu, fa, fc;
+        scan64_gates(A, U, Z, ta, tc, te, fa, fc, vec + vScan * kChunk);
         gate[i] = make_float4(g_a, g_be, g_mu, g_et);
         vec[vA * kChunk + i] = A;
         vec[vU * kChunk + i] = U;
         vec[vZ * kChunk + i] = Z;
+        vec[vB * kChunk + i] = tc;
+        vec[vF * kChunk + i] = fa;
+        vec[vLam * kChunk + i] = fc;
     }
     __syncthreads();
 
@@ -242,33 +284,15 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         // every warp but warp 1 (224 threads, named barrier 2) from here to L
         const int t7 = warp == 0 ? lane : tid - 32;
         if (warp == 0) {
-            // ---- b_i = alpha_i b_{i-1} + beta_i mubar_i and the carry vectors
-            //      that do not need Gamma, in this warp alone (tokens 2l, 2l+1
-            //      per lane): an affine prefix scan of the maps x -> a x + c,
-            //      composed pairwise first
+            // ---- the carry vectors that do not need Gamma (tokens 2l, 2l+1
+            //      per lane), to the prepared block
             const int i0 = 2 * lane, i1 = i0 + 1;
             const float4 g0 = gate[i0], g1 = gate[i1];
             const float A0 = vec[vA * kChunk + i0], A1 = vec[vA * kChunk + i1];
             const float U0 = vec[vU * kChunk + i0], U1 = vec[vU * kChunk + i1];
             const float Z0 = vec[vZ * kChunk + i0], Z1 = vec[vZ * kChunk + i1];
-            const float c0 = (Z0 == 0.f) ? g0.y * __expf(U0) : 0.f;
-            const float c1 = (Z1 == 0.f) ? g1.y * __expf(U1) : 0.f;
-            float ca = g1.x * g0.x, cb = g1.x * c0 + c1;          // the pair's map
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float pa = __shfl_up_sync(0xffffffffu, ca, d);
-                const float pb = __shfl_up_sync(0xffffffffu, cb, d);
-                if (lane >= d) {
-                    cb = ca * pb + cb;
-                    ca = ca * pa;
-                }
-            }
-            float bprev = __shfl_up_sync(0xffffffffu, cb, 1);     // b_{i0 - 1}
-            if (lane == 0) bprev = 0.f;
-            const float b0 = g0.x * bprev + c0, b1 = cb;
-            vec[vB * kChunk + i0] = b0;
-            vec[vB * kChunk + i1] = b1;
-            __syncwarp();
+            const float b0 = vec[vB * kChunk + i0], b1 = vec[vB * kChunk + i1];
+            const float bprev = lane == 0 ? 0.f : vec[vB * kChunk + i0 - 1];   // b_0 = 0
             const int last = n - 1;
             const float Al = vec[vA * kChunk + last], Ul = vec[vU * kChunk + last];
             const float Zl = vec[vZ * kChunk + last], bl = vec[vB * kChunk + last];
@@ -278,7 +302,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                     make_float2(v0 ? x0 : 0.f, v1 ? x1 : 0.f);
             };
             put2(kVecAbar, __expf(A0), __expf(A1));
-            put2(kVecBmA, bprev * g0.x, b0 * g1.x);               // b_0 = 0 before the first token
+            put2(kVecBmA, bprev * g0.x, b0 * g1.x);
             put2(kVecB, b0, b1);
             put2(kVecGM, (Zl == Z0) ? __expf(Ul - U0) * g0.w : 0.f,
                  (Zl == Z1) ? __expf(Ul - U1) * g1.w : 0.f);
@@ -287,23 +311,6 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 const float s0 = lane == 0 ? __expf(Al) : (lane == 1 ? ((Zl == 0.f) ? __expf(Ul) : 0.f) : 0.f);
                 const float s1 = lane == 0 ? bl : (lane == 1 ? (float)n : 0.f);
                 *reinterpret_cast<float2 *>(gv + kVecScal * kChunk + 2 * lane) = make_float2(s0, s1);
-            }
-            // ---- per segment s = 1..3 (rows r0 = 16 s ..): F_s(r) = prod of
-            //      alpha over [r0, r] and lambda_s(r) = alpha_r lambda_s(r-1) +
-            //      beta_r prod_{u=r0}^{r} mu_u (lambda_s(r0-1) = 0)
-            if (lane < 3) {
-                const int r0 = 16 * (lane + 1);
-                float F = 1.f, lam = 0.f, mt = 1.f;
-#pragma unroll 4
-                for (int rr = 0; rr < 16; ++rr) {
-                    const int r = r0 + rr;
-                    const float4 gr = gate[r];
-                    F *= gr.x;
-                    mt *= gr.z;
-                    lam = gr.x * lam + gr.y * mt;
-                    vec[vF * kChunk + r] = F;
-                    vec[vLam * kChunk + r] = lam;
-                }
             }
         } else if (warp == 2 || warp == 3) {
             // ---- Gt = Gamma Diag(eta) on the four diagonal 16-blocks: thread
