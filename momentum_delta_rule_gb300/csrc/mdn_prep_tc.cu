@@ -362,23 +362,29 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                                   vec[(vC + 1) * kChunk + j] * vec[vLam * kChunk + 47];
         }
         asm volatile("bar.sync 2, 224;" ::: "memory");
-        // ... then every other entry left of the diagonal blocks at once:
-        // segment 1 rows 16..30 x columns 0..15, segment 2 rows 32..46 x
-        // 0..31, segment 3 rows 48..63 x 0..47
-        for (int idx = t7; idx < 240 + 480 + 768; idx += kThreadsP - 32) {
-            int sg, rr, j;
-            if (idx < 240) {
-                sg = 1; rr = idx >> 4; j = idx & 15;
-            } else if (idx < 720) {
-                const int k = idx - 240;
-                sg = 2; rr = k >> 5; j = k & 31;
+        // ... then every other entry left of the diagonal blocks at once,
+        // one thread per (row, 8 columns): segment 1 rows 16..30 x 2 groups,
+        // segment 2 rows 32..46 x 4, segment 3 rows 48..63 x 6
+        if (t7 < 30 + 60 + 96) {
+            int sg, r, jg;
+            if (t7 < 30) {
+                sg = 1; r = 16 + (t7 >> 1); jg = t7 & 1;
+            } else if (t7 < 90) {
+                const int k = t7 - 30;
+                sg = 2; r = 32 + (k >> 2); jg = k & 3;
             } else {
-                const int k = idx - 720;
-                sg = 3; rr = k / 48; j = k - rr * 48;
+                const int k = t7 - 90;
+                sg = 3; r = 48 + k / 6; jg = k - (k / 6) * 6;
             }
-            const int r0 = 16 * sg, r = r0 + rr;
-            Gt[r * LM + j] = vec[vF * kChunk + r] * Gt[(r0 - 1) * LM + j] +
-                             vec[(vC + sg - 1) * kChunk + j] * vec[vLam * kChunk + r];
+            const int r0 = 16 * sg, j0 = 8 * jg;
+            const float F = vec[vF * kChunk + r], lam = vec[vLam * kChunk + r];
+            const float4 c0 = *reinterpret_cast<const float4 *>(vec + (vC + sg - 1) * kChunk + j0);
+            const float4 c1 = *reinterpret_cast<const float4 *>(vec + (vC + sg - 1) * kChunk + j0 + 4);
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const float *src = Gt + (r0 - 1) * LM + j0;
+            float *dst = Gt + r * LM + j0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = F * src[e] + c[e] * lam;
         }
     }
     __syncthreads();   // Gt complete
@@ -462,14 +468,15 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         const int blk = warp * 2 + (lane >> 4);
         const int c = lane & 15;
         const float *lb = Ldg + blk * 16 * LB;
+        // column c of (I + L_d)^{-1}: right-looking forward substitution,
+        // every row's update at step k independent of the others
         float t[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = 0.f;
+        for (int r = 0; r < 16; ++r) t[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int k = 0; k < r; ++k) acc += lb[r * LB + k] * t[k];
-            t[r] = (r < c) ? 0.f : ((r == c) ? 1.f : -acc);
-        }
+        for (int k = 0; k < 15; ++k)
+#pragma unroll
+            for (int r = k + 1; r < 16; ++r) t[r] = fmaf(-lb[r * LB + k], t[k], t[r]);
         asm volatile("bar.sync 1, 64;" ::: "memory");    // every lane has read its block of L
         float *db = Ldg + blk * 16 * LB;                  // D replaces L_d in place
 #pragma unroll
