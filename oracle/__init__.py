@@ -17,6 +17,6 @@ Contents
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 what the pages and the mathematics fix (special-case reductions, the
 two-step worked example, the block transition matrix and its spectrum, the
-second-order identity, brute force on tiny inputs).  Which pin covers which
-function is listed in DESIGN.md.
+second-order identity, brute force on tiny inputs); each test names the
+passage of the pages it follows.
 """
