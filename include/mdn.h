@@ -146,6 +146,47 @@ mdn_status mdn_chunk_fwd_vres(const void *q, const void *k, const void *v,
                               int H, int dk, int dv, mdn_dtype dtype, int chunk,
                               void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * mdn_chunk_state_slots — how many chunk slots the entry-state outputs of
+ * mdn_chunk_fwd_states must hold: B * ceil(T / 64) for equal-length batches
+ * (packed == 0, n_seq == B), floor(T_total / 64) + n_seq for packed
+ * sequences (packed != 0, T_total = B * T; an upper bound of
+ * sum_s ceil(L_s / 64)).  Returns 0 for negative sizes.
+ */
+size_t mdn_chunk_state_slots(int n_seq, int B, int T, int packed);
+
+/*
+ * mdn_chunk_fwd_states — mdn_chunk_fwd that also writes the entry states of
+ * every chunk: for chunk c of sequence s (its tokens 64 c .. 64 c + 63, the
+ * last chunk possibly shorter), the states after the sequence's first 64 c
+ * tokens, S_{64c} and M_{64c} (for c = 0 the initial states).  These are
+ * the chunk-boundary states the chunk carry of the slides' frame "Chunk
+ * outputs combine incoming states and local writes" (Eqs. (17)-(18)) passes
+ * on; a gradient pass can start every chunk from them instead of replaying
+ * the sequence.
+ *
+ * Arguments as mdn_chunk_fwd, plus
+ *   S_chunks, M_chunks  fp32 outputs [slots, H, dk, dv], slots at least
+ *          mdn_chunk_state_slots(...), both required when B * T > 0,
+ *          16-byte aligned, overlapping no other argument.  Chunk c of
+ *          sequence s sits at slot s * ceil(T / 64) + c (equal lengths) or
+ *          off_s + c with off_s = sum_{s' < s} ceil(L_{s'} / 64) (packed);
+ *          other slots are not written.
+ * Memory: 2 * dk * dv * 4 bytes per (chunk, head), 128 KiB at d = 128, i.e.
+ * 2 KiB per (token, head) against 768 B for that token's bf16 q, k and v.
+ * Errors: as mdn_chunk_fwd; MDN_ERR_INVALID_ARG for a missing, misaligned
+ * or aliasing state output.  o, S_T and M_T are the values mdn_chunk_fwd
+ * writes.
+ */
+mdn_status mdn_chunk_fwd_states(const void *q, const void *k, const void *v,
+                                const float *alpha, const float *mu, const float *eta,
+                                const float *beta, const float *S0, const float *M0,
+                                void *o, float *S_T, float *M_T, float *S_chunks,
+                                float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                                int B, int T, int H, int dk, int dv, mdn_dtype dtype,
+                                int chunk, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
 /* Implementation paths of mdn_chunk_fwd (reported by the profiled variant). */
 typedef enum mdn_path {
     MDN_PATH_CUDA_CORE = 0,   /* fp32 FFMA kernels: fp32 inputs, head size 64 */

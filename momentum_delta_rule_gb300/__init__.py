@@ -10,7 +10,10 @@ other code path.  If the library is missing, every call raises.
 Entry points (same names as the C ABI):
   chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
             cu_seqlens=None, ...)               -> (o, S_T, M_T)
-            (return_vres=True: (o, S_T, M_T, vres) via mdn_chunk_fwd_vres)
+            (return_vres=True: (o, S_T, M_T, vres) via mdn_chunk_fwd_vres;
+             return_chunk_states=True: (o, S_T, M_T, S_chunks, M_chunks)
+             via mdn_chunk_fwd_states)
+  chunk_state_slots(n_seq, B, T, packed)
   decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None) -> o
   prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
                  log_mu_min=-2.0, comba_d=0.0) -> (q_hat, k_hat, alpha, beta, mu, eta)
@@ -22,7 +25,8 @@ import os
 
 import torch
 
-__all__ = ["chunk_fwd", "decode_step", "prepare_inputs", "workspace_size", "device_status",
+__all__ = ["chunk_fwd", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
+           "device_status",
            "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
 
@@ -41,7 +45,8 @@ CHUNK = 64
 EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_workspace_size", "mdn_chunk_fwd",
                     "mdn_chunk_fwd_profiled", "mdn_chunk_fwd_static_ws",
-                    "mdn_chunk_fwd_vres", "mdn_prepare_inputs",
+                    "mdn_chunk_fwd_vres", "mdn_chunk_state_slots",
+                    "mdn_chunk_fwd_states", "mdn_prepare_inputs",
                     "mdn_decode_step", "mdn_get_device_status"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
@@ -83,6 +88,11 @@ def lib():
     L.mdn_chunk_fwd_vres.restype = c_int
     L.mdn_chunk_fwd_vres.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, vp, ip]
                                      + [c_int] * 8 + [vp, c_size, vp])
+    L.mdn_chunk_state_slots.restype = c_size
+    L.mdn_chunk_state_slots.argtypes = [c_int] * 4
+    L.mdn_chunk_fwd_states.restype = c_int
+    L.mdn_chunk_fwd_states.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, fp, fp, ip]
+                                       + [c_int] * 8 + [vp, c_size, vp])
     L.mdn_chunk_fwd_static_ws.restype = c_int
     L.mdn_chunk_fwd_static_ws.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, ip]
                                           + [c_int] * 8 + [vp])
@@ -147,7 +157,8 @@ def workspace_size(n_seq, T_total, H, D, dtype):
 def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
               cu_seqlens=None, o=None, S_T=None, M_T=None,
               output_final_state=True, workspace=None, stream=None,
-              stage_events=None, info=None, return_vres=False, vres=None):
+              stage_events=None, info=None, return_vres=False, vres=None,
+              return_chunk_states=False, S_chunks=None, M_chunks=None):
     """Prefill over whole sequences (``mdn_chunk_fwd``).
 
     q, k ``[B, T, H, D]`` and v ``[B, T, H, D]`` (fp32 or bf16, same dtype);
@@ -155,7 +166,10 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
     ``cu_seqlens`` int32 CUDA tensor ``[n_seq + 1]`` for packed sequences
     (then B == 1).  Returns ``(o, S_T, M_T)``; the states are None when
     ``output_final_state`` is False.  With ``return_vres`` (or a ``vres``
-    buffer shaped like v) the per-token residuals come fourth.
+    buffer shaped like v) the per-token residuals come fourth.  With
+    ``return_chunk_states`` (or ``S_chunks``/``M_chunks`` buffers of
+    ``[chunk_state_slots(...), H, D, D]`` fp32) the entry states of every
+    chunk come fourth and fifth (``mdn_chunk_fwd_states``).
     """
     L = lib()
     if q.dim() != 4:
@@ -201,6 +215,22 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
         _check_cuda("vres", vres, q.dtype, dev)
         if tuple(vres.shape) != (B, T, H, D):
             raise ValueError("vres must have the shape of v")
+    want_states = return_chunk_states or S_chunks is not None or M_chunks is not None
+    if want_states:
+        if want_vres or stage_events is not None or info is not None:
+            raise ValueError("the chunk states come alone, without residuals or stage events")
+        slots = chunk_state_slots(n_seq, B, T, cu_seqlens is not None)
+        for name in ("S_chunks", "M_chunks"):
+            t = S_chunks if name == "S_chunks" else M_chunks
+            if t is None:
+                t = torch.empty((max(slots, 1), H, D, D), dtype=torch.float32, device=dev)
+            _check_cuda(name, t, torch.float32, dev)
+            if t.dim() != 4 or t.shape[0] < slots or tuple(t.shape[1:]) != (H, D, D):
+                raise ValueError("%s must be [>= %d, H, D, D]" % (name, slots))
+            if name == "S_chunks":
+                S_chunks = t
+            else:
+                M_chunks = t
     need = int(L.mdn_chunk_fwd_workspace_size(n_seq, B * T, H, D, D, code))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
@@ -210,6 +240,11 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
             _ptr(cu_seqlens), n_seq, B, T, H, D, D, code, CHUNK,
             _ptr(workspace), workspace.numel(), _stream_handle(dev, stream))
     with torch.cuda.device(dev):
+        if want_states:
+            st = L.mdn_chunk_fwd_states(*(args[:12] + (_ptr(S_chunks), _ptr(M_chunks)) + args[12:]))
+            if st != MDN_OK:
+                raise MdnError(st, "mdn_chunk_fwd_states")
+            return o, S_T, M_T, S_chunks, M_chunks
         if want_vres:
             st = L.mdn_chunk_fwd_vres(*(args[:12] + (_ptr(vres),) + args[12:]))
             if st != MDN_OK:
@@ -232,6 +267,13 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
     if st != MDN_OK:
         raise MdnError(st, "mdn_chunk_fwd")
     return o, S_T, M_T
+
+
+def chunk_state_slots(n_seq, B, T, packed):
+    """Chunk slots the entry-state outputs need (``mdn_chunk_state_slots``):
+    chunk c of sequence s at slot s * ceil(T / 64) + c, or, packed, at
+    sum_{s' < s} ceil(L_s' / 64) + c."""
+    return int(lib().mdn_chunk_state_slots(int(n_seq), int(B), int(T), 1 if packed else 0))
 
 
 def decode_step(q, k, v, alpha, mu, eta, S, M, beta=None, o=None, stream=None):

@@ -105,6 +105,7 @@ mdn_status chunk_fwd_impl(
     const void *q, const void *k, const void *v, const float *alpha,
     const float *mu, const float *eta, const float *beta, const float *S0,
     const float *M0, void *o, float *S_T, float *M_T, void *vres,
+    float *S_chunks, float *M_chunks,
     const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
     mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
     void *stream, void *const *stage_events, int n_stage_events,
@@ -130,7 +131,7 @@ mdn_status chunk_fwd_impl(
     // ---- pointers
     if (!alpha || !mu || !eta) return MDN_ERR_INVALID_ARG;
     if (T_total > 0 && (!q || !k || !v || !o)) return MDN_ERR_INVALID_ARG;
-    const void *ptrs16[] = {q, k, v, o, S0, M0, S_T, M_T, vres};
+    const void *ptrs16[] = {q, k, v, o, S0, M0, S_T, M_T, vres, S_chunks, M_chunks};
     for (const void *ptr : ptrs16)
         if (ptr && !aligned16(ptr)) return MDN_ERR_INVALID_ARG;
     const void *ptrs4[] = {alpha, mu, eta, beta, cu_seqlens};
@@ -156,6 +157,7 @@ mdn_status chunk_fwd_impl(
     p.q = q; p.k = k; p.v = v;
     p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
     p.S0 = S0; p.M0 = M0; p.o = o; p.S_T = S_T; p.M_T = M_T; p.vres = vres;
+    p.S_chunks = S_chunks; p.M_chunks = M_chunks;
     p.cu_seqlens = cu_seqlens;
     p.n_seq = n_seq; p.B = B; p.T = T; p.H = H; p.D = dk;
     p.T_total = (int)T_total;
@@ -213,7 +215,7 @@ mdn_status mdn_chunk_fwd_profiled(
     mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
     void *stream, void *const *stage_events, int n_stage_events,
     int *path_out) {
-    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr,
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr, nullptr, nullptr,
                           cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
                           workspace_bytes, stream, stage_events, n_stage_events, path_out);
 }
@@ -225,7 +227,7 @@ mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,
                          const int32_t *cu_seqlens, int n_seq, int B, int T,
                          int H, int dk, int dv, mdn_dtype dtype, int chunk,
                          void *workspace, size_t workspace_bytes, void *stream) {
-    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr,
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr, nullptr, nullptr,
                           cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
                           workspace_bytes, stream, nullptr, 0, nullptr);
 }
@@ -239,9 +241,35 @@ mdn_status mdn_chunk_fwd_vres(const void *q, const void *k, const void *v,
                               void *workspace, size_t workspace_bytes, void *stream) {
     if ((long)B * T > 0 && !vres) return MDN_ERR_INVALID_ARG;
     if (vres && (vres == o || vres == v || vres == q || vres == k)) return MDN_ERR_INVALID_ARG;
-    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, vres,
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, vres, nullptr, nullptr,
                           cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
                           workspace_bytes, stream, nullptr, 0, nullptr);
+}
+
+size_t mdn_chunk_state_slots(int n_seq, int B, int T, int packed) {
+    if (n_seq < 0 || B < 0 || T < 0) return 0;
+    const long T_total = (long)B * T;
+    if (T_total > 0x7fffffffL) return 0;
+    if (packed) return (size_t)chunk_slots_bound(n_seq, (int)T_total);
+    return (size_t)B * (size_t)((T + mdn::kChunk - 1) / mdn::kChunk);
+}
+
+mdn_status mdn_chunk_fwd_states(const void *q, const void *k, const void *v,
+                                const float *alpha, const float *mu, const float *eta,
+                                const float *beta, const float *S0, const float *M0,
+                                void *o, float *S_T, float *M_T, float *S_chunks,
+                                float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                                int B, int T, int H, int dk, int dv, mdn_dtype dtype,
+                                int chunk, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    if ((long)B * T > 0 && (!S_chunks || !M_chunks)) return MDN_ERR_INVALID_ARG;
+    if (S_chunks && S_chunks == M_chunks) return MDN_ERR_INVALID_ARG;
+    const void *others[] = {q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T};
+    for (const void *ptr : others)
+        if (ptr && (ptr == S_chunks || ptr == M_chunks)) return MDN_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr,
+                          S_chunks, M_chunks, cu_seqlens, n_seq, B, T, H, dk, dv, dtype,
+                          chunk, workspace, workspace_bytes, stream, nullptr, 0, nullptr);
 }
 
 mdn_status mdn_prepare_inputs(const void *q_in, const void *k_in, const float *z_alpha,

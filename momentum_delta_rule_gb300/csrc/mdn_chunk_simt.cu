@@ -469,6 +469,16 @@ chunk_state_simt_kernel(ChunkProblem p) {
         const float *vg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffVec);
 
         __syncthreads();   // previous chunk finished with every buffer
+        if (p.S_chunks) {
+            // the entry state of this chunk, at its chunk slot
+            const size_t cs = ((size_t)(slot0 + c) * p.H + h) * D * D;
+            for (int idx = tid; idx < D * kNS; idx += kThreadsS) {
+                const int d = idx / kNS, cx = idx - d * kNS;
+                const size_t g = cs + (size_t)d * D + col0 + cx;
+                p.S_chunks[g] = Ss[idx];
+                p.M_chunks[g] = Ms[idx];
+            }
+        }
 #pragma unroll
         for (int idx = tid; idx < kChunk * D; idx += kThreadsS) {
             const int i = idx / D, d = idx - i * D;

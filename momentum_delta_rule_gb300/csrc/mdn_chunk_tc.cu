@@ -150,12 +150,26 @@ __device__ __forceinline__ void rescale_state(uint32_t st_s, uint32_t st_m, cons
     tmem_st_wait();
 }
 
+// One thread's 16 columns of row d of the entry state of chunk slot `slot`
+// (layout [slot, H, dk, dv]); `off` = d * dk + first column.
+__device__ __forceinline__ void store_chunk_state(const ChunkProblem &p, int slot, int h, size_t off,
+                                                  const float *S, const float *M) {
+    const size_t base = ((size_t)slot * p.H + h) * kD * kD + off;
+#pragma unroll
+    for (int j = 0; j < kEpiCols; j += 4) {
+        *reinterpret_cast<float4 *>(p.S_chunks + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        *reinterpret_cast<float4 *>(p.M_chunks + base + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
+    }
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int NS>
+// kChunkStates: also write the entry state of every chunk (a separate
+// instantiation, so the plain forward carries none of its registers).
+template <int NS, bool kChunkStates>
 __global__ void __launch_bounds__(Cfg<NS>::kThreads, 1)
 chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_q,
@@ -332,6 +346,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state);
+                if (kChunkStates) store_chunk_state(p, slot0, h, st_off - (size_t)sh * kD * kD, S, M);
             }
         }
         // Token rows: the lower 16 lanes of this warp's quadrant hold the K
@@ -445,8 +460,8 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             tc_fence_after();
             {
                 const bool more = c + 1 < nchunks;
+                float S[kEpiCols], M[kEpiCols];
                 if (more) {
-                    float S[kEpiCols], M[kEpiCols];
                     tmem_ld16(st_s, S);
                     tmem_ld16(st_m, M);
                     tmem_ld_wait();
@@ -460,6 +475,9 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                     if (more) mbar_arrive(&bars->state);
                     mbar_arrive(&bars->empty[st]);
                 }
+                // the next chunk's entry state, after the chain has moved on
+                if (kChunkStates && more)
+                    store_chunk_state(p, slot0 + c + 1, h, st_off - (size_t)sh * kD * kD, S, M);
             }
             // ---- outputs of this chunk (off the critical path)
             if (in_chunk) {
@@ -524,11 +542,11 @@ bool make_map(CUtensorMap *map, const void *base, int T_total, int H, bool swizz
     return r == CUDA_SUCCESS;
 }
 
-template <int NS>
+template <int NS, bool kChunkStates>
 cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const CUtensorMap &mk,
                               const CUtensorMap &mq, const CUtensorMap &mv) {
     using C = Cfg<NS>;
-    auto kern = chunk_state_tc_kernel<NS>;
+    auto kern = chunk_state_tc_kernel<NS, kChunkStates>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)C::kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -580,9 +598,16 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
         return cudaErrorInvalidValue;
     const long chains = (long)p.n_seq * p.H;
     const int sms = sm_count();
-    if (sms > 0 && chains * Cfg<16>::kSlices <= sms) return launch_state_tc_t<16>(p, st, mk, mq, mv);
-    if (sms > 0 && chains * Cfg<32>::kSlices <= sms) return launch_state_tc_t<32>(p, st, mk, mq, mv);
-    return launch_state_tc_t<64>(p, st, mk, mq, mv);
+    const int ns = (sms > 0 && chains * Cfg<16>::kSlices <= sms) ? 16
+                 : (sms > 0 && chains * Cfg<32>::kSlices <= sms) ? 32 : 64;
+    if (p.S_chunks) {
+        if (ns == 16) return launch_state_tc_t<16, true>(p, st, mk, mq, mv);
+        if (ns == 32) return launch_state_tc_t<32, true>(p, st, mk, mq, mv);
+        return launch_state_tc_t<64, true>(p, st, mk, mq, mv);
+    }
+    if (ns == 16) return launch_state_tc_t<16, false>(p, st, mk, mq, mv);
+    if (ns == 32) return launch_state_tc_t<32, false>(p, st, mk, mq, mv);
+    return launch_state_tc_t<64, false>(p, st, mk, mq, mv);
 }
 
 }  // namespace mdn

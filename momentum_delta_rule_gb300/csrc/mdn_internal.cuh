@@ -69,6 +69,7 @@ struct ChunkProblem {
     void *o;
     float *S_T, *M_T;
     void *vres;                  // per-token residuals like v, or nullptr
+    float *S_chunks, *M_chunks;  // entry states of every chunk [slot, H, dk, dv], or nullptr
     const int32_t *cu_seqlens;   // device, or nullptr for equal lengths
     int n_seq, B, T, H, D;       // dk == dv == D
     int T_total;                 // B * T

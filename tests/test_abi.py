@@ -157,3 +157,44 @@ def test_binding_requires_cuda_tensors():
     g = torch.zeros(1, 64, 1)
     with pytest.raises(ValueError):
         mdn.chunk_fwd(x, x, x, g, g, g)
+
+
+def _chunk_states(L, Sc, Mc, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
+                beta=None, S0=None, M0=None, o=FAKE, S_T=None, M_T=None,
+                cu=None, n_seq=2, B=2, T=64, H=2, dk=128, dv=128, dtype=1,
+                chunk=64, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    return L.mdn_chunk_fwd_states(args["q"], args["k"], args["v"], args["alpha"],
+                                  args["mu"], args["eta"], args["beta"], args["S0"],
+                                  args["M0"], args["o"], args["S_T"], args["M_T"], Sc, Mc,
+                                  args["cu"], args["n_seq"], args["B"], args["T"],
+                                  args["H"], args["dk"], args["dv"], args["dtype"],
+                                  args["chunk"], args["ws"], args["ws_bytes"],
+                                  args["stream"])
+
+
+SC, MC = ctypes.c_void_p(0x50000), ctypes.c_void_p(0x60000)
+
+
+@pytest.mark.parametrize("Sc,Mc,over,code", [
+    (None, MC, {}, 1),                               # both required when tokens exist
+    (SC, None, {}, 1),
+    (SC, SC, {}, 1),                                 # the same buffer twice
+    (FAKE, MC, {}, 1),                               # aliases the inputs
+    (ctypes.c_void_p(0x50008), MC, {}, 1),           # not 16-byte aligned
+    (SC, MC, dict(S0=MC), 1),                        # aliases an initial state
+    (SC, MC, dict(chunk=32), 2),                     # the rest as mdn_chunk_fwd
+    (SC, MC, dict(q=None), 1),
+])
+def test_chunk_fwd_states_rejects(L, Sc, Mc, over, code):
+    assert _chunk_states(L, Sc, Mc, **over) == code
+
+
+def test_chunk_state_slots(L):
+    # equal lengths: B * ceil(T / 64); packed: floor(T_total / 64) + n_seq
+    assert mdn.chunk_state_slots(2, 2, 130, False) == 6
+    assert mdn.chunk_state_slots(4, 4, 64, False) == 4
+    assert mdn.chunk_state_slots(0, 0, 0, False) == 0
+    assert mdn.chunk_state_slots(3, 1, 300, True) == 300 // 64 + 3
+    assert mdn.chunk_state_slots(-1, 1, 10, False) == 0
