@@ -55,6 +55,25 @@ def test_mu_zero_and_beta_zero():
     compare(x, gpu_chunk_fwd(x), chains(x))
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp32", 128)])
+def test_gate_extremes(dtype, D):
+    """Gates at the ends of their ranges: alpha down to 1e-4 (the chunk's
+    alpha product underflows fp32 well inside a chunk), mu = 1 exactly over
+    whole chunks (momentum never decays), mu = 0 runs, eta up to 2, beta up
+    to 3, and tokens with alpha = 1 and eta = 0 (no write at all)."""
+    w = W.Workload("gate_edges", dtype=dtype, state="randn", seed=15)
+    x = W.make_prefill(w, B=2, T=260, H=2, D=D, with_beta=True)
+    g = torch.Generator().manual_seed(16)
+    x["alpha"][:, 0:40] = 10.0 ** (-4.0 * torch.rand(x["alpha"][:, 0:40].shape, generator=g))
+    x["mu"][:, 64:192] = 1.0
+    x["mu"][:, 200:210] = 0.0
+    x["eta"][:, 120:180] = 2.0 * torch.rand(x["eta"][:, 120:180].shape, generator=g)
+    x["beta"][:, 150:230] = 3.0 * torch.rand(x["beta"][:, 150:230].shape, generator=g)
+    x["alpha"][:, 240:250] = 1.0
+    x["eta"][:, 240:250] = 0.0
+    compare(x, gpu_chunk_fwd(x), chains(x))
+
+
 def test_state_alias_and_optional_states():
     import momentum_delta_rule_gb300 as mdn
     w = W.Workload("alias", dtype="bf16", state="randn", seed=13)
