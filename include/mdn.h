@@ -22,6 +22,11 @@
  *  - All device work is enqueued on `stream` (a cudaStream_t; NULL means the
  *    legacy default stream) and runs asynchronously; a call returns as soon as
  *    its kernels are enqueued.
+ *  - The enqueueing calls (mdn_chunk_fwd and its variants, mdn_decode_step,
+ *    mdn_prepare_inputs) may be captured into a CUDA graph once one call has
+ *    run on the device (the first call looks up the device's status word with
+ *    cudaGetSymbolAddress); a replay reads the pointers given at capture.
+ *    mdn_get_device_status synchronises and must not be captured.
  *  - Gates and states are fp32.  q, k, v, o share one element type `dtype`.
  *    Accumulation is fp32.  Inputs are never modified (except the in-place
  *    states of mdn_decode_step).
