@@ -107,7 +107,7 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
  *
  * Arguments
  *   q, k, v        inputs (dtype)
- *   alpha, mu, eta gates (fp32), required
+ *   alpha, mu, eta gates (fp32), required when B * T > 0
  *   beta           step gate (fp32) or NULL for beta = 1
  *   S0, M0         initial states or NULL for zero (each independently)
  *   o              output (dtype), written for every token

@@ -129,7 +129,7 @@ mdn_status chunk_fwd_impl(
     if (T_total > 0x7fffffffL / 2) return MDN_ERR_INVALID_ARG;
     if ((long)T_total * H * dk > 0x7fffffffffffL) return MDN_ERR_INVALID_ARG;
     // ---- pointers
-    if (!alpha || !mu || !eta) return MDN_ERR_INVALID_ARG;
+    if (T_total > 0 && (!alpha || !mu || !eta)) return MDN_ERR_INVALID_ARG;
     if (T_total > 0 && (!q || !k || !v || !o)) return MDN_ERR_INVALID_ARG;
     const void *ptrs16[] = {q, k, v, o, S0, M0, S_T, M_T, vres, S_chunks, M_chunks};
     for (const void *ptr : ptrs16)

@@ -198,3 +198,10 @@ def test_chunk_state_slots(L):
     assert mdn.chunk_state_slots(0, 0, 0, False) == 0
     assert mdn.chunk_state_slots(3, 1, 300, True) == 300 // 64 + 3
     assert mdn.chunk_state_slots(-1, 1, 10, False) == 0
+
+
+def test_chunk_fwd_accepts_null_tensors_without_tokens(L):
+    # no tokens: q, k, v, o and the gates may be null (empty tensors); the
+    # call is not an argument error (it needs a device to go further)
+    st = _chunk(L, q=None, k=None, v=None, o=None, alpha=None, mu=None, eta=None, T=0)
+    assert st != mdn.MDN_ERR_INVALID_ARG
