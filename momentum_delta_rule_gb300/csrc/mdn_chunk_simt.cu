@@ -504,18 +504,25 @@ chunk_state_simt_kernel(ChunkProblem p) {
         for (int idx = tid; idx < kVecRows * kChunk; idx += kThreadsS) vec[idx] = vg[idx];
         __syncthreads();
 
-        // ---- K S_0, K M_0, Q S_0, Q M_0 for 8 token rows x 1 column
+        // ---- K S_0, K M_0, Q S_0, Q M_0 for kRowsA token rows x 1 column;
+        //      the K and Q rows (the same for the whole warp) four at a time
         float ks[kRowsA] = {}, km[kRowsA] = {}, qs[kRowsA] = {}, qm[kRowsA] = {};
-        for (int d = 0; d < D; ++d) {
-            const float sv = Ss[d * kNS + cc], mv = Ms[d * kNS + cc];
+        for (int d = 0; d < D; d += 4) {
+            float sv[4], mv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                sv[u] = Ss[(d + u) * kNS + cc];
+                mv[u] = Ms[(d + u) * kNS + cc];
+            }
 #pragma unroll
             for (int r = 0; r < kRowsA; ++r) {
                 const int i = wg * kRowsA + r;
-                const float kv = Ks[i * D + d], qv = Qs[i * D + d];
-                ks[r] += kv * sv;
-                km[r] += kv * mv;
-                qs[r] += qv * sv;
-                qm[r] += qv * mv;
+                const float4 kv = *reinterpret_cast<const float4 *>(Ks + i * D + d);
+                const float4 qv = *reinterpret_cast<const float4 *>(Qs + i * D + d);
+                ks[r] += kv.x * sv[0] + kv.y * sv[1] + kv.z * sv[2] + kv.w * sv[3];
+                km[r] += kv.x * mv[0] + kv.y * mv[1] + kv.z * mv[2] + kv.w * mv[3];
+                qs[r] += qv.x * sv[0] + qv.y * sv[1] + qv.z * sv[2] + qv.w * sv[3];
+                qm[r] += qv.x * mv[0] + qv.y * mv[1] + qv.z * mv[2] + qv.w * mv[3];
             }
         }
         float oint[kRowsA];
@@ -528,16 +535,38 @@ chunk_state_simt_kernel(ChunkProblem p) {
         }
         __syncthreads();
 
-        // ---- residuals Vres = T R, outputs O = O_inter + (A_O T) R
+        // ---- residuals Vres = T R, outputs O = O_inter + (A_O T) R: the
+        //      warp's rows i0 .. i0 + kRowsA - 1 share every R column j < i0
+        //      (read once, four at a time with the rows of T and A_O T), then
+        //      the triangle j = i0 .. i
+        static_assert(kRowsA == 4, "four token rows per warp");
+        const int i0 = wg * kRowsA;
+        float vrr[kRowsA] = {}, oir[kRowsA] = {};
+        for (int j = 0; j < i0; j += 4) {
+            float rv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) rv[u] = Rs[(j + u) * kNS + cc];
+#pragma unroll
+            for (int r = 0; r < kRowsA; ++r) {
+                const float4 tv = *reinterpret_cast<const float4 *>(Ts + (i0 + r) * kChunk + j);
+                const float4 av = *reinterpret_cast<const float4 *>(AOTs + (i0 + r) * kChunk + j);
+                vrr[r] += tv.x * rv[0] + tv.y * rv[1] + tv.z * rv[2] + tv.w * rv[3];
+                oir[r] += av.x * rv[0] + av.y * rv[1] + av.z * rv[2] + av.w * rv[3];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRowsA; ++u) {
+            const float rv = Rs[(i0 + u) * kNS + cc];
+#pragma unroll
+            for (int r = u; r < kRowsA; ++r) {
+                vrr[r] += Ts[(i0 + r) * kChunk + i0 + u] * rv;
+                oir[r] += AOTs[(i0 + r) * kChunk + i0 + u] * rv;
+            }
+        }
 #pragma unroll
         for (int r = 0; r < kRowsA; ++r) {
-            const int i = wg * kRowsA + r;
-            float vr = 0.f, oi = 0.f;
-            for (int j = 0; j <= i; ++j) {
-                const float rv = Rs[j * kNS + cc];
-                vr += Ts[i * kChunk + j] * rv;
-                oi += AOTs[i * kChunk + j] * rv;
-            }
+            const int i = i0 + r;
+            const float vr = vrr[r], oi = oir[r];
             Vr[i * kNS + cc] = vr;
             if (i < n) og0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(oint[r] + oi);
             if (rg0 && i < n) rg0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(vr);
@@ -550,19 +579,28 @@ chunk_state_simt_kernel(ChunkProblem p) {
         const float abar_n = vec[kVecScal * kChunk + 0];
         const float b_n = vec[kVecScal * kChunk + 1];
         const float mubar_n = vec[kVecScal * kChunk + 2];
-#pragma unroll 4
-        for (int r = 0; r < kRowsC; ++r) {
-            const int d = wg * kRowsC + r;
-            float as = 0.f, am = 0.f;
-            for (int i = 0; i < n; ++i) {
-                const float kv = Ks[i * D + d];
-                const float vv = Vr[i * kNS + cc];
-                as += kv * (vec[kVecGS * kChunk + i] * vv);
-                am += kv * (vec[kVecGM * kChunk + i] * vv);
+        // the warp's kRowsC state rows d0 .. d0 + kRowsC - 1 at once: per
+        // token, its weighted residuals once and the K row four at a time
+        static_assert(kRowsC % 4 == 0, "state rows per warp");
+        const int d0 = wg * kRowsC;
+        float as[kRowsC] = {}, am[kRowsC] = {};
+        for (int i = 0; i < n; ++i) {
+            const float vv = Vr[i * kNS + cc];
+            const float gsv = vec[kVecGS * kChunk + i] * vv;
+            const float gmv = vec[kVecGM * kChunk + i] * vv;
+#pragma unroll
+            for (int r = 0; r < kRowsC; r += 4) {
+                const float4 kv = *reinterpret_cast<const float4 *>(Ks + i * D + d0 + r);
+                as[r] += kv.x * gsv; as[r + 1] += kv.y * gsv; as[r + 2] += kv.z * gsv; as[r + 3] += kv.w * gsv;
+                am[r] += kv.x * gmv; am[r + 1] += kv.y * gmv; am[r + 2] += kv.z * gmv; am[r + 3] += kv.w * gmv;
             }
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsC; ++r) {
+            const int d = d0 + r;
             const float so = Ss[d * kNS + cc], mo = Ms[d * kNS + cc];
-            Ss[d * kNS + cc] = abar_n * so - b_n * mo + as;
-            Ms[d * kNS + cc] = mubar_n * mo - am;
+            Ss[d * kNS + cc] = abar_n * so - b_n * mo + as[r];
+            Ms[d * kNS + cc] = mubar_n * mo - am[r];
         }
     }
     __syncthreads();
