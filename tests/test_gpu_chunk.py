@@ -142,6 +142,16 @@ def test_varlen_packed_full_size_sampled():
     compare(x, out, _sample(x, 4) + [shortest])
 
 
+def test_very_long_sequence_sampled():
+    """One sequence of 131072 tokens: a chain of 2048 chunks, eight times the
+    longest benchmark sequence; one head compared in full against the
+    oracle, so error growth along the chain would show."""
+    w = W.Workload("very_long", dtype="bf16", state="randn", seed=17)
+    x = W.make_prefill(w, B=1, T=131072, H=2, D=128)
+    out = gpu_chunk_fwd(x)
+    compare(x, out, chains(x)[:1])
+
+
 def test_path_selection():
     """bf16 inputs with head size 128 run on the tensor-core path; fp32 inputs
     and head size 64 on the CUDA-core path."""
