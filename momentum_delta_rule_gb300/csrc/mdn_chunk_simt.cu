@@ -25,6 +25,8 @@
 // alpha_i) K, so the state pass needs only K S_0 and K M_0.  Writing
 // R = V - Diag(abar) K S_0 + Diag(b_{i-1} alpha_i) K M_0, the residuals are
 // Vres = T R and the in-chunk output term is (A_O T) R.
+#include <type_traits>
+
 #include "mdn_internal.cuh"
 
 namespace mdn {
@@ -411,9 +413,21 @@ struct StateSmem {
                                  + 2 * kChunk * kChunk   // T, AOT
                                  + kVecRows * kChunk     // vectors
                                  + 2 * D * kNS           // S, M slices
-                                 + 2 * kChunk * kNS;     // R, scaled residuals
+                                 + 2 * kChunk * kNS      // R, scaled residuals
+                                 + kChunk * D            // the next chunk's K
+                                 + kVecRows * kChunk;    // ... and vectors
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
+
+// 16-byte asynchronous copy global -> shared; src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <int D, typename Tin>
 __global__ void __launch_bounds__(kThreadsS)
@@ -439,6 +453,13 @@ chunk_state_simt_kernel(ChunkProblem p) {
     float *Ms = Ss + D * kNS;
     float *Rs = Ms + D * kNS;
     float *Vr = Rs + kChunk * kNS;
+    float *Kalt = Vr + kChunk * kNS;           // the next chunk's K ...
+    float *vecalt = Kalt + kChunk * D;         // ... and vectors
+    // fp32 inputs are copied as they are, so the next chunk's tiles stream in
+    // with asynchronous copies while this chunk computes (K and the vectors
+    // double-buffered, Q and V once the residuals are formed, T and A_O T once
+    // the outputs are); bf16 inputs are converted by plain loads per chunk.
+    constexpr bool kAsync = std::is_same<Tin, float>::value;
 
     int start, len, slot0;
     sequence_range(p, s, start, len, slot0);
@@ -460,6 +481,50 @@ chunk_state_simt_kernel(ChunkProblem p) {
     Tin *og0 = static_cast<Tin *>(p.o) + (size_t)h * D + col0;
     Tin *rg0 = p.vres ? static_cast<Tin *>(p.vres) + (size_t)h * D + col0 : nullptr;
 
+    // asynchronous copies of chunk cn's tiles (fp32 inputs only); rows past
+    // the chunk end are zero-filled
+    auto rows_of = [&](int cn, int &t0n, int &nn) {
+        t0n = start + cn * kChunk;
+        nn = min(kChunk, len - cn * kChunk);
+    };
+    auto copy_kq = [&](int cn, float *dst, const Tin *src0) {
+        int t0n, nn;
+        rows_of(cn, t0n, nn);
+        for (int idx = tid; idx < kChunk * D / 4; idx += kThreadsS) {
+            const int i = idx / (D / 4), q4 = idx - i * (D / 4);
+            const bool v = i < nn;
+            const Tin *src = src0 + (size_t)(t0n + (v ? i : 0)) * rs + 4 * q4;
+            cp_async16(dst + i * D + 4 * q4, src, v ? 16u : 0u);
+        }
+    };
+    auto copy_v = [&](int cn) {
+        int t0n, nn;
+        rows_of(cn, t0n, nn);
+        for (int idx = tid; idx < kChunk * kNS / 4; idx += kThreadsS) {
+            const int i = idx / (kNS / 4), q4 = idx - i * (kNS / 4);
+            const bool v = i < nn;
+            const Tin *src = vg0 + (size_t)(t0n + (v ? i : 0)) * rs + 4 * q4;
+            cp_async16(Vs + i * kNS + 4 * q4, src, v ? 16u : 0u);
+        }
+    };
+    auto block_of = [&](int cn) {
+        return p.prep + ((size_t)(slot0 + cn) * p.H + h) * p.prep_stride;
+    };
+    auto copy_floats = [&](float *dst, const unsigned char *src, int nfloats) {
+        for (int idx = tid; idx < nfloats / 4; idx += kThreadsS)
+            cp_async16(dst + 4 * idx, src + 16 * (size_t)idx, 16u);
+    };
+    if (kAsync && nchunks > 0) {
+        const unsigned char *b0 = block_of(0);
+        copy_kq(0, Ks, kg0);
+        copy_kq(0, Qs, qg0);
+        copy_v(0);
+        copy_floats(Ts, b0 + PrepLayout<float>::kOffT, kChunk * kChunk);
+        copy_floats(AOTs, b0 + PrepLayout<float>::kOffAOT, kChunk * kChunk);
+        copy_floats(vec, b0 + PrepLayout<float>::kOffVec, kVecRows * kChunk);
+        cp_async_commit();
+    }
+
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = start + c * kChunk;
         const int n = min(kChunk, len - c * kChunk);
@@ -468,6 +533,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
         const float *AOTg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffAOT);
         const float *vg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffVec);
 
+        if (kAsync) cp_async_wait_all();   // this chunk's tiles have landed
         __syncthreads();   // previous chunk finished with every buffer
         if (p.S_chunks) {
             // the entry state of this chunk, at its chunk slot
@@ -479,29 +545,31 @@ chunk_state_simt_kernel(ChunkProblem p) {
                 p.M_chunks[g] = Ms[idx];
             }
         }
+        if (!kAsync) {
 #pragma unroll
-        for (int idx = tid; idx < kChunk * D; idx += kThreadsS) {
-            const int i = idx / D, d = idx - i * D;
-            float kv = 0.f, qv = 0.f;
-            if (i < n) {
-                kv = to_f32(kg0[(size_t)(t0 + i) * rs + d]);
-                qv = to_f32(qg0[(size_t)(t0 + i) * rs + d]);
+            for (int idx = tid; idx < kChunk * D; idx += kThreadsS) {
+                const int i = idx / D, d = idx - i * D;
+                float kv = 0.f, qv = 0.f;
+                if (i < n) {
+                    kv = to_f32(kg0[(size_t)(t0 + i) * rs + d]);
+                    qv = to_f32(qg0[(size_t)(t0 + i) * rs + d]);
+                }
+                Ks[idx] = kv;
+                Qs[idx] = qv;
             }
-            Ks[idx] = kv;
-            Qs[idx] = qv;
-        }
 #pragma unroll
-        for (int idx = tid; idx < kChunk * kNS; idx += kThreadsS) {
-            const int i = idx / kNS, cx = idx - i * kNS;
-            Vs[idx] = (i < n) ? to_f32(vg0[(size_t)(t0 + i) * rs + cx]) : 0.f;
-        }
+            for (int idx = tid; idx < kChunk * kNS; idx += kThreadsS) {
+                const int i = idx / kNS, cx = idx - i * kNS;
+                Vs[idx] = (i < n) ? to_f32(vg0[(size_t)(t0 + i) * rs + cx]) : 0.f;
+            }
 #pragma unroll
-        for (int idx = tid; idx < kChunk * kChunk; idx += kThreadsS) {
-            Ts[idx] = Tg[idx];
-            AOTs[idx] = AOTg[idx];
-        }
+            for (int idx = tid; idx < kChunk * kChunk; idx += kThreadsS) {
+                Ts[idx] = Tg[idx];
+                AOTs[idx] = AOTg[idx];
+            }
 #pragma unroll
-        for (int idx = tid; idx < kVecRows * kChunk; idx += kThreadsS) vec[idx] = vg[idx];
+            for (int idx = tid; idx < kVecRows * kChunk; idx += kThreadsS) vec[idx] = vg[idx];
+        }
         __syncthreads();
 
         // ---- K S_0, K M_0, Q S_0, Q M_0 for kRowsA token rows x 1 column;
@@ -534,6 +602,13 @@ chunk_state_simt_kernel(ChunkProblem p) {
             oint[r] = vec[kVecAbar * kChunk + i] * qs[r] - vec[kVecB * kChunk + i] * qm[r];
         }
         __syncthreads();
+        if (kAsync && c + 1 < nchunks) {
+            // Q and V are free now; K and the vectors go to the other buffers
+            copy_kq(c + 1, Qs, qg0);
+            copy_v(c + 1);
+            copy_kq(c + 1, Kalt, kg0);
+            copy_floats(vecalt, block_of(c + 1) + PrepLayout<float>::kOffVec, kVecRows * kChunk);
+        }
 
         // ---- residuals Vres = T R, outputs O = O_inter + (A_O T) R: the
         //      warp's rows i0 .. i0 + kRowsA - 1 share every R column j < i0
@@ -572,6 +647,13 @@ chunk_state_simt_kernel(ChunkProblem p) {
             if (rg0 && i < n) rg0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(vr);
         }
         __syncthreads();
+        if (kAsync && c + 1 < nchunks) {
+            // T and A_O T are free now
+            const unsigned char *bn = block_of(c + 1);
+            copy_floats(Ts, bn + PrepLayout<float>::kOffT, kChunk * kChunk);
+            copy_floats(AOTs, bn + PrepLayout<float>::kOffAOT, kChunk * kChunk);
+            cp_async_commit();
+        }
 
         // ---- carry, both from the old S_0, M_0:
         //      S <- abar_n S - b_n M + sum_i k_i gamma_{n,i} eta_i vres_i^T
@@ -601,6 +683,10 @@ chunk_state_simt_kernel(ChunkProblem p) {
             const float so = Ss[d * kNS + cc], mo = Ms[d * kNS + cc];
             Ss[d * kNS + cc] = abar_n * so - b_n * mo + as[r];
             Ms[d * kNS + cc] = mubar_n * mo - am[r];
+        }
+        if (kAsync) {               // the next chunk's K and vectors are in the other buffers
+            float *t = Ks; Ks = Kalt; Kalt = t;
+            t = vec; vec = vecalt; vecalt = t;
         }
     }
     __syncthreads();
