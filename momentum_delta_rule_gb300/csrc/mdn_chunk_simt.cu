@@ -97,8 +97,11 @@ template <int D>
 struct PrepSmem {
     static constexpr int LD = D + 1;          // padded row stride of K, Q
     static constexpr int LM = kChunk + 1;     // padded row stride of 64x64
-    static constexpr int kFloats =
-        2 * kChunk * LD + 4 * kChunk * LM + 12 * kChunk + 64;
+    // K and Q are read only by the Gram products; L, T and A_O take their
+    // place afterwards, so that two (d = 128) or three (d = 64) CTAs share an SM
+    static constexpr int kKQ = 2 * kChunk * LD, kLTA = 3 * kChunk * LM;
+    static constexpr int kShared = kKQ > kLTA ? kKQ : kLTA;
+    static constexpr int kFloats = kShared + kChunk * LM + 12 * kChunk + 64;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
@@ -152,13 +155,13 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     const int tid = threadIdx.x;
 
     extern __shared__ float smem[];
-    float *Ks = smem;                      // [64][LD]
-    float *Qs = Ks + kChunk * LD;          // [64][LD]
-    float *G = Qs + kChunk * LD;           // Gamma [64][LM]
-    float *L = G + kChunk * LM;            // system matrix (strict lower)
+    float *Ks = smem;                      // [64][LD], until the Gram products
+    float *Qs = Ks + kChunk * LD;          // [64][LD], until the Gram products
+    float *L = smem;                       // system matrix (strict lower), after them
     float *Tm = L + kChunk * LM;           // its inverse
     float *AO = Tm + kChunk * LM;          // output operator (lower)
-    float *va = AO + kChunk * LM;          // alpha
+    float *G = smem + SM::kShared;         // Gamma [64][LM]
+    float *va = G + kChunk * LM;           // alpha
     float *vb = va + kChunk;               // beta
     float *ve = vb + kChunk;               // eta
     float *vA = ve + kChunk;               // A_i = sum log alpha
@@ -250,6 +253,7 @@ chunk_prep_simt_kernel(ChunkProblem p) {
                     gq[r][c] += qr[r] * kc[c];
                 }
         }
+        __syncthreads();   // every thread is done with K and Q: L, T, A_O replace them
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
