@@ -33,7 +33,7 @@ namespace mdn {
 namespace {
 
 constexpr int kThreads = 256;     // prep
-constexpr int kThreadsS = 512;    // state pass: 16 warps, 4 token rows and D/16 state rows each
+// state pass: 16 row groups of 4 token rows and D/16 state rows, x 32 or 64 columns
 
 // ------------------------------------------------------------- offsets
 
@@ -408,18 +408,20 @@ chunk_prep_simt_kernel(ChunkProblem p) {
 
 // --------------------------------------------------------------- state
 
-constexpr int kNS = 32;   // state columns per CTA
-
-template <int D>
+// The state pass runs 16 row groups x NSC state columns per CTA (NSC = 32:
+// 512 threads; NSC = 64: 1024 threads, so that fp32 prefills with many
+// (sequence, head) chains at d = 128 fit the GPU in one wave).  With
+// NSC = 32 the next chunk's K and vectors are double-buffered.
+template <int D, int NSC>
 struct StateSmem {
+    static constexpr bool kPrefetchK = NSC == 32;
     static constexpr int kFloats = 2 * kChunk * D        // K, Q
-                                 + kChunk * kNS          // V slice
+                                 + kChunk * NSC          // V slice
                                  + 2 * kChunk * kChunk   // T, AOT
                                  + kVecRows * kChunk     // vectors
-                                 + 2 * D * kNS           // S, M slices
-                                 + 2 * kChunk * kNS      // R, scaled residuals
-                                 + kChunk * D            // the next chunk's K
-                                 + kVecRows * kChunk;    // ... and vectors
+                                 + 2 * D * NSC           // S, M slices
+                                 + 2 * kChunk * NSC      // R, scaled residuals
+                                 + (kPrefetchK ? kChunk * D + kVecRows * kChunk : 0);
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
@@ -433,17 +435,22 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-template <int D, typename Tin>
-__global__ void __launch_bounds__(kThreadsS)
+template <int D, typename Tin, int NSC>
+__global__ void __launch_bounds__(16 * NSC)
 chunk_state_simt_kernel(ChunkProblem p) {
+    constexpr int kNS = NSC;                            // state columns of this CTA
+    constexpr int kThreadsS = 16 * NSC;                 // 16 row groups x kNS columns
     constexpr int kSlices = D / kNS;
-    constexpr int kRowsA = kChunk / (kThreadsS / 32);   // token rows per warp
-    constexpr int kRowsC = D / (kThreadsS / 32);        // state rows per warp
+    constexpr int kRowsA = kChunk / 16;                 // token rows per row group
+    constexpr int kRowsC = D / 16;                      // state rows per row group
     const int slice = blockIdx.x % kSlices;
     const int kh = blockIdx.x / kSlices;
     const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
     const int sh = s * p.H + h;
-    const int tid = threadIdx.x, cc = tid & 31, wg = tid >> 5;
+    // thread = (row group wg, column cc); a warp is 32 adjacent columns of one
+    // row group, so the row group's K, Q and T rows are warp-wide broadcasts
+    const int tid = threadIdx.x;
+    const int cc = ((tid >> 5) % (kNS / 32)) * 32 + (tid & 31), wg = (tid >> 5) / (kNS / 32);
     const int col0 = slice * kNS;
 
     extern __shared__ float smem[];
@@ -464,6 +471,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
     // double-buffered, Q and V once the residuals are formed, T and A_O T once
     // the outputs are); bf16 inputs are converted by plain loads per chunk.
     constexpr bool kAsync = std::is_same<Tin, float>::value;
+    constexpr bool kPrefK = kAsync && StateSmem<D, NSC>::kPrefetchK;
 
     int start, len, slot0;
     sequence_range(p, s, start, len, slot0);
@@ -539,6 +547,14 @@ chunk_state_simt_kernel(ChunkProblem p) {
 
         if (kAsync) cp_async_wait_all();   // this chunk's tiles have landed
         __syncthreads();   // previous chunk finished with every buffer
+        if (kAsync && !kPrefK && c > 0) {
+            // K and the vectors have no second buffer at this width
+            copy_kq(c, Ks, kg0);
+            copy_floats(vec, block_of(c) + PrepLayout<float>::kOffVec, kVecRows * kChunk);
+            cp_async_commit();
+            cp_async_wait_all();
+            __syncthreads();
+        }
         if (p.S_chunks) {
             // the entry state of this chunk, at its chunk slot
             const size_t cs = ((size_t)(slot0 + c) * p.H + h) * D * D;
@@ -610,8 +626,10 @@ chunk_state_simt_kernel(ChunkProblem p) {
             // Q and V are free now; K and the vectors go to the other buffers
             copy_kq(c + 1, Qs, qg0);
             copy_v(c + 1);
-            copy_kq(c + 1, Kalt, kg0);
-            copy_floats(vecalt, block_of(c + 1) + PrepLayout<float>::kOffVec, kVecRows * kChunk);
+            if (kPrefK) {
+                copy_kq(c + 1, Kalt, kg0);
+                copy_floats(vecalt, block_of(c + 1) + PrepLayout<float>::kOffVec, kVecRows * kChunk);
+            }
         }
 
         // ---- residuals Vres = T R, outputs O = O_inter + (A_O T) R: the
@@ -688,7 +706,7 @@ chunk_state_simt_kernel(ChunkProblem p) {
             Ss[d * kNS + cc] = abar_n * so - b_n * mo + as[r];
             Ms[d * kNS + cc] = mubar_n * mo - am[r];
         }
-        if (kAsync) {               // the next chunk's K and vectors are in the other buffers
+        if (kPrefK) {               // the next chunk's K and vectors are in the other buffers
             float *t = Ks; Ks = Kalt; Kalt = t;
             t = vec; vec = vecalt; vecalt = t;
         }
@@ -714,16 +732,28 @@ cudaError_t launch_prep_t(const ChunkProblem &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <int D, typename Tin>
+template <int D, typename Tin, int NSC>
 cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
-    auto ks = chunk_state_simt_kernel<D, Tin>;
+    auto ks = chunk_state_simt_kernel<D, Tin, NSC>;
     cudaError_t err = cudaFuncSetAttribute(
-        ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)StateSmem<D>::kBytes);
+        ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)StateSmem<D, NSC>::kBytes);
     if (err != cudaSuccess) return err;
-    const long blocks = (long)p.n_seq * p.H * (D / kNS);
+    const long blocks = (long)p.n_seq * p.H * (D / NSC);
     if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    ks<<<(unsigned)blocks, kThreadsS, StateSmem<D>::kBytes, st>>>(p);
+    ks<<<(unsigned)blocks, 16 * NSC, StateSmem<D, NSC>::kBytes, st>>>(p);
     return cudaGetLastError();
+}
+
+int sm_count_simt() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev] = c;
+    }
+    return count[dev];
 }
 
 }  // namespace
@@ -745,11 +775,15 @@ cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st) {
 
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st) {
     if (p.D == 128) {
-        return p.dtype == MDN_BF16 ? launch_state_t<128, __nv_bfloat16>(p, st)
-                                   : launch_state_t<128, float>(p, st);
+        if (p.dtype == MDN_BF16) return launch_state_t<128, __nv_bfloat16, 32>(p, st);
+        // 64-column CTAs once 32-column ones would need more than one wave
+        const long chains = (long)p.n_seq * p.H;
+        const int sms = sm_count_simt();
+        if (sms > 0 && chains * (128 / 32) > sms) return launch_state_t<128, float, 64>(p, st);
+        return launch_state_t<128, float, 32>(p, st);
     }
-    return p.dtype == MDN_BF16 ? launch_state_t<64, __nv_bfloat16>(p, st)
-                               : launch_state_t<64, float>(p, st);
+    return p.dtype == MDN_BF16 ? launch_state_t<64, __nv_bfloat16, 32>(p, st)
+                               : launch_state_t<64, float, 32>(p, st);
 }
 
 }  // namespace mdn

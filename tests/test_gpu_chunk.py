@@ -142,6 +142,16 @@ def test_varlen_packed_full_size_sampled():
     compare(x, out, _sample(x, 4) + [shortest])
 
 
+def test_fp32_many_chains_wide_cuda_core_slices():
+    """fp32 inputs at d = 128 with more chains than 32-column CTAs fit in one
+    wave (>= 39 chains on 152 SMs): the CUDA-core state pass then runs
+    64-column CTAs of 1024 threads; ragged chunks and mu = 0 entries."""
+    w = W.Workload("fp32_wide", dtype="fp32", state="randn", seed=18)
+    x = W.make_prefill(w, B=3, T=130, H=16, D=128, with_beta=True)
+    x["mu"][:, ::7] = 0.0
+    compare(x, gpu_chunk_fwd(x), chains(x)[::6])
+
+
 def test_very_long_sequence_sampled():
     """One sequence of 131072 tokens: a chain of 2048 chunks, eight times the
     longest benchmark sequence; one head compared in full against the
