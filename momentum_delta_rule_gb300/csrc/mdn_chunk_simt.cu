@@ -744,18 +744,6 @@ cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-int sm_count_simt() {
-    static int count[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (count[dev] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        count[dev] = c;
-    }
-    return count[dev];
-}
-
 }  // namespace
 
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
@@ -778,7 +766,7 @@ cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st) {
         if (p.dtype == MDN_BF16) return launch_state_t<128, __nv_bfloat16, 32>(p, st);
         // 64-column CTAs once 32-column ones would need more than one wave
         const long chains = (long)p.n_seq * p.H;
-        const int sms = sm_count_simt();
+        const int sms = device_sm_count();
         if (sms > 0 && chains * (128 / 32) > sms) return launch_state_t<128, float, 64>(p, st);
         return launch_state_t<128, float, 32>(p, st);
     }

@@ -571,18 +571,6 @@ cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const CUte
     return cudaLaunchKernelEx(&cfg, kern, p, mk, mq, mv);
 }
 
-int sm_count() {
-    static int count[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (count[dev] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        count[dev] = c;
-    }
-    return count[dev];
-}
-
 }  // namespace
 
 // The slice width trades per-chunk latency (narrow slices: smaller MMAs and
@@ -597,7 +585,7 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
         !make_map(&mv, p.v, Tt, p.H, true))
         return cudaErrorInvalidValue;
     const long chains = (long)p.n_seq * p.H;
-    const int sms = sm_count();
+    const int sms = device_sm_count();
     const int ns = (sms > 0 && chains * Cfg<16>::kSlices <= sms) ? 16
                  : (sms > 0 && chains * Cfg<32>::kSlices <= sms) ? 32 : 64;
     if (p.S_chunks) {

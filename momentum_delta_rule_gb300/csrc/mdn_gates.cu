@@ -289,18 +289,6 @@ prepare_inputs_stream_kernel(InputsProblem p, long ntiles) {
     }
 }
 
-int sm_count_inputs() {
-    static int count[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (count[dev] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        count[dev] = c;
-    }
-    return count[dev];
-}
-
 template <int D, typename T>
 cudaError_t launch_t(const InputsProblem &p, cudaStream_t st) {
     constexpr int EL = 16 / (int)sizeof(T);
@@ -312,7 +300,7 @@ cudaError_t launch_t(const InputsProblem &p, cudaStream_t st) {
     // one-shot kernel
     const long ntiles = p.rows / R;
     if (ntiles > 0) {
-        const int sms = sm_count_inputs();
+        const int sms = device_sm_count();
         long blocks = (long)(sms > 0 ? sms : 1) * kStreamBlocksPerSM;
         if (blocks > ntiles) blocks = ntiles;
         auto k = prepare_inputs_stream_kernel<D, T>;

@@ -112,6 +112,20 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 
+// Multiprocessor count of the current device, cached per device (0 when it
+// cannot be read).
+inline int device_sm_count() {
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
 // ---------------------------------------------------------------- device
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
