@@ -261,8 +261,10 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (the
+        // whole warp waits, lane 0 issues and commits)
+        {
+            const bool l0 = lane == 0;
             const uint32_t b1 = smem_u32(smem + C::kOffB1);
             const uint32_t rr = smem_u32(smem + C::kOffR);
             const uint32_t b3 = smem_u32(smem + C::kOffB3);
@@ -270,46 +272,54 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 const int st = c & 1, use = c >> 1;
                 const uint32_t kq = smem_u32(smem + st * kStageBytes);
                 const uint32_t prep = kq + kOffPrep;
-                if (!mbar_wait(&bars->full[st], use & 1, abort)) break;
-                if (!mbar_wait(&bars->state, c & 1, abort)) break;
+                if (!warp_wait(&bars->full[st], use & 1, abort)) break;
+                if (!warp_wait(&bars->state, c & 1, abort)) break;
                 tc_fence_after();
-                // MMA1: D1 = [K; Q] [S | M]; K-steps of 16 over dk (two 64-wide halves)
+                if (l0) {
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
+                    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
+                            const uint64_t b = sdesc_sw128(b1 + (kb * 4 + kk) * 2048, 16384, 1024);
+                            mma_bf16(tmem + C::kColD1, a, b, C::kIdesc1, (kb | kk) != 0);
+                        }
+                    mma_commit(&bars->d1);
+                }
+                __syncwarp();
+                if (!warp_wait(&bars->r, c & 1, abort)) break;
+                tc_fence_after();
+                if (l0) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(b1 + (kb * 4 + kk) * 2048, 16384, 1024);
-                        mma_bf16(tmem + C::kColD1, a, b, C::kIdesc1, (kb | kk) != 0);
+                        const uint64_t a = sdesc_sw128(prep + kk * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
+                        mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, kk != 0);
                     }
-                mma_commit(&bars->d1);
-                if (!mbar_wait(&bars->r, c & 1, abort)) break;
-                tc_fence_after();
-                // MMA2: D2 = [T; A_O T] R; K-steps of 16 tokens
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(prep + kk * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
-                    mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, kk != 0);
+                    mma_commit(&bars->d2);
                 }
-                mma_commit(&bars->d2);
-                if (!mbar_wait(&bars->v, c & 1, abort)) break;
+                __syncwarp();
+                if (!warp_wait(&bars->v, c & 1, abort)) break;
                 tc_fence_after();
-                // MMA3: [S | M] += K^T [gS Vres | -gM Vres]; K-steps of 16 tokens
+                if (l0) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    // K tokens 16kk..16kk+15 sit at tile rows 32kk..32kk+15
-                    const uint64_t a = sdesc_sw128(kq + kk * 4096, 16384, 1024);
-                    const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
-                    mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(kq + kk * 4096, 16384, 1024);
+                        const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
+                        mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
+                    }
+                    mma_commit(&bars->d3);
+                    mma_commit(&bars->empty[st]);
                 }
-                mma_commit(&bars->d3);
-                mma_commit(&bars->empty[st]);
+                __syncwarp();
             }
             // drain: all issued MMAs complete before TMEM is freed
-            mma_commit(&bars->drain);
-            int dummy = 0;
-            mbar_wait(&bars->drain, 0, &dummy);
+            if (l0) {
+                mma_commit(&bars->drain);
+                int dummy = 0;
+                mbar_wait(&bars->drain, 0, &dummy);
+            }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------ epilogue
