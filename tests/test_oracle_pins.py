@@ -458,3 +458,30 @@ def test_decode_steps_equal_forward():
         np.testing.assert_allclose(o[n], o_f[-1], atol=1e-13)
         np.testing.assert_allclose(S[n], S_f[0], atol=1e-13)
         np.testing.assert_allclose(M[n], M_f[0], atol=1e-13)
+
+
+@pytest.mark.parametrize("C", [16, 32, 64])
+def test_chunkwise_at_kernel_chunk_sizes_packed(C):
+    """The chunkwise form at the kernel's chunk size (64) and below, over packed
+    sequences with full chunks, ragged tails, an empty sequence, per-sequence
+    initial states and zero momentum gates, equals the token recurrence to
+    rounding (slides Appendix C, chunk carry Eqs. (40)-(42); partial last
+    chunk per the reading that each sequence is chunked from its own start)."""
+    rng = np.random.default_rng(13)
+    lens = [70, 0, 64, 17, 150]
+    T = sum(lens)
+    x = _rand_inputs(rng, T, 2, 8, 6)
+    x["mu"][::7] = 0.0
+    cu = np.cumsum([0] + lens)
+    S0 = rng.standard_normal((len(lens), 2, 8, 6)) * 0.3
+    M0 = rng.standard_normal((len(lens), 2, 8, 6)) * 0.3
+    o, S, M = recurrence.forward(x["q"], x["k"], x["v"], x["alpha"], x["mu"],
+                                 x["eta"], x["beta"], S0, M0, cu_seqlens=cu)
+    o2, S2, M2 = chunkwise.chunk_forward_packed(
+        x["q"], x["k"], x["v"], x["alpha"], x["mu"], x["eta"], x["beta"],
+        S0, M0, cu, C=C)
+    np.testing.assert_allclose(o2, o, atol=1e-12)
+    np.testing.assert_allclose(S2, S, atol=1e-12)
+    np.testing.assert_allclose(M2, M, atol=1e-12)
+    np.testing.assert_array_equal(S2[1], S0[1])            # empty sequence
+    np.testing.assert_array_equal(M2[1], M0[1])
