@@ -11,6 +11,8 @@ Contents
   recurrence   fp64 token-by-token recurrence (C, OpenMP) — the parity oracle
   coefficients fp64 chunk coefficients in four independent forms
   chunkwise    fp64 chunkwise-parallel forward (Gamma, shifted Gamma, solve)
+  backward     fp64 gradient of the recurrence (reverse sweep over states
+               rebuilt from the saved residuals), for the backward pass
   build        compiles the C oracle with gcc (building the checker is not
                using it)
 
