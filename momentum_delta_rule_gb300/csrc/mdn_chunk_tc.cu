@@ -9,12 +9,12 @@
 // with the chunk-local matrices T and A_O T and the coefficient vectors taken
 // from the prepared block of the prep kernel:
 //
-//   MMA1  D1 = [K; Q] [S_0 | M_0]          (M=128 tokens x2, N=2x64, K=dk)
+//   MMA1  D1 = [K; Q] [S_0 | M_0]          (M=128 rows, N=2 NS, K=dk)
 //         R  = V - Diag(abar) K S_0 + Diag(b_{i-1} alpha_i) K M_0
 //         O_inter = Diag(abar) Q S_0 - Diag(b) Q M_0
-//   MMA2  D2 = [T; A_O T] R                 (M=128, N=64, K=64 tokens)
-//         Vres = rows 0..63,  O = O_inter + rows 64..127
-//   MMA3  [S | M] += K^T [Diag(gS) Vres | -Diag(gM) Vres]  (M=dk, N=2x64, K=64)
+//   MMA2  D2 = [T; A_O T] R                 (M=128, N=NS, K=64 tokens)
+//         Vres = the T rows,  O = O_inter + the A_O T rows
+//   MMA3  [S | M] += K^T [Diag(gS) Vres | -Diag(gM) Vres]  (M=dk, N=2 NS, K=64)
 //
 // with gS_i = gamma_{n,i} eta_i and gM_i = prod_{u>i} mu_u eta_i.  The fp32
 // state [S | M] of the slice lives in TMEM as MMA3's accumulator; before MMA3
@@ -22,13 +22,17 @@
 // carries use the old S_0, M_0), off the critical path while MMA2 runs.  Only
 // a bf16 copy of the state goes to shared memory, as MMA1's B operand.
 //
-// One CTA owns one (sequence, head, 64-column slice): columns of S and M
-// evolve independently (column j of Vres depends only on column j of S_0 and
-// M_0), so the two slices of a head never communicate.
+// One CTA owns one (sequence, head, NS-column slice), NS = 64, 32 or 16 (the
+// launcher takes the narrowest whose grid still fits one CTA per SM, else
+// 64): columns of S and M evolve independently (column j of Vres depends
+// only on column j of S_0 and M_0), so the slices of a head never
+// communicate.  A second instantiation also stores every chunk's entry state
+// (S, M) for a gradient pass; the plain forward's kernel carries none of it.
 //
-// Warp roles (18 warps for 64-column slices): 0 TMA producer, 1 MMA issuer
-// + TMEM owner, 2..17 epilogue (TMEM lane quadrant = warp % 4, 16-column
-// group of the slice = (warp-2)/4).  A warp reaches only the TMEM lanes of
+// Warp roles (2 + NS / 4 warps, 18 for NS = 64): 0 TMA producer, 1 MMA
+// issuer + TMEM owner (all lanes wait, lane 0 issues), the rest epilogue
+// (TMEM lane quadrant = warp % 4, 16-column group of the slice =
+// (warp-2)/4).  A warp reaches only the TMEM lanes of
 // its quadrant, and the warps of a quadrant share one scheduler; [K; Q] and
 // [T; A_O T] rows are therefore interleaved in blocks of 16 (tc_row), so that
 // every quadrant holds 16 token rows and 16 query rows and the token-row
