@@ -205,3 +205,24 @@ def test_chunk_fwd_accepts_null_tensors_without_tokens(L):
     # call is not an argument error (it needs a device to go further)
     st = _chunk(L, q=None, k=None, v=None, o=None, alpha=None, mu=None, eta=None, T=0)
     assert st != mdn.MDN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library every call raises: there is no CPU or
+    PyTorch fallback on the product path."""
+    import subprocess
+    import sys
+    code = (
+        "import momentum_delta_rule_gb300 as mdn\n"
+        "mdn.LIB_PATH = %r\n"
+        "try:\n"
+        "    mdn.abi_version()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised', 'not built' in str(e) or 'libmdn' in str(e))\n"
+        "else:\n"
+        "    print('returned')\n" % str(tmp_path / "absent" / "libmdn.so"))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True,
+                         text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "raised True", out.stdout + out.stderr
