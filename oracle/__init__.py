@@ -13,6 +13,8 @@ Contents
   chunkwise    fp64 chunkwise-parallel forward (Gamma, shifted Gamma, solve)
   backward     fp64 gradient of the recurrence (reverse sweep over states
                rebuilt from the saved residuals), for the backward pass
+  chunkwise_backward  fp64 gradient of the chunkwise form (per-chunk dense
+               products, state adjoints carried backwards across chunks)
   build        compiles the C oracle with gcc (building the checker is not
                using it)
 

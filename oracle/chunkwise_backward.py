@@ -1,0 +1,169 @@
+"""Gradient of the MDN chunkwise form, fp64 numpy (oracle, TEST INFRASTRUCTURE).
+
+The chunk algebra a chunked gradient pass follows, for one (sequence, head)
+chain, checked against the token-level reverse sweep of ``backward.py``.
+Forward per chunk of n tokens (slides, frames "Solve the unknown residuals
+with a lower triangular system" and "Chunk outputs combine incoming states
+and local writes"; reading notes 2.4-2.5), with P = Diag(alpha) K and
+Kh = Diag(eta) K:
+
+    L    = (P Kh^T) . Gamma_m,   T = (I + L)^{-1}
+    R    = V - Diag(abar_m) P S_0 + Diag(b_m) P M_0,   Vres = T R
+    A    = (Q Kh^T) . Gamma
+    O    = Diag(abar) Q S_0 - Diag(b) Q M_0 + A Vres
+    S_n  = abar_n S_0 - b_n M_0 + [Diag(Gamma_{n,:}) Kh]^T Vres
+    M_n  = mubar_n M_0 - [Diag(mu_tail) Kh]^T Vres
+
+(``.`` the elementwise product.)  Its reverse, given dO, dS_n and dM_n:
+
+    dVres = A^T dO + WS dS_n - WM dM_n          (WS, WM the two carry rows)
+    dR    = T^T dVres;   dL = -dR Vres^T;   dV = dR
+    dQ    = Diag(abar) dO S_0^T - Diag(b) dO M_0^T + (dO Vres^T . Gamma) Kh
+    dS_0  = abar_n dS_n + (Diag(abar) Q)^T dO - (Diag(abar_m) P)^T dR
+    dM_0  = mubar_n dM_n - b_n dS_n - (Diag(b) Q)^T dO + (Diag(b_m) P)^T dR
+
+and dK collects the P and Kh adjoints.  dS_0, dM_0 are the adjoints at the
+previous chunk's end: the chain over chunks runs backwards like the forward's
+state pass runs forwards.
+
+Gate gradients go through the chunk coefficients (Gamma, its row shift, abar,
+b, their shifted copies, mu_tail and the chunk totals).  Each of these is a
+sum of products in which any single gate appears at most once (Gamma_{i,j} =
+sum_r beta_r prod alpha prod mu over disjoint index ranges), so it is affine
+in each gate on its own, and its exact partial derivative with respect to
+that gate is its value with the gate set to 1 minus its value with the gate
+set to 0.  Plus alpha's direct use in P and eta's in Kh.  The coefficients
+come from ``coefficients.chunk_vectors`` (the triple-sum definition).
+"""
+import numpy as np
+
+from . import coefficients as coef
+
+
+def _coeffs(alpha, mu, beta):
+    cv = coef.chunk_vectors(alpha, mu, beta)
+    return dict(G=cv["Gamma"], Gm=cv["Gamma_m"], abar=cv["abar"], b=cv["b"],
+                abar_m=cv["abar_m"], b_m=cv["b_m"], mu_tail=cv["mu_tail"],
+                abar_n=cv["abar"][-1], b_n=cv["b"][-1], mubar_n=cv["mubar"][-1])
+
+
+def _chunk_forward(Q, K, V, a, m, e, bt, S0, M0):
+    c = _coeffs(a, m, bt)
+    n = K.shape[0]
+    P = a[:, None] * K
+    Kh = e[:, None] * K
+    X = P @ Kh.T
+    T = np.linalg.inv(np.eye(n) + X * c["Gm"])
+    R = V - (c["abar_m"][:, None] * P) @ S0 + (c["b_m"][:, None] * P) @ M0
+    Vres = T @ R
+    Y = Q @ Kh.T
+    A = Y * c["G"]
+    O = c["abar"][:, None] * (Q @ S0) - c["b"][:, None] * (Q @ M0) + A @ Vres
+    WS = c["G"][-1, :][:, None] * Kh
+    WM = c["mu_tail"][:, None] * Kh
+    S_n = c["abar_n"] * S0 - c["b_n"] * M0 + WS.T @ Vres
+    M_n = c["mubar_n"] * M0 - WM.T @ Vres
+    saved = dict(c=c, P=P, Kh=Kh, X=X, T=T, R=R, Vres=Vres, Y=Y, A=A, WS=WS, WM=WM)
+    return O, S_n, M_n, saved
+
+
+def _chunk_backward(Q, K, V, a, m, e, bt, S0, M0, dO, dSn, dMn, sv):
+    c, P, Kh, X, T = sv["c"], sv["P"], sv["Kh"], sv["X"], sv["T"]
+    Vres, Y, A, WS, WM = sv["Vres"], sv["Y"], sv["A"], sv["WS"], sv["WM"]
+    n = K.shape[0]
+    dc = {name: np.zeros_like(np.asarray(val, np.float64)) for name, val in c.items()}
+    # the carry
+    dVres = WS @ dSn - WM @ dMn
+    dWS = Vres @ dSn.T
+    dWM = -Vres @ dMn.T
+    dS0 = c["abar_n"] * dSn
+    dM0 = -c["b_n"] * dSn + c["mubar_n"] * dMn
+    dc["abar_n"] = np.sum(S0 * dSn)
+    dc["b_n"] = -np.sum(M0 * dSn)
+    dc["mubar_n"] = np.sum(M0 * dMn)
+    dc["G"][-1, :] += np.sum(dWS * Kh, axis=1)
+    dc["mu_tail"] = np.sum(dWM * Kh, axis=1)
+    dKh = c["G"][-1, :][:, None] * dWS + c["mu_tail"][:, None] * dWM
+    # the output
+    dA = dO @ Vres.T
+    dVres = dVres + A.T @ dO
+    QS0, QM0 = Q @ S0, Q @ M0
+    dQ = c["abar"][:, None] * (dO @ S0.T) - c["b"][:, None] * (dO @ M0.T)
+    dS0 = dS0 + (c["abar"][:, None] * Q).T @ dO
+    dM0 = dM0 - (c["b"][:, None] * Q).T @ dO
+    dc["abar"] = np.sum(QS0 * dO, axis=1)
+    dc["b"] = -np.sum(QM0 * dO, axis=1)
+    dY = dA * c["G"]
+    dc["G"] += dA * Y
+    dQ = dQ + dY @ Kh
+    dKh = dKh + dY.T @ Q
+    # the residual system
+    dR = T.T @ dVres
+    dL = -dR @ Vres.T
+    dX = dL * c["Gm"]
+    dc["Gm"] = dL * X
+    dP = dX @ Kh
+    dKh = dKh + dX.T @ P
+    dV = dR
+    dPS = -dR @ S0.T          # adjoint of Diag(abar_m) P
+    dPM = dR @ M0.T           # adjoint of Diag(b_m) P
+    dP = dP + c["abar_m"][:, None] * dPS + c["b_m"][:, None] * dPM
+    dc["abar_m"] = np.sum(P * dPS, axis=1)
+    dc["b_m"] = np.sum(P * dPM, axis=1)
+    dS0 = dS0 - (c["abar_m"][:, None] * P).T @ dR
+    dM0 = dM0 + (c["b_m"][:, None] * P).T @ dR
+    # P = Diag(alpha) K, Kh = Diag(eta) K
+    dK = a[:, None] * dP + e[:, None] * dKh
+    da = np.sum(dP * K, axis=1)
+    de = np.sum(dKh * K, axis=1)
+    # coefficients -> gates: exact partials of affine functions of one gate
+    gates = {"alpha": a, "mu": m, "beta": bt}
+    dg = {name: np.zeros(n) for name in gates}
+    for name in gates:
+        for u in range(n):
+            hi = {kk: vv.copy() for kk, vv in gates.items()}
+            lo = {kk: vv.copy() for kk, vv in gates.items()}
+            hi[name][u], lo[name][u] = 1.0, 0.0
+            c1 = _coeffs(hi["alpha"], hi["mu"], hi["beta"])
+            c0 = _coeffs(lo["alpha"], lo["mu"], lo["beta"])
+            dg[name][u] = sum(np.sum(dc[kk] * (np.asarray(c1[kk]) - np.asarray(c0[kk])))
+                              for kk in dc)
+    return dict(dq=dQ, dk=dK, dv=dV, dalpha=da + dg["alpha"], dmu=dg["mu"],
+                deta=de, dbeta=dg["beta"]), dS0, dM0
+
+
+def chain_backward(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
+                   do=None, dS_T=None, dM_T=None, C=64):
+    """One chain: q, k [T, dk]; v, do [T, dv]; gates [T]; states [dk, dv].
+    Gradients of <o, do> + <S_T, dS_T> + <M_T, dM_T>, chunk by chunk: the
+    forward keeps each chunk's entry states, the reverse walks the chunks
+    from the last, carrying the state adjoints."""
+    q, k, v = (np.asarray(x, np.float64) for x in (q, k, v))
+    alpha, mu, eta = (np.asarray(x, np.float64).reshape(-1) for x in (alpha, mu, eta))
+    T, dk = k.shape
+    dv = v.shape[1]
+    beta = np.ones(T) if beta is None else np.asarray(beta, np.float64).reshape(-1)
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, np.float64)
+    M = np.zeros((dk, dv)) if M0 is None else np.array(M0, np.float64)
+    do = np.zeros((T, dv)) if do is None else np.asarray(do, np.float64)
+    dS = np.zeros((dk, dv)) if dS_T is None else np.array(dS_T, np.float64)
+    dM = np.zeros((dk, dv)) if dM_T is None else np.array(dM_T, np.float64)
+    starts = list(range(0, T, C))
+    entries = []
+    for s0 in starts:
+        sl = slice(s0, min(s0 + C, T))
+        entries.append((S, M))
+        _, S, M, _ = _chunk_forward(q[sl], k[sl], v[sl], alpha[sl], mu[sl],
+                                    eta[sl], beta[sl], S, M)
+    g = {name: np.zeros_like(x) for name, x in
+         (("dq", q), ("dk", k), ("dv", v), ("dalpha", alpha), ("dmu", mu),
+          ("deta", eta), ("dbeta", beta))}
+    for s0, (Se, Me) in zip(reversed(starts), reversed(entries)):
+        sl = slice(s0, min(s0 + C, T))
+        args = (q[sl], k[sl], v[sl], alpha[sl], mu[sl], eta[sl], beta[sl], Se, Me)
+        _, _, _, saved = _chunk_forward(*args)
+        gc, dS, dM = _chunk_backward(*args, do[sl], dS, dM, saved)
+        for name, val in gc.items():
+            g[name][sl] = val
+    g["dS0"], g["dM0"] = dS, dM
+    return g

@@ -7,12 +7,13 @@ the mathematics that defines it: central finite differences of the forward
 oracle (the C token recurrence, written independently), entry by entry on a
 tiny case and along random directions on packed sequences; and the rebuilt
 states to the forward's own states.  Planted mistakes show that the
-difference check fails when a term is wrong.
+difference check fails when a term is wrong.  The chunkwise gradient
+(``oracle/chunkwise_backward.py``) is pinned to the token-level sweep.
 """
 import numpy as np
 import pytest
 
-from oracle import backward as bwd, recurrence
+from oracle import backward as bwd, chunkwise_backward as cbwd, recurrence
 
 NAMES = ("q", "k", "v", "alpha", "mu", "eta", "beta", "S0", "M0")
 
@@ -200,3 +201,51 @@ def test_unplanted_copy_passes():
     W = _weights(rng, x, 2)
     errs = _directional_errors(_planted("none"), x, cu, W, rng)
     assert max(errs.values()) < 1e-7, errs
+
+
+# --------------------------------------------------------------------------
+# the chunkwise gradient (the algebra a chunked gradient pass follows)
+
+
+@pytest.mark.parametrize("C,T", [(1, 5), (2, 7), (3, 12), (4, 9), (8, 20), (16, 37)])
+@pytest.mark.parametrize("with_beta", [True, False])
+def test_chunkwise_gradient_equals_token_sweep(C, T, with_beta):
+    """Chunk by chunk (dense products per chunk, state adjoints carried
+    backwards across chunks, gate partials through the chunk coefficients)
+    equals the token-level reverse sweep to rounding, with zero momentum
+    gates and a ragged last chunk."""
+    rng = np.random.default_rng(300 + 7 * C + T)
+    x, cu = _inputs(rng, [T], 1, 3, 4, mu_zero_every=3)
+    if not with_beta:
+        x["beta"] = None
+    W = _weights(rng, x, 1)
+    g = bwd.backward(**x, do=W[0], dS_T=W[1], dM_T=W[2], cu_seqlens=cu)
+    gc = cbwd.chain_backward(
+        x["q"][:, 0], x["k"][:, 0], x["v"][:, 0], x["alpha"][:, 0], x["mu"][:, 0],
+        x["eta"][:, 0], None if x["beta"] is None else x["beta"][:, 0],
+        x["S0"][0, 0], x["M0"][0, 0], W[0][:, 0], W[1][0, 0], W[2][0, 0], C=C)
+    for name in ("dq", "dk", "dv", "dalpha", "dmu", "deta", "dbeta"):
+        np.testing.assert_allclose(gc[name], g[name][:, 0], atol=1e-12, err_msg=name)
+    np.testing.assert_allclose(gc["dS0"], g["dS0"][0, 0], atol=1e-12)
+    np.testing.assert_allclose(gc["dM0"], g["dM0"][0, 0], atol=1e-12)
+
+
+def test_chunkwise_gradient_with_strict_lower_gamma_fails(monkeypatch):
+    """Deleting Gamma's diagonal instead of shifting its rows (the mistake the
+    slides' backup frame warns about) breaks the chunkwise gradient too."""
+    rng = np.random.default_rng(320)
+    x, cu = _inputs(rng, [10], 1, 3, 3)
+    W = _weights(rng, x, 1)
+    g = bwd.backward(**x, do=W[0], dS_T=W[1], dM_T=W[2], cu_seqlens=cu)
+    real = cbwd._coeffs
+
+    def strict(a, m, b):
+        c = real(a, m, b)
+        c["Gm"] = np.tril(c["G"], -1)
+        return c
+    monkeypatch.setattr(cbwd, "_coeffs", strict)
+    gc = cbwd.chain_backward(
+        x["q"][:, 0], x["k"][:, 0], x["v"][:, 0], x["alpha"][:, 0], x["mu"][:, 0],
+        x["eta"][:, 0], x["beta"][:, 0], x["S0"][0, 0], x["M0"][0, 0],
+        W[0][:, 0], W[1][0, 0], W[2][0, 0], C=4)
+    assert np.abs(gc["dk"] - g["dk"][:, 0]).max() > 1e-3
