@@ -32,8 +32,11 @@ sum of products in which any single gate appears at most once (Gamma_{i,j} =
 sum_r beta_r prod alpha prod mu over disjoint index ranges), so it is affine
 in each gate on its own, and its exact partial derivative with respect to
 that gate is its value with the gate set to 1 minus its value with the gate
-set to 0.  Plus alpha's direct use in P and eta's in Kh.  The coefficients
-come from ``coefficients.chunk_vectors`` (the triple-sum definition).
+set to 0 (``gate_partials_by_evaluation``, the definition).
+``gate_partials_closed_form`` writes the same partials as sums over Gamma's
+index triangle, the form a kernel can follow.  Plus alpha's direct use in P
+and eta's in Kh.  The coefficients come from ``coefficients.chunk_vectors``
+(the triple-sum definition).
 """
 import numpy as np
 
@@ -67,7 +70,78 @@ def _chunk_forward(Q, K, V, a, m, e, bt, S0, M0):
     return O, S_n, M_n, saved
 
 
-def _chunk_backward(Q, K, V, a, m, e, bt, S0, M0, dO, dSn, dMn, sv):
+def gate_partials_by_evaluation(a, m, bt, dc):
+    """Gate gradients through the coefficients, one gate at a time: each
+    coefficient is affine in any single gate, so its exact partial is its
+    value at gate = 1 minus its value at gate = 0 (the plain definition;
+    O(C^4) per chunk)."""
+    gates = {"alpha": a, "mu": m, "beta": bt}
+    n = len(a)
+    dg = {name: np.zeros(n) for name in gates}
+    for name in gates:
+        for u in range(n):
+            hi = {kk: vv.copy() for kk, vv in gates.items()}
+            lo = {kk: vv.copy() for kk, vv in gates.items()}
+            hi[name][u], lo[name][u] = 1.0, 0.0
+            c1 = _coeffs(hi["alpha"], hi["mu"], hi["beta"])
+            c0 = _coeffs(lo["alpha"], lo["mu"], lo["beta"])
+            dg[name][u] = sum(np.sum(dc[kk] * (np.asarray(c1[kk]) - np.asarray(c0[kk])))
+                              for kk in dc)
+    return dg["alpha"], dg["mu"], dg["beta"]
+
+
+def gate_partials_closed_form(a, m, bt, dc):
+    """The same gate gradients as sums over Gamma's index triangle, without
+    dividing by any gate (mu may be 0).
+
+    Positions -1 (an origin before the chunk) and 0..n-1 (the tokens);
+    A(r, i) = prod_{u=r+1}^{i} alpha_u, Mu(j, r) = prod_{u=j+1}^{r} mu_u, so
+    that Gamma_{i,j} = sum_{r=max(j,0)}^{i} beta_r A(r, i) Mu(j, r), b_i is
+    the origin's column, abar_i = A(-1, i), mu_tail_j = Mu(j, n-1) and
+    mubar_n = Mu(-1, n-1).  With the extended adjoint dGx (the origin in
+    column 0) and F[i, m] = sum_{j=-1}^{m} dGx[i, j] Mu(j, m):
+
+        dbeta_r  = sum_{i>=r} A(r, i) F[i, r]
+        dalpha_u = sum_{i>=u} A(u, i) [sum_{r<u} beta_r A(r, u-1) F[i, r]
+                                       + dabar_i A(-1, u-1)]
+        dmu_u    = sum_{i>=u} F[i, u-1] sum_{r=u}^{i} beta_r A(r, i) Mu(u, r)
+                   + sum_{j<u} dmu_tail_j Mu(j, u-1) Mu(u, n-1)
+
+    (the partial of a product is the product of its two sides of the gate)."""
+    n = len(a)
+    A = lambda r, i: float(np.prod(a[r + 1:i + 1]))
+    Mu = lambda j, r: float(np.prod(m[j + 1:r + 1]))
+    # fold the shifted and end copies into the base coefficients
+    dG = dc["G"].copy()
+    dG[:-1, :] += dc["Gm"][1:, :]
+    dabar = dc["abar"].copy()
+    dabar[:-1] += dc["abar_m"][1:]
+    dabar[-1] += dc["abar_n"]
+    db = dc["b"].copy()
+    db[:-1] += dc["b_m"][1:]
+    db[-1] += dc["b_n"]
+    dGx = np.zeros((n, n + 1))            # column j + 1 for position j
+    dGx[:, 0] = db
+    dGx[:, 1:] = dG
+    dmt = np.concatenate([[dc["mubar_n"]], dc["mu_tail"]])   # positions -1..n-1
+    F = np.zeros((n, n + 1))              # column m + 1 for m = -1..n-1
+    for i in range(n):
+        for mm in range(-1, i + 1):
+            F[i, mm + 1] = sum(dGx[i, j + 1] * Mu(j, mm) for j in range(-1, mm + 1))
+    dbeta = np.array([sum(A(r, i) * F[i, r + 1] for i in range(r, n)) for r in range(n)])
+    dalpha = np.zeros(n)
+    dmu = np.zeros(n)
+    for u in range(n):
+        for i in range(u, n):
+            inner = sum(bt[r] * A(r, u - 1) * F[i, r + 1] for r in range(u))
+            dalpha[u] += A(u, i) * (inner + dabar[i] * A(-1, u - 1))
+            dmu[u] += F[i, u] * sum(bt[r] * A(r, i) * Mu(u, r) for r in range(u, i + 1))
+        dmu[u] += sum(dmt[j + 1] * Mu(j, u - 1) for j in range(-1, u)) * Mu(u, n - 1)
+    return dalpha, dmu, dbeta
+
+
+def _chunk_backward(Q, K, V, a, m, e, bt, S0, M0, dO, dSn, dMn, sv,
+                    gate_partials=gate_partials_by_evaluation):
     c, P, Kh, X, T = sv["c"], sv["P"], sv["Kh"], sv["X"], sv["T"]
     Vres, Y, A, WS, WM = sv["Vres"], sv["Y"], sv["A"], sv["WS"], sv["WM"]
     n = K.shape[0]
@@ -116,24 +190,15 @@ def _chunk_backward(Q, K, V, a, m, e, bt, S0, M0, dO, dSn, dMn, sv):
     dK = a[:, None] * dP + e[:, None] * dKh
     da = np.sum(dP * K, axis=1)
     de = np.sum(dKh * K, axis=1)
-    # coefficients -> gates: exact partials of affine functions of one gate
-    gates = {"alpha": a, "mu": m, "beta": bt}
-    dg = {name: np.zeros(n) for name in gates}
-    for name in gates:
-        for u in range(n):
-            hi = {kk: vv.copy() for kk, vv in gates.items()}
-            lo = {kk: vv.copy() for kk, vv in gates.items()}
-            hi[name][u], lo[name][u] = 1.0, 0.0
-            c1 = _coeffs(hi["alpha"], hi["mu"], hi["beta"])
-            c0 = _coeffs(lo["alpha"], lo["mu"], lo["beta"])
-            dg[name][u] = sum(np.sum(dc[kk] * (np.asarray(c1[kk]) - np.asarray(c0[kk])))
-                              for kk in dc)
-    return dict(dq=dQ, dk=dK, dv=dV, dalpha=da + dg["alpha"], dmu=dg["mu"],
-                deta=de, dbeta=dg["beta"]), dS0, dM0
+    # coefficients -> gates
+    ga, gm, gb = gate_partials(a, m, bt, dc)
+    return dict(dq=dQ, dk=dK, dv=dV, dalpha=da + ga, dmu=gm,
+                deta=de, dbeta=gb), dS0, dM0
 
 
 def chain_backward(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
-                   do=None, dS_T=None, dM_T=None, C=64):
+                   do=None, dS_T=None, dM_T=None, C=64,
+                   gate_partials=gate_partials_by_evaluation):
     """One chain: q, k [T, dk]; v, do [T, dv]; gates [T]; states [dk, dv].
     Gradients of <o, do> + <S_T, dS_T> + <M_T, dM_T>, chunk by chunk: the
     forward keeps each chunk's entry states, the reverse walks the chunks
@@ -162,7 +227,7 @@ def chain_backward(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
         sl = slice(s0, min(s0 + C, T))
         args = (q[sl], k[sl], v[sl], alpha[sl], mu[sl], eta[sl], beta[sl], Se, Me)
         _, _, _, saved = _chunk_forward(*args)
-        gc, dS, dM = _chunk_backward(*args, do[sl], dS, dM, saved)
+        gc, dS, dM = _chunk_backward(*args, do[sl], dS, dM, saved, gate_partials)
         for name, val in gc.items():
             g[name][sl] = val
     g["dS0"], g["dM0"] = dS, dM

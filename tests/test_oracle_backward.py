@@ -249,3 +249,39 @@ def test_chunkwise_gradient_with_strict_lower_gamma_fails(monkeypatch):
         x["eta"][:, 0], x["beta"][:, 0], x["S0"][0, 0], x["M0"][0, 0],
         W[0][:, 0], W[1][0, 0], W[2][0, 0], C=4)
     assert np.abs(gc["dk"] - g["dk"][:, 0]).max() > 1e-3
+
+
+@pytest.mark.parametrize("n,seed", [(1, 0), (2, 1), (5, 2), (9, 3), (16, 4)])
+def test_closed_form_gate_partials_equal_evaluation(n, seed):
+    """The gate gradients as sums over Gamma's index triangle equal the exact
+    gate-by-gate partials, for arbitrary coefficient adjoints, with zero and
+    unit gates among them."""
+    rng = np.random.default_rng(400 + seed)
+    a = np.exp(-rng.uniform(0, 0.5, n))
+    m = rng.uniform(0, 1, n)
+    if n > 2:
+        m[::2] = 0.0
+    bt = rng.uniform(0, 1, n)
+    a[-1] = 1.0
+    c = cbwd._coeffs(a, m, bt)
+    dc = {kk: rng.standard_normal(np.shape(vv)) for kk, vv in c.items()}
+    dc = {kk: (float(vv) if np.ndim(vv) == 0 else vv) for kk, vv in dc.items()}
+    ref = cbwd.gate_partials_by_evaluation(a, m, bt, dc)
+    got = cbwd.gate_partials_closed_form(a, m, bt, dc)
+    for r, g_ in zip(ref, got):
+        np.testing.assert_allclose(g_, r, atol=1e-12)
+
+
+@pytest.mark.parametrize("C,T", [(4, 13), (16, 37)])
+def test_chunkwise_gradient_closed_form_equals_token_sweep(C, T):
+    rng = np.random.default_rng(500 + C)
+    x, cu = _inputs(rng, [T], 1, 3, 4, mu_zero_every=4)
+    W = _weights(rng, x, 1)
+    g = bwd.backward(**x, do=W[0], dS_T=W[1], dM_T=W[2], cu_seqlens=cu)
+    gc = cbwd.chain_backward(
+        x["q"][:, 0], x["k"][:, 0], x["v"][:, 0], x["alpha"][:, 0], x["mu"][:, 0],
+        x["eta"][:, 0], x["beta"][:, 0], x["S0"][0, 0], x["M0"][0, 0],
+        W[0][:, 0], W[1][0, 0], W[2][0, 0], C=C,
+        gate_partials=cbwd.gate_partials_closed_form)
+    for name in ("dq", "dk", "dv", "dalpha", "dmu", "deta", "dbeta"):
+        np.testing.assert_allclose(gc[name], g[name][:, 0], atol=1e-12, err_msg=name)
