@@ -92,25 +92,40 @@ def gate_partials_by_evaluation(a, m, bt, dc):
 
 def gate_partials_closed_form(a, m, bt, dc):
     """The same gate gradients as sums over Gamma's index triangle, without
-    dividing by any gate (mu may be 0).
+    dividing by any gate (mu may be 0), in O(C^2) per chunk.
 
     Positions -1 (an origin before the chunk) and 0..n-1 (the tokens);
     A(r, i) = prod_{u=r+1}^{i} alpha_u, Mu(j, r) = prod_{u=j+1}^{r} mu_u, so
     that Gamma_{i,j} = sum_{r=max(j,0)}^{i} beta_r A(r, i) Mu(j, r), b_i is
     the origin's column, abar_i = A(-1, i), mu_tail_j = Mu(j, n-1) and
-    mubar_n = Mu(-1, n-1).  With the extended adjoint dGx (the origin in
-    column 0) and F[i, m] = sum_{j=-1}^{m} dGx[i, j] Mu(j, m):
+    mubar_n = Mu(-1, n-1).  With the extended adjoint dGx (the origin's
+    column first) and F[i, m] = sum_{j=-1}^{m} dGx[i, j] Mu(j, m):
 
         dbeta_r  = sum_{i>=r} A(r, i) F[i, r]
-        dalpha_u = sum_{i>=u} A(u, i) [sum_{r<u} beta_r A(r, u-1) F[i, r]
-                                       + dabar_i A(-1, u-1)]
-        dmu_u    = sum_{i>=u} F[i, u-1] sum_{r=u}^{i} beta_r A(r, i) Mu(u, r)
-                   + sum_{j<u} dmu_tail_j Mu(j, u-1) Mu(u, n-1)
+        dalpha_u = sum_{i>=u} A(u, i) [I[i, u] + dabar_i A(-1, u-1)],
+                   I[i, u] = sum_{r<u} beta_r A(r, u-1) F[i, r]
+        dmu_u    = sum_{i>=u} F[i, u-1] G[i, u] + Tl_u Mu(u, n-1),
+                   G[i, u] = sum_{r=u}^{i} beta_r A(r, i) Mu(u, r),
+                   Tl_u = sum_{j<u} dmu_tail_j Mu(j, u-1)
 
-    (the partial of a product is the product of its two sides of the gate)."""
+    (the partial of a product is the product of its two sides of the gate).
+    Each inner sum follows a one-step recurrence: F[i, m] = mu_m F[i, m-1] +
+    dGx[i, m], I[i, u+1] = alpha_u I[i, u] + beta_u F[i, u], G[i, u-1] =
+    beta_{u-1} A(u-1, i) + mu_u G[i, u], Tl_{u+1} = mu_u Tl_u + dmu_tail_u."""
     n = len(a)
-    A = lambda r, i: float(np.prod(a[r + 1:i + 1]))
-    Mu = lambda j, r: float(np.prod(m[j + 1:r + 1]))
+    # product tables by multiplication only: At[r + 1, i] = A(r, i), i >= r
+    At = np.zeros((n + 1, n))
+    Mt = np.zeros((n + 1, n))
+    for r in range(-1, n):
+        pa = pm = 1.0
+        if r >= 0:
+            At[r + 1, r] = Mt[r + 1, r] = 1.0
+        for i in range(r + 1, n):
+            pa *= a[i]
+            pm *= m[i]
+            At[r + 1, i] = pa
+            Mt[r + 1, i] = pm
+    A = lambda r, i: 1.0 if i == r else At[r + 1, i]
     # fold the shifted and end copies into the base coefficients
     dG = dc["G"].copy()
     dG[:-1, :] += dc["Gm"][1:, :]
@@ -120,23 +135,29 @@ def gate_partials_closed_form(a, m, bt, dc):
     db = dc["b"].copy()
     db[:-1] += dc["b_m"][1:]
     db[-1] += dc["b_n"]
-    dGx = np.zeros((n, n + 1))            # column j + 1 for position j
-    dGx[:, 0] = db
-    dGx[:, 1:] = dG
-    dmt = np.concatenate([[dc["mubar_n"]], dc["mu_tail"]])   # positions -1..n-1
-    F = np.zeros((n, n + 1))              # column m + 1 for m = -1..n-1
+    # F[i, m + 1] for m = -1..i
+    F = np.zeros((n, n + 1))
     for i in range(n):
-        for mm in range(-1, i + 1):
-            F[i, mm + 1] = sum(dGx[i, j + 1] * Mu(j, mm) for j in range(-1, mm + 1))
+        F[i, 0] = db[i]
+        for mm in range(0, i + 1):
+            F[i, mm + 1] = m[mm] * F[i, mm] + dG[i, mm]
     dbeta = np.array([sum(A(r, i) * F[i, r + 1] for i in range(r, n)) for r in range(n)])
     dalpha = np.zeros(n)
     dmu = np.zeros(n)
-    for u in range(n):
-        for i in range(u, n):
-            inner = sum(bt[r] * A(r, u - 1) * F[i, r + 1] for r in range(u))
+    for i in range(n):
+        inner = 0.0                                  # I[i, u]
+        for u in range(0, i + 1):
             dalpha[u] += A(u, i) * (inner + dabar[i] * A(-1, u - 1))
-            dmu[u] += F[i, u] * sum(bt[r] * A(r, i) * Mu(u, r) for r in range(u, i + 1))
-        dmu[u] += sum(dmt[j + 1] * Mu(j, u - 1) for j in range(-1, u)) * Mu(u, n - 1)
+            inner = a[u] * inner + bt[u] * F[i, u + 1]
+        g = bt[i]                                    # G[i, u], u = i down to 0
+        for u in range(i, -1, -1):
+            dmu[u] += F[i, u] * g
+            if u > 0:
+                g = bt[u - 1] * A(u - 1, i) + m[u] * g
+    tl = dc["mubar_n"]                               # Tl_u
+    for u in range(n):
+        dmu[u] += tl * (1.0 if u == n - 1 else Mt[u + 1, n - 1])
+        tl = m[u] * tl + dc["mu_tail"][u]
     return dalpha, dmu, dbeta
 
 

@@ -272,8 +272,9 @@ def test_closed_form_gate_partials_equal_evaluation(n, seed):
         np.testing.assert_allclose(g_, r, atol=1e-12)
 
 
-@pytest.mark.parametrize("C,T", [(4, 13), (16, 37)])
+@pytest.mark.parametrize("C,T", [(4, 13), (16, 37), (64, 150)])
 def test_chunkwise_gradient_closed_form_equals_token_sweep(C, T):
+    """At the kernel's chunk size too (two full chunks and a ragged one)."""
     rng = np.random.default_rng(500 + C)
     x, cu = _inputs(rng, [T], 1, 3, 4, mu_zero_every=4)
     W = _weights(rng, x, 1)
