@@ -11,7 +11,8 @@ import torch
 
 import workloads as W
 from oracle import recurrence
-from tests._helpers import TOL, chains, to_dev
+from oracle import backward as bwd
+from tests._helpers import TOL, chains, oracle_chains, to_dev
 
 pytestmark = pytest.mark.gpu
 C = 64
@@ -100,3 +101,49 @@ def test_chunk_states_cuda_core_path():
     w = W.Workload("cs_fp32", dtype="fp32", state="randn", seed=54)
     x = W.make_prefill(w, B=2, T=130, H=2, D=64, with_beta=True)
     _check(x)
+
+
+def test_states_rebuilt_from_saved_residuals():
+    """What a gradient pass keeps (slides, "Backward computation" block: save
+    the residuals, rebuild the states): each chunk's states rebuilt from the
+    forward's saved entry states and saved residuals, by M' = mu M -
+    eta k vres^T and S' = alpha S - beta M', match the oracle's states at the
+    next chunk boundary and at the sequence end (ragged last chunk, mu = 0
+    entries, nonzero initial states)."""
+    import momentum_delta_rule_gb300 as mdn
+    w = W.Workload("cs_rebuild", dtype="bf16", state="randn", seed=55)
+    x = W.make_prefill(w, B=2, T=150, H=2, D=128, with_beta=True)
+    x["mu"][:, ::7] = 0.0
+    d = to_dev(x)
+    args = (d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"], d["beta"],
+            d["S0"], d["M0"])
+    _, _, _, Sc, Mc = mdn.chunk_fwd(*args, return_chunk_states=True)
+    _, _, _, vres = mdn.chunk_fwd(*args, return_vres=True)
+    torch.cuda.synchronize()
+    Sc, Mc = Sc.double().cpu().numpy(), Mc.double().cpu().numpy()
+    D, H = x["D"], x["H"]
+    vres = vres.double().cpu().numpy().reshape(-1, H, D)
+    k = x["k"].double().numpy().reshape(-1, H, D)
+    g = {n: x[n].double().numpy().reshape(-1, H) for n in ("alpha", "mu", "eta", "beta")}
+    ch = chains(x)
+    finals = oracle_chains(x, ch)
+    lens = [c.stop - c.start for (_, h, c) in ch if h == 0]
+    slot0 = np.concatenate([[0], np.cumsum([(L + C - 1) // C for L in lens])])
+    got, want = [], []
+    for (s, h, sl) in ch:
+        L = sl.stop - sl.start
+        ref = _oracle_chunk_states(x, s, h, sl)
+        nch = (L + C - 1) // C
+        slot = slot0[s]
+        for c in range(nch):
+            seg = slice(sl.start + c * C, sl.start + min((c + 1) * C, L))
+            S_all, M_all = bwd.rebuild_states(
+                k[seg, h][:, None], g["alpha"][seg, h][:, None], g["mu"][seg, h][:, None],
+                g["eta"][seg, h][:, None], g["beta"][seg, h][:, None],
+                vres[seg, h][:, None], Sc[slot + c, h][None], Mc[slot + c, h][None])
+            target = ref[c + 1] if c + 1 < nch else finals[(s, h)][1:]
+            got.append(np.stack([S_all[-1, 0], M_all[-1, 0]]))
+            want.append(np.stack([target[0], target[1]]))
+    got, want = np.stack(got), np.stack(want)
+    err = np.linalg.norm(got - want) / np.linalg.norm(want)
+    assert err <= TOL["bf16"], err
