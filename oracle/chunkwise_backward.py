@@ -253,3 +253,35 @@ def chain_backward(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
             g[name][sl] = val
     g["dS0"], g["dM0"] = dS, dM
     return g
+
+
+def chunk_backward_packed(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
+                          do=None, dS_T=None, dM_T=None, cu_seqlens=None, C=64,
+                          gate_partials=gate_partials_closed_form):
+    """Packed layout (q, k [T_total, H, dk]; v, do [T_total, H, dv]; gates
+    [T_total, H]; states and their adjoints [n_seq, H, dk, dv]), one chain at
+    a time.  Returns the same dict as ``backward.backward``."""
+    q = np.asarray(q, np.float64)
+    T_total, H, dk = q.shape
+    dv = np.asarray(v).shape[-1]
+    cu = [0, T_total] if cu_seqlens is None else [int(c) for c in cu_seqlens]
+    n_seq = len(cu) - 1
+    pick = lambda x, sl, h: None if x is None else np.asarray(x, np.float64)[sl, h]
+    pick_s = lambda x, s, h: None if x is None else np.asarray(x, np.float64)[s, h]
+    g = {"dq": np.zeros_like(q), "dk": np.zeros((T_total, H, dk)),
+         "dv": np.zeros((T_total, H, dv)), "dalpha": np.zeros((T_total, H)),
+         "dmu": np.zeros((T_total, H)), "deta": np.zeros((T_total, H)),
+         "dbeta": np.zeros((T_total, H)), "dS0": np.zeros((n_seq, H, dk, dv)),
+         "dM0": np.zeros((n_seq, H, dk, dv))}
+    for s in range(n_seq):
+        sl = slice(cu[s], cu[s + 1])
+        for h in range(H):
+            gc = chain_backward(pick(q, sl, h), pick(k, sl, h), pick(v, sl, h),
+                                pick(alpha, sl, h), pick(mu, sl, h), pick(eta, sl, h),
+                                pick(beta, sl, h), pick_s(S0, s, h), pick_s(M0, s, h),
+                                pick(do, sl, h), pick_s(dS_T, s, h), pick_s(dM_T, s, h),
+                                C=C, gate_partials=gate_partials)
+            for name in ("dq", "dk", "dv", "dalpha", "dmu", "deta", "dbeta"):
+                g[name][sl, h] = gc[name]
+            g["dS0"][s, h], g["dM0"][s, h] = gc["dS0"], gc["dM0"]
+    return g

@@ -286,3 +286,17 @@ def test_chunkwise_gradient_closed_form_equals_token_sweep(C, T):
         gate_partials=cbwd.gate_partials_closed_form)
     for name in ("dq", "dk", "dv", "dalpha", "dmu", "deta", "dbeta"):
         np.testing.assert_allclose(gc[name], g[name][:, 0], atol=1e-12, err_msg=name)
+
+
+def test_chunkwise_gradient_packed_heads():
+    """The packed, multi-head form (an empty sequence, ragged chunks) equals
+    the token sweep over the same layout."""
+    rng = np.random.default_rng(600)
+    lens = [70, 0, 9, 33]
+    x, cu = _inputs(rng, lens, 2, 3, 4, mu_zero_every=5)
+    W = _weights(rng, x, len(lens))
+    g = bwd.backward(**x, do=W[0], dS_T=W[1], dM_T=W[2], cu_seqlens=cu)
+    gc = cbwd.chunk_backward_packed(**x, do=W[0], dS_T=W[1], dM_T=W[2],
+                                    cu_seqlens=cu, C=16)
+    for name in g:
+        np.testing.assert_allclose(gc[name], g[name], atol=1e-12, err_msg=name)
