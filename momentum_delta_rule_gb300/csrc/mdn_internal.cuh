@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "mdn.h"
 
 namespace mdn {
@@ -115,15 +117,17 @@ cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 // Multiprocessor count of the current device, cached per device (0 when it
 // cannot be read).
 inline int device_sm_count() {
-    static int count[64] = {0};
+    // per device, filled on first use; atomic because host threads driving
+    // different streams may launch concurrently
+    static std::atomic<int> count[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (count[dev] == 0) {
-        int c = 0;
+    int c = count[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        count[dev] = c;
+        count[dev].store(c, std::memory_order_relaxed);
     }
-    return count[dev];
+    return c;
 }
 
 // ---------------------------------------------------------------- device
