@@ -1,6 +1,7 @@
 // C ABI of the MDN library: argument validation, workspace layout, dispatch
 // and the device status word.  Declarations and the contract: include/mdn.h.
 #include <stdint.h>
+#include <atomic>
 #include <string.h>
 
 #include "mdn_internal.cuh"
@@ -13,9 +14,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Filled on a device's first call.  Host threads may call concurrently:
+// `status` is written before `checked` is published (release) and read only
+// after `checked` is seen (acquire).
 struct DeviceInfo {
-    int checked;      // 0 = unknown, 1 = supported, -1 = unsupported
-    int *status;      // device address of g_mdn_status
+    std::atomic<int> checked;     // 0 = unknown, 1 = supported, -1 = unsupported
+    std::atomic<int *> status;    // device address of g_mdn_status
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -30,7 +34,8 @@ mdn_status current_device(int **status) {
     }
     if (dev < 0 || dev >= kMaxDevices) return MDN_ERR_UNSUPPORTED;
     DeviceInfo &di = g_dev[dev];
-    if (di.checked == 0) {
+    int checked = di.checked.load(std::memory_order_acquire);
+    if (checked == 0) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -38,19 +43,20 @@ mdn_status current_device(int **status) {
             return MDN_ERR_CUDA;
         }
         if (major != 10 || minor != 3) {
-            di.checked = -1;
+            checked = -1;
         } else {
             void *addr = nullptr;
             if (cudaGetSymbolAddress(&addr, g_mdn_status) != cudaSuccess) {
                 cudaGetLastError();
                 return MDN_ERR_CUDA;
             }
-            di.status = static_cast<int *>(addr);
-            di.checked = 1;
+            di.status.store(static_cast<int *>(addr), std::memory_order_relaxed);
+            checked = 1;
         }
+        di.checked.store(checked, std::memory_order_release);
     }
-    if (di.checked < 0) return MDN_ERR_UNSUPPORTED;
-    *status = di.status;
+    if (checked < 0) return MDN_ERR_UNSUPPORTED;
+    *status = di.status.load(std::memory_order_relaxed);
     return MDN_OK;
 }
 

@@ -18,6 +18,8 @@
 // in the same call.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "mdn_internal.cuh"
 
 static __device__ __align__(256) unsigned char g_mdn_static_ws[MDN_STATIC_WORKSPACE_BYTES];
@@ -25,7 +27,7 @@ static __device__ __align__(256) unsigned char g_mdn_static_ws[MDN_STATIC_WORKSP
 namespace {
 
 constexpr int kMaxDevices = 64;
-void *g_static_ws_addr[kMaxDevices];   // device address of g_mdn_static_ws, per device
+std::atomic<void *> g_static_ws_addr[kMaxDevices];   // device address of g_mdn_static_ws, per device
 
 }  // namespace
 
@@ -51,15 +53,15 @@ extern "C" mdn_status mdn_chunk_fwd_static_ws(
         return MDN_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return MDN_ERR_UNSUPPORTED;
-    if (g_static_ws_addr[dev] == nullptr) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_mdn_static_ws) != cudaSuccess || addr == nullptr) {
+    void *ws = g_static_ws_addr[dev].load(std::memory_order_relaxed);
+    if (ws == nullptr) {
+        if (cudaGetSymbolAddress(&ws, g_mdn_static_ws) != cudaSuccess || ws == nullptr) {
             cudaGetLastError();
             return MDN_ERR_CUDA;
         }
-        g_static_ws_addr[dev] = addr;
+        g_static_ws_addr[dev].store(ws, std::memory_order_relaxed);
     }
     return mdn_chunk_fwd(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, cu_seqlens, n_seq,
-                         B, T, H, dk, dv, dtype, chunk, g_static_ws_addr[dev],
+                         B, T, H, dk, dv, dtype, chunk, ws,
                          (size_t)MDN_STATIC_WORKSPACE_BYTES, stream);
 }
