@@ -300,3 +300,25 @@ def test_chunkwise_gradient_packed_heads():
                                     cu_seqlens=cu, C=16)
     for name in g:
         np.testing.assert_allclose(gc[name], g[name], atol=1e-12, err_msg=name)
+
+
+@pytest.mark.parametrize("C", [3, 16, 64])
+def test_chunkwise_gradient_forward_equals_recurrence(C):
+    """The forward the chunkwise gradient differentiates (chunk by chunk,
+    with its own saved quantities) is the recurrence itself."""
+    rng = np.random.default_rng(700 + C)
+    x, cu = _inputs(rng, [100], 1, 4, 3, mu_zero_every=6)
+    o_ref, S_ref, M_ref = recurrence.forward(
+        x["q"], x["k"], x["v"], x["alpha"], x["mu"], x["eta"], x["beta"],
+        x["S0"], x["M0"], cu_seqlens=cu)
+    S, M = x["S0"][0, 0], x["M0"][0, 0]
+    o = []
+    for s0 in range(0, 100, C):
+        sl = slice(s0, min(s0 + C, 100))
+        O, S, M, _ = cbwd._chunk_forward(
+            x["q"][sl, 0], x["k"][sl, 0], x["v"][sl, 0], x["alpha"][sl, 0],
+            x["mu"][sl, 0], x["eta"][sl, 0], x["beta"][sl, 0], S, M)
+        o.append(O)
+    np.testing.assert_allclose(np.concatenate(o), o_ref[:, 0], atol=1e-12)
+    np.testing.assert_allclose(S, S_ref[0, 0], atol=1e-12)
+    np.testing.assert_allclose(M, M_ref[0, 0], atol=1e-12)
