@@ -1,10 +1,21 @@
 #!/usr/bin/env python3
 """Benchmark of the MDN memory update on one GB300 (or N replicas).
 
-Main metric: chunkwise-forward tokens/s on the 400M-model-shaped prefill
-(B=8, H=8, T=2048, d=128, bf16 q/k/v, fp32 gates and states), plus the
-roofline fraction of its dominant kernel.  The decode step (256 sequences x
-16 heads x d=128, 1000 steps) is reported beside it in ``decode``.
+Main metric: chunkwise-forward tokens/s on the largest prefill workload, the
+variable-length packed batch (32768 tokens in sequences of 128..4096 tokens,
+H=16, d=128, bf16 q/k/v, fp32 gates and states), with the roofline of its
+dominant kernel and of the whole call.  The other prefill workloads (the
+400M- and 1.3B-model-shaped batches, the tiny fp32 case) follow under
+``other_workloads`` with the same keys; the decode step (256 sequences x 16
+heads x d=128, 1000 steps) is reported in ``decode``.
+
+Algorithmic work (what the method itself must move and compute, per token
+and head, d = dk = dv, C = 64): 12 d^2 + 8 C d + 4 C d + C^2 / 3 FLOP; HBM
+bytes: q, k, v read and o written (4 d elements), the gates (3 or 4 fp32),
+plus per (sequence, head) the initial states read (when given) and the final
+states written (2 d^2 fp32 each).  The prepared blocks the two kernels pass
+through HBM are an intermediate of this implementation, reported as such,
+never as algorithmic bytes.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
@@ -50,7 +61,7 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["mdn", "reference"], default="mdn")
-    p.add_argument("--workload", default=W.PREFILL_400M.name,
+    p.add_argument("--workload", default=W.VARLEN_PACKED.name,
                    choices=[w.name for w in W.ALL if not w.decode_steps])
     p.add_argument("--decode-steps", type=int, default=W.DECODE.decode_steps)
     p.add_argument("--no-decode", action="store_true")
@@ -148,13 +159,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_record(kernel_key, source_file):
-    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
-    the current source of the kernel (sha256 of its .cu file)."""
+def traffic_record(kernel_key, workload, source_file):
+    """Per-launch DRAM bytes of one kernel on one workload from a committed
+    ncu summary, if it was taken on the current source of the kernel (sha256
+    of its .cu file)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel_key)
+            rec = json.load(f).get("%s|%s" % (kernel_key, workload))
         with open(source_file, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
     except (OSError, ValueError, AttributeError):
@@ -166,41 +178,62 @@ def traffic_record(kernel_key, source_file):
 
 # ---------------------------------------------------------------- work units
 
-def flops_per_token_head(d, C=64):
-    """Algorithmic FLOPs of each stage per (token, head)."""
-    state = 12 * d * d + 4 * C * d        # K[S|M], Q[S|M], carry; T R, (A_O T) R
-    prep = 4 * C * d + 2 * C * C + C * C // 3   # two Grams, A_O T, triangular inverse
-    return {"prep": prep, "state": state}
+def path_flops_per_token_head(d, C=64):
+    """The method's algorithmic FLOPs per (token, head) for the whole chunk
+    forward: state products 12 d^2 (K and Q against [S | M], the carry),
+    Grams and the Y, Z rows 8 C d, U and the intra-chunk output 4 C d, the
+    triangular solve C^2 / 3."""
+    return 12 * d * d + 8 * C * d + 4 * C * d + C * C // 3
+
+
+def kernel_flops_per_token_head(d, C=64):
+    """FLOPs each kernel of this implementation performs per (token, head):
+    the state pass the state products and [T; A_O T] R (12 d^2 + 4 C d), the
+    prep the two Grams, A_O T and the triangular inverse."""
+    return {"prep": 4 * C * d + 2 * C * C + C * C // 3,
+            "state": 12 * d * d + 4 * C * d}
 
 
 PREP_BLOCK_BYTES = {True: 18432, False: 34816}   # tensor-core / CUDA-core layout
 
 
-def stage_bytes(x, tensor):
-    """Algorithmic HBM bytes of each stage.
-
-    prep : q and k read, the alpha/mu/eta (and beta) gates read, one prepared
-           block per (chunk, head) written.
-    state: q, k, v read and o written, the prepared blocks read, the initial
-           states read (when given) and the final states written.
-    """
+def io_bytes(x):
+    """Algorithmic HBM bytes, split by what reads or writes them."""
     el = 2 if x["dtype"] == "bf16" else 4
-    th = x["B"] * x["T"] * x["H"]
+    th = sum(seq_lengths(x)) * x["H"]
     D = x["D"]
-    chunks = sum((L + 63) // 64 for L in seq_lengths(x)) * x["H"]
-    blk = PREP_BLOCK_BYTES[bool(tensor)] * chunks
     n_gates = 3 + (1 if x["beta"] is not None else 0)
     n_chain = x["n_seq"] * x["H"]
-    states = (2 if x["S0"] is not None else 0) + 2
-    return {"prep": th * 2 * D * el + th * n_gates * 4 + blk,
-            "state": th * 4 * D * el + blk + n_chain * states * D * D * 4}
+    state = n_chain * D * D * 4
+    return {"qk": th * 2 * D * el, "v": th * D * el, "o": th * D * el,
+            "gates": th * n_gates * 4,
+            "states_in": 2 * state if x["S0"] is not None else 0,
+            "states_out": 2 * state}
 
 
-def stage_roofline(name, x, tensor, ms, peaks, peak_src):
-    """Binding roofline of one stage: whichever of HBM bytes or FLOPs needs
-    more time at the measured peak."""
-    fl = flops_per_token_head(x["D"])[name] * sum(seq_lengths(x)) * x["H"]
-    by = stage_bytes(x, tensor)[name]
+def intermediate_bytes(x, tensor):
+    """Prepared blocks written by the prep kernel and read by the state pass
+    (an intermediate of this implementation, not algorithmic work)."""
+    chunks = sum((L + 63) // 64 for L in seq_lengths(x)) * x["H"]
+    return PREP_BLOCK_BYTES[bool(tensor)] * chunks
+
+
+def algorithmic(x, what):
+    """(bytes, flops) of the whole path ("call") or of one kernel."""
+    b = io_bytes(x)
+    th = sum(seq_lengths(x)) * x["H"]
+    if what == "call":
+        return (sum(b.values()), path_flops_per_token_head(x["D"]) * th)
+    fl = kernel_flops_per_token_head(x["D"])[what] * th
+    if what == "prep":
+        return b["qk"] + b["gates"], fl
+    return b["qk"] + b["v"] + b["o"] + b["states_in"] + b["states_out"], fl
+
+
+def roofline_of(x, what, tensor, ms, peaks, peak_src):
+    """Binding roofline of the whole call or one kernel: whichever of its
+    algorithmic HBM bytes or FLOPs needs more time at the measured peak."""
+    by, fl = algorithmic(x, what)
     s = ms / 1e3
     if tensor:
         tflops_peak = peaks["bf16_tflops"]
@@ -210,18 +243,19 @@ def stage_roofline(name, x, tensor, ms, peaks, peak_src):
         fl_src = "fp32 FFMA from unit counts (152 SMs x 128 lanes x 2 x max clock)"
     t_fl = fl / (tflops_peak * 1e12)
     t_by = by / (peaks["hbm_gbs"] * 1e9)
+    common = {"algorithmic_bytes": by, "algorithmic_flops": fl, "ms": ms}
     if t_by >= t_fl:
         ach = by / s / 1e9
-        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": by,
-                "algorithmic_flops": fl, "kernel_ms": ms,
-                "peak_source": "%s HBM copy" % peak_src,
-                "other_roof_frac": (fl / s / 1e12) / tflops_peak}
-    ach = fl / s / 1e12
-    return {"bound": "tensor" if tensor else "alu", "achieved": ach, "peak": tflops_peak,
-            "unit": "TFLOP/s", "frac": ach / tflops_peak, "algorithmic_bytes": by,
-            "algorithmic_flops": fl, "kernel_ms": ms, "peak_source": fl_src,
-            "other_roof_frac": (by / s / 1e9) / peaks["hbm_gbs"]}
+        r = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": ach / peaks["hbm_gbs"], "peak_source": "%s HBM copy" % peak_src,
+             "other_roof_frac": (fl / s / 1e12) / tflops_peak}
+    else:
+        ach = fl / s / 1e12
+        r = {"bound": "tensor" if tensor else "alu", "achieved": ach, "peak": tflops_peak,
+             "unit": "TFLOP/s", "frac": ach / tflops_peak, "peak_source": fl_src,
+             "other_roof_frac": (by / s / 1e9) / peaks["hbm_gbs"]}
+    r.update(common)
+    return r
 
 
 def seq_lengths(x):
@@ -551,7 +585,7 @@ def time_decode(mdn, steps, dev, peaks):
             "roofline": {"bound": "hbm", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": traffic_record("decode_step", os.path.join(
+                         "traffic": traffic_record("decode_step", w.name, os.path.join(
                              ROOT, "momentum_delta_rule_gb300", "csrc", "mdn_decode.cu"))}}
 
 
@@ -575,6 +609,60 @@ def whole_job_rate(tokens_per_rank, max_ms, steps, world):
     replica of `tokens_per_rank` tokens per step, and the slowest rank's time
     (`max_ms` over `steps` steps) bounds the job."""
     return world * tokens_per_rank / (max_ms / steps / 1e3)
+
+
+KERNEL_SOURCES = {"chunk_prep_tc": "mdn_prep_tc.cu", "chunk_state_tc": "mdn_chunk_tc.cu",
+                  "chunk_prep_simt": "mdn_chunk_simt.cu", "chunk_state_simt": "mdn_chunk_simt.cu"}
+
+
+def measure_prefill(mdn, w, x, dev, args, steps, warmup, world, flush, peaks, peak_src,
+                    e2e=True):
+    """Device-timed chunk forward of one workload with its rooflines (the
+    dominant kernel's and the whole call's) and, optionally, the same metric
+    end to end from pinned host buffers."""
+    x_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    r = time_prefill(mdn, x_dev, w, steps, warmup, world, flush)
+    max_ms = max_over_ranks(r["total_ms"], world, dev)
+    tokens = sum(seq_lengths(x))
+    out = {"ms_per_step": max_ms / steps,
+           "value": whole_job_rate(tokens, max_ms, steps, world),
+           "tokens_per_step": tokens, "wall_s": r["wall_s"],
+           "gpu_launches": r["launches_per_step"] * steps}
+    tensor = r["path"] == 1
+    out["path"] = "tensor_core" if tensor else "cuda_core"
+    names = ["prep", "state"]
+    stage = max(range(2), key=lambda i: r["stage_ms"][i])
+    kind = "tc" if tensor else "simt"
+    stages = {}
+    for i, nm in enumerate(names):
+        key = "chunk_%s_%s" % (nm, kind)
+        rf = roofline_of(x, nm, tensor, r["stage_ms"][i], peaks, peak_src)
+        rf["kernel"] = key
+        rf["traffic"] = traffic_record(key, w.name, os.path.join(
+            ROOT, "momentum_delta_rule_gb300", "csrc", KERNEL_SOURCES[key]))
+        stages[nm] = rf
+    out["roofline"] = stages[names[stage]]
+    out["roofline_call"] = roofline_of(x, "call", tensor, out["ms_per_step"], peaks, peak_src)
+    out["roofline_call"]["what"] = "whole chunk forward (every kernel of the call)"
+    out["stages"] = stages
+    out["intermediate_bytes"] = {
+        "prepared_blocks": intermediate_bytes(x, tensor),
+        "what": "written by the prep kernel and read by the state pass; "
+                "not algorithmic work"}
+    out["config"] = config_of(w, x, "flushed before every timed step: 256 MiB written, "
+                                    "then another 256 MiB read")
+    out["dtype"] = "bf16" if tensor else "f32"
+    if e2e and not args.no_e2e:
+        n = max(3, min(steps, 10))
+        e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, n, 2)
+        e_ms = max_over_ranks(e_ms, world, dev)
+        out["e2e"] = {"value": whole_job_rate(tokens, e_ms, 1, world), "unit": "tokens/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": e_ms,
+                      "streams": "copies in, kernels and copies out on three streams, "
+                                 "two device buffer sets"}
+    out["_x_dev"] = x_dev
+    return out
 
 
 def main():
@@ -601,51 +689,31 @@ def main():
         return
     w = W.BY_NAME[args.workload]
     x = W.make_prefill(w)
-    x_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     flush = L2Flush(L2_FLUSH_BYTES, dev)
 
     clocks = ClockSampler(local).start()
-    r = time_prefill(mdn, x_dev, w, args.steps, args.warmup, world, flush)
+    m = measure_prefill(mdn, w, x, dev, args, args.steps, args.warmup, world, flush,
+                        peaks, peak_src, e2e=False)
     clk = clocks.stop()
-    max_ms = max_over_ranks(r["total_ms"], world, dev)
-    tokens = sum(seq_lengths(x))
-    ms_per_step = max_ms / args.steps
-    value = whole_job_rate(tokens, max_ms, args.steps, world)
-
-    # dominant kernel roofline (per launch, live CUDA-event duration)
-    tensor = r["path"] == 1
-    stage = max(range(2), key=lambda i: r["stage_ms"][i])
-    stage_name = ["prep", "state"][stage]
-    kernel_key = "chunk_%s_%s" % (stage_name, "tc" if tensor else "simt")
-    src = os.path.join(ROOT, "momentum_delta_rule_gb300", "csrc",
-                       ("mdn_prep_tc.cu" if stage_name == "prep" else "mdn_chunk_tc.cu")
-                       if tensor else "mdn_chunk_simt.cu")
-    roofline = stage_roofline(stage_name, x, tensor, r["stage_ms"][stage], peaks, peak_src)
-    roofline["kernel"] = kernel_key
-    roofline["traffic"] = traffic_record(kernel_key, src)
-    other = 1 - stage
-    stages = {["prep", "state"][i]: stage_roofline(["prep", "state"][i], x, tensor,
-                                                   r["stage_ms"][i], peaks, peak_src)
-              for i in range(2)}
-
-    line = {"metric": "MDN chunkwise fwd tokens/s", "value": value,
+    x_dev = m.pop("_x_dev")
+    tensor = m["path"] == "tensor_core"
+    line = {"metric": "MDN chunkwise fwd tokens/s", "value": m["value"],
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if tensor else "f32", "data": "synthetic",
-            "config": config_of(w, x, "flushed before every timed step: 256 MiB written, "
-                                      "then another 256 MiB read"),
-            "gpu_launches": r["launches_per_step"] * args.steps,
-            "path": "tensor_core" if tensor else "cuda_core",
-            "roofline": roofline, "stages": stages, "clocks": clk, "peaks": peak_src}
-
+            "dtype": m["dtype"], "data": "synthetic", "config": m["config"],
+            "gpu_launches": m["gpu_launches"], "path": m["path"],
+            "roofline": m["roofline"], "roofline_call": m["roofline_call"],
+            "stages": m["stages"], "intermediate_bytes": m["intermediate_bytes"],
+            "clocks": clk, "peaks": peak_src}
+    tokens = m["tokens_per_step"]
     if not args.no_vres and tensor:
         v_ms, v_bytes = time_vres(mdn, x_dev, max(3, min(args.steps, 10)), 2, flush)
         line["vres"] = {"what": "forward that also writes every token's residual "
                                 "(mdn_chunk_fwd_vres)",
                         "ms_per_step": v_ms, "tokens_per_s": tokens / (v_ms / 1e3),
                         "extra_bytes_written": v_bytes,
-                        "overhead_vs_forward": v_ms / ms_per_step - 1.0}
+                        "overhead_vs_forward": v_ms / m["ms_per_step"] - 1.0}
     if not args.no_inputs:
         line["inputs"] = time_inputs(mdn, x_dev, max(3, min(args.steps, 10)), 2, flush, peaks)
     if not args.no_e2e:
@@ -656,25 +724,21 @@ def main():
                        "ms_per_step": e_ms,
                        "streams": "copies in, kernels and copies out on three streams, "
                                   "two device buffer sets"}
+    del x_dev
     if not args.no_decode:
         line["decode"] = time_decode(mdn, args.decode_steps, dev, peaks)
     if not args.no_other_workloads:
         others = {}
+        n = max(3, min(args.steps, 5))
         for wo in W.ALL:
             if wo.decode_steps or wo.name == w.name:
                 continue
             xo = W.make_prefill(wo)
-            xo_dev = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in xo.items()}
-            ro = time_prefill(mdn, xo_dev, wo, max(3, min(args.steps, 5)), 3, world, flush)
-            tok = sum(seq_lengths(xo))
-            t_o = ro["path"] == 1
-            others[wo.name] = {
-                "tokens_per_s": tok / (ro["total_ms"] / max(3, min(args.steps, 5)) / 1e3),
-                "ms_per_step": ro["total_ms"] / max(3, min(args.steps, 5)),
-                "path": "tensor_core" if t_o else "cuda_core",
-                "stages": {nm: stage_roofline(nm, xo, t_o, ro["stage_ms"][i], peaks, peak_src)
-                           for i, nm in enumerate(["prep", "state"])}}
-            del xo_dev
+            mo = measure_prefill(mdn, wo, xo, dev, args, n, 3, world, flush, peaks, peak_src,
+                                 e2e=wo.D == 128)
+            mo.pop("_x_dev")
+            mo["tokens_per_s"] = mo.pop("value")
+            others[wo.name] = mo
         line["other_workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_oracle(x, args.cpu_seconds)

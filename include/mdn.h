@@ -102,7 +102,12 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
  *   decreasing, cu_seqlens[n_seq] == T): B must be 1 and the n_seq sequences
  *   are packed along T; sequence s owns tokens [cu_seqlens[s],
  *   cu_seqlens[s+1]).  Empty sequences are allowed (their final states equal
- *   their initial states).
+ *   their initial states).  cu_seqlens lives on the device, so it is checked
+ *   there: an array that breaks one of the three conditions makes the call
+ *   write MDN_ERR_INVALID_ARG into the device status word (see
+ *   mdn_get_device_status) and treat every sequence as empty (o is then not
+ *   written; S_T, M_T receive the initial states).  With T == 0 every
+ *   sequence is empty and cu_seqlens is not read.
  * States S0, M0, S_T, M_T: [n_seq, H, dk, dv] fp32.
  *
  * Arguments
@@ -239,8 +244,11 @@ mdn_status mdn_chunk_fwd_profiled(
  *    exceeds MDN_STATIC_WORKSPACE_BYTES the call returns MDN_ERR_UNSUPPORTED
  *    and enqueues nothing.
  *  - Set-up: the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current).  With lazy module
+ *    loading (the CUDA default) that lookup is also when the array receives
+ *    its device memory, so it can fail with MDN_ERR_CUDA if the device is out
+ *    of memory then: make the first call on each device before reserving the
+ *    device's memory, and before any stream capture.
  *  - Sharing: every call on a device uses the same array.  Nothing in it must
  *    start at zero (each call writes all it reads), but calls whose work
  *    overlaps on the GPU (other streams, other host threads) race on it:
@@ -308,10 +316,32 @@ mdn_status mdn_decode_step(const void *q, const void *k, const void *v,
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns MDN_OK if no kernel reported a problem since the
  * last read, MDN_ERR_DEVICE_TIMEOUT if a bounded device-side wait expired
- * (that launch's outputs are then undefined), MDN_ERR_CUDA if the
- * synchronisation or the read failed.
+ * (that launch's outputs are then undefined), MDN_ERR_INVALID_ARG if a chunk
+ * forward found its cu_seqlens malformed (see mdn_chunk_fwd), MDN_ERR_CUDA
+ * if the synchronisation or the read failed.
  */
 mdn_status mdn_get_device_status(void *stream);
+
+/*
+ * mdn_wait_selftest — checks the device-side failure path on the current
+ * device without faulting it.  Every wait inside the library's kernels is
+ * bounded: when it expires the kernel records MDN_ERR_DEVICE_TIMEOUT in the
+ * device status word, stops its other warps, frees its tensor memory and
+ * returns, so the context stays usable.  This call enqueues one small
+ * kernel (one CTA of two warps holding 32 tensor-memory columns) that waits
+ * with that same helper on a barrier nothing ever arrives at, with a limit
+ * of limit_us microseconds instead of the kernels' 1 s, so the limit always
+ * expires.  A later mdn_get_device_status(stream) then returns
+ * MDN_ERR_DEVICE_TIMEOUT (and clears it).  Not part of the method (the
+ * paper has no counterpart); it exists so that tests can exercise the
+ * timeout path.
+ *
+ * Arguments: limit_us in [1, 1000000]; stream as elsewhere.
+ * Errors: MDN_ERR_INVALID_ARG for limit_us out of range; MDN_ERR_UNSUPPORTED
+ * for a device other than compute capability 10.3; MDN_ERR_CUDA for a failed
+ * launch.
+ */
+mdn_status mdn_wait_selftest(int limit_us, void *stream);
 
 #ifdef __cplusplus
 }

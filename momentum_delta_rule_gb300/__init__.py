@@ -18,7 +18,8 @@ Entry points (same names as the C ABI):
   prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
                  log_mu_min=-2.0, comba_d=0.0) -> (q_hat, k_hat, alpha, beta, mu, eta)
   workspace_size(n_seq, T_total, H, D, dtype)
-  device_status(stream=None), abi_version(), status_string(code)
+  device_status(stream=None), wait_selftest(limit_us), abi_version(),
+  status_string(code)
 """
 import ctypes
 import os
@@ -26,7 +27,7 @@ import os
 import torch
 
 __all__ = ["chunk_fwd", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
-           "device_status",
+           "device_status", "wait_selftest",
            "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
 
@@ -47,7 +48,8 @@ EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_profiled", "mdn_chunk_fwd_static_ws",
                     "mdn_chunk_fwd_vres", "mdn_chunk_state_slots",
                     "mdn_chunk_fwd_states", "mdn_prepare_inputs",
-                    "mdn_decode_step", "mdn_get_device_status"]
+                    "mdn_decode_step", "mdn_get_device_status",
+                    "mdn_wait_selftest"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
 
@@ -104,6 +106,8 @@ def lib():
                                      + [c_int] * 4 + [c_float] * 6 + [vp])
     L.mdn_get_device_status.restype = c_int
     L.mdn_get_device_status.argtypes = [vp]
+    L.mdn_wait_selftest.restype = c_int
+    L.mdn_wait_selftest.argtypes = [c_int, vp]
     _LIB = L
     return L
 
@@ -349,6 +353,17 @@ def prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
     if st != MDN_OK:
         raise MdnError(st, "mdn_prepare_inputs")
     return (q_out, k_out) + tuple(gates)
+
+
+def wait_selftest(limit_us=2000, stream=None, device=None):
+    """Enqueue the library's bounded-wait self-test (a kernel waiting on a
+    barrier nothing arrives at, for ``limit_us`` microseconds); a later
+    ``device_status()`` reports ``MDN_ERR_DEVICE_TIMEOUT``."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = lib().mdn_wait_selftest(int(limit_us), _stream_handle(dev, stream))
+    if st != MDN_OK:
+        raise MdnError(st, "mdn_wait_selftest")
 
 
 def device_status(stream=None, device=None):

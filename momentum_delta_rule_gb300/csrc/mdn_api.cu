@@ -103,23 +103,19 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
 
 }  // extern "C"
 
-namespace {
+namespace mdn {
 
-// Every chunk-forward entry point: validation, workspace carve-up, path
-// choice and the launches.  vres (nullable) receives the per-token residuals.
-mdn_status chunk_fwd_impl(
-    const void *q, const void *k, const void *v, const float *alpha,
-    const float *mu, const float *eta, const float *beta, const float *S0,
-    const float *M0, void *o, float *S_T, float *M_T, void *vres,
-    float *S_chunks, float *M_chunks,
-    const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
-    mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
-    void *stream, void *const *stage_events, int n_stage_events,
-    int *path_out) {
-    if (n_stage_events != 0 && n_stage_events != 3) return MDN_ERR_INVALID_ARG;
-    if (n_stage_events && !stage_events) return MDN_ERR_INVALID_ARG;
-    for (int i = 0; i < n_stage_events; ++i)
-        if (!stage_events[i]) return MDN_ERR_INVALID_ARG;
+// Argument checks shared by every chunk-forward entry point (the workspace
+// is checked by the caller, since the entry points get it differently), then,
+// if `status` is not null, the device check, whose success stores the device
+// status word there.
+mdn_status chunk_fwd_check(const void *q, const void *k, const void *v, const float *alpha,
+                           const float *mu, const float *eta, const float *beta,
+                           const float *S0, const float *M0, const void *o, const float *S_T,
+                           const float *M_T, const void *vres, const float *S_chunks,
+                           const float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                           int B, int T, int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                           int **status) {
     // ---- shapes
     if (B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || n_seq < 0)
         return MDN_ERR_INVALID_ARG;
@@ -147,6 +143,34 @@ mdn_status chunk_fwd_impl(
         (M_T && M_T != M0 && M0 && (const void *)M_T == (const void *)S0))
         return MDN_ERR_INVALID_ARG;
     if (S_T && M_T && S_T == M_T) return MDN_ERR_INVALID_ARG;
+    // ---- device
+    return status ? current_device(status) : MDN_OK;
+}
+
+}  // namespace mdn
+
+namespace {
+
+// Every chunk-forward entry point: validation, workspace carve-up, path
+// choice and the launches.  vres (nullable) receives the per-token residuals.
+mdn_status chunk_fwd_impl(
+    const void *q, const void *k, const void *v, const float *alpha,
+    const float *mu, const float *eta, const float *beta, const float *S0,
+    const float *M0, void *o, float *S_T, float *M_T, void *vres,
+    float *S_chunks, float *M_chunks,
+    const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
+    mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
+    void *stream, void *const *stage_events, int n_stage_events,
+    int *path_out) {
+    if (n_stage_events != 0 && n_stage_events != 3) return MDN_ERR_INVALID_ARG;
+    if (n_stage_events && !stage_events) return MDN_ERR_INVALID_ARG;
+    for (int i = 0; i < n_stage_events; ++i)
+        if (!stage_events[i]) return MDN_ERR_INVALID_ARG;
+    mdn_status st = mdn::chunk_fwd_check(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T,
+                                         vres, S_chunks, M_chunks, cu_seqlens, n_seq, B, T, H,
+                                         dk, dv, dtype, chunk, nullptr);
+    if (st != MDN_OK) return st;
+    const long T_total = (long)B * T;
     const size_t need = mdn_chunk_fwd_workspace_size(n_seq, (int)T_total, H, dk, dv, dtype);
     if (n_seq > 0 && T_total > 0) {
         if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
@@ -154,7 +178,7 @@ mdn_status chunk_fwd_impl(
     }
 
     int *status = nullptr;
-    mdn_status st = current_device(&status);
+    st = current_device(&status);
     if (st != MDN_OK) return st;
     if (n_seq == 0) return MDN_OK;
 
@@ -164,12 +188,13 @@ mdn_status chunk_fwd_impl(
     p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
     p.S0 = S0; p.M0 = M0; p.o = o; p.S_T = S_T; p.M_T = M_T; p.vres = vres;
     p.S_chunks = S_chunks; p.M_chunks = M_chunks;
-    p.cu_seqlens = cu_seqlens;
+    // with no tokens every sequence is empty: cu_seqlens is not read
+    p.cu_seqlens = T_total > 0 ? cu_seqlens : nullptr;
     p.n_seq = n_seq; p.B = B; p.T = T; p.H = H; p.D = dk;
     p.T_total = (int)T_total;
     p.dtype = dtype;
     p.status = status;
-    if (cu_seqlens) {
+    if (p.cu_seqlens) {
         p.max_chunks = (int)chunk_slots_bound(n_seq, (int)T_total);
     } else {
         p.max_chunks = B * ((T + mdn::kChunk - 1) / mdn::kChunk);
@@ -177,7 +202,7 @@ mdn_status chunk_fwd_impl(
     if (T_total == 0) p.max_chunks = 0;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     p.chunk_offsets = reinterpret_cast<int32_t *>(ws);
-    p.seq_order = (cu_seqlens && ws)
+    p.seq_order = (p.cu_seqlens && ws)
                       ? reinterpret_cast<int32_t *>(ws + round256(sizeof(int32_t) * ((size_t)n_seq + 1)))
                       : nullptr;
     p.prep = ws ? ws + meta_bytes(n_seq) : nullptr;
@@ -194,7 +219,7 @@ mdn_status chunk_fwd_impl(
     if (path_out) *path_out = path;
     cudaError_t err = cudaSuccess;
     if (ev[0]) err = cudaEventRecord(ev[0], cs);
-    if (err == cudaSuccess && cu_seqlens && p.max_chunks > 0)
+    if (err == cudaSuccess && p.cu_seqlens && p.max_chunks > 0)
         err = mdn::launch_chunk_offsets(p, cs);
     if (err == cudaSuccess)
         err = tensor ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs);
@@ -357,6 +382,19 @@ mdn_status mdn_decode_step(const void *q, const void *k, const void *v,
     p.N = N; p.H = H; p.D = dk; p.dtype = dtype;
     p.status = status;
     if (mdn::launch_decode(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    return MDN_OK;
+}
+
+mdn_status mdn_wait_selftest(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000) return MDN_ERR_INVALID_ARG;
+    int *status = nullptr;
+    mdn_status st = current_device(&status);
+    if (st != MDN_OK) return st;
+    if (mdn::launch_wait_selftest((uint64_t)limit_us * 1000u, status,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return MDN_ERR_CUDA;
     }

@@ -41,10 +41,31 @@ constexpr int kThreads = 256;     // prep
 // order[] = the sequences sorted by decreasing length (ties by index): the
 // rank of s counts the sequences that come before it.  Quadratic in n_seq,
 // so beyond kMaxOrdered sequences the order is the identity.
+//
+// The offsets are checked first: cu[0] == 0, cu[s] <= cu[s + 1] and
+// cu[n_seq] == T_total.  An offset array that breaks any of these would put
+// chunk slots past the workspace and token rows past the tensors, so it is
+// rejected on the device: MDN_ERR_INVALID_ARG goes to the status word, every
+// chunk offset is written as 0 (every later kernel then finds no chunk to
+// work on, and each state pass clamps its sequence to no tokens) and the
+// order is the identity.
 constexpr int kMaxOrdered = 4096;
 
 __global__ void __launch_bounds__(1024)
-chunk_offsets_kernel(const int32_t *cu, int n_seq, int32_t *off, int32_t *order) {
+chunk_offsets_kernel(const int32_t *cu, int n_seq, int T_total, int32_t *off, int32_t *order,
+                     int *status) {
+    int bad = 0;
+    for (int s = threadIdx.x; s < n_seq; s += blockDim.x)
+        bad |= cu[s] > cu[s + 1];
+    if (threadIdx.x == 0) bad |= (cu[0] != 0) || (cu[n_seq] != T_total);
+    if (__syncthreads_or(bad)) {
+        for (int s = threadIdx.x; s <= n_seq; s += blockDim.x) {
+            off[s] = 0;
+            if (order && s < n_seq) order[s] = s;
+        }
+        if (threadIdx.x == 0 && status) atomicExch(status, (int)MDN_ERR_INVALID_ARG);
+        return;
+    }
     if (order) {
         for (int s = threadIdx.x; s < n_seq; s += blockDim.x) {
             int rank = s;
@@ -747,8 +768,8 @@ cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
-    chunk_offsets_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.chunk_offsets,
-                                              p.seq_order);
+    chunk_offsets_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.T_total,
+                                              p.chunk_offsets, p.seq_order, p.status);
     return cudaGetLastError();
 }
 

@@ -106,6 +106,17 @@ struct InputsProblem {
     float a, b, s, tau, log_mu_min, comba_d;
 };
 
+// Shape and pointer checks of the chunk-forward entry points (all but the
+// workspace), then, if `status` is not null, the device check, whose success
+// stores the device status word there.
+mdn_status chunk_fwd_check(const void *q, const void *k, const void *v, const float *alpha,
+                           const float *mu, const float *eta, const float *beta,
+                           const float *S0, const float *M0, const void *o, const float *S_T,
+                           const float *M_T, const void *vres, const float *S_chunks,
+                           const float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                           int B, int T, int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                           int **status);
+
 cudaError_t launch_prepare_inputs(const InputsProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
@@ -113,6 +124,7 @@ cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t st);
 
 // Multiprocessor count of the current device, cached per device (0 when it
 // cannot be read).
@@ -195,9 +207,15 @@ __device__ __forceinline__ void sequence_range(const ChunkProblem &p, int s,
         len = p.T;
         slot0 = s * ((p.T + kChunk - 1) / kChunk);
     } else {
+        // Packed sequences exist only with T_total > 0 (the API drops
+        // cu_seqlens otherwise), so the chunk offsets have been computed.
+        // The sequence keeps at most the chunks its offsets give it: all of
+        // them for valid offsets (ceil(len / 64)), none when the offsets
+        // kernel rejected cu_seqlens and zeroed them.
         start = p.cu_seqlens[s];
         len = p.cu_seqlens[s + 1] - start;
-        slot0 = len > 0 ? p.chunk_offsets[s] : 0;   // offsets exist only if T > 0
+        slot0 = p.chunk_offsets[s];
+        len = max(0, min(len, (p.chunk_offsets[s + 1] - slot0) * kChunk));
     }
 }
 

@@ -12,10 +12,13 @@
 // The array below is a file-scope __device__ variable.  Its name in host code
 // is only a host-side stand-in, not a device address: the device address is
 // fetched with cudaGetSymbolAddress, once per device, with that device
-// current, on the first call made on that device.  Every call on a device
-// shares the array and it keeps the previous call's contents; nothing in it
-// needs to start at zero, because every byte a call reads was written earlier
-// in the same call.
+// current, on the first call made on that device.  Under lazy module loading
+// that first lookup is also where this file's module is loaded and the array
+// gets its device memory, so the first call on each device must come before
+// the caller reserves the device's memory (and before any stream capture).
+// Every call on a device shares the array and it keeps the previous call's
+// contents; nothing in it needs to start at zero, because every byte a call
+// reads was written earlier in the same call.
 #include <stdint.h>
 
 #include <atomic>
@@ -27,7 +30,10 @@ static __device__ __align__(256) unsigned char g_mdn_static_ws[MDN_STATIC_WORKSP
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::atomic<void *> g_static_ws_addr[kMaxDevices];   // device address of g_mdn_static_ws, per device
+// Device address of g_mdn_static_ws, per device.  Relaxed ordering is
+// enough: the cached value is the same pointer whichever thread looks it up
+// (a second lookup is harmless) and it guards no other data.
+std::atomic<void *> g_static_ws_addr[kMaxDevices];
 
 }  // namespace
 
@@ -36,14 +42,14 @@ extern "C" mdn_status mdn_chunk_fwd_static_ws(
     const float *eta, const float *beta, const float *S0, const float *M0, void *o,
     float *S_T, float *M_T, const int32_t *cu_seqlens, int n_seq, int B, int T, int H,
     int dk, int dv, mdn_dtype dtype, int chunk, void *stream) {
+    // the same shape, pointer and device checks as mdn_chunk_fwd, first, so
+    // that every error it would report comes back here unchanged
+    int *status = nullptr;
+    const mdn_status st = mdn::chunk_fwd_check(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T,
+                                               M_T, nullptr, nullptr, nullptr, cu_seqlens, n_seq,
+                                               B, T, H, dk, dv, dtype, chunk, &status);
+    if (st != MDN_OK) return st;
     const long T_total = (long)B * (long)T;
-    const bool sizes_ok = B >= 0 && T >= 0 && n_seq >= 0 && H > 0 && dk > 0 && dv > 0 &&
-                          T_total <= 0x3fffffffL;
-    if (!sizes_ok) {
-        // let the regular entry point report the invalid argument
-        return mdn_chunk_fwd(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, cu_seqlens,
-                             n_seq, B, T, H, dk, dv, dtype, chunk, nullptr, 0, stream);
-    }
     const size_t need = mdn_chunk_fwd_workspace_size(n_seq, (int)T_total, H, dk, dv, dtype);
     if (need > (size_t)MDN_STATIC_WORKSPACE_BYTES) return MDN_ERR_UNSUPPORTED;
 

@@ -80,6 +80,32 @@ def test_chunk_fwd_rejects(L, over, code):
     assert _chunk(L, **over) == code
 
 
+def _chunk_static(L, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
+                beta=None, S0=None, M0=None, o=FAKE, S_T=None, M_T=None,
+                cu=None, n_seq=2, B=2, T=64, H=2, dk=128, dv=128, dtype=1,
+                chunk=64, stream=None)
+    args.update(over)
+    return L.mdn_chunk_fwd_static_ws(args["q"], args["k"], args["v"], args["alpha"],
+                                     args["mu"], args["eta"], args["beta"], args["S0"],
+                                     args["M0"], args["o"], args["S_T"], args["M_T"],
+                                     args["cu"], args["n_seq"], args["B"], args["T"],
+                                     args["H"], args["dk"], args["dv"], args["dtype"],
+                                     args["chunk"], args["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    # the argument errors of mdn_chunk_fwd come first, even for problems whose
+    # scratch would exceed the fixed array
+    (dict(n_seq=1 << 24), 1), (dict(q=None), 1), (dict(dtype=5), 1),
+    (dict(cu=FAKE, B=2), 1), (dict(S_T=FAKE, M_T=FAKE), 1),
+    (dict(chunk=32), 2), (dict(dk=96, dv=96), 2),
+    (dict(chunk=32, n_seq=1 << 24, B=1 << 24), 2),
+])
+def test_chunk_fwd_static_ws_rejects_like_chunk_fwd(L, over, code):
+    assert _chunk_static(L, **over) == code
+
+
 def _chunk_vres(L, vres, **over):
     args = dict(q=FAKE, k=FAKE, v=FAKE, alpha=FAKE, mu=FAKE, eta=FAKE,
                 beta=None, S0=None, M0=None, o=FAKE, S_T=None, M_T=None,
