@@ -197,6 +197,68 @@ mdn_status mdn_chunk_fwd_states(const void *q, const void *k, const void *v,
                                 int chunk, void *workspace, size_t workspace_bytes,
                                 void *stream);
 
+/*
+ * Bytes of device workspace mdn_chunk_bwd needs (a multiple of 256; 0 for
+ * invalid sizes): per (chunk slot, head) the chunk's matrices and vectors
+ * (84 KB), the state adjoints at the chunk's end (2 dk dv fp32) and the
+ * residual adjoints (64 dv fp32); the slot bound is mdn_chunk_state_slots'.
+ */
+size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk,
+                                    int dv, mdn_dtype dtype);
+
+/*
+ * mdn_chunk_bwd — gradient of the chunk forward: given the adjoints of its
+ * outputs (dout for o, dS_T and dM_T for the final states), the gradients
+ * with respect to every input, q, k, v, the four gates and the initial
+ * states.
+ *
+ * Defined by: the pages give the training storage policy, not gradient
+ * formulas: the forward keeps what the backward needs so that states need
+ * not be stored per token (slides, frame "The implementation trades saved
+ * residuals for throughput" and its "Backward computation" block; reading
+ * notes, end of section 2.6).  Here the saved data are the entry states of
+ * every chunk (mdn_chunk_fwd_states), and the result is the exact
+ * vector-Jacobian product of the chunk equations (frames "Solve the unknown
+ * residuals with a lower triangular system", Eqs. (15)-(18), and "Chunk
+ * outputs combine incoming states and local writes", Appendix C Eqs.
+ * (40)-(42)): a reverse pass over the chunks carries the state adjoints,
+ * then every chunk forms its input gradients in parallel.  The gates'
+ * gradients go through the chunk coefficients without dividing by a gate,
+ * so mu = 0 is exact.  Arithmetic is fp32 on the CUDA cores.
+ *
+ * Layout and sizes as mdn_chunk_fwd (equal lengths, or packed with
+ * cu_seqlens; the same device checks of cu_seqlens apply).
+ * Arguments
+ *   q, k, v, alpha, mu, eta, beta   the forward's inputs (beta NULL: 1)
+ *   S_chunks, M_chunks   the forward's chunk entry states, exactly as
+ *                  mdn_chunk_fwd_states wrote them for these inputs and
+ *                  initial states (fp32 [slots, H, dk, dv])
+ *   dout           adjoint of o (dtype, laid out like o); required
+ *   dS_T, dM_T     adjoints of the final states (fp32 [n_seq, H, dk, dv]) or
+ *                  NULL for zero
+ *   dq, dk, dv     gradients (dtype, laid out like q, k, v); required
+ *   dalpha, dmu, deta   gradients of the gates (fp32 [B, T, H]); required
+ *   dbeta          gradient of beta (fp32) or NULL to skip it; with beta
+ *                  NULL it is the gradient at beta = 1
+ *   dS0, dM0       gradients of the initial states (fp32) or NULL to skip
+ *   workspace      at least mdn_chunk_bwd_workspace_size(...) bytes,
+ *                  256-byte aligned; contents undefined on exit
+ * Every output must be distinct from every input and from the other
+ * outputs.  Errors: as mdn_chunk_fwd, and MDN_ERR_INVALID_ARG for a missing
+ * required pointer, a misaligned one, an output that aliases, or a workspace
+ * that is too small.
+ */
+mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *mu, const float *eta,
+                         const float *beta, const float *S_chunks,
+                         const float *M_chunks, const void *dout,
+                         const float *dS_T, const float *dM_T, void *dq,
+                         void *dk_out, void *dv_out, float *dalpha, float *dmu,
+                         float *deta, float *dbeta, float *dS0, float *dM0,
+                         const int32_t *cu_seqlens, int n_seq, int B, int T,
+                         int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* Implementation paths of mdn_chunk_fwd (reported by the profiled variant). */
 typedef enum mdn_path {
     MDN_PATH_CUDA_CORE = 0,   /* fp32 FFMA kernels: fp32 inputs, head size 64 */

@@ -26,7 +26,7 @@ import os
 
 import torch
 
-__all__ = ["chunk_fwd", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
+__all__ = ["chunk_fwd", "chunk_bwd", "chunk_bwd_workspace_size", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
            "device_status", "wait_selftest",
            "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
@@ -49,7 +49,8 @@ EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_vres", "mdn_chunk_state_slots",
                     "mdn_chunk_fwd_states", "mdn_prepare_inputs",
                     "mdn_decode_step", "mdn_get_device_status",
-                    "mdn_wait_selftest"]
+                    "mdn_wait_selftest", "mdn_chunk_bwd_workspace_size",
+                    "mdn_chunk_bwd"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
 
@@ -108,6 +109,10 @@ def lib():
     L.mdn_get_device_status.argtypes = [vp]
     L.mdn_wait_selftest.restype = c_int
     L.mdn_wait_selftest.argtypes = [c_int, vp]
+    L.mdn_chunk_bwd_workspace_size.restype = c_size
+    L.mdn_chunk_bwd_workspace_size.argtypes = [c_int] * 6
+    L.mdn_chunk_bwd.restype = c_int
+    L.mdn_chunk_bwd.argtypes = [vp] * 22 + [c_int] * 8 + [vp, c_size, vp]
     _LIB = L
     return L
 
@@ -353,6 +358,76 @@ def prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
     if st != MDN_OK:
         raise MdnError(st, "mdn_prepare_inputs")
     return (q_out, k_out) + tuple(gates)
+
+
+def chunk_bwd(q, k, v, alpha, mu, eta, S_chunks, M_chunks, dout, beta=None,
+              dS_T=None, dM_T=None, cu_seqlens=None, need_dbeta=True,
+              need_dstates=True, workspace=None, stream=None):
+    """Gradients of the chunk forward (``mdn_chunk_bwd``).
+
+    Inputs as ``chunk_fwd`` plus the forward's chunk entry states
+    ``S_chunks``, ``M_chunks`` (``chunk_fwd(..., return_chunk_states=True)``),
+    the adjoint ``dout`` of o and optionally ``dS_T``, ``dM_T``.  Returns a
+    dict with dq, dk, dv (dtype of q), dalpha, dmu, deta, dbeta (fp32, dbeta
+    None unless ``need_dbeta``), dS0, dM0 (None unless ``need_dstates``).
+    """
+    L = lib()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, D]")
+    B, T, H, D = q.shape
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _check_cuda(name, t, q.dtype, dev)
+        if tuple(t.shape) != (B, T, H, D):
+            raise ValueError("%s must be [B, T, H, D]" % name)
+    for name, t in (("alpha", alpha), ("mu", mu), ("eta", eta), ("beta", beta)):
+        if name != "beta" and t is None:
+            raise ValueError("%s is required" % name)
+        _check_cuda(name, t, torch.float32, dev)
+        if t is not None and tuple(t.shape) != (B, T, H):
+            raise ValueError("%s must be [B, T, H]" % name)
+    if cu_seqlens is not None:
+        _check_cuda("cu_seqlens", cu_seqlens, torch.int32, dev)
+        n_seq = cu_seqlens.numel() - 1
+    else:
+        n_seq = B
+    slots = chunk_state_slots(n_seq, B, T, cu_seqlens is not None)
+    for name, t in (("S_chunks", S_chunks), ("M_chunks", M_chunks)):
+        _check_cuda(name, t, torch.float32, dev)
+        if t.dim() != 4 or t.shape[0] < slots or tuple(t.shape[1:]) != (H, D, D):
+            raise ValueError("%s must be [>= %d, H, D, D]" % (name, slots))
+    for name, t in (("dS_T", dS_T), ("dM_T", dM_T)):
+        _check_cuda(name, t, torch.float32, dev)
+        if t is not None and tuple(t.shape) != (n_seq, H, D, D):
+            raise ValueError("%s must be [n_seq, H, D, D]" % name)
+    g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+         "dalpha": torch.empty_like(alpha), "dmu": torch.empty_like(alpha),
+         "deta": torch.empty_like(alpha),
+         "dbeta": torch.empty_like(alpha) if need_dbeta else None,
+         "dS0": (torch.empty((n_seq, H, D, D), dtype=torch.float32, device=dev)
+                 if need_dstates else None)}
+    g["dM0"] = torch.empty_like(g["dS0"]) if need_dstates else None
+    need = int(L.mdn_chunk_bwd_workspace_size(n_seq, B * T, H, D, D, code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace, torch.uint8, dev)
+    with torch.cuda.device(dev):
+        st = L.mdn_chunk_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(mu), _ptr(eta), _ptr(beta),
+            _ptr(S_chunks), _ptr(M_chunks), _ptr(dout), _ptr(dS_T), _ptr(dM_T),
+            _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dalpha"]), _ptr(g["dmu"]),
+            _ptr(g["deta"]), _ptr(g["dbeta"]), _ptr(g["dS0"]), _ptr(g["dM0"]),
+            _ptr(cu_seqlens), n_seq, B, T, H, D, D, code, CHUNK, _ptr(workspace),
+            workspace.numel(), _stream_handle(dev, stream))
+    if st != MDN_OK:
+        raise MdnError(st, "mdn_chunk_bwd")
+    return g
+
+
+def chunk_bwd_workspace_size(n_seq, T_total, H, D, dtype):
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().mdn_chunk_bwd_workspace_size(n_seq, T_total, H, D, D, code))
 
 
 def wait_selftest(limit_us=2000, stream=None, device=None):

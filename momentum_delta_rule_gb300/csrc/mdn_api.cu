@@ -388,6 +388,103 @@ mdn_status mdn_decode_step(const void *q, const void *k, const void *v,
     return MDN_OK;
 }
 
+size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk, int dv,
+                                    mdn_dtype dtype) {
+    if (n_seq < 0 || T_total < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
+    if (dtype != MDN_F32 && dtype != MDN_BF16) return 0;
+    const size_t per = mdn::BwdLayout::kBytes + sizeof(float) * (2 * (size_t)dk * dv +
+                                                                 (size_t)mdn::kChunk * dv);
+    const size_t slots = (size_t)chunk_slots_bound(n_seq, T_total) * (size_t)H;
+    return round256(meta_bytes(n_seq) + slots * per);
+}
+
+mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *mu, const float *eta, const float *beta,
+                         const float *S_chunks, const float *M_chunks, const void *dout,
+                         const float *dS_T, const float *dM_T, void *dq, void *dk_out,
+                         void *dv_out, float *dalpha, float *dmu, float *deta, float *dbeta,
+                         float *dS0, float *dM0, const int32_t *cu_seqlens, int n_seq, int B,
+                         int T, int H, int dk, int dv, mdn_dtype dtype, int chunk,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    // shapes and the forward's own inputs as mdn_chunk_fwd checks them
+    mdn_status st = mdn::chunk_fwd_check(q, k, v, alpha, mu, eta, beta, nullptr, nullptr, dout,
+                                         nullptr, nullptr, nullptr, nullptr, nullptr, cu_seqlens,
+                                         n_seq, B, T, H, dk, dv, dtype, chunk, nullptr);
+    if (st != MDN_OK) return st;
+    const long T_total = (long)B * T;
+    if (T_total > 0) {
+        const void *need[] = {S_chunks, M_chunks, dq, dk_out, dv_out, dalpha, dmu, deta};
+        for (const void *ptr : need)
+            if (!ptr) return MDN_ERR_INVALID_ARG;
+    }
+    const void *ptrs16[] = {S_chunks, M_chunks, dS_T, dM_T, dq, dk_out, dv_out, dS0, dM0};
+    for (const void *ptr : ptrs16)
+        if (ptr && !aligned16(ptr)) return MDN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {dalpha, dmu, deta, dbeta};
+    for (const void *ptr : ptrs4)
+        if (ptr && ((uintptr_t)ptr & 3u)) return MDN_ERR_INVALID_ARG;
+    // no output may be an input or another output
+    const void *ins[] = {q, k, v, alpha, mu, eta, beta, S_chunks, M_chunks, dout, dS_T, dM_T,
+                         cu_seqlens};
+    const void *outs[] = {dq, dk_out, dv_out, dalpha, dmu, deta, dbeta, dS0, dM0};
+    for (int a = 0; a < 9; ++a) {
+        if (!outs[a]) continue;
+        for (const void *in : ins)
+            if (in == outs[a]) return MDN_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 9; ++b)
+            if (outs[b] == outs[a]) return MDN_ERR_INVALID_ARG;
+    }
+    const size_t need = mdn_chunk_bwd_workspace_size(n_seq, (int)T_total, H, dk, dv, dtype);
+    if (n_seq > 0 && T_total > 0) {
+        if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
+            return MDN_ERR_INVALID_ARG;
+    }
+    int *status = nullptr;
+    st = current_device(&status);
+    if (st != MDN_OK) return st;
+    if (n_seq == 0) return MDN_OK;
+
+    mdn::BwdProblem p;
+    memset(&p, 0, sizeof(p));
+    mdn::ChunkProblem &L = p.loc;
+    L.cu_seqlens = T_total > 0 ? cu_seqlens : nullptr;
+    L.n_seq = n_seq; L.B = B; L.T = T; L.H = H; L.D = dk;
+    L.T_total = (int)T_total;
+    L.dtype = dtype;
+    L.status = status;
+    L.max_chunks = T_total == 0 ? 0
+                 : L.cu_seqlens ? (int)chunk_slots_bound(n_seq, (int)T_total)
+                                : B * ((T + mdn::kChunk - 1) / mdn::kChunk);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    L.chunk_offsets = reinterpret_cast<int32_t *>(ws);
+    L.seq_order = (L.cu_seqlens && ws && L.max_chunks > 0)
+                      ? reinterpret_cast<int32_t *>(ws + round256(sizeof(int32_t) * ((size_t)n_seq + 1)))
+                      : nullptr;
+    const size_t slots = ws ? (size_t)chunk_slots_bound(n_seq, (int)T_total) * (size_t)H : 0;
+    unsigned char *base = ws ? ws + meta_bytes(n_seq) : nullptr;
+    p.prep = base;
+    p.adj = base ? reinterpret_cast<float *>(base + slots * mdn::BwdLayout::kBytes) : nullptr;
+    p.dR = p.adj ? p.adj + slots * 2 * (size_t)dk * dv : nullptr;
+    p.q = q; p.k = k; p.v = v; p.dout = dout;
+    p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
+    p.S_chunks = S_chunks; p.M_chunks = M_chunks;
+    p.dS_T = dS_T; p.dM_T = dM_T;
+    p.dq = dq; p.dk = dk_out; p.dv = dv_out;
+    p.dalpha = dalpha; p.dmu = dmu; p.deta = deta; p.dbeta = dbeta;
+    p.dS0 = dS0; p.dM0 = dM0;
+    p.D = dk;
+    p.dtype = dtype;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    if (L.cu_seqlens && L.max_chunks > 0) err = mdn::launch_chunk_offsets(L, cs);
+    if (err == cudaSuccess) err = mdn::launch_chunk_bwd(p, cs);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return MDN_ERR_CUDA;
+    }
+    return MDN_OK;
+}
+
 mdn_status mdn_wait_selftest(int limit_us, void *stream) {
     if (limit_us < 1 || limit_us > 1000000) return MDN_ERR_INVALID_ARG;
     int *status = nullptr;

@@ -106,6 +106,33 @@ struct InputsProblem {
     float a, b, s, tau, log_mu_min, comba_d;
 };
 
+// Gradient pass (mdn_chunk_bwd).  `loc` carries the chunk geometry (packed
+// offsets, sequence order, status word) for the shared location helpers.
+struct BwdProblem {
+    ChunkProblem loc;
+    const void *q, *k, *v, *dout;
+    const float *alpha, *mu, *eta, *beta;
+    const float *S_chunks, *M_chunks;  // entry states of every chunk [slot, H, dk, dv]
+    const float *dS_T, *dM_T;          // adjoints of the final states, or nullptr (zero)
+    void *dq, *dk, *dv;
+    float *dalpha, *dmu, *deta, *dbeta;
+    float *dS0, *dM0;
+    unsigned char *prep;               // per (slot, head): chunk matrices and vectors
+    float *adj;                        // per (slot, head): dS, dM at the chunk's end [2, dk, dv]
+    float *dR;                         // per (slot, head): residual adjoints [64, dv]
+    int D;
+    mdn_dtype dtype;
+};
+
+// Per-(slot, head) block of the gradient pass, fp32: five 64 x 64 matrices
+// (T, A = (Q Kh^T) . Gamma, X = P Kh^T, Y = Q Kh^T, Gamma), then vector rows.
+struct BwdLayout {
+    static constexpr int kMat = kChunk * kChunk;
+    enum { kT = 0, kA = 1, kX = 2, kY = 3, kG = 4, kMats = 5 };
+    enum { vAbar = 0, vB, vAbarM, vBM, vGS, vMuTail, vScal, kRows = 8 };
+    static constexpr size_t kBytes = sizeof(float) * ((size_t)kMats * kMat + (size_t)kRows * kChunk);
+};
+
 // Shape and pointer checks of the chunk-forward entry points (all but the
 // workspace), then, if `status` is not null, the device check, whose success
 // stores the device status word there.
@@ -125,6 +152,7 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t st);
+cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t st);
 
 // Multiprocessor count of the current device, cached per device (0 when it
 // cannot be read).

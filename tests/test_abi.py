@@ -252,3 +252,39 @@ def test_missing_library_fails_loudly(tmp_path):
                          text=True, timeout=300)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "raised True", out.stdout + out.stderr
+
+
+def _bwd(L, **over):
+    P = lambda a: ctypes.c_void_p(a)
+    args = dict(q=P(0x10000), k=P(0x11000), v=P(0x12000), alpha=P(0x13000), mu=P(0x14000),
+                eta=P(0x15000), beta=None, Sc=P(0x16000), Mc=P(0x17000), do=P(0x18000),
+                dS=None, dM=None, dq=P(0x20000), dk=P(0x21000), dv=P(0x22000),
+                da=P(0x23000), dmu=P(0x24000), de=P(0x25000), db=None, dS0=None, dM0=None,
+                cu=None, n_seq=2, B=2, T=64, H=2, dkd=128, dvd=128, dtype=1, chunk=64,
+                ws=P(0x100000), ws_bytes=1 << 40, stream=None)
+    args.update(over)
+    a = args
+    return L.mdn_chunk_bwd(a["q"], a["k"], a["v"], a["alpha"], a["mu"], a["eta"], a["beta"],
+                           a["Sc"], a["Mc"], a["do"], a["dS"], a["dM"], a["dq"], a["dk"],
+                           a["dv"], a["da"], a["dmu"], a["de"], a["db"], a["dS0"], a["dM0"],
+                           a["cu"], a["n_seq"], a["B"], a["T"], a["H"], a["dkd"], a["dvd"],
+                           a["dtype"], a["chunk"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Sc=None), 1), (dict(do=None), 1), (dict(dq=None), 1), (dict(dmu=None), 1),
+    (dict(dv=ctypes.c_void_p(0x10000)), 1),          # an output aliasing an input
+    (dict(dk=ctypes.c_void_p(0x20000)), 1),          # two outputs the same
+    (dict(dS0=ctypes.c_void_p(0x30008)), 1),         # misaligned
+    (dict(ws=None), 1), (dict(ws_bytes=256), 1),
+    (dict(n_seq=3), 1), (dict(chunk=32), 2), (dict(dkd=96, dvd=96), 2),
+])
+def test_chunk_bwd_rejects(L, over, code):
+    assert _bwd(L, **over) == code
+
+
+def test_chunk_bwd_workspace_size(L):
+    a = mdn.chunk_bwd_workspace_size(8, 16384, 8, 128, 1)
+    per = 5 * 64 * 64 * 4 + 8 * 64 * 4 + 2 * 128 * 128 * 4 + 64 * 128 * 4
+    assert a >= (16384 // 64 + 8) * 8 * per and a % 256 == 0
+    assert mdn.chunk_bwd_workspace_size(-1, 10, 1, 64, 1) == 0

@@ -8,8 +8,6 @@ import bench
 import workloads as W
 
 
-
-
 def test_path_flops_per_token_head():
     assert bench.path_flops_per_token_head(128) == 12 * 128 * 128 + 12 * 64 * 128 + 64 * 64 // 3
     assert bench.path_flops_per_token_head(128) == 296277
