@@ -71,6 +71,8 @@ def parse():
     p.add_argument("--no-inputs", action="store_true",
                    help="skip timing the gate / query-key preparation kernel")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-backward", action="store_true",
+                   help="skip timing the gradient pass")
     p.add_argument("--no-other-workloads", action="store_true",
                    help="skip timing the other prefill workloads")
     p.add_argument("--decode-only", action="store_true",
@@ -477,6 +479,68 @@ def time_inputs(mdn, x_dev, steps, warmup, flush, peaks):
                          "algorithmic_bytes": nbytes}}
 
 
+def bwd_flops_per_token_head(d, C=64):
+    """FLOPs the gradient pass performs per (token, head): the state products
+    of the chunk kernel (P S0, P M0, Q S0, Q M0, Kh dS, Kh dM and the three
+    n x dk accumulators, 24 d^2), the reverse chain (WS dS, WM dM and the two
+    state-adjoint updates, 12 d^2), and the chunk-local products (Grams, T R,
+    dO Vres^T, dR Vres^T, A^T dO, T^T dVres and the four C x C by C x d
+    products, 14 C d), plus the triangular inverse (C^2 / 3)."""
+    return 36 * d * d + 14 * C * d + C * C // 3
+
+
+def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
+    """mdn_chunk_bwd on the workload (its forward's chunk entry states taken
+    once beforehand, random adjoints of o and of the final states), L2
+    flushed before every timed call: ms per call, tokens/s, and the FFMA
+    roofline of the whole pass (it runs on the CUDA cores in fp32)."""
+    d = x_dev
+    _, _, _, Sc, Mc = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
+                                    d["beta"], d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"],
+                                    return_chunk_states=True)
+    g = torch.Generator(device=d["q"].device).manual_seed(11)
+    do = torch.randn(d["v"].shape, generator=g, device=d["v"].device).to(d["v"].dtype)
+    n_seq, H, D = d["n_seq"], d["H"], d["D"]
+    dS = torch.randn((n_seq, H, D, D), generator=g, device=do.device) * 0.1
+    dM = torch.randn((n_seq, H, D, D), generator=g, device=do.device) * 0.1
+    need = mdn.chunk_bwd_workspace_size(n_seq, d["B"] * d["T"], H, D, d["q"].dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=do.device)
+
+    def call():
+        return mdn.chunk_bwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"], Sc, Mc,
+                             do, beta=d["beta"], dS_T=dS, dM_T=dM, cu_seqlens=d["cu_seqlens"],
+                             workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(do.device)
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        call()
+        b.record(cur)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    st = mdn.device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after the gradient pass" % st)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    tokens = sum(seq_lengths(x))
+    fl = bwd_flops_per_token_head(D) * tokens * H
+    peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    ach = fl / (ms / 1e3) / 1e12
+    return {"what": "gradient pass (mdn_chunk_bwd) from the forward's chunk entry states",
+            "ms_per_call": ms, "tokens_per_s": tokens / (ms / 1e3),
+            "ratio_to_forward": None, "gpu_launches_per_call": 3 + (1 if d["cu_seqlens"] is not None else 0),
+            "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                         "frac": ach / peak, "algorithmic_flops": fl,
+                         "peak_source": "fp32 FFMA from unit counts (152 SMs x 128 lanes x 2 x max clock)"}}
+
+
 def time_e2e(mdn, x, x_dev, steps, warmup):
     """Same metric through the public API from pinned host buffers: every
     step copies its inputs host->device, runs, and copies o and the final
@@ -716,6 +780,10 @@ def main():
                         "overhead_vs_forward": v_ms / m["ms_per_step"] - 1.0}
     if not args.no_inputs:
         line["inputs"] = time_inputs(mdn, x_dev, max(3, min(args.steps, 10)), 2, flush, peaks)
+    if not args.no_backward:
+        line["backward"] = time_backward(mdn, x, x_dev, max(3, min(args.steps, 10)), 2, flush,
+                                         peaks)
+        line["backward"]["ratio_to_forward"] = line["backward"]["ms_per_call"] / m["ms_per_step"]
     if not args.no_e2e:
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
         e_ms = max_over_ranks(e_ms, world, dev)

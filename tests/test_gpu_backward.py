@@ -80,6 +80,8 @@ def _compare(x, got, do, dS, dM, sel, tol=None):
         a, b = np.concatenate([np.ravel(t) for t in a]), np.concatenate([np.ravel(t) for t in b])
         den = np.linalg.norm(b)
         errs[n] = float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
+    print("gradient rel L2 (%s):" % x["dtype"],
+          " ".join("%s %.2e" % (n, e) for n, e in errs.items()))
     for n, e in errs.items():
         assert np.isfinite(e), (n, e)
         assert e <= tol, "%s rel L2 %.3e > %.1e (%s)" % (n, e, tol, errs)
@@ -139,7 +141,8 @@ def _sample(x, n, seed):
     return [ch[i] for i in sorted(idx)]
 
 
-@pytest.mark.parametrize("w", [W.PREFILL_400M, W.VARLEN_PACKED], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.PREFILL_400M, W.PREFILL_1P3B_LONG, W.VARLEN_PACKED],
+                         ids=lambda w: w.name)
 def test_full_size_sampled(w):
     x = W.make_prefill(w)
     do, dS, dM = _adjoints(x, 60)
