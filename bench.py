@@ -73,6 +73,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-backward", action="store_true",
                    help="skip timing the gradient pass")
+    p.add_argument("--no-block", action="store_true",
+                   help="skip timing the token-mixer block")
     p.add_argument("--no-other-workloads", action="store_true",
                    help="skip timing the other prefill workloads")
     p.add_argument("--decode-only", action="store_true",
@@ -541,6 +543,53 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
                          "peak_source": "fp32 FFMA from unit counts (152 SMs x 128 lanes x 2 x max clock)"}}
 
 
+def time_block(mdn, x_dev, steps, warmup, flush):
+    """mdn_block_fwd (the token-mixer block around the core) on the
+    workload's token layout with d_model = H d and seeded random weights:
+    ms per call and tokens/s."""
+    d = x_dev
+    dev = d["q"].device
+    H, D = d["H"], d["D"]
+    dm = H * D
+    g = torch.Generator(device=dev).manual_seed(13)
+    dt = d["q"].dtype
+    T_total = d["B"] * d["T"]
+    B, T = (1, T_total) if d["cu_seqlens"] is not None else (d["B"], d["T"])
+    xb = torch.randn((B, T, dm), generator=g, device=dev).to(dt)
+    W_in = (torch.randn((dm, 4 * H * D + 4 * H), generator=g, device=dev) / dm ** 0.5).to(dt)
+    conv_w = torch.randn((3 * H * D, 4), generator=g, device=dev) * 0.5
+    rms_w = torch.ones(D, device=dev)
+    W_o = (torch.randn((H * D, dm), generator=g, device=dev) / dm ** 0.5).to(dt)
+    need = mdn.block_fwd_workspace_size(d["n_seq"], T_total, H, D, dm, dt)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def call():
+        mdn.block_fwd(xb, W_in, conv_w, rms_w, W_o, H, D, cu_seqlens=d["cu_seqlens"],
+                      workspace=ws, **GATE_PARAMS)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        call()
+        b.record(cur)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    gemm_flops = 2 * T_total * dm * (4 * H * D + 4 * H) + 2 * T_total * H * D * dm
+    return {"what": "token-mixer block (mdn_block_fwd): projection GEMM, short convolution, "
+                    "gates and q/k, MDN core, RMSNorm and output gate, output GEMM",
+            "d_model": dm, "ms_per_call": ms, "tokens_per_s": T_total / (ms / 1e3),
+            "projection_flops": gemm_flops,
+            "weights": "seeded random (no trained weights are needed to time the block)"}
+
+
 def time_e2e(mdn, x, x_dev, steps, warmup):
     """Same metric through the public API from pinned host buffers: every
     step copies its inputs host->device, runs, and copies o and the final
@@ -784,6 +833,8 @@ def main():
         line["backward"] = time_backward(mdn, x, x_dev, max(3, min(args.steps, 10)), 2, flush,
                                          peaks)
         line["backward"]["ratio_to_forward"] = line["backward"]["ms_per_call"] / m["ms_per_step"]
+    if not args.no_block and tensor:
+        line["block"] = time_block(mdn, x_dev, max(3, min(args.steps, 10)), 2, flush)
     if not args.no_e2e:
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, max(3, min(args.steps, 10)), 2)
         e_ms = max_over_ranks(e_ms, world, dev)

@@ -259,6 +259,57 @@ mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v,
                          int H, int dk, int dv, mdn_dtype dtype, int chunk,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Bytes of device workspace mdn_block_fwd needs (a multiple of 256; 0 for
+ * invalid sizes).
+ */
+size_t mdn_block_fwd_workspace_size(int n_seq, int T_total, int H, int d,
+                                    int d_model, mdn_dtype dtype);
+
+/*
+ * mdn_block_fwd — the MDN token-mixer block around the memory core.
+ *
+ * Defined by: slides, frame "The memory sits inside a familiar
+ * language-model block" (Sec. 3.3, Fig. 3 of the paper) and reading notes
+ * section 2.9: project, short-convolve and activate q, k, v; correct the
+ * query (q - d k, Comba) and L2-normalise q and k; generate the four gates
+ * (mdn_prepare_inputs' parameterisation); update memory and momentum
+ * (mdn_chunk_fwd); then y_t = W_o [sigmoid(W_g x_t) * RMSNorm(o_t)].
+ * Readings where the pages are silent: the short convolution is causal,
+ * depthwise along the tokens, of width 4 without bias, and restarts at
+ * every sequence start; SiLU follows it on q, k and v; RMSNorm runs over
+ * each head's d outputs with one weight vector of d entries shared by the
+ * heads and epsilon rms_eps.
+ *
+ * Layout (row-major, innermost last): x, y [B * T, d_model] (dtype);
+ *   W_in [d_model, 4 H d + 4 H] (dtype), columns q | k | v | g (H d each,
+ *   head-major) | z_alpha | z_beta | z_mu | z_eta (H each);
+ *   conv_w [3 H d, 4] fp32 (tap j multiplies the input 3 - j tokens back),
+ *   rows in W_in's q | k | v column order; rms_w [d] fp32;
+ *   W_o [H d, d_model] (dtype); states as mdn_chunk_fwd ([n_seq, H, d, d]
+ *   fp32, S0/M0 NULL for zero, S_T/M_T NULL to skip); cu_seqlens as
+ *   mdn_chunk_fwd (packed sequences; the convolution restarts at each).
+ *   Gate parameters a, b, s, tau, log_mu_min, comba_d as mdn_prepare_inputs.
+ * The two projections run as cuBLAS GEMMs (fp32 accumulation; bf16 inputs
+ * give fp32 projections, then bf16 q, k, v, o and y); the first call on a
+ * device creates that device's cuBLAS handle (cuBLAS allocates a little
+ * device memory of its own then); GEMM scratch comes from the workspace.
+ * Calls on one device are serialised by the library.
+ * Errors: MDN_ERR_INVALID_ARG for missing or misaligned pointers (16 bytes,
+ * 4 for cu_seqlens), inconsistent sizes or a short workspace;
+ * MDN_ERR_UNSUPPORTED for d not in {64, 128} or d_model not a multiple of 8;
+ * the errors of mdn_prepare_inputs and mdn_chunk_fwd; MDN_ERR_CUDA for a
+ * failed launch or GEMM.
+ */
+mdn_status mdn_block_fwd(const void *x, const void *W_in, const float *conv_w,
+                         const float *rms_w, const void *W_o, float a, float b,
+                         float s, float tau, float log_mu_min, float comba_d,
+                         float rms_eps, const float *S0, const float *M0,
+                         void *y, float *S_T, float *M_T,
+                         const int32_t *cu_seqlens, int n_seq, int B, int T,
+                         int H, int d, int d_model, mdn_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* Implementation paths of mdn_chunk_fwd (reported by the profiled variant). */
 typedef enum mdn_path {
     MDN_PATH_CUDA_CORE = 0,   /* fp32 FFMA kernels: fp32 inputs, head size 64 */

@@ -26,7 +26,7 @@ import os
 
 import torch
 
-__all__ = ["chunk_fwd", "chunk_bwd", "chunk_bwd_workspace_size", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
+__all__ = ["chunk_fwd", "chunk_bwd", "block_fwd", "chunk_bwd_workspace_size", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
            "device_status", "wait_selftest",
            "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
@@ -50,7 +50,7 @@ EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_states", "mdn_prepare_inputs",
                     "mdn_decode_step", "mdn_get_device_status",
                     "mdn_wait_selftest", "mdn_chunk_bwd_workspace_size",
-                    "mdn_chunk_bwd"]
+                    "mdn_chunk_bwd", "mdn_block_fwd_workspace_size", "mdn_block_fwd"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
 
@@ -109,6 +109,12 @@ def lib():
     L.mdn_get_device_status.argtypes = [vp]
     L.mdn_wait_selftest.restype = c_int
     L.mdn_wait_selftest.argtypes = [c_int, vp]
+    L.mdn_block_fwd_workspace_size.restype = c_size
+    L.mdn_block_fwd_workspace_size.argtypes = [c_int] * 6
+    c_float = ctypes.c_float
+    L.mdn_block_fwd.restype = c_int
+    L.mdn_block_fwd.argtypes = ([vp] * 5 + [c_float] * 7 + [vp] * 6 + [c_int] * 7
+                                + [vp, c_size, vp])
     L.mdn_chunk_bwd_workspace_size.restype = c_size
     L.mdn_chunk_bwd_workspace_size.argtypes = [c_int] * 6
     L.mdn_chunk_bwd.restype = c_int
@@ -423,6 +429,62 @@ def chunk_bwd(q, k, v, alpha, mu, eta, S_chunks, M_chunks, dout, beta=None,
     if st != MDN_OK:
         raise MdnError(st, "mdn_chunk_bwd")
     return g
+
+
+def block_fwd(x, W_in, conv_w, rms_w, W_o, H, d, a, b, s, tau, log_mu_min=-2.0,
+              comba_d=0.0, rms_eps=1e-6, S0=None, M0=None, cu_seqlens=None,
+              output_final_state=True, workspace=None, stream=None):
+    """The MDN token-mixer block (``mdn_block_fwd``): x ``[B, T, d_model]``
+    (or packed ``[1, sum T, d_model]`` with ``cu_seqlens``), weights as the
+    header describes.  Returns ``(y, S_T, M_T)``."""
+    L = lib()
+    if x.dim() != 3:
+        raise ValueError("x must be [B, T, d_model]")
+    B, T, d_model = x.shape
+    dev = x.device
+    code = _dtype_code(x.dtype)
+    n_cols = 4 * H * d + 4 * H
+    for name, t, shape, dt in (("x", x, (B, T, d_model), x.dtype),
+                               ("W_in", W_in, (d_model, n_cols), x.dtype),
+                               ("conv_w", conv_w, (3 * H * d, 4), torch.float32),
+                               ("rms_w", rms_w, (d,), torch.float32),
+                               ("W_o", W_o, (H * d, d_model), x.dtype)):
+        _check_cuda(name, t, dt, dev)
+        if tuple(t.shape) != shape:
+            raise ValueError("%s must be %s" % (name, shape))
+    if cu_seqlens is not None:
+        _check_cuda("cu_seqlens", cu_seqlens, torch.int32, dev)
+        n_seq = cu_seqlens.numel() - 1
+    else:
+        n_seq = B
+    for name, t in (("S0", S0), ("M0", M0)):
+        _check_cuda(name, t, torch.float32, dev)
+        if t is not None and tuple(t.shape) != (n_seq, H, d, d):
+            raise ValueError("%s must be [n_seq, H, d, d]" % name)
+    y = torch.empty_like(x)
+    S_T = M_T = None
+    if output_final_state:
+        S_T = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+        M_T = torch.empty_like(S_T)
+    need = int(L.mdn_block_fwd_workspace_size(n_seq, B * T, H, d, d_model, code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check_cuda("workspace", workspace, torch.uint8, dev)
+    with torch.cuda.device(dev):
+        st = L.mdn_block_fwd(_ptr(x), _ptr(W_in), _ptr(conv_w), _ptr(rms_w), _ptr(W_o),
+                             float(a), float(b), float(s), float(tau), float(log_mu_min),
+                             float(comba_d), float(rms_eps), _ptr(S0), _ptr(M0), _ptr(y),
+                             _ptr(S_T), _ptr(M_T), _ptr(cu_seqlens), n_seq, B, T, H, d,
+                             d_model, code, _ptr(workspace), workspace.numel(),
+                             _stream_handle(dev, stream))
+    if st != MDN_OK:
+        raise MdnError(st, "mdn_block_fwd")
+    return y, S_T, M_T
+
+
+def block_fwd_workspace_size(n_seq, T_total, H, d, d_model, dtype):
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().mdn_block_fwd_workspace_size(n_seq, T_total, H, d, d_model, code))
 
 
 def chunk_bwd_workspace_size(n_seq, T_total, H, D, dtype):

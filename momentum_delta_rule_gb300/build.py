@@ -67,7 +67,7 @@ def build(force=False, verbose=False, extra_flags=()):
     if (force or procs or not os.path.exists(LIB_PATH)
             or os.path.getmtime(LIB_PATH) < _newest(objs)):
         tmp = LIB_PATH + ".tmp.%d" % os.getpid()
-        cmd = [NVCC, ARCH, "-shared", "-o", tmp] + objs
+        cmd = [NVCC, ARCH, "-shared", "-o", tmp] + objs + ["-lcublas"]
         if verbose:
             print(" ".join(cmd), flush=True)
         subprocess.run(cmd, check=True)

@@ -288,3 +288,28 @@ def test_chunk_bwd_workspace_size(L):
     per = 5 * 64 * 64 * 4 + 8 * 64 * 4 + 2 * 128 * 128 * 4 + 64 * 128 * 4
     assert a >= (16384 // 64 + 8) * 8 * per and a % 256 == 0
     assert mdn.chunk_bwd_workspace_size(-1, 10, 1, 64, 1) == 0
+
+
+def _block(L, **over):
+    P = lambda a: ctypes.c_void_p(a)
+    args = dict(x=P(0x10000), W_in=P(0x20000), conv=P(0x30000), rms=P(0x40000), W_o=P(0x50000),
+                a=1.0, b=0.0, s=1.0, tau=1.0, lmin=-2.0, cd=0.0, eps=1e-6, S0=None, M0=None,
+                y=P(0x60000), S_T=None, M_T=None, cu=None, n_seq=2, B=2, T=64, H=2, d=128,
+                dm=256, dtype=1, ws=P(0x100000), ws_bytes=1 << 40, stream=None)
+    args.update(over)
+    a = args
+    return L.mdn_block_fwd(a["x"], a["W_in"], a["conv"], a["rms"], a["W_o"], a["a"], a["b"],
+                           a["s"], a["tau"], a["lmin"], a["cd"], a["eps"], a["S0"], a["M0"],
+                           a["y"], a["S_T"], a["M_T"], a["cu"], a["n_seq"], a["B"], a["T"],
+                           a["H"], a["d"], a["dm"], a["dtype"], a["ws"], a["ws_bytes"],
+                           a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(x=None), 1), (dict(W_o=None), 1), (dict(conv=None), 1),
+    (dict(y=ctypes.c_void_p(0x60008)), 1), (dict(ws=None), 1), (dict(ws_bytes=1024), 1),
+    (dict(n_seq=3), 1), (dict(dtype=4), 1), (dict(eps=-1.0), 1),
+    (dict(d=96), 2), (dict(dm=100), 2),
+])
+def test_block_fwd_rejects(L, over, code):
+    assert _block(L, **over) == code
