@@ -69,6 +69,15 @@ size_t meta_bytes(int n_seq) {
            round256(sizeof(int32_t) * ((size_t)n_seq + 1));
 }
 
+// fp32 inputs reach the tensor cores as hi / lo bf16 parts of q, k and v:
+// six [T_total, H, d] bf16 arrays after the prepared blocks.
+size_t split_part_bytes(int T_total, int H, int d) {
+    return (((size_t)T_total * H * d * 2) + 255) & ~(size_t)255;
+}
+size_t split_bytes(int T_total, int H, int d, mdn_dtype dtype) {
+    return dtype == MDN_F32 ? 6 * split_part_bytes(T_total, H, d) : 0;
+}
+
 // Upper bound on the chunk slots of any split of T_total into n_seq
 // sequences: sum ceil(L_s / 64) <= floor(T_total / 64) + n_seq.
 long chunk_slots_bound(int n_seq, int T_total) {
@@ -98,7 +107,7 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
     if (dtype != MDN_F32 && dtype != MDN_BF16) return 0;
     const size_t prep = (size_t)chunk_slots_bound(n_seq, T_total) * (size_t)H *
                         mdn::kPrepBytesMax;
-    return round256(meta_bytes(n_seq) + prep);
+    return round256(meta_bytes(n_seq) + prep) + split_bytes(T_total, H, dk, dtype);
 }
 
 }  // extern "C"
@@ -212,17 +221,29 @@ mdn_status chunk_fwd_impl(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     for (int i = 0; i < n_stage_events; ++i) ev[i] = static_cast<cudaEvent_t>(stage_events[i]);
-    // bf16 inputs with head size 128 run on the tensor cores; fp32 inputs (an
-    // fp32-level error bound) and head size 64 on the CUDA cores.
-    const bool tensor = dtype == MDN_BF16 && dk == 128 && T_total > 0;
+    // The state pass runs on the tensor cores for every input: bf16 inputs
+    // directly (prep on the tensor cores too), fp32 inputs as hi / lo bf16
+    // parts with three products per contraction, their T and A_O T from the
+    // fp32 prep (an fp32-level error bound needs the fp32 inverse).  With no
+    // tokens only the initial states pass through (CUDA-core kernel).
+    const bool tensor = T_total > 0;
+    const bool split = tensor && dtype == MDN_F32;
+    if (split) {
+        const size_t part = split_part_bytes((int)T_total, H, dk);
+        unsigned char *sp = ws + round256(meta_bytes(n_seq) + (size_t)chunk_slots_bound(
+                                              n_seq, (int)T_total) * (size_t)H * mdn::kPrepBytesMax);
+        p.q_hi = sp; p.q_lo = sp + part; p.k_hi = sp + 2 * part;
+        p.k_lo = sp + 3 * part; p.v_hi = sp + 4 * part; p.v_lo = sp + 5 * part;
+    }
     const int path = tensor ? MDN_PATH_TENSOR_CORE : MDN_PATH_CUDA_CORE;
     if (path_out) *path_out = path;
     cudaError_t err = cudaSuccess;
     if (ev[0]) err = cudaEventRecord(ev[0], cs);
     if (err == cudaSuccess && p.cu_seqlens && p.max_chunks > 0)
         err = mdn::launch_chunk_offsets(p, cs);
+    if (err == cudaSuccess && split) err = mdn::launch_split_inputs(p, cs);
     if (err == cudaSuccess)
-        err = tensor ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs);
+        err = (tensor && !split) ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs);
     if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
     if (err == cudaSuccess)
         err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_chunk_state_simt(p, cs);

@@ -28,6 +28,7 @@
 #include <type_traits>
 
 #include "mdn_internal.cuh"
+#include "mdn_sm100.cuh"
 
 namespace mdn {
 namespace {
@@ -378,11 +379,34 @@ chunk_prep_simt_kernel(ChunkProblem p) {
         __syncthreads();
     }
 
-    // ---- write the prepared block
+    // ---- write the prepared block: row-major fp32 T and A_O T, or, when the
+    //      tensor-core state pass takes fp32 inputs (split operands), the
+    //      operand [T; A_O T] of its second product as hi / lo bf16 parts in
+    //      the 128-byte-swizzled layout, rows interleaved by tc_row
     unsigned char *blk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
     float *Tg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffT);
     float *AOTg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffAOT);
     float *vec = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffVec);
+    static_assert(PrepLayout<float>::kOffVec == PrepLayoutTC::kSplitVec, "vector rows");
+    const bool split_tc = p.k_hi != nullptr;
+    auto put4 = [&](int op_row, int col4, const float *x) {
+        // four consecutive columns col4..col4+3 = half of a 16-byte chunk
+        float r[4];
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r[e] = x[e] - __bfloat162float(__float2bfloat16_rn(x[e]));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            __nv_bfloat162 a = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+            __nv_bfloat162 b = __floats2bfloat162_rn(r[2 * e], r[2 * e + 1]);
+            hi[e] = *reinterpret_cast<uint32_t *>(&a);
+            lo[e] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        const uint32_t off = sm100::sw128_offset((uint32_t)op_row, (uint32_t)(col4 >> 3)) +
+                             (uint32_t)(col4 & 4) * 2;
+        *reinterpret_cast<uint2 *>(blk + off) = make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2 *>(blk + PrepLayoutTC::kSplitLo + off) = make_uint2(lo[0], lo[1]);
+    };
     {
         const int ti = tid >> 4, tj = tid & 15;
         float acc[4][4] = {};
@@ -398,14 +422,25 @@ chunk_prep_simt_kernel(ChunkProblem p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[r][c] += ar[r] * tc[c];
         }
+        if (split_tc) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = 4 * ti + r, j = 4 * tj + c;
-                AOTg[i * kChunk + j] = acc[r][c];
-                Tg[i * kChunk + j] = Tm[i * LM + j];
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * ti + r;
+                const float t4[4] = {Tm[i * LM + 4 * tj], Tm[i * LM + 4 * tj + 1],
+                                     Tm[i * LM + 4 * tj + 2], Tm[i * LM + 4 * tj + 3]};
+                put4(tc_row(i), 4 * tj, t4);
+                put4(tc_row(kChunk + i), 4 * tj, acc[r]);
             }
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i = 4 * ti + r, j = 4 * tj + c;
+                    AOTg[i * kChunk + j] = acc[r][c];
+                    Tg[i * kChunk + j] = Tm[i * LM + j];
+                }
+        }
     }
     if (tid < kChunk) {
         const int i = tid;
@@ -765,7 +800,44 @@ cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// fp32 q, k, v -> their hi / lo bf16 parts (hi = bf16(x), lo = bf16(x - hi)),
+// four elements per thread and tensor.
+__global__ void __launch_bounds__(256)
+split_inputs_kernel(const float4 *q, const float4 *k, const float4 *v, long n4, uint2 *q_hi,
+                    uint2 *q_lo, uint2 *k_hi, uint2 *k_lo, uint2 *v_hi, uint2 *v_lo) {
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 *src[3] = {q, k, v};
+        uint2 *hi[3] = {q_hi, k_hi, v_hi}, *lo[3] = {q_lo, k_lo, v_lo};
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            const float4 x = src[t][i];
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(x.x, x.y);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(x.z, x.w);
+            const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+            const __nv_bfloat162 l0 = __floats2bfloat162_rn(x.x - f0.x, x.y - f0.y);
+            const __nv_bfloat162 l1 = __floats2bfloat162_rn(x.z - f1.x, x.w - f1.y);
+            hi[t][i] = make_uint2(*reinterpret_cast<const uint32_t *>(&h0),
+                                  *reinterpret_cast<const uint32_t *>(&h1));
+            lo[t][i] = make_uint2(*reinterpret_cast<const uint32_t *>(&l0),
+                                  *reinterpret_cast<const uint32_t *>(&l1));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_split_inputs(const ChunkProblem &p, cudaStream_t st) {
+    const long n4 = (long)p.T_total * p.H * p.D / 4;
+    if (n4 == 0) return cudaSuccess;
+    const int blocks = (int)((n4 + 255) / 256 < 152L * 8 ? (n4 + 255) / 256 : 152L * 8);
+    split_inputs_kernel<<<blocks, 256, 0, st>>>(
+        static_cast<const float4 *>(p.q), static_cast<const float4 *>(p.k),
+        static_cast<const float4 *>(p.v), n4, static_cast<uint2 *>(p.q_hi),
+        static_cast<uint2 *>(p.q_lo), static_cast<uint2 *>(p.k_hi), static_cast<uint2 *>(p.k_lo),
+        static_cast<uint2 *>(p.v_hi), static_cast<uint2 *>(p.v_lo));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
     chunk_offsets_kernel<<<1, 1024, 0, st>>>(p.cu_seqlens, p.n_seq, p.T_total,

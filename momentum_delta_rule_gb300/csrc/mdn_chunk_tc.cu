@@ -1,6 +1,6 @@
 // MDN chunkwise forward — sequential state pass on the 5th-generation tensor
-// cores (tcgen05, TMEM accumulators, TMA-staged operands), bf16 inputs, head
-// size 128.
+// cores (tcgen05, TMEM accumulators, TMA-staged operands), head size 64 or
+// 128, bf16 inputs, or fp32 inputs through split bf16 operands.
 //
 // Chunk equations ("MDN: Parallelizing Stepwise Momentum for Delta Linear
 // Attention" slides, frames "Solve the unknown residuals with a lower
@@ -22,25 +22,35 @@
 // carries use the old S_0, M_0), off the critical path while MMA2 runs.  Only
 // a bf16 copy of the state goes to shared memory, as MMA1's B operand.
 //
-// One CTA owns one (sequence, head, NS-column slice), NS = 64, 32 or 16 (the
-// launcher takes the narrowest whose grid still fits one CTA per SM, else
-// 64): columns of S and M evolve independently (column j of Vres depends
-// only on column j of S_0 and M_0), so the slices of a head never
-// communicate.  A second instantiation also stores every chunk's entry state
-// (S, M) for a gradient pass; the plain forward's kernel carries none of it.
+// fp32 inputs (kSplit): every operand X is held as two bf16 parts, X_hi =
+// bf16(X) and X_lo = bf16(X - X_hi), which carry about 16 significant bits,
+// and each product is taken as A_hi B_hi + A_hi B_lo + A_lo B_hi (three MMA
+// groups into the same fp32 accumulator); the dropped A_lo B_lo and the
+// parts' own rounding leave relative errors near 1e-5.  The q, k, v parts
+// come from a conversion kernel, T and A_O T's parts from the fp32 prep.  The
+// stage is single-buffered there (the split operands double its size).
+//
+// One CTA owns one (sequence, head, NS-column slice): columns of S and M
+// evolve independently (column j of Vres depends only on column j of S_0 and
+// M_0), so the slices of a head never communicate.  A second instantiation
+// also stores every chunk's entry state (S, M) for a gradient pass.
 //
 // Warp roles (2 + NS / 4 warps, 18 for NS = 64): 0 TMA producer, 1 MMA
 // issuer + TMEM owner (all lanes wait, lane 0 issues), the rest epilogue
 // (TMEM lane quadrant = warp % 4, 16-column group of the slice =
-// (warp-2)/4).  A warp reaches only the TMEM lanes of
-// its quadrant, and the warps of a quadrant share one scheduler; [K; Q] and
-// [T; A_O T] rows are therefore interleaved in blocks of 16 (tc_row), so that
-// every quadrant holds 16 token rows and 16 query rows and the token-row
-// steps (R, Vres) use all four schedulers (16x32bx2 TMEM loads: lanes t and
-// t + 16 take 8 columns each).
+// (warp-2)/4).  A warp reaches only the TMEM lanes of its quadrant, and the
+// warps of a quadrant share one scheduler; [K; Q] and [T; A_O T] rows are
+// therefore interleaved in blocks of 16 (tc_row), so that every quadrant
+// holds 16 token rows and 16 query rows and the token-row steps (R, Vres)
+// use all four schedulers (16x32bx2 TMEM loads: lanes t and t + 16 take 8
+// columns each).  With head size 64, MMA3 is an M = 64 product, whose row r
+// sits in TMEM lane 32 (r / 16) + r % 16: lanes 0..15 of each quadrant hold
+// the state rows.
 // Every wait is bounded (1 s); on expiry the CTA records
 // MDN_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "mdn_internal.cuh"
 #include "mdn_sm100.cuh"
@@ -50,39 +60,49 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kD = 128;                  // head size (dk = dv)
-constexpr int kStages = 2;
 constexpr int kEpiCols = 16;             // state columns per epilogue thread
-
-// shared memory of one pipeline stage (byte offsets from the stage base)
-constexpr uint32_t kKQBytes = 32768;     // per 64-wide dk half: K rows, then Q rows
+constexpr uint32_t kKQHalf = 16384;      // one 64-wide dk half: 64 K rows + 64 Q rows, swizzled
 constexpr uint32_t kVBytes = 8192;       // V tile, 64 tokens x 64 columns, swizzled
-constexpr uint32_t kPrepBytes = (uint32_t)PrepLayoutTC::kBytes;   // 18432
-constexpr uint32_t kOffV = kKQBytes;
-constexpr uint32_t kOffPrep = kKQBytes + kVBytes;
-constexpr uint32_t kStageBytes = kKQBytes + kVBytes + kPrepBytes;  // 59392
 
-// Everything that depends on the slice width NS (state columns per CTA).
+// Everything that depends on the head size D, the slice width NS (state
+// columns per CTA) and the operand form (kSplit: hi and lo bf16 parts).
 // In the N dimension of [S | M]-shaped operands, S takes columns [0, NS) and
 // M [NS, 2NS); operands are MN-major in blocks of 64 columns, so for NS = 64
 // the M half is a second block and for NS = 32 or 16 it shares the block.
-template <int NS>
+template <int D, int NS, bool kSplit>
 struct Cfg {
     static_assert(NS == 16 || NS == 32 || NS == 64, "slice width");
-    static constexpr int kSlices = kD / NS;
+    static_assert(D == 64 || D == 128, "head size");
+    static constexpr int kHalves = D / 64;
+    static constexpr int kStages = kSplit ? 1 : 2;
+    static constexpr int kParts = kSplit ? 2 : 1;
+    static constexpr int kSlices = D / NS;
     static constexpr int kEpiWarps = 4 * NS / kEpiCols;      // 4 lane quadrants
     static constexpr int kThreads = 32 * (2 + kEpiWarps);
+    // one pipeline stage: [K; Q] parts, V parts, the prepared block
+    static constexpr uint32_t kKQPart = kHalves * kKQHalf;
+    static constexpr uint32_t kOffV = kParts * kKQPart;
+    static constexpr uint32_t kOffPrep = kOffV + kParts * kVBytes;
+    static constexpr uint32_t kPrepBytes =
+        kSplit ? (uint32_t)PrepLayoutTC::kSplitBytes : (uint32_t)PrepLayoutTC::kBytes;
+    static constexpr uint32_t kPrepLo = (uint32_t)PrepLayoutTC::kSplitLo;   // lo part (split)
+    static constexpr uint32_t kPrepVec =
+        kSplit ? (uint32_t)PrepLayoutTC::kSplitVec : (uint32_t)PrepLayoutTC::kOffVec;
+    static constexpr uint32_t kStageBytes = kOffPrep + kPrepBytes;
+    static_assert(kStageBytes % 1024 == 0, "stage alignment");
+    // operands written by the epilogue
     static constexpr uint32_t kOffB1 = kStages * kStageBytes;  // [S | M] bf16, dk rows x 2NS
-    static constexpr uint32_t kB1Bytes = NS == 64 ? 32768 : 16384;
-    static constexpr uint32_t kB1M = NS == 64 ? 16384 : 0;    // byte offset of the M half
-    static constexpr uint32_t kOffR = kOffB1 + kB1Bytes;      // R bf16, 64 token rows x NS
-    static constexpr uint32_t kRBytes = 8192;
-    static constexpr uint32_t kOffB3 = kOffR + kRBytes;       // [gS Vres | -gM Vres]
-    static constexpr uint32_t kB3Bytes = NS == 64 ? 16384 : 8192;
+    static constexpr uint32_t kB1Part = (NS == 64 ? 2 : 1) * D * 128;
+    static constexpr uint32_t kB1M = NS == 64 ? D * 128 : 0;    // byte offset of the M half
+    static constexpr uint32_t kOffR = kOffB1 + kParts * kB1Part; // R bf16, 64 token rows x NS
+    static constexpr uint32_t kRPart = 8192;
+    static constexpr uint32_t kOffB3 = kOffR + kParts * kRPart;  // [gS Vres | -gM Vres]
+    static constexpr uint32_t kB3Part = NS == 64 ? 16384 : 8192;
     static constexpr uint32_t kB3M = NS == 64 ? 8192 : 0;
     static constexpr uint32_t kChM = NS == 64 ? 0 : NS / 8;   // chunk offset of the M half
-    static constexpr uint32_t kOffBar = kOffB3 + kB3Bytes;
+    static constexpr uint32_t kOffBar = kOffB3 + kParts * kB3Part;
     static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
     // tensor memory columns
     static constexpr uint32_t kColD1 = 0;                     // 2NS columns
     static constexpr uint32_t kColD2 = 2 * NS;                // NS columns
@@ -90,12 +110,12 @@ struct Cfg {
     static constexpr uint32_t kTmemCols = 8 * NS;
     static constexpr uint32_t kIdesc1 = idesc_bf16(128, 2 * NS, false, true);
     static constexpr uint32_t kIdesc2 = idesc_bf16(128, NS, false, true);
-    static constexpr uint32_t kIdesc3 = idesc_bf16(128, 2 * NS, true, true);
+    static constexpr uint32_t kIdesc3 = idesc_bf16(D, 2 * NS, true, true);
 };
 
 struct Bars {
-    uint64_t full[kStages];    // TMA bytes of a stage landed
-    uint64_t empty[kStages];   // stage free again (MMA commit + every epilogue warp)
+    uint64_t full[2];          // TMA bytes of a stage landed
+    uint64_t empty[2];         // stage free again (MMA commit + every epilogue warp)
     uint64_t d1, r, d2, v, d3, state, drain;   // d3: the state accumulation finished
     uint32_t tmem_base;
     int abort;
@@ -118,19 +138,39 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &raw, float *f) {
     }
 }
 
-// Write 16 fp32 values as bf16 into row `row`, 16-byte chunks [chunk0,
-// chunk0+2) of a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_row16(unsigned char *tile, uint32_t row, uint32_t chunk0,
-                                            const float *x, float scale) {
+// Eight fp32 values (times `scale`) as one 16-byte chunk of bf16, and, for a
+// split operand, the chunk of what the first rounding left over.
+__device__ __forceinline__ void pack8(const float *x, float scale, uint4 &hi, uint4 &lo) {
+    float y[8], r[8];
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        uint4 w;
-        w.x = pack_bf16x2(scale * x[8 * cc + 0], scale * x[8 * cc + 1]);
-        w.y = pack_bf16x2(scale * x[8 * cc + 2], scale * x[8 * cc + 3]);
-        w.z = pack_bf16x2(scale * x[8 * cc + 4], scale * x[8 * cc + 5]);
-        w.w = pack_bf16x2(scale * x[8 * cc + 6], scale * x[8 * cc + 7]);
-        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, chunk0 + cc)) = w;
+    for (int e = 0; e < 8; ++e) {
+        y[e] = scale * x[e];
+        r[e] = y[e] - __bfloat162float(__float2bfloat16_rn(y[e]));
     }
+    hi = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+    lo = make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]),
+                    pack_bf16x2(r[6], r[7]));
+}
+
+// Write 8 values into 16-byte chunk `chunk` of row `row` of a 128-byte-swizzled
+// operand tile, and the lo part `part_bytes` further on (split operands).
+template <bool kSplit>
+__device__ __forceinline__ void put8(unsigned char *tile, uint32_t part_bytes, uint32_t row,
+                                     uint32_t chunk, const float *x, float scale) {
+    uint4 hi, lo;
+    pack8(x, scale, hi, lo);
+    const uint32_t off = sw128_offset(row, chunk);
+    *reinterpret_cast<uint4 *>(tile + off) = hi;
+    if (kSplit) *reinterpret_cast<uint4 *>(tile + part_bytes + off) = lo;
+}
+
+// Write 16 fp32 values into row `row`, 16-byte chunks [chunk0, chunk0+2).
+template <bool kSplit>
+__device__ __forceinline__ void store_row16(unsigned char *tile, uint32_t part_bytes, uint32_t row,
+                                            uint32_t chunk0, const float *x) {
+    put8<kSplit>(tile, part_bytes, row, chunk0, x, 1.f);
+    put8<kSplit>(tile, part_bytes, row, chunk0 + 1, x + 8, 1.f);
 }
 
 // In-place rescale of this thread's 16 columns of the TMEM state for the
@@ -156,9 +196,10 @@ __device__ __forceinline__ void rescale_state(uint32_t st_s, uint32_t st_m, cons
 
 // One thread's 16 columns of row d of the entry state of chunk slot `slot`
 // (layout [slot, H, dk, dv]); `off` = d * dk + first column.
+template <int D>
 __device__ __forceinline__ void store_chunk_state(const ChunkProblem &p, int slot, int h, size_t off,
                                                   const float *S, const float *M) {
-    const size_t base = ((size_t)slot * p.H + h) * kD * kD + off;
+    const size_t base = ((size_t)slot * p.H + h) * D * D + off;
 #pragma unroll
     for (int j = 0; j < kEpiCols; j += 4) {
         *reinterpret_cast<float4 *>(p.S_chunks + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -171,20 +212,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// Eight consecutive outputs (o or the residuals) of one token row.
+__device__ __forceinline__ void store_out8(__nv_bfloat16 *dst, const float *x) {
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                                 pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+}
+__device__ __forceinline__ void store_out8(float *dst, const float *x) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4 *>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+// The tensor maps of one launch: K, Q, V, and for split operands their lo
+// parts.
+struct Maps {
+    CUtensorMap k, q, v, k_lo, q_lo, v_lo;
+};
+
 // kChunkStates: also write the entry state of every chunk (a separate
 // instantiation, so the plain forward carries none of its registers).
-template <int NS, bool kChunkStates>
-__global__ void __launch_bounds__(Cfg<NS>::kThreads, 1)
-chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
-                      const __grid_constant__ CUtensorMap map_q,
-                      const __grid_constant__ CUtensorMap map_v) {
+template <int D, int NS, bool kChunkStates, bool kSplit>
+__global__ void __launch_bounds__(Cfg<D, NS, kSplit>::kThreads, 1)
+chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Bars *bars = reinterpret_cast<Bars *>(smem + Cfg<NS>::kOffBar);
+    using C = Cfg<D, NS, kSplit>;
+    using Tio = typename std::conditional<kSplit, float, __nv_bfloat16>::type;
+    constexpr int kStages = C::kStages;
+    Bars *bars = reinterpret_cast<Bars *>(smem + C::kOffBar);
     volatile int *abort = &bars->abort;
 
-    using C = Cfg<NS>;
     constexpr int kEpiWarps = C::kEpiWarps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x % C::kSlices;
@@ -218,9 +275,14 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&map_k);
-        prefetch_tensormap(&map_q);
-        prefetch_tensormap(&map_v);
+        prefetch_tensormap(&maps.k);
+        prefetch_tensormap(&maps.q);
+        prefetch_tensormap(&maps.v);
+        if (kSplit) {
+            prefetch_tensormap(&maps.k_lo);
+            prefetch_tensormap(&maps.q_lo);
+            prefetch_tensormap(&maps.v_lo);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -234,27 +296,33 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int last_use[kStages] = {-1, -1};
+            int last_use[2] = {-1, -1};
             for (int c = 0; c < nchunks; ++c) {
-                const int st = c & 1, use = c >> 1;
+                const int st = c % kStages, use = c / kStages;
                 if (c == 0) grid_dependency_wait();   // the prepared blocks are complete
                 if (!mbar_wait(&bars->empty[st], (use & 1) ^ 1, abort)) break;
-                unsigned char *stage = smem + st * kStageBytes;
+                unsigned char *stage = smem + st * C::kStageBytes;
                 const int t0 = start + c * kChunk;
                 const unsigned char *blk =
                     p.prep + ((size_t)(slot0 + c) * p.H + h) * p.prep_stride;
-                mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+                mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
                 // [K; Q] rows interleaved by 16 (tc_row): 16-token boxes
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
+                for (int part = 0; part < C::kParts; ++part) {
+                    const CUtensorMap *mk = part ? &maps.k_lo : &maps.k;
+                    const CUtensorMap *mq = part ? &maps.q_lo : &maps.q;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        unsigned char *dst = stage + hh * 16384 + g * 4096;
-                        tma_load_3d(dst, &map_k, &bars->full[st], 64 * hh, h, t0 + 16 * g);
-                        tma_load_3d(dst + 2048, &map_q, &bars->full[st], 64 * hh, h, t0 + 16 * g);
-                    }
-                tma_load_3d(stage + kOffV, &map_v, &bars->full[st], col0, h, t0);
-                bulk_load(stage + kOffPrep, blk, kPrepBytes, &bars->full[st]);
+                    for (int hh = 0; hh < C::kHalves; ++hh)
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            unsigned char *dst = stage + part * C::kKQPart + hh * kKQHalf + g * 4096;
+                            tma_load_3d(dst, mk, &bars->full[st], 64 * hh, h, t0 + 16 * g);
+                            tma_load_3d(dst + 2048, mq, &bars->full[st], 64 * hh, h, t0 + 16 * g);
+                        }
+                    tma_load_3d(stage + C::kOffV + part * kVBytes, part ? &maps.v_lo : &maps.v,
+                                &bars->full[st], col0, h, t0);
+                }
+                bulk_load(stage + C::kOffPrep, blk, C::kPrepBytes, &bars->full[st]);
                 last_use[st] = use;
             }
             // drain: every issued copy must land before the CTA may exit
@@ -266,28 +334,35 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (the
-        // whole warp waits, lane 0 issues and commits)
+        // whole warp waits, lane 0 issues and commits).  Split operands take
+        // three passes per product: (hi, hi), (hi, lo), (lo, hi).
         {
             const bool l0 = lane == 0;
             const uint32_t b1 = smem_u32(smem + C::kOffB1);
             const uint32_t rr = smem_u32(smem + C::kOffR);
             const uint32_t b3 = smem_u32(smem + C::kOffB3);
+            constexpr uint32_t kLbo1 = C::kB1M ? C::kB1M : 16384;
             for (int c = 0; c < nchunks; ++c) {
-                const int st = c & 1, use = c >> 1;
-                const uint32_t kq = smem_u32(smem + st * kStageBytes);
-                const uint32_t prep = kq + kOffPrep;
+                const int st = c % kStages, use = c / kStages;
+                const uint32_t kq = smem_u32(smem + st * C::kStageBytes);
+                const uint32_t prep = kq + C::kOffPrep;
                 if (!warp_wait(&bars->full[st], use & 1, abort)) break;
                 if (!warp_wait(&bars->state, c & 1, abort)) break;
                 tc_fence_after();
                 if (l0) {
 #pragma unroll
-                    for (int kb = 0; kb < 2; ++kb)
+                    for (int pass = 0; pass < (kSplit ? 3 : 1); ++pass) {
+                        const uint32_t a0 = kq + (pass == 2 ? C::kKQPart : 0u);
+                        const uint32_t bb = b1 + (pass == 1 ? C::kB1Part : 0u);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
-                            const uint64_t b = sdesc_sw128(b1 + (kb * 4 + kk) * 2048, 16384, 1024);
-                            mma_bf16(tmem + C::kColD1, a, b, C::kIdesc1, (kb | kk) != 0);
-                        }
+                        for (int kb = 0; kb < C::kHalves; ++kb)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t a = sdesc_sw128(a0 + kb * kKQHalf + kk * 32, 16, 1024);
+                                const uint64_t b = sdesc_sw128(bb + (kb * 4 + kk) * 2048, kLbo1, 1024);
+                                mma_bf16(tmem + C::kColD1, a, b, C::kIdesc1, (pass | kb | kk) != 0);
+                            }
+                    }
                     mma_commit(&bars->d1);
                 }
                 __syncwarp();
@@ -295,10 +370,15 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_after();
                 if (l0) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(prep + kk * 32, 16, 1024);
-                        const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
-                        mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, kk != 0);
+                    for (int pass = 0; pass < (kSplit ? 3 : 1); ++pass) {
+                        const uint32_t a0 = prep + (pass == 2 ? C::kPrepLo : 0u);
+                        const uint32_t bb = rr + (pass == 1 ? C::kRPart : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(a0 + kk * 32, 16, 1024);
+                            const uint64_t b = sdesc_sw128(bb + kk * 2048, 8192, 1024);
+                            mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, (pass | kk) != 0);
+                        }
                     }
                     mma_commit(&bars->d2);
                 }
@@ -307,10 +387,15 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 tc_fence_after();
                 if (l0) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = sdesc_sw128(kq + kk * 4096, 16384, 1024);
-                        const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
-                        mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
+                    for (int pass = 0; pass < (kSplit ? 3 : 1); ++pass) {
+                        const uint32_t a0 = kq + (pass == 2 ? C::kKQPart : 0u);
+                        const uint32_t bb = b3 + (pass == 1 ? C::kB3Part : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(a0 + kk * 4096, kKQHalf, 1024);
+                            const uint64_t b = sdesc_sw128(bb + kk * 2048, 8192, 1024);
+                            mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
+                        }
                     }
                     mma_commit(&bars->d3);
                     mma_commit(&bars->empty[st]);
@@ -332,11 +417,13 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         const int c0 = qc * kEpiCols;           // first column (within the slice)
         const uint32_t ch0 = qc * 2;            // first 16-byte chunk of those columns
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        const int row = 32 * q + lane;          // TMEM lane = D row
-        const int d = row;                      // state row (dk index)
+        // state row of this thread: lane = row for head size 128; lanes
+        // 0..15 of each quadrant for 64 (the M = 64 product's rows)
+        const bool row_ok = D == 128 || lane < 16;
+        const int d = D == 128 ? 32 * q + lane : 16 * q + (lane & 15);
         const uint32_t st_s = lane_base + C::kColSt + c0;       // S columns of this thread
         const uint32_t st_m = lane_base + C::kColSt + NS + c0;  // M columns
-        const size_t st_off = (size_t)sh * kD * kD + (size_t)d * kD + col0 + c0;
+        const size_t st_off = (size_t)sh * D * D + (size_t)d * D + col0 + c0;
         unsigned char *b1 = smem + C::kOffB1;
         unsigned char *rt = smem + C::kOffR;
         unsigned char *b3 = smem + C::kOffB3;
@@ -345,8 +432,8 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
 #pragma unroll
             for (int j = 0; j < kEpiCols; j += 4) {
                 float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), mv = sv;
-                if (p.S0) sv = *reinterpret_cast<const float4 *>(p.S0 + st_off + j);
-                if (p.M0) mv = *reinterpret_cast<const float4 *>(p.M0 + st_off + j);
+                if (p.S0 && row_ok) sv = *reinterpret_cast<const float4 *>(p.S0 + st_off + j);
+                if (p.M0 && row_ok) mv = *reinterpret_cast<const float4 *>(p.M0 + st_off + j);
                 S[j] = sv.x; S[j + 1] = sv.y; S[j + 2] = sv.z; S[j + 3] = sv.w;
                 M[j] = mv.x; M[j + 1] = mv.y; M[j + 2] = mv.z; M[j + 3] = mv.w;
             }
@@ -354,13 +441,16 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             tmem_st16(st_m, M);
             tmem_st_wait();
             if (nchunks > 0) {
-                store_row16(b1, d, ch0, S, 1.f);
-                store_row16(b1 + C::kB1M, d, ch0 + C::kChM, M, 1.f);
+                if (row_ok) {
+                    store_row16<kSplit>(b1, C::kB1Part, d, ch0, S);
+                    store_row16<kSplit>(b1 + C::kB1M, C::kB1Part, d, ch0 + C::kChM, M);
+                }
                 fence_proxy_async();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state);
-                if (kChunkStates) store_chunk_state(p, slot0, h, st_off - (size_t)sh * kD * kD, S, M);
+                if (kChunkStates && row_ok)
+                    store_chunk_state<D>(p, slot0, h, st_off - (size_t)sh * D * D, S, M);
             }
         }
         // Token rows: the lower 16 lanes of this warp's quadrant hold the K
@@ -372,14 +462,13 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
         const uint32_t chk = (uint32_t)(cg >> 3);     // their 16-byte chunk
         const uint32_t lk = tmem + ((uint32_t)(32 * q) << 16);        // K / T rows
         const uint32_t lq = tmem + ((uint32_t)(32 * q + 16) << 16);   // Q / A_O T rows
-        const size_t rs = (size_t)p.H * kD;
-        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * kD + col0 + cg;
-        __nv_bfloat16 *vg = p.vres ? static_cast<__nv_bfloat16 *>(p.vres) + (size_t)h * kD + col0 + cg
-                                   : nullptr;
+        const size_t rs = (size_t)p.H * D;
+        Tio *og = static_cast<Tio *>(p.o) + (size_t)h * D + col0 + cg;
+        Tio *vg = p.vres ? static_cast<Tio *>(p.vres) + (size_t)h * D + col0 + cg : nullptr;
         for (int c = 0; c < nchunks; ++c) {
-            const int st = c & 1, use = c >> 1;
-            unsigned char *stage = smem + st * kStageBytes;
-            const float *vec = reinterpret_cast<const float *>(stage + kOffPrep + PrepLayoutTC::kOffVec);
+            const int st = c % kStages, use = c / kStages;
+            unsigned char *stage = smem + st * C::kStageBytes;
+            const float *vec = reinterpret_cast<const float *>(stage + C::kOffPrep + C::kPrepVec);
             const int n = min(kChunk, len - c * kChunk);
             const int t0 = start + c * kChunk;
             if (!warp_wait(&bars->full[st], use & 1, abort)) break;
@@ -393,26 +482,35 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
             const float cbq = vec[kVecB * kChunk + tok];
             const float gs = vec[kVecGS * kChunk + tok];
             const float gm = vec[kVecGM * kChunk + tok];
-            uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
-            if (in_chunk) vraw = *reinterpret_cast<const uint4 *>(stage + kOffV + sw128_offset(tok, chk));
+            float vv[8];
+            {
+                uint4 vraw = make_uint4(0u, 0u, 0u, 0u), vlo = vraw;
+                if (in_chunk) {
+                    vraw = *reinterpret_cast<const uint4 *>(stage + C::kOffV + sw128_offset(tok, chk));
+                    if (kSplit)
+                        vlo = *reinterpret_cast<const uint4 *>(stage + C::kOffV + kVBytes +
+                                                               sw128_offset(tok, chk));
+                }
+                unpack_bf16x8(vraw, vv);
+                if (kSplit) {
+                    float vl[8];
+                    unpack_bf16x8(vlo, vl);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vv[e] += vl[e];
+                }
+            }
 
             // ---- R = V - abar K S_0 + b_{i-1} alpha_i K M_0: the critical step
             if (!warp_wait(&bars->d1, c & 1, abort)) break;
             tc_fence_after();
             {
-                float xs[8], xm[8], vv[8], r[8];
+                float xs[8], xm[8], r[8];
                 tmem_ld_16x2x8(lk + C::kColD1 + c0, xs);
                 tmem_ld_16x2x8(lk + C::kColD1 + NS + c0, xm);
                 tmem_ld_wait();
-                unpack_bf16x8(vraw, vv);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) r[e] = vv[e] - abk * xs[e] + cbk * xm[e];
-                uint4 w;
-                w.x = pack_bf16x2(r[0], r[1]);
-                w.y = pack_bf16x2(r[2], r[3]);
-                w.z = pack_bf16x2(r[4], r[5]);
-                w.w = pack_bf16x2(r[6], r[7]);
-                *reinterpret_cast<uint4 *>(rt + sw128_offset(tok, chk)) = w;
+                put8<kSplit>(rt, C::kRPart, tok, chk, r, 1.f);
                 fence_proxy_async();
                 tc_fence_before();
                 __syncwarp();
@@ -437,26 +535,11 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                 float x[8];
                 tmem_ld_16x2x8(lk + C::kColD2 + c0, x);
                 tmem_ld_wait();
-                uint4 w;
-                w.x = pack_bf16x2(gs * x[0], gs * x[1]);
-                w.y = pack_bf16x2(gs * x[2], gs * x[3]);
-                w.z = pack_bf16x2(gs * x[4], gs * x[5]);
-                w.w = pack_bf16x2(gs * x[6], gs * x[7]);
-                *reinterpret_cast<uint4 *>(b3 + sw128_offset(tok, chk)) = w;
-                w.x = pack_bf16x2(-gm * x[0], -gm * x[1]);
-                w.y = pack_bf16x2(-gm * x[2], -gm * x[3]);
-                w.z = pack_bf16x2(-gm * x[4], -gm * x[5]);
-                w.w = pack_bf16x2(-gm * x[6], -gm * x[7]);
-                *reinterpret_cast<uint4 *>(b3 + C::kB3M + sw128_offset(tok, chk + C::kChM)) = w;
+                put8<kSplit>(b3, C::kB3Part, tok, chk, x, gs);
+                put8<kSplit>(b3 + C::kB3M, C::kB3Part, tok, chk + C::kChM, x, -gm);
                 fence_proxy_async();
-                if (vg && in_chunk) {
-                    // the residuals themselves, for a gradient pass
-                    w.x = pack_bf16x2(x[0], x[1]);
-                    w.y = pack_bf16x2(x[2], x[3]);
-                    w.z = pack_bf16x2(x[4], x[5]);
-                    w.w = pack_bf16x2(x[6], x[7]);
-                    *reinterpret_cast<uint4 *>(vg + (size_t)(t0 + tok) * rs) = w;
-                }
+                // the residuals themselves, for a gradient pass
+                if (vg && in_chunk) store_out8(vg + (size_t)(t0 + tok) * rs, x);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->v);
@@ -479,8 +562,10 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                     tmem_ld16(st_s, S);
                     tmem_ld16(st_m, M);
                     tmem_ld_wait();
-                    store_row16(b1, d, ch0, S, 1.f);
-                    store_row16(b1 + C::kB1M, d, ch0 + C::kChM, M, 1.f);
+                    if (row_ok) {
+                        store_row16<kSplit>(b1, C::kB1Part, d, ch0, S);
+                        store_row16<kSplit>(b1 + C::kB1M, C::kB1Part, d, ch0 + C::kChM, M);
+                    }
                     fence_proxy_async();
                 }
                 tc_fence_before();
@@ -490,30 +575,27 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap 
                     mbar_arrive(&bars->empty[st]);
                 }
                 // the next chunk's entry state, after the chain has moved on
-                if (kChunkStates && more)
-                    store_chunk_state(p, slot0 + c + 1, h, st_off - (size_t)sh * kD * kD, S, M);
+                if (kChunkStates && more && row_ok)
+                    store_chunk_state<D>(p, slot0 + c + 1, h, st_off - (size_t)sh * D * D, S, M);
             }
             // ---- outputs of this chunk (off the critical path)
-            if (in_chunk) {
-                uint4 w;
-                w.x = pack_bf16x2(oint[0], oint[1]);
-                w.y = pack_bf16x2(oint[2], oint[3]);
-                w.z = pack_bf16x2(oint[4], oint[5]);
-                w.w = pack_bf16x2(oint[6], oint[7]);
-                *reinterpret_cast<uint4 *>(og + (size_t)(t0 + tok) * rs) = w;
-            }
+            if (in_chunk) store_out8(og + (size_t)(t0 + tok) * rs, oint);
         }
         if (!*abort) {
+            // every lane takes part in the warp's loads; lanes with a state
+            // row store it
             float S[kEpiCols], M[kEpiCols];
             tmem_ld16(st_s, S);
             tmem_ld16(st_m, M);
             tmem_ld_wait();
+            if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < kEpiCols; j += 4) {
-                if (p.S_T)
-                    *reinterpret_cast<float4 *>(p.S_T + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-                if (p.M_T)
-                    *reinterpret_cast<float4 *>(p.M_T + st_off + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
+                for (int j = 0; j < kEpiCols; j += 4) {
+                    if (p.S_T)
+                        *reinterpret_cast<float4 *>(p.S_T + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                    if (p.M_T)
+                        *reinterpret_cast<float4 *>(p.M_T + st_off + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
+                }
             }
         }
     }
@@ -540,27 +622,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, h, t); box 64 x 1 x box_t.
-bool make_map(CUtensorMap *map, const void *base, int T_total, int H, bool swizzle,
-              int box_t = 64) {
+// [T_total, H, D] bf16 viewed as a 3-D tensor (d, h, t); box 64 x 1 x box_t.
+bool make_map(CUtensorMap *map, const void *base, int T_total, int H, int D, int box_t) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)box_t};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int NS, bool kChunkStates>
-cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const CUtensorMap &mk,
-                              const CUtensorMap &mq, const CUtensorMap &mv) {
-    using C = Cfg<NS>;
-    auto kern = chunk_state_tc_kernel<NS, kChunkStates>;
+template <int D, int NS, bool kChunkStates, bool kSplit>
+cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
+    using C = Cfg<D, NS, kSplit>;
+    auto kern = chunk_state_tc_kernel<D, NS, kChunkStates, kSplit>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)C::kSmemBytes);
     if (err != cudaSuccess) return err;
@@ -582,34 +661,65 @@ cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p, mk, mq, mv);
+    return cudaLaunchKernelEx(&cfg, kern, p, maps);
+}
+
+// Split operands at head size 128 leave no room for 64-column slices (their
+// single stage and doubled operands exceed a CTA's shared memory): 32.
+template <int D, bool kSplit>
+constexpr int kWidestSlice = (kSplit && D == 128) ? 32 : 64;
+
+template <int D, bool kSplit>
+cudaError_t launch_state_tc_d(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
+    const long chains = (long)p.n_seq * p.H;
+    const int sms = device_sm_count();
+    const int ns = (sms > 0 && chains * (D / 16) <= sms) ? 16
+                 : ((sms > 0 && chains * (D / 32) <= sms) || kWidestSlice<D, kSplit> == 32) ? 32
+                                                                                         : 64;
+    if (p.S_chunks) {
+        if (ns == 16) return launch_state_tc_t<D, 16, true, kSplit>(p, st, maps);
+        if (ns == 32) return launch_state_tc_t<D, 32, true, kSplit>(p, st, maps);
+        if constexpr (kWidestSlice<D, kSplit> == 64)
+            return launch_state_tc_t<D, 64, true, kSplit>(p, st, maps);
+        return cudaErrorInvalidConfiguration;
+    }
+    if (ns == 16) return launch_state_tc_t<D, 16, false, kSplit>(p, st, maps);
+    if (ns == 32) return launch_state_tc_t<D, 32, false, kSplit>(p, st, maps);
+    if constexpr (kWidestSlice<D, kSplit> == 64)
+        return launch_state_tc_t<D, 64, false, kSplit>(p, st, maps);
+    return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace
 
 // The slice width trades per-chunk latency (narrow slices: smaller MMAs and
 // epilogues) against CTA count: the narrowest slices (16, 32 or 64 columns)
-// whose CTAs still fit on the GPU in one wave.
+// whose CTAs still fit on the GPU in one wave.  bf16 inputs read q, k, v
+// directly; fp32 inputs read their hi / lo bf16 parts.
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
-    if (p.D != kD || p.dtype != MDN_BF16) return cudaErrorInvalidValue;
+    if (p.D != 64 && p.D != 128) return cudaErrorInvalidValue;
+    const bool split = p.dtype == MDN_F32;
+    if (split && !p.k_hi) return cudaErrorInvalidValue;
     if (p.prep_stride % 16 != 0) return cudaErrorInvalidValue;
-    CUtensorMap mk, mq, mv;
+    Maps maps;
     const int Tt = p.T_total > 0 ? p.T_total : 1;
-    if (!make_map(&mk, p.k, Tt, p.H, true, 16) || !make_map(&mq, p.q, Tt, p.H, true, 16) ||
-        !make_map(&mv, p.v, Tt, p.H, true))
+    const void *k = split ? p.k_hi : p.k, *q = split ? p.q_hi : p.q;
+    const void *v = split ? p.v_hi : p.v;
+    if (!make_map(&maps.k, k, Tt, p.H, p.D, 16) || !make_map(&maps.q, q, Tt, p.H, p.D, 16) ||
+        !make_map(&maps.v, v, Tt, p.H, p.D, 64))
         return cudaErrorInvalidValue;
-    const long chains = (long)p.n_seq * p.H;
-    const int sms = device_sm_count();
-    const int ns = (sms > 0 && chains * Cfg<16>::kSlices <= sms) ? 16
-                 : (sms > 0 && chains * Cfg<32>::kSlices <= sms) ? 32 : 64;
-    if (p.S_chunks) {
-        if (ns == 16) return launch_state_tc_t<16, true>(p, st, mk, mq, mv);
-        if (ns == 32) return launch_state_tc_t<32, true>(p, st, mk, mq, mv);
-        return launch_state_tc_t<64, true>(p, st, mk, mq, mv);
-    }
-    if (ns == 16) return launch_state_tc_t<16, false>(p, st, mk, mq, mv);
-    if (ns == 32) return launch_state_tc_t<32, false>(p, st, mk, mq, mv);
-    return launch_state_tc_t<64, false>(p, st, mk, mq, mv);
+    maps.k_lo = maps.k;
+    maps.q_lo = maps.q;
+    maps.v_lo = maps.v;
+    if (split && (!make_map(&maps.k_lo, p.k_lo, Tt, p.H, p.D, 16) ||
+                  !make_map(&maps.q_lo, p.q_lo, Tt, p.H, p.D, 16) ||
+                  !make_map(&maps.v_lo, p.v_lo, Tt, p.H, p.D, 64)))
+        return cudaErrorInvalidValue;
+    if (p.D == 128)
+        return split ? launch_state_tc_d<128, true>(p, st, maps)
+                     : launch_state_tc_d<128, false>(p, st, maps);
+    return split ? launch_state_tc_d<64, true>(p, st, maps)
+                 : launch_state_tc_d<64, false>(p, st, maps);
 }
 
 }  // namespace mdn

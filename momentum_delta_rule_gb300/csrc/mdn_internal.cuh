@@ -59,6 +59,11 @@ struct PrepLayoutTC {
     static constexpr size_t kOffAOT = 8192;
     static constexpr size_t kOffVec = 16384;
     static constexpr size_t kBytes = 16384 + sizeof(float) * kChunk * kVecRows;
+    // fp32 inputs: the operand [T; A_O T] as two bf16 parts, hi = bf16(x)
+    // at 0 and lo = bf16(x - hi) at kSplitLo, then the vectors
+    static constexpr size_t kSplitLo = 16384;
+    static constexpr size_t kSplitVec = 32768;
+    static constexpr size_t kSplitBytes = 32768 + sizeof(float) * kChunk * kVecRows;
 };
 
 // Largest prepared block of any path (fp32 matrices).
@@ -82,6 +87,9 @@ struct ChunkProblem {
     unsigned char *prep;         // max_chunks * H prepared blocks
     size_t prep_stride;          // bytes per prepared block
     int *status;                 // device status word
+    // fp32 inputs on the tensor cores: q, k, v as hi / lo bf16 parts
+    // [T_total, H, D] in the workspace (null for bf16 inputs)
+    void *q_hi, *q_lo, *k_hi, *k_lo, *v_hi, *v_lo;
 };
 
 struct DecodeProblem {
@@ -147,6 +155,7 @@ mdn_status chunk_fwd_check(const void *q, const void *k, const void *v, const fl
 cudaError_t launch_prepare_inputs(const InputsProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
+cudaError_t launch_split_inputs(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);

@@ -47,7 +47,6 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kD = 128;
 constexpr int kThreadsP = 256;
 constexpr int LM = kChunk + 1;                 // padded fp32 row stride
 
@@ -174,9 +173,11 @@ __device__ __forceinline__ void scan64_gates(float &A, float &U, float &Z, float
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreadsP, 4)
 chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q) {
+    constexpr int kHalves = D / 64;           // 64-wide d_k halves of the K and Q tiles
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -224,11 +225,12 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         bars->abort = 0;
         fence_mbar_init();
         // K and Q tiles: their latency gates only the Gram MMA
-        mbar_arrive_expect_tx(&bars->tma, 32768);
-        tma_load_3d(smem + kOffKQ + 0, &map_k, &bars->tma, 0, h, loc.t0);
-        tma_load_3d(smem + kOffKQ + 8192, &map_q, &bars->tma, 0, h, loc.t0);
-        tma_load_3d(smem + kOffKQ + 16384, &map_k, &bars->tma, 64, h, loc.t0);
-        tma_load_3d(smem + kOffKQ + 24576, &map_q, &bars->tma, 64, h, loc.t0);
+        mbar_arrive_expect_tx(&bars->tma, 16384 * kHalves);
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+            tma_load_3d(smem + kOffKQ + hh * 16384, &map_k, &bars->tma, 64 * hh, h, loc.t0);
+            tma_load_3d(smem + kOffKQ + hh * 16384 + 8192, &map_q, &bars->tma, 64 * hh, h, loc.t0);
+        }
     }
     if (warp == 2) {
         tmem_alloc(&bars->tmem_base, kTmemColsP);
@@ -267,7 +269,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             if (mbar_wait(&bars->tma, 0, abort)) {
                 tc_fence_after();
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
+                for (int kb = 0; kb < kHalves; ++kb)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t a = sdesc_sw128(kq + kb * 16384 + kk * 32, 16, 1024);
@@ -665,11 +667,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_p() {
     return fn;
 }
 
-bool make_map_p(CUtensorMap *map, const void *base, int T_total, int H) {
+bool make_map_p(CUtensorMap *map, const void *base, int T_total, int H, int D) {
     auto fn = encode_fn_p();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
@@ -677,21 +679,27 @@ bool make_map_p(CUtensorMap *map, const void *base, int T_total, int H) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st) {
-    if (p.D != kD || p.dtype != MDN_BF16) return cudaErrorInvalidValue;
-    if (p.max_chunks == 0) return cudaSuccess;
+template <int D>
+cudaError_t launch_prep_tc_t(const ChunkProblem &p, cudaStream_t st) {
     CUtensorMap mk, mq;
-    if (!make_map_p(&mk, p.k, p.T_total, p.H) || !make_map_p(&mq, p.q, p.T_total, p.H))
+    if (!make_map_p(&mk, p.k, p.T_total, p.H, D) || !make_map_p(&mq, p.q, p.T_total, p.H, D))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(chunk_prep_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = chunk_prep_tc_kernel<D>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemP);
     if (err != cudaSuccess) return err;
     dim3 grid(p.max_chunks, p.H);
-    chunk_prep_tc_kernel<<<grid, kThreadsP, kSmemP, st>>>(p, mk, mq);
+    kern<<<grid, kThreadsP, kSmemP, st>>>(p, mk, mq);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+// bf16 inputs, head size 64 or 128.
+cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st) {
+    if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16) return cudaErrorInvalidValue;
+    if (p.max_chunks == 0) return cudaSuccess;
+    return p.D == 128 ? launch_prep_tc_t<128>(p, st) : launch_prep_tc_t<64>(p, st);
 }
 
 }  // namespace mdn

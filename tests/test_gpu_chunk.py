@@ -142,10 +142,10 @@ def test_varlen_packed_full_size_sampled():
     compare(x, out, _sample(x, 4) + [shortest])
 
 
-def test_fp32_many_chains_wide_cuda_core_slices():
+def test_fp32_many_chains_two_waves():
     """fp32 inputs at d = 128 with more chains than 32-column CTAs fit in one
-    wave (>= 39 chains on 152 SMs): the CUDA-core state pass then runs
-    64-column CTAs of 1024 threads; ragged chunks and mu = 0 entries."""
+    wave (>= 39 chains on 152 SMs): the split-operand state pass keeps
+    32-column slices and runs two waves; ragged chunks and mu = 0 entries."""
     w = W.Workload("fp32_wide", dtype="fp32", state="randn", seed=18)
     x = W.make_prefill(w, B=3, T=130, H=16, D=128, with_beta=True)
     x["mu"][:, ::7] = 0.0
@@ -163,24 +163,39 @@ def test_very_long_sequence_sampled():
 
 
 def test_path_selection():
-    """bf16 inputs with head size 128 run on the tensor-core path; fp32 inputs
-    and head size 64 on the CUDA-core path."""
+    """Every input runs on the tensor-core path: bf16 directly, fp32 as hi /
+    lo bf16 parts, head size 64 and 128 alike."""
     import momentum_delta_rule_gb300 as mdn
-    for dtype, D, want in (("bf16", 128, mdn.MDN_PATH_TENSOR_CORE),
-                           ("fp32", 128, mdn.MDN_PATH_CUDA_CORE),
-                           ("bf16", 64, mdn.MDN_PATH_CUDA_CORE)):
+    for dtype, D in (("bf16", 128), ("fp32", 128), ("bf16", 64), ("fp32", 64)):
         w = W.Workload("path", dtype=dtype, state="zero", seed=15)
         x = W.make_prefill(w, B=1, T=70, H=1, D=D)
         info = {}
         gpu_chunk_fwd(x, info=info)
-        assert info["path"] == want, (dtype, D, info)
+        assert info["path"] == mdn.MDN_PATH_TENSOR_CORE, (dtype, D, info)
 
 
-@pytest.mark.parametrize("B,H", [(2, 2), (5, 5), (5, 10)])
-def test_slice_widths(B, H):
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("fp32", 128), ("bf16", 64), ("fp32", 64)])
+@pytest.mark.parametrize("B,H", [(2, 2), (5, 5), (5, 10), (7, 11)])
+def test_slice_widths(B, H, dtype, D):
     """The tensor-core state pass picks 16-, 32- or 64-column state slices by
-    the number of (sequence, head) chains (4, 25 and 50 chains here select
-    each width on a 152-SM GPU); every width must match the oracle."""
-    w = W.Workload("widths", dtype="bf16", state="randn", seed=16)
-    x = W.make_prefill(w, B=B, T=130, H=H, D=128, with_beta=True)
+    the number of (sequence, head) chains (4, 25, 50 and 77 chains here select
+    each width on a 152-SM GPU at head size 128; fp32 there stops at 32);
+    every width, head size and input type must match the oracle."""
+    w = W.Workload("widths", dtype=dtype, state="randn", seed=16)
+    x = W.make_prefill(w, B=B, T=130, H=H, D=D, with_beta=True)
+    compare(x, gpu_chunk_fwd(x), chains(x))
+
+
+def test_fp32_prefill_400m_shapes_sampled():
+    """fp32 inputs at the 400M-model shapes (B8 H8 T2048 d128) on the
+    tensor cores with split operands: sampled chains within the fp32
+    tolerance."""
+    w = W.Workload("fp32_400m", dtype="fp32", state="zero", seed=1)
+    x = W.make_prefill(w, B=8, T=2048, H=8, D=128)
+    compare(x, gpu_chunk_fwd(x), _sample(x, 3, seed=5))
+
+
+def test_fp32_packed_with_empty_sequences():
+    w = W.Workload("fp32_var", dtype="fp32", state="randn", seed=18)
+    x = W.make_prefill(w, H=2, D=64, lengths=[1, 64, 0, 65, 130, 7, 0], with_beta=True)
     compare(x, gpu_chunk_fwd(x), chains(x))

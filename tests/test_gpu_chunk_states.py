@@ -2,8 +2,8 @@
 chunk c of every sequence, the states after its first 64 c tokens, against
 the oracle recurrence run chunk by chunk from the previous chunk's states
 (split-sequence state passing, which the oracle's own tests pin).  Covers
-both implementation paths (tensor-core slices of 16 and 64 columns, and
-the CUDA-core path), ragged last chunks, packed sequences with empty
+tensor-core slices of 16 and 64 columns, fp32 inputs (split operands) and
+head size 64, ragged last chunks, packed sequences with empty
 members, mu = 0 entries and nonzero initial states."""
 import numpy as np
 import pytest
@@ -97,9 +97,10 @@ def test_chunk_states_packed_with_empty_sequences():
     _check(x)
 
 
-def test_chunk_states_cuda_core_path():
-    w = W.Workload("cs_fp32", dtype="fp32", state="randn", seed=54)
-    x = W.make_prefill(w, B=2, T=130, H=2, D=64, with_beta=True)
+@pytest.mark.parametrize("dtype,D", [("fp32", 64), ("fp32", 128), ("bf16", 64)])
+def test_chunk_states_split_and_head_size_64(dtype, D):
+    w = W.Workload("cs_fp32", dtype=dtype, state="randn", seed=54)
+    x = W.make_prefill(w, B=2, T=130, H=2, D=D, with_beta=True)
     _check(x)
 
 
