@@ -198,7 +198,7 @@ def kernel_flops_per_token_head(d, C=64):
             "state": 12 * d * d + 4 * C * d}
 
 
-PREP_BLOCK_BYTES = {True: 18432, False: 34816}   # tensor-core / CUDA-core layout
+PREP_BLOCK_BYTES = {"bf16": 18432, "fp32": 34816}   # bf16 operands / split hi-lo operands
 
 
 def io_bytes(x):
@@ -215,11 +215,15 @@ def io_bytes(x):
             "states_out": 2 * state}
 
 
-def intermediate_bytes(x, tensor):
-    """Prepared blocks written by the prep kernel and read by the state pass
-    (an intermediate of this implementation, not algorithmic work)."""
+def intermediate_bytes(x, tensor=True):
+    """Prepared blocks written by the prep kernel and read by the state pass,
+    and for fp32 inputs the hi / lo bf16 parts of q, k, v (intermediates of
+    this implementation, not algorithmic work)."""
     chunks = sum((L + 63) // 64 for L in seq_lengths(x)) * x["H"]
-    return PREP_BLOCK_BYTES[bool(tensor)] * chunks
+    blocks = PREP_BLOCK_BYTES[x["dtype"]] * chunks
+    if x["dtype"] == "fp32":
+        blocks += 2 * 3 * 2 * sum(seq_lengths(x)) * x["H"] * x["D"]   # written, then read
+    return blocks
 
 
 def algorithmic(x, what):
@@ -236,10 +240,20 @@ def algorithmic(x, what):
 
 def roofline_of(x, what, tensor, ms, peaks, peak_src):
     """Binding roofline of the whole call or one kernel: whichever of its
-    algorithmic HBM bytes or FLOPs needs more time at the measured peak."""
+    algorithmic HBM bytes or FLOPs needs more time at the measured peak.
+    bf16 inputs: the bf16 tensor peak.  fp32 inputs: the state pass's
+    contractions are three bf16 products each (split operands), so its peak
+    is a third of the bf16 one; the fp32 prep runs on the CUDA cores (FFMA
+    peak)."""
     by, fl = algorithmic(x, what)
     s = ms / 1e3
-    if tensor:
+    fp32 = x["dtype"] == "fp32"
+    if fp32 and what == "prep":
+        tensor = False
+    if tensor and fp32:
+        tflops_peak = peaks["bf16_tflops"] / 3.0
+        fl_src = "%s bf16 burst / 3 (split operands: three bf16 products per fp32 one)" % peak_src
+    elif tensor:
         tflops_peak = peaks["bf16_tflops"]
         fl_src = "%s bf16 burst" % peak_src
     else:
@@ -759,12 +773,13 @@ def measure_prefill(mdn, w, x, dev, args, steps, warmup, world, flush, peaks, pe
     out["roofline_call"]["what"] = "whole chunk forward (every kernel of the call)"
     out["stages"] = stages
     out["intermediate_bytes"] = {
-        "prepared_blocks": intermediate_bytes(x, tensor),
-        "what": "written by the prep kernel and read by the state pass; "
+        "bytes": intermediate_bytes(x),
+        "what": "prepared blocks written by the prep kernel and read by the state pass "
+                "(and, for fp32 inputs, the hi / lo bf16 parts of q, k, v); "
                 "not algorithmic work"}
     out["config"] = config_of(w, x, "flushed before every timed step: 256 MiB written, "
                                     "then another 256 MiB read")
-    out["dtype"] = "bf16" if tensor else "f32"
+    out["dtype"] = "bf16" if x["dtype"] == "bf16" else "f32 (split bf16 operands)"
     if e2e and not args.no_e2e:
         n = max(3, min(steps, 10))
         e_ms, h2d, d2h = time_e2e(mdn, x, x_dev, n, 2)
@@ -849,7 +864,9 @@ def main():
     if not args.no_other_workloads:
         others = {}
         n = max(3, min(args.steps, 5))
-        for wo in W.ALL:
+        extra = [W.Workload("prefill_400m_fp32_B8_H8_T2048_d128", B=8, T=2048, H=8, D=128,
+                            dtype="fp32", state="zero", seed=1)]
+        for wo in W.ALL + extra:
             if wo.decode_steps or wo.name == w.name:
                 continue
             xo = W.make_prefill(wo)

@@ -312,8 +312,12 @@ mdn_status mdn_block_fwd(const void *x, const void *W_in, const float *conv_w,
 
 /* Implementation paths of mdn_chunk_fwd (reported by the profiled variant). */
 typedef enum mdn_path {
-    MDN_PATH_CUDA_CORE = 0,   /* fp32 FFMA kernels: fp32 inputs, head size 64 */
-    MDN_PATH_TENSOR_CORE = 1  /* tcgen05 kernels: bf16 inputs, head size 128 */
+    MDN_PATH_CUDA_CORE = 0,   /* no tensor-core work: a call without tokens
+                                 (the initial states pass through) */
+    MDN_PATH_TENSOR_CORE = 1  /* tcgen05 state pass: every call with tokens;
+                                 bf16 inputs directly (tcgen05 prep), fp32
+                                 inputs as hi / lo bf16 parts with three
+                                 products per contraction (fp32 prep) */
 } mdn_path;
 
 /*

@@ -225,7 +225,7 @@ mdn_status chunk_fwd_impl(
     // directly (prep on the tensor cores too), fp32 inputs as hi / lo bf16
     // parts with three products per contraction, their T and A_O T from the
     // fp32 prep (an fp32-level error bound needs the fp32 inverse).  With no
-    // tokens only the initial states pass through (CUDA-core kernel).
+    // tokens only the initial states pass through.
     const bool tensor = T_total > 0;
     const bool split = tensor && dtype == MDN_F32;
     if (split) {
@@ -246,7 +246,7 @@ mdn_status chunk_fwd_impl(
         err = (tensor && !split) ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs);
     if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
     if (err == cudaSuccess)
-        err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_chunk_state_simt(p, cs);
+        err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_states_passthrough(p, cs);
     if (err == cudaSuccess && ev[2]) err = cudaEventRecord(ev[2], cs);
     if (err != cudaSuccess) {
         cudaGetLastError();

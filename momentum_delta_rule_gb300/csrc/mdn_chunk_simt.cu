@@ -1,17 +1,17 @@
-// MDN chunkwise forward, CUDA-core (FFMA) path.
+// MDN chunkwise forward, the CUDA-core (FFMA) kernels around the tensor-core
+// state pass:
 //
-// Serves fp32 inputs (where one bf16/tf32 tensor-core pass would not hold an
-// fp32-level error) and head size 64.  It follows the same two-stage plan as
-// the tensor-core path:
-//
-//   prep  (one CTA per chunk and head, all chunks in parallel)
-//         log-space prefix scans of alpha and mu, the coefficient matrix
-//         Gamma, the Gram matrices K K^T and Q K^T, the unit-lower-triangular
-//         system matrix, its inverse T and the intra-chunk output operator
-//         A_O T, written to a prepared block in the workspace;
-//   state (one CTA per sequence, head and 32-column slice, chunks in order)
-//         the state-dependent part of each chunk: residual right-hand side,
-//         residuals, outputs and the carry of S and M.
+//   offsets  the chunk offsets and longest-first order of packed sequences,
+//            with the device-side check of cu_seqlens;
+//   prep     for fp32 inputs (one CTA per chunk and head, all chunks in
+//            parallel): log-space prefix scans of alpha and mu, the
+//            coefficient matrix Gamma, the Gram matrices K K^T and Q K^T, the
+//            unit-lower-triangular system matrix, its inverse T and the
+//            intra-chunk output operator A_O T, all in fp32 (an fp32-level
+//            error bound needs the fp32 inverse), written as the hi / lo
+//            bf16 parts of the state pass's operand [T; A_O T];
+//   split    fp32 q, k, v as hi / lo bf16 parts for the state pass;
+//   states   calls without tokens: final states = initial states.
 //
 // Equations: "MDN: Parallelizing Stepwise Momentum for Delta Linear
 // Attention" slides, frames "Reorder the triangular sum ..." (Eqs. (7)-(9)),
@@ -19,12 +19,6 @@
 // (15)-(18)), "Chunk outputs combine incoming states and local writes"
 // (Appendix C Eqs. (40)-(42)), backup frames on the one-row shift and on the
 // log-domain coefficients (Algorithm 1); reading notes sections 2.3-2.6.
-//
-// With p_i = alpha_i k_i the residual right-hand side simplifies:
-// Diag(abar_shifted) P = Diag(abar) K and Diag(b_shifted) P = Diag(b_{i-1}
-// alpha_i) K, so the state pass needs only K S_0 and K M_0.  Writing
-// R = V - Diag(abar) K S_0 + Diag(b_{i-1} alpha_i) K M_0, the residuals are
-// Vres = T R and the in-chunk output term is (A_O T) R.
 #include <type_traits>
 
 #include "mdn_internal.cuh"
@@ -34,7 +28,6 @@ namespace mdn {
 namespace {
 
 constexpr int kThreads = 256;     // prep
-// state pass: 16 row groups of 4 token rows and D/16 state rows, x 32 or 64 columns
 
 // ------------------------------------------------------------- offsets
 
@@ -462,317 +455,16 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     }
 }
 
-// --------------------------------------------------------------- state
+// ----------------------------------------------------- no-token calls
 
-// The state pass runs 16 row groups x NSC state columns per CTA (NSC = 32:
-// 512 threads; NSC = 64: 1024 threads, so that fp32 prefills with many
-// (sequence, head) chains at d = 128 fit the GPU in one wave).  With
-// NSC = 32 the next chunk's K and vectors are double-buffered.
-template <int D, int NSC>
-struct StateSmem {
-    static constexpr bool kPrefetchK = NSC == 32;
-    static constexpr int kFloats = 2 * kChunk * D        // K, Q
-                                 + kChunk * NSC          // V slice
-                                 + 2 * kChunk * kChunk   // T, AOT
-                                 + kVecRows * kChunk     // vectors
-                                 + 2 * D * NSC           // S, M slices
-                                 + 2 * kChunk * NSC      // R, scaled residuals
-                                 + (kPrefetchK ? kChunk * D + kVecRows * kChunk : 0);
-    static constexpr size_t kBytes = sizeof(float) * kFloats;
-};
-
-// 16-byte asynchronous copy global -> shared; src_bytes 0 fills zeros.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-template <int D, typename Tin, int NSC>
-__global__ void __launch_bounds__(16 * NSC)
-chunk_state_simt_kernel(ChunkProblem p) {
-    constexpr int kNS = NSC;                            // state columns of this CTA
-    constexpr int kThreadsS = 16 * NSC;                 // 16 row groups x kNS columns
-    constexpr int kSlices = D / kNS;
-    constexpr int kRowsA = kChunk / 16;                 // token rows per row group
-    constexpr int kRowsC = D / 16;                      // state rows per row group
-    const int slice = blockIdx.x % kSlices;
-    const int kh = blockIdx.x / kSlices;
-    const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
-    const int sh = s * p.H + h;
-    // thread = (row group wg, column cc); a warp is 32 adjacent columns of one
-    // row group, so the row group's K, Q and T rows are warp-wide broadcasts
-    const int tid = threadIdx.x;
-    const int cc = ((tid >> 5) % (kNS / 32)) * 32 + (tid & 31), wg = (tid >> 5) / (kNS / 32);
-    const int col0 = slice * kNS;
-
-    extern __shared__ float smem[];
-    float *Ks = smem;
-    float *Qs = Ks + kChunk * D;
-    float *Vs = Qs + kChunk * D;
-    float *Ts = Vs + kChunk * kNS;
-    float *AOTs = Ts + kChunk * kChunk;
-    float *vec = AOTs + kChunk * kChunk;
-    float *Ss = vec + kVecRows * kChunk;
-    float *Ms = Ss + D * kNS;
-    float *Rs = Ms + D * kNS;
-    float *Vr = Rs + kChunk * kNS;
-    float *Kalt = Vr + kChunk * kNS;           // the next chunk's K ...
-    float *vecalt = Kalt + kChunk * D;         // ... and vectors
-    // fp32 inputs are copied as they are, so the next chunk's tiles stream in
-    // with asynchronous copies while this chunk computes (K and the vectors
-    // double-buffered, Q and V once the residuals are formed, T and A_O T once
-    // the outputs are); bf16 inputs are converted by plain loads per chunk.
-    constexpr bool kAsync = std::is_same<Tin, float>::value;
-    constexpr bool kPrefK = kAsync && StateSmem<D, NSC>::kPrefetchK;
-
-    int start, len, slot0;
-    sequence_range(p, s, start, len, slot0);
-    const int nchunks = (len + kChunk - 1) / kChunk;
-    const size_t st_off = (size_t)sh * D * D;
-
-#pragma unroll
-    for (int idx = tid; idx < D * kNS; idx += kThreadsS) {
-        const int d = idx / kNS, c = idx - d * kNS;
-        const size_t g = st_off + (size_t)d * D + col0 + c;
-        Ss[idx] = p.S0 ? p.S0[g] : 0.f;
-        Ms[idx] = p.M0 ? p.M0[g] : 0.f;
-    }
-
-    const size_t rs = (size_t)p.H * D;
-    const Tin *kg0 = static_cast<const Tin *>(p.k) + (size_t)h * D;
-    const Tin *qg0 = static_cast<const Tin *>(p.q) + (size_t)h * D;
-    const Tin *vg0 = static_cast<const Tin *>(p.v) + (size_t)h * D + col0;
-    Tin *og0 = static_cast<Tin *>(p.o) + (size_t)h * D + col0;
-    Tin *rg0 = p.vres ? static_cast<Tin *>(p.vres) + (size_t)h * D + col0 : nullptr;
-
-    // asynchronous copies of chunk cn's tiles (fp32 inputs only); rows past
-    // the chunk end are zero-filled
-    auto rows_of = [&](int cn, int &t0n, int &nn) {
-        t0n = start + cn * kChunk;
-        nn = min(kChunk, len - cn * kChunk);
-    };
-    auto copy_kq = [&](int cn, float *dst, const Tin *src0) {
-        int t0n, nn;
-        rows_of(cn, t0n, nn);
-        for (int idx = tid; idx < kChunk * D / 4; idx += kThreadsS) {
-            const int i = idx / (D / 4), q4 = idx - i * (D / 4);
-            const bool v = i < nn;
-            const Tin *src = src0 + (size_t)(t0n + (v ? i : 0)) * rs + 4 * q4;
-            cp_async16(dst + i * D + 4 * q4, src, v ? 16u : 0u);
-        }
-    };
-    auto copy_v = [&](int cn) {
-        int t0n, nn;
-        rows_of(cn, t0n, nn);
-        for (int idx = tid; idx < kChunk * kNS / 4; idx += kThreadsS) {
-            const int i = idx / (kNS / 4), q4 = idx - i * (kNS / 4);
-            const bool v = i < nn;
-            const Tin *src = vg0 + (size_t)(t0n + (v ? i : 0)) * rs + 4 * q4;
-            cp_async16(Vs + i * kNS + 4 * q4, src, v ? 16u : 0u);
-        }
-    };
-    auto block_of = [&](int cn) {
-        return p.prep + ((size_t)(slot0 + cn) * p.H + h) * p.prep_stride;
-    };
-    auto copy_floats = [&](float *dst, const unsigned char *src, int nfloats) {
-        for (int idx = tid; idx < nfloats / 4; idx += kThreadsS)
-            cp_async16(dst + 4 * idx, src + 16 * (size_t)idx, 16u);
-    };
-    if (kAsync && nchunks > 0) {
-        const unsigned char *b0 = block_of(0);
-        copy_kq(0, Ks, kg0);
-        copy_kq(0, Qs, qg0);
-        copy_v(0);
-        copy_floats(Ts, b0 + PrepLayout<float>::kOffT, kChunk * kChunk);
-        copy_floats(AOTs, b0 + PrepLayout<float>::kOffAOT, kChunk * kChunk);
-        copy_floats(vec, b0 + PrepLayout<float>::kOffVec, kVecRows * kChunk);
-        cp_async_commit();
-    }
-
-    for (int c = 0; c < nchunks; ++c) {
-        const int t0 = start + c * kChunk;
-        const int n = min(kChunk, len - c * kChunk);
-        const unsigned char *blk = p.prep + ((size_t)(slot0 + c) * p.H + h) * p.prep_stride;
-        const float *Tg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffT);
-        const float *AOTg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffAOT);
-        const float *vg = reinterpret_cast<const float *>(blk + PrepLayout<float>::kOffVec);
-
-        if (kAsync) cp_async_wait_all();   // this chunk's tiles have landed
-        __syncthreads();   // previous chunk finished with every buffer
-        if (kAsync && !kPrefK && c > 0) {
-            // K and the vectors have no second buffer at this width
-            copy_kq(c, Ks, kg0);
-            copy_floats(vec, block_of(c) + PrepLayout<float>::kOffVec, kVecRows * kChunk);
-            cp_async_commit();
-            cp_async_wait_all();
-            __syncthreads();
-        }
-        if (p.S_chunks) {
-            // the entry state of this chunk, at its chunk slot
-            const size_t cs = ((size_t)(slot0 + c) * p.H + h) * D * D;
-            for (int idx = tid; idx < D * kNS; idx += kThreadsS) {
-                const int d = idx / kNS, cx = idx - d * kNS;
-                const size_t g = cs + (size_t)d * D + col0 + cx;
-                p.S_chunks[g] = Ss[idx];
-                p.M_chunks[g] = Ms[idx];
-            }
-        }
-        if (!kAsync) {
-#pragma unroll
-            for (int idx = tid; idx < kChunk * D; idx += kThreadsS) {
-                const int i = idx / D, d = idx - i * D;
-                float kv = 0.f, qv = 0.f;
-                if (i < n) {
-                    kv = to_f32(kg0[(size_t)(t0 + i) * rs + d]);
-                    qv = to_f32(qg0[(size_t)(t0 + i) * rs + d]);
-                }
-                Ks[idx] = kv;
-                Qs[idx] = qv;
-            }
-#pragma unroll
-            for (int idx = tid; idx < kChunk * kNS; idx += kThreadsS) {
-                const int i = idx / kNS, cx = idx - i * kNS;
-                Vs[idx] = (i < n) ? to_f32(vg0[(size_t)(t0 + i) * rs + cx]) : 0.f;
-            }
-#pragma unroll
-            for (int idx = tid; idx < kChunk * kChunk; idx += kThreadsS) {
-                Ts[idx] = Tg[idx];
-                AOTs[idx] = AOTg[idx];
-            }
-#pragma unroll
-            for (int idx = tid; idx < kVecRows * kChunk; idx += kThreadsS) vec[idx] = vg[idx];
-        }
-        __syncthreads();
-
-        // ---- K S_0, K M_0, Q S_0, Q M_0 for kRowsA token rows x 1 column;
-        //      the K and Q rows (the same for the whole warp) four at a time
-        float ks[kRowsA] = {}, km[kRowsA] = {}, qs[kRowsA] = {}, qm[kRowsA] = {};
-        for (int d = 0; d < D; d += 4) {
-            float sv[4], mv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                sv[u] = Ss[(d + u) * kNS + cc];
-                mv[u] = Ms[(d + u) * kNS + cc];
-            }
-#pragma unroll
-            for (int r = 0; r < kRowsA; ++r) {
-                const int i = wg * kRowsA + r;
-                const float4 kv = *reinterpret_cast<const float4 *>(Ks + i * D + d);
-                const float4 qv = *reinterpret_cast<const float4 *>(Qs + i * D + d);
-                ks[r] += kv.x * sv[0] + kv.y * sv[1] + kv.z * sv[2] + kv.w * sv[3];
-                km[r] += kv.x * mv[0] + kv.y * mv[1] + kv.z * mv[2] + kv.w * mv[3];
-                qs[r] += qv.x * sv[0] + qv.y * sv[1] + qv.z * sv[2] + qv.w * sv[3];
-                qm[r] += qv.x * mv[0] + qv.y * mv[1] + qv.z * mv[2] + qv.w * mv[3];
-            }
-        }
-        float oint[kRowsA];
-#pragma unroll
-        for (int r = 0; r < kRowsA; ++r) {
-            const int i = wg * kRowsA + r;
-            Rs[i * kNS + cc] = Vs[i * kNS + cc] - vec[kVecAbar * kChunk + i] * ks[r]
-                               + vec[kVecBmA * kChunk + i] * km[r];
-            oint[r] = vec[kVecAbar * kChunk + i] * qs[r] - vec[kVecB * kChunk + i] * qm[r];
-        }
-        __syncthreads();
-        if (kAsync && c + 1 < nchunks) {
-            // Q and V are free now; K and the vectors go to the other buffers
-            copy_kq(c + 1, Qs, qg0);
-            copy_v(c + 1);
-            if (kPrefK) {
-                copy_kq(c + 1, Kalt, kg0);
-                copy_floats(vecalt, block_of(c + 1) + PrepLayout<float>::kOffVec, kVecRows * kChunk);
-            }
-        }
-
-        // ---- residuals Vres = T R, outputs O = O_inter + (A_O T) R: the
-        //      warp's rows i0 .. i0 + kRowsA - 1 share every R column j < i0
-        //      (read once, four at a time with the rows of T and A_O T), then
-        //      the triangle j = i0 .. i
-        static_assert(kRowsA == 4, "four token rows per warp");
-        const int i0 = wg * kRowsA;
-        float vrr[kRowsA] = {}, oir[kRowsA] = {};
-        for (int j = 0; j < i0; j += 4) {
-            float rv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) rv[u] = Rs[(j + u) * kNS + cc];
-#pragma unroll
-            for (int r = 0; r < kRowsA; ++r) {
-                const float4 tv = *reinterpret_cast<const float4 *>(Ts + (i0 + r) * kChunk + j);
-                const float4 av = *reinterpret_cast<const float4 *>(AOTs + (i0 + r) * kChunk + j);
-                vrr[r] += tv.x * rv[0] + tv.y * rv[1] + tv.z * rv[2] + tv.w * rv[3];
-                oir[r] += av.x * rv[0] + av.y * rv[1] + av.z * rv[2] + av.w * rv[3];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kRowsA; ++u) {
-            const float rv = Rs[(i0 + u) * kNS + cc];
-#pragma unroll
-            for (int r = u; r < kRowsA; ++r) {
-                vrr[r] += Ts[(i0 + r) * kChunk + i0 + u] * rv;
-                oir[r] += AOTs[(i0 + r) * kChunk + i0 + u] * rv;
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kRowsA; ++r) {
-            const int i = i0 + r;
-            const float vr = vrr[r], oi = oir[r];
-            Vr[i * kNS + cc] = vr;
-            if (i < n) og0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(oint[r] + oi);
-            if (rg0 && i < n) rg0[(size_t)(t0 + i) * rs + cc] = from_f32<Tin>(vr);
-        }
-        __syncthreads();
-        if (kAsync && c + 1 < nchunks) {
-            // T and A_O T are free now
-            const unsigned char *bn = block_of(c + 1);
-            copy_floats(Ts, bn + PrepLayout<float>::kOffT, kChunk * kChunk);
-            copy_floats(AOTs, bn + PrepLayout<float>::kOffAOT, kChunk * kChunk);
-            cp_async_commit();
-        }
-
-        // ---- carry, both from the old S_0, M_0:
-        //      S <- abar_n S - b_n M + sum_i k_i gamma_{n,i} eta_i vres_i^T
-        //      M <- mubar_n M - sum_i k_i (prod_{u>i} mu_u) eta_i vres_i^T
-        const float abar_n = vec[kVecScal * kChunk + 0];
-        const float b_n = vec[kVecScal * kChunk + 1];
-        const float mubar_n = vec[kVecScal * kChunk + 2];
-        // the warp's kRowsC state rows d0 .. d0 + kRowsC - 1 at once: per
-        // token, its weighted residuals once and the K row four at a time
-        static_assert(kRowsC % 4 == 0, "state rows per warp");
-        const int d0 = wg * kRowsC;
-        float as[kRowsC] = {}, am[kRowsC] = {};
-        for (int i = 0; i < n; ++i) {
-            const float vv = Vr[i * kNS + cc];
-            const float gsv = vec[kVecGS * kChunk + i] * vv;
-            const float gmv = vec[kVecGM * kChunk + i] * vv;
-#pragma unroll
-            for (int r = 0; r < kRowsC; r += 4) {
-                const float4 kv = *reinterpret_cast<const float4 *>(Ks + i * D + d0 + r);
-                as[r] += kv.x * gsv; as[r + 1] += kv.y * gsv; as[r + 2] += kv.z * gsv; as[r + 3] += kv.w * gsv;
-                am[r] += kv.x * gmv; am[r + 1] += kv.y * gmv; am[r + 2] += kv.z * gmv; am[r + 3] += kv.w * gmv;
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kRowsC; ++r) {
-            const int d = d0 + r;
-            const float so = Ss[d * kNS + cc], mo = Ms[d * kNS + cc];
-            Ss[d * kNS + cc] = abar_n * so - b_n * mo + as[r];
-            Ms[d * kNS + cc] = mubar_n * mo - am[r];
-        }
-        if (kPrefK) {               // the next chunk's K and vectors are in the other buffers
-            float *t = Ks; Ks = Kalt; Kalt = t;
-            t = vec; vec = vecalt; vecalt = t;
-        }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < D * kNS; idx += kThreadsS) {
-        const int d = idx / kNS, cx = idx - d * kNS;
-        const size_t g = st_off + (size_t)d * D + col0 + cx;
-        if (p.S_T) p.S_T[g] = Ss[idx];
-        if (p.M_T) p.M_T[g] = Ms[idx];
+// With no tokens every sequence is empty: its final states are its initial
+// states (zero when absent).  One thread per state element.
+__global__ void __launch_bounds__(256)
+states_passthrough_kernel(const float *S0, const float *M0, float *S_T, float *M_T, long n) {
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += stride) {
+        if (S_T) S_T[i] = S0 ? S0[i] : 0.f;
+        if (M_T) M_T[i] = M0 ? M0[i] : 0.f;
     }
 }
 
@@ -785,18 +477,6 @@ cudaError_t launch_prep_t(const ChunkProblem &p, cudaStream_t st) {
     if (err != cudaSuccess) return err;
     dim3 grid(p.max_chunks, p.H);
     kp<<<grid, kThreads, PrepSmem<D>::kBytes, st>>>(p);
-    return cudaGetLastError();
-}
-
-template <int D, typename Tin, int NSC>
-cudaError_t launch_state_t(const ChunkProblem &p, cudaStream_t st) {
-    auto ks = chunk_state_simt_kernel<D, Tin, NSC>;
-    cudaError_t err = cudaFuncSetAttribute(
-        ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)StateSmem<D, NSC>::kBytes);
-    if (err != cudaSuccess) return err;
-    const long blocks = (long)p.n_seq * p.H * (D / NSC);
-    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
-    ks<<<(unsigned)blocks, 16 * NSC, StateSmem<D, NSC>::kBytes, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -854,17 +534,12 @@ cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st) {
                                : launch_prep_t<64, float>(p, st);
 }
 
-cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st) {
-    if (p.D == 128) {
-        if (p.dtype == MDN_BF16) return launch_state_t<128, __nv_bfloat16, 32>(p, st);
-        // 64-column CTAs once 32-column ones would need more than one wave
-        const long chains = (long)p.n_seq * p.H;
-        const int sms = device_sm_count();
-        if (sms > 0 && chains * (128 / 32) > sms) return launch_state_t<128, float, 64>(p, st);
-        return launch_state_t<128, float, 32>(p, st);
-    }
-    return p.dtype == MDN_BF16 ? launch_state_t<64, __nv_bfloat16, 32>(p, st)
-                               : launch_state_t<64, float, 32>(p, st);
+cudaError_t launch_states_passthrough(const ChunkProblem &p, cudaStream_t st) {
+    const long n = (long)p.n_seq * p.H * p.D * p.D;
+    if (n == 0 || (!p.S_T && !p.M_T)) return cudaSuccess;
+    const int blocks = (int)((n + 255) / 256 < 152L * 8 ? (n + 255) / 256 : 152L * 8);
+    states_passthrough_kernel<<<blocks, 256, 0, st>>>(p.S0, p.M0, p.S_T, p.M_T, n);
+    return cudaGetLastError();
 }
 
 }  // namespace mdn

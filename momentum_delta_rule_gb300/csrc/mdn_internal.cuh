@@ -158,7 +158,7 @@ cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_split_inputs(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
-cudaError_t launch_chunk_state_simt(const ChunkProblem &p, cudaStream_t st);
+cudaError_t launch_states_passthrough(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t st);
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t st);

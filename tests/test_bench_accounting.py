@@ -47,3 +47,15 @@ def test_roofline_binding_side():
     assert r["bound"] == "hbm"
     assert r["frac"] == pytest.approx(by / 1e-4 / 1e9 / 6785.2)
     assert r["other_roof_frac"] == pytest.approx(fl / 1e-4 / 1e12 / 1904.9)
+
+
+def test_fp32_state_pass_peak_is_a_third_of_bf16():
+    w = W.Workload("acc_fp32", B=1, T=128, H=2, D=128, dtype="fp32", state="zero", seed=0)
+    x = W.make_prefill(w)
+    peaks = {"hbm_gbs": 6785.2, "bf16_tflops": 1904.9}
+    r = bench.roofline_of(x, "state", True, 1e-9, peaks, "measured")   # FLOP-bound at d = 128
+    assert r["bound"] == "tensor" and r["peak"] == pytest.approx(1904.9 / 3)
+    p = bench.roofline_of(x, "prep", True, 1e-9, peaks, "measured")
+    assert p["bound"] == "alu"                      # the fp32 prep runs on the CUDA cores
+    # fp32 intermediates: the split prepared blocks and the q, k, v parts
+    assert bench.intermediate_bytes(x) == 34816 * 2 * 2 + 2 * 3 * 2 * 128 * 2 * 128
