@@ -50,7 +50,7 @@ def test_roofline_binding_side():
 
 
 def test_fp32_state_pass_peak_is_a_third_of_bf16():
-    w = W.Workload("acc_fp32", B=1, T=128, H=2, D=128, dtype="fp32", state="zero", seed=0)
+    w = W.Workload("acc_fp32", B=1, T=2048, H=2, D=128, dtype="fp32", state="none", seed=0)
     x = W.make_prefill(w)
     peaks = {"hbm_gbs": 6785.2, "bf16_tflops": 1904.9}
     r = bench.roofline_of(x, "state", True, 1e-9, peaks, "measured")   # FLOP-bound at d = 128
@@ -58,4 +58,4 @@ def test_fp32_state_pass_peak_is_a_third_of_bf16():
     p = bench.roofline_of(x, "prep", True, 1e-9, peaks, "measured")
     assert p["bound"] == "alu"                      # the fp32 prep runs on the CUDA cores
     # fp32 intermediates: the split prepared blocks and the q, k, v parts
-    assert bench.intermediate_bytes(x) == 34816 * 2 * 2 + 2 * 3 * 2 * 128 * 2 * 128
+    assert bench.intermediate_bytes(x) == 34816 * 32 * 2 + 2 * 3 * 2 * 2048 * 2 * 128
