@@ -62,7 +62,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["mdn", "reference"], default="mdn")
     p.add_argument("--workload", default=W.VARLEN_PACKED.name,
-                   choices=[w.name for w in W.ALL if not w.decode_steps])
+                   choices=[n for n, w in W.BY_NAME.items() if not w.decode_steps])
     p.add_argument("--decode-steps", type=int, default=W.DECODE.decode_steps)
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -864,9 +864,7 @@ def main():
     if not args.no_other_workloads:
         others = {}
         n = max(3, min(args.steps, 5))
-        extra = [W.Workload("prefill_400m_fp32_B8_H8_T2048_d128", B=8, T=2048, H=8, D=128,
-                            dtype="fp32", state="zero", seed=1)]
-        for wo in W.ALL + extra:
+        for wo in W.ALL + [W.PREFILL_400M_FP32]:
             if wo.decode_steps or wo.name == w.name:
                 continue
             xo = W.make_prefill(wo)

@@ -54,7 +54,11 @@ DECODE = Workload("decode_N256_H16_d128_1000steps", B=256, T=1, H=16, D=128,
                   dtype="bf16", state="randn", decode_steps=1000, seed=4)
 
 ALL = [TINY_FP32, PREFILL_400M, PREFILL_1P3B_LONG, VARLEN_PACKED, DECODE]
-BY_NAME = {w.name: w for w in ALL}
+# fp32 inputs at the 400M-model shapes: a timing and parity case of the
+# split-operand tensor-core path, not one of the five workloads above
+PREFILL_400M_FP32 = Workload("prefill_400m_fp32_B8_H8_T2048_d128", B=8, T=2048, H=8, D=128,
+                             dtype="fp32", state="zero", seed=1)
+BY_NAME = {w.name: w for w in ALL + [PREFILL_400M_FP32]}
 
 TORCH_DTYPE = {"fp32": torch.float32, "bf16": torch.bfloat16}
 
