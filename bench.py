@@ -759,10 +759,12 @@ def measure_prefill(mdn, w, x, dev, args, steps, warmup, world, flush, peaks, pe
     out["path"] = "tensor_core" if tensor else "cuda_core"
     names = ["prep", "state"]
     stage = max(range(2), key=lambda i: r["stage_ms"][i])
-    kind = "tc" if tensor else "simt"
     stages = {}
     for i, nm in enumerate(names):
-        key = "chunk_%s_%s" % (nm, kind)
+        # the state pass is tcgen05 for every input; the prep is tcgen05 for
+        # bf16 inputs and the fp32 CUDA-core kernel for fp32 inputs
+        tc = tensor and (nm == "state" or x["dtype"] == "bf16")
+        key = "chunk_%s_%s" % (nm, "tc" if tc else "simt")
         rf = roofline_of(x, nm, tensor, r["stage_ms"][i], peaks, peak_src)
         rf["kernel"] = key
         rf["traffic"] = traffic_record(key, w.name, os.path.join(
