@@ -43,6 +43,7 @@
 #include <type_traits>
 
 #include "mdn_internal.cuh"
+#include "mdn_sm100.cuh"
 
 namespace mdn {
 namespace {
@@ -68,6 +69,72 @@ struct PrepBwdSmem {
     static constexpr int kFloats = 2 * C * LD + 4 * C * LP + 4 * C + BL::kRows * C;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// The tensor-core chain's operand block of one (slot, head): T^T and (A T)^T
+// (A = Y . Gamma, formed here into the scratch `AT`, which may overlay the
+// dead K tile) in the token slots of the swizzled tc_row order, zero query
+// slots, and the per-token coefficients of the chain.  Every thread of the
+// CTA takes part (it synchronises the block).
+__device__ void write_chain_block(const BwdProblem &p, int gc, int h, int n, const float *Tm,
+                                  const float *X, const float *Y, const float *G, float *AT,
+                                  const float *vec, const float *ga, const float *ge) {
+    using CL = BwdChainLayout;
+    const int tid = threadIdx.x;
+    (void)X;
+    // AT[i][t] = sum_j A[i][j] T[j][t], A[i][j] = Y[i][j] Gamma[i][j]
+    {
+        const int i = tid >> 2, tq = tid & 3;
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        for (int j = 0; j <= i; ++j) {
+            const float a = Y[i * LP + j] * G[i * LP + j];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] = fmaf(a, Tm[j * LP + tq + 4 * e], acc[e]);
+        }
+        __syncthreads();                       // AT may overlay K: every reader is done
+#pragma unroll
+        for (int e = 0; e < 16; ++e) AT[i * LP + tq + 4 * e] = acc[e];
+    }
+    __syncthreads();
+    unsigned char *blk = p.tcblk + ((size_t)gc * p.loc.H + h) * CL::kBytes;
+    // row r of the operand: the token slot of token t holds column t of the
+    // matrix (its transpose's row t); 16-byte chunk c holds entries 8c..8c+7
+    for (int idx = tid; idx < 2 * 128 * 8; idx += blockDim.x) {
+        const int which = idx >> 10, r = (idx >> 3) & 127, c = idx & 7;
+        const int g = r >> 5, w = r & 31;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (w < 16) {
+            const int t = 16 * g + w;
+            const float *M = which ? AT : Tm;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = M[(8 * c + e) * LP + t];
+            v = make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
+                           pack_bf2(x[6], x[7]));
+        }
+        *reinterpret_cast<uint4 *>(blk + (which ? CL::kOffATt : CL::kOffTt) +
+                                   sm100::sw128_offset((uint32_t)r, (uint32_t)c)) = v;
+    }
+    float *cv = reinterpret_cast<float *>(blk + CL::kOffVec);
+    if (tid < C) {
+        const int t = tid;
+        const bool in = t < n;
+        cv[CL::vCS * C + t] = in ? vec[BL::vGS * C + t] * ge[t] : 0.f;
+        cv[CL::vCM * C + t] = in ? -vec[BL::vMuTail * C + t] * ge[t] : 0.f;
+        cv[CL::vBS * C + t] = in ? -vec[BL::vAbarM * C + t] * ga[t] : 0.f;
+        cv[CL::vBM * C + t] = in ? vec[BL::vBM * C + t] * ga[t] : 0.f;
+        cv[CL::vQS * C + t] = in ? vec[BL::vAbar * C + t] : 0.f;
+        cv[CL::vQM * C + t] = in ? -vec[BL::vB * C + t] : 0.f;
+        cv[CL::vScal * C + t] = t < 4 ? vec[BL::vScal * C + t] : 0.f;
+        cv[7 * C + t] = 0.f;
+    }
+}
 
 template <int D, typename Tin>
 __global__ void __launch_bounds__(256)
@@ -202,6 +269,7 @@ bwd_prep_kernel(const BwdProblem p) {
     }
     for (int idx = tid; idx < BL::kRows * C; idx += blockDim.x)
         blk[BL::kMats * BL::kMat + idx] = idx < 7 * C ? vec[idx] : 0.f;
+    if (p.tcblk) write_chain_block(p, gc, h, n, Tm, X, Y, G, Kf, vec, ga, ge);
 }
 
 // ------------------------------------------------------------------ chain
@@ -768,7 +836,11 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         kp<<<dim3(p.loc.max_chunks, H), 256, PrepBwdSmem<D>::kBytes, st>>>(p);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    {
+    if (p.tcblk) {
+        // bf16 inputs: the reverse chain on the tensor cores
+        cudaError_t err = launch_bwd_chain_tc(p, st);
+        if (err != cudaSuccess) return err;
+    } else {
         auto kc = bwd_chain_kernel<D, Tin>;
         cudaError_t err = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)ChainSmem<D>::kBytes);

@@ -128,8 +128,21 @@ struct BwdProblem {
     unsigned char *prep;               // per (slot, head): chunk matrices and vectors
     float *adj;                        // per (slot, head): dS, dM at the chunk's end [2, dk, dv]
     float *dR;                         // per (slot, head): residual adjoints [64, dv]
+    unsigned char *tcblk;              // per (slot, head): the tensor-core chain's operands, or null
     int D;
     mdn_dtype dtype;
+};
+
+// Per-(slot, head) operand block of the tensor-core reverse chain (bf16
+// inputs): T^T and (A T)^T as bf16 in the 128-byte-swizzled K-major operand
+// layout, their 64 rows in the token slots of the tc_row order (the query
+// slots zero), then kRows rows of 64 fp32 per-token coefficients.
+struct BwdChainLayout {
+    static constexpr size_t kOffTt = 0;
+    static constexpr size_t kOffATt = 16384;
+    static constexpr size_t kOffVec = 32768;
+    enum { vCS = 0, vCM, vBS, vBM, vQS, vQM, vScal, kRows = 8 };
+    static constexpr size_t kBytes = 32768 + sizeof(float) * kChunk * kRows;
 };
 
 // Per-(slot, head) block of the gradient pass, fp32: five 64 x 64 matrices
@@ -162,6 +175,7 @@ cudaError_t launch_states_passthrough(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t st);
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t st);
+cudaError_t launch_bwd_chain_tc(const BwdProblem &p, cudaStream_t st);
 
 // Multiprocessor count of the current device, cached per device (0 when it
 // cannot be read).
