@@ -447,12 +447,127 @@ bwd_chain_kernel(const BwdProblem p) {
 // Row sums the slab phase accumulates per token row i (indices into rowacc).
 enum { rAbar = 0, rB, rAbarM, rBM, rGLast, rMuTail, kRowAcc = 8 };
 
+// The gates' gradients through the chunk coefficients, from dG (the adjoint
+// of Gamma with the row-shifted copy's folded in, rows < n, C x LP), the
+// per-row sums `rowacc` (kRowAcc rows) and the adjoints of the chunk totals
+// dcs = (d abar_n, d b_n, d mubar_n).  `scr` holds kGateScratch floats: F
+// [C][C + 2], I, G', the product tables A(r, i), Mu(r, i) ((C + 1) x C each)
+// and three vectors.  Every thread of a CTA of at least 193 threads takes
+// part; writes dalpha, dmu, deta and dbeta of the chunk's tokens.
+constexpr int kGateScratch = C * (LP + 1) + 2 * C * LP + 2 * (C + 1) * C + 3 * C;
+
+__device__ void gate_gradients(const BwdProblem &p, int t0, int n, int h, const float *dGx,
+                               float *scr, const float *ga, const float *gm, const float *gb,
+                               const float *rowacc, const float *dcs) {
+    const int tid = threadIdx.x, H = p.loc.H;
+    float *Fm = scr;
+    float *Im = Fm + C * (LP + 1), *Gg = Im + C * LP;
+    float *At = Gg + C * LP, *Mt = At + (C + 1) * C;
+    float *dab = Mt + (C + 1) * C, *dbv = dab + C, *Tl = dbv + C;
+    if (tid <= C) {
+        // A(r, i) = prod_{u=r+1}^{i} alpha_u, Mu(r, i) = prod_{u=r+1}^{i} mu_u,
+        // r = tid - 1 (row r + 1 of the tables), 1 on the diagonal i == r
+        const int r = tid - 1;
+        float pa = 1.f, pmu = 1.f;
+        for (int ii = 0; ii < C; ++ii) {
+            float va = 0.f, vm = 0.f;
+            if (ii == r) {
+                va = vm = 1.f;
+            } else if (ii > r && ii < n) {
+                pa *= ga[ii];
+                pmu *= gm[ii];
+                va = pa;
+                vm = pmu;
+            }
+            At[tid * C + ii] = va;
+            Mt[tid * C + ii] = vm;
+        }
+    } else if (tid >= 128 && tid < 128 + C) {
+        // the folded vector adjoints: d abar_i plus the shifted copy's (at
+        // i + 1) and the chunk total's (at n - 1); d b_i likewise
+        const int r = tid - 128;
+        float va = 0.f, vb = 0.f;
+        if (r < n) {
+            va = rowacc[rAbar * C + r];
+            vb = rowacc[rB * C + r];
+            if (r + 1 < n) {
+                va += rowacc[rAbarM * C + r + 1];
+                vb += rowacc[rBM * C + r + 1];
+            }
+            if (r == n - 1) {
+                va += dcs[0];
+                vb += dcs[1];
+            }
+        }
+        dab[r] = va;
+        dbv[r] = vb;
+    } else if (tid == 192) {
+        // Tl_u = sum_{j<u} dmu_tail_j Mu(j, u-1), started from d mubar_n
+        float tl = dcs[2];
+        for (int u = 0; u < C; ++u) {
+            Tl[u] = tl;
+            if (u < n) tl = gm[u] * tl + rowacc[rMuTail * C + u];
+        }
+    }
+    __syncthreads();
+    if (tid < C) {
+        const int r = tid;                       // row r of the triangle
+        // F[r, m + 1] = mu_m F[r, m] + dG[r, m], F[r, 0] = db_r
+        float f = dbv[r];
+        Fm[r * (LP + 1) + 0] = f;
+        for (int m = 0; m < C; ++m) {
+            if (m <= r && r < n) f = gm[m] * f + dGx[r * LP + m];
+            else f = 0.f;
+            Fm[r * (LP + 1) + m + 1] = f;
+        }
+    }
+    __syncthreads();
+    if (tid < C) {
+        const int r = tid;
+        // I[r, u] = sum_{v<u} beta_v A(v, u-1) F[r, v+1] (alpha's inner sum),
+        // u = 0..r, and G'[r, u] = sum_{v=u}^{r} beta_v A(v, r) Mu(u, v) (mu's)
+        float inner = 0.f;
+        for (int u = 0; u < C; ++u) {
+            const bool in = u <= r && r < n;
+            Im[r * LP + u] = in ? inner : 0.f;
+            if (in) inner = ga[u] * inner + gb[u] * Fm[r * (LP + 1) + u + 1];
+        }
+        float g = r < n ? gb[r] : 0.f;
+        for (int u = C - 1; u >= 0; --u) {
+            if (u <= r && r < n) {
+                Gg[r * LP + u] = g;
+                if (u > 0) g = gb[u - 1] * At[u * C + r] + gm[u] * g;
+            } else {
+                Gg[r * LP + u] = 0.f;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < n) {
+        const int u = tid;
+        float db = 0.f, dal = 0.f, dmu = 0.f;
+        const float a_prev = u > 0 ? At[u - 1] : 1.f;       // A(-1, u-1)
+        for (int r = u; r < n; ++r) {
+            const float Aur = At[(u + 1) * C + r];            // A(u, r)
+            db = fmaf(Aur, Fm[r * (LP + 1) + u + 1], db);
+            dal = fmaf(Aur, Im[r * LP + u] + dab[r] * a_prev, dal);
+            dmu = fmaf(Fm[r * (LP + 1) + u], Gg[r * LP + u], dmu);
+        }
+        dmu = fmaf(Tl[u], Mt[(u + 1) * C + n - 1], dmu);     // Mu(u, n-1)
+        const size_t gi = (size_t)(t0 + u) * H + h;
+        p.dalpha[gi] = rowacc[6 * C + u] + dal;
+        p.dmu[gi] = dmu;
+        p.deta[gi] = rowacc[7 * C + u];
+        if (p.dbeta) p.dbeta[gi] = db;
+    }
+}
+
 template <int D>
 struct ChunkSmem {
     static constexpr int LD = D + 1;
     static constexpr int kSlab = 4 * D * LS + 4 * C * LS;
     static constexpr int kPh4 = 5 * C * LP;
-    static constexpr int kPh5 = C * LP + C * (LP + 1) + 2 * C * LP + 2 * (C + 1) * C + 4 * C;
+    static constexpr int kPh5 = C * LP + kGateScratch;
     static constexpr int kUnion = kSlab > kPh4 ? (kSlab > kPh5 ? kSlab : kPh5) : (kPh4 > kPh5 ? kPh4 : kPh5);
     static constexpr int kFloats = 2 * C * LD + C * LP + BL::kRows * C + 4 * C + kRowAcc * C +
                                    16 * 4 + kUnion;
@@ -719,110 +834,56 @@ bwd_chunk_kernel(const BwdProblem p) {
         for (int mm = 0; mm < 8; ++mm) G[i * LP + q8 + 8 * mm] = vals[mm];
     }
     __syncthreads();
-    // ---- phase 5: the gates through the coefficients.  Layout over the
-    // union region: dG (over G), F [C][C + 2], I, G', then the product tables
-    // A(r, i), Mu(r, i) ((C + 1) x C each) and three vectors.
-    const float *dGx = G;
-    float *Fm = U + C * LP;
-    float *Im = Fm + C * (LP + 1), *Gg = Im + C * LP;
-    float *At = Gg + C * LP, *Mt = At + (C + 1) * C;
-    float *dab = Mt + (C + 1) * C, *dbv = dab + C, *Tl = dbv + C;
-    if (tid <= C) {
-        // A(r, i) = prod_{u=r+1}^{i} alpha_u, Mu(r, i) = prod_{u=r+1}^{i} mu_u,
-        // r = tid - 1 (row r + 1 of the tables), 1 on the diagonal i == r
-        const int r = tid - 1;
-        float pa = 1.f, pmu = 1.f;
-        for (int ii = 0; ii < C; ++ii) {
-            float va = 0.f, vm = 0.f;
-            if (ii == r) {
-                va = vm = 1.f;
-            } else if (ii > r && ii < n) {
-                pa *= ga[ii];
-                pmu *= gm[ii];
-                va = pa;
-                vm = pmu;
-            }
-            At[tid * C + ii] = va;
-            Mt[tid * C + ii] = vm;
-        }
-    } else if (tid >= 128 && tid < 128 + C) {
-        // the folded vector adjoints: d abar_i plus the shifted copy's (at
-        // i + 1) and the chunk total's (at n - 1); d b_i likewise
-        const int r = tid - 128;
-        float va = 0.f, vb = 0.f;
-        if (r < n) {
-            va = rowacc[rAbar * C + r];
-            vb = rowacc[rB * C + r];
-            if (r + 1 < n) {
-                va += rowacc[rAbarM * C + r + 1];
-                vb += rowacc[rBM * C + r + 1];
-            }
-            if (r == n - 1) {
-                va += dcs[0];
-                vb += dcs[1];
-            }
-        }
-        dab[r] = va;
-        dbv[r] = vb;
-    } else if (tid == 192) {
-        // Tl_u = sum_{j<u} dmu_tail_j Mu(j, u-1), started from d mubar_n
-        float tl = dcs[2];
-        for (int u = 0; u < C; ++u) {
-            Tl[u] = tl;
-            if (u < n) tl = gm[u] * tl + rowacc[rMuTail * C + u];
-        }
-    }
-    __syncthreads();
+    // ---- phase 5: the gates through the coefficients
+    gate_gradients(p, t0, n, h, G, U + C * LP, ga, gm, gb, rowacc, dcs);
+}
+
+// ------------------------------------------------------------------ gates
+
+// The gate stage after the tensor-core chunk kernel (bf16 inputs), which
+// leaves per (slot, head), over matrices of the gradient block it no longer
+// needs: dA . Y in the Y slot, dL . X in the X slot (rows < n; the lower
+// triangle), and in the A slot the kRowAcc row sums followed by the three
+// state inner products <S0, dS>, <M0, dS>, <M0, dM>.
+constexpr size_t kGateSmem = sizeof(float) * (C * LP + kGateScratch + 3 * C + kRowAcc * C);
+
+__global__ void __launch_bounds__(256)
+bwd_gates_kernel(const BwdProblem p) {
+    extern __shared__ float sm[];
+    float *dG = sm, *scr = dG + C * LP;
+    float *ga = scr + kGateScratch, *gm = ga + C, *gb = gm + C, *rowacc = gb + C;
+    const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
+    ChunkLoc loc;
+    if (!locate_chunk(p.loc, gc, loc)) return;
+    const int n = loc.n, t0 = loc.t0;
+    const float *blk = bwd_block(p, gc, h);
+    const float *ra = blk + BL::kA * BL::kMat;
+    const float *W1 = blk + BL::kY * BL::kMat, *W2 = blk + BL::kX * BL::kMat;
     if (tid < C) {
-        const int r = tid;                       // row r of the triangle
-        // F[r, m + 1] = mu_m F[r, m] + dG[r, m], F[r, 0] = db_r
-        float f = dbv[r];
-        Fm[r * (LP + 1) + 0] = f;
-        for (int m = 0; m < C; ++m) {
-            if (m <= r && r < n) f = gm[m] * f + dGx[r * LP + m];
-            else f = 0.f;
-            Fm[r * (LP + 1) + m + 1] = f;
+        float a = 0.f, m = 0.f, b = 0.f;
+        if (tid < n) {
+            const size_t gi = (size_t)(t0 + tid) * H + h;
+            a = p.alpha[gi];
+            m = p.mu[gi];
+            b = p.beta ? p.beta[gi] : 1.f;
         }
+        ga[tid] = a; gm[tid] = m; gb[tid] = b;
     }
+    for (int idx = tid; idx < kRowAcc * C; idx += blockDim.x) rowacc[idx] = ra[idx];
+    // dG = dA . Y, plus the carry row on the last row, plus dL . X one row up
+    for (int idx = tid; idx < C * C; idx += blockDim.x) {
+        const int r = idx >> 6, m = idx & 63;
+        float v = 0.f;
+        if (r < n && m <= r) {
+            v = W1[idx];
+            if (r + 1 < n) v += W2[idx + C];
+            if (r == n - 1) v += ra[rGLast * C + m];
+        }
+        dG[r * LP + m] = v;
+    }
+    const float dcs[3] = {ra[kRowAcc * C + 0], -ra[kRowAcc * C + 1], ra[kRowAcc * C + 2]};
     __syncthreads();
-    if (tid < C) {
-        const int r = tid;
-        // I[r, u] = sum_{v<u} beta_v A(v, u-1) F[r, v+1] (alpha's inner sum),
-        // u = 0..r, and G'[r, u] = sum_{v=u}^{r} beta_v A(v, r) Mu(u, v) (mu's)
-        float inner = 0.f;
-        for (int u = 0; u < C; ++u) {
-            const bool in = u <= r && r < n;
-            Im[r * LP + u] = in ? inner : 0.f;
-            if (in) inner = ga[u] * inner + gb[u] * Fm[r * (LP + 1) + u + 1];
-        }
-        float g = r < n ? gb[r] : 0.f;
-        for (int u = C - 1; u >= 0; --u) {
-            if (u <= r && r < n) {
-                Gg[r * LP + u] = g;
-                if (u > 0) g = gb[u - 1] * At[u * C + r] + gm[u] * g;
-            } else {
-                Gg[r * LP + u] = 0.f;
-            }
-        }
-    }
-    __syncthreads();
-    if (tid < n) {
-        const int u = tid;
-        float db = 0.f, dal = 0.f, dmu = 0.f;
-        const float a_prev = u > 0 ? At[u - 1] : 1.f;       // A(-1, u-1)
-        for (int r = u; r < n; ++r) {
-            const float Aur = At[(u + 1) * C + r];            // A(u, r)
-            db = fmaf(Aur, Fm[r * (LP + 1) + u + 1], db);
-            dal = fmaf(Aur, Im[r * LP + u] + dab[r] * a_prev, dal);
-            dmu = fmaf(Fm[r * (LP + 1) + u], Gg[r * LP + u], dmu);
-        }
-        dmu = fmaf(Tl[u], Mt[(u + 1) * C + n - 1], dmu);     // Mu(u, n-1)
-        const size_t gi = (size_t)(t0 + u) * H + h;
-        p.dalpha[gi] = rowacc[6 * C + u] + dal;
-        p.dmu[gi] = dmu;
-        p.deta[gi] = rowacc[7 * C + u];
-        if (p.dbeta) p.dbeta[gi] = db;
-    }
+    gate_gradients(p, t0, n, h, dG, scr, ga, gm, gb, rowacc, dcs);
 }
 
 template <int D, typename Tin>
@@ -837,9 +898,17 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if (p.tcblk) {
-        // bf16 inputs: the reverse chain on the tensor cores
+        // bf16 inputs: the reverse chain and the chunk products on the
+        // tensor cores, then the gates' partials on the CUDA cores
         cudaError_t err = launch_bwd_chain_tc(p, st);
+        if (err == cudaSuccess) err = launch_bwd_chunk_tc(p, st);
         if (err != cudaSuccess) return err;
+        auto kg = bwd_gates_kernel;
+        if ((err = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kGateSmem)) != cudaSuccess)
+            return err;
+        kg<<<dim3(p.loc.max_chunks, H), 256, kGateSmem, st>>>(p);
+        return cudaGetLastError();
     } else {
         auto kc = bwd_chain_kernel<D, Tin>;
         cudaError_t err = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -32,6 +32,36 @@
 #include "mdn_sm100.cuh"
 
 namespace mdn {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_b() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// A [T_total, H, D] bf16 token tensor as a 3-D TMA map (D innermost, then
+// the head, then the token), boxes of 64 columns x 1 head x box_t tokens,
+// 128-byte swizzle.
+bool make_token_map_bf16(CUtensorMap *map, const void *base, int T_total, int H, int D,
+                         int box_t) {
+    auto fn = encode_fn_b();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_t};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 using namespace sm100;
@@ -465,31 +495,6 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
     if (threadIdx.x == 0 && *abort && L.status) atomicExch(L.status, (int)MDN_ERR_DEVICE_TIMEOUT);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_b() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-bool make_map_b(CUtensorMap *map, const void *base, int T_total, int H, int D, int box_t) {
-    auto fn = encode_fn_b();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T_total};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_t};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int NS>
 cudaError_t launch_chain_tc_t(const BwdProblem &p, cudaStream_t st, const CUtensorMap &mk,
                               const CUtensorMap &mq, const CUtensorMap &mo) {
@@ -525,8 +530,9 @@ cudaError_t launch_bwd_chain_tc(const BwdProblem &p, cudaStream_t st) {
     if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16 || !p.tcblk) return cudaErrorInvalidValue;
     const int Tt = p.loc.T_total > 0 ? p.loc.T_total : 1;
     CUtensorMap mk, mq, mo;
-    if (!make_map_b(&mk, p.k, Tt, p.loc.H, p.D, 16) || !make_map_b(&mq, p.q, Tt, p.loc.H, p.D, 16) ||
-        !make_map_b(&mo, p.dout, Tt, p.loc.H, p.D, 64))
+    if (!make_token_map_bf16(&mk, p.k, Tt, p.loc.H, p.D, 16) ||
+        !make_token_map_bf16(&mq, p.q, Tt, p.loc.H, p.D, 16) ||
+        !make_token_map_bf16(&mo, p.dout, Tt, p.loc.H, p.D, 64))
         return cudaErrorInvalidValue;
     return p.D == 128 ? launch_chain_tc_d<128>(p, st, mk, mq, mo)
                       : launch_chain_tc_d<64>(p, st, mk, mq, mo);

@@ -176,6 +176,7 @@ cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t st);
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t st);
 cudaError_t launch_bwd_chain_tc(const BwdProblem &p, cudaStream_t st);
+cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st);
 
 // Multiprocessor count of the current device, cached per device (0 when it
 // cannot be read).

@@ -291,4 +291,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
 }
 
 }  // namespace sm100
+
+// Host: a [T_total, H, D] bf16 token tensor as a 3-D TMA map (boxes of 64
+// columns x 1 head x box_t tokens, 128-byte swizzle); false on failure.
+bool make_token_map_bf16(CUtensorMap *map, const void *base, int T_total, int H, int D,
+                         int box_t);
+
 }  // namespace mdn
