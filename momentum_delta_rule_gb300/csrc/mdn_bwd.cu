@@ -34,12 +34,16 @@
 //   recurrences along each row (O(C^2) per chunk, no division by a gate, so
 //   mu = 0 is exact).
 //
-// Three kernels after the packed-offset kernel:
+// fp32 inputs, three kernels after the packed-offset kernel:
 //   bwd_prep   (chunk, head)            coefficients, Grams, T, A -> workspace
 //   bwd_chain  (sequence, head, 32 cols) the reverse chain; dV; every chunk's
 //                                       end adjoints -> workspace
 //   bwd_chunk  (chunk, head)            the state products in 32-column slabs,
 //                                       then dQ, dK and the gate gradients
+// bf16 inputs: the forward's tensor-core prep (T, A_O T), bwd_vec (Gamma and
+// the vectors), the reverse chain and the chunk products on the tensor cores
+// (mdn_bwd_tc.cu, mdn_bwd_chunk_tc.cu), then bwd_gates (the gate gradients
+// through the coefficients, as at the end of bwd_chunk).
 #include <type_traits>
 
 #include "mdn_internal.cuh"
@@ -69,72 +73,6 @@ struct PrepBwdSmem {
     static constexpr int kFloats = 2 * C * LD + 4 * C * LP + 4 * C + BL::kRows * C;
     static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
-
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// The tensor-core chain's operand block of one (slot, head): T^T and (A T)^T
-// (A = Y . Gamma, formed here into the scratch `AT`, which may overlay the
-// dead K tile) in the token slots of the swizzled tc_row order, zero query
-// slots, and the per-token coefficients of the chain.  Every thread of the
-// CTA takes part (it synchronises the block).
-__device__ void write_chain_block(const BwdProblem &p, int gc, int h, int n, const float *Tm,
-                                  const float *X, const float *Y, const float *G, float *AT,
-                                  const float *vec, const float *ga, const float *ge) {
-    using CL = BwdChainLayout;
-    const int tid = threadIdx.x;
-    (void)X;
-    // AT[i][t] = sum_j A[i][j] T[j][t], A[i][j] = Y[i][j] Gamma[i][j]
-    {
-        const int i = tid >> 2, tq = tid & 3;
-        float acc[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-        for (int j = 0; j <= i; ++j) {
-            const float a = Y[i * LP + j] * G[i * LP + j];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) acc[e] = fmaf(a, Tm[j * LP + tq + 4 * e], acc[e]);
-        }
-        __syncthreads();                       // AT may overlay K: every reader is done
-#pragma unroll
-        for (int e = 0; e < 16; ++e) AT[i * LP + tq + 4 * e] = acc[e];
-    }
-    __syncthreads();
-    unsigned char *blk = p.tcblk + ((size_t)gc * p.loc.H + h) * CL::kBytes;
-    // row r of the operand: the token slot of token t holds column t of the
-    // matrix (its transpose's row t); 16-byte chunk c holds entries 8c..8c+7
-    for (int idx = tid; idx < 2 * 128 * 8; idx += blockDim.x) {
-        const int which = idx >> 10, r = (idx >> 3) & 127, c = idx & 7;
-        const int g = r >> 5, w = r & 31;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (w < 16) {
-            const int t = 16 * g + w;
-            const float *M = which ? AT : Tm;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = M[(8 * c + e) * LP + t];
-            v = make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
-                           pack_bf2(x[6], x[7]));
-        }
-        *reinterpret_cast<uint4 *>(blk + (which ? CL::kOffATt : CL::kOffTt) +
-                                   sm100::sw128_offset((uint32_t)r, (uint32_t)c)) = v;
-    }
-    float *cv = reinterpret_cast<float *>(blk + CL::kOffVec);
-    if (tid < C) {
-        const int t = tid;
-        const bool in = t < n;
-        cv[CL::vCS * C + t] = in ? vec[BL::vGS * C + t] * ge[t] : 0.f;
-        cv[CL::vCM * C + t] = in ? -vec[BL::vMuTail * C + t] * ge[t] : 0.f;
-        cv[CL::vBS * C + t] = in ? -vec[BL::vAbarM * C + t] * ga[t] : 0.f;
-        cv[CL::vBM * C + t] = in ? vec[BL::vBM * C + t] * ga[t] : 0.f;
-        cv[CL::vQS * C + t] = in ? vec[BL::vAbar * C + t] : 0.f;
-        cv[CL::vQM * C + t] = in ? -vec[BL::vB * C + t] : 0.f;
-        cv[CL::vScal * C + t] = t < 4 ? vec[BL::vScal * C + t] : 0.f;
-        cv[7 * C + t] = 0.f;
-    }
-}
 
 template <int D, typename Tin>
 __global__ void __launch_bounds__(256)
@@ -269,7 +207,90 @@ bwd_prep_kernel(const BwdProblem p) {
     }
     for (int idx = tid; idx < BL::kRows * C; idx += blockDim.x)
         blk[BL::kMats * BL::kMat + idx] = idx < 7 * C ? vec[idx] : 0.f;
-    if (p.tcblk) write_chain_block(p, gc, h, n, Tm, X, Y, G, Kf, vec, ga, ge);
+}
+
+// The coefficients of the tensor-core gradient (bf16 inputs), whose matrices
+// T and A_O T come from the forward's tensor-core prep: Gamma and the vector
+// rows into the gradient block, and the reverse chain's per-token
+// coefficients into the operand block, over the forward's carry vectors.
+__global__ void __launch_bounds__(128)
+bwd_vec_kernel(const BwdProblem p) {
+    using CL = BwdChainLayout;
+    __shared__ float ga[C], gm[C], ge[C], gb[C], vec[BL::kRows * C];
+    const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
+    ChunkLoc loc;
+    if (!locate_chunk(p.loc, gc, loc)) return;
+    const int n = loc.n;
+    if (tid < C) {
+        float a = 1.f, m = 0.f, e = 0.f, b = 0.f;
+        if (tid < n) {
+            const size_t gi = (size_t)(loc.t0 + tid) * H + h;
+            a = p.alpha[gi];
+            m = p.mu[gi];
+            e = p.eta[gi];
+            b = p.beta ? p.beta[gi] : 1.f;
+        }
+        ga[tid] = a; gm[tid] = m; ge[tid] = e; gb[tid] = b;
+    }
+    __syncthreads();
+    float *blk = bwd_block(p, gc, h);
+    if (tid < C) {
+        // column j of Gamma by its recurrence (as in the prep above), its
+        // last row gS and mu_tail_j
+        const int j = tid;
+        float *G = blk + BL::kG * BL::kMat;
+        float g = 0.f, mm = 1.f, gl = 0.f;
+        for (int i = 0; i < C; ++i) {
+            float out = 0.f;
+            if (i >= j && i < n) {
+                mm = (i == j) ? 1.f : mm * gm[i];
+                g = (i == j) ? gb[i] : ga[i] * g + gb[i] * mm;
+                out = g;
+                if (i == n - 1) gl = g;
+            }
+            G[i * C + j] = out;
+        }
+        float mt = 1.f;
+        for (int u = j + 1; u < n; ++u) mt *= gm[u];
+        vec[BL::vGS * C + j] = j < n ? gl : 0.f;
+        vec[BL::vMuTail * C + j] = j < n ? mt : 0.f;
+    } else if (tid == C) {
+        float ab = 1.f, bb = 0.f, mub = 1.f;
+        for (int i = 0; i < C; ++i) {
+            const float abm = ab, bm = bb;
+            if (i < n) {
+                ab *= ga[i];
+                mub *= gm[i];
+                bb = ga[i] * bb + gb[i] * mub;
+            }
+            const bool in = i < n;
+            vec[BL::vAbarM * C + i] = in ? abm : 0.f;
+            vec[BL::vBM * C + i] = in ? bm : 0.f;
+            vec[BL::vAbar * C + i] = in ? ab : 0.f;
+            vec[BL::vB * C + i] = in ? bb : 0.f;
+        }
+        vec[BL::vScal * C + 0] = ab;
+        vec[BL::vScal * C + 1] = bb;
+        vec[BL::vScal * C + 2] = mub;
+        vec[BL::vScal * C + 3] = (float)n;
+        for (int i = 4; i < C; ++i) vec[BL::vScal * C + i] = 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < BL::kRows * C; idx += blockDim.x)
+        blk[BL::kMats * BL::kMat + idx] = idx < 7 * C ? vec[idx] : 0.f;
+    if (tid < C) {
+        const int t = tid;
+        const bool in = t < n;
+        float *cv = reinterpret_cast<float *>(p.tcblk + ((size_t)gc * H + h) * CL::kBytes + CL::kOffVec);
+        cv[CL::vCS * C + t] = in ? vec[BL::vGS * C + t] * ge[t] : 0.f;
+        cv[CL::vCM * C + t] = in ? -vec[BL::vMuTail * C + t] * ge[t] : 0.f;
+        cv[CL::vBS * C + t] = in ? -vec[BL::vAbarM * C + t] * ga[t] : 0.f;
+        cv[CL::vBM * C + t] = in ? vec[BL::vBM * C + t] * ga[t] : 0.f;
+        cv[CL::vQS * C + t] = in ? vec[BL::vAbar * C + t] : 0.f;
+        cv[CL::vQM * C + t] = in ? -vec[BL::vB * C + t] : 0.f;
+        cv[CL::vScal * C + t] = t < 4 ? vec[BL::vScal * C + t] : 0.f;
+        cv[7 * C + t] = 0.f;
+    }
 }
 
 // ------------------------------------------------------------------ chain
@@ -889,6 +910,30 @@ bwd_gates_kernel(const BwdProblem p) {
 template <int D, typename Tin>
 cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
     const int H = p.loc.H;
+    if (p.tcblk) {
+        // bf16 inputs: the forward's tensor-core prep writes T and A_O T into
+        // the operand blocks, the coefficient kernel Gamma and the vectors;
+        // the reverse chain and the chunk products run on the tensor cores,
+        // the gates' partials on the CUDA cores
+        ChunkProblem fp = p.loc;
+        fp.q = p.q;
+        fp.k = p.k;
+        fp.alpha = p.alpha; fp.mu = p.mu; fp.eta = p.eta; fp.beta = p.beta;
+        fp.prep = p.tcblk;
+        fp.prep_stride = BwdChainLayout::kBytes;
+        cudaError_t err = launch_chunk_prep_tc(fp, st);
+        if (err != cudaSuccess) return err;
+        bwd_vec_kernel<<<dim3(p.loc.max_chunks, H), 128, 0, st>>>(p);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if ((err = launch_bwd_chain_tc(p, st)) != cudaSuccess) return err;
+        if ((err = launch_bwd_chunk_tc(p, st)) != cudaSuccess) return err;
+        auto kg = bwd_gates_kernel;
+        if ((err = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kGateSmem)) != cudaSuccess)
+            return err;
+        kg<<<dim3(p.loc.max_chunks, H), 256, kGateSmem, st>>>(p);
+        return cudaGetLastError();
+    }
     if (p.loc.max_chunks > 0) {
         auto kp = bwd_prep_kernel<D, Tin>;
         cudaError_t err = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -897,19 +942,7 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         kp<<<dim3(p.loc.max_chunks, H), 256, PrepBwdSmem<D>::kBytes, st>>>(p);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    if (p.tcblk) {
-        // bf16 inputs: the reverse chain and the chunk products on the
-        // tensor cores, then the gates' partials on the CUDA cores
-        cudaError_t err = launch_bwd_chain_tc(p, st);
-        if (err == cudaSuccess) err = launch_bwd_chunk_tc(p, st);
-        if (err != cudaSuccess) return err;
-        auto kg = bwd_gates_kernel;
-        if ((err = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kGateSmem)) != cudaSuccess)
-            return err;
-        kg<<<dim3(p.loc.max_chunks, H), 256, kGateSmem, st>>>(p);
-        return cudaGetLastError();
-    } else {
+    {
         auto kc = bwd_chain_kernel<D, Tin>;
         cudaError_t err = cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)ChainSmem<D>::kBytes);

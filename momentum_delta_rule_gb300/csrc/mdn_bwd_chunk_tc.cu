@@ -63,35 +63,43 @@ struct GradCfg {
     static constexpr uint32_t kOffDS = kOffM0 + kState;
     static constexpr uint32_t kOffDM = kOffDS + kState;
     static constexpr uint32_t kOffV = kOffDM + kState;     // V, then R in place
-    static constexpr uint32_t kOffT = kOffV + kTok;        // T, 64 x 64
-    // Vres over S0 (MMA1 and MMA3 are done when it is written); the
-    // operands of MMA6 and MMA7 over M0, dS, dM when those have the room
-    static constexpr uint32_t kOffVres = kOffS0;
-    static constexpr bool kOverlay = 3 * kState >= 2 * kHalf;
-    static constexpr uint32_t kOffA6 = kOverlay ? kOffM0 : kOffT + 8192;
+    // Once MMA1 and MMA3 are done: the forward prep's [T; A_O T] tile and
+    // Vres over S0, the key tile of the Gram product over M0 (then the
+    // operands of MMA6 and MMA7 over M0 once the Gram product is done),
+    // where the head size leaves those regions the room; else beside.
+    static constexpr bool kOverlay = kState >= 2 * kHalf;
+    static constexpr uint32_t kOffTile = kOverlay ? kOffS0 : kOffV + kTok;
+    static constexpr uint32_t kOffVres = kOverlay ? kOffS0 + kHalf : kOffS0;
+    static constexpr uint32_t kOffKt = kOffM0;
+    static constexpr uint32_t kOffA6 = kOverlay ? kOffM0 : kOffTile + kHalf;
     static constexpr uint32_t kOffA7 = kOffA6 + kHalf;
-    static constexpr uint32_t kOffCoef = kOverlay ? kOffT + 8192 : kOffA7 + kHalf;
+    static constexpr uint32_t kOffCoef = kOverlay ? kOffV + kTok : kOffA7 + kHalf;
     // coefficients (vector rows, alpha, eta), the two column halves' row sums,
     // per-warp inner products
     static constexpr int kCoefFloats = BL::kRows * C + 2 * C + 2 * kSums * C + 8 * 4;
     static constexpr uint32_t kOffBar = kOffCoef + ((kCoefFloats * 4 + 127) / 128) * 128;
     static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
-    static_assert(kOffVres + kTok <= kOffM0, "Vres overlay");
+    static_assert(kOffVres + kTok <= kOffM0 && kTok <= kState, "overlays");
+    static_assert(!kOverlay || kOffA7 + kHalf <= kOffDS, "overlays");
     static constexpr uint32_t kColS1 = 0, kColM1 = D, kColS3 = 2 * D, kColM3 = 3 * D;
-    static constexpr uint32_t kTmemCols = 4 * D;
+    static constexpr uint32_t kColG = 3 * D + 64 > 4 * D - 64 ? 4 * D : 3 * D + 64;  // Gram, 64 columns
+    static constexpr uint32_t kTmemCols = 512;
     static constexpr int kThreads = 320;
     static constexpr uint32_t kTxBytes = 2 * kStage + kTok;
+    static constexpr uint32_t kTx2Bytes = kHalf + kTok;
+    static_assert(kColG + 64 <= kTmemCols, "TMEM columns");
     static constexpr uint32_t kIdescKS = idesc_bf16(128, D, false, true);   // MMA1, MMA6
     static constexpr uint32_t kIdescKK = idesc_bf16(128, D, false, false);  // MMA3
-    static constexpr uint32_t kIdescT = idesc_bf16(64, D, false, true);     // MMA2
+    static constexpr uint32_t kIdescT = idesc_bf16(128, D, false, true);    // MMA2
+    static constexpr uint32_t kIdescG = idesc_bf16(128, 64, false, false);  // Gram
     static constexpr uint32_t kIdescV = idesc_bf16(64, D, false, false);    // MMA4
     static constexpr uint32_t kIdescA = idesc_bf16(128, 64, false, false);  // MMA5
     static constexpr uint32_t kIdesc7 = idesc_bf16(64, D, true, true);      // MMA7
 };
 
 struct GradBars {
-    uint64_t full, st, d13, r, d2, v, d45, y, d67, drain;
+    uint64_t full, full2, st, d13, r, d2, v, d45, y, d67, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -166,7 +174,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_o,
                     const __grid_constant__ CUtensorMap map_r,
-                    const __grid_constant__ CUtensorMap map_v) {
+                    const __grid_constant__ CUtensorMap map_v,
+                    const __grid_constant__ CUtensorMap map_kt) {
     using G = GradCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -182,6 +191,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->full, 1);
+        mbar_init(&bars->full2, 1);
         mbar_init(&bars->st, 8);
         mbar_init(&bars->d13, 1);
         mbar_init(&bars->r, 8);
@@ -200,6 +210,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         prefetch_tensormap(&map_o);
         prefetch_tensormap(&map_r);
         prefetch_tensormap(&map_v);
+        prefetch_tensormap(&map_kt);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, G::kTmemCols);
@@ -227,8 +238,20 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 }
                 tma_load_3d(smem + G::kOffV + hh * kTokHalf, &map_v, &bars->full, 64 * hh, h, t0);
             }
+            // once MMA1 and MMA3 have read the states: the operand tile of
+            // the forward prep and the 64 key rows of the Gram product
+            bool go = mbar_wait(&bars->d13, 0, abort);
+            if (go) {
+                mbar_arrive_expect_tx(&bars->full2, G::kTx2Bytes);
+                const unsigned char *tile = p.tcblk + ((size_t)gc * H + h) * BwdChainLayout::kBytes;
+                bulk_load(smem + G::kOffTile, tile + BwdChainLayout::kOffTile, kHalf, &bars->full2);
+#pragma unroll
+                for (int hh = 0; hh < G::kHalves; ++hh)
+                    tma_load_3d(smem + G::kOffKt + hh * kTokHalf, &map_kt, &bars->full2, 64 * hh, h, t0);
+            }
             int dummy = 0;
             mbar_wait(&bars->full, 0, &dummy);     // no copy in flight at exit
+            if (go) mbar_wait(&bars->full2, 0, &dummy);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -236,7 +259,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         const uint32_t kq = smem_u32(smem + G::kOffKQ), orr = smem_u32(smem + G::kOffOR);
         const uint32_t s0 = smem_u32(smem + G::kOffS0), m0 = smem_u32(smem + G::kOffM0);
         const uint32_t ds = smem_u32(smem + G::kOffDS), dm = smem_u32(smem + G::kOffDM);
-        const uint32_t vt = smem_u32(smem + G::kOffV), tt = smem_u32(smem + G::kOffT);
+        const uint32_t vt = smem_u32(smem + G::kOffV), tt = smem_u32(smem + G::kOffTile);
+        const uint32_t kt = smem_u32(smem + G::kOffKt);
         const uint32_t vr = smem_u32(smem + G::kOffVres);
         const uint32_t a6 = smem_u32(smem + G::kOffA6), a7 = smem_u32(smem + G::kOffA7);
         constexpr uint32_t kLboS = G::kHalves > 1 ? G::kStateHalf : 8192;
@@ -263,16 +287,22 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 mma_commit(&bars->d13);
             }
             __syncwarp();
-            ok = warp_wait(&bars->r, 0, abort);
+            ok = warp_wait(&bars->r, 0, abort) && warp_wait(&bars->full2, 0, abort);
         }
         if (ok) {
             tc_fence_after();
             if (l0) {
-                // MMA2: Vres = T R
+                // MMA2: [T; A_O T] R (the T rows give Vres); the Gram
+                // product [K; Q] K^T (B: the key tile, K-major)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16(tmem + G::kColS1, sdesc_sw128(tt + s * 32, 16, 1024),
                              sdesc_sw128(vt + s * 2048, kTokHalf, 1024), G::kIdescT, s != 0);
+#pragma unroll
+                for (int s = 0; s < kSteps; ++s)
+                    mma_bf16(tmem + G::kColG, sdesc_sw128(kq + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024),
+                             sdesc_sw128(kt + (s >> 2) * kTokHalf + (s & 3) * 32, 16, 1024), G::kIdescG,
+                             s != 0);
                 mma_commit(&bars->d2);
             }
             __syncwarp();
@@ -338,7 +368,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         const unsigned char *kq = smem + G::kOffKQ, *orr = smem + G::kOffOR;
         float sc[3] = {0.f, 0.f, 0.f};
 
-        // ---- the state tiles (bf16) and their inner products, T, coefficients
+        // ---- the state tiles (bf16), their inner products, the coefficients
         {
             const size_t sbase = ((size_t)gc * H + h) * D * D;
             const float *S0g = p.S_chunks + sbase, *M0g = p.M_chunks + sbase;
@@ -364,12 +394,6 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 put8(smem + G::kOffM0 + off, k, c8 & 7, m);
                 put8(smem + G::kOffDS + off, k, c8 & 7, a);
                 put8(smem + G::kOffDM + off, k, c8 & 7, b);
-            }
-            for (int idx = e; idx < C * 8; idx += 256) {
-                const int i = idx >> 3, c = idx & 7;
-                float x[8];
-                load8(blk + BL::kT * BL::kMat + i * C + 8 * c, x);
-                put8(smem + G::kOffT, i, c, x);
             }
             for (int idx = e; idx < BL::kRows * C; idx += 256) vec[idx] = blk[BL::kMats * BL::kMat + idx];
             if (e < C) {
@@ -500,6 +524,9 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 tmem_st16(lb + G::kColS1 + j, u1);
             }
             tmem_st_wait();
+            // W1 = dA . Y, Y = (Q K^T) Diag(eta), and W2 = dL . X, X = Diag(alpha)
+            // (K K^T) Diag(eta), for the gates (the Gram rows of the other
+            // half-warp: each token's key and query rows share a warp)
             float *Wy = blk + BL::kY * BL::kMat, *Wx = blk + BL::kX * BL::kMat;
             const float *Gm = blk + BL::kG * BL::kMat;
             unsigned char *a6 = smem + G::kOffA6, *a7 = smem + G::kOffA7;
@@ -510,17 +537,19 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 float x[16], g[16], w[16], y[16], ys[16];
                 __syncwarp();
                 tmem_ld16(lb + G::kColM3 + m0, x);
+                tmem_ld16(lb + G::kColG + m0, w);
                 tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) w[u] = __shfl_xor_sync(0xffffffffu, w[u], 16);
                 if (first) {
                     // dA row t: dY = dA . Gamma, and dA . Y for the gates
                     load16(Gm + t * C + m0, g);
-                    load16(Wy + t * C + m0, w);
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int m = m0 + u;
                         const bool on = in && m <= t;
                         y[u] = on ? x[u] * g[u] : 0.f;
-                        w[u] = on ? x[u] * w[u] : 0.f;
+                        w[u] = on ? x[u] * w[u] * ge[m] : 0.f;
                         ys[u] = y[u] * ge[m];
                     }
                     store16(Wy + t * C + m0, w);
@@ -529,13 +558,12 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 } else {
                     // dL row t (= -(dR Vres^T)): dX = dL . Gamma_m, and dL . X
                     load16(Gm + (t > 0 ? t - 1 : 0) * C + m0, g);
-                    load16(Wx + t * C + m0, w);
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int m = m0 + u;
                         const bool on = in && m < t;
                         y[u] = on ? -x[u] * g[u] : 0.f;
-                        w[u] = on ? -x[u] * w[u] : 0.f;
+                        w[u] = on ? -x[u] * w[u] * a_t * ge[m] : 0.f;
                         ys[u] = y[u] * ge[m];
                         g[u] = a_t * y[u];
                     }
@@ -644,7 +672,7 @@ cudaError_t launch_chunk_tc_d(const BwdProblem &p, cudaStream_t st, const CUtens
                                            (int)G::kSmemBytes);
     if (err != cudaSuccess) return err;
     kern<<<dim3(p.loc.max_chunks, p.loc.H), G::kThreads, G::kSmemBytes, st>>>(
-        p, maps[0], maps[1], maps[2], maps[3], maps[4]);
+        p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
     return cudaGetLastError();
 }
 
@@ -653,13 +681,13 @@ cudaError_t launch_chunk_tc_d(const BwdProblem &p, cudaStream_t st, const CUtens
 // bf16 inputs: the chunk products of the gradient on the tensor cores, after
 // the gradient prep and the reverse chain.
 cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st) {
-    if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16 || !p.prep || !p.adj)
+    if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16 || !p.prep || !p.adj || !p.tcblk)
         return cudaErrorInvalidValue;
     if (p.loc.max_chunks <= 0 || p.loc.T_total <= 0) return cudaSuccess;
-    CUtensorMap maps[5];
-    const void *src[5] = {p.k, p.q, p.dout, p.dv, p.v};
-    const int box[5] = {16, 16, 16, 16, 64};
-    for (int i = 0; i < 5; ++i)
+    CUtensorMap maps[6];
+    const void *src[6] = {p.k, p.q, p.dout, p.dv, p.v, p.k};
+    const int box[6] = {16, 16, 16, 16, 64, 64};
+    for (int i = 0; i < 6; ++i)
         if (!make_token_map_bf16(&maps[i], src[i], p.loc.T_total, p.loc.H, p.D, box[i]))
             return cudaErrorInvalidValue;
     return p.D == 128 ? launch_chunk_tc_d<128>(p, st, maps) : launch_chunk_tc_d<64>(p, st, maps);

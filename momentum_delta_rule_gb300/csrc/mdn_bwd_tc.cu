@@ -4,7 +4,8 @@
 //
 // Per chunk of n tokens, walking the chunks from the last, with the state
 // adjoints dS, dM at the chunk's end in TMEM (fp32) and the chunk's
-// operands from the gradient prep (T^T, (A T)^T, per-token coefficients):
+// operand block (the forward prep's [T; A_O T] tile, read transposed as an
+// MN-major operand, and the per-token coefficients):
 //
 //   MMA-U  D2  = (A T)^T dO                            (state-independent)
 //   MMA1   D1  = [K; Q] [dS | dM]                      (K rows used)
@@ -103,7 +104,7 @@ struct ChainCfg {
     static constexpr uint32_t kColSt = 4 * NS;
     static constexpr uint32_t kTmemCols = 8 * NS;
     static constexpr uint32_t kIdesc1 = idesc_bf16(128, 2 * NS, false, true);
-    static constexpr uint32_t kIdesc2 = idesc_bf16(128, NS, false, true);
+    static constexpr uint32_t kIdesc2 = idesc_bf16(64, NS, true, true);
     static constexpr uint32_t kIdesc3 = idesc_bf16(D, 2 * NS, true, true);
 };
 
@@ -281,10 +282,11 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             if (!warp_wait_c(&bars->state, i & 1, abort)) break;
             tc_fence_after();
             if (l0) {
-                // MMA-U: D2 = (A T)^T dO, then MMA1: D1 = [K; Q] [dS | dM]
+                // MMA-U: D2 = (A T)^T dO (A: the A_O T rows of the tile, read
+                // MN-major, 16 rows i per step), then MMA1: D1 = [K; Q] [dS | dM]
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(blk + CL::kOffATt + kk * 32, 16, 1024);
+                    const uint64_t a = sdesc_sw128(blk + CL::kOffTile + kk * 4096 + 2048, kKQHalf, 1024);
                     const uint64_t b = sdesc_sw128(ob + kk * 2048, 8192, 1024);
                     mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, kk != 0);
                 }
@@ -302,10 +304,10 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             if (!warp_wait_c(&bars->r, i & 1, abort)) break;
             tc_fence_after();
             if (l0) {
-                // MMA2: D2 += T^T R''
+                // MMA2: D2 += T^T R'' (A: the T rows of the tile, MN-major)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = sdesc_sw128(blk + CL::kOffTt + kk * 32, 16, 1024);
+                    const uint64_t a = sdesc_sw128(blk + CL::kOffTile + kk * 4096, kKQHalf, 1024);
                     const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
                     mma_bf16(tmem + C::kColD2, a, b, C::kIdesc2, 1);
                 }

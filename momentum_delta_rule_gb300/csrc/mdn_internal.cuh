@@ -133,17 +133,18 @@ struct BwdProblem {
     mdn_dtype dtype;
 };
 
-// Per-(slot, head) operand block of the tensor-core reverse chain (bf16
-// inputs): T^T and (A T)^T as bf16 in the 128-byte-swizzled K-major operand
-// layout, their 64 rows in the token slots of the tc_row order (the query
-// slots zero), then kRows rows of 64 fp32 per-token coefficients.
+// Per-(slot, head) operand block of the tensor-core gradient kernels (bf16
+// inputs): the forward prep's operand tile [T; A_O T] (PrepLayoutTC: bf16,
+// 128-byte-swizzled K-major, rows in the tc_row order), then kRows rows of
+// 64 fp32 per-token coefficients of the reverse chain, which replace the
+// forward's carry vectors there.
 struct BwdChainLayout {
-    static constexpr size_t kOffTt = 0;
-    static constexpr size_t kOffATt = 16384;
-    static constexpr size_t kOffVec = 32768;
+    static constexpr size_t kOffTile = 0;
+    static constexpr size_t kOffVec = PrepLayoutTC::kOffVec;
     enum { vCS = 0, vCM, vBS, vBM, vQS, vQM, vScal, kRows = 8 };
-    static constexpr size_t kBytes = 32768 + sizeof(float) * kChunk * kRows;
+    static constexpr size_t kBytes = kOffVec + sizeof(float) * kChunk * kRows;
 };
+static_assert(BwdChainLayout::kBytes == PrepLayoutTC::kBytes, "the forward prep writes the block");
 
 // Per-(slot, head) block of the gradient pass, fp32: five 64 x 64 matrices
 // (T, A = (Q Kh^T) . Gamma, X = P Kh^T, Y = Q Kh^T, Gamma), then vector rows.
