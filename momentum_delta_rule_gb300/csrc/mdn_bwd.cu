@@ -867,8 +867,9 @@ bwd_chunk_kernel(const BwdProblem p) {
 // triangle), and in the A slot the kRowAcc row sums followed by the three
 // state inner products <S0, dS>, <M0, dS>, <M0, dM>.
 constexpr size_t kGateSmem = sizeof(float) * (C * LP + kGateScratch + 3 * C + kRowAcc * C);
+constexpr int kGateThreads = 256;
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kGateThreads)
 bwd_gates_kernel(const BwdProblem p) {
     extern __shared__ float sm[];
     float *dG = sm, *scr = dG + C * LP;
@@ -890,15 +891,27 @@ bwd_gates_kernel(const BwdProblem p) {
         }
         ga[tid] = a; gm[tid] = m; gb[tid] = b;
     }
-    for (int idx = tid; idx < kRowAcc * C; idx += blockDim.x) rowacc[idx] = ra[idx];
+    for (int idx = tid; idx < kRowAcc * C; idx += kGateThreads) rowacc[idx] = ra[idx];
     // dG = dA . Y, plus the carry row on the last row, plus dL . X one row up
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
+    // (every load of a thread issued before the first use)
+    constexpr int kPer = C * C / kGateThreads;
+    float w1[kPer], w2[kPer], gl[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tid + kGateThreads * u;
+        w1[u] = W1[idx];
+        w2[u] = idx + C < C * C ? W2[idx + C] : 0.f;
+        gl[u] = ra[rGLast * C + (idx & 63)];
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int idx = tid + kGateThreads * u;
         const int r = idx >> 6, m = idx & 63;
         float v = 0.f;
         if (r < n && m <= r) {
-            v = W1[idx];
-            if (r + 1 < n) v += W2[idx + C];
-            if (r == n - 1) v += ra[rGLast * C + m];
+            v = w1[u];
+            if (r + 1 < n) v += w2[u];
+            if (r == n - 1) v += gl[u];
         }
         dG[r * LP + m] = v;
     }
@@ -931,7 +944,7 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         if ((err = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kGateSmem)) != cudaSuccess)
             return err;
-        kg<<<dim3(p.loc.max_chunks, H), 256, kGateSmem, st>>>(p);
+        kg<<<dim3(p.loc.max_chunks, H), kGateThreads, kGateSmem, st>>>(p);
         return cudaGetLastError();
     }
     if (p.loc.max_chunks > 0) {

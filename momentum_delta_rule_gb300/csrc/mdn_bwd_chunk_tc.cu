@@ -73,7 +73,14 @@ struct GradCfg {
     static constexpr uint32_t kOffKt = kOffM0;
     static constexpr uint32_t kOffA6 = kOverlay ? kOffM0 : kOffTile + kHalf;
     static constexpr uint32_t kOffA7 = kOffA6 + kHalf;
-    static constexpr uint32_t kOffCoef = kOverlay ? kOffV + kTok : kOffA7 + kHalf;
+    // Gamma (fp32 64 x 64) over V once MMA2 is done, where V has the room
+    static constexpr uint32_t kOffGam = kOverlay ? kOffV : kOffA7 + kHalf;
+    // dA . Y and dL . X (fp32, 64 x 64 each, in two 32-column boxes) staged
+    // for their TMA stores over dS, dM once MMA4 is done, where those have
+    // the room; dQ and dK (bf16) over [dO; dR] once MMA5 is done
+    static constexpr uint32_t kOffWst = kOverlay ? kOffDS : kOffGam + 16384;
+    static constexpr uint32_t kOffQKst = kOffOR;
+    static constexpr uint32_t kOffCoef = kOverlay ? kOffV + kTok : kOffWst + 2 * kHalf;
     // coefficients (vector rows, alpha, eta), the two column halves' row sums,
     // per-warp inner products
     static constexpr int kCoefFloats = BL::kRows * C + 2 * C + 2 * kSums * C + 8 * 4;
@@ -81,12 +88,14 @@ struct GradCfg {
     static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
     static_assert(kOffVres + kTok <= kOffM0 && kTok <= kState, "overlays");
-    static_assert(!kOverlay || kOffA7 + kHalf <= kOffDS, "overlays");
+    static_assert(!kOverlay || (kOffA7 + kHalf <= kOffDS && kTok >= 16384 && 2 * kState >= 2 * kHalf),
+                  "overlays");
+    static_assert(kStage == 2 * kTok, "dQ, dK staging");
     static constexpr uint32_t kColS1 = 0, kColM1 = D, kColS3 = 2 * D, kColM3 = 3 * D;
     static constexpr uint32_t kColG = 3 * D + 64 > 4 * D - 64 ? 4 * D : 3 * D + 64;  // Gram, 64 columns
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kThreads = 320;
-    static constexpr uint32_t kTxBytes = 2 * kStage + kTok;
+    static constexpr uint32_t kTxBytes = 2 * kStage + kTok + 2 * kState;
     static constexpr uint32_t kTx2Bytes = kHalf + kTok;
     static_assert(kColG + 64 <= kTmemCols, "TMEM columns");
     static constexpr uint32_t kIdescKS = idesc_bf16(128, D, false, true);   // MMA1, MMA6
@@ -99,7 +108,7 @@ struct GradCfg {
 };
 
 struct GradBars {
-    uint64_t full, full2, st, d13, r, d2, v, d45, y, d67, drain;
+    uint64_t full, full2, full3, st, d13, r, d2, v, d45, y, d67, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -126,6 +135,17 @@ __device__ __forceinline__ void get16(const unsigned char *tile, int row, uint32
     }
 }
 
+__device__ __forceinline__ void get8(const unsigned char *tile, int row, uint32_t chunk, float *f) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(tile + sw128_offset((uint32_t)row, chunk));
+    const __nv_bfloat162 *hv = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(hv[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
 __device__ __forceinline__ void put8(unsigned char *tile, int row, uint32_t chunk, const float *x) {
     *reinterpret_cast<uint4 *>(tile + sw128_offset((uint32_t)row, chunk)) =
         make_uint4(pk2(x[0], x[1]), pk2(x[2], x[3]), pk2(x[4], x[5]), pk2(x[6], x[7]));
@@ -134,6 +154,15 @@ __device__ __forceinline__ void put8(unsigned char *tile, int row, uint32_t chun
 __device__ __forceinline__ void put16(unsigned char *tile, int row, uint32_t c0, const float *x) {
     put8(tile, row, c0, x);
     put8(tile, row, c0 + 1, x + 8);
+}
+
+// 16 fp32 values of row t, columns 16 cc .. 16 cc + 15 of a 32-column box
+// (64 rows x 128 bytes, 128-byte swizzled) staged for a TMA store.
+__device__ __forceinline__ void stage_w(unsigned char *box, int t, int cc, const float *w) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(box + sw128_offset((uint32_t)t, (uint32_t)(4 * cc + i))) =
+            make_float4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 __device__ __forceinline__ void load8(const float *g, float *x) {
@@ -146,12 +175,6 @@ __device__ __forceinline__ void load8(const float *g, float *x) {
 __device__ __forceinline__ void load16(const float *g, float *x) {
     load8(g, x);
     load8(g + 8, x + 8);
-}
-
-__device__ __forceinline__ void store16(float *g, const float *x) {
-#pragma unroll
-    for (int i = 0; i < 16; i += 4)
-        *reinterpret_cast<float4 *>(g + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
 }
 
 __device__ __forceinline__ void store16_bf16(void *g, const float *x) {
@@ -175,7 +198,11 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const __grid_constant__ CUtensorMap map_o,
                     const __grid_constant__ CUtensorMap map_r,
                     const __grid_constant__ CUtensorMap map_v,
-                    const __grid_constant__ CUtensorMap map_kt) {
+                    const __grid_constant__ CUtensorMap map_kt,
+                    const __grid_constant__ CUtensorMap map_dq,
+                    const __grid_constant__ CUtensorMap map_dk,
+                    const __grid_constant__ CUtensorMap map_wy,
+                    const __grid_constant__ CUtensorMap map_wx) {
     using G = GradCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -192,6 +219,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
     if (threadIdx.x == 0) {
         mbar_init(&bars->full, 1);
         mbar_init(&bars->full2, 1);
+        mbar_init(&bars->full3, 1);
         mbar_init(&bars->st, 8);
         mbar_init(&bars->d13, 1);
         mbar_init(&bars->r, 8);
@@ -238,6 +266,12 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 }
                 tma_load_3d(smem + G::kOffV + hh * kTokHalf, &map_v, &bars->full, 64 * hh, h, t0);
             }
+            // the adjoints at the chunk's end, as the reverse chain left them
+            // (bf16 operand tiles dS, dM)
+            const unsigned char *adj = reinterpret_cast<const unsigned char *>(p.adj) +
+                                       ((size_t)gc * H + h) * 2 * G::kState;
+            bulk_load(smem + G::kOffDS, adj, G::kState, &bars->full);
+            bulk_load(smem + G::kOffDM, adj + G::kState, G::kState, &bars->full);
             // once MMA1 and MMA3 have read the states: the operand tile of
             // the forward prep and the 64 key rows of the Gram product
             bool go = mbar_wait(&bars->d13, 0, abort);
@@ -249,9 +283,16 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 for (int hh = 0; hh < G::kHalves; ++hh)
                     tma_load_3d(smem + G::kOffKt + hh * kTokHalf, &map_kt, &bars->full2, 64 * hh, h, t0);
             }
+            // once MMA2 has read R: Gamma over V
+            bool go3 = go && mbar_wait(&bars->d2, 0, abort);
+            if (go3) {
+                mbar_arrive_expect_tx(&bars->full3, 16384);
+                bulk_load(smem + G::kOffGam, blk + BL::kG * BL::kMat, 16384, &bars->full3);
+            }
             int dummy = 0;
             mbar_wait(&bars->full, 0, &dummy);     // no copy in flight at exit
             if (go) mbar_wait(&bars->full2, 0, &dummy);
+            if (go3) mbar_wait(&bars->full3, 0, &dummy);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -368,38 +409,62 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         const unsigned char *kq = smem + G::kOffKQ, *orr = smem + G::kOffOR;
         float sc[3] = {0.f, 0.f, 0.f};
 
-        // ---- the state tiles (bf16), their inner products, the coefficients
+        // ---- the entry-state tiles (bf16), the inner products with the
+        //      adjoint tiles, the coefficients
         {
+            // the coefficients first (their latency overlaps the states')
+            float vpre[BL::kRows * C / 256];
+#pragma unroll
+            for (int u = 0; u < BL::kRows * C / 256; ++u) vpre[u] = blk[BL::kMats * BL::kMat + e + 256 * u];
+            float g_a = 0.f, g_e = 0.f;
+            if (e < n) {
+                const size_t gi = (size_t)(t0 + e) * H + h;
+                g_a = p.alpha[gi];
+                g_e = p.eta[gi];
+            }
             const size_t sbase = ((size_t)gc * H + h) * D * D;
             const float *S0g = p.S_chunks + sbase, *M0g = p.M_chunks + sbase;
-            const float *dSg = p.adj + ((size_t)gc * H + h) * 2 * D * D, *dMg = dSg + D * D;
+            const unsigned char *dst = smem + G::kOffDS, *dmt = smem + G::kOffDM;
             constexpr int kCh = D / 8;
-#pragma unroll 2
-            for (int idx = e; idx < D * kCh; idx += 256) {
-                const int k = idx / kCh, c8 = idx - k * kCh;
-                const size_t g = (size_t)k * D + 8 * c8;
-                float s[8], m[8], a[8], b[8];
-                load8(S0g + g, s);
-                load8(M0g + g, m);
-                load8(dSg + g, a);
-                load8(dMg + g, b);
+            constexpr int kIter = D * kCh / 256;         // 16-byte output chunks per thread
+            constexpr int kBatch = kIter;                 // every load in flight at once
+            bool have = false;
+#pragma unroll 1
+            for (int b0 = 0; b0 < kIter; b0 += kBatch) {
+                float s[kBatch][8], m[kBatch][8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    sc[0] = fmaf(s[u], a[u], sc[0]);
-                    sc[1] = fmaf(m[u], a[u], sc[1]);
-                    sc[2] = fmaf(m[u], b[u], sc[2]);
+                for (int u = 0; u < kBatch; ++u) {
+                    const int idx = e + 256 * (b0 + u);
+                    const size_t g = (size_t)(idx / kCh) * D + 8 * (idx % kCh);
+                    load8(S0g + g, s[u]);
+                    load8(M0g + g, m[u]);
                 }
-                const uint32_t off = (c8 >> 3) * G::kStateHalf;
-                put8(smem + G::kOffS0 + off, k, c8 & 7, s);
-                put8(smem + G::kOffM0 + off, k, c8 & 7, m);
-                put8(smem + G::kOffDS + off, k, c8 & 7, a);
-                put8(smem + G::kOffDM + off, k, c8 & 7, b);
+                if (!have) have = mbar_wait(&bars->full, 0, abort);
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int idx = e + 256 * (b0 + u);
+                    const int k = idx / kCh, c8 = idx % kCh;
+                    const uint32_t off = (c8 >> 3) * G::kStateHalf;
+                    if (have) {
+                        float a[8], b[8];
+                        get8(dst + off, k, c8 & 7, a);
+                        get8(dmt + off, k, c8 & 7, b);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            sc[0] = fmaf(s[u][v], a[v], sc[0]);
+                            sc[1] = fmaf(m[u][v], a[v], sc[1]);
+                            sc[2] = fmaf(m[u][v], b[v], sc[2]);
+                        }
+                    }
+                    put8(smem + G::kOffS0 + off, k, c8 & 7, s[u]);
+                    put8(smem + G::kOffM0 + off, k, c8 & 7, m[u]);
+                }
             }
-            for (int idx = e; idx < BL::kRows * C; idx += 256) vec[idx] = blk[BL::kMats * BL::kMat + idx];
+#pragma unroll
+            for (int u = 0; u < BL::kRows * C / 256; ++u) vec[e + 256 * u] = vpre[u];
             if (e < C) {
-                const size_t gi = (size_t)(t0 + e) * H + h;
-                ga[e] = e < n ? p.alpha[gi] : 0.f;
-                ge[e] = e < n ? p.eta[gi] : 0.f;
+                ga[e] = g_a;
+                ge[e] = g_e;
             }
             fence_proxy_async();
             __syncwarp();
@@ -524,11 +589,16 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 tmem_st16(lb + G::kColS1 + j, u1);
             }
             tmem_st_wait();
+            ok = warp_wait(&bars->full3, 0, abort);         // Gamma in shared memory
+        }
+        if (ok) {
             // W1 = dA . Y, Y = (Q K^T) Diag(eta), and W2 = dL . X, X = Diag(alpha)
             // (K K^T) Diag(eta), for the gates (the Gram rows of the other
             // half-warp: each token's key and query rows share a warp)
-            float *Wy = blk + BL::kY * BL::kMat, *Wx = blk + BL::kX * BL::kMat;
-            const float *Gm = blk + BL::kG * BL::kMat;
+            const float *Gm = reinterpret_cast<const float *>(smem + G::kOffGam);
+            // this thread's W rows: dA . Y in the first 16 KB, dL . X in the
+            // second, column box ch
+            unsigned char *wst = smem + G::kOffWst + (first ? 0u : (uint32_t)kHalf) + ch * 8192;
             unsigned char *a6 = smem + G::kOffA6, *a7 = smem + G::kOffA7;
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
@@ -552,7 +622,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                         w[u] = on ? x[u] * w[u] * ge[m] : 0.f;
                         ys[u] = y[u] * ge[m];
                     }
-                    store16(Wy + t * C + m0, w);
+                    stage_w(wst, t, cc, w);
                     put16(a6, rowK, c0, ys);
                     put16(a7, rowQ, c0, y);
                 } else {
@@ -567,7 +637,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                         ys[u] = y[u] * ge[m];
                         g[u] = a_t * y[u];
                     }
-                    store16(Wx + t * C + m0, w);
+                    stage_w(wst, t, cc, w);
                     put16(a6, rowQ, c0, ys);
                     put16(a7, rowK, c0, g);
                 }
@@ -585,6 +655,10 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             const size_t row = ((size_t)(t0 + t) * H + h) * D;
             __nv_bfloat16 *dqg = static_cast<__nv_bfloat16 *>(p.dq) + row;
             __nv_bfloat16 *dkg = static_cast<__nv_bfloat16 *>(p.dk) + row;
+            // rows of a 16-row group that the chunk end cuts are stored here;
+            // the full groups go out as TMA boxes from the staging tiles
+            const bool ragged = 16 * (t >> 4) + 16 > n;
+            unsigned char *qkst = smem + G::kOffQKst;
 #pragma unroll 1
             for (int cc = 0; cc < kCC; ++cc) {
                 const int j = j0 + 16 * cc;
@@ -602,7 +676,10 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                         dsum = fmaf(kh[u], kk[u], dsum);
                         pv[u] = a_t * pv[u] + e_t * kh[u];
                     }
-                    if (in) {
+                    const uint32_t hq = (uint32_t)(j >> 6) * kTokHalf, c0 = (uint32_t)((j & 63) >> 3);
+                    put16(qkst + hq, t, c0, x);
+                    put16(qkst + G::kTok + hq, t, c0, pv);
+                    if (in && ragged) {
                         store16_bf16(dqg + j, x);
                         store16_bf16(dkg + j, pv);
                     }
@@ -613,6 +690,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             }
         }
 
+        fence_proxy_async();                 // the staged tiles, for the TMA stores
         // ---- the row sums of both column halves and the inner products to
         //      the gradient block's A slot
         {
@@ -641,6 +719,25 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         }
         epi_sync();
         if (!*abort) {
+            if (e == 0) {
+                // dA . Y and dL . X into the gradient block; dQ and dK rows of
+                // the full 16-row groups
+                const int bi = gc * H + h;
+                const unsigned char *wst = smem + G::kOffWst;
+                tma_store_3d(&map_wy, wst, 0, 0, bi);
+                tma_store_3d(&map_wy, wst + 8192, 32, 0, bi);
+                tma_store_3d(&map_wx, wst + kHalf, 0, 0, bi);
+                tma_store_3d(&map_wx, wst + kHalf + 8192, 32, 0, bi);
+                const unsigned char *qkst = smem + G::kOffQKst;
+                for (int g = 0; g < 4 && 16 * g + 16 <= n; ++g)
+#pragma unroll
+                    for (int hh = 0; hh < G::kHalves; ++hh) {
+                        tma_store_3d(&map_dq, qkst + hh * kTokHalf + g * 2048, 64 * hh, h, t0 + 16 * g);
+                        tma_store_3d(&map_dk, qkst + G::kTok + hh * kTokHalf + g * 2048, 64 * hh, h,
+                                     t0 + 16 * g);
+                    }
+                bulk_commit_group();
+            }
             float *ra = blk + BL::kA * BL::kMat;
             for (int idx = e; idx < kSums * C; idx += 256) {
                 const int k = idx / C, tt = idx - k * C;
@@ -653,6 +750,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 for (int w = 0; w < 8; ++w) s += red[w * 4 + e];
                 ra[kSums * C + e] = s;
             }
+            if (e == 0) bulk_wait_group_read0();   // the staging tiles stay until read
         }
     }
 
@@ -672,7 +770,7 @@ cudaError_t launch_chunk_tc_d(const BwdProblem &p, cudaStream_t st, const CUtens
                                            (int)G::kSmemBytes);
     if (err != cudaSuccess) return err;
     kern<<<dim3(p.loc.max_chunks, p.loc.H), G::kThreads, G::kSmemBytes, st>>>(
-        p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
+        p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9]);
     return cudaGetLastError();
 }
 
@@ -684,12 +782,22 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st) {
     if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16 || !p.prep || !p.adj || !p.tcblk)
         return cudaErrorInvalidValue;
     if (p.loc.max_chunks <= 0 || p.loc.T_total <= 0) return cudaSuccess;
-    CUtensorMap maps[6];
-    const void *src[6] = {p.k, p.q, p.dout, p.dv, p.v, p.k};
-    const int box[6] = {16, 16, 16, 16, 64, 64};
-    for (int i = 0; i < 6; ++i)
+    CUtensorMap maps[10];
+    const void *src[8] = {p.k, p.q, p.dout, p.dv, p.v, p.k, p.dq, p.dk};
+    const int box[8] = {16, 16, 16, 16, 64, 64, 16, 16};
+    for (int i = 0; i < 8; ++i)
         if (!make_token_map_bf16(&maps[i], src[i], p.loc.T_total, p.loc.H, p.D, box[i]))
             return cudaErrorInvalidValue;
+    // the gradient blocks' Y and X slots as [block][64 rows][64 columns] fp32
+    const uint64_t blocks = (uint64_t)p.loc.max_chunks * p.loc.H;
+    const uint64_t dims[3] = {64, 64, blocks};
+    const uint64_t strides[2] = {64 * sizeof(float), BL::kBytes};
+    const uint32_t wbox[3] = {32, 64, 1};
+    if (!make_map_3d(&maps[8], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.prep + BL::kY * BL::kMat * sizeof(float),
+                     dims, strides, wbox) ||
+        !make_map_3d(&maps[9], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.prep + BL::kX * BL::kMat * sizeof(float),
+                     dims, strides, wbox))
+        return cudaErrorInvalidValue;
     return p.D == 128 ? launch_chunk_tc_d<128>(p, st, maps) : launch_chunk_tc_d<64>(p, st, maps);
 }
 

@@ -26,7 +26,7 @@
 // warp roles, TMEM layout, tc_row interleaving, bounded waits); MMA3 here
 // runs over all 128 staged rows, the K rows against dR and the Q rows
 // against dO.  Writes dV (= dR) in the input dtype and fp32, and the
-// adjoints at every chunk's end (fp32) for the chunk kernel.
+// adjoints at every chunk's end as bf16 operand tiles for the chunk kernel.
 #include <cudaTypedefs.h>
 
 #include "mdn_internal.cuh"
@@ -61,6 +61,19 @@ bool make_token_map_bf16(CUtensorMap *map, const void *base, int T_total, int H,
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
+                 const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]) {
+    auto fn = encode_fn_b();
+    if (!fn) return false;
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t st[2] = {strides[0], strides[1]};
+    cuuint32_t b[3] = {box[0], box[1], box[2]};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, type, 3, const_cast<void *>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 namespace {
@@ -170,17 +183,19 @@ __device__ __forceinline__ bool warp_wait_c(uint64_t *bar, uint32_t parity, vola
     return __all_sync(0xffffffffu, ok);
 }
 
-// One thread's 16 columns of row d of the adjoints at the end of chunk slot
-// `slot` (fp32 [slot, H, 2, dk, dv] in the workspace).
+// One thread's 16 columns (from column j) of row d of the adjoints at the
+// end of chunk slot `slot`, as the chunk kernel's bf16 operand tiles: per
+// (slot, head) dS then dM, each D rows x D columns in 64-column halves of
+// D rows x 128 bytes, 128-byte swizzled.
 template <int D>
-__device__ __forceinline__ void store_adjoint(const BwdProblem &p, int slot, int h, size_t off,
+__device__ __forceinline__ void store_adjoint(const BwdProblem &p, int slot, int h, int d, int j,
                                               const float *S, const float *M) {
-    float *base = p.adj + ((size_t)slot * p.loc.H + h) * 2 * D * D + off;
-#pragma unroll
-    for (int j = 0; j < kEpiCols; j += 4) {
-        *reinterpret_cast<float4 *>(base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        *reinterpret_cast<float4 *>(base + (size_t)D * D + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
-    }
+    unsigned char *base = reinterpret_cast<unsigned char *>(p.adj) +
+                          ((size_t)slot * p.loc.H + h) * 2 * D * D * sizeof(__nv_bfloat16);
+    const uint32_t off = (uint32_t)(j >> 6) * (D * 128);
+    const uint32_t c0 = (uint32_t)((j & 63) >> 3);
+    store_row16(base + off, d, c0, S);
+    store_row16(base + (size_t)D * D * sizeof(__nv_bfloat16) + off, d, c0, M);
 }
 
 template <int D, int NS>
@@ -373,7 +388,7 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state);
-                if (row_ok) store_adjoint<D>(p, slot0 + nch - 1, h, st_row, S, M);
+                if (row_ok) store_adjoint<D>(p, slot0 + nch - 1, h, d, col0 + c0, S, M);
             }
         }
         const int tok = 16 * q + (lane & 15);
@@ -470,7 +485,7 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     if (more) mbar_arrive(&bars->state);
                     mbar_arrive(&bars->empty[st]);
                 }
-                if (more && row_ok) store_adjoint<D>(p, slot0 + c - 1, h, st_row, S, M);
+                if (more && row_ok) store_adjoint<D>(p, slot0 + c - 1, h, d, col0 + c0, S, M);
             }
         }
         if (!*abort) {

@@ -101,6 +101,23 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Shared -> global tensor copy of one box (bulk-group completion); the
+// coordinates must not be negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y,
+                                             int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Wait until every committed bulk group of this thread has finished reading
+// its shared-memory source.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {
     asm volatile(
@@ -296,5 +313,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
 // columns x 1 head x box_t tokens, 128-byte swizzle); false on failure.
 bool make_token_map_bf16(CUtensorMap *map, const void *base, int T_total, int H, int D,
                          int box_t);
+
+// Host: a 3-D TMA map with 128-byte swizzle (dims innermost first, byte
+// strides of the outer two); false on failure.
+bool make_map_3d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
+                 const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]);
 
 }  // namespace mdn
