@@ -95,7 +95,11 @@ struct GradCfg {
     static constexpr uint32_t kColG = 3 * D + 64 > 4 * D - 64 ? 4 * D : 3 * D + 64;  // Gram, 64 columns
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kThreads = 320;
-    static constexpr uint32_t kTxBytes = 2 * kStage + kTok + 2 * kState;
+    // the entry states arrive as fp32 (bulk copies, D x D x 4 bytes each):
+    // S0 over the S0 and M0 tiles' regions, M0 over the dS and dM tiles'
+    static constexpr uint32_t kStateF32 = 2 * kState;
+    static constexpr uint32_t kTxBytes = 2 * kStage + kTok + 2 * kStateF32;
+    static constexpr uint32_t kTxAdj = 2 * kState;
     static constexpr uint32_t kTx2Bytes = kHalf + kTok;
     static_assert(kColG + 64 <= kTmemCols, "TMEM columns");
     static constexpr uint32_t kIdescKS = idesc_bf16(128, D, false, true);   // MMA1, MMA6
@@ -108,7 +112,7 @@ struct GradCfg {
 };
 
 struct GradBars {
-    uint64_t full, full2, full3, st, d13, r, d2, v, d45, y, d67, drain;
+    uint64_t full, fulla, full2, full3, rd, st, d13, r, d2, v, d45, y, d67, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -218,6 +222,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->full, 1);
+        mbar_init(&bars->fulla, 1);
+        mbar_init(&bars->rd, 8);
         mbar_init(&bars->full2, 1);
         mbar_init(&bars->full3, 1);
         mbar_init(&bars->st, 8);
@@ -266,12 +272,21 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 }
                 tma_load_3d(smem + G::kOffV + hh * kTokHalf, &map_v, &bars->full, 64 * hh, h, t0);
             }
-            // the adjoints at the chunk's end, as the reverse chain left them
-            // (bf16 operand tiles dS, dM)
-            const unsigned char *adj = reinterpret_cast<const unsigned char *>(p.adj) +
-                                       ((size_t)gc * H + h) * 2 * G::kState;
-            bulk_load(smem + G::kOffDS, adj, G::kState, &bars->full);
-            bulk_load(smem + G::kOffDM, adj + G::kState, G::kState, &bars->full);
+            // the chunk's entry states, fp32, over the regions of the bf16
+            // tiles (the epilogue converts them)
+            const size_t sbase = ((size_t)gc * H + h) * D * D;
+            bulk_load(smem + G::kOffS0, p.S_chunks + sbase, G::kStateF32, &bars->full);
+            bulk_load(smem + G::kOffDS, p.M_chunks + sbase, G::kStateF32, &bars->full);
+            // once the fp32 states are read: the adjoints at the chunk's end
+            // as the reverse chain left them (bf16 operand tiles dS, dM)
+            bool goa = mbar_wait(&bars->rd, 0, abort);
+            if (goa) {
+                mbar_arrive_expect_tx(&bars->fulla, G::kTxAdj);
+                const unsigned char *adj = reinterpret_cast<const unsigned char *>(p.adj) +
+                                           ((size_t)gc * H + h) * 2 * G::kState;
+                bulk_load(smem + G::kOffDS, adj, G::kState, &bars->fulla);
+                bulk_load(smem + G::kOffDM, adj + G::kState, G::kState, &bars->fulla);
+            }
             // once MMA1 and MMA3 have read the states: the operand tile of
             // the forward prep and the 64 key rows of the Gram product
             bool go = mbar_wait(&bars->d13, 0, abort);
@@ -291,6 +306,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             }
             int dummy = 0;
             mbar_wait(&bars->full, 0, &dummy);     // no copy in flight at exit
+            if (goa) mbar_wait(&bars->fulla, 0, &dummy);
             if (go) mbar_wait(&bars->full2, 0, &dummy);
             if (go3) mbar_wait(&bars->full3, 0, &dummy);
         }
@@ -347,7 +363,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 mma_commit(&bars->d2);
             }
             __syncwarp();
-            ok = warp_wait(&bars->v, 0, abort);
+            ok = warp_wait(&bars->v, 0, abort) && warp_wait(&bars->fulla, 0, abort);
         }
         if (ok) {
             tc_fence_after();
@@ -422,42 +438,57 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 g_a = p.alpha[gi];
                 g_e = p.eta[gi];
             }
-            const size_t sbase = ((size_t)gc * H + h) * D * D;
-            const float *S0g = p.S_chunks + sbase, *M0g = p.M_chunks + sbase;
             const unsigned char *dst = smem + G::kOffDS, *dmt = smem + G::kOffDM;
+            const float *S0f = reinterpret_cast<const float *>(smem + G::kOffS0);
+            const float *M0f = reinterpret_cast<const float *>(smem + G::kOffDS);
             constexpr int kCh = D / 8;
             constexpr int kIter = D * kCh / 256;         // 16-byte output chunks per thread
-            constexpr int kBatch = kIter;                 // every load in flight at once
-            bool have = false;
-#pragma unroll 1
-            for (int b0 = 0; b0 < kIter; b0 += kBatch) {
-                float s[kBatch][8], m[kBatch][8];
+            float s[kIter][8], m[kIter][8];
+            bool have = warp_wait(&bars->full, 0, abort);
+            if (have) {
 #pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int idx = e + 256 * (b0 + u);
-                    const size_t g = (size_t)(idx / kCh) * D + 8 * (idx % kCh);
-                    load8(S0g + g, s[u]);
-                    load8(M0g + g, m[u]);
+                for (int u = 0; u < kIter; ++u) {
+                    const int idx = e + 256 * u;
+                    const int off = (idx / kCh) * D + 8 * (idx % kCh);
+                    load8(S0f + off, s[u]);
+                    load8(M0f + off, m[u]);
                 }
-                if (!have) have = mbar_wait(&bars->full, 0, abort);
+            }
+            // the fp32 copies are read: the adjoint tiles may land over M0's,
+            // and (after every epilogue warp is here) the bf16 tiles over S0's
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->rd);
+            epi_sync();
+            if (have) {
 #pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int idx = e + 256 * (b0 + u);
+                for (int u = 0; u < kIter; ++u) {
+                    const int idx = e + 256 * u;
                     const int k = idx / kCh, c8 = idx % kCh;
                     const uint32_t off = (c8 >> 3) * G::kStateHalf;
-                    if (have) {
-                        float a[8], b[8];
-                        get8(dst + off, k, c8 & 7, a);
-                        get8(dmt + off, k, c8 & 7, b);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            sc[0] = fmaf(s[u][v], a[v], sc[0]);
-                            sc[1] = fmaf(m[u][v], a[v], sc[1]);
-                            sc[2] = fmaf(m[u][v], b[v], sc[2]);
-                        }
-                    }
                     put8(smem + G::kOffS0 + off, k, c8 & 7, s[u]);
                     put8(smem + G::kOffM0 + off, k, c8 & 7, m[u]);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->st);
+            // <S0, dS>, <M0, dS>, <M0, dM> while MMA1 and MMA3 run
+            if (have && mbar_wait(&bars->fulla, 0, abort)) {
+#pragma unroll
+                for (int u = 0; u < kIter; ++u) {
+                    const int idx = e + 256 * u;
+                    const int k = idx / kCh, c8 = idx % kCh;
+                    const uint32_t off = (c8 >> 3) * G::kStateHalf;
+                    float a[8], b[8];
+                    get8(dst + off, k, c8 & 7, a);
+                    get8(dmt + off, k, c8 & 7, b);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        sc[0] = fmaf(s[u][v], a[v], sc[0]);
+                        sc[1] = fmaf(m[u][v], a[v], sc[1]);
+                        sc[2] = fmaf(m[u][v], b[v], sc[2]);
+                    }
                 }
             }
 #pragma unroll
@@ -466,9 +497,6 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 ga[e] = g_a;
                 ge[e] = g_e;
             }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->st);
         }
         epi_sync();                          // the coefficients are in shared memory
         const float a_t = ga[t], e_t = ge[t];
