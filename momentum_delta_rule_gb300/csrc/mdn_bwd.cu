@@ -469,44 +469,28 @@ bwd_chain_kernel(const BwdProblem p) {
 enum { rAbar = 0, rB, rAbarM, rBM, rGLast, rMuTail, kRowAcc = 8 };
 
 // The gates' gradients through the chunk coefficients, from dG (the adjoint
-// of Gamma with the row-shifted copy's folded in, rows < n, C x LP), the
-// per-row sums `rowacc` (kRowAcc rows) and the adjoints of the chunk totals
-// dcs = (d abar_n, d b_n, d mubar_n).  `scr` holds kGateScratch floats: F
-// [C][C + 2], I, G', the product tables A(r, i), Mu(r, i) ((C + 1) x C each)
-// and three vectors.  Every thread of a CTA of at least 193 threads takes
-// part; writes dalpha, dmu, deta and dbeta of the chunk's tokens.
-constexpr int kGateScratch = C * (LP + 1) + 2 * C * LP + 2 * (C + 1) * C + 3 * C;
+// of Gamma with the row-shifted copy's folded in, rows < n, C x LP; F
+// replaces it in place), the per-row sums `rowacc` (kRowAcc rows), the
+// adjoints of the chunk totals dcs = (d abar_n, d b_n, d mubar_n) and the
+// chunk's vectors abar_{i-1} and mu_tail_i.  The products A(r, i) =
+// prod_{u=r+1}^{i} alpha_u are formed as running products along the loops.
+// `scr` holds kGateScratch floats: I and G' (C rows of LP floats, so that a
+// warp's threads walking rows or columns hit distinct banks) and two
+// vectors.  Every thread of a CTA of at least 128 threads takes part;
+// writes dalpha, dmu, deta and dbeta of the chunk's tokens.
+constexpr int kGateScratch = 2 * C * LP + 2 * C;
 
-__device__ void gate_gradients(const BwdProblem &p, int t0, int n, int h, const float *dGx,
-                               float *scr, const float *ga, const float *gm, const float *gb,
-                               const float *rowacc, const float *dcs) {
+__device__ void gate_gradients(const BwdProblem &p, int t0, int n, int h, float *dGF, float *scr,
+                               const float *ga, const float *gm, const float *gb,
+                               const float *rowacc, const float *dcs, const float *abar_m,
+                               const float *mu_tail) {
     const int tid = threadIdx.x, H = p.loc.H;
-    float *Fm = scr;
-    float *Im = Fm + C * (LP + 1), *Gg = Im + C * LP;
-    float *At = Gg + C * LP, *Mt = At + (C + 1) * C;
-    float *dab = Mt + (C + 1) * C, *dbv = dab + C, *Tl = dbv + C;
-    if (tid <= C) {
-        // A(r, i) = prod_{u=r+1}^{i} alpha_u, Mu(r, i) = prod_{u=r+1}^{i} mu_u,
-        // r = tid - 1 (row r + 1 of the tables), 1 on the diagonal i == r
-        const int r = tid - 1;
-        float pa = 1.f, pmu = 1.f;
-        for (int ii = 0; ii < C; ++ii) {
-            float va = 0.f, vm = 0.f;
-            if (ii == r) {
-                va = vm = 1.f;
-            } else if (ii > r && ii < n) {
-                pa *= ga[ii];
-                pmu *= gm[ii];
-                va = pa;
-                vm = pmu;
-            }
-            At[tid * C + ii] = va;
-            Mt[tid * C + ii] = vm;
-        }
-    } else if (tid >= 128 && tid < 128 + C) {
-        // the folded vector adjoints: d abar_i plus the shifted copy's (at
-        // i + 1) and the chunk total's (at n - 1); d b_i likewise
-        const int r = tid - 128;
+    float *Im = scr, *Gg = Im + C * LP;
+    float *dab = Gg + C * LP, *Tl = dab + C;
+    if (tid < C) {
+        const int r = tid;                       // row r of the triangle
+        // the folded vector adjoints: d abar_r plus the shifted copy's (at
+        // r + 1) and the chunk total's (at n - 1); d b_r likewise
         float va = 0.f, vb = 0.f;
         if (r < n) {
             va = rowacc[rAbar * C + r];
@@ -521,8 +505,18 @@ __device__ void gate_gradients(const BwdProblem &p, int t0, int n, int h, const 
             }
         }
         dab[r] = va;
-        dbv[r] = vb;
-    } else if (tid == 192) {
+        // F[r, m + 1] = mu_m F[r, m] + dG[r, m], F[r, 0] = db_r, over dG's row
+        // (each dG entry is read before its slot is written)
+        float *row = dGF + r * LP;
+        float f = vb, nxt = row[0];
+        row[0] = f;
+        for (int m = 0; m < C; ++m) {
+            const float cur = nxt;
+            if (m + 1 < C) nxt = row[m + 1];
+            f = (m <= r && r < n) ? gm[m] * f + cur : 0.f;
+            row[m + 1] = f;
+        }
+    } else if (tid == C) {
         // Tl_u = sum_{j<u} dmu_tail_j Mu(j, u-1), started from d mubar_n
         float tl = dcs[2];
         for (int u = 0; u < C; ++u) {
@@ -531,33 +525,26 @@ __device__ void gate_gradients(const BwdProblem &p, int t0, int n, int h, const 
         }
     }
     __syncthreads();
+    const float *Fm = dGF;
     if (tid < C) {
-        const int r = tid;                       // row r of the triangle
-        // F[r, m + 1] = mu_m F[r, m] + dG[r, m], F[r, 0] = db_r
-        float f = dbv[r];
-        Fm[r * (LP + 1) + 0] = f;
-        for (int m = 0; m < C; ++m) {
-            if (m <= r && r < n) f = gm[m] * f + dGx[r * LP + m];
-            else f = 0.f;
-            Fm[r * (LP + 1) + m + 1] = f;
-        }
-    }
-    __syncthreads();
-    if (tid < C) {
+        // I[r, u] = sum_{v<u} beta_v A(v, u-1) F[r, v+1] (alpha's inner sum)
         const int r = tid;
-        // I[r, u] = sum_{v<u} beta_v A(v, u-1) F[r, v+1] (alpha's inner sum),
-        // u = 0..r, and G'[r, u] = sum_{v=u}^{r} beta_v A(v, r) Mu(u, v) (mu's)
         float inner = 0.f;
         for (int u = 0; u < C; ++u) {
             const bool in = u <= r && r < n;
             Im[r * LP + u] = in ? inner : 0.f;
-            if (in) inner = ga[u] * inner + gb[u] * Fm[r * (LP + 1) + u + 1];
+            if (in) inner = ga[u] * inner + gb[u] * Fm[r * LP + u + 1];
         }
-        float g = r < n ? gb[r] : 0.f;
+    } else if (tid < 2 * C) {
+        // G'[r, u] = sum_{v=u}^{r} beta_v A(v, r) Mu(u, v) (mu's), u = r .. 0,
+        // with the running product P = A(u - 1, r) = prod_{w=u}^{r} alpha_w
+        const int r = tid - C;
+        float g = r < n ? gb[r] : 0.f, P = 1.f;
         for (int u = C - 1; u >= 0; --u) {
             if (u <= r && r < n) {
                 Gg[r * LP + u] = g;
-                if (u > 0) g = gb[u - 1] * At[u * C + r] + gm[u] * g;
+                P *= ga[u];
+                if (u > 0) g = gb[u - 1] * P + gm[u] * g;
             } else {
                 Gg[r * LP + u] = 0.f;
             }
@@ -566,15 +553,15 @@ __device__ void gate_gradients(const BwdProblem &p, int t0, int n, int h, const 
     __syncthreads();
     if (tid < n) {
         const int u = tid;
-        float db = 0.f, dal = 0.f, dmu = 0.f;
-        const float a_prev = u > 0 ? At[u - 1] : 1.f;       // A(-1, u-1)
+        float db = 0.f, dal = 0.f, dmu = 0.f, Aur = 1.f;    // A(u, r), r = u first
+        const float a_prev = abar_m[u];                      // A(-1, u-1)
         for (int r = u; r < n; ++r) {
-            const float Aur = At[(u + 1) * C + r];            // A(u, r)
-            db = fmaf(Aur, Fm[r * (LP + 1) + u + 1], db);
+            if (r > u) Aur *= ga[r];
+            db = fmaf(Aur, Fm[r * LP + u + 1], db);
             dal = fmaf(Aur, Im[r * LP + u] + dab[r] * a_prev, dal);
-            dmu = fmaf(Fm[r * (LP + 1) + u], Gg[r * LP + u], dmu);
+            dmu = fmaf(Fm[r * LP + u], Gg[r * LP + u], dmu);
         }
-        dmu = fmaf(Tl[u], Mt[(u + 1) * C + n - 1], dmu);     // Mu(u, n-1)
+        dmu = fmaf(Tl[u], mu_tail[u], dmu);                  // Mu(u, n-1)
         const size_t gi = (size_t)(t0 + u) * H + h;
         p.dalpha[gi] = rowacc[6 * C + u] + dal;
         p.dmu[gi] = dmu;
@@ -856,7 +843,8 @@ bwd_chunk_kernel(const BwdProblem p) {
     }
     __syncthreads();
     // ---- phase 5: the gates through the coefficients
-    gate_gradients(p, t0, n, h, G, U + C * LP, ga, gm, gb, rowacc, dcs);
+    gate_gradients(p, t0, n, h, G, U + C * LP, ga, gm, gb, rowacc, dcs, vec + BL::vAbarM * C,
+                   vec + BL::vMuTail * C);
 }
 
 // ------------------------------------------------------------------ gates
@@ -866,14 +854,15 @@ bwd_chunk_kernel(const BwdProblem p) {
 // needs: dA . Y in the Y slot, dL . X in the X slot (rows < n; the lower
 // triangle), and in the A slot the kRowAcc row sums followed by the three
 // state inner products <S0, dS>, <M0, dS>, <M0, dM>.
-constexpr size_t kGateSmem = sizeof(float) * (C * LP + kGateScratch + 3 * C + kRowAcc * C);
-constexpr int kGateThreads = 256;
+constexpr size_t kGateSmem = sizeof(float) * (C * LP + kGateScratch + 5 * C + kRowAcc * C);
+constexpr int kGateThreads = 128;
 
 __global__ void __launch_bounds__(kGateThreads)
 bwd_gates_kernel(const BwdProblem p) {
     extern __shared__ float sm[];
     float *dG = sm, *scr = dG + C * LP;
-    float *ga = scr + kGateScratch, *gm = ga + C, *gb = gm + C, *rowacc = gb + C;
+    float *ga = scr + kGateScratch, *gm = ga + C, *gb = gm + C, *abm = gb + C, *mtl = abm + C;
+    float *rowacc = mtl + C;
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
     if (!locate_chunk(p.loc, gc, loc)) return;
@@ -881,6 +870,7 @@ bwd_gates_kernel(const BwdProblem p) {
     const float *blk = bwd_block(p, gc, h);
     const float *ra = blk + BL::kA * BL::kMat;
     const float *W1 = blk + BL::kY * BL::kMat, *W2 = blk + BL::kX * BL::kMat;
+    const float *vec = blk + BL::kMats * BL::kMat;
     if (tid < C) {
         float a = 0.f, m = 0.f, b = 0.f;
         if (tid < n) {
@@ -890,34 +880,39 @@ bwd_gates_kernel(const BwdProblem p) {
             b = p.beta ? p.beta[gi] : 1.f;
         }
         ga[tid] = a; gm[tid] = m; gb[tid] = b;
+        abm[tid] = vec[BL::vAbarM * C + tid];
+        mtl[tid] = vec[BL::vMuTail * C + tid];
     }
     for (int idx = tid; idx < kRowAcc * C; idx += kGateThreads) rowacc[idx] = ra[idx];
     // dG = dA . Y, plus the carry row on the last row, plus dL . X one row up
-    // (every load of a thread issued before the first use)
-    constexpr int kPer = C * C / kGateThreads;
-    float w1[kPer], w2[kPer], gl[kPer];
+    // (the loads of a batch issued before their first use)
+    constexpr int kPer = 16, kBatches = C * C / (kGateThreads * kPer);
+#pragma unroll 1
+    for (int bt = 0; bt < kBatches; ++bt) {
+        float w1[kPer], w2[kPer], gl[kPer];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tid + kGateThreads * u;
-        w1[u] = W1[idx];
-        w2[u] = idx + C < C * C ? W2[idx + C] : 0.f;
-        gl[u] = ra[rGLast * C + (idx & 63)];
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int idx = tid + kGateThreads * u;
-        const int r = idx >> 6, m = idx & 63;
-        float v = 0.f;
-        if (r < n && m <= r) {
-            v = w1[u];
-            if (r + 1 < n) v += w2[u];
-            if (r == n - 1) v += gl[u];
+        for (int u = 0; u < kPer; ++u) {
+            const int idx = tid + kGateThreads * (bt * kPer + u);
+            w1[u] = W1[idx];
+            w2[u] = idx + C < C * C ? W2[idx + C] : 0.f;
+            gl[u] = ra[rGLast * C + (idx & 63)];
         }
-        dG[r * LP + m] = v;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int idx = tid + kGateThreads * (bt * kPer + u);
+            const int r = idx >> 6, m = idx & 63;
+            float v = 0.f;
+            if (r < n && m <= r) {
+                v = w1[u];
+                if (r + 1 < n) v += w2[u];
+                if (r == n - 1) v += gl[u];
+            }
+            dG[r * LP + m] = v;
+        }
     }
     const float dcs[3] = {ra[kRowAcc * C + 0], -ra[kRowAcc * C + 1], ra[kRowAcc * C + 2]};
     __syncthreads();
-    gate_gradients(p, t0, n, h, dG, scr, ga, gm, gb, rowacc, dcs);
+    gate_gradients(p, t0, n, h, dG, scr, ga, gm, gb, rowacc, dcs, abm, mtl);
 }
 
 template <int D, typename Tin>
