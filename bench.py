@@ -505,11 +505,28 @@ def bwd_flops_per_token_head(d, C=64):
     return 36 * d * d + 14 * C * d + C * C // 3
 
 
+def bwd_bytes(x):
+    """Algorithmic HBM bytes of one gradient pass: q, k, v and dO read, dq,
+    dk, dv written (input dtype); the four gates read and their gradients
+    written (fp32); every chunk's entry states read (fp32, the saved data);
+    the final-state adjoints read and dS0, dM0 written (fp32)."""
+    lens = seq_lengths(x)
+    th = sum(lens) * x["H"]
+    D = x["D"]
+    el = 4 if x["dtype"] == "fp32" else 2
+    chunks = sum((n + 63) // 64 for n in lens) * x["H"]
+    seq_heads = len(lens) * x["H"]
+    return (7 * th * D * el + 8 * th * 4 + chunks * 2 * D * D * 4 +
+            seq_heads * 4 * D * D * 4)
+
+
 def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     """mdn_chunk_bwd on the workload (its forward's chunk entry states taken
     once beforehand, random adjoints of o and of the final states), L2
-    flushed before every timed call: ms per call, tokens/s, and the FFMA
-    roofline of the whole pass (it runs on the CUDA cores in fp32)."""
+    flushed before every timed call: ms per call, tokens/s, and the roofline
+    of the whole pass: whichever of its algorithmic bytes (HBM) or FLOPs
+    (bf16 tensor peak: the bf16 pass runs its products on tcgen05; fp32
+    inputs take the CUDA-core kernels, FFMA peak) needs more time."""
     d = x_dev
     _, _, _, Sc, Mc = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
                                     d["beta"], d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"],
@@ -547,14 +564,30 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
     tokens = sum(seq_lengths(x))
     fl = bwd_flops_per_token_head(D) * tokens * H
-    peak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-    ach = fl / (ms / 1e3) / 1e12
+    by = bwd_bytes(x)
+    s = ms / 1e3
+    bf16 = x["dtype"] != "fp32"
+    if bf16:
+        fpeak, fsrc, fbound = peaks["bf16_tflops"], "measured bf16 burst", "tensor"
+    else:
+        fpeak = SMS * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        fsrc, fbound = "fp32 FFMA from unit counts (152 SMs x 128 lanes x 2 x max clock)", "alu"
+    f_fl = fl / s / 1e12 / fpeak
+    f_by = by / s / 1e9 / peaks["hbm_gbs"]
+    if f_by >= f_fl:
+        roof = {"bound": "hbm", "achieved": by / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": f_by, "peak_source": "measured HBM copy", "other_roof_frac": f_fl}
+    else:
+        roof = {"bound": fbound, "achieved": fl / s / 1e12, "peak": fpeak, "unit": "TFLOP/s",
+                "frac": f_fl, "peak_source": fsrc, "other_roof_frac": f_by}
+    roof.update({"algorithmic_bytes": by, "algorithmic_flops": fl})
+    launches = (5 if bf16 else 3) + (1 if d["cu_seqlens"] is not None else 0)
     return {"what": "gradient pass (mdn_chunk_bwd) from the forward's chunk entry states",
-            "ms_per_call": ms, "tokens_per_s": tokens / (ms / 1e3),
-            "ratio_to_forward": None, "gpu_launches_per_call": 3 + (1 if d["cu_seqlens"] is not None else 0),
-            "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                         "frac": ach / peak, "algorithmic_flops": fl,
-                         "peak_source": "fp32 FFMA from unit counts (152 SMs x 128 lanes x 2 x max clock)"}}
+            "ms_per_call": ms, "tokens_per_s": tokens / s,
+            "ratio_to_forward": None, "gpu_launches_per_call": launches,
+            "kernels": ("chunk_prep_tc (the forward's), bwd_vec, bwd_chain_tc, bwd_chunk_tc, "
+                        "bwd_gates" if bf16 else "bwd_prep, bwd_chain, bwd_chunk"),
+            "roofline": roof}
 
 
 def time_block(mdn, x_dev, steps, warmup, flush):

@@ -59,3 +59,22 @@ def test_fp32_state_pass_peak_is_a_third_of_bf16():
     assert p["bound"] == "alu"                      # the fp32 prep runs on the CUDA cores
     # fp32 intermediates: the split prepared blocks and the q, k, v parts
     assert bench.intermediate_bytes(x) == 34816 * 32 * 2 + 2 * 3 * 2 * 2048 * 2 * 128
+
+
+def test_backward_bytes_varlen():
+    # q, k, v, dO in and dq, dk, dv out (bf16), four gates in and four
+    # gradients out (fp32), every chunk's entry states (fp32), and per
+    # (sequence, head) the final-state adjoints in and dS0, dM0 out
+    x = W.make_prefill(W.VARLEN_PACKED)
+    lens = bench.seq_lengths(x)
+    th = 32768 * 16
+    chunks = sum((n + 63) // 64 for n in lens) * 16
+    assert chunks == 523 * 16
+    want = th * (7 * 128 * 2 + 8 * 4) + chunks * 2 * 128 * 128 * 4 + len(lens) * 16 * 4 * 128 * 128 * 4
+    assert bench.bwd_bytes(x) == want
+
+
+def test_backward_flops_per_token_head():
+    # the vector-Jacobian product's state products (24 d^2 in the chunk
+    # products, 12 d^2 in the reverse chain), 14 C d chunk-local, C^2 / 3
+    assert bench.bwd_flops_per_token_head(128) == 36 * 128 * 128 + 14 * 64 * 128 + 64 * 64 // 3
