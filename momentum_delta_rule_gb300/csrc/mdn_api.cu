@@ -413,9 +413,13 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk, int d
                                     mdn_dtype dtype) {
     if (n_seq < 0 || T_total < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
     if (dtype != MDN_F32 && dtype != MDN_BF16) return 0;
-    const size_t per = mdn::BwdLayout::kBytes + sizeof(float) * (2 * (size_t)dk * dv +
-                                                                 (size_t)mdn::kChunk * dv) +
-                       (dtype == MDN_BF16 ? mdn::BwdChainLayout::kBytes : 0);
+    // per (chunk slot, head): the gradient block, then the chunk-end adjoints
+    // (fp32 inputs: fp32, and the residual adjoints dR; bf16 inputs: bf16
+    // operand tiles, and the tensor-core operand block)
+    const size_t per = mdn::BwdLayout::kBytes +
+                       (dtype == MDN_BF16
+                            ? sizeof(__nv_bfloat16) * 2 * (size_t)dk * dv + mdn::BwdChainLayout::kBytes
+                            : sizeof(float) * (2 * (size_t)dk * dv + (size_t)mdn::kChunk * dv));
     const size_t slots = (size_t)chunk_slots_bound(n_seq, T_total) * (size_t)H;
     return round256(meta_bytes(n_seq) + slots * per);
 }
@@ -486,12 +490,17 @@ mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
     unsigned char *base = ws ? ws + meta_bytes(n_seq) : nullptr;
     p.prep = base;
     p.adj = base ? reinterpret_cast<float *>(base + slots * mdn::BwdLayout::kBytes) : nullptr;
-    p.dR = p.adj ? p.adj + slots * 2 * (size_t)dk * dv : nullptr;
-    // bf16 inputs run the reverse chain on the tensor cores: its operand
-    // blocks follow (fp32 inputs keep the fp32 chain, for the fp32 bound)
-    p.tcblk = (p.dR && dtype == MDN_BF16 && T_total > 0)
-                  ? reinterpret_cast<unsigned char *>(p.dR + slots * (size_t)mdn::kChunk * dv)
-                  : nullptr;
+    if (dtype == MDN_BF16) {
+        // bf16 inputs run on the tensor cores: the adjoints as bf16 operand
+        // tiles, then the operand blocks
+        p.tcblk = (p.adj && T_total > 0)
+                      ? reinterpret_cast<unsigned char *>(p.adj) +
+                            slots * sizeof(__nv_bfloat16) * 2 * (size_t)dk * dv
+                      : nullptr;
+    } else {
+        // fp32 inputs keep the fp32 kernels (for the fp32 bound)
+        p.dR = p.adj ? p.adj + slots * 2 * (size_t)dk * dv : nullptr;
+    }
     p.q = q; p.k = k; p.v = v; p.dout = dout;
     p.alpha = alpha; p.mu = mu; p.eta = eta; p.beta = beta;
     p.S_chunks = S_chunks; p.M_chunks = M_chunks;

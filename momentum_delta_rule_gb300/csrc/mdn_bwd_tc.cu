@@ -25,8 +25,8 @@
 // slice) - the adjoint states are column-independent like the states -,
 // warp roles, TMEM layout, tc_row interleaving, bounded waits); MMA3 here
 // runs over all 128 staged rows, the K rows against dR and the Q rows
-// against dO.  Writes dV (= dR) in the input dtype and fp32, and the
-// adjoints at every chunk's end as bf16 operand tiles for the chunk kernel.
+// against dO.  Writes dV (= dR) in the input dtype, and the adjoints at
+// every chunk's end as bf16 operand tiles for the chunk kernel.
 #include <cudaTypedefs.h>
 
 #include "mdn_internal.cuh"
@@ -314,6 +314,18 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                         mma_bf16(tmem + C::kColD1, a, b, C::kIdesc1, (kb | kk) != 0);
                     }
                 mma_commit(&bars->d1);
+                if constexpr (NS == 64) {
+                    // the adjoints at this chunk's end leave as they sit in
+                    // B1: one 64-column half of the chunk kernel's dS and dM
+                    // operand tiles each
+                    const int c = nch - 1 - i;
+                    unsigned char *dst = reinterpret_cast<unsigned char *>(p.adj) +
+                                         ((size_t)(slot0 + c) * L.H + h) * 2 * D * D * 2 +
+                                         (size_t)slice * D * 128;
+                    bulk_store(dst, smem + C::kOffB1, D * 128);
+                    bulk_store(dst + (size_t)D * D * 2, smem + C::kOffB1 + C::kB1M, D * 128);
+                    bulk_commit_group();
+                }
             }
             __syncwarp();
             if (!warp_wait_c(&bars->r, i & 1, abort)) break;
@@ -339,6 +351,8 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const uint64_t b = sdesc_sw128(b3 + kk * 2048, kLbo3, 1024);
                     mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
                 }
+                // B1 is rewritten once MMA3 is done: its copy-out has read it
+                if constexpr (NS == 64) bulk_wait_group_read0();
                 mma_commit(&bars->d3);
                 mma_commit(&bars->empty[st]);
             }
@@ -348,6 +362,7 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             mma_commit(&bars->drain);
             int dummy = 0;
             mbar_wait(&bars->drain, 0, &dummy);
+            if constexpr (NS == 64) bulk_wait_group0();
         }
         __syncwarp();
     } else {
@@ -388,7 +403,7 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state);
-                if (row_ok) store_adjoint<D>(p, slot0 + nch - 1, h, d, col0 + c0, S, M);
+                if (NS != 64 && row_ok) store_adjoint<D>(p, slot0 + nch - 1, h, d, col0 + c0, S, M);
             }
         }
         const int tok = 16 * q + (lane & 15);
@@ -449,21 +464,16 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 put8s(b3, rk, chk, x, bs);
                 put8s(b3 + C::kB3M, rk, chk + C::kChM, x, bm);
                 fence_proxy_async();
-                if (in_chunk) {
+                if (in_chunk)
                     *reinterpret_cast<uint4 *>(dvg + (size_t)(t0 + tok) * rs) =
                         make_uint4(pk2(x[0], x[1]), pk2(x[2], x[3]), pk2(x[4], x[5]), pk2(x[6], x[7]));
-                    float *dr = p.dR + ((size_t)(slot0 + c) * L.H + h) * kChunk * D +
-                                (size_t)tok * D + col0 + cg;
-                    *reinterpret_cast<float4 *>(dr) = make_float4(x[0], x[1], x[2], x[3]);
-                    *reinterpret_cast<float4 *>(dr + 4) = make_float4(x[4], x[5], x[6], x[7]);
-                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->v);
             }
             // ---- the adjoints at this chunk's start: bf16 copy for the next
-            //      (earlier) chunk's MMA1, and fp32 to the workspace as the
-            //      previous chunk's end adjoints
+            //      (earlier) chunk's MMA1, and to the workspace as the
+            //      previous chunk's end adjoints (bf16 operand tiles)
             if (!warp_wait_c(&bars->d3, i & 1, abort)) break;
             tc_fence_after();
             {
@@ -485,7 +495,7 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     if (more) mbar_arrive(&bars->state);
                     mbar_arrive(&bars->empty[st]);
                 }
-                if (more && row_ok) store_adjoint<D>(p, slot0 + c - 1, h, d, col0 + c0, S, M);
+                if (NS != 64 && more && row_ok) store_adjoint<D>(p, slot0 + c - 1, h, d, col0 + c0, S, M);
             }
         }
         if (!*abort) {

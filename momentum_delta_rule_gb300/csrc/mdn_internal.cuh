@@ -126,8 +126,9 @@ struct BwdProblem {
     float *dalpha, *dmu, *deta, *dbeta;
     float *dS0, *dM0;
     unsigned char *prep;               // per (slot, head): chunk matrices and vectors
-    float *adj;                        // per (slot, head): dS, dM at the chunk's end [2, dk, dv]
-    float *dR;                         // per (slot, head): residual adjoints [64, dv]
+    float *adj;                        // per (slot, head): dS, dM at the chunk's end, fp32
+                                       // [2, dk, dv] (fp32 inputs) or bf16 operand tiles
+    float *dR;                         // per (slot, head): residual adjoints [64, dv] (fp32 inputs)
     unsigned char *tcblk;              // per (slot, head): the tensor-core chain's operands, or null
     int D;
     mdn_dtype dtype;

@@ -284,9 +284,18 @@ def test_chunk_bwd_rejects(L, over, code):
 
 
 def test_chunk_bwd_workspace_size(L):
-    a = mdn.chunk_bwd_workspace_size(8, 16384, 8, 128, 1)
-    per = 5 * 64 * 64 * 4 + 8 * 64 * 4 + 2 * 128 * 128 * 4 + 64 * 128 * 4
-    assert a >= (16384 // 64 + 8) * 8 * per and a % 256 == 0
+    # per (chunk slot, head): the gradient block (five 64 x 64 fp32 matrices,
+    # eight 64-float vector rows), then fp32 inputs: the fp32 chunk-end
+    # adjoints and the residual adjoints; bf16 inputs: the adjoints as bf16
+    # tiles and the tensor-core operand block (18 KiB)
+    blk = 5 * 64 * 64 * 4 + 8 * 64 * 4
+    slots = (16384 // 64 + 8) * 8
+    meta = 2 * 256
+    f32 = mdn.chunk_bwd_workspace_size(8, 16384, 8, 128, 0)
+    bf16 = mdn.chunk_bwd_workspace_size(8, 16384, 8, 128, 1)
+    assert f32 == meta + slots * (blk + 2 * 128 * 128 * 4 + 64 * 128 * 4)
+    assert bf16 == meta + slots * (blk + 2 * 128 * 128 * 2 + 18432)
+    assert f32 % 256 == 0 and bf16 % 256 == 0
     assert mdn.chunk_bwd_workspace_size(-1, 10, 1, 64, 1) == 0
 
 
