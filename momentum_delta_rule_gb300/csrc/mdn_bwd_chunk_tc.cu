@@ -169,16 +169,21 @@ __device__ __forceinline__ void stage_w(unsigned char *box, int t, int cc, const
             make_float4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
+// The same 16 values read back.
+__device__ __forceinline__ void get_w(const unsigned char *box, int t, int cc, float *w) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 v =
+            *reinterpret_cast<const float4 *>(box + sw128_offset((uint32_t)t, (uint32_t)(4 * cc + i)));
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+}
+
 __device__ __forceinline__ void load8(const float *g, float *x) {
     const float4 a = *reinterpret_cast<const float4 *>(g);
     const float4 b = *reinterpret_cast<const float4 *>(g + 4);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
-__device__ __forceinline__ void load16(const float *g, float *x) {
-    load8(g, x);
-    load8(g + 8, x + 8);
 }
 
 __device__ __forceinline__ void store16_bf16(void *g, const float *x) {
@@ -206,7 +211,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const __grid_constant__ CUtensorMap map_dq,
                     const __grid_constant__ CUtensorMap map_dk,
                     const __grid_constant__ CUtensorMap map_wy,
-                    const __grid_constant__ CUtensorMap map_wx) {
+                    const __grid_constant__ CUtensorMap map_wx,
+                    const __grid_constant__ CUtensorMap map_gam) {
     using G = GradCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -245,6 +251,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         prefetch_tensormap(&map_r);
         prefetch_tensormap(&map_v);
         prefetch_tensormap(&map_kt);
+        prefetch_tensormap(&map_gam);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, G::kTmemCols);
@@ -301,8 +308,11 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             // once MMA2 has read R: Gamma over V
             bool go3 = go && mbar_wait(&bars->d2, 0, abort);
             if (go3) {
+                // Gamma as two 32-column boxes, 128-byte swizzled (a row per
+                // lane reads without bank conflicts)
                 mbar_arrive_expect_tx(&bars->full3, 16384);
-                bulk_load(smem + G::kOffGam, blk + BL::kG * BL::kMat, 16384, &bars->full3);
+                tma_load_3d(smem + G::kOffGam, &map_gam, &bars->full3, 0, 0, gc * H + h);
+                tma_load_3d(smem + G::kOffGam + 8192, &map_gam, &bars->full3, 32, 0, gc * H + h);
             }
             int dummy = 0;
             mbar_wait(&bars->full, 0, &dummy);     // no copy in flight at exit
@@ -401,6 +411,15 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     mma_bf16(tmem + G::kColS1, sdesc_sw128(a7 + s * 2048, kHalf, 1024),
                              sdesc_sw128(kq + s * 2048, kHalf, 1024), G::kIdesc7, 1);
                 mma_commit(&bars->d67);
+                // dA . Y and dL . X, staged by every epilogue warp before it
+                // arrived: into the gradient block
+                const int bi = gc * H + h;
+                const unsigned char *wst = smem + G::kOffWst;
+                tma_store_3d(&map_wy, wst, 0, 0, bi);
+                tma_store_3d(&map_wy, wst + 8192, 32, 0, bi);
+                tma_store_3d(&map_wx, wst + kHalf, 0, 0, bi);
+                tma_store_3d(&map_wx, wst + kHalf + 8192, 32, 0, bi);
+                bulk_commit_group();
             }
             __syncwarp();
         }
@@ -408,6 +427,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             mma_commit(&bars->drain);
             int dummy = 0;
             mbar_wait(&bars->drain, 0, &dummy);
+            bulk_wait_group_read0();     // the staged W tiles stay until read
         }
         __syncwarp();
     } else {
@@ -519,10 +539,12 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 const int j = j0 + 16 * cc;
                 const int hh = j >> 6;
                 const uint32_t c0 = (uint32_t)((j & 63) >> 3);
-                float xs[16], xm[16];
+                float xs[16], xm[16], ys[16], ym[16];
                 __syncwarp();
                 tmem_ld16(lb + G::kColS1 + j, xs);
                 tmem_ld16(lb + G::kColM1 + j, xm);
+                tmem_ld16(lb + G::kColS3 + j, ys);
+                tmem_ld16(lb + G::kColM3 + j, ym);
                 tmem_ld_wait();
                 if (first) {
                     float v[16], r[16];
@@ -547,12 +569,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                         acc1 = fmaf(-xm[u], o[u], acc1);
                     }
                 }
-                float ys[16], ym[16];
-                __syncwarp();
-                tmem_ld16(lb + G::kColS3 + j, ys);
-                tmem_ld16(lb + G::kColM3 + j, ym);
-                tmem_ld_wait();
                 const float cS = first ? abar : -abm, cM = first ? -bb : bm;
+                __syncwarp();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) ys[u] = in ? cS * ys[u] + cM * ym[u] : 0.f;
                 tmem_st16(lb + G::kColS3 + j, ys);
@@ -623,7 +641,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             // W1 = dA . Y, Y = (Q K^T) Diag(eta), and W2 = dL . X, X = Diag(alpha)
             // (K K^T) Diag(eta), for the gates (the Gram rows of the other
             // half-warp: each token's key and query rows share a warp)
-            const float *Gm = reinterpret_cast<const float *>(smem + G::kOffGam);
+            const unsigned char *Gm = smem + G::kOffGam;
             // this thread's W rows: dA . Y in the first 16 KB, dL . X in the
             // second, column box ch
             unsigned char *wst = smem + G::kOffWst + (first ? 0u : (uint32_t)kHalf) + ch * 8192;
@@ -641,7 +659,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 for (int u = 0; u < 16; ++u) w[u] = __shfl_xor_sync(0xffffffffu, w[u], 16);
                 if (first) {
                     // dA row t: dY = dA . Gamma, and dA . Y for the gates
-                    load16(Gm + t * C + m0, g);
+                    get_w(Gm + ch * 8192, t, cc, g);
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int m = m0 + u;
@@ -655,7 +673,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     put16(a7, rowQ, c0, y);
                 } else {
                     // dL row t (= -(dR Vres^T)): dX = dL . Gamma_m, and dL . X
-                    load16(Gm + (t > 0 ? t - 1 : 0) * C + m0, g);
+                    get_w(Gm + ch * 8192, t > 0 ? t - 1 : 0, cc, g);
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int m = m0 + u;
@@ -748,14 +766,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         epi_sync();
         if (!*abort) {
             if (e == 0) {
-                // dA . Y and dL . X into the gradient block; dQ and dK rows of
-                // the full 16-row groups
-                const int bi = gc * H + h;
-                const unsigned char *wst = smem + G::kOffWst;
-                tma_store_3d(&map_wy, wst, 0, 0, bi);
-                tma_store_3d(&map_wy, wst + 8192, 32, 0, bi);
-                tma_store_3d(&map_wx, wst + kHalf, 0, 0, bi);
-                tma_store_3d(&map_wx, wst + kHalf + 8192, 32, 0, bi);
+                // dQ and dK rows of the full 16-row groups
                 const unsigned char *qkst = smem + G::kOffQKst;
                 for (int g = 0; g < 4 && 16 * g + 16 <= n; ++g)
 #pragma unroll
@@ -798,7 +809,8 @@ cudaError_t launch_chunk_tc_d(const BwdProblem &p, cudaStream_t st, const CUtens
                                            (int)G::kSmemBytes);
     if (err != cudaSuccess) return err;
     kern<<<dim3(p.loc.max_chunks, p.loc.H), G::kThreads, G::kSmemBytes, st>>>(
-        p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9]);
+        p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9],
+        maps[10]);
     return cudaGetLastError();
 }
 
@@ -810,7 +822,7 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st) {
     if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16 || !p.prep || !p.adj || !p.tcblk)
         return cudaErrorInvalidValue;
     if (p.loc.max_chunks <= 0 || p.loc.T_total <= 0) return cudaSuccess;
-    CUtensorMap maps[10];
+    CUtensorMap maps[11];
     const void *src[8] = {p.k, p.q, p.dout, p.dv, p.v, p.k, p.dq, p.dk};
     const int box[8] = {16, 16, 16, 16, 64, 64, 16, 16};
     for (int i = 0; i < 8; ++i)
@@ -824,6 +836,8 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st) {
     if (!make_map_3d(&maps[8], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.prep + BL::kY * BL::kMat * sizeof(float),
                      dims, strides, wbox) ||
         !make_map_3d(&maps[9], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.prep + BL::kX * BL::kMat * sizeof(float),
+                     dims, strides, wbox) ||
+        !make_map_3d(&maps[10], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.prep + BL::kG * BL::kMat * sizeof(float),
                      dims, strides, wbox))
         return cudaErrorInvalidValue;
     return p.D == 128 ? launch_chunk_tc_d<128>(p, st, maps) : launch_chunk_tc_d<64>(p, st, maps);
