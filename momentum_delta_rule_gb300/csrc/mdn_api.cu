@@ -242,8 +242,8 @@ mdn_status chunk_fwd_impl(
     if (err == cudaSuccess && p.cu_seqlens && p.max_chunks > 0)
         err = mdn::launch_chunk_offsets(p, cs);
     if (err == cudaSuccess && split) err = mdn::launch_split_inputs(p, cs);
-    if (err == cudaSuccess)
-        err = (tensor && !split) ? mdn::launch_chunk_prep_tc(p, cs) : mdn::launch_chunk_prep_simt(p, cs);
+    if (err == cudaSuccess && tensor)
+        err = split ? mdn::launch_chunk_prep_simt(p, cs) : mdn::launch_chunk_prep_tc(p, cs);
     if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
     if (err == cudaSuccess)
         err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_states_passthrough(p, cs);

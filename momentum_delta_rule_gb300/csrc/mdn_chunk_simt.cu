@@ -5,11 +5,13 @@
 //            with the device-side check of cu_seqlens;
 //   prep     for fp32 inputs (one CTA per chunk and head, all chunks in
 //            parallel): log-space prefix scans of alpha and mu, the
-//            coefficient matrix Gamma, the Gram matrices K K^T and Q K^T, the
-//            unit-lower-triangular system matrix, its inverse T and the
-//            intra-chunk output operator A_O T, all in fp32 (an fp32-level
-//            error bound needs the fp32 inverse), written as the hi / lo
-//            bf16 parts of the state pass's operand [T; A_O T];
+//            coefficient matrix Gamma, the Gram matrices K K^T and Q K^T on
+//            the tensor cores (split operands: hi hi + hi lo + lo hi of the
+//            bf16 parts, one fp32 accumulator), the unit-lower-triangular
+//            system matrix, its inverse T and the intra-chunk output
+//            operator A_O T in fp32 (an fp32-level error bound needs the
+//            fp32 inverse), written as the hi / lo bf16 parts of the state
+//            pass's operand [T; A_O T];
 //   split    fp32 q, k, v as hi / lo bf16 parts for the state pass;
 //   states   calls without tokens: final states = initial states.
 //
@@ -110,15 +112,28 @@ chunk_offsets_kernel(const int32_t *cu, int n_seq, int T_total, int32_t *off, in
 
 template <int D>
 struct PrepSmem {
-    static constexpr int LD = D + 1;          // padded row stride of K, Q
     static constexpr int LM = kChunk + 1;     // padded row stride of 64x64
-    // K and Q are read only by the Gram products; L, T and A_O take their
-    // place afterwards, so that two (d = 128) or three (d = 64) CTAs share an SM
-    static constexpr int kKQ = 2 * kChunk * LD, kLTA = 3 * kChunk * LM;
-    static constexpr int kShared = kKQ > kLTA ? kKQ : kLTA;
-    static constexpr int kFloats = kShared + kChunk * LM + 12 * kChunk + 64;
-    static constexpr size_t kBytes = sizeof(float) * kFloats;
+    static constexpr int kHalves = D / 64;
+    // The hi and lo [K; Q] tiles (bf16, 128 rows - the keys, then the
+    // queries - x 64 columns per 16 KiB half, 128-byte swizzled) are read
+    // only by the Gram products; L, T and A_O (fp32) take their place
+    // afterwards, so that two (d = 128) or three (d = 64) CTAs share an SM.
+    static constexpr size_t kTiles = 2 * kHalves * 16384;
+    static constexpr size_t kLTA = sizeof(float) * 3 * kChunk * LM;
+    static constexpr size_t kShared = ((kTiles > kLTA ? kTiles : kLTA) + 1023) / 1024 * 1024;
+    static constexpr int kFloats = kChunk * LM + 12 * kChunk + 64;   // Gamma, vectors, exchange
+    static constexpr size_t kOffBar = kShared + sizeof(float) * kFloats;
+    static constexpr size_t kBytes = kOffBar + 64 + 1024;            // + barriers, alignment
 };
+
+struct PrepBars {
+    uint64_t tma, gram;
+    uint32_t tmem_base;
+    int abort, issued;
+};
+
+constexpr uint32_t kTmemColsPS = 64;
+constexpr uint32_t kIdescGramS = sm100::idesc_bf16(128, 64, false, false);
 
 // Inclusive sum over the 64 lanes of warps 0 and 1.  Every thread of the
 // block must call it (it synchronises the block).
@@ -158,24 +173,28 @@ __device__ __forceinline__ float scan64_affine(float a, float c, float *xch) {
     return c;
 }
 
-template <int D, typename Tin>
+template <int D>
 __global__ void __launch_bounds__(kThreads)
-chunk_prep_simt_kernel(ChunkProblem p) {
+chunk_prep_split_kernel(ChunkProblem p, const __grid_constant__ CUtensorMap map_khi,
+                        const __grid_constant__ CUtensorMap map_qhi,
+                        const __grid_constant__ CUtensorMap map_klo,
+                        const __grid_constant__ CUtensorMap map_qlo) {
     using SM = PrepSmem<D>;
-    constexpr int LD = SM::LD, LM = SM::LM;
+    using namespace sm100;
+    constexpr int LM = SM::LM;
     const int gc = blockIdx.x, h = blockIdx.y;
     ChunkLoc loc;
     if (!locate_chunk(p, gc, loc)) return;
     const int n = loc.n;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    extern __shared__ float smem[];
-    float *Ks = smem;                      // [64][LD], until the Gram products
-    float *Qs = Ks + kChunk * LD;          // [64][LD], until the Gram products
-    float *L = smem;                       // system matrix (strict lower), after them
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    float *L = reinterpret_cast<float *>(base);      // system matrix (strict lower), after the Grams
     float *Tm = L + kChunk * LM;           // its inverse
     float *AO = Tm + kChunk * LM;          // output operator (lower)
-    float *G = smem + SM::kShared;         // Gamma [64][LM]
+    float *G = reinterpret_cast<float *>(base + SM::kShared);   // Gamma [64][LM]
     float *va = G + kChunk * LM;           // alpha
     float *vb = va + kChunk;               // beta
     float *ve = vb + kChunk;               // eta
@@ -186,21 +205,35 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     float *vm = vbb + kChunk;              // mu
     float *vgs = vm + kChunk;              // gamma_{n,j} (Gamma's last row, kept for the carry)
     float *xch = vgs + kChunk;             // scan exchange
+    PrepBars *bars = reinterpret_cast<PrepBars *>(base + SM::kOffBar);
+    volatile int *abort = &bars->abort;
 
-    const size_t rs = (size_t)p.H * D;     // token row stride
-    const Tin *kg = static_cast<const Tin *>(p.k) + (size_t)loc.t0 * rs + (size_t)h * D;
-    const Tin *qg = static_cast<const Tin *>(p.q) + (size_t)loc.t0 * rs + (size_t)h * D;
+    if (tid == 0) {
+        mbar_init(&bars->tma, 1);
+        mbar_init(&bars->gram, 1);
+        bars->abort = 0;
+        bars->issued = 0;
+        fence_mbar_init();
+        // the hi and lo parts of the chunk's keys (rows 0..63) and queries
+        // (rows 64..127); their latency hides behind the scans and Gamma
+        mbar_arrive_expect_tx(&bars->tma, (uint32_t)SM::kTiles);
 #pragma unroll
-    for (int idx = tid; idx < kChunk * D; idx += kThreads) {
-        const int i = idx / D, d = idx - i * D;
-        float kv = 0.f, qv = 0.f;
-        if (i < n) {
-            kv = to_f32(kg[(size_t)i * rs + d]);
-            qv = to_f32(qg[(size_t)i * rs + d]);
+        for (int hh = 0; hh < SM::kHalves; ++hh) {
+            unsigned char *hi = base + hh * 16384, *lo = base + (SM::kHalves + hh) * 16384;
+            tma_load_3d(hi, &map_khi, &bars->tma, 64 * hh, h, loc.t0);
+            tma_load_3d(hi + 8192, &map_qhi, &bars->tma, 64 * hh, h, loc.t0);
+            tma_load_3d(lo, &map_klo, &bars->tma, 64 * hh, h, loc.t0);
+            tma_load_3d(lo + 8192, &map_qlo, &bars->tma, 64 * hh, h, loc.t0);
         }
-        Ks[i * LD + d] = kv;
-        Qs[i * LD + d] = qv;
     }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemColsPS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
 
     // ---- gates and log-space prefix scans (lanes 0..63 = tokens)
     float a = 1.f, mu = 0.f, be = 0.f, et = 0.f;
@@ -248,40 +281,76 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     }
     __syncthreads();
 
-    // ---- Gram tiles: thread owns a 4 x 4 block of both 64 x 64 products
-    {
-        const int ti = tid >> 4, tj = tid & 15;
-        float gk[4][4] = {}, gq[4][4] = {};
-        for (int d = 0; d < D; ++d) {
-            float kr[4], qr[4], kc[4];
+    // ---- the Gram products [K; Q] K^T on the tensor cores, split operands:
+    //      hi hi^T + hi lo^T + lo hi^T into one fp32 accumulator (M = 128: the
+    //      key rows, then the query rows; N = 64: the tile's first 64 rows)
+    if (tid == 32) {
+        if (mbar_wait(&bars->tma, 0, abort)) {
+            tc_fence_after();
+            const uint32_t hi = smem_u32(base), lo = hi + SM::kHalves * 16384;
+            const uint32_t as[3] = {hi, hi, lo}, bs[3] = {hi, lo, hi};
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                kr[r] = Ks[(4 * ti + r) * LD + d];
-                qr[r] = Qs[(4 * ti + r) * LD + d];
-                kc[r] = Ks[(4 * tj + r) * LD + d];
-            }
+            for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+                for (int kb = 0; kb < SM::kHalves; ++kb)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    gk[r][c] += kr[r] * kc[c];
-                    gq[r][c] += qr[r] * kc[c];
-                }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t off = kb * 16384 + kk * 32;
+                        mma_bf16(tmem, sdesc_sw128(as[pr] + off, 16, 1024),
+                                 sdesc_sw128(bs[pr] + off, 16, 1024), kIdescGramS,
+                                 (pr | kb | kk) != 0);
+                    }
+            mma_commit(&bars->gram);
+            bars->issued = 1;
+        } else {
+            int dummy = 0;               // the copy must land before the CTA exits
+            mbar_wait(&bars->tma, 0, &dummy);
         }
-        __syncthreads();   // every thread is done with K and Q: L, T, A_O replace them
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = 4 * ti + r, j = 4 * tj + c;
-                // (P Khat^T) . Gamma_shifted: alpha_i (k_i.k_j) eta_j gamma_{i-1,j}, j < i
-                L[i * LM + j] = (j < i) ? va[i] * gk[r][c] * ve[j] * G[(i - 1) * LM + j] : 0.f;
-                // (Q Khat^T) . Gamma: (q_i.k_j) eta_j gamma_{i,j}, j <= i
-                AO[i * LM + j] = (j <= i) ? gq[r][c] * ve[j] * G[i * LM + j] : 0.f;
-                Tm[i * LM + j] = (i == j) ? 1.f : 0.f;
-            }
     }
+    {
+        // the Gram rows -> L = (P Khat^T) . Gamma_shifted (key rows) and
+        // A_O = (Q Khat^T) . Gamma (query rows), masked past the chunk end;
+        // they overwrite the tiles, which the finished MMAs no longer read
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->gram, 0, abort));
+        const int q = warp & 3, half = warp >> 2, row = 32 * q + lane;
+        if (ok) {
+            tc_fence_after();
+            float x[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + half * 32, x);
+            tmem_ld_wait();
+            if (row < kChunk) {
+                const int i = row;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    // alpha_i (k_i.k_j) eta_j gamma_{i-1,j}, j < i
+                    L[i * LM + j] = (j < i && i < n) ? va[i] * x[jj] * ve[j] * G[(i - 1) * LM + j] : 0.f;
+                }
+            } else {
+                const int i = row - kChunk;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    // (q_i.k_j) eta_j gamma_{i,j}, j <= i
+                    AO[i * LM + j] = (j <= i && i < n) ? x[jj] * ve[j] * G[i * LM + j] : 0.f;
+                }
+            }
+        }
+        for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+            const int i = idx >> 6, j = idx & 63;
+            Tm[i * LM + j] = (i == j) ? 1.f : 0.f;
+        }
+    }
+    tc_fence_before();
     __syncthreads();
+    if (warp == 1) {
+        if (lane == 0 && bars->issued) {
+            int dummy = 0;               // no MMA in flight when TMEM is freed
+            mbar_wait(&bars->gram, 0, &dummy);
+        }
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemColsPS);
+    }
 
     // ---- T = (I + L)^{-1}, blocked: diagonal 16x16 blocks by forward
     //      substitution in registers (one lane per column), then
@@ -377,11 +446,7 @@ chunk_prep_simt_kernel(ChunkProblem p) {
     //      operand [T; A_O T] of its second product as hi / lo bf16 parts in
     //      the 128-byte-swizzled layout, rows interleaved by tc_row
     unsigned char *blk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
-    float *Tg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffT);
-    float *AOTg = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffAOT);
-    float *vec = reinterpret_cast<float *>(blk + PrepLayout<float>::kOffVec);
-    static_assert(PrepLayout<float>::kOffVec == PrepLayoutTC::kSplitVec, "vector rows");
-    const bool split_tc = p.k_hi != nullptr;
+    float *vec = reinterpret_cast<float *>(blk + PrepLayoutTC::kSplitVec);
     auto put4 = [&](int op_row, int col4, const float *x) {
         // four consecutive columns col4..col4+3 = half of a 16-byte chunk
         float r[4];
@@ -415,24 +480,13 @@ chunk_prep_simt_kernel(ChunkProblem p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[r][c] += ar[r] * tc[c];
         }
-        if (split_tc) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = 4 * ti + r;
-                const float t4[4] = {Tm[i * LM + 4 * tj], Tm[i * LM + 4 * tj + 1],
-                                     Tm[i * LM + 4 * tj + 2], Tm[i * LM + 4 * tj + 3]};
-                put4(tc_row(i), 4 * tj, t4);
-                put4(tc_row(kChunk + i), 4 * tj, acc[r]);
-            }
-        } else {
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int i = 4 * ti + r, j = 4 * tj + c;
-                    AOTg[i * kChunk + j] = acc[r][c];
-                    Tg[i * kChunk + j] = Tm[i * LM + j];
-                }
+        for (int r = 0; r < 4; ++r) {
+            const int i = 4 * ti + r;
+            const float t4[4] = {Tm[i * LM + 4 * tj], Tm[i * LM + 4 * tj + 1],
+                                 Tm[i * LM + 4 * tj + 2], Tm[i * LM + 4 * tj + 3]};
+            put4(tc_row(i), 4 * tj, t4);
+            put4(tc_row(kChunk + i), 4 * tj, acc[r]);
         }
     }
     if (tid < kChunk) {
@@ -453,6 +507,7 @@ chunk_prep_simt_kernel(ChunkProblem p) {
         if (i == 3) sc = (float)n;
         vec[kVecScal * kChunk + i] = sc;
     }
+    if (tid == 0 && *abort && p.status) atomicExch(p.status, (int)MDN_ERR_DEVICE_TIMEOUT);
 }
 
 // ----------------------------------------------------- no-token calls
@@ -468,15 +523,21 @@ states_passthrough_kernel(const float *S0, const float *M0, float *S_T, float *M
     }
 }
 
-template <int D, typename Tin>
+template <int D>
 cudaError_t launch_prep_t(const ChunkProblem &p, cudaStream_t st) {
     if (p.max_chunks == 0) return cudaSuccess;
-    auto kp = chunk_prep_simt_kernel<D, Tin>;
+    CUtensorMap mkh, mqh, mkl, mql;
+    if (!make_token_map_bf16(&mkh, p.k_hi, p.T_total, p.H, D, 64) ||
+        !make_token_map_bf16(&mqh, p.q_hi, p.T_total, p.H, D, 64) ||
+        !make_token_map_bf16(&mkl, p.k_lo, p.T_total, p.H, D, 64) ||
+        !make_token_map_bf16(&mql, p.q_lo, p.T_total, p.H, D, 64))
+        return cudaErrorInvalidValue;
+    auto kp = chunk_prep_split_kernel<D>;
     cudaError_t err = cudaFuncSetAttribute(
         kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepSmem<D>::kBytes);
     if (err != cudaSuccess) return err;
     dim3 grid(p.max_chunks, p.H);
-    kp<<<grid, kThreads, PrepSmem<D>::kBytes, st>>>(p);
+    kp<<<grid, kThreads, PrepSmem<D>::kBytes, st>>>(p, mkh, mqh, mkl, mql);
     return cudaGetLastError();
 }
 
@@ -525,13 +586,12 @@ cudaError_t launch_chunk_offsets(const ChunkProblem &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// fp32 inputs, after their hi / lo parts are written (launch_split_inputs).
 cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st) {
-    if (p.D == 128) {
-        return p.dtype == MDN_BF16 ? launch_prep_t<128, __nv_bfloat16>(p, st)
-                                   : launch_prep_t<128, float>(p, st);
-    }
-    return p.dtype == MDN_BF16 ? launch_prep_t<64, __nv_bfloat16>(p, st)
-                               : launch_prep_t<64, float>(p, st);
+    if (p.dtype != MDN_F32 || (p.D != 64 && p.D != 128)) return cudaErrorInvalidValue;
+    if (p.max_chunks == 0) return cudaSuccess;
+    if (!p.k_hi || !p.q_hi || !p.k_lo || !p.q_lo) return cudaErrorInvalidValue;
+    return p.D == 128 ? launch_prep_t<128>(p, st) : launch_prep_t<64>(p, st);
 }
 
 cudaError_t launch_states_passthrough(const ChunkProblem &p, cudaStream_t st) {
