@@ -243,8 +243,8 @@ def roofline_of(x, what, tensor, ms, peaks, peak_src):
     algorithmic HBM bytes or FLOPs needs more time at the measured peak.
     bf16 inputs: the bf16 tensor peak.  fp32 inputs: the state pass's
     contractions are three bf16 products each (split operands), so its peak
-    is a third of the bf16 one; the fp32 prep runs on the CUDA cores (FFMA
-    peak)."""
+    is a third of the bf16 one; the fp32 prep's inverse and A_O T run on the
+    CUDA cores around its tcgen05 Grams, so it is held to the FFMA peak."""
     by, fl = algorithmic(x, what)
     s = ms / 1e3
     fp32 = x["dtype"] == "fp32"
@@ -772,7 +772,7 @@ def whole_job_rate(tokens_per_rank, max_ms, steps, world):
 
 
 KERNEL_SOURCES = {"chunk_prep_tc": "mdn_prep_tc.cu", "chunk_state_tc": "mdn_chunk_tc.cu",
-                  "chunk_prep_simt": "mdn_chunk_simt.cu", "chunk_state_simt": "mdn_chunk_simt.cu"}
+                  "chunk_prep_split": "mdn_chunk_simt.cu"}
 
 
 def measure_prefill(mdn, w, x, dev, args, steps, warmup, world, flush, peaks, peak_src,
@@ -795,9 +795,10 @@ def measure_prefill(mdn, w, x, dev, args, steps, warmup, world, flush, peaks, pe
     stages = {}
     for i, nm in enumerate(names):
         # the state pass is tcgen05 for every input; the prep is tcgen05 for
-        # bf16 inputs and the fp32 CUDA-core kernel for fp32 inputs
+        # bf16 inputs, and for fp32 inputs the split-operand Grams on
+        # tcgen05 around an fp32 inverse on the CUDA cores
         tc = tensor and (nm == "state" or x["dtype"] == "bf16")
-        key = "chunk_%s_%s" % (nm, "tc" if tc else "simt")
+        key = "chunk_%s_%s" % (nm, "tc" if tc else "split")
         rf = roofline_of(x, nm, tensor, r["stage_ms"][i], peaks, peak_src)
         rf["kernel"] = key
         rf["traffic"] = traffic_record(key, w.name, os.path.join(

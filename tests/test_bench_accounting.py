@@ -56,7 +56,7 @@ def test_fp32_state_pass_peak_is_a_third_of_bf16():
     r = bench.roofline_of(x, "state", True, 1e-9, peaks, "measured")   # FLOP-bound at d = 128
     assert r["bound"] == "tensor" and r["peak"] == pytest.approx(1904.9 / 3)
     p = bench.roofline_of(x, "prep", True, 1e-9, peaks, "measured")
-    assert p["bound"] == "alu"                      # the fp32 prep runs on the CUDA cores
+    assert p["bound"] == "alu"                      # the fp32 prep's inverse: CUDA cores
     # fp32 intermediates: the split prepared blocks and the q, k, v parts
     assert bench.intermediate_bytes(x) == 34816 * 32 * 2 + 2 * 3 * 2 * 2048 * 2 * 128
 
