@@ -607,6 +607,398 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     if (threadIdx.x == 0 && *abort && p.status) atomicExch(p.status, (int)MDN_ERR_DEVICE_TIMEOUT);
 }
 
+// ------------------------------------------------------------------ dual
+
+// Both 64-column slices of a head (d = 128, bf16 inputs) in one CTA, as two
+// chains A (columns 0..63) and B (64..127) whose steps interleave: while the
+// epilogue warps work on one slice's step, the tensor cores run the other
+// slice's product.  Per chunk the MMA thread issues MMA1_A, MMA1_B, MMA2_A,
+// MMA2_B, MMA3_A, MMA3_B and the epilogue runs R_A, R_B, Vres_A, Vres_B,
+// state_A, state_B, each waiting only on its own slice's barrier.  TMEM:
+// slice X owns columns [256 X, 256 X + 256): MMA1's [S | M] products at
+// +0 (MMA2's product later over their S part, once the R step has read both
+// the key and the query rows), the fp32 state [S | M] at +128.  Shared
+// memory holds one V tile (both slices' columns) apart from the double-
+// buffered [K; Q] stages: the next chunk's V is copied in once both R steps
+// have read the current one; and each slice's R sits over the S half of its
+// MMA3 operand, which is written only after MMA2 has read R and read by MMA3
+// before the next R.
+struct DualCfg {
+    static constexpr int D = 128, NS = 64;
+    static constexpr int kHalves = 2;
+    static constexpr int kEpiWarps = 16;
+    static constexpr int kThreads = 32 * (2 + kEpiWarps);
+    static constexpr uint32_t kOffPrep = kHalves * kKQHalf;          // [K; Q], then the block
+    static constexpr uint32_t kPrepBytes = (uint32_t)PrepLayoutTC::kBytes;
+    static constexpr uint32_t kPrepVec = (uint32_t)PrepLayoutTC::kOffVec;
+    static constexpr uint32_t kStageBytes = kOffPrep + kPrepBytes;
+    static_assert(kStageBytes % 1024 == 0, "stage alignment");
+    static constexpr uint32_t kOffB1 = 2 * kStageBytes;             // per slice [S | M] bf16
+    static constexpr uint32_t kB1Bytes = 2 * D * 128;
+    static constexpr uint32_t kB1M = D * 128;
+    static constexpr uint32_t kOffB3 = kOffB1 + 2 * kB1Bytes;       // per slice [gS Vres | -gM Vres];
+    static constexpr uint32_t kB3Bytes = 16384;                     // R over its S half
+    static constexpr uint32_t kB3M = 8192;
+    static constexpr uint32_t kOffV = kOffB3 + 2 * kB3Bytes;        // V, 64 tokens x 128 columns
+    static constexpr uint32_t kVTile = 2 * kVBytes;
+    static constexpr uint32_t kOffBar = kOffV + kVTile;
+    static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kSliceCols = 256;                    // per slice
+    static constexpr uint32_t kColSt = 128;                        // state, within a slice
+    static constexpr uint32_t kIdesc1 = idesc_bf16(128, 2 * NS, false, true);
+    static constexpr uint32_t kIdesc2 = idesc_bf16(128, NS, false, true);
+    static constexpr uint32_t kIdesc3 = idesc_bf16(D, 2 * NS, true, true);
+};
+
+struct DualBars {
+    uint64_t full[2], empty[2], vfull, vempty;
+    uint64_t d1[2], r[2], d2[2], v[2], d3[2], state[2];   // per slice
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(DualBars) <= 256, "barrier block");
+
+template <bool kChunkStates>
+__global__ void __launch_bounds__(DualCfg::kThreads, 1)
+chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
+    using C = DualCfg;
+    constexpr int D = C::D;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    DualBars *bars = reinterpret_cast<DualBars *>(smem + C::kOffBar);
+    volatile int *abort = &bars->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (p.cu_seqlens != nullptr) grid_dependency_wait();
+    const int kh = blockIdx.x;
+    const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
+    const int sh = s * p.H + h;
+    int start, len, slot0;
+    sequence_range(p, s, start, len, slot0);
+    const int nchunks = (len + kChunk - 1) / kChunk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->full[i], 1);
+            mbar_init(&bars->empty[i], 1 + C::kEpiWarps);
+            mbar_init(&bars->d1[i], 1);
+            mbar_init(&bars->r[i], C::kEpiWarps);
+            mbar_init(&bars->d2[i], 1);
+            mbar_init(&bars->v[i], C::kEpiWarps);
+            mbar_init(&bars->d3[i], 1);
+            mbar_init(&bars->state[i], C::kEpiWarps);
+        }
+        mbar_init(&bars->vfull, 1);
+        mbar_init(&bars->vempty, C::kEpiWarps);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&maps.k);
+        prefetch_tensormap(&maps.q);
+        prefetch_tensormap(&maps.v);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int last_use[2] = {-1, -1}, v_last = -1;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c & 1, use = c >> 1;
+                if (c == 0) grid_dependency_wait();
+                if (!mbar_wait(&bars->empty[st], (use & 1) ^ 1, abort)) break;
+                unsigned char *stage = smem + st * C::kStageBytes;
+                const int t0 = start + c * kChunk;
+                const unsigned char *blk = p.prep + ((size_t)(slot0 + c) * p.H + h) * p.prep_stride;
+                mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
+#pragma unroll
+                for (int hh = 0; hh < C::kHalves; ++hh)
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        unsigned char *dst = stage + hh * kKQHalf + g * 4096;
+                        tma_load_3d(dst, &maps.k, &bars->full[st], 64 * hh, h, t0 + 16 * g);
+                        tma_load_3d(dst + 2048, &maps.q, &bars->full[st], 64 * hh, h, t0 + 16 * g);
+                    }
+                bulk_load(stage + C::kOffPrep, blk, C::kPrepBytes, &bars->full[st]);
+                last_use[st] = use;
+                // V of this chunk, once both R steps of the previous one are done
+                if (!mbar_wait(&bars->vempty, (c & 1) ^ 1, abort)) break;
+                mbar_arrive_expect_tx(&bars->vfull, C::kVTile);
+                tma_load_3d(smem + C::kOffV, &maps.v, &bars->vfull, 0, h, t0);
+                tma_load_3d(smem + C::kOffV + kVBytes, &maps.v, &bars->vfull, 64, h, t0);
+                v_last = c;
+            }
+            for (int st = 0; st < 2; ++st) {
+                if (last_use[st] < 0) continue;
+                int dummy = 0;
+                mbar_wait(&bars->full[st], last_use[st] & 1, &dummy);
+            }
+            if (v_last >= 0) {
+                int dummy = 0;
+                mbar_wait(&bars->vfull, v_last & 1, &dummy);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        const bool l0 = lane == 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c & 1, use = c >> 1;
+            const uint32_t kq = smem_u32(smem + st * C::kStageBytes);
+            const uint32_t prep = kq + C::kOffPrep;
+            bool ok = warp_wait(&bars->full[st], use & 1, abort);
+            // MMA1 of both slices: D = [K; Q] [S | M]
+            for (int x = 0; x < 2 && ok; ++x) {
+                ok = warp_wait(&bars->state[x], c & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                if (l0) {
+                    const uint32_t b1 = smem_u32(smem + C::kOffB1 + x * C::kB1Bytes);
+#pragma unroll
+                    for (int kb = 0; kb < C::kHalves; ++kb)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sdesc_sw128(kq + kb * kKQHalf + kk * 32, 16, 1024);
+                            const uint64_t b = sdesc_sw128(b1 + (kb * 4 + kk) * 2048, C::kB1M, 1024);
+                            mma_bf16(tmem + x * C::kSliceCols, a, b, C::kIdesc1, (kb | kk) != 0);
+                        }
+                    mma_commit(&bars->d1[x]);
+                }
+                __syncwarp();
+            }
+            // MMA2 of both slices: D = [T; A_O T] R, over MMA1's S columns
+            for (int x = 0; x < 2 && ok; ++x) {
+                ok = warp_wait(&bars->r[x], c & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                if (l0) {
+                    const uint32_t rr = smem_u32(smem + C::kOffB3 + x * C::kB3Bytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(prep + kk * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(rr + kk * 2048, 8192, 1024);
+                        mma_bf16(tmem + x * C::kSliceCols, a, b, C::kIdesc2, kk != 0);
+                    }
+                    mma_commit(&bars->d2[x]);
+                }
+                __syncwarp();
+            }
+            // MMA3 of both slices: [S | M] += K^T [gS Vres | -gM Vres]
+            for (int x = 0; x < 2 && ok; ++x) {
+                ok = warp_wait(&bars->v[x], c & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                if (l0) {
+                    const uint32_t b3 = smem_u32(smem + C::kOffB3 + x * C::kB3Bytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = sdesc_sw128(kq + kk * 4096, kKQHalf, 1024);
+                        const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
+                        mma_bf16(tmem + x * C::kSliceCols + C::kColSt, a, b, C::kIdesc3, 1);
+                    }
+                    mma_commit(&bars->d3[x]);
+                    if (x == 1) mma_commit(&bars->empty[st]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+        if (l0) {
+            mma_commit(&bars->drain);
+            int dummy = 0;
+            mbar_wait(&bars->drain, 0, &dummy);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int qc = (warp - 2) >> 2;
+        const int c0 = qc * kEpiCols;                    // first column within a slice
+        const uint32_t ch0 = qc * 2;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        const int d = 32 * q + lane;                     // state row
+        const size_t st_row = (size_t)d * D + c0;        // + 64 x for slice x
+        unsigned char *b1 = smem + C::kOffB1;
+        unsigned char *b3 = smem + C::kOffB3;
+        auto st_s = [&](int x) { return lane_base + x * C::kSliceCols + C::kColSt + c0; };
+        auto st_m = [&](int x) { return lane_base + x * C::kSliceCols + C::kColSt + C::NS + c0; };
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+            float S[kEpiCols], M[kEpiCols];
+            const size_t off = (size_t)sh * D * D + st_row + 64 * x;
+#pragma unroll
+            for (int j = 0; j < kEpiCols; j += 4) {
+                float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), mv = sv;
+                if (p.S0) sv = *reinterpret_cast<const float4 *>(p.S0 + off + j);
+                if (p.M0) mv = *reinterpret_cast<const float4 *>(p.M0 + off + j);
+                S[j] = sv.x; S[j + 1] = sv.y; S[j + 2] = sv.z; S[j + 3] = sv.w;
+                M[j] = mv.x; M[j + 1] = mv.y; M[j + 2] = mv.z; M[j + 3] = mv.w;
+            }
+            tmem_st16(st_s(x), S);
+            tmem_st16(st_m(x), M);
+            tmem_st_wait();
+            if (nchunks > 0) {
+                unsigned char *bx = b1 + x * C::kB1Bytes;
+                store_row16<false>(bx, 0, d, ch0, S);
+                store_row16<false>(bx + C::kB1M, 0, d, ch0, M);
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->state[x]);
+                if (kChunkStates) store_chunk_state<D>(p, slot0, h, st_row + 64 * x, S, M);
+            }
+        }
+        const int tok = 16 * q + (lane & 15);
+        const int cg = c0 + 8 * (lane >> 4);
+        const uint32_t chk = (uint32_t)(cg >> 3);
+        const uint32_t lk = tmem + ((uint32_t)(32 * q) << 16);
+        const uint32_t lq = tmem + ((uint32_t)(32 * q + 16) << 16);
+        const size_t rs = (size_t)p.H * D;
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * D + cg;
+        __nv_bfloat16 *vg = p.vres ? static_cast<__nv_bfloat16 *>(p.vres) + (size_t)h * D + cg : nullptr;
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1, use = c >> 1;
+            unsigned char *stage = smem + st * C::kStageBytes;
+            const float *vec = reinterpret_cast<const float *>(stage + C::kOffPrep + C::kPrepVec);
+            const int n = min(kChunk, len - c * kChunk);
+            const int t0 = start + c * kChunk;
+            const bool in_chunk = tok < n;
+            ok = warp_wait(&bars->full[st], use & 1, abort) && warp_wait(&bars->vfull, c & 1, abort);
+            if (!ok) break;
+            // V of this thread's token row, both slices (zero past the chunk end)
+            uint4 vraw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+            if (in_chunk) {
+                vraw[0] = *reinterpret_cast<const uint4 *>(smem + C::kOffV + sw128_offset(tok, chk));
+                vraw[1] = *reinterpret_cast<const uint4 *>(smem + C::kOffV + kVBytes +
+                                                           sw128_offset(tok, chk));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->vempty);   // V read: the next one may land
+            const float ab = vec[kVecAbar * kChunk + tok];
+            const float cbk = in_chunk ? vec[kVecBmA * kChunk + tok] : 0.f;
+            const float abk = in_chunk ? ab : 0.f;
+            const float cbq = vec[kVecB * kChunk + tok];
+            const float gs = vec[kVecGS * kChunk + tok];
+            const float gm = vec[kVecGM * kChunk + tok];
+            float oint[2][8];
+            // ---- R and O_inter of each slice (both row sets of MMA1 read
+            //      before MMA2 may overwrite them), then the state rescale
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                ok = warp_wait(&bars->d1[x], c & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                float vv[8], xs[8], xm[8], ys[8], ym[8], r[8];
+                unpack_bf16x8(vraw[x], vv);
+                const uint32_t dx = x * C::kSliceCols;
+                tmem_ld_16x2x8(lk + dx + c0, xs);
+                tmem_ld_16x2x8(lk + dx + C::NS + c0, xm);
+                tmem_ld_16x2x8(lq + dx + c0, ys);
+                tmem_ld_16x2x8(lq + dx + C::NS + c0, ym);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    r[e] = vv[e] - abk * xs[e] + cbk * xm[e];
+                    oint[x][e] = ab * ys[e] - cbq * ym[e];
+                }
+                put8<false>(b3 + x * C::kB3Bytes, 0, tok, chk, r, 1.f);
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->r[x]);
+                rescale_state(st_s(x), st_m(x), vec);
+            }
+            if (!ok) break;
+            // ---- Vres of each slice: MMA3's B operand; O = O_inter + O_intra
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                ok = warp_wait(&bars->d2[x], c & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                float xv[8], xo[8];
+                const uint32_t dx = x * C::kSliceCols;
+                tmem_ld_16x2x8(lk + dx + c0, xv);
+                tmem_ld_16x2x8(lq + dx + c0, xo);
+                tmem_ld_wait();
+                unsigned char *bx = b3 + x * C::kB3Bytes;
+                put8<false>(bx, 0, tok, chk, xv, gs);
+                put8<false>(bx + C::kB3M, 0, tok, chk, xv, -gm);
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->v[x]);
+                if (in_chunk) {
+                    if (vg) store_out8(vg + (size_t)(t0 + tok) * rs + 64 * x, xv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xo[e] += oint[x][e];
+                    store_out8(og + (size_t)(t0 + tok) * rs + 64 * x, xo);
+                }
+            }
+            if (!ok) break;
+            // ---- new state of each slice: bf16 copy for the next MMA1
+            const bool more = c + 1 < nchunks;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                ok = warp_wait(&bars->d3[x], c & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                float S[kEpiCols], M[kEpiCols];
+                if (more) {
+                    tmem_ld16(st_s(x), S);
+                    tmem_ld16(st_m(x), M);
+                    tmem_ld_wait();
+                    unsigned char *bx = b1 + x * C::kB1Bytes;
+                    store_row16<false>(bx, 0, d, ch0, S);
+                    store_row16<false>(bx + C::kB1M, 0, d, ch0, M);
+                    fence_proxy_async();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (more) mbar_arrive(&bars->state[x]);
+                    if (x == 1) mbar_arrive(&bars->empty[st]);
+                }
+                if (kChunkStates && more) store_chunk_state<D>(p, slot0 + c + 1, h, st_row + 64 * x, S, M);
+            }
+        }
+        if (!*abort) {
+#pragma unroll 1
+            for (int x = 0; x < 2; ++x) {
+                float S[kEpiCols], M[kEpiCols];
+                tmem_ld16(st_s(x), S);
+                tmem_ld16(st_m(x), M);
+                tmem_ld_wait();
+                const size_t off = (size_t)sh * D * D + st_row + 64 * x;
+#pragma unroll
+                for (int j = 0; j < kEpiCols; j += 4) {
+                    if (p.S_T)
+                        *reinterpret_cast<float4 *>(p.S_T + off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                    if (p.M_T)
+                        *reinterpret_cast<float4 *>(p.M_T + off + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+    if (threadIdx.x == 0 && *abort && p.status) atomicExch(p.status, (int)MDN_ERR_DEVICE_TIMEOUT);
+}
+
 // ------------------------------------------------------------------ host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -669,10 +1061,43 @@ cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const Maps
 template <int D, bool kSplit>
 constexpr int kWidestSlice = (kSplit && D == 128) ? 32 : 64;
 
+template <bool kChunkStates>
+cudaError_t launch_state_dual(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
+    using C = DualCfg;
+    auto kern = chunk_state_dual_kernel<kChunkStates>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)C::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.maxThreadsPerBlock < C::kThreads) return cudaErrorLaunchOutOfResources;
+    const long blocks = (long)p.n_seq * p.H;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, maps);
+}
+
 template <int D, bool kSplit>
 cudaError_t launch_state_tc_d(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
     const long chains = (long)p.n_seq * p.H;
     const int sms = device_sm_count();
+    // bf16 at head size 128 with more 64-column slices than SMs: both slices
+    // of a head in one CTA, their steps interleaved
+    if constexpr (D == 128 && !kSplit) {
+        if (sms > 0 && chains * 2 > sms)
+            return p.S_chunks ? launch_state_dual<true>(p, st, maps) : launch_state_dual<false>(p, st, maps);
+    }
     const int ns = (sms > 0 && chains * (D / 16) <= sms) ? 16
                  : ((sms > 0 && chains * (D / 32) <= sms) || kWidestSlice<D, kSplit> == 32) ? 32
                                                                                          : 64;

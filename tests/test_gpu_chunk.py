@@ -178,9 +178,10 @@ def test_path_selection():
 @pytest.mark.parametrize("B,H", [(2, 2), (5, 5), (5, 10), (7, 11)])
 def test_slice_widths(B, H, dtype, D):
     """The tensor-core state pass picks 16-, 32- or 64-column state slices by
-    the number of (sequence, head) chains (4, 25, 50 and 77 chains here select
-    each width on a 152-SM GPU at head size 128; fp32 there stops at 32);
-    every width, head size and input type must match the oracle."""
+    the number of (sequence, head) chains (4, 25 and 50 chains here select
+    each width on a 152-SM GPU at head size 128; fp32 there stops at 32), and
+    beyond one wave of 64-column slices (77 chains, bf16, head size 128) both
+    slices of a head in one CTA; every form must match the oracle."""
     w = W.Workload("widths", dtype=dtype, state="randn", seed=16)
     x = W.make_prefill(w, B=B, T=130, H=H, D=D, with_beta=True)
     compare(x, gpu_chunk_fwd(x), chains(x))
@@ -199,3 +200,16 @@ def test_fp32_packed_with_empty_sequences():
     w = W.Workload("fp32_var", dtype="fp32", state="randn", seed=18)
     x = W.make_prefill(w, H=2, D=64, lengths=[1, 64, 0, 65, 130, 7, 0], with_beta=True)
     compare(x, gpu_chunk_fwd(x), chains(x))
+
+
+def test_dual_slices_packed_with_empty_sequences():
+    """More (sequence, head) chains than one wave of 64-column slices holds
+    (bf16, d = 128): one CTA carries both slices of a head, their steps
+    interleaved.  Packed sequences of every ragged length, empty members,
+    initial states, beta and mu = 0 entries."""
+    lengths = [1, 63, 64, 65, 0, 130, 7, 200, 0, 129] * 5
+    w = W.Workload("dual", dtype="bf16", state="randn", seed=19)
+    x = W.make_prefill(w, H=4, D=128, lengths=lengths, with_beta=True)
+    x["mu"][:, ::9] = 0.0
+    out = gpu_chunk_fwd(x)
+    compare(x, out, chains(x)[::7])

@@ -97,6 +97,13 @@ def test_chunk_states_packed_with_empty_sequences():
     _check(x)
 
 
+def test_chunk_states_dual_slices():
+    """Enough chains that both 64-column slices of a head share a CTA."""
+    w = W.Workload("cs_dual", dtype="bf16", state="randn", seed=55)
+    x = W.make_prefill(w, B=40, T=130, H=2, D=128, with_beta=True)
+    _check(x, max_chains=10)
+
+
 @pytest.mark.parametrize("dtype,D", [("fp32", 64), ("fp32", 128), ("bf16", 64)])
 def test_chunk_states_split_and_head_size_64(dtype, D):
     w = W.Workload("cs_fp32", dtype=dtype, state="randn", seed=54)

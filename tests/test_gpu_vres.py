@@ -70,6 +70,13 @@ def test_vres_small_ragged(T, dtype, D):
     _check(W.make_prefill(w, B=2, T=T, H=2, D=D, with_beta=True))
 
 
+def test_vres_dual_slices():
+    """Enough chains that both 64-column slices of a head share a CTA."""
+    w = W.Workload("vres_dual", dtype="bf16", state="randn", seed=22)
+    x = W.make_prefill(w, B=40, T=130, H=2, D=128, with_beta=True)
+    _check(x, chains(x)[::5])
+
+
 def test_vres_varlen_with_empty_sequences():
     _check(W.make_prefill(W.VARLEN_PACKED, H=2, lengths=[1, 64, 0, 65, 130, 7, 0]))
 
