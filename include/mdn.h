@@ -224,7 +224,11 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk,
  * (40)-(42)): a reverse pass over the chunks carries the state adjoints,
  * then every chunk forms its input gradients in parallel.  The gates'
  * gradients go through the chunk coefficients without dividing by a gate,
- * so mu = 0 is exact.  Arithmetic is fp32 on the CUDA cores.
+ * so mu = 0 is exact.  bf16 inputs: the reverse pass and the per-chunk
+ * products on the tensor cores (bf16 operands, fp32 accumulation; T and
+ * A_O T from the forward's own prep), the gate gradients in fp32 on the
+ * CUDA cores; relative errors a few 1e-3.  fp32 inputs: every step in fp32
+ * on the CUDA cores (relative errors near 1e-6).
  *
  * Layout and sizes as mdn_chunk_fwd (equal lengths, or packed with
  * cu_seqlens; the same device checks of cu_seqlens apply).
