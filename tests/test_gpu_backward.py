@@ -160,3 +160,13 @@ def test_deterministic():
     b = _gpu_grads(x, do, dS, dM)
     for n in NAMES:
         assert torch.equal(a[n], b[n]), n
+
+
+def test_many_chains_dual_slice_forward():
+    """Enough (sequence, head) chains that the forward's state pass carries
+    both 64-column slices of a head per CTA: the gradient from the entry
+    states that kernel saved."""
+    w = W.Workload("bwd_dual", dtype="bf16", state="randn", seed=64)
+    x = W.make_prefill(w, B=40, T=130, H=2, D=128, with_beta=True)
+    do, dS, dM = _adjoints(x, 65)
+    _compare(x, _gpu_grads(x, do, dS, dM), do, dS, dM, chains(x)[::9])

@@ -88,3 +88,50 @@ def test_decode_steps_graph_replay():
     for t in range(3):
         assert torch.equal(outs[t], ref[t])
     assert torch.equal(S, S2) and torch.equal(M, M2)
+
+
+def test_chunk_bwd_graph_replay():
+    """The gradient pass (packed sequences, bf16: the offsets, the forward's
+    prep, the coefficient, chain, chunk and gate kernels) captured once and
+    replayed on new inputs and saved states written into the captured
+    buffers: bit for bit the direct call's gradients."""
+    import momentum_delta_rule_gb300 as mdn
+    lengths = [100, 0, 257, 64, 1]
+    xs = [W.make_prefill(W.Workload("graph_bwd%d" % i, dtype="bf16", state="randn", seed=70 + i),
+                         H=2, D=128, lengths=lengths, with_beta=True) for i in range(2)]
+
+    def inputs(x):
+        d = to_dev(x)
+        _, _, _, Sc, Mc = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
+                                        d["beta"], d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"],
+                                        return_chunk_states=True)
+        g = torch.Generator(device="cuda").manual_seed(80)
+        d["do"] = torch.randn(d["v"].shape, generator=g, device="cuda").to(d["v"].dtype)
+        d["dS"] = torch.randn(d["S0"].shape, generator=g, device="cuda") * 0.1
+        d["dM"] = torch.randn(d["M0"].shape, generator=g, device="cuda") * 0.1
+        d["Sc"], d["Mc"] = Sc, Mc
+        return d
+
+    d, d2 = inputs(xs[0]), inputs(xs[1])
+    need = mdn.chunk_bwd_workspace_size(d["n_seq"], d["q"].shape[1], 2, 128, d["q"].dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = {}
+
+    def call(e):
+        return mdn.chunk_bwd(e["q"], e["k"], e["v"], e["alpha"], e["mu"], e["eta"], e["Sc"],
+                             e["Mc"], e["do"], beta=e["beta"], dS_T=e["dS"], dM_T=e["dM"],
+                             cu_seqlens=e["cu_seqlens"], workspace=ws)
+
+    def run():
+        out["g"] = call(d)
+
+    g = _capture(run)
+    for n in ("q", "k", "v", "alpha", "mu", "eta", "beta", "Sc", "Mc", "do", "dS", "dM"):
+        d[n].copy_(d2[n])
+    g.replay()
+    torch.cuda.synchronize()
+    ref = call(d2)
+    torch.cuda.synchronize()
+    for n, t in out["g"].items():
+        assert torch.equal(t, ref[n]), n
+    assert mdn.device_status() == mdn.MDN_OK
