@@ -1,4 +1,6 @@
-// MDN chunkwise gradient pass (CUDA cores, fp32 arithmetic).
+// MDN chunkwise gradient pass: the CUDA-core kernels (all of them for fp32
+// inputs, in fp32; for bf16 inputs the coefficient and gate kernels around
+// the tensor-core chain and chunk kernels).
 //
 // The pages give the storage policy of training, not the gradient formulas:
 // the forward keeps what the backward needs so that the states need not be
@@ -942,13 +944,20 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         kg<<<dim3(p.loc.max_chunks, H), kGateThreads, kGateSmem, st>>>(p);
         return cudaGetLastError();
     }
-    if (p.loc.max_chunks > 0) {
-        auto kp = bwd_prep_kernel<D, Tin>;
-        cudaError_t err = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)PrepBwdSmem<D>::kBytes);
-        if (err != cudaSuccess) return err;
-        kp<<<dim3(p.loc.max_chunks, H), 256, PrepBwdSmem<D>::kBytes, st>>>(p);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    // fp32 inputs (bf16 inputs reach here only without tokens: the chain
+    // alone passes the final-state adjoints through)
+    constexpr bool kF32 = std::is_same<Tin, float>::value;
+    if constexpr (kF32) {
+        if (p.loc.max_chunks > 0) {
+            auto kp = bwd_prep_kernel<D, Tin>;
+            cudaError_t err = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)PrepBwdSmem<D>::kBytes);
+            if (err != cudaSuccess) return err;
+            kp<<<dim3(p.loc.max_chunks, H), 256, PrepBwdSmem<D>::kBytes, st>>>(p);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
+    } else if (p.loc.max_chunks > 0) {
+        return cudaErrorInvalidValue;
     }
     {
         auto kc = bwd_chain_kernel<D, Tin>;
@@ -960,13 +969,15 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         if (blocks > 0) kc<<<(unsigned)blocks, 512, ChainSmem<D>::kBytes, st>>>(p);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    if (p.loc.max_chunks > 0) {
-        auto kk = bwd_chunk_kernel<D, Tin>;
-        cudaError_t err = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)ChunkSmem<D>::kBytes);
-        if (err != cudaSuccess) return err;
-        kk<<<dim3(p.loc.max_chunks, H), 512, ChunkSmem<D>::kBytes, st>>>(p);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if constexpr (kF32) {
+        if (p.loc.max_chunks > 0) {
+            auto kk = bwd_chunk_kernel<D, Tin>;
+            cudaError_t err = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)ChunkSmem<D>::kBytes);
+            if (err != cudaSuccess) return err;
+            kk<<<dim3(p.loc.max_chunks, H), 512, ChunkSmem<D>::kBytes, st>>>(p);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
     }
     return cudaSuccess;
 }

@@ -1,5 +1,5 @@
-// MDN chunkwise forward, the CUDA-core (FFMA) kernels around the tensor-core
-// state pass:
+// MDN chunkwise forward, the kernels around the tensor-core state pass that
+// run mostly on the CUDA cores:
 //
 //   offsets  the chunk offsets and longest-first order of packed sequences,
 //            with the device-side check of cu_seqlens;

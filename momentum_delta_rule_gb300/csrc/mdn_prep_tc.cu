@@ -1,6 +1,7 @@
 // MDN chunkwise forward — chunk-local preparation on the tensor cores
-// (bf16 inputs, head size 128).  One CTA per (chunk, head); all chunks of all
-// sequences in parallel.
+// (bf16 inputs, head size 64 or 128).  One CTA per (chunk, head); all chunks
+// of all sequences in parallel.  The gradient pass runs it too, for the same
+// T and A_O T.
 //
 // Per chunk of n <= 64 tokens ("MDN: Parallelizing Stepwise Momentum for
 // Delta Linear Attention" slides, frames "Reorder the triangular sum ..."

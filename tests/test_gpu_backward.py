@@ -170,3 +170,15 @@ def test_many_chains_dual_slice_forward():
     x = W.make_prefill(w, B=40, T=130, H=2, D=128, with_beta=True)
     do, dS, dM = _adjoints(x, 65)
     _compare(x, _gpu_grads(x, do, dS, dM), do, dS, dM, chains(x)[::9])
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_no_tokens_passes_state_adjoints_through(dtype):
+    """Sequences without tokens: nothing depends on the inputs, and the
+    initial states' gradients are the final states' adjoints unchanged."""
+    w = W.Workload("bwd_empty", dtype=dtype, state="randn", seed=66)
+    x = W.make_prefill(w, H=2, D=128, lengths=[0, 0, 0])
+    do, dS, dM = _adjoints(x, 67)
+    got = _gpu_grads(x, do, dS, dM)
+    assert got["dq"].numel() == 0
+    assert torch.equal(got["dS0"], dS) and torch.equal(got["dM0"], dM)
