@@ -180,8 +180,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                      const __grid_constant__ CUtensorMap map_q) {
     constexpr int kHalves = D / 64;           // 64-wide d_k halves of the K and Q tiles
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = align_smem_1024(smem_raw);
     BarsP *bars = reinterpret_cast<BarsP *>(smem + kOffBarP);
     volatile int *abort = &bars->abort;
     float4 *gate = reinterpret_cast<float4 *>(smem + kOffGate);   // (alpha, beta, mu, eta)
@@ -319,9 +318,11 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             // ---- Gt = Gamma Diag(eta) on the four diagonal 16-blocks: thread
             //      = (block b, column j = 16 b + jj), the column recurrence
             //      from its diagonal entry down to the block's last row
+            //      (the column is kept in registers and stored after the
+            //      loop, so no gate load waits behind a store)
             const int t = tid - 64, blk = t >> 4, j = 16 * blk + (t & 15);
             const float et = gate[j].w;
-            float m = 0.f, g = 0.f;
+            float m = 0.f, g = 0.f, col[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const int r = 16 * blk + rr;
@@ -329,8 +330,11 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
                 const bool diag = (r == j);
                 m = diag ? et : gr.z * m;
                 g = (diag ? 0.f : gr.x * g) + gr.y * m;
-                if (r >= j) Gt[r * LM + j] = g;
+                col[rr] = g;
             }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                if (16 * blk + rr >= j) Gt[(16 * blk + rr) * LM + j] = col[rr];
         } else {
             // ---- column factors c_j^(s) = eta_j prod_{u=j+1}^{r0-1} mu_u for
             //      the columns j < r0 = 16 s left of segment s, from the
@@ -386,8 +390,11 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
             const float *src = Gt + (r0 - 1) * LM + j0;
             float *dst = Gt + r * LM + j0;
+            float sv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] = F * src[e] + c[e] * lam;
+            for (int e = 0; e < 8; ++e) sv[e] = src[e];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = F * sv[e] + c[e] * lam;
         }
     }
     __syncthreads();   // Gt complete

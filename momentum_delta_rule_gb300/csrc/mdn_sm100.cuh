@@ -19,6 +19,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to 1024 bytes (the 128-byte
+// swizzle's period), formed as an offset from the array itself so that the
+// compiler still sees shared-memory accesses through the result (a round trip
+// through an integer would leave it a generic pointer).
+__device__ __forceinline__ unsigned char *align_smem_1024(unsigned char *raw) {
+    const uint32_t a = smem_u32(raw);
+    return raw + (((a + 1023u) & ~1023u) - a);
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
