@@ -215,8 +215,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const __grid_constant__ CUtensorMap map_gam) {
     using G = GradCfg<D>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = align_smem_1024(smem_raw);
     GradBars *bars = reinterpret_cast<GradBars *>(smem + G::kOffBar);
     volatile int *abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -204,8 +204,7 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_o) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = align_smem_1024(smem_raw);
     using C = ChainCfg<D, NS>;
     ChainBars *bars = reinterpret_cast<ChainBars *>(smem + C::kOffBar);
     volatile int *abort = &bars->abort;

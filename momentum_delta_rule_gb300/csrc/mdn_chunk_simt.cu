@@ -189,8 +189,7 @@ chunk_prep_split_kernel(ChunkProblem p, const __grid_constant__ CUtensorMap map_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *base = align_smem_1024(smem_raw);
     float *L = reinterpret_cast<float *>(base);      // system matrix (strict lower), after the Grams
     float *Tm = L + kChunk * LM;           // its inverse
     float *AO = Tm + kChunk * LM;          // output operator (lower)

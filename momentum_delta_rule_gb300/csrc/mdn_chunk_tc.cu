@@ -234,8 +234,7 @@ template <int D, int NS, bool kChunkStates, bool kSplit>
 __global__ void __launch_bounds__(Cfg<D, NS, kSplit>::kThreads, 1)
 chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = align_smem_1024(smem_raw);
     using C = Cfg<D, NS, kSplit>;
     using Tio = typename std::conditional<kSplit, float, __nv_bfloat16>::type;
     constexpr int kStages = C::kStages;
@@ -667,8 +666,7 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
     using C = DualCfg;
     constexpr int D = C::D;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = align_smem_1024(smem_raw);
     DualBars *bars = reinterpret_cast<DualBars *>(smem + C::kOffBar);
     volatile int *abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

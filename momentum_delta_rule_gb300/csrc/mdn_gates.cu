@@ -165,8 +165,7 @@ prepare_inputs_stream_kernel(InputsProblem p, long ntiles) {
     constexpr int kPer = kPackets / (32 * kStreamComputeWarps);
     static_assert(kPackets % (32 * kStreamComputeWarps) == 0, "tile split");
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = sm100::align_smem_1024(smem_raw);
     StreamBars *bars = reinterpret_cast<StreamBars *>(smem + 4 * kTileBytes);
     volatile int *abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
