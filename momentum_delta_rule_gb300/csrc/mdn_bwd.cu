@@ -87,7 +87,7 @@ bwd_prep_kernel(const BwdProblem p) {
 
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     ChunkLoc loc;
-    if (!locate_chunk(p.loc, gc, loc)) return;
+    if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n, H = p.loc.H;
     if (tid < C) {
         float a = 1.f, m = 0.f, e = 0.f, b = 0.f;
@@ -221,7 +221,7 @@ bwd_vec_kernel(const BwdProblem p) {
     __shared__ float ga[C], gm[C], ge[C], gb[C], vec[BL::kRows * C];
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
-    if (!locate_chunk(p.loc, gc, loc)) return;
+    if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n;
     if (tid < C) {
         float a = 1.f, m = 0.f, e = 0.f, b = 0.f;
@@ -599,7 +599,7 @@ bwd_chunk_kernel(const BwdProblem p) {
 
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
-    if (!locate_chunk(p.loc, gc, loc)) return;
+    if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n, t0 = loc.t0;
     const float *blk = bwd_block(p, gc, h);
     load_kq<D, Tin>(p, t0, n, h, Kf, Qf);
@@ -867,7 +867,7 @@ bwd_gates_kernel(const BwdProblem p) {
     float *rowacc = mtl + C;
     const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
-    if (!locate_chunk(p.loc, gc, loc)) return;
+    if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n, t0 = loc.t0;
     const float *blk = bwd_block(p, gc, h);
     const float *ra = blk + BL::kA * BL::kMat;

@@ -221,7 +221,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gc = blockIdx.x, h = blockIdx.y, H = p.loc.H;
     ChunkLoc loc;
-    if (!locate_chunk(p.loc, gc, loc)) return;      // the whole CTA, before any barrier
+    if (!locate_chunk_cta(p.loc, gc, loc)) return;      // the whole CTA, before any barrier
     const int n = loc.n, t0 = loc.t0;
     float *blk = reinterpret_cast<float *>(p.prep + ((size_t)gc * H + h) * BL::kBytes);
 

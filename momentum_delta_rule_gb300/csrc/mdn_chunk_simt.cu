@@ -184,7 +184,7 @@ chunk_prep_split_kernel(ChunkProblem p, const __grid_constant__ CUtensorMap map_
     constexpr int LM = SM::LM;
     const int gc = blockIdx.x, h = blockIdx.y;
     ChunkLoc loc;
-    if (!locate_chunk(p, gc, loc)) return;
+    if (!locate_chunk_cta(p, gc, loc)) return;
     const int n = loc.n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 

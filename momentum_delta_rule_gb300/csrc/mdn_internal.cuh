@@ -246,6 +246,29 @@ __device__ __forceinline__ bool locate_chunk(const ChunkProblem &p, int gc,
     return true;
 }
 
+// locate_chunk for a whole CTA at once (every thread calls it; uniform
+// result): for packed sequences the containing sequence is the count of
+// chunk offsets at or below gc, taken in one round of parallel loads per
+// blockDim.x sequences instead of a chain of dependent loads.
+__device__ __forceinline__ bool locate_chunk_cta(const ChunkProblem &p, int gc, ChunkLoc &loc) {
+    if (p.cu_seqlens == nullptr) return locate_chunk(p, gc, loc);
+    const int32_t *off = p.chunk_offsets;
+    const int total = off[p.n_seq];
+    int lo = 0;
+    for (int base = 1; base < p.n_seq; base += blockDim.x) {
+        const int s = base + (int)threadIdx.x;
+        lo += __syncthreads_count(s < p.n_seq && off[s] <= gc);
+    }
+    if (gc >= total) return false;
+    const int start = p.cu_seqlens[lo];
+    const int len = p.cu_seqlens[lo + 1] - start;
+    const int c = gc - off[lo];
+    loc.seq = lo;
+    loc.t0 = start + c * kChunk;
+    loc.n = min(kChunk, len - c * kChunk);
+    return true;
+}
+
 // The state pass walks sequences longest first when an order is given, so the
 // longest chains start in the first wave (longest-processing-time order).
 __device__ __forceinline__ int ordered_sequence(const ChunkProblem &p, int k) {

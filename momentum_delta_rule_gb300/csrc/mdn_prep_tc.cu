@@ -200,7 +200,7 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     grid_launch_dependents();
     const int gc = blockIdx.x, h = blockIdx.y;
     ChunkLoc loc;
-    if (!locate_chunk(p, gc, loc)) return;
+    if (!locate_chunk_cta(p, gc, loc)) return;
     const int n = loc.n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned char *pblk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
@@ -351,50 +351,46 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             }
         }
         asm volatile("bar.sync 2, 224;" ::: "memory");
-        // Left of the diagonal blocks the recurrence is affine in the
-        // segment's start row:  Gt_{r,j} = F_s(r) Gt_{r0-1,j} + c_j^(s)
-        // lambda_s(r)  (j < r0, every term non-negative).  Rows 31 and 47
-        // first, in order (the next segments start from them) ...
-        if (warp == 2 || warp == 3) {
-            const int j = tid - 64;
-            float e = Gt[15 * LM + j];
-            if (j < 16) {
-                e = vec[vF * kChunk + 31] * e + vec[vC * kChunk + j] * vec[vLam * kChunk + 31];
-                Gt[31 * LM + j] = e;
-            } else if (j < 32) {
-                e = Gt[31 * LM + j];
-            }
-            if (j < 32)
-                Gt[47 * LM + j] = vec[vF * kChunk + 47] * e +
-                                  vec[(vC + 1) * kChunk + j] * vec[vLam * kChunk + 47];
-        }
-        asm volatile("bar.sync 2, 224;" ::: "memory");
-        // ... then every other entry left of the diagonal blocks at once,
-        // one thread per (row, 8 columns): segment 1 rows 16..30 x 2 groups,
-        // segment 2 rows 32..46 x 4, segment 3 rows 48..63 x 6
-        if (t7 < 30 + 60 + 96) {
+        // Left of the diagonal blocks the recurrence is affine in a segment's
+        // start row:  Gt_{r,j} = F_s(r) Gt_{r0-1,j} + c_j^(s) lambda_s(r)
+        // (j < r0, every term non-negative).  Row r0 - 1 is itself in the
+        // diagonal block of column j or follows from an earlier segment the
+        // same way, so each entry is reached from the last row of its
+        // column's diagonal block through whole segments (factors F and
+        // lambda at the segment's last row) and then its own segment: one
+        // thread per (row, 8 columns), segment 1 rows 16..31 x 2 groups,
+        // segment 2 rows 32..47 x 4, segment 3 rows 48..63 x 6
+        if (t7 < 32 + 64 + 96) {
             int sg, r, jg;
-            if (t7 < 30) {
+            if (t7 < 32) {
                 sg = 1; r = 16 + (t7 >> 1); jg = t7 & 1;
-            } else if (t7 < 90) {
-                const int k = t7 - 30;
+            } else if (t7 < 96) {
+                const int k = t7 - 32;
                 sg = 2; r = 32 + (k >> 2); jg = k & 3;
             } else {
-                const int k = t7 - 90;
+                const int k = t7 - 96;
                 sg = 3; r = 48 + k / 6; jg = k - (k / 6) * 6;
             }
-            const int r0 = 16 * sg, j0 = 8 * jg;
+            const int j0 = 8 * jg, tb = j0 >> 4;
+            const float *src = Gt + (16 * tb + 15) * LM + j0;
+            float e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) e[k] = src[k];
+            for (int u = tb + 1; u < sg; ++u) {
+                const float Fu = vec[vF * kChunk + 16 * u + 15], Lu = vec[vLam * kChunk + 16 * u + 15];
+                const float4 c0 = *reinterpret_cast<const float4 *>(vec + (vC + u - 1) * kChunk + j0);
+                const float4 c1 = *reinterpret_cast<const float4 *>(vec + (vC + u - 1) * kChunk + j0 + 4);
+                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) e[k] = Fu * e[k] + c[k] * Lu;
+            }
             const float F = vec[vF * kChunk + r], lam = vec[vLam * kChunk + r];
             const float4 c0 = *reinterpret_cast<const float4 *>(vec + (vC + sg - 1) * kChunk + j0);
             const float4 c1 = *reinterpret_cast<const float4 *>(vec + (vC + sg - 1) * kChunk + j0 + 4);
             const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            const float *src = Gt + (r0 - 1) * LM + j0;
             float *dst = Gt + r * LM + j0;
-            float sv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sv[e] = src[e];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] = F * sv[e] + c[e] * lam;
+            for (int k = 0; k < 8; ++k) dst[k] = F * e[k] + c[k] * lam;
         }
     }
     __syncthreads();   // Gt complete
@@ -472,8 +468,10 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
     //      N^4 = 0):  I + L = (I + L_d)(I + N)  and
     //      T = (I + N)^{-1} D = D - N D + N^2 D - N^3 D.
     //      D by forward substitution in registers (one lane per column of a
-    //      block), then three MMAs, each epilogue writing the next bf16
-    //      operands.
+    //      block), written in fp32 over L_d and in bf16 (row-major) as an MMA
+    //      operand while the other warps zero that operand outside the
+    //      diagonal blocks; then three MMAs, each epilogue writing the next
+    //      bf16 operands.
     if (warp < 2) {
         const int blk = warp * 2 + (lane >> 4);
         const int c = lane & 15;
@@ -489,22 +487,21 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
             for (int r = k + 1; r < 16; ++r) t[r] = fmaf(-lb[r * LB + k], t[k], t[r]);
         asm volatile("bar.sync 1, 64;" ::: "memory");    // every lane has read its block of L
         float *db = Ldg + blk * 16 * LB;                  // D replaces L_d in place
+        const int col = 16 * blk + c;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) db[r * LB + c] = t[r];
-    }
-    __syncthreads();
-    // D in bf16, row-major (zero outside the diagonal blocks)
-    for (int idx = tid; idx < kChunk * 8; idx += kThreadsP) {
-        const int r = idx >> 3, c = idx & 7;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if ((c >> 1) == (r >> 4)) {
-            const float *src = Ldg + ((r >> 4) * 16 + (r & 15)) * LB + 8 * (c & 1);
-            w.x = pack2(src[0], src[1]);
-            w.y = pack2(src[2], src[3]);
-            w.z = pack2(src[4], src[5]);
-            w.w = pack2(src[6], src[7]);
+        for (int r = 0; r < 16; ++r) {
+            db[r * LB + c] = t[r];
+            *reinterpret_cast<__nv_bfloat16 *>(Dbf + sw128_offset(16 * blk + r, (uint32_t)(col >> 3)) +
+                                               2 * (col & 7)) = __float2bfloat16_rn(t[r]);
         }
-        *reinterpret_cast<uint4 *>(Dbf + sw128_offset(r, c)) = w;
+    } else {
+        // the 16-byte pieces of D off its diagonal blocks: rows r, pieces
+        // cc with cc / 2 != r / 16 (six per row)
+        for (int idx = tid - 64; idx < kChunk * 6; idx += kThreadsP - 64) {
+            const int r = idx / 6, k = idx - (idx / 6) * 6;
+            const int cc = k + (k >= 2 * (r >> 4) ? 2 : 0);
+            *reinterpret_cast<uint4 *>(Dbf + sw128_offset(r, cc)) = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     fence_proxy_async();
     tc_fence_before();
