@@ -508,15 +508,16 @@ def bwd_flops_per_token_head(d, C=64):
 def bwd_bytes(x):
     """Algorithmic HBM bytes of one gradient pass: q, k, v and dO read, dq,
     dk, dv written (input dtype); the four gates read and their gradients
-    written (fp32); every chunk's entry states read (fp32, the saved data);
-    the final-state adjoints read and dS0, dM0 written (fp32)."""
+    written (fp32); every chunk's entry states read (the saved data, in the
+    input dtype); the final-state adjoints read and dS0, dM0 written
+    (fp32)."""
     lens = seq_lengths(x)
     th = sum(lens) * x["H"]
     D = x["D"]
     el = 4 if x["dtype"] == "fp32" else 2
     chunks = sum((n + 63) // 64 for n in lens) * x["H"]
     seq_heads = len(lens) * x["H"]
-    return (7 * th * D * el + 8 * th * 4 + chunks * 2 * D * D * 4 +
+    return (7 * th * D * el + 8 * th * 4 + chunks * 2 * D * D * el +
             seq_heads * 4 * D * D * 4)
 
 

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MDN_ABI_VERSION 1
+#define MDN_ABI_VERSION 2
 
 typedef enum mdn_status {
     MDN_OK = 0,
@@ -176,14 +176,18 @@ size_t mdn_chunk_state_slots(int n_seq, int B, int T, int packed);
  * the sequence.
  *
  * Arguments as mdn_chunk_fwd, plus
- *   S_chunks, M_chunks  fp32 outputs [slots, H, dk, dv], slots at least
+ *   S_chunks, M_chunks  outputs [slots, H, dk, dv] (row-major) in the
+ *          input precision: bf16 for bf16 inputs (the gradient pass uses
+ *          them as bf16 tensor-core operands, so nothing it reads is
+ *          lost), fp32 for fp32 inputs.  slots at least
  *          mdn_chunk_state_slots(...), both required when B * T > 0,
  *          16-byte aligned, overlapping no other argument.  Chunk c of
  *          sequence s sits at slot s * ceil(T / 64) + c (equal lengths) or
  *          off_s + c with off_s = sum_{s' < s} ceil(L_{s'} / 64) (packed);
  *          other slots are not written.
- * Memory: 2 * dk * dv * 4 bytes per (chunk, head), 128 KiB at d = 128, i.e.
- * 2 KiB per (token, head) against 768 B for that token's bf16 q, k and v.
+ * Memory: 2 * dk * dv * (2 or 4) bytes per (chunk, head): 64 KiB at d = 128
+ * for bf16 inputs, i.e. 1 KiB per (token, head) against 768 B for that
+ * token's q, k and v.
  * Errors: as mdn_chunk_fwd; MDN_ERR_INVALID_ARG for a missing, misaligned
  * or aliasing state output.  o, S_T and M_T are the values mdn_chunk_fwd
  * writes.
@@ -191,8 +195,8 @@ size_t mdn_chunk_state_slots(int n_seq, int B, int T, int packed);
 mdn_status mdn_chunk_fwd_states(const void *q, const void *k, const void *v,
                                 const float *alpha, const float *mu, const float *eta,
                                 const float *beta, const float *S0, const float *M0,
-                                void *o, float *S_T, float *M_T, float *S_chunks,
-                                float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                                void *o, float *S_T, float *M_T, void *S_chunks,
+                                void *M_chunks, const int32_t *cu_seqlens, int n_seq,
                                 int B, int T, int H, int dk, int dv, mdn_dtype dtype,
                                 int chunk, void *workspace, size_t workspace_bytes,
                                 void *stream);
@@ -236,7 +240,8 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk,
  *   q, k, v, alpha, mu, eta, beta   the forward's inputs (beta NULL: 1)
  *   S_chunks, M_chunks   the forward's chunk entry states, exactly as
  *                  mdn_chunk_fwd_states wrote them for these inputs and
- *                  initial states (fp32 [slots, H, dk, dv])
+ *                  initial states ([slots, H, dk, dv], bf16 or fp32 as
+ *                  the inputs)
  *   dout           adjoint of o (dtype, laid out like o); required
  *   dS_T, dM_T     adjoints of the final states (fp32 [n_seq, H, dk, dv]) or
  *                  NULL for zero
@@ -254,8 +259,8 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk,
  */
 mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v,
                          const float *alpha, const float *mu, const float *eta,
-                         const float *beta, const float *S_chunks,
-                         const float *M_chunks, const void *dout,
+                         const float *beta, const void *S_chunks,
+                         const void *M_chunks, const void *dout,
                          const float *dS_T, const float *dM_T, void *dq,
                          void *dk_out, void *dv_out, float *dalpha, float *dmu,
                          float *deta, float *dbeta, float *dS0, float *dM0,

@@ -183,8 +183,9 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
     ``output_final_state`` is False.  With ``return_vres`` (or a ``vres``
     buffer shaped like v) the per-token residuals come fourth.  With
     ``return_chunk_states`` (or ``S_chunks``/``M_chunks`` buffers of
-    ``[chunk_state_slots(...), H, D, D]`` fp32) the entry states of every
-    chunk come fourth and fifth (``mdn_chunk_fwd_states``).
+    ``[chunk_state_slots(...), H, D, D]`` in the dtype of q) the entry
+    states of every chunk come fourth and fifth (``mdn_chunk_fwd_states``;
+    bf16 for bf16 inputs, as the gradient pass reads them).
     """
     L = lib()
     if q.dim() != 4:
@@ -238,8 +239,8 @@ def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,
         for name in ("S_chunks", "M_chunks"):
             t = S_chunks if name == "S_chunks" else M_chunks
             if t is None:
-                t = torch.empty((max(slots, 1), H, D, D), dtype=torch.float32, device=dev)
-            _check_cuda(name, t, torch.float32, dev)
+                t = torch.empty((max(slots, 1), H, D, D), dtype=q.dtype, device=dev)
+            _check_cuda(name, t, q.dtype, dev)
             if t.dim() != 4 or t.shape[0] < slots or tuple(t.shape[1:]) != (H, D, D):
                 raise ValueError("%s must be [>= %d, H, D, D]" % (name, slots))
             if name == "S_chunks":
@@ -400,7 +401,7 @@ def chunk_bwd(q, k, v, alpha, mu, eta, S_chunks, M_chunks, dout, beta=None,
         n_seq = B
     slots = chunk_state_slots(n_seq, B, T, cu_seqlens is not None)
     for name, t in (("S_chunks", S_chunks), ("M_chunks", M_chunks)):
-        _check_cuda(name, t, torch.float32, dev)
+        _check_cuda(name, t, q.dtype, dev)
         if t.dim() != 4 or t.shape[0] < slots or tuple(t.shape[1:]) != (H, D, D):
             raise ValueError("%s must be [>= %d, H, D, D]" % (name, slots))
     for name, t in (("dS_T", dS_T), ("dM_T", dM_T)):

@@ -121,8 +121,8 @@ namespace mdn {
 mdn_status chunk_fwd_check(const void *q, const void *k, const void *v, const float *alpha,
                            const float *mu, const float *eta, const float *beta,
                            const float *S0, const float *M0, const void *o, const float *S_T,
-                           const float *M_T, const void *vres, const float *S_chunks,
-                           const float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                           const float *M_T, const void *vres, const void *S_chunks,
+                           const void *M_chunks, const int32_t *cu_seqlens, int n_seq,
                            int B, int T, int H, int dk, int dv, mdn_dtype dtype, int chunk,
                            int **status) {
     // ---- shapes
@@ -166,7 +166,7 @@ mdn_status chunk_fwd_impl(
     const void *q, const void *k, const void *v, const float *alpha,
     const float *mu, const float *eta, const float *beta, const float *S0,
     const float *M0, void *o, float *S_T, float *M_T, void *vres,
-    float *S_chunks, float *M_chunks,
+    void *S_chunks, void *M_chunks,
     const int32_t *cu_seqlens, int n_seq, int B, int T, int H, int dk, int dv,
     mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
     void *stream, void *const *stage_events, int n_stage_events,
@@ -309,8 +309,8 @@ size_t mdn_chunk_state_slots(int n_seq, int B, int T, int packed) {
 mdn_status mdn_chunk_fwd_states(const void *q, const void *k, const void *v,
                                 const float *alpha, const float *mu, const float *eta,
                                 const float *beta, const float *S0, const float *M0,
-                                void *o, float *S_T, float *M_T, float *S_chunks,
-                                float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                                void *o, float *S_T, float *M_T, void *S_chunks,
+                                void *M_chunks, const int32_t *cu_seqlens, int n_seq,
                                 int B, int T, int H, int dk, int dv, mdn_dtype dtype,
                                 int chunk, void *workspace, size_t workspace_bytes,
                                 void *stream) {
@@ -426,7 +426,7 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk, int d
 
 mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
                          const float *mu, const float *eta, const float *beta,
-                         const float *S_chunks, const float *M_chunks, const void *dout,
+                         const void *S_chunks, const void *M_chunks, const void *dout,
                          const float *dS_T, const float *dM_T, void *dq, void *dk_out,
                          void *dv_out, float *dalpha, float *dmu, float *deta, float *dbeta,
                          float *dS0, float *dM0, const int32_t *cu_seqlens, int n_seq, int B,

@@ -85,7 +85,9 @@ bwd_prep_kernel(const BwdProblem p) {
     float *G = Qf + C * LD, *X = G + C * LP, *Y = X + C * LP, *Tm = Y + C * LP;
     float *ga = Tm + C * LP, *gm = ga + C, *ge = gm + C, *gb = ge + C, *vec = gb + C;
 
-    const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    int gc, h;
+    chunk_head_of_block(p.loc.H, gc, h);
+    const int tid = threadIdx.x;
     ChunkLoc loc;
     if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n, H = p.loc.H;
@@ -219,7 +221,9 @@ __global__ void __launch_bounds__(128)
 bwd_vec_kernel(const BwdProblem p) {
     using CL = BwdChainLayout;
     __shared__ float ga[C], gm[C], ge[C], gb[C], vec[BL::kRows * C];
-    const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
+    int gc, h;
+    chunk_head_of_block(p.loc.H, gc, h);
+    const int tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
     if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n;
@@ -597,7 +601,9 @@ bwd_chunk_kernel(const BwdProblem p) {
     float *S0s = U, *M0s = S0s + D * LS, *dSs = M0s + D * LS, *dMs = dSs + D * LS;
     float *Vs = dMs + D * LS, *dOs = Vs + C * LS, *dRs = dOs + C * LS, *Rs = dRs + C * LS;
 
-    const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
+    int gc, h;
+    chunk_head_of_block(p.loc.H, gc, h);
+    const int tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
     if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n, t0 = loc.t0;
@@ -643,7 +649,8 @@ bwd_chunk_kernel(const BwdProblem p) {
         for (int idx = tid; idx < D * NSB; idx += blockDim.x) {
             const int k = idx / NSB, j = idx - k * NSB;
             const size_t g = (size_t)k * D + c0 + j;
-            const float s0 = p.S_chunks[sbase + g], m0 = p.M_chunks[sbase + g];
+            const float s0 = static_cast<const float *>(p.S_chunks)[sbase + g];
+            const float m0 = static_cast<const float *>(p.M_chunks)[sbase + g];
             const float ds = adj[g], dm = adj[(size_t)D * D + g];
             S0s[k * LS + j] = s0;
             M0s[k * LS + j] = m0;
@@ -865,7 +872,9 @@ bwd_gates_kernel(const BwdProblem p) {
     float *dG = sm, *scr = dG + C * LP;
     float *ga = scr + kGateScratch, *gm = ga + C, *gb = gm + C, *abm = gb + C, *mtl = abm + C;
     float *rowacc = mtl + C;
-    const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.loc.H;
+    int gc, h;
+    chunk_head_of_block(p.loc.H, gc, h);
+    const int tid = threadIdx.x, H = p.loc.H;
     ChunkLoc loc;
     if (!locate_chunk_cta(p.loc, gc, loc)) return;
     const int n = loc.n, t0 = loc.t0;
@@ -931,9 +940,11 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         fp.alpha = p.alpha; fp.mu = p.mu; fp.eta = p.eta; fp.beta = p.beta;
         fp.prep = p.tcblk;
         fp.prep_stride = BwdChainLayout::kBytes;
+        dim3 cg;
+        if (!chunk_head_grid(p.loc.max_chunks, H, cg)) return cudaErrorInvalidConfiguration;
         cudaError_t err = launch_chunk_prep_tc(fp, st);
         if (err != cudaSuccess) return err;
-        bwd_vec_kernel<<<dim3(p.loc.max_chunks, H), 128, 0, st>>>(p);
+        bwd_vec_kernel<<<cg, 128, 0, st>>>(p);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
         if ((err = launch_bwd_chain_tc(p, st)) != cudaSuccess) return err;
         if ((err = launch_bwd_chunk_tc(p, st)) != cudaSuccess) return err;
@@ -941,7 +952,7 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         if ((err = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kGateSmem)) != cudaSuccess)
             return err;
-        kg<<<dim3(p.loc.max_chunks, H), kGateThreads, kGateSmem, st>>>(p);
+        kg<<<cg, kGateThreads, kGateSmem, st>>>(p);
         return cudaGetLastError();
     }
     // fp32 inputs (bf16 inputs reach here only without tokens: the chain
@@ -953,7 +964,9 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
             cudaError_t err = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)PrepBwdSmem<D>::kBytes);
             if (err != cudaSuccess) return err;
-            kp<<<dim3(p.loc.max_chunks, H), 256, PrepBwdSmem<D>::kBytes, st>>>(p);
+            dim3 cg;
+            if (!chunk_head_grid(p.loc.max_chunks, H, cg)) return cudaErrorInvalidConfiguration;
+            kp<<<cg, 256, PrepBwdSmem<D>::kBytes, st>>>(p);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     } else if (p.loc.max_chunks > 0) {
@@ -975,7 +988,9 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
             cudaError_t err = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)ChunkSmem<D>::kBytes);
             if (err != cudaSuccess) return err;
-            kk<<<dim3(p.loc.max_chunks, H), 512, ChunkSmem<D>::kBytes, st>>>(p);
+            dim3 cg;
+            if (!chunk_head_grid(p.loc.max_chunks, H, cg)) return cudaErrorInvalidConfiguration;
+            kk<<<cg, 512, ChunkSmem<D>::kBytes, st>>>(p);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }

@@ -8,7 +8,8 @@
 // unknown residuals with a lower triangular system", Eqs. (15)-(18), and
 // "Chunk outputs combine incoming states and local writes", Appendix C
 // Eqs. (40)-(42)), with P = Diag(alpha) K, Kh = Diag(eta) K and the chunk's
-// entry states S0, M0, as seven products over operands in their stored
+// entry states S0, M0 (saved by the forward in bf16, copied straight into
+// their operand tiles), as seven products over operands in their stored
 // layouts (the [K; Q] and [dO; dR] tiles in the tc_row order):
 //
 //   MMA1  [K; Q] S0, [K; Q] M0   R  = V - Diag(abar_m) P S0 + Diag(b_m) P M0
@@ -95,10 +96,10 @@ struct GradCfg {
     static constexpr uint32_t kColG = 3 * D + 64 > 4 * D - 64 ? 4 * D : 3 * D + 64;  // Gram, 64 columns
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kThreads = 320;
-    // the entry states arrive as fp32 (bulk copies, D x D x 4 bytes each):
-    // S0 over the S0 and M0 tiles' regions, M0 over the dS and dM tiles'
-    static constexpr uint32_t kStateF32 = 2 * kState;
-    static constexpr uint32_t kTxBytes = 2 * kStage + kTok + 2 * kStateF32;
+    // copies: [K; Q] and the entry-state tiles (MMA1); [dO; dR] and V (MMA3,
+    // the first epilogue); the adjoint tiles (MMA4)
+    static constexpr uint32_t kTxFull = kStage + 2 * kState;
+    static constexpr uint32_t kTxO = kStage + kTok;
     static constexpr uint32_t kTxAdj = 2 * kState;
     static constexpr uint32_t kTx2Bytes = kHalf + kTok;
     static_assert(kColG + 64 <= kTmemCols, "TMEM columns");
@@ -112,7 +113,7 @@ struct GradCfg {
 };
 
 struct GradBars {
-    uint64_t full, fulla, full2, full3, rd, st, d13, r, d2, v, d45, y, d67, drain;
+    uint64_t full, fullo, fulla, full2, full3, rd, d13, r, d2, v, d45, y, d67, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -179,13 +180,6 @@ __device__ __forceinline__ void get_w(const unsigned char *box, int t, int cc, f
     }
 }
 
-__device__ __forceinline__ void load8(const float *g, float *x) {
-    const float4 a = *reinterpret_cast<const float4 *>(g);
-    const float4 b = *reinterpret_cast<const float4 *>(g + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
 __device__ __forceinline__ void store16_bf16(void *g, const float *x) {
     uint4 *d = reinterpret_cast<uint4 *>(g);
     d[0] = make_uint4(pk2(x[0], x[1]), pk2(x[2], x[3]), pk2(x[4], x[5]), pk2(x[6], x[7]));
@@ -212,14 +206,18 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const __grid_constant__ CUtensorMap map_dk,
                     const __grid_constant__ CUtensorMap map_wy,
                     const __grid_constant__ CUtensorMap map_wx,
-                    const __grid_constant__ CUtensorMap map_gam) {
+                    const __grid_constant__ CUtensorMap map_gam,
+                    const __grid_constant__ CUtensorMap map_s0,
+                    const __grid_constant__ CUtensorMap map_m0) {
     using G = GradCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = align_smem_1024(smem_raw);
     GradBars *bars = reinterpret_cast<GradBars *>(smem + G::kOffBar);
     volatile int *abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gc = blockIdx.x, h = blockIdx.y, H = p.loc.H;
+    int gc, h;
+    chunk_head_of_block(p.loc.H, gc, h);
+    const int H = p.loc.H;
     ChunkLoc loc;
     if (!locate_chunk_cta(p.loc, gc, loc)) return;      // the whole CTA, before any barrier
     const int n = loc.n, t0 = loc.t0;
@@ -227,11 +225,11 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->full, 1);
+        mbar_init(&bars->fullo, 1);
         mbar_init(&bars->fulla, 1);
         mbar_init(&bars->rd, 8);
         mbar_init(&bars->full2, 1);
         mbar_init(&bars->full3, 1);
-        mbar_init(&bars->st, 8);
         mbar_init(&bars->d13, 1);
         mbar_init(&bars->r, 8);
         mbar_init(&bars->d2, 1);
@@ -251,6 +249,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         prefetch_tensormap(&map_v);
         prefetch_tensormap(&map_kt);
         prefetch_tensormap(&map_gam);
+        prefetch_tensormap(&map_s0);
+        prefetch_tensormap(&map_m0);
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, G::kTmemCols);
@@ -264,8 +264,11 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->full, G::kTxBytes);
+            mbar_arrive_expect_tx(&bars->full, G::kTxFull);
             unsigned char *kq = smem + G::kOffKQ, *orr = smem + G::kOffOR;
+            const int bi = gc * H + h;
+            // [K; Q] and the chunk's entry states (bf16 [dk, dv] rows; the
+            // copy lays them out as the swizzled MN-major operand tiles)
 #pragma unroll
             for (int hh = 0; hh < G::kHalves; ++hh) {
 #pragma unroll
@@ -273,29 +276,33 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     const uint32_t off = hh * kHalf + g * 4096;
                     tma_load_3d(kq + off, &map_k, &bars->full, 64 * hh, h, t0 + 16 * g);
                     tma_load_3d(kq + off + 2048, &map_q, &bars->full, 64 * hh, h, t0 + 16 * g);
-                    tma_load_3d(orr + off, &map_o, &bars->full, 64 * hh, h, t0 + 16 * g);
-                    tma_load_3d(orr + off + 2048, &map_r, &bars->full, 64 * hh, h, t0 + 16 * g);
                 }
-                tma_load_3d(smem + G::kOffV + hh * kTokHalf, &map_v, &bars->full, 64 * hh, h, t0);
+                tma_load_3d(smem + G::kOffS0 + hh * G::kStateHalf, &map_s0, &bars->full, 64 * hh, 0, bi);
+                tma_load_3d(smem + G::kOffM0 + hh * G::kStateHalf, &map_m0, &bars->full, 64 * hh, 0, bi);
             }
-            // the chunk's entry states, fp32, over the regions of the bf16
-            // tiles (the epilogue converts them)
-            const size_t sbase = ((size_t)gc * H + h) * D * D;
-            bulk_load(smem + G::kOffS0, p.S_chunks + sbase, G::kStateF32, &bars->full);
-            bulk_load(smem + G::kOffDS, p.M_chunks + sbase, G::kStateF32, &bars->full);
-            // once the fp32 states are read: the adjoints at the chunk's end
-            // as the reverse chain left them (bf16 operand tiles dS, dM)
-            bool goa = mbar_wait(&bars->rd, 0, abort);
-            if (goa) {
-                mbar_arrive_expect_tx(&bars->fulla, G::kTxAdj);
-                const unsigned char *adj = reinterpret_cast<const unsigned char *>(p.adj) +
-                                           ((size_t)gc * H + h) * 2 * G::kState;
-                bulk_load(smem + G::kOffDS, adj, G::kState, &bars->fulla);
-                bulk_load(smem + G::kOffDM, adj + G::kState, G::kState, &bars->fulla);
+            // [dO; dR] and V
+            mbar_arrive_expect_tx(&bars->fullo, G::kTxO);
+#pragma unroll
+            for (int hh = 0; hh < G::kHalves; ++hh) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint32_t off = hh * kHalf + g * 4096;
+                    tma_load_3d(orr + off, &map_o, &bars->fullo, 64 * hh, h, t0 + 16 * g);
+                    tma_load_3d(orr + off + 2048, &map_r, &bars->fullo, 64 * hh, h, t0 + 16 * g);
+                }
+                tma_load_3d(smem + G::kOffV + hh * kTokHalf, &map_v, &bars->fullo, 64 * hh, h, t0);
             }
-            // once MMA1 and MMA3 have read the states: the operand tile of
-            // the forward prep and the 64 key rows of the Gram product
-            bool go = mbar_wait(&bars->d13, 0, abort);
+            // the adjoints at the chunk's end as the reverse chain left them
+            // (bf16 operand tiles dS, dM)
+            mbar_arrive_expect_tx(&bars->fulla, G::kTxAdj);
+            const unsigned char *adj = reinterpret_cast<const unsigned char *>(p.adj) +
+                                       ((size_t)gc * H + h) * 2 * G::kState;
+            bulk_load(smem + G::kOffDS, adj, G::kState, &bars->fulla);
+            bulk_load(smem + G::kOffDM, adj + G::kState, G::kState, &bars->fulla);
+            // once MMA1, MMA3 and the epilogue have read the states: the
+            // operand tile of the forward prep and the 64 key rows of the
+            // Gram product, over them
+            bool go = mbar_wait(&bars->d13, 0, abort) && mbar_wait(&bars->rd, 0, abort);
             if (go) {
                 mbar_arrive_expect_tx(&bars->full2, G::kTx2Bytes);
                 const unsigned char *tile = p.tcblk + ((size_t)gc * H + h) * BwdChainLayout::kBytes;
@@ -315,7 +322,8 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             }
             int dummy = 0;
             mbar_wait(&bars->full, 0, &dummy);     // no copy in flight at exit
-            if (goa) mbar_wait(&bars->fulla, 0, &dummy);
+            mbar_wait(&bars->fullo, 0, &dummy);
+            mbar_wait(&bars->fulla, 0, &dummy);
             if (go) mbar_wait(&bars->full2, 0, &dummy);
             if (go3) mbar_wait(&bars->full3, 0, &dummy);
         }
@@ -331,7 +339,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         const uint32_t a6 = smem_u32(smem + G::kOffA6), a7 = smem_u32(smem + G::kOffA7);
         constexpr uint32_t kLboS = G::kHalves > 1 ? G::kStateHalf : 8192;
         constexpr int kSteps = D / 16;
-        bool ok = warp_wait(&bars->full, 0, abort) && warp_wait(&bars->st, 0, abort);
+        bool ok = warp_wait(&bars->full, 0, abort);
         if (ok) {
             tc_fence_after();
             if (l0) {
@@ -342,6 +350,13 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                     mma_bf16(tmem + G::kColS1, a, sdesc_sw128(s0 + s * 2048, kLboS, 1024), G::kIdescKS, s != 0);
                     mma_bf16(tmem + G::kColM1, a, sdesc_sw128(m0 + s * 2048, kLboS, 1024), G::kIdescKS, s != 0);
                 }
+            }
+            __syncwarp();
+            ok = warp_wait(&bars->fullo, 0, abort);
+        }
+        if (ok) {
+            tc_fence_after();
+            if (l0) {
                 // MMA3: [dO; dR] S0^T and [dO; dR] M0^T (B: the same tiles, K-major)
 #pragma unroll
                 for (int s = 0; s < kSteps; ++s) {
@@ -457,41 +472,26 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                 g_a = p.alpha[gi];
                 g_e = p.eta[gi];
             }
+            const unsigned char *s0t = smem + G::kOffS0, *m0t = smem + G::kOffM0;
             const unsigned char *dst = smem + G::kOffDS, *dmt = smem + G::kOffDM;
-            const float *S0f = reinterpret_cast<const float *>(smem + G::kOffS0);
-            const float *M0f = reinterpret_cast<const float *>(smem + G::kOffDS);
             constexpr int kCh = D / 8;
-            constexpr int kIter = D * kCh / 256;         // 16-byte output chunks per thread
+            constexpr int kIter = D * kCh / 256;         // 16-byte chunks of a tile per thread
             float s[kIter][8], m[kIter][8];
             bool have = warp_wait(&bars->full, 0, abort);
             if (have) {
 #pragma unroll
                 for (int u = 0; u < kIter; ++u) {
                     const int idx = e + 256 * u;
-                    const int off = (idx / kCh) * D + 8 * (idx % kCh);
-                    load8(S0f + off, s[u]);
-                    load8(M0f + off, m[u]);
+                    const int k = idx / kCh, c8 = idx % kCh;
+                    const uint32_t off = (c8 >> 3) * G::kStateHalf;
+                    get8(s0t + off, k, c8 & 7, s[u]);
+                    get8(m0t + off, k, c8 & 7, m[u]);
                 }
             }
-            // the fp32 copies are read: the adjoint tiles may land over M0's,
-            // and (after every epilogue warp is here) the bf16 tiles over S0's
+            // the state tiles are read: later copies may land over them
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->rd);
-            epi_sync();
-            if (have) {
-#pragma unroll
-                for (int u = 0; u < kIter; ++u) {
-                    const int idx = e + 256 * u;
-                    const int k = idx / kCh, c8 = idx % kCh;
-                    const uint32_t off = (c8 >> 3) * G::kStateHalf;
-                    put8(smem + G::kOffS0 + off, k, c8 & 7, s[u]);
-                    put8(smem + G::kOffM0 + off, k, c8 & 7, m[u]);
-                }
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->st);
             // <S0, dS>, <M0, dS>, <M0, dM> while MMA1 and MMA3 run
             if (have && mbar_wait(&bars->fulla, 0, abort)) {
 #pragma unroll
@@ -529,7 +529,7 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
         const int j0 = ch * (D / 2);
 
         // ---- R and the state terms of dQ, dP
-        bool ok = warp_wait(&bars->full, 0, abort) && warp_wait(&bars->d13, 0, abort);
+        bool ok = warp_wait(&bars->fullo, 0, abort) && warp_wait(&bars->d13, 0, abort);
         if (ok) {
             tc_fence_after();
             unsigned char *vt = smem + G::kOffV;
@@ -807,9 +807,11 @@ cudaError_t launch_chunk_tc_d(const BwdProblem &p, cudaStream_t st, const CUtens
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)G::kSmemBytes);
     if (err != cudaSuccess) return err;
-    kern<<<dim3(p.loc.max_chunks, p.loc.H), G::kThreads, G::kSmemBytes, st>>>(
+    dim3 grid;
+    if (!chunk_head_grid(p.loc.max_chunks, p.loc.H, grid)) return cudaErrorInvalidConfiguration;
+    kern<<<grid, G::kThreads, G::kSmemBytes, st>>>(
         p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9],
-        maps[10]);
+        maps[10], maps[11], maps[12]);
     return cudaGetLastError();
 }
 
@@ -821,7 +823,7 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st) {
     if ((p.D != 64 && p.D != 128) || p.dtype != MDN_BF16 || !p.prep || !p.adj || !p.tcblk)
         return cudaErrorInvalidValue;
     if (p.loc.max_chunks <= 0 || p.loc.T_total <= 0) return cudaSuccess;
-    CUtensorMap maps[11];
+    CUtensorMap maps[13];
     const void *src[8] = {p.k, p.q, p.dout, p.dv, p.v, p.k, p.dq, p.dk};
     const int box[8] = {16, 16, 16, 16, 64, 64, 16, 16};
     for (int i = 0; i < 8; ++i)
@@ -838,6 +840,14 @@ cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t st) {
                      dims, strides, wbox) ||
         !make_map_3d(&maps[10], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.prep + BL::kG * BL::kMat * sizeof(float),
                      dims, strides, wbox))
+        return cudaErrorInvalidValue;
+    // the chunk entry states, bf16 [block][dk rows][dv columns], as 64-column
+    // boxes of all dk rows
+    const uint64_t sdims[3] = {(uint64_t)p.D, (uint64_t)p.D, blocks};
+    const uint64_t sstrides[2] = {(uint64_t)p.D * 2, (uint64_t)p.D * p.D * 2};
+    const uint32_t sbox[3] = {64, (uint32_t)p.D, 1};
+    if (!make_map_3d(&maps[11], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.S_chunks, sdims, sstrides, sbox) ||
+        !make_map_3d(&maps[12], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.M_chunks, sdims, sstrides, sbox))
         return cudaErrorInvalidValue;
     return p.D == 128 ? launch_chunk_tc_d<128>(p, st, maps) : launch_chunk_tc_d<64>(p, st, maps);
 }

@@ -182,7 +182,8 @@ chunk_prep_split_kernel(ChunkProblem p, const __grid_constant__ CUtensorMap map_
     using SM = PrepSmem<D>;
     using namespace sm100;
     constexpr int LM = SM::LM;
-    const int gc = blockIdx.x, h = blockIdx.y;
+    int gc, h;
+    chunk_head_of_block(p.H, gc, h);
     ChunkLoc loc;
     if (!locate_chunk_cta(p, gc, loc)) return;
     const int n = loc.n;
@@ -535,7 +536,8 @@ cudaError_t launch_prep_t(const ChunkProblem &p, cudaStream_t st) {
     cudaError_t err = cudaFuncSetAttribute(
         kp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PrepSmem<D>::kBytes);
     if (err != cudaSuccess) return err;
-    dim3 grid(p.max_chunks, p.H);
+    dim3 grid;
+    if (!chunk_head_grid(p.max_chunks, p.H, grid)) return cudaErrorInvalidConfiguration;
     kp<<<grid, kThreads, PrepSmem<D>::kBytes, st>>>(p, mkh, mqh, mkl, mql);
     return cudaGetLastError();
 }

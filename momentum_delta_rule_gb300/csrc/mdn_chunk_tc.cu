@@ -194,19 +194,6 @@ __device__ __forceinline__ void rescale_state(uint32_t st_s, uint32_t st_m, cons
     tmem_st_wait();
 }
 
-// One thread's 16 columns of row d of the entry state of chunk slot `slot`
-// (layout [slot, H, dk, dv]); `off` = d * dk + first column.
-template <int D>
-__device__ __forceinline__ void store_chunk_state(const ChunkProblem &p, int slot, int h, size_t off,
-                                                  const float *S, const float *M) {
-    const size_t base = ((size_t)slot * p.H + h) * D * D + off;
-#pragma unroll
-    for (int j = 0; j < kEpiCols; j += 4) {
-        *reinterpret_cast<float4 *>(p.S_chunks + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        *reinterpret_cast<float4 *>(p.M_chunks + base + j) = make_float4(M[j], M[j + 1], M[j + 2], M[j + 3]);
-    }
-}
-
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
@@ -220,6 +207,21 @@ __device__ __forceinline__ void store_out8(__nv_bfloat16 *dst, const float *x) {
 __device__ __forceinline__ void store_out8(float *dst, const float *x) {
     *reinterpret_cast<float4 *>(dst) = make_float4(x[0], x[1], x[2], x[3]);
     *reinterpret_cast<float4 *>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+// One thread's 16 columns of row d of the entry state of chunk slot `slot`
+// (layout [slot, H, dk, dv], element type Ts: bf16 for bf16 inputs, fp32
+// for fp32 inputs); `off` = d * dk + first column.
+template <int D, typename Ts>
+__device__ __forceinline__ void store_chunk_state(const ChunkProblem &p, int slot, int h, size_t off,
+                                                  const float *S, const float *M) {
+    const size_t base = ((size_t)slot * p.H + h) * D * D + off;
+    Ts *sd = static_cast<Ts *>(p.S_chunks) + base, *md = static_cast<Ts *>(p.M_chunks) + base;
+#pragma unroll
+    for (int j = 0; j < kEpiCols; j += 8) {
+        store_out8(sd + j, S + j);
+        store_out8(md + j, M + j);
+    }
 }
 
 // The tensor maps of one launch: K, Q, V, and for split operands their lo
@@ -449,7 +451,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state);
                 if (kChunkStates && row_ok)
-                    store_chunk_state<D>(p, slot0, h, st_off - (size_t)sh * D * D, S, M);
+                    store_chunk_state<D, Tio>(p, slot0, h, st_off - (size_t)sh * D * D, S, M);
             }
         }
         // Token rows: the lower 16 lanes of this warp's quadrant hold the K
@@ -575,7 +577,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
                 }
                 // the next chunk's entry state, after the chain has moved on
                 if (kChunkStates && more && row_ok)
-                    store_chunk_state<D>(p, slot0 + c + 1, h, st_off - (size_t)sh * D * D, S, M);
+                    store_chunk_state<D, Tio>(p, slot0 + c + 1, h, st_off - (size_t)sh * D * D, S, M);
             }
             // ---- outputs of this chunk (off the critical path)
             if (in_chunk) store_out8(og + (size_t)(t0 + tok) * rs, oint);
@@ -854,7 +856,7 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state[x]);
-                if (kChunkStates) store_chunk_state<D>(p, slot0, h, st_row + 64 * x, S, M);
+                if (kChunkStates) store_chunk_state<D, __nv_bfloat16>(p, slot0, h, st_row + 64 * x, S, M);
             }
         }
         const int tok = 16 * q + (lane & 15);
@@ -968,7 +970,7 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                     if (more) mbar_arrive(&bars->state[x]);
                     if (x == 1) mbar_arrive(&bars->empty[st]);
                 }
-                if (kChunkStates && more) store_chunk_state<D>(p, slot0 + c + 1, h, st_row + 64 * x, S, M);
+                if (kChunkStates && more) store_chunk_state<D, __nv_bfloat16>(p, slot0 + c + 1, h, st_row + 64 * x, S, M);
             }
         }
         if (!*abort) {

@@ -76,7 +76,8 @@ struct ChunkProblem {
     void *o;
     float *S_T, *M_T;
     void *vres;                  // per-token residuals like v, or nullptr
-    float *S_chunks, *M_chunks;  // entry states of every chunk [slot, H, dk, dv], or nullptr
+    void *S_chunks, *M_chunks;   // entry states of every chunk [slot, H, dk, dv] (bf16 for
+                                 // bf16 inputs, fp32 for fp32), or nullptr
     const int32_t *cu_seqlens;   // device, or nullptr for equal lengths
     int n_seq, B, T, H, D;       // dk == dv == D
     int T_total;                 // B * T
@@ -120,7 +121,8 @@ struct BwdProblem {
     ChunkProblem loc;
     const void *q, *k, *v, *dout;
     const float *alpha, *mu, *eta, *beta;
-    const float *S_chunks, *M_chunks;  // entry states of every chunk [slot, H, dk, dv]
+    const void *S_chunks, *M_chunks;   // entry states of every chunk [slot, H, dk, dv],
+                                       // in the input precision
     const float *dS_T, *dM_T;          // adjoints of the final states, or nullptr (zero)
     void *dq, *dk, *dv;
     float *dalpha, *dmu, *deta, *dbeta;
@@ -162,8 +164,8 @@ struct BwdLayout {
 mdn_status chunk_fwd_check(const void *q, const void *k, const void *v, const float *alpha,
                            const float *mu, const float *eta, const float *beta,
                            const float *S0, const float *M0, const void *o, const float *S_T,
-                           const float *M_T, const void *vres, const float *S_chunks,
-                           const float *M_chunks, const int32_t *cu_seqlens, int n_seq,
+                           const float *M_T, const void *vres, const void *S_chunks,
+                           const void *M_chunks, const int32_t *cu_seqlens, int n_seq,
                            int B, int T, int H, int dk, int dv, mdn_dtype dtype, int chunk,
                            int **status);
 
@@ -244,6 +246,21 @@ __device__ __forceinline__ bool locate_chunk(const ChunkProblem &p, int gc,
     loc.t0 = start + c * kChunk;
     loc.n = min(kChunk, len - c * kChunk);
     return true;
+}
+
+// Chunk-parallel kernels run one CTA per (chunk, head) on a 1-D grid with the
+// head varying fastest, so that the heads of a chunk, whose rows of q, k and
+// v sit side by side in memory, are resident together and read whole rows.
+inline bool chunk_head_grid(int max_chunks, int H, dim3 &grid) {
+    const long long n = (long long)max_chunks * H;
+    if (n <= 0 || n > 0x7fffffffLL) return false;
+    grid = dim3((unsigned)n);
+    return true;
+}
+__device__ __forceinline__ void chunk_head_of_block(int H, int &gc, int &h) {
+    const unsigned b = blockIdx.x;
+    gc = (int)(b / (unsigned)H);
+    h = (int)(b - (unsigned)gc * (unsigned)H);
 }
 
 // locate_chunk for a whole CTA at once (every thread calls it; uniform

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert mdn.abi_version() == 1
+    assert mdn.abi_version() == 2
     for code in range(5):
         s = mdn.status_string(code)
         assert s.startswith("MDN")

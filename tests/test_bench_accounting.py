@@ -63,14 +63,14 @@ def test_fp32_state_pass_peak_is_a_third_of_bf16():
 
 def test_backward_bytes_varlen():
     # q, k, v, dO in and dq, dk, dv out (bf16), four gates in and four
-    # gradients out (fp32), every chunk's entry states (fp32), and per
+    # gradients out (fp32), every chunk's entry states (bf16, as saved), and per
     # (sequence, head) the final-state adjoints in and dS0, dM0 out
     x = W.make_prefill(W.VARLEN_PACKED)
     lens = bench.seq_lengths(x)
     th = 32768 * 16
     chunks = sum((n + 63) // 64 for n in lens) * 16
     assert chunks == 523 * 16
-    want = th * (7 * 128 * 2 + 8 * 4) + chunks * 2 * 128 * 128 * 4 + len(lens) * 16 * 4 * 128 * 128 * 4
+    want = th * (7 * 128 * 2 + 8 * 4) + chunks * 2 * 128 * 128 * 2 + len(lens) * 16 * 4 * 128 * 128 * 4
     assert bench.bwd_bytes(x) == want
 
 
