@@ -862,16 +862,22 @@ bwd_chunk_kernel(const BwdProblem p) {
 // leaves per (slot, head), over matrices of the gradient block it no longer
 // needs: dA . Y in the Y slot, dL . X in the X slot (rows < n; the lower
 // triangle), and in the A slot the kRowAcc row sums followed by the three
-// state inner products <S0, dS>, <M0, dS>, <M0, dM>.
-constexpr size_t kGateSmem = sizeof(float) * (C * LP + kGateScratch + 5 * C + kRowAcc * C);
+// state inner products <S0, dS>, <M0, dS>, <M0, dM>.  The two products and
+// the row sums arrive by bulk copy (the products into the scratch area the
+// gate recurrences use later): plain loads of them would be capped by the
+// little L1 left beside four CTAs' shared memory.
+constexpr size_t kGateSmem = sizeof(float) * (C * LP + kGateScratch + 5 * C + kRowAcc * C) + 16;
 constexpr int kGateThreads = 128;
 
 __global__ void __launch_bounds__(kGateThreads)
 bwd_gates_kernel(const BwdProblem p) {
+    using namespace sm100;
     extern __shared__ float sm[];
     float *dG = sm, *scr = dG + C * LP;
     float *ga = scr + kGateScratch, *gm = ga + C, *gb = gm + C, *abm = gb + C, *mtl = abm + C;
     float *rowacc = mtl + C;
+    uint64_t *cbar = reinterpret_cast<uint64_t *>(rowacc + kRowAcc * C);
+    volatile int *abort = reinterpret_cast<volatile int *>(cbar + 1);
     int gc, h;
     chunk_head_of_block(p.loc.H, gc, h);
     const int tid = threadIdx.x, H = p.loc.H;
@@ -880,8 +886,17 @@ bwd_gates_kernel(const BwdProblem p) {
     const int n = loc.n, t0 = loc.t0;
     const float *blk = bwd_block(p, gc, h);
     const float *ra = blk + BL::kA * BL::kMat;
-    const float *W1 = blk + BL::kY * BL::kMat, *W2 = blk + BL::kX * BL::kMat;
     const float *vec = blk + BL::kMats * BL::kMat;
+    float *W1 = scr, *W2 = scr + C * C;      // dA . Y and dL . X as copied
+    if (tid == 0) {
+        mbar_init(cbar, 1);
+        *abort = 0;
+        fence_mbar_init();
+        mbar_arrive_expect_tx(cbar, 2 * C * C * 4 + kRowAcc * C * 4);
+        bulk_load(W1, blk + BL::kY * BL::kMat, C * C * 4, cbar);
+        bulk_load(W2, blk + BL::kX * BL::kMat, C * C * 4, cbar);
+        bulk_load(rowacc, ra, kRowAcc * C * 4, cbar);
+    }
     if (tid < C) {
         float a = 0.f, m = 0.f, b = 0.f;
         if (tid < n) {
@@ -894,35 +909,30 @@ bwd_gates_kernel(const BwdProblem p) {
         abm[tid] = vec[BL::vAbarM * C + tid];
         mtl[tid] = vec[BL::vMuTail * C + tid];
     }
-    for (int idx = tid; idx < kRowAcc * C; idx += kGateThreads) rowacc[idx] = ra[idx];
+    const float dcs[3] = {ra[kRowAcc * C + 0], -ra[kRowAcc * C + 1], ra[kRowAcc * C + 2]};
+    __syncthreads();                         // the barrier is initialised
     // dG = dA . Y, plus the carry row on the last row, plus dL . X one row up
-    // (the loads of a batch issued before their first use)
-    constexpr int kPer = 16, kBatches = C * C / (kGateThreads * kPer);
-#pragma unroll 1
-    for (int bt = 0; bt < kBatches; ++bt) {
-        float w1[kPer], w2[kPer], gl[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int idx = tid + kGateThreads * (bt * kPer + u);
-            w1[u] = W1[idx];
-            w2[u] = idx + C < C * C ? W2[idx + C] : 0.f;
-            gl[u] = ra[rGLast * C + (idx & 63)];
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int idx = tid + kGateThreads * (bt * kPer + u);
+    if (mbar_wait(cbar, 0, abort)) {
+        for (int idx = tid; idx < C * C; idx += kGateThreads) {
             const int r = idx >> 6, m = idx & 63;
             float v = 0.f;
             if (r < n && m <= r) {
-                v = w1[u];
-                if (r + 1 < n) v += w2[u];
-                if (r == n - 1) v += gl[u];
+                v = W1[idx];
+                if (r + 1 < n) v += W2[idx + C];
+                if (r == n - 1) v += rowacc[rGLast * C + m];
             }
             dG[r * LP + m] = v;
         }
     }
-    const float dcs[3] = {ra[kRowAcc * C + 0], -ra[kRowAcc * C + 1], ra[kRowAcc * C + 2]};
     __syncthreads();
+    if (*abort) {
+        if (tid == 0) {
+            int dummy = 0;                   // the copies land before the CTA exits
+            mbar_wait(cbar, 0, &dummy);
+            if (p.loc.status) atomicExch(p.loc.status, (int)MDN_ERR_DEVICE_TIMEOUT);
+        }
+        return;
+    }
     gate_gradients(p, t0, n, h, dG, scr, ga, gm, gb, rowacc, dcs, abm, mtl);
 }
 
