@@ -527,11 +527,21 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     flushed before every timed call: ms per call, tokens/s, and the roofline
     of the whole pass: whichever of its algorithmic bytes (HBM) or FLOPs
     (bf16 tensor peak: the bf16 pass runs its products on tcgen05; fp32
-    inputs take the CUDA-core kernels, FFMA peak) needs more time."""
+    inputs take the CUDA-core kernels, FFMA peak) needs more time.  Also
+    the forward that saves those states (mdn_chunk_fwd_states), timed the
+    same way, and the training step they make together."""
     d = x_dev
     _, _, _, Sc, Mc = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
                                     d["beta"], d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"],
                                     return_chunk_states=True)
+    fws = torch.empty(max(256, mdn.workspace_size(d["n_seq"], d["B"] * d["T"], d["H"], d["D"],
+                                                  d["q"].dtype)),
+                      dtype=torch.uint8, device=d["q"].device)
+
+    def fwd_call():
+        return mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"], d["beta"],
+                             d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"], workspace=fws,
+                             S_chunks=Sc, M_chunks=Mc)
     g = torch.Generator(device=d["q"].device).manual_seed(11)
     do = torch.randn(d["v"].shape, generator=g, device=d["v"].device).to(d["v"].dtype)
     n_seq, H, D = d["n_seq"], d["H"], d["D"]
@@ -545,24 +555,28 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
                              do, beta=d["beta"], dS_T=dS, dM_T=dM, cu_seqlens=d["cu_seqlens"],
                              workspace=ws)
 
-    for _ in range(warmup):
-        flush.zero_()
-        call()
-    torch.cuda.synchronize()
-    cur = torch.cuda.current_stream(do.device)
-    ts = []
-    for _ in range(steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(cur)
-        call()
-        b.record(cur)
-        ts.append((a, b))
-    torch.cuda.synchronize()
-    st = mdn.device_status()
-    if st != 0:
-        raise RuntimeError("device status %d after the gradient pass" % st)
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ts)
+    def timed(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream(do.device)
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            fn()
+            b.record(cur)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        st = mdn.device_status()
+        if st != 0:
+            raise RuntimeError("device status %d after the gradient pass" % st)
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    fwd_ms = timed(fwd_call)
+    ms = timed(call)
     tokens = sum(seq_lengths(x))
     fl = bwd_flops_per_token_head(D) * tokens * H
     by = bwd_bytes(x)
@@ -585,6 +599,9 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     launches = (5 if bf16 else 3) + (1 if d["cu_seqlens"] is not None else 0)
     return {"what": "gradient pass (mdn_chunk_bwd) from the forward's chunk entry states",
             "ms_per_call": ms, "tokens_per_s": tokens / s,
+            "forward_with_states_ms": fwd_ms,
+            "training_step": {"what": "mdn_chunk_fwd_states + mdn_chunk_bwd",
+                              "ms": fwd_ms + ms, "tokens_per_s": tokens / ((fwd_ms + ms) / 1e3)},
             "ratio_to_forward": None, "gpu_launches_per_call": launches,
             "kernels": ("chunk_prep_tc (the forward's), bwd_vec, bwd_chain_tc, bwd_chunk_tc, "
                         "bwd_gates" if bf16 else "bwd_prep, bwd_chain, bwd_chunk"),

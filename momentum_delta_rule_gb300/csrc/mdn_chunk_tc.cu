@@ -224,10 +224,12 @@ __device__ __forceinline__ void store_chunk_state(const ChunkProblem &p, int slo
     }
 }
 
-// The tensor maps of one launch: K, Q, V, and for split operands their lo
-// parts.
+// The tensor maps of one launch: K, Q, V, for split operands their lo
+// parts, and for the saved chunk states of bf16 inputs the bf16 [block, dk,
+// dv] arrays as boxes of 64 columns by all dk rows (the layout of a 64-column
+// state operand tile).
 struct Maps {
-    CUtensorMap k, q, v, k_lo, q_lo, v_lo;
+    CUtensorMap k, q, v, k_lo, q_lo, v_lo, sc, mc;
 };
 
 // kChunkStates: also write the entry state of every chunk (a separate
@@ -240,6 +242,10 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     using C = Cfg<D, NS, kSplit>;
     using Tio = typename std::conditional<kSplit, float, __nv_bfloat16>::type;
     constexpr int kStages = C::kStages;
+    // bf16 entry states of 64-column slices leave as tensor stores of the
+    // operand tile; narrower slices (S and M share a tile row) and fp32
+    // store from the epilogue's registers
+    constexpr bool kTmaStates = kChunkStates && !kSplit && NS == 64;
     Bars *bars = reinterpret_cast<Bars *>(smem + C::kOffBar);
     volatile int *abort = &bars->abort;
 
@@ -365,6 +371,14 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
                             }
                     }
                     mma_commit(&bars->d1);
+                    if constexpr (kTmaStates) {
+                        // the chunk's entry state, already the bf16 operand
+                        // tile: out to its slot by tensor stores
+                        const int z = (slot0 + c) * p.H + h;
+                        tma_store_3d(&maps.sc, smem + C::kOffB1, col0, 0, z);
+                        tma_store_3d(&maps.mc, smem + C::kOffB1 + C::kB1M, col0, 0, z);
+                        bulk_commit_group();
+                    }
                 }
                 __syncwarp();
                 if (!warp_wait(&bars->r, c & 1, abort)) break;
@@ -398,16 +412,20 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
                             mma_bf16(tmem + C::kColSt, a, b, C::kIdesc3, 1);
                         }
                     }
+                    // the epilogue rewrites the state tile after d3
+                    if constexpr (kTmaStates) bulk_wait_group_read0();
                     mma_commit(&bars->d3);
                     mma_commit(&bars->empty[st]);
                 }
                 __syncwarp();
             }
-            // drain: all issued MMAs complete before TMEM is freed
+            // drain: all issued MMAs complete before TMEM is freed, the
+            // state stores before the CTA exits
             if (l0) {
                 mma_commit(&bars->drain);
                 int dummy = 0;
                 mbar_wait(&bars->drain, 0, &dummy);
+                if constexpr (kTmaStates) bulk_wait_group0();
             }
             __syncwarp();
         }
@@ -450,7 +468,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state);
-                if (kChunkStates && row_ok)
+                if (kChunkStates && !kTmaStates && row_ok)
                     store_chunk_state<D, Tio>(p, slot0, h, st_off - (size_t)sh * D * D, S, M);
             }
         }
@@ -576,7 +594,7 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
                     mbar_arrive(&bars->empty[st]);
                 }
                 // the next chunk's entry state, after the chain has moved on
-                if (kChunkStates && more && row_ok)
+                if (kChunkStates && !kTmaStates && more && row_ok)
                     store_chunk_state<D, Tio>(p, slot0 + c + 1, h, st_off - (size_t)sh * D * D, S, M);
             }
             // ---- outputs of this chunk (off the critical path)
@@ -774,6 +792,15 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                             mma_bf16(tmem + x * C::kSliceCols, a, b, C::kIdesc1, (kb | kk) != 0);
                         }
                     mma_commit(&bars->d1[x]);
+                    if constexpr (kChunkStates) {
+                        // the chunk's entry state of this slice, already the
+                        // bf16 operand tile: out to its slot by tensor stores
+                        const unsigned char *bx = smem + C::kOffB1 + x * C::kB1Bytes;
+                        const int z = (slot0 + c) * p.H + h;
+                        tma_store_3d(&maps.sc, bx, 64 * x, 0, z);
+                        tma_store_3d(&maps.mc, bx + C::kB1M, 64 * x, 0, z);
+                        bulk_commit_group();
+                    }
                 }
                 __syncwarp();
             }
@@ -807,6 +834,8 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                         const uint64_t b = sdesc_sw128(b3 + kk * 2048, 8192, 1024);
                         mma_bf16(tmem + x * C::kSliceCols + C::kColSt, a, b, C::kIdesc3, 1);
                     }
+                    // the epilogue rewrites the state tiles after d3
+                    if (kChunkStates && x == 0) bulk_wait_group_read0();
                     mma_commit(&bars->d3[x]);
                     if (x == 1) mma_commit(&bars->empty[st]);
                 }
@@ -818,6 +847,7 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
             mma_commit(&bars->drain);
             int dummy = 0;
             mbar_wait(&bars->drain, 0, &dummy);
+            if (kChunkStates) bulk_wait_group0();    // the state stores land before exit
         }
         __syncwarp();
     } else {
@@ -856,7 +886,6 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->state[x]);
-                if (kChunkStates) store_chunk_state<D, __nv_bfloat16>(p, slot0, h, st_row + 64 * x, S, M);
             }
         }
         const int tok = 16 * q + (lane & 15);
@@ -970,7 +999,6 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                     if (more) mbar_arrive(&bars->state[x]);
                     if (x == 1) mbar_arrive(&bars->empty[st]);
                 }
-                if (kChunkStates && more) store_chunk_state<D, __nv_bfloat16>(p, slot0 + c + 1, h, st_row + 64 * x, S, M);
             }
         }
         if (!*abort) {
@@ -1140,6 +1168,17 @@ cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st) {
                   !make_map(&maps.q_lo, p.q_lo, Tt, p.H, p.D, 16) ||
                   !make_map(&maps.v_lo, p.v_lo, Tt, p.H, p.D, 64)))
         return cudaErrorInvalidValue;
+    maps.sc = maps.k;
+    maps.mc = maps.k;
+    if (p.S_chunks && !split) {
+        const uint64_t blocks = (uint64_t)(p.max_chunks > 0 ? p.max_chunks : 1) * p.H;
+        const uint64_t sdims[3] = {(uint64_t)p.D, (uint64_t)p.D, blocks};
+        const uint64_t sstrides[2] = {(uint64_t)p.D * 2, (uint64_t)p.D * p.D * 2};
+        const uint32_t sbox[3] = {64, (uint32_t)p.D, 1};
+        if (!make_map_3d(&maps.sc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.S_chunks, sdims, sstrides, sbox) ||
+            !make_map_3d(&maps.mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.M_chunks, sdims, sstrides, sbox))
+            return cudaErrorInvalidValue;
+    }
     if (p.D == 128)
         return split ? launch_state_tc_d<128, true>(p, st, maps)
                      : launch_state_tc_d<128, false>(p, st, maps);
