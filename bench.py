@@ -529,7 +529,9 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     (bf16 tensor peak: the bf16 pass runs its products on tcgen05; fp32
     inputs take the CUDA-core kernels, FFMA peak) needs more time.  Also
     the forward that saves those states (mdn_chunk_fwd_states), timed the
-    same way, and the training step they make together."""
+    same way, the gradient pass that also reuses that forward's T and A_O T
+    (its workspace kept), and the training step those two make (each timed
+    after an L2 flush, as a layer's backward runs long after its forward)."""
     d = x_dev
     _, _, _, Sc, Mc = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
                                     d["beta"], d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"],
@@ -550,10 +552,17 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     need = mdn.chunk_bwd_workspace_size(n_seq, d["B"] * d["T"], H, D, d["q"].dtype)
     ws = torch.empty(need, dtype=torch.uint8, device=do.device)
 
+    bf16_in = d["q"].dtype == torch.bfloat16
+
     def call():
         return mdn.chunk_bwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"], Sc, Mc,
                              do, beta=d["beta"], dS_T=dS, dM_T=dM, cu_seqlens=d["cu_seqlens"],
                              workspace=ws)
+
+    def call_reuse():
+        return mdn.chunk_bwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"], Sc, Mc,
+                             do, beta=d["beta"], dS_T=dS, dM_T=dM, cu_seqlens=d["cu_seqlens"],
+                             workspace=ws, fwd_workspace=fws)
 
     def timed(fn):
         for _ in range(warmup):
@@ -577,6 +586,7 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
 
     fwd_ms = timed(fwd_call)
     ms = timed(call)
+    reuse_ms = timed(call_reuse) if bf16_in else ms
     tokens = sum(seq_lengths(x))
     fl = bwd_flops_per_token_head(D) * tokens * H
     by = bwd_bytes(x)
@@ -600,8 +610,10 @@ def time_backward(mdn, x, x_dev, steps, warmup, flush, peaks):
     return {"what": "gradient pass (mdn_chunk_bwd) from the forward's chunk entry states",
             "ms_per_call": ms, "tokens_per_s": tokens / s,
             "forward_with_states_ms": fwd_ms,
-            "training_step": {"what": "mdn_chunk_fwd_states + mdn_chunk_bwd",
-                              "ms": fwd_ms + ms, "tokens_per_s": tokens / ((fwd_ms + ms) / 1e3)},
+            "ms_per_call_reusing_forward_workspace": reuse_ms,
+            "training_step": {"what": "mdn_chunk_fwd_states + mdn_chunk_bwd reusing its T, A_O T",
+                              "ms": fwd_ms + reuse_ms,
+                              "tokens_per_s": tokens / ((fwd_ms + reuse_ms) / 1e3)},
             "ratio_to_forward": None, "gpu_launches_per_call": launches,
             "kernels": ("chunk_prep_tc (the forward's), bwd_vec, bwd_chain_tc, bwd_chunk_tc, "
                         "bwd_gates" if bf16 else "bwd_prep, bwd_chain, bwd_chunk"),

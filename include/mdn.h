@@ -242,6 +242,13 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk,
  *                  mdn_chunk_fwd_states wrote them for these inputs and
  *                  initial states ([slots, H, dk, dv], bf16 or fp32 as
  *                  the inputs)
+ *   fwd_workspace  NULL, or (bf16 inputs) the workspace that
+ *                  mdn_chunk_fwd_states used for these inputs, unchanged
+ *                  since that call: the gradient then takes the matrices T
+ *                  and A_O T from the chunk blocks the forward left there
+ *                  instead of recomputing them (its prep kernel is skipped;
+ *                  the results are the same bits).  Read only; 256-byte
+ *                  aligned.  Ignored for fp32 inputs.
  *   dout           adjoint of o (dtype, laid out like o); required
  *   dS_T, dM_T     adjoints of the final states (fp32 [n_seq, H, dk, dv]) or
  *                  NULL for zero
@@ -260,7 +267,8 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk,
 mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v,
                          const float *alpha, const float *mu, const float *eta,
                          const float *beta, const void *S_chunks,
-                         const void *M_chunks, const void *dout,
+                         const void *M_chunks, const void *fwd_workspace,
+                         const void *dout,
                          const float *dS_T, const float *dM_T, void *dq,
                          void *dk_out, void *dv_out, float *dalpha, float *dmu,
                          float *deta, float *dbeta, float *dS0, float *dM0,

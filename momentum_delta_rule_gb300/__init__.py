@@ -118,7 +118,7 @@ def lib():
     L.mdn_chunk_bwd_workspace_size.restype = c_size
     L.mdn_chunk_bwd_workspace_size.argtypes = [c_int] * 6
     L.mdn_chunk_bwd.restype = c_int
-    L.mdn_chunk_bwd.argtypes = [vp] * 22 + [c_int] * 8 + [vp, c_size, vp]
+    L.mdn_chunk_bwd.argtypes = [vp] * 23 + [c_int] * 8 + [vp, c_size, vp]
     _LIB = L
     return L
 
@@ -369,14 +369,17 @@ def prepare_inputs(q, k, z_alpha, z_beta, z_mu, z_eta, a, b, s, tau,
 
 def chunk_bwd(q, k, v, alpha, mu, eta, S_chunks, M_chunks, dout, beta=None,
               dS_T=None, dM_T=None, cu_seqlens=None, need_dbeta=True,
-              need_dstates=True, workspace=None, stream=None):
+              need_dstates=True, workspace=None, stream=None, fwd_workspace=None):
     """Gradients of the chunk forward (``mdn_chunk_bwd``).
 
     Inputs as ``chunk_fwd`` plus the forward's chunk entry states
     ``S_chunks``, ``M_chunks`` (``chunk_fwd(..., return_chunk_states=True)``),
-    the adjoint ``dout`` of o and optionally ``dS_T``, ``dM_T``.  Returns a
-    dict with dq, dk, dv (dtype of q), dalpha, dmu, deta, dbeta (fp32, dbeta
-    None unless ``need_dbeta``), dS0, dM0 (None unless ``need_dstates``).
+    the adjoint ``dout`` of o and optionally ``dS_T``, ``dM_T``.
+    ``fwd_workspace``: the uint8 workspace the state-saving forward used for
+    these inputs, unchanged since (bf16 inputs: its T and A_O T are reused),
+    or None.  Returns a dict with dq, dk, dv (dtype of q), dalpha, dmu,
+    deta, dbeta (fp32, dbeta None unless ``need_dbeta``), dS0, dM0 (None
+    unless ``need_dstates``).
     """
     L = lib()
     if q.dim() != 4:
@@ -404,6 +407,11 @@ def chunk_bwd(q, k, v, alpha, mu, eta, S_chunks, M_chunks, dout, beta=None,
         _check_cuda(name, t, q.dtype, dev)
         if t.dim() != 4 or t.shape[0] < slots or tuple(t.shape[1:]) != (H, D, D):
             raise ValueError("%s must be [>= %d, H, D, D]" % (name, slots))
+    if fwd_workspace is not None:
+        _check_cuda("fwd_workspace", fwd_workspace, torch.uint8, dev)
+        fneed = int(L.mdn_chunk_fwd_workspace_size(n_seq, B * T, H, D, D, code))
+        if fwd_workspace.numel() < fneed:
+            raise ValueError("fwd_workspace must hold %d bytes" % fneed)
     for name, t in (("dS_T", dS_T), ("dM_T", dM_T)):
         _check_cuda(name, t, torch.float32, dev)
         if t is not None and tuple(t.shape) != (n_seq, H, D, D):
@@ -422,7 +430,7 @@ def chunk_bwd(q, k, v, alpha, mu, eta, S_chunks, M_chunks, dout, beta=None,
     with torch.cuda.device(dev):
         st = L.mdn_chunk_bwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(mu), _ptr(eta), _ptr(beta),
-            _ptr(S_chunks), _ptr(M_chunks), _ptr(dout), _ptr(dS_T), _ptr(dM_T),
+            _ptr(S_chunks), _ptr(M_chunks), _ptr(fwd_workspace), _ptr(dout), _ptr(dS_T), _ptr(dM_T),
             _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dalpha"]), _ptr(g["dmu"]),
             _ptr(g["deta"]), _ptr(g["dbeta"]), _ptr(g["dS0"]), _ptr(g["dM0"]),
             _ptr(cu_seqlens), n_seq, B, T, H, D, D, code, CHUNK, _ptr(workspace),

@@ -426,7 +426,8 @@ size_t mdn_chunk_bwd_workspace_size(int n_seq, int T_total, int H, int dk, int d
 
 mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
                          const float *mu, const float *eta, const float *beta,
-                         const void *S_chunks, const void *M_chunks, const void *dout,
+                         const void *S_chunks, const void *M_chunks,
+                         const void *fwd_workspace, const void *dout,
                          const float *dS_T, const float *dM_T, void *dq, void *dk_out,
                          void *dv_out, float *dalpha, float *dmu, float *deta, float *dbeta,
                          float *dS0, float *dM0, const int32_t *cu_seqlens, int n_seq, int B,
@@ -449,9 +450,10 @@ mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
     const void *ptrs4[] = {dalpha, dmu, deta, dbeta};
     for (const void *ptr : ptrs4)
         if (ptr && ((uintptr_t)ptr & 3u)) return MDN_ERR_INVALID_ARG;
+    if (fwd_workspace && ((uintptr_t)fwd_workspace & 255u)) return MDN_ERR_INVALID_ARG;
     // no output may be an input or another output
     const void *ins[] = {q, k, v, alpha, mu, eta, beta, S_chunks, M_chunks, dout, dS_T, dM_T,
-                         cu_seqlens};
+                         cu_seqlens, fwd_workspace};
     const void *outs[] = {dq, dk_out, dv_out, dalpha, dmu, deta, dbeta, dS0, dM0};
     for (int a = 0; a < 9; ++a) {
         if (!outs[a]) continue;
@@ -497,6 +499,12 @@ mdn_status mdn_chunk_bwd(const void *q, const void *k, const void *v, const floa
                       ? reinterpret_cast<unsigned char *>(p.adj) +
                             slots * sizeof(__nv_bfloat16) * 2 * (size_t)dk * dv
                       : nullptr;
+        // the forward's prepared blocks, laid out as mdn_chunk_fwd lays out
+        // its workspace: their [T; A_O T] tiles are the gradient's
+        if (fwd_workspace && p.tcblk) {
+            p.fwd_tile = static_cast<const unsigned char *>(fwd_workspace) + meta_bytes(n_seq);
+            p.fwd_tile_stride = mdn::kPrepBytesMax;
+        }
     } else {
         // fp32 inputs keep the fp32 kernels (for the fp32 bound)
         p.dR = p.adj ? p.adj + slots * 2 * (size_t)dk * dv : nullptr;

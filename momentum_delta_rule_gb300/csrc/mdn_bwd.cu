@@ -952,7 +952,9 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t st) {
         fp.prep_stride = BwdChainLayout::kBytes;
         dim3 cg;
         if (!chunk_head_grid(p.loc.max_chunks, H, cg)) return cudaErrorInvalidConfiguration;
-        cudaError_t err = launch_chunk_prep_tc(fp, st);
+        // (the forward's own blocks, when the caller kept them, already hold
+        // the same tiles)
+        cudaError_t err = p.fwd_tile ? cudaSuccess : launch_chunk_prep_tc(fp, st);
         if (err != cudaSuccess) return err;
         bwd_vec_kernel<<<cg, 128, 0, st>>>(p);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -305,7 +305,9 @@ bwd_chunk_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
             bool go = mbar_wait(&bars->d13, 0, abort) && mbar_wait(&bars->rd, 0, abort);
             if (go) {
                 mbar_arrive_expect_tx(&bars->full2, G::kTx2Bytes);
-                const unsigned char *tile = p.tcblk + ((size_t)gc * H + h) * BwdChainLayout::kBytes;
+                const unsigned char *tile =
+                    p.fwd_tile ? p.fwd_tile + ((size_t)gc * H + h) * p.fwd_tile_stride
+                               : p.tcblk + ((size_t)gc * H + h) * BwdChainLayout::kBytes;
                 bulk_load(smem + G::kOffTile, tile + BwdChainLayout::kOffTile, kHalf, &bars->full2);
 #pragma unroll
                 for (int hh = 0; hh < G::kHalves; ++hh)

@@ -270,7 +270,16 @@ bwd_chain_tc_kernel(const BwdProblem p, const __grid_constant__ CUtensorMap map_
                         tma_load_3d(dst + 2048, &map_q, &bars->full[st], 64 * hh, h, t0 + 16 * g);
                     }
                 tma_load_3d(stage + C::kOffO, &map_o, &bars->full[st], col0, h, t0);
-                bulk_load(stage + C::kOffBlk, blk, C::kBlkBytes, &bars->full[st]);
+                if (p.fwd_tile) {
+                    // the tile from the forward's prepared block, the
+                    // coefficient rows from the operand block
+                    const unsigned char *ft = p.fwd_tile + ((size_t)(slot0 + c) * L.H + h) * p.fwd_tile_stride;
+                    bulk_load(stage + C::kOffBlk, ft + CL::kOffTile, (uint32_t)CL::kOffVec, &bars->full[st]);
+                    bulk_load(stage + C::kOffBlk + CL::kOffVec, blk + CL::kOffVec,
+                              C::kBlkBytes - (uint32_t)CL::kOffVec, &bars->full[st]);
+                } else {
+                    bulk_load(stage + C::kOffBlk, blk, C::kBlkBytes, &bars->full[st]);
+                }
                 last_use[st] = use;
             }
             for (int st = 0; st < C::kStages; ++st) {

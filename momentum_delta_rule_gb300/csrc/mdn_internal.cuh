@@ -132,6 +132,9 @@ struct BwdProblem {
                                        // [2, dk, dv] (fp32 inputs) or bf16 operand tiles
     float *dR;                         // per (slot, head): residual adjoints [64, dv] (fp32 inputs)
     unsigned char *tcblk;              // per (slot, head): the tensor-core chain's operands, or null
+    const unsigned char *fwd_tile;     // the forward's prepared blocks (their [T; A_O T] tiles
+                                       // serve as the operand blocks' tiles), or null
+    size_t fwd_tile_stride;
     int D;
     mdn_dtype dtype;
 };

@@ -265,7 +265,7 @@ def _bwd(L, **over):
     args.update(over)
     a = args
     return L.mdn_chunk_bwd(a["q"], a["k"], a["v"], a["alpha"], a["mu"], a["eta"], a["beta"],
-                           a["Sc"], a["Mc"], a["do"], a["dS"], a["dM"], a["dq"], a["dk"],
+                           a["Sc"], a["Mc"], a.get("fws"), a["do"], a["dS"], a["dM"], a["dq"], a["dk"],
                            a["dv"], a["da"], a["dmu"], a["de"], a["db"], a["dS0"], a["dM0"],
                            a["cu"], a["n_seq"], a["B"], a["T"], a["H"], a["dkd"], a["dvd"],
                            a["dtype"], a["chunk"], a["ws"], a["ws_bytes"], a["stream"])
@@ -276,6 +276,8 @@ def _bwd(L, **over):
     (dict(dv=ctypes.c_void_p(0x10000)), 1),          # an output aliasing an input
     (dict(dk=ctypes.c_void_p(0x20000)), 1),          # two outputs the same
     (dict(dS0=ctypes.c_void_p(0x30008)), 1),         # misaligned
+    (dict(fws=ctypes.c_void_p(0x200010)), 1),        # forward workspace not 256-aligned
+    (dict(dq=ctypes.c_void_p(0x200000), fws=ctypes.c_void_p(0x200000)), 1),   # output aliasing it
     (dict(ws=None), 1), (dict(ws_bytes=256), 1),
     (dict(n_seq=3), 1), (dict(chunk=32), 2), (dict(dkd=96, dvd=96), 2),
 ])

@@ -182,3 +182,39 @@ def test_no_tokens_passes_state_adjoints_through(dtype):
     got = _gpu_grads(x, do, dS, dM)
     assert got["dq"].numel() == 0
     assert torch.equal(got["dS0"], dS) and torch.equal(got["dM0"], dM)
+
+
+@pytest.mark.parametrize("lengths,B,T,H", [
+    (None, 3, 150, 2),                          # equal lengths, ragged last chunk
+    ([1, 64, 0, 65, 130, 7, 0], 1, None, 2),    # packed with empty members
+    (None, 40, 130, 2),                         # both slices of a head per state CTA
+])
+def test_forward_workspace_reuse_is_bit_identical(lengths, B, T, H):
+    """The gradient that takes T and A_O T from the state-saving forward's
+    workspace (its prep kernel skipped) equals, bit for bit, the gradient
+    that recomputes them."""
+    import momentum_delta_rule_gb300 as mdn
+    w = W.Workload("bwd_reuse", dtype="bf16", state="randn", seed=61)
+    if lengths is None:
+        x = W.make_prefill(w, B=B, T=T, H=H, D=128, with_beta=True)
+    else:
+        x = W.make_prefill(w, H=H, D=128, lengths=lengths, with_beta=True)
+    do, dS, dM = _adjoints(x, 62)
+    d = to_dev(x)
+    n_seq = x["n_seq"]
+    fws = torch.empty(max(256, mdn.workspace_size(n_seq, d["q"].shape[0] * d["q"].shape[1], H, 128,
+                                                  d["q"].dtype)), dtype=torch.uint8, device="cuda")
+    _, _, _, Sc, Mc = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
+                                    d["beta"], d["S0"], d["M0"], cu_seqlens=d["cu_seqlens"],
+                                    workspace=fws, return_chunk_states=True)
+    args = (d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"], Sc, Mc, do.cuda())
+    kw = dict(beta=d["beta"], dS_T=dS.cuda(), dM_T=dM.cuda(), cu_seqlens=d["cu_seqlens"])
+    g0 = mdn.chunk_bwd(*args, **kw)
+    g1 = mdn.chunk_bwd(*args, fwd_workspace=fws, **kw)
+    torch.cuda.synchronize()
+    assert mdn.device_status() == mdn.MDN_OK
+    for n in g0:
+        if g0[n] is None:
+            assert g1[n] is None
+            continue
+        assert torch.equal(g0[n], g1[n]), n
