@@ -162,6 +162,53 @@ namespace {
 
 // Every chunk-forward entry point: validation, workspace carve-up, path
 // choice and the launches.  vres (nullable) receives the per-token residuals.
+// Long equal-length bf16 sequences whose state pass runs narrow slices (16
+// or 32 state columns per CTA, each CTA leaving room on its SM for a prep
+// CTA) are walked in time segments: the prep of segment k + 1 runs beside
+// the state pass of segment k, which hides all but the first segment's prep.
+// Segment k + 1's state pass starts from the states segment k left in S_T,
+// M_T, so the path needs both (and no per-token or per-chunk side outputs).
+// Segments of 16 chunks, then each twice the previous, the last taking the
+// rest (or absorbing a remainder under a quarter segment): a segment's prep, on
+// the SM room the state CTAs leave, runs at ~27 prepared blocks per µs,
+// against the ~11 per µs the state pass of 16 heads consumes beside it (1.4
+// µs per chunk), so the next segment's prep ends before the current state
+// pass even at twice its length.
+constexpr int kSegFirst = 16;
+constexpr int kSegMinChunks = 128;
+
+bool use_segments(const mdn::ChunkProblem &p) {
+    if (p.cu_seqlens || p.dtype != MDN_BF16 || p.vres || p.S_chunks || !p.S_T || !p.M_T)
+        return false;
+    if ((p.T + mdn::kChunk - 1) / mdn::kChunk < kSegMinChunks) return false;
+    const int ns = mdn::chunk_state_slice_width(p);
+    return ns == 16 || ns == 32;
+}
+
+cudaError_t launch_segments(const mdn::ChunkProblem &p, cudaStream_t cs) {
+    const int cps = (p.T + mdn::kChunk - 1) / mdn::kChunk;
+    cudaError_t err = cudaSuccess;
+    int c0 = 0;
+    for (int k = 0, len = kSegFirst; c0 < cps && err == cudaSuccess; ++k, len *= 2) {
+        const int c1 = cps - (c0 + len) < len / 4 ? cps : c0 + len;
+        const bool last = c1 == cps;
+        mdn::ChunkProblem q = p;
+        q.seg_c0 = c0;
+        q.seg_c1 = c1;
+        q.seg_mode = k > 0 ? mdn::kSegPrepFollower : 0;
+        err = mdn::launch_chunk_prep_tc(q, cs);
+        if (err != cudaSuccess) break;
+        if (k > 0) {            // from the states the previous segment left
+            q.S0 = p.S_T;
+            q.M0 = p.M_T;
+        }
+        q.seg_mode = (last ? 0 : mdn::kSegStateTrigger) | (k > 0 ? mdn::kSegStateWaitFirst : 0);
+        err = mdn::launch_chunk_state_tc(q, cs);
+        c0 = c1;
+    }
+    return err;
+}
+
 mdn_status chunk_fwd_impl(
     const void *q, const void *k, const void *v, const float *alpha,
     const float *mu, const float *eta, const float *beta, const float *S0,
@@ -242,11 +289,16 @@ mdn_status chunk_fwd_impl(
     if (err == cudaSuccess && p.cu_seqlens && p.max_chunks > 0)
         err = mdn::launch_chunk_offsets(p, cs);
     if (err == cudaSuccess && split) err = mdn::launch_split_inputs(p, cs);
-    if (err == cudaSuccess && tensor)
-        err = split ? mdn::launch_chunk_prep_simt(p, cs) : mdn::launch_chunk_prep_tc(p, cs);
-    if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
-    if (err == cudaSuccess)
-        err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_states_passthrough(p, cs);
+    if (tensor && !ev[1] && use_segments(p)) {
+        // (stage events mark the prep and the state pass apart: whole sequences)
+        if (err == cudaSuccess) err = launch_segments(p, cs);
+    } else {
+        if (err == cudaSuccess && tensor)
+            err = split ? mdn::launch_chunk_prep_simt(p, cs) : mdn::launch_chunk_prep_tc(p, cs);
+        if (err == cudaSuccess && ev[1]) err = cudaEventRecord(ev[1], cs);
+        if (err == cudaSuccess)
+            err = tensor ? mdn::launch_chunk_state_tc(p, cs) : mdn::launch_states_passthrough(p, cs);
+    }
     if (err == cudaSuccess && ev[2]) err = cudaEventRecord(ev[2], cs);
     if (err != cudaSuccess) {
         cudaGetLastError();

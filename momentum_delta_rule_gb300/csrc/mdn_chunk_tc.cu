@@ -234,7 +234,7 @@ struct Maps {
 
 // kChunkStates: also write the entry state of every chunk (a separate
 // instantiation, so the plain forward carries none of its registers).
-template <int D, int NS, bool kChunkStates, bool kSplit>
+template <int D, int NS, bool kChunkStates, bool kSplit, bool kSeg>
 __global__ void __launch_bounds__(Cfg<D, NS, kSplit>::kThreads, 1)
 chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -257,13 +257,28 @@ chunk_state_tc_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     // dependent launch).  Packed sequences read the chunk offsets first: wait
     // for the preceding grids right away.  Fixed-length batches run their
     // setup and initial-state loads first; the producer waits before its
-    // first prepared-block copy.
+    // first prepared-block copy.  A later time segment reads the states the
+    // previous one left, so it waits first too; a segment with a successor
+    // lets that successor's prep start as soon as all its CTAs run.
+    if constexpr (kSeg) {
+        if (p.seg_mode & kSegStateTrigger) grid_launch_dependents();
+        if (p.seg_mode & kSegStateWaitFirst) grid_dependency_wait();
+    }
     if (p.cu_seqlens != nullptr) grid_dependency_wait();
     const int s = ordered_sequence(p, kh / p.H), h = kh % p.H;
     const int sh = s * p.H + h;                 // (sequence, head) of the states
     const int col0 = slice * NS;
     int start, len, slot0;
     sequence_range(p, s, start, len, slot0);
+    if constexpr (kSeg) {
+        // a time segment: chunks [seg_c0, seg_c1) of the sequence, whole
+        // chunks but for the sequence's last
+        const int all = (len + kChunk - 1) / kChunk;
+        const int c0 = min(p.seg_c0, all), c1 = min(p.seg_c1, all);
+        start += c0 * kChunk;
+        slot0 += c0;
+        len = min(len - c0 * kChunk, (c1 - c0) * kChunk);
+    }
     const int nchunks = (len + kChunk - 1) / kChunk;
 
     if (threadIdx.x == 0) {
@@ -1059,10 +1074,22 @@ bool make_map(CUtensorMap *map, const void *base, int T_total, int H, int D, int
 template <int D, int NS, bool kChunkStates, bool kSplit>
 cudaError_t launch_state_tc_t(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
     using C = Cfg<D, NS, kSplit>;
-    auto kern = chunk_state_tc_kernel<D, NS, kChunkStates, kSplit>;
+    // time segments (narrow slices of the plain forward only) are a separate
+    // instantiation
+    constexpr bool kSegOk = NS != 64 && !kChunkStates;
+    if (is_segment(p) && !kSegOk) return cudaErrorInvalidValue;
+    auto kern = (kSegOk && is_segment(p)) ? chunk_state_tc_kernel<D, NS, kChunkStates, kSplit, kSegOk>
+                                          : chunk_state_tc_kernel<D, NS, kChunkStates, kSplit, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)C::kSmemBytes);
     if (err != cudaSuccess) return err;
+    if (is_segment(p)) {
+        // the largest shared-memory carveout: the next segment's prep CTAs
+        // fit beside this pass's CTAs
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
+    }
     cudaFuncAttributes fa;
     err = cudaFuncGetAttributes(&fa, kern);
     if (err != cudaSuccess) return err;
@@ -1116,19 +1143,30 @@ cudaError_t launch_state_dual(const ChunkProblem &p, cudaStream_t st, const Maps
     return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 
+// Slice width for a problem: 0 for both 64-column slices of a head in one
+// CTA (bf16 at head size 128 with more 64-column slices than SMs), else the
+// narrowest slices (16, 32 or 64 columns) whose CTAs fit on the GPU in one
+// wave.
 template <int D, bool kSplit>
-cudaError_t launch_state_tc_d(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
+int slice_width_d(const ChunkProblem &p) {
     const long chains = (long)p.n_seq * p.H;
     const int sms = device_sm_count();
-    // bf16 at head size 128 with more 64-column slices than SMs: both slices
-    // of a head in one CTA, their steps interleaved
+    if (D == 128 && !kSplit && sms > 0 && chains * 2 > sms) return 0;
+    return (sms > 0 && chains * (D / 16) <= sms) ? 16
+           : ((sms > 0 && chains * (D / 32) <= sms) || kWidestSlice<D, kSplit> == 32) ? 32
+                                                                                     : 64;
+}
+
+template <int D, bool kSplit>
+cudaError_t launch_state_tc_d(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
+    const int ns = slice_width_d<D, kSplit>(p);
+    // both slices of a head in one CTA, their steps interleaved
     if constexpr (D == 128 && !kSplit) {
-        if (sms > 0 && chains * 2 > sms)
+        if (ns == 0) {
+            if (is_segment(p)) return cudaErrorInvalidValue;    // whole sequences only
             return p.S_chunks ? launch_state_dual<true>(p, st, maps) : launch_state_dual<false>(p, st, maps);
+        }
     }
-    const int ns = (sms > 0 && chains * (D / 16) <= sms) ? 16
-                 : ((sms > 0 && chains * (D / 32) <= sms) || kWidestSlice<D, kSplit> == 32) ? 32
-                                                                                         : 64;
     if (p.S_chunks) {
         if (ns == 16) return launch_state_tc_t<D, 16, true, kSplit>(p, st, maps);
         if (ns == 32) return launch_state_tc_t<D, 32, true, kSplit>(p, st, maps);
@@ -1144,6 +1182,12 @@ cudaError_t launch_state_tc_d(const ChunkProblem &p, cudaStream_t st, const Maps
 }
 
 }  // namespace
+
+int chunk_state_slice_width(const ChunkProblem &p) {
+    const bool split = p.dtype == MDN_F32;
+    if (p.D == 128) return split ? slice_width_d<128, true>(p) : slice_width_d<128, false>(p);
+    return split ? slice_width_d<64, true>(p) : slice_width_d<64, false>(p);
+}
 
 // The slice width trades per-chunk latency (narrow slices: smaller MMAs and
 // epilogues) against CTA count: the narrowest slices (16, 32 or 64 columns)

@@ -91,7 +91,26 @@ struct ChunkProblem {
     // fp32 inputs on the tensor cores: q, k, v as hi / lo bf16 parts
     // [T_total, H, D] in the workspace (null for bf16 inputs)
     void *q_hi, *q_lo, *k_hi, *k_lo, *v_hi, *v_lo;
+    // A time segment of equal-length sequences: chunks [seg_c0, seg_c1) of
+    // every sequence (seg_c1 <= seg_c0: the whole sequences), and how the
+    // segment's kernels meet their neighbours in the stream (kSeg* bits).
+    int seg_c0, seg_c1;
+    int seg_mode;
 };
+
+// seg_mode bits.  Segment k's state pass lets the next launch (segment
+// k + 1's prep) start once all its CTAs run, so that prep fills what the
+// state CTAs leave of the SMs; that prep neither lets its own dependent (the
+// state pass of segment k + 1) start early nor finishes before segment k's
+// state pass has: its last CTA waits for it.  Segment k + 1's state pass
+// therefore finds the states segment k left in S_T, M_T complete.
+enum SegMode {
+    kSegStateTrigger = 1,     // state pass: trigger the dependent launch at start
+    kSegStateWaitFirst = 2,   // state pass: wait for the preceding grids before reading S0, M0
+    kSegPrepFollower = 4,     // prep: no early trigger; the last CTA waits for the preceding grid
+};
+
+__host__ __device__ inline bool is_segment(const ChunkProblem &p) { return p.seg_c1 > p.seg_c0; }
 
 struct DecodeProblem {
     const void *q, *k, *v;
@@ -178,6 +197,8 @@ cudaError_t launch_chunk_prep_simt(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_split_inputs(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_prep_tc(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_chunk_state_tc(const ChunkProblem &p, cudaStream_t st);
+// The slice width (state columns per CTA) the state pass picks for p.
+int chunk_state_slice_width(const ChunkProblem &p);
 cudaError_t launch_states_passthrough(const ChunkProblem &p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeProblem &p, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t st);

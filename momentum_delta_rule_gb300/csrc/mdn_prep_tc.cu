@@ -174,7 +174,7 @@ __device__ __forceinline__ void scan64_gates(float &A, float &U, float &Z, float
     }
 }
 
-template <int D>
+template <int D, bool kSeg>
 __global__ void __launch_bounds__(kThreadsP, 4)
 chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q) {
@@ -196,11 +196,26 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
 
     // The state pass may be scheduled as soon as every CTA of this grid has
     // started; it waits for this grid's completion before it reads a
-    // prepared block.
-    grid_launch_dependents();
-    const int gc = blockIdx.x, h = blockIdx.y;
+    // prepared block.  The prep of a later time segment, which runs beside
+    // the previous segment's state pass, lets no dependent start early, and
+    // its last CTA outlives that state pass (SegMode).
+    const bool follower = kSeg && (p.seg_mode & kSegPrepFollower) != 0;
+    const bool last_cta = blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1;
+    if (!follower) grid_launch_dependents();
+    int gc = blockIdx.x;
+    if constexpr (kSeg) {
+        // the segment's chunks of every sequence (equal lengths), sequence-major
+        const int len = p.seg_c1 - p.seg_c0, cps = (p.T + kChunk - 1) / kChunk;
+        const int s = blockIdx.x / len;
+        gc = s * cps + p.seg_c0 + (blockIdx.x - s * len);
+    }
+    const int h = blockIdx.y;
     ChunkLoc loc;
-    if (!locate_chunk_cta(p, gc, loc)) return;
+    if (!locate_chunk_cta(p, gc, loc)) {
+        if constexpr (kSeg)
+            if (follower && last_cta && threadIdx.x == 0) grid_dependency_wait();
+        return;
+    }
     const int n = loc.n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned char *pblk = p.prep + ((size_t)gc * p.H + h) * p.prep_stride;
@@ -657,6 +672,8 @@ chunk_prep_tc_kernel(const ChunkProblem p, const __grid_constant__ CUtensorMap m
         tmem_dealloc(tmem, kTmemColsP);
     }
     if (tid == 0 && *abort && p.status) atomicExch(p.status, (int)MDN_ERR_DEVICE_TIMEOUT);
+    if constexpr (kSeg)
+        if (follower && last_cta && tid == 0) grid_dependency_wait();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_p() {
@@ -689,13 +706,37 @@ cudaError_t launch_prep_tc_t(const ChunkProblem &p, cudaStream_t st) {
     CUtensorMap mk, mq;
     if (!make_map_p(&mk, p.k, p.T_total, p.H, D) || !make_map_p(&mq, p.q, p.T_total, p.H, D))
         return cudaErrorInvalidValue;
-    auto kern = chunk_prep_tc_kernel<D>;
+    // time segments are a separate instantiation
+    auto kern = is_segment(p) ? chunk_prep_tc_kernel<D, true> : chunk_prep_tc_kernel<D, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemP);
     if (err != cudaSuccess) return err;
+    if (is_segment(p)) {
+        // the largest shared-memory carveout, so that a CTA fits beside a
+        // state-pass CTA (which needs most of it)
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
+    }
     dim3 grid(p.max_chunks, p.H);
-    kern<<<grid, kThreadsP, kSmemP, st>>>(p, mk, mq);
-    return cudaGetLastError();
+    if (is_segment(p)) grid.x = (unsigned)(p.n_seq * (p.seg_c1 - p.seg_c0));
+    if (!(p.seg_mode & kSegPrepFollower)) {
+        kern<<<grid, kThreadsP, kSmemP, st>>>(p, mk, mq);
+        return cudaGetLastError();
+    }
+    // a later segment's prep: a programmatic dependent of the previous
+    // segment's state pass, so it starts once that pass's CTAs all run
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreadsP);
+    cfg.dynamicSmemBytes = kSmemP;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, mk, mq);
 }
 
 }  // namespace

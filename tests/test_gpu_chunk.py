@@ -120,6 +120,32 @@ def test_split_sequence_state_passing():
     assert rel(S2, full[1]) < 1e-3 and rel(M2, full[2]) < 1e-3
 
 
+@pytest.mark.parametrize("D,T", [(128, 9000), (64, 8256)])
+def test_time_segments_bit_identical(D, T):
+    """Long equal-length sequences whose state pass runs narrow slices are
+    walked in time segments, the prep of the next segment beside the state
+    pass of the current one, each segment starting from the states the
+    previous one left in S_T, M_T.  The segments' kernels do the same
+    arithmetic as one pass over whole sequences, which runs when no final
+    states are asked for: the outputs match it bit for bit, also with the
+    final states written over the initial ones (S_T aliasing S0); one chain
+    against the oracle."""
+    import momentum_delta_rule_gb300 as mdn
+    w = W.Workload("segments", dtype="bf16", state="randn", seed=19)
+    x = W.make_prefill(w, B=1, T=T, H=3, D=D, with_beta=True)
+    seg = gpu_chunk_fwd(x)
+    whole = gpu_chunk_fwd(x, output_final_state=False)
+    assert whole[1] is None
+    assert torch.equal(seg[0], whole[0])
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    S, M = d["S0"].clone(), d["M0"].clone()
+    o, S_T, M_T = mdn.chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["mu"], d["eta"],
+                                d["beta"], S, M, S_T=S, M_T=M)
+    torch.cuda.synchronize()
+    assert torch.equal(o, seg[0]) and torch.equal(S, seg[1]) and torch.equal(M, seg[2])
+    compare(x, seg, chains(x)[:1])
+
+
 # ---------------------------------------------------------------- full size
 
 def test_prefill_400m_full_size_sampled():

@@ -55,6 +55,37 @@ def test_chunk_fwd_graph_replay(dtype, D):
     assert torch.equal(o, ref[0]) and torch.equal(S_T, ref[1]) and torch.equal(M_T, ref[2])
 
 
+def test_chunk_fwd_time_segments_graph_replay():
+    """A long equal-length prefill that runs in time segments (each later
+    segment's prep a programmatic dependent of the previous segment's state
+    pass) captured and replayed on new inputs."""
+    import momentum_delta_rule_gb300 as mdn
+    B, T, H, D = 1, 8256, 2, 128
+    x1 = W.make_prefill(W.Workload("graph_seg", dtype="bf16", state="randn", seed=63),
+                        B=B, T=T, H=H, D=D)
+    x2 = W.make_prefill(W.Workload("graph_seg2", dtype="bf16", state="randn", seed=64),
+                        B=B, T=T, H=H, D=D)
+    d = to_dev(x1)
+    names = ["q", "k", "v", "alpha", "mu", "eta", "S0", "M0"]
+    o = torch.empty_like(d["v"])
+    S_T = torch.empty((B, H, D, D), device="cuda")
+    M_T = torch.empty_like(S_T)
+    ws = torch.empty(mdn.workspace_size(B, B * T, H, D, d["q"].dtype), dtype=torch.uint8,
+                     device="cuda")
+
+    def run():
+        mdn.chunk_fwd(*(d[n] for n in names[:6]), None, d["S0"], d["M0"], o=o, S_T=S_T,
+                      M_T=M_T, workspace=ws)
+
+    g = _capture(run)
+    for n in names:
+        d[n].copy_(x2[n].to("cuda"))
+    g.replay()
+    torch.cuda.synchronize()
+    ref = gpu_chunk_fwd(x2)
+    assert torch.equal(o, ref[0]) and torch.equal(S_T, ref[1]) and torch.equal(M_T, ref[2])
+
+
 def test_decode_steps_graph_replay():
     import momentum_delta_rule_gb300 as mdn
     w = W.Workload("graph_decode", B=8, T=1, H=4, D=128, dtype="bf16", state="randn",
