@@ -118,7 +118,11 @@ size_t mdn_chunk_fwd_workspace_size(int n_seq, int T_total, int H, int dk,
  *   o              output (dtype), written for every token
  *   S_T, M_T       final states, or NULL to skip writing that state.  S_T may
  *                  alias S0 and M_T may alias M0 (same pointer, not partial
- *                  overlap); no other output may overlap an input.
+ *                  overlap); no other output may overlap an input.  Long
+ *                  equal-length bf16 sequences with both given run in time
+ *                  segments that hand their states on through S_T, M_T
+ *                  (the next segment's preparation overlapping the current
+ *                  segment's state pass); the results are the same bits.
  *   workspace      device scratch of at least workspace_bytes >=
  *                  mdn_chunk_fwd_workspace_size(...), 256-byte aligned; its
  *                  contents on entry do not matter and are undefined on exit.
