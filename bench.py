@@ -427,7 +427,9 @@ def time_prefill(mdn, x_dev, w, steps, warmup, world, flush):
     return {"total_ms": sum(total), "stage_ms": [statistics.mean(stage0),
                                                  statistics.mean(stage1)],
             "wall_s": wall, "path": info.get("path"),
-            "launches_per_step": 2 + (1 if x_dev["cu_seqlens"] is not None else 0)}
+            "launches_per_step": mdn.chunk_fwd_kernel_count(
+                x_dev["n_seq"], x_dev["B"], x_dev["T"], x_dev["H"], x_dev["D"], x_dev["q"].dtype,
+                x_dev["cu_seqlens"] is not None)}
 
 
 def time_vres(mdn, x_dev, steps, warmup, flush):

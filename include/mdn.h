@@ -350,7 +350,9 @@ typedef enum mdn_path {
  *                   stage.  Stages: 0 = per-chunk preparation (offsets,
  *                   coefficients, Gram matrices, triangular inverse),
  *                   1 = sequential state pass (residuals, outputs, carry).
- *                   n_stage_events must be 0 or 3.
+ *                   n_stage_events must be 0 or 3.  With stage events the
+ *                   call runs whole sequences (no time segments), so that
+ *                   the two stages follow one another.
  *   path_out        NULL, or receives the mdn_path that ran.
  */
 mdn_status mdn_chunk_fwd_profiled(
@@ -361,6 +363,20 @@ mdn_status mdn_chunk_fwd_profiled(
     mdn_dtype dtype, int chunk, void *workspace, size_t workspace_bytes,
     void *stream, void *const *stage_events, int n_stage_events,
     int *path_out);
+
+/*
+ * mdn_chunk_fwd_kernel_count — how many kernels one mdn_chunk_fwd call with
+ * these sizes enqueues on the current device (a diagnostic, e.g. for launch
+ * counts in a benchmark; it does not launch anything).  `packed` is nonzero
+ * when cu_seqlens is given (then B is 1 and T the packed total),
+ * `final_states` nonzero when both S_T and M_T are given.  The count covers
+ * the chunk-offset kernel (packed sequences), the split of fp32 inputs, the
+ * preparation and the state pass, or, for long equal-length bf16 sequences
+ * on narrow state slices, two kernels per time segment.  0 for sizes the
+ * call would reject.  No citation: a property of this implementation.
+ */
+int mdn_chunk_fwd_kernel_count(int n_seq, int B, int T, int H, int dk, int dv, mdn_dtype dtype,
+                               int packed, int final_states);
 
 /* Size of the library-owned scratch array of mdn_chunk_fwd_static_ws. */
 #define MDN_STATIC_WORKSPACE_BYTES (32u << 20)

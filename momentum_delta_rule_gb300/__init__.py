@@ -26,7 +26,7 @@ import os
 
 import torch
 
-__all__ = ["chunk_fwd", "chunk_bwd", "block_fwd", "chunk_bwd_workspace_size", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
+__all__ = ["chunk_fwd", "chunk_fwd_kernel_count", "chunk_bwd", "block_fwd", "chunk_bwd_workspace_size", "chunk_state_slots", "decode_step", "prepare_inputs", "workspace_size",
            "device_status", "wait_selftest",
            "abi_version", "status_string", "MdnError", "lib", "LIB_PATH",
            "EXPORTED_SYMBOLS"]
@@ -50,7 +50,8 @@ EXPORTED_SYMBOLS = ["mdn_abi_version", "mdn_status_string",
                     "mdn_chunk_fwd_states", "mdn_prepare_inputs",
                     "mdn_decode_step", "mdn_get_device_status",
                     "mdn_wait_selftest", "mdn_chunk_bwd_workspace_size",
-                    "mdn_chunk_bwd", "mdn_block_fwd_workspace_size", "mdn_block_fwd"]
+                    "mdn_chunk_bwd", "mdn_block_fwd_workspace_size", "mdn_block_fwd",
+                    "mdn_chunk_fwd_kernel_count"]
 MDN_PATH_CUDA_CORE = 0
 MDN_PATH_TENSOR_CORE = 1
 
@@ -81,6 +82,8 @@ def lib():
     L.mdn_status_string.argtypes = [c_int]
     L.mdn_chunk_fwd_workspace_size.restype = c_size
     L.mdn_chunk_fwd_workspace_size.argtypes = [c_int] * 5 + [c_int]
+    L.mdn_chunk_fwd_kernel_count.restype = c_int
+    L.mdn_chunk_fwd_kernel_count.argtypes = [c_int] * 9
     L.mdn_chunk_fwd.restype = c_int
     L.mdn_chunk_fwd.argtypes = ([vp] * 3 + [fp] * 6 + [vp, fp, fp, ip]
                                 + [c_int] * 8 + [vp, c_size, vp])
@@ -167,6 +170,15 @@ def _check_cuda(name, t, dtype=None, device=None):
 def workspace_size(n_seq, T_total, H, D, dtype):
     code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
     return int(lib().mdn_chunk_fwd_workspace_size(n_seq, T_total, H, D, D, code))
+
+
+def chunk_fwd_kernel_count(n_seq, B, T, H, D, dtype, packed, final_states=True):
+    """Kernels one ``chunk_fwd`` call with these sizes enqueues on the current
+    device (``mdn_chunk_fwd_kernel_count``); 0 for rejected sizes."""
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().mdn_chunk_fwd_kernel_count(int(n_seq), int(B), int(T), int(H), int(D),
+                                                int(D), code, 1 if packed else 0,
+                                                1 if final_states else 0))
 
 
 def chunk_fwd(q, k, v, alpha, mu, eta, beta=None, S0=None, M0=None,

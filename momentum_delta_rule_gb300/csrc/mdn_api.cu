@@ -177,12 +177,28 @@ namespace {
 constexpr int kSegFirst = 16;
 constexpr int kSegMinChunks = 128;
 
-bool use_segments(const mdn::ChunkProblem &p) {
-    if (p.cu_seqlens || p.dtype != MDN_BF16 || p.vres || p.S_chunks || !p.S_T || !p.M_T)
-        return false;
+bool segments_apply(const mdn::ChunkProblem &p, bool packed, bool side_outputs,
+                    bool final_states) {
+    if (packed || p.dtype != MDN_BF16 || side_outputs || !final_states) return false;
     if ((p.T + mdn::kChunk - 1) / mdn::kChunk < kSegMinChunks) return false;
     const int ns = mdn::chunk_state_slice_width(p);
     return ns == 16 || ns == 32;
+}
+
+bool use_segments(const mdn::ChunkProblem &p) {
+    return segments_apply(p, p.cu_seqlens != nullptr, p.vres || p.S_chunks, p.S_T && p.M_T);
+}
+
+// The end of the segment that starts at chunk c0 (its length `len`), out of
+// cps chunks.
+int segment_end(int c0, int len, int cps) {
+    return cps - (c0 + len) < len / 4 ? cps : c0 + len;
+}
+
+int segment_count(int cps) {
+    int n = 0;
+    for (int c0 = 0, len = kSegFirst; c0 < cps; len *= 2, ++n) c0 = segment_end(c0, len, cps);
+    return n;
 }
 
 cudaError_t launch_segments(const mdn::ChunkProblem &p, cudaStream_t cs) {
@@ -190,7 +206,7 @@ cudaError_t launch_segments(const mdn::ChunkProblem &p, cudaStream_t cs) {
     cudaError_t err = cudaSuccess;
     int c0 = 0;
     for (int k = 0, len = kSegFirst; c0 < cps && err == cudaSuccess; ++k, len *= 2) {
-        const int c1 = cps - (c0 + len) < len / 4 ? cps : c0 + len;
+        const int c1 = segment_end(c0, len, cps);
         const bool last = c1 == cps;
         mdn::ChunkProblem q = p;
         q.seg_c0 = c0;
@@ -322,6 +338,24 @@ mdn_status mdn_chunk_fwd_profiled(
     return chunk_fwd_impl(q, k, v, alpha, mu, eta, beta, S0, M0, o, S_T, M_T, nullptr, nullptr, nullptr,
                           cu_seqlens, n_seq, B, T, H, dk, dv, dtype, chunk, workspace,
                           workspace_bytes, stream, stage_events, n_stage_events, path_out);
+}
+
+int mdn_chunk_fwd_kernel_count(int n_seq, int B, int T, int H, int dk, int dv, mdn_dtype dtype,
+                               int packed, int final_states) {
+    if (n_seq <= 0 || B <= 0 || T < 0 || H <= 0 || dk != dv || (dk != 64 && dk != 128) ||
+        (dtype != MDN_F32 && dtype != MDN_BF16))
+        return 0;
+    if ((long)B * T == 0) return 1;                 // the initial states pass through
+    mdn::ChunkProblem p;
+    memset(&p, 0, sizeof(p));
+    p.n_seq = n_seq; p.B = B; p.T = T; p.H = H; p.D = dk; p.dtype = dtype;
+    p.T_total = B * T;
+    int n = (packed ? 1 : 0) + (dtype == MDN_F32 ? 1 : 0);   // chunk offsets, split inputs
+    if (segments_apply(p, packed != 0, false, final_states != 0))
+        n += 2 * segment_count((T + mdn::kChunk - 1) / mdn::kChunk);
+    else
+        n += 2;                                     // prep, state pass
+    return n;
 }
 
 mdn_status mdn_chunk_fwd(const void *q, const void *k, const void *v,

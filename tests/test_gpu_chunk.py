@@ -133,6 +133,10 @@ def test_time_segments_bit_identical(D, T):
     import momentum_delta_rule_gb300 as mdn
     w = W.Workload("segments", dtype="bf16", state="randn", seed=19)
     x = W.make_prefill(w, B=1, T=T, H=3, D=D, with_beta=True)
+    # four segments (16, 32, 64 and the rest), two kernels each; one pass
+    # without final states
+    assert mdn.chunk_fwd_kernel_count(1, 1, T, 3, D, torch.bfloat16, False) == 8
+    assert mdn.chunk_fwd_kernel_count(1, 1, T, 3, D, torch.bfloat16, False, False) == 2
     seg = gpu_chunk_fwd(x)
     whole = gpu_chunk_fwd(x, output_final_state=False)
     assert whole[1] is None
