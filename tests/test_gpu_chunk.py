@@ -120,8 +120,8 @@ def test_split_sequence_state_passing():
     assert rel(S2, full[1]) < 1e-3 and rel(M2, full[2]) < 1e-3
 
 
-@pytest.mark.parametrize("D,T", [(128, 9000), (64, 8256)])
-def test_time_segments_bit_identical(D, T):
+@pytest.mark.parametrize("D,T,H", [(128, 9000, 3), (64, 8256, 3), (128, 8256, 24)])
+def test_time_segments_bit_identical(D, T, H):
     """Long equal-length sequences whose state pass runs narrow slices are
     walked in time segments, the prep of the next segment beside the state
     pass of the current one, each segment starting from the states the
@@ -132,11 +132,11 @@ def test_time_segments_bit_identical(D, T):
     against the oracle."""
     import momentum_delta_rule_gb300 as mdn
     w = W.Workload("segments", dtype="bf16", state="randn", seed=19)
-    x = W.make_prefill(w, B=1, T=T, H=3, D=D, with_beta=True)
-    # four segments (16, 32, 64 and the rest), two kernels each; one pass
-    # without final states
-    assert mdn.chunk_fwd_kernel_count(1, 1, T, 3, D, torch.bfloat16, False) == 8
-    assert mdn.chunk_fwd_kernel_count(1, 1, T, 3, D, torch.bfloat16, False, False) == 2
+    x = W.make_prefill(w, B=1, T=T, H=H, D=D, with_beta=True)
+    # four segments (16, 32, 64 and the rest), two kernels each, on 16- or
+    # (24 heads of 128) 32-column slices; one pass without final states
+    assert mdn.chunk_fwd_kernel_count(1, 1, T, H, D, torch.bfloat16, False) == 8
+    assert mdn.chunk_fwd_kernel_count(1, 1, T, H, D, torch.bfloat16, False, False) == 2
     seg = gpu_chunk_fwd(x)
     whole = gpu_chunk_fwd(x, output_final_state=False)
     assert whole[1] is None
