@@ -120,8 +120,9 @@ def test_split_sequence_state_passing():
     assert rel(S2, full[1]) < 1e-3 and rel(M2, full[2]) < 1e-3
 
 
-@pytest.mark.parametrize("D,T,H", [(128, 9000, 3), (64, 8256, 3), (128, 8256, 24)])
-def test_time_segments_bit_identical(D, T, H):
+@pytest.mark.parametrize("D,B,T,H", [(128, 1, 9000, 3), (64, 1, 8256, 3), (128, 1, 8256, 24),
+                                     (128, 2, 8200, 4)])
+def test_time_segments_bit_identical(D, B, T, H):
     """Long equal-length sequences whose state pass runs narrow slices are
     walked in time segments, the prep of the next segment beside the state
     pass of the current one, each segment starting from the states the
@@ -132,11 +133,11 @@ def test_time_segments_bit_identical(D, T, H):
     against the oracle."""
     import momentum_delta_rule_gb300 as mdn
     w = W.Workload("segments", dtype="bf16", state="randn", seed=19)
-    x = W.make_prefill(w, B=1, T=T, H=H, D=D, with_beta=True)
+    x = W.make_prefill(w, B=B, T=T, H=H, D=D, with_beta=True)
     # four segments (16, 32, 64 and the rest), two kernels each, on 16- or
     # (24 heads of 128) 32-column slices; one pass without final states
-    assert mdn.chunk_fwd_kernel_count(1, 1, T, H, D, torch.bfloat16, False) == 8
-    assert mdn.chunk_fwd_kernel_count(1, 1, T, H, D, torch.bfloat16, False, False) == 2
+    assert mdn.chunk_fwd_kernel_count(B, B, T, H, D, torch.bfloat16, False) == 8
+    assert mdn.chunk_fwd_kernel_count(B, B, T, H, D, torch.bfloat16, False, False) == 2
     seg = gpu_chunk_fwd(x)
     whole = gpu_chunk_fwd(x, output_final_state=False)
     assert whole[1] is None
@@ -147,7 +148,7 @@ def test_time_segments_bit_identical(D, T, H):
                                 d["beta"], S, M, S_T=S, M_T=M)
     torch.cuda.synchronize()
     assert torch.equal(o, seg[0]) and torch.equal(S, seg[1]) and torch.equal(M, seg[2])
-    compare(x, seg, chains(x)[:1])
+    compare(x, seg, chains(x)[:1] + chains(x)[-1:])
 
 
 # ---------------------------------------------------------------- full size
