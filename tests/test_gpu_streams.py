@@ -59,6 +59,33 @@ def test_concurrent_streams_match_serial():
     assert mdn.device_status() == 0
 
 
+def test_concurrent_time_segmented_prefills():
+    """Two long equal-length prefills that each run in time segments (each
+    later segment's prep a programmatic dependent of the previous segment's
+    state pass, waiting for it before it completes) enqueued on two streams
+    at once: the dependencies stay within each stream, and each result
+    equals the same call made alone, bit for bit."""
+    import momentum_delta_rule_gb300 as mdn
+    xs = [to_dev(W.make_prefill(W.Workload("cc_seg%d" % i, dtype="bf16", state="randn",
+                                           seed=74 + i), B=1, T=8256, H=4, D=128))
+          for i in range(2)]
+    assert mdn.chunk_fwd_kernel_count(1, 1, 8256, 4, 128, torch.bfloat16, False) > 2
+    refs = [_prefill(mdn, x) for x in xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for x, st in zip(xs, streams):
+        with torch.cuda.stream(st):
+            outs.append(_prefill(mdn, x, st))
+    torch.cuda.synchronize()
+    for got, want in zip(outs, refs):
+        for g, w in zip(got, want):
+            assert torch.equal(g, w)
+    assert mdn.device_status() == 0
+
+
 @pytest.mark.parametrize("lengths", [[0], [0, 0, 0]])
 def test_empty_problems(lengths):
     import momentum_delta_rule_gb300 as mdn
