@@ -695,7 +695,7 @@ struct DualBars {
 };
 static_assert(sizeof(DualBars) <= 256, "barrier block");
 
-template <bool kChunkStates>
+template <bool kChunkStates, bool kVres>
 __global__ void __launch_bounds__(DualCfg::kThreads, 1)
 chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps) {
     using C = DualCfg;
@@ -910,7 +910,9 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
         const uint32_t lq = tmem + ((uint32_t)(32 * q + 16) << 16);
         const size_t rs = (size_t)p.H * D;
         __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(p.o) + (size_t)h * D + cg;
-        __nv_bfloat16 *vg = p.vres ? static_cast<__nv_bfloat16 *>(p.vres) + (size_t)h * D + cg : nullptr;
+        // the residual output is a separate instantiation (its pointer and
+        // stores would cost the plain pass registers)
+        __nv_bfloat16 *vg = kVres ? static_cast<__nv_bfloat16 *>(p.vres) + (size_t)h * D + cg : nullptr;
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1, use = c >> 1;
@@ -984,7 +986,7 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->v[x]);
                 if (in_chunk) {
-                    if (vg) store_out8(vg + (size_t)(t0 + tok) * rs + 64 * x, xv);
+                    if constexpr (kVres) store_out8(vg + (size_t)(t0 + tok) * rs + 64 * x, xv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) xo[e] += oint[x][e];
                     store_out8(og + (size_t)(t0 + tok) * rs + 64 * x, xo);
@@ -1119,7 +1121,8 @@ constexpr int kWidestSlice = (kSplit && D == 128) ? 32 : 64;
 template <bool kChunkStates>
 cudaError_t launch_state_dual(const ChunkProblem &p, cudaStream_t st, const Maps &maps) {
     using C = DualCfg;
-    auto kern = chunk_state_dual_kernel<kChunkStates>;
+    auto kern = p.vres ? chunk_state_dual_kernel<kChunkStates, true>
+                       : chunk_state_dual_kernel<kChunkStates, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)C::kSmemBytes);
     if (err != cudaSuccess) return err;
