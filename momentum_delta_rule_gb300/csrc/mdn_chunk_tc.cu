@@ -194,6 +194,30 @@ __device__ __forceinline__ void rescale_state(uint32_t st_s, uint32_t st_m, cons
     tmem_st_wait();
 }
 
+// The same rescale eight columns at a time: half the registers at its peak
+// (the dual-slice pass runs it while one slice's O_inter is still held).
+__device__ __forceinline__ void rescale_state_halves(uint32_t st_s, uint32_t st_m, const float *vec) {
+    const float ab_n = vec[kVecScal * kChunk + 0];
+    const float b_n = vec[kVecScal * kChunk + 1];
+    const float mb_n = vec[kVecScal * kChunk + 2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float S[8], M[8];
+        tmem_ld8(st_s + 8 * hf, S);
+        tmem_ld8(st_m + 8 * hf, M);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float s_old = S[j];
+            S[j] = ab_n * s_old - b_n * M[j];
+            M[j] = mb_n * M[j];
+        }
+        tmem_st8(st_s + 8 * hf, S);
+        tmem_st8(st_m + 8 * hf, M);
+    }
+    tmem_st_wait();
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
@@ -964,7 +988,7 @@ chunk_state_dual_kernel(const ChunkProblem p, const __grid_constant__ Maps maps)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->r[x]);
-                rescale_state(st_s(x), st_m(x), vec);
+                rescale_state_halves(st_s(x), st_m(x), vec);
             }
             if (!ok) break;
             // ---- Vres of each slice: MMA3's B operand; O = O_inter + O_intra
