@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import momentum_delta_rule_gb300 as mdn
 
@@ -224,6 +225,21 @@ def test_chunk_state_slots(L):
     assert mdn.chunk_state_slots(0, 0, 0, False) == 0
     assert mdn.chunk_state_slots(3, 1, 300, True) == 300 // 64 + 3
     assert mdn.chunk_state_slots(-1, 1, 10, False) == 0
+
+
+def test_kernel_count_host_rules(L):
+    # sequences under 128 chunks run as one pass on any device: prep + state
+    # pass, plus the packed chunk offsets and the fp32 split of the inputs;
+    # no tokens: one pass-through of the initial states; bad sizes: 0
+    bf16, f32 = torch.bfloat16, torch.float32
+    assert mdn.chunk_fwd_kernel_count(2, 2, 2048, 8, 128, bf16, False) == 2
+    assert mdn.chunk_fwd_kernel_count(3, 1, 5000, 16, 128, bf16, True) == 3
+    assert mdn.chunk_fwd_kernel_count(1, 1, 256, 2, 64, f32, False) == 3
+    assert mdn.chunk_fwd_kernel_count(3, 1, 700, 4, 64, f32, True) == 4
+    assert mdn.chunk_fwd_kernel_count(2, 2, 0, 4, 128, bf16, False) == 1
+    assert mdn.chunk_fwd_kernel_count(1, 1, 64, 4, 96, bf16, False) == 0
+    assert mdn.chunk_fwd_kernel_count(1, 1, 64, 0, 128, bf16, False) == 0
+    assert mdn.chunk_fwd_kernel_count(0, 1, 64, 4, 128, bf16, False) == 0
 
 
 def test_chunk_fwd_accepts_null_tensors_without_tokens(L):
